@@ -1,0 +1,6 @@
+"""CPU oracle for the Orthros attention hot path (test infrastructure only).
+
+Only the tests, the package smoke check and the benchmark's CPU-baseline leg
+import this package. The CUDA library never does.
+"""
+from .orthros_ref import Oracle, build, decode, max_threads, prefill  # noqa: F401

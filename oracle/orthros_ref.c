@@ -1,0 +1,380 @@
+/*
+ * orthros_ref.c -- plain CPU oracle for the Orthros attention hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing in the product path links, loads or calls
+ * this file; only the tests, the package smoke check and the benchmark's CPU
+ * baseline do. It shares no code, header or constant with the CUDA library.
+ *
+ * What it computes (Orthros: Phase-Aware Heterogeneous Attention for Efficient
+ * Transformers, paperz.arrangedbits.com full text):
+ *   - Sec. 3.1, base query  q_t  = alpha  (.) q_t  + beta    (element-wise affine)
+ *   - Sec. 3.1, output query q'_t = alpha' (.) q'_t + beta'
+ *   - Sec. 3.1, Eq. 4: sliding-window attention of every position t over keys
+ *     max(1, t-w+1) .. t (1-indexed; here 0-indexed: max(0, t-w+1) .. t)
+ *   - Sec. 3.1, Eq. 5: full causal cross-attention of every output position t
+ *     over keys 1 .. t (0-indexed: 0 .. t), against the same K/V
+ *   - Sec. 3.2 "Decoding": the base token first appends its K/V to the cache,
+ *     then runs Eq. 4; the output token runs Eq. 5 over the whole history.
+ *   - Sec. 2.1, Eq. 1: the logit is q k^T / sqrt(d_h) (the scale is an argument).
+ *   - Alg. 1, lines 6-7: heads are split after the affine, so alpha/beta hold
+ *     one value per (query head, channel); grouped K/V heads follow the
+ *     contiguous-group convention kv = h / (Hq / Hkv).
+ *
+ * Arithmetic: inputs are float (bf16 inputs are widened exactly by the caller);
+ * every intermediate and every output is double. Softmax is the two-pass exact
+ * form: max, then sum of exp(s - max). lse = max + ln(sum), natural log.
+ * No blocking, fusion, online rescaling or reordering beyond the definition.
+ *
+ * Parallelism: OpenMP over independent (sequence, head, row) units only.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define REF_OK 0
+#define REF_EINVAL 1
+#define REF_ENOMEM 2
+
+/*
+ * One query row against the key range [lo, hi] (inclusive).
+ * krow[j] / vrow[j] point at key / value j of the right K/V head.
+ * qa is the already-affined query (double). Writes o[0..d) and *lse.
+ * w is scratch of length hi - lo + 1.
+ */
+static void attend_row(const double *qa, const float *const *krow,
+                       const float *const *vrow, int lo, int hi, int d,
+                       double scale, double *o, double *lse, double *w)
+{
+    double m = -INFINITY;
+    for (int j = lo; j <= hi; ++j) {
+        const float *kj = krow[j];
+        double dot = 0.0;
+        for (int c = 0; c < d; ++c)
+            dot += qa[c] * (double)kj[c];
+        double s = scale * dot;
+        w[j - lo] = s;
+        if (s > m)
+            m = s;
+    }
+    double l = 0.0;
+    for (int c = 0; c < d; ++c)
+        o[c] = 0.0;
+    for (int j = lo; j <= hi; ++j) {
+        double p = exp(w[j - lo] - m);
+        const float *vj = vrow[j];
+        l += p;
+        for (int c = 0; c < d; ++c)
+            o[c] += p * (double)vj[c];
+    }
+    for (int c = 0; c < d; ++c)
+        o[c] /= l;
+    *lse = m + log(l);
+}
+
+/* Sec. 3.1: scale-offset affine of one raw query row. */
+static void affine(const float *qraw, const float *alpha, const float *beta,
+                   int d, double *qa)
+{
+    for (int c = 0; c < d; ++c)
+        qa[c] = (double)alpha[c] * (double)qraw[c] + (double)beta[c];
+}
+
+static int check_common(int B, int T, int Hq, int Hkv, int d, int window)
+{
+    if (B < 0 || T < 0 || Hq < 1 || Hkv < 1 || d < 1 || window < 1)
+        return REF_EINVAL;
+    if (Hq % Hkv != 0)
+        return REF_EINVAL;
+    return REF_OK;
+}
+
+/*
+ * Prefill over B sequences of T tokens (Sec. 3.2 regimes PT / SFT / Prefill).
+ *
+ * q       [B, T, Hq, d]     raw (pre-affine) queries of the base tokens
+ * k, v    [B, T, Hkv, d]
+ * alpha_base, beta_base, alpha_out, beta_out   [Hq, d]
+ * out_indptr [B+1], out_positions [n_out]: output rows of sequence b are
+ *         out_positions[out_indptr[b] .. out_indptr[b+1]), positions in [0, T)
+ * q_out   [n_out, Hq, d] raw output-stream queries, or NULL: then the raw
+ *         query of output row r is q[b, out_positions[r]] (one shared Q
+ *         projection, Alg. 1 line 5 with X_cross duplicated from X, Alg. 2).
+ * base_rows, n_base_rows: if base_rows is NULL every position is computed and
+ *         o_base is [B, T, Hq, d], lse_base [B, Hq, T]; otherwise only the
+ *         listed positions are computed (for every b and h) and the outputs are
+ *         compact: o_base [B, n_base_rows, Hq, d], lse_base [B, Hq, n_base_rows].
+ *         n_base_rows = 0 with a non-NULL list computes no base rows.
+ * o_out [n_out, Hq, d], lse_out [n_out, Hq]  (may be NULL when n_out == 0)
+ */
+int orthros_ref_prefill(const float *q, const float *k, const float *v,
+                        const float *alpha_base, const float *beta_base,
+                        const float *alpha_out, const float *beta_out,
+                        const int32_t *out_indptr, const int32_t *out_positions,
+                        const float *q_out, int B, int T, int Hq, int Hkv,
+                        int d, int window, double scale,
+                        const int32_t *base_rows, int n_base_rows,
+                        double *o_base, double *lse_base, double *o_out,
+                        double *lse_out, int nthreads)
+{
+    if (check_common(B, T, Hq, Hkv, d, window) != REF_OK)
+        return REF_EINVAL;
+    const int g = Hq / Hkv;
+    const int nrows = base_rows ? n_base_rows : T;
+    for (int i = 0; base_rows && i < n_base_rows; ++i)
+        if (base_rows[i] < 0 || base_rows[i] >= T)
+            return REF_EINVAL;
+    const int n_out = out_indptr ? out_indptr[B] : 0;
+    for (int b = 0; out_indptr && b < B; ++b)
+        for (int r = out_indptr[b]; r < out_indptr[b + 1]; ++r)
+            if (out_positions[r] < 0 || out_positions[r] >= T)
+                return REF_EINVAL;
+
+    /* key / value row tables: krow[b][kv][j] */
+    const size_t ntab = (size_t)B * Hkv * (size_t)(T > 0 ? T : 1);
+    const float **krow = (const float **)malloc(ntab * sizeof(*krow));
+    const float **vrow = (const float **)malloc(ntab * sizeof(*vrow));
+    if (!krow || !vrow) {
+        free(krow);
+        free(vrow);
+        return REF_ENOMEM;
+    }
+    for (int b = 0; b < B; ++b)
+        for (int kv = 0; kv < Hkv; ++kv)
+            for (int j = 0; j < T; ++j) {
+                size_t tab = ((size_t)b * Hkv + kv) * T + j;
+                size_t off = (((size_t)b * T + j) * Hkv + kv) * (size_t)d;
+                krow[tab] = k + off;
+                vrow[tab] = v + off;
+            }
+
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int err = REF_OK;
+
+    /* base stream: Eq. 4 at every (b, h, listed position) */
+    const long long nbase = (long long)B * Hq * nrows;
+#pragma omp parallel
+    {
+        double *qa = (double *)malloc(sizeof(double) * d);
+        double *o = (double *)malloc(sizeof(double) * d);
+        double *w = (double *)malloc(sizeof(double) * (T > 0 ? T : 1));
+        const int ok = qa && o && w;
+        if (!ok) {
+#pragma omp atomic write
+            err = REF_ENOMEM;
+        }
+        {
+#pragma omp for schedule(dynamic, 16)
+            for (long long u = 0; u < nbase; ++u) {
+                if (!ok)
+                    continue;
+                const int i = (int)(u % nrows);
+                const int h = (int)((u / nrows) % Hq);
+                const int b = (int)(u / ((long long)nrows * Hq));
+                const int t = base_rows ? base_rows[i] : i;
+                const int kv = h / g;
+                const size_t qoff = (((size_t)b * T + t) * Hq + h) * (size_t)d;
+                affine(q + qoff, alpha_base + (size_t)h * d,
+                       beta_base + (size_t)h * d, d, qa);
+                const int lo = t - window + 1 > 0 ? t - window + 1 : 0;
+                const size_t tab = ((size_t)b * Hkv + kv) * T;
+                double lse;
+                attend_row(qa, krow + tab, vrow + tab, lo, t, d, scale, o, &lse, w);
+                const size_t orow = (((size_t)b * nrows + i) * Hq + h) * (size_t)d;
+                memcpy(o_base + orow, o, sizeof(double) * d);
+                lse_base[((size_t)b * Hq + h) * nrows + i] = lse;
+            }
+        }
+        free(qa);
+        free(o);
+        free(w);
+    }
+
+    /* output stream: Eq. 5 at every output row */
+    const long long nout_units = (long long)n_out * Hq;
+#pragma omp parallel
+    {
+        double *qa = (double *)malloc(sizeof(double) * d);
+        double *o = (double *)malloc(sizeof(double) * d);
+        double *w = (double *)malloc(sizeof(double) * (T > 0 ? T : 1));
+        const int ok = qa && o && w;
+        if (!ok) {
+#pragma omp atomic write
+            err = REF_ENOMEM;
+        }
+        {
+#pragma omp for schedule(dynamic, 4)
+            for (long long u = 0; u < nout_units; ++u) {
+                if (!ok)
+                    continue;
+                const int r = (int)(u / Hq);
+                const int h = (int)(u % Hq);
+                int b = 0;
+                while (out_indptr[b + 1] <= r)
+                    ++b;
+                const int t = out_positions[r];
+                const int kv = h / g;
+                const float *qraw =
+                    q_out ? q_out + ((size_t)r * Hq + h) * (size_t)d
+                          : q + (((size_t)b * T + t) * Hq + h) * (size_t)d;
+                affine(qraw, alpha_out + (size_t)h * d,
+                       beta_out + (size_t)h * d, d, qa);
+                const size_t tab = ((size_t)b * Hkv + kv) * T;
+                double lse;
+                attend_row(qa, krow + tab, vrow + tab, 0, t, d, scale, o, &lse, w);
+                memcpy(o_out + ((size_t)r * Hq + h) * (size_t)d, o,
+                       sizeof(double) * d);
+                lse_out[(size_t)r * Hq + h] = lse;
+            }
+        }
+        free(qa);
+        free(o);
+        free(w);
+    }
+
+    free(krow);
+    free(vrow);
+    return err;
+}
+
+/*
+ * One decoding step (Sec. 3.2 "Decoding", Sec. 3.1 decoupled pair) for B
+ * sequences over a paged cache.
+ *
+ * q, q_out        [B, Hq, d] raw queries of the base / output token
+ *                 (q_out NULL: the output token's raw query equals q)
+ * k_new, v_new    [B, Hkv, d]
+ * k_cache, v_cache [num_pages, page_size, Hkv, d]; token j of sequence b lives
+ *                 in page block_table[b * max_pages + j / page_size], slot
+ *                 j % page_size. MODIFIED: the new K/V is written at position
+ *                 L = cache_lens[b] before either query runs.
+ * cache_lens      [B] lengths before the append (not modified)
+ * base row: keys max(0, L-w+1) .. L;  output row: keys 0 .. L.
+ * o_base, o_out [B, Hq, d]; lse_base, lse_out [B, Hq]
+ */
+int orthros_ref_decode(const float *q, const float *q_out, const float *k_new,
+                       const float *v_new, float *k_cache, float *v_cache,
+                       const int32_t *block_table, int max_pages, int page_size,
+                       int num_pages, const int32_t *cache_lens,
+                       const float *alpha_base, const float *beta_base,
+                       const float *alpha_out, const float *beta_out, int B,
+                       int Hq, int Hkv, int d, int window, double scale,
+                       double *o_base, double *lse_base, double *o_out,
+                       double *lse_out, int nthreads)
+{
+    if (check_common(B, 1, Hq, Hkv, d, window) != REF_OK || page_size < 1 ||
+        max_pages < 1 || num_pages < 1)
+        return REF_EINVAL;
+    const int g = Hq / Hkv;
+    const size_t tok = (size_t)Hkv * d; /* floats per token in a page */
+    int maxlen = 1;
+    for (int b = 0; b < B; ++b) {
+        const int L = cache_lens[b];
+        if (L < 0 || L / page_size >= max_pages)
+            return REF_EINVAL;
+        for (int p = 0; p <= L / page_size; ++p) {
+            const int pg = block_table[(size_t)b * max_pages + p];
+            if (pg < 0 || pg >= num_pages)
+                return REF_EINVAL;
+        }
+        if (L + 1 > maxlen)
+            maxlen = L + 1;
+    }
+
+    /* append first: the base token updates the KV cache */
+    for (int b = 0; b < B; ++b) {
+        const int L = cache_lens[b];
+        const int pg = block_table[(size_t)b * max_pages + L / page_size];
+        const size_t off = ((size_t)pg * page_size + L % page_size) * tok;
+        memcpy(k_cache + off, k_new + (size_t)b * tok, sizeof(float) * tok);
+        memcpy(v_cache + off, v_new + (size_t)b * tok, sizeof(float) * tok);
+    }
+
+    const float **krow = (const float **)malloc(sizeof(*krow) * (size_t)B * Hkv * maxlen);
+    const float **vrow = (const float **)malloc(sizeof(*vrow) * (size_t)B * Hkv * maxlen);
+    if (!krow || !vrow) {
+        free(krow);
+        free(vrow);
+        return REF_ENOMEM;
+    }
+    for (int b = 0; b < B; ++b)
+        for (int kv = 0; kv < Hkv; ++kv)
+            for (int j = 0; j <= cache_lens[b]; ++j) {
+                const int pg = block_table[(size_t)b * max_pages + j / page_size];
+                const size_t off =
+                    ((size_t)pg * page_size + j % page_size) * tok + (size_t)kv * d;
+                krow[((size_t)b * Hkv + kv) * maxlen + j] = k_cache + off;
+                vrow[((size_t)b * Hkv + kv) * maxlen + j] = v_cache + off;
+            }
+
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int err = REF_OK;
+    const long long nunits = (long long)B * Hq * 2;
+#pragma omp parallel
+    {
+        double *qa = (double *)malloc(sizeof(double) * d);
+        double *w = (double *)malloc(sizeof(double) * maxlen);
+        const int ok = qa && w;
+        if (!ok) {
+#pragma omp atomic write
+            err = REF_ENOMEM;
+        }
+        {
+#pragma omp for schedule(dynamic, 1)
+            for (long long u = 0; u < nunits; ++u) {
+                if (!ok)
+                    continue;
+                const int stream = (int)(u % 2); /* 0 base, 1 output */
+                const int h = (int)((u / 2) % Hq);
+                const int b = (int)(u / (2LL * Hq));
+                const int L = cache_lens[b];
+                const int kv = h / g;
+                const size_t qoff = ((size_t)b * Hq + h) * (size_t)d;
+                const size_t tab = ((size_t)b * Hkv + kv) * maxlen;
+                double lse;
+                if (stream == 0) {
+                    affine(q + qoff, alpha_base + (size_t)h * d,
+                           beta_base + (size_t)h * d, d, qa);
+                    const int lo = L - window + 1 > 0 ? L - window + 1 : 0;
+                    attend_row(qa, krow + tab, vrow + tab, lo, L, d, scale,
+                               o_base + qoff, &lse, w);
+                    lse_base[(size_t)b * Hq + h] = lse;
+                } else {
+                    affine((q_out ? q_out : q) + qoff, alpha_out + (size_t)h * d,
+                           beta_out + (size_t)h * d, d, qa);
+                    attend_row(qa, krow + tab, vrow + tab, 0, L, d, scale,
+                               o_out + qoff, &lse, w);
+                    lse_out[(size_t)b * Hq + h] = lse;
+                }
+            }
+        }
+        free(qa);
+        free(w);
+    }
+    free(krow);
+    free(vrow);
+    return err;
+}
+
+/* Threads the OpenMP runtime would use (reported next to the CPU timing). */
+int orthros_ref_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
