@@ -1,0 +1,435 @@
+#!/usr/bin/env python
+"""Benchmark of the Orthros attention hot path on GB300.
+
+Prints ONE JSON line (rank 0). The headline `value` is prefill attention
+throughput (TFLOP/s of useful work: in-band query-key pairs of the base
+stream plus the output rows' causal pairs, 4*d FLOP per pair and head) on a
+128K-token prefill at the Llama-3.1-8B attention shape (GQA 32/8, d = 128,
+window 4096, one output row at the last prompt token), through
+orthros_prefill with inputs resident in HBM. The same line carries the
+decoding throughput (KV-cache GB/s, every cached K/V byte counted once per
+step) of 32 paged sequences with 16K-32K cached tokens over 128 steps.
+
+A step = one orthros_prefill call: K/V cache fill, the fp16 key pre-pass,
+the banded base-stream kernel, the output row(s), and their combine.
+
+--impl reference runs the CPU oracle instead (the reference arm of this
+repository: a deliberately plain program, timed on a bounded sample).
+Multi-GPU: every rank runs its own replica of the workload (the work shards by
+sequence and head with no exchange); value sums all ranks' work over the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "prefill attn TFLOP/s & decode KV GB/s (Llama-8B shape, 128K) vs roofline"
+
+
+# ----------------------------------------------------------------------------
+# work accounting (useful FLOPs / algorithmic bytes)
+# ----------------------------------------------------------------------------
+def band_pairs(T: int, w: int) -> int:
+    """Query-key pairs of the sliding-window stream for one (sequence, head)."""
+    if w >= T:
+        return T * (T + 1) // 2
+    return w * (w + 1) // 2 + (T - w) * w
+
+
+def prefill_flops(wl, positions_per_seq) -> dict:
+    """Useful FLOPs: 2*d for q.k plus 2*d for p*v per pair and query head."""
+    per_pair = 4 * wl.d * wl.Hq * wl.B
+    swa = band_pairs(wl.T, wl.window) * per_pair
+    cross = sum(t + 1 for t in positions_per_seq) * 4 * wl.d * wl.Hq
+    return dict(swa=swa, cross=cross, total=swa + cross)
+
+
+def decode_bytes(lens0, steps, Hkv, d, elem=2) -> int:
+    """Each cached K and V element read once per step (cache after the append)."""
+    tot = 0
+    for s in range(steps):
+        tot += sum(int(L) + s + 1 for L in lens0) * Hkv * d * elem * 2
+    return tot
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for n, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (replicas; torch.distributed only for barrier + max)
+# ----------------------------------------------------------------------------
+class Dist:
+    def __init__(self, enable: bool):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1 and enable:
+            import torch
+            import torch.distributed as dist
+
+            torch.cuda.set_device(self.local)
+            dist.init_process_group("nccl")
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+
+        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sust=d.get("bf16_tflops_sustained"),
+                    src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sust=1700.0, src="fallback")
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle baseline (bounded sample)
+# ----------------------------------------------------------------------------
+def oracle_sample(wl_inputs, wl, target_s: float, seed: int = 0):
+    """Time the oracle on base rows of the prefill workload (full windows),
+    growing the sample until it takes about target_s seconds. Returns
+    (TFLOP/s, threads, description)."""
+    import numpy as np
+
+    import oracle
+
+    f32 = {n: wl_inputs[n].float().numpy() for n in ("q", "k", "v", "alpha_base", "beta_base", "alpha_out",
+                                                     "beta_out")}
+    nthreads = len(os.sched_getaffinity(0))
+    empty_indptr = np.zeros(wl.B + 1, np.int32)
+    empty_pos = np.zeros(0, np.int32)
+    rng = np.random.default_rng(seed)
+    n = 1
+    while True:
+        rows = np.sort(rng.choice(np.arange(wl.window, wl.T), size=n, replace=False)).astype(np.int32)
+        t0 = time.perf_counter()
+        oracle.prefill(f32["q"], f32["k"], f32["v"], f32["alpha_base"], f32["beta_base"], f32["alpha_out"],
+                       f32["beta_out"], empty_indptr, empty_pos, wl.window, wl.scale, base_rows=rows,
+                       nthreads=nthreads)
+        dt = time.perf_counter() - t0
+        flops = n * wl.B * wl.Hq * wl.window * 4 * wl.d
+        if dt >= target_s or n >= wl.T - wl.window:
+            break
+        n = min(wl.T - wl.window, max(n * 2, int(n * target_s / max(dt, 1e-3) * 1.05)))
+    desc = (f"{n} base rows x {wl.Hq} heads with full {wl.window}-key windows of the {wl.T}-token prefill "
+            f"({flops / 1e9:.1f} GFLOP useful, {dt:.1f} s)")
+    return flops / dt / 1e12, nthreads, desc
+
+
+def run_reference(args, dist):
+    """The reference arm: the CPU oracle as it stands, same metric and config."""
+    if dist.rank != 0:
+        return
+    from efficient_long_context_gb300 import workloads as W
+
+    import oracle
+
+    oracle.build()
+    wl = W.PREFILL_128K
+    inputs = W.make_prefill(wl)
+    per_step_s = float(os.environ.get("ORTHROS_REF_STEP_S", "4"))
+    vals = []
+    for _ in range(args.warmup):
+        oracle_sample(inputs, wl, per_step_s / 4)
+    desc = cores = None
+    t_all = time.perf_counter()
+    for s in range(args.steps):
+        v, cores, desc = oracle_sample(inputs, wl, per_step_s, seed=s)
+        vals.append(v)
+    elapsed = time.perf_counter() - t_all
+    value = statistics.mean(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) inputs of the 128K prefill workload)",
+            "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
+                       "window": wl.window, "out_rows": "last position"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
+# the GPU arm
+# ----------------------------------------------------------------------------
+def run_ours(args, dist):
+    import torch
+
+    import efficient_long_context_gb300 as ola
+    from efficient_long_context_gb300 import build as B
+    from efficient_long_context_gb300 import workloads as W
+
+    B.build()
+    torch.cuda.set_device(dist.local)
+    dev = torch.device("cuda", dist.local)
+    peaks = load_peaks()
+
+    # ---------------- prefill workload, resident in HBM ----------------
+    wl = W.PREFILL_128K
+    inputs = W.make_prefill(wl)
+    q, k, v = (inputs[n].to(dev) for n in ("q", "k", "v"))
+    aff = [inputs[n].to(dev) for n in ("alpha_base", "beta_base", "alpha_out", "beta_out")]
+    indptr = inputs["out_indptr"]
+    pos = inputs["out_positions"].to(dev)
+    n_out = int(indptr[-1])
+    P = 64
+    max_pages = (wl.T + P - 1) // P
+    num_pages = wl.B * max_pages
+    k_cache = torch.empty((num_pages, P, wl.Hkv, wl.d), dtype=wl.dtype, device=dev)
+    v_cache = torch.empty_like(k_cache)
+    block_table = torch.arange(num_pages, dtype=torch.int32, device=dev).view(wl.B, max_pages)
+    o_base = torch.empty_like(q)
+    lse_base = torch.empty((wl.B, wl.Hq, wl.T), dtype=torch.float32, device=dev)
+    o_out = torch.empty((n_out, wl.Hq, wl.d), dtype=wl.dtype, device=dev)
+    lse_out = torch.empty((n_out, wl.Hq), dtype=torch.float32, device=dev)
+    ws = torch.empty(ola.orthros_prefill_workspace_size(wl.B, wl.T, wl.Hq, wl.Hkv, wl.d, n_out, wl.window,
+                                                        wl.dtype), dtype=torch.uint8, device=dev)
+    outs = (o_base, lse_base, o_out, lse_out)
+    stream = torch.cuda.current_stream(dev)
+
+    def prefill_step():
+        ola.orthros_prefill(q, k, v, *aff, indptr, pos, wl.window, wl.scale, out=outs, k_cache=k_cache,
+                            v_cache=v_cache, block_table=block_table, page_size=P, workspace=ws, stream=stream)
+
+    flops = prefill_flops(wl, [int(t) for t in inputs["out_positions"]])
+    for _ in range(max(args.warmup, 3)):
+        prefill_step()
+    torch.cuda.synchronize()
+    rc, bits = ola.orthros_check(ws)
+    if rc != 0:
+        raise RuntimeError(f"prefill flagged device status {rc} bits 0x{bits:x}")
+
+    clocks = ClockSampler(dist.local)
+    clocks.start()
+    time.sleep(0.3)
+    dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ola.orthros_profile_begin()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        prefill_step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    prof = ola.orthros_profile_end()
+    dist.barrier()
+    ms_local = ev0.elapsed_time(ev1)
+    ms_total = dist.max(ms_local)
+    ms_step = ms_total / args.steps
+    value = flops["total"] * dist.world / (ms_step * 1e-3) / 1e12
+
+    # dominant kernel: the banded base-stream kernel
+    dom_name, (dom_launches, dom_ms) = max(prof.items(), key=lambda kv: kv[1][1])
+    dom_avg_ms = dom_ms / dom_launches
+    dom_flops = flops["swa"] if "base" in dom_name or "prefill_tc" in dom_name else flops["total"]
+    achieved = dom_flops / (dom_avg_ms * 1e-3) / 1e12
+    launches = sum(n for n, _ in prof.values())
+
+    # ---------------- decoding workload ----------------
+    dec = W.DECODE_32
+    st = W.make_decode(dec, steps=args.decode_steps)
+    dm = st.meta
+    kc, vc = st.k_cache.to(dev), st.v_cache.to(dev)
+    bt = st.block_table.to(dev)
+    lens_steps = (st.cache_lens[None, :].to(torch.int64) + torch.arange(dm["steps"])[:, None]).to(torch.int32).to(dev)
+    dq, dk, dv = st.q.to(dev), st.k_new.to(dev), st.v_new.to(dev)
+    daff = [a.to(dev) for a in (st.alpha_base, st.beta_base, st.alpha_out, st.beta_out)]
+    d_ob = torch.empty((dec.B, dec.Hq, dec.d), dtype=dec.dtype, device=dev)
+    d_oo = torch.empty_like(d_ob)
+    d_lb = torch.empty((dec.B, dec.Hq), dtype=torch.float32, device=dev)
+    d_lo = torch.empty_like(d_lb)
+    d_ws = torch.empty(ola.orthros_decode_workspace_size(dec.B, dec.Hq, dec.Hkv, dec.d, dm["max_pages"], dec.page_size,
+                                                         dec.dtype), dtype=torch.uint8, device=dev)
+    d_outs = (d_ob, d_lb, d_oo, d_lo)
+
+    def decode_step(s):
+        ola.orthros_decode(dq[s], dk[s], dv[s], kc, vc, bt, lens_steps[s], *daff, dec.window, dec.scale,
+                           out=d_outs, workspace=d_ws, stream=stream)
+
+    for s in range(max(args.warmup, 3)):
+        decode_step(s)
+    torch.cuda.synchronize()
+    rc, bits = ola.orthros_check(d_ws)
+    if rc != 0:
+        raise RuntimeError(f"decode flagged device status {rc} bits 0x{bits:x}")
+    dist.barrier()
+    ola.orthros_profile_begin()
+    ev0.record(stream)
+    for s in range(dm["steps"]):
+        decode_step(s)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    dprof = ola.orthros_profile_end()
+    clk = clocks.stop()
+    d_ms = dist.max(ev0.elapsed_time(ev1))
+    d_bytes = decode_bytes(st.cache_lens.tolist(), dm["steps"], dec.Hkv, dec.d)
+    d_gbs = d_bytes * dist.world / (d_ms * 1e-3) / 1e9
+    d_dom, (d_dom_n, d_dom_ms) = max(dprof.items(), key=lambda kv: kv[1][1])
+    d_achieved = d_bytes / (d_dom_ms * 1e-3) / 1e9  # bytes of all steps / summed time of that kernel
+    del kc, vc, dq, dk, dv
+
+    # ---------------- end to end: host buffers, copies inside the timed region ----------------
+    h_in = {n: inputs[n].pin_memory() for n in ("q", "k", "v")}
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    e2e_steps = max(1, min(args.steps, 3))
+    prefill_step()
+    torch.cuda.synchronize()
+    dist.barrier()
+    ev0.record(stream)
+    for _ in range(e2e_steps):
+        q.copy_(h_in["q"], non_blocking=True)
+        k.copy_(h_in["k"], non_blocking=True)
+        v.copy_(h_in["v"], non_blocking=True)
+        prefill_step()
+        for hbuf, dbuf in zip(h_out, outs):
+            hbuf.copy_(dbuf, non_blocking=True)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = dist.max(ev0.elapsed_time(ev1)) / e2e_steps
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    e2e_value = flops["total"] * dist.world / (e2e_ms * 1e-3) / 1e12
+
+    # ---------------- CPU baseline (rank 0, N = 1 only) ----------------
+    cpu = None
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        v_cpu, cores, desc = oracle_sample(inputs, wl, args.cpu_seconds)
+        cpu = {"value": v_cpu, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
+
+    if dist.rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": dist.world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) q/k/v, affines 1+0.1N / 0.1N; no dataset)",
+            "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
+                       "window": wl.window, "out_rows": "last position (prefill regime)", "page_size": P,
+                       "useful_tflop_per_step": flops["total"] / 1e12,
+                       "l2": "inputs larger than L2 (q 1 GiB, k/v 256 MiB each)",
+                       "parallelism": f"replicas x{dist.world}"},
+            "roofline": {"bound": "tensor", "kernel": dom_name, "achieved": achieved, "peak": peaks["bf16"],
+                         "unit": "TFLOP/s", "frac": achieved / peaks["bf16"], "traffic": None,
+                         "peak_source": f"{peaks['src']} bf16 dense (burst)",
+                         "avg_launch_ms": dom_avg_ms},
+            "kernels": {n: {"launches": c, "total_ms": t} for n, (c, t) in prof.items()},
+            "gpu_launches": launches,
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms, "steps": e2e_steps},
+            "decode": {"value": d_gbs, "unit": "GB/s", "workload": dec.name, "steps": dm["steps"],
+                       "ms_per_step": d_ms / dm["steps"], "bytes": d_bytes,
+                       "roofline": {"bound": "hbm", "kernel": d_dom, "achieved": d_achieved, "peak": peaks["hbm"],
+                                    "unit": "GB/s", "frac": d_achieved / peaks["hbm"], "traffic": None,
+                                    "peak_source": f"{peaks['src']} HBM copy"},
+                       "frac_of_hbm": d_gbs / peaks["hbm"],
+                       "kernels": {n: {"launches": c, "total_ms": t} for n, (c, t) in dprof.items()},
+                       "gpu_launches": sum(n for n, _ in dprof.values())},
+            "cpu_baseline": cpu,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--decode-steps", type=int, default=None,
+                    help="decoding steps to time (default: the workload's 128)")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target length of the oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    dist = Dist(enable=args.impl == "ours")
+    try:
+        if args.impl == "reference":
+            run_reference(args, dist)
+        else:
+            run_ours(args, dist)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,231 @@
+"""ctypes binding of include/orthros_attn.h (argument marshalling only)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+import torch
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+ORTHROS_BF16 = 0
+ORTHROS_F32 = 1
+_DTYPES = {torch.bfloat16: ORTHROS_BF16, torch.float32: ORTHROS_F32}
+
+STATUS_NAMES = {0: "ORTHROS_OK", 1: "ORTHROS_EINVAL", 2: "ORTHROS_EUNSUPPORTED", 3: "ORTHROS_ECUDA",
+                4: "ORTHROS_EWORKSPACE", 5: "ORTHROS_EDEVICE", 6: "ORTHROS_ETIMEOUT"}
+
+# the public symbols of include/orthros_attn.h
+EXPORTS = ("orthros_prefill_workspace_size", "orthros_prefill", "orthros_decode_workspace_size",
+           "orthros_decode", "orthros_check", "orthros_profile_begin", "orthros_profile_end",
+           "orthros_status_string", "orthros_last_error")
+
+
+class KernelTime(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int), ("total_ms", ctypes.c_double)]
+
+
+class OrthrosError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load_library(path: str | None = None):
+    """Load liborthros_attn.so (built by efficient_long_context_gb300.build)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or _build.LIB
+        if not os.path.exists(p):
+            raise OrthrosError(-1, f"{p} is missing: run efficient_long_context_gb300.build.build() first "
+                                   "(there is no fallback path)")
+        lib = ctypes.CDLL(p)
+        vp, i32, f32p, i32p, sz = ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_float), \
+            ctypes.POINTER(ctypes.c_int32), ctypes.c_size_t
+        lib.orthros_prefill_workspace_size.restype = sz
+        lib.orthros_prefill_workspace_size.argtypes = [i32] * 7 + [i32]
+        lib.orthros_prefill.restype = i32
+        lib.orthros_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32p, vp, i32, vp,
+                                        i32, i32, i32, i32, i32, i32, ctypes.c_float, i32,
+                                        vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp, sz, vp]
+        lib.orthros_decode_workspace_size.restype = sz
+        lib.orthros_decode_workspace_size.argtypes = [i32] * 7
+        lib.orthros_decode.restype = i32
+        lib.orthros_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp,
+                                       vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float, i32,
+                                       vp, vp, vp, vp, vp, sz, vp]
+        lib.orthros_check.restype = i32
+        lib.orthros_check.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
+        lib.orthros_profile_begin.restype = i32
+        lib.orthros_profile_begin.argtypes = []
+        lib.orthros_profile_end.restype = i32
+        lib.orthros_profile_end.argtypes = [ctypes.POINTER(KernelTime), i32]
+        lib.orthros_status_string.restype = ctypes.c_char_p
+        lib.orthros_status_string.argtypes = [i32]
+        lib.orthros_last_error.restype = ctypes.c_char_p
+        lib.orthros_last_error.argtypes = []
+        del f32p
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def orthros_status_string(status: int) -> str:
+    return load_library().orthros_status_string(int(status)).decode()
+
+
+def orthros_last_error() -> str:
+    return load_library().orthros_last_error().decode()
+
+
+def _raise_if(rc: int, lib):
+    if rc != 0:
+        raise OrthrosError(rc, lib.orthros_last_error().decode())
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, torch.Tensor):
+        return ctypes.c_void_p(t.data_ptr()) if t.numel() else ctypes.c_void_p(0)
+    return t
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype not in _DTYPES:
+        raise OrthrosError(1, f"unsupported element type {t.dtype}")
+    return _DTYPES[t.dtype]
+
+
+def _contig(name, t):
+    if t is not None and not t.is_contiguous():
+        raise OrthrosError(1, f"{name} must be contiguous")
+    return t
+
+
+def orthros_prefill_workspace_size(B, T, Hq, Hkv, d, n_out, window, dtype=torch.bfloat16) -> int:
+    return int(load_library().orthros_prefill_workspace_size(B, T, Hq, Hkv, d, n_out, window, _DTYPES[dtype]))
+
+
+def orthros_decode_workspace_size(B, Hq, Hkv, d, max_pages, page_size, dtype=torch.bfloat16) -> int:
+    return int(load_library().orthros_decode_workspace_size(B, Hq, Hkv, d, max_pages, page_size, _DTYPES[dtype]))
+
+
+def orthros_prefill(q, k, v, alpha_base, beta_base, alpha_out, beta_out, out_indptr, out_positions,
+                    window, scale=None, *, q_out=None, out=None, k_cache=None, v_cache=None,
+                    block_table=None, page_size=0, workspace=None, stream=None):
+    """orthros_prefill of include/orthros_attn.h on torch CUDA tensors.
+
+    out_indptr is a HOST int32 array-like [B+1]; every other tensor lives on
+    the GPU. Returns (o_base [B,T,Hq,d], lse_base [B,Hq,T], o_out [n_out,Hq,d],
+    lse_out [n_out,Hq]), allocated here unless `out` gives all four.
+    """
+    lib = load_library()
+    B, T, Hq, d = q.shape
+    Hkv = k.shape[2]
+    indptr = np.ascontiguousarray(np.asarray(out_indptr.cpu() if isinstance(out_indptr, torch.Tensor)
+                                             else out_indptr, dtype=np.int32))
+    n_out = int(indptr[-1]) if indptr.size else 0
+    if scale is None:
+        scale = d ** -0.5
+    for name, t in (("q", q), ("k", k), ("v", v), ("q_out", q_out), ("out_positions", out_positions)):
+        _contig(name, t)
+    if out is None:
+        o_base = torch.empty_like(q)
+        lse_base = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
+        o_out = torch.empty((n_out, Hq, d), dtype=q.dtype, device=q.device)
+        lse_out = torch.empty((n_out, Hq), dtype=torch.float32, device=q.device)
+    else:
+        o_base, lse_base, o_out, lse_out = out
+    if workspace is None:
+        ws = orthros_prefill_workspace_size(B, T, Hq, Hkv, d, n_out, window, q.dtype)
+        workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=q.device)
+    max_pages = block_table.shape[1] if block_table is not None else 0
+    num_pages = k_cache.shape[0] if k_cache is not None else 0
+    rc = lib.orthros_prefill(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(alpha_base), _ptr(beta_base), _ptr(alpha_out), _ptr(beta_out),
+        indptr.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), _ptr(out_positions), n_out, _ptr(q_out),
+        B, T, Hq, Hkv, d, int(window), float(scale), _dtype(q),
+        _ptr(o_base), _ptr(lse_base), _ptr(o_out), _ptr(lse_out),
+        _ptr(k_cache), _ptr(v_cache), _ptr(block_table), max_pages, int(page_size), num_pages,
+        _ptr(workspace), workspace.numel(), _stream(stream))
+    _raise_if(rc, lib)
+    return o_base, lse_base, o_out, lse_out
+
+
+def orthros_decode(q, k_new, v_new, k_cache, v_cache, block_table, cache_lens, alpha_base, beta_base,
+                   alpha_out, beta_out, window, scale=None, *, q_out=None, out=None, workspace=None,
+                   stream=None):
+    """orthros_decode of include/orthros_attn.h on torch CUDA tensors.
+
+    k_cache / v_cache [num_pages, page_size, Hkv, d] are updated in place.
+    Returns (o_base [B,Hq,d], lse_base [B,Hq], o_out [B,Hq,d], lse_out [B,Hq]).
+    """
+    lib = load_library()
+    B, Hq, d = q.shape
+    Hkv = k_new.shape[1]
+    num_pages, page_size = k_cache.shape[0], k_cache.shape[1]
+    max_pages = block_table.shape[1]
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        o_base = torch.empty_like(q)
+        o_out = torch.empty_like(q)
+        lse_base = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+        lse_out = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    else:
+        o_base, lse_base, o_out, lse_out = out
+    if workspace is None:
+        ws = orthros_decode_workspace_size(B, Hq, Hkv, d, max_pages, page_size, q.dtype)
+        workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=q.device)
+    rc = lib.orthros_decode(
+        _ptr(q), _ptr(q_out), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+        max_pages, page_size, num_pages, _ptr(cache_lens),
+        _ptr(alpha_base), _ptr(beta_base), _ptr(alpha_out), _ptr(beta_out),
+        B, Hq, Hkv, d, int(window), float(scale), _dtype(q),
+        _ptr(o_base), _ptr(lse_base), _ptr(o_out), _ptr(lse_out),
+        _ptr(workspace), workspace.numel(), _stream(stream))
+    _raise_if(rc, lib)
+    return o_base, lse_base, o_out, lse_out
+
+
+def orthros_check(workspace, stream=None):
+    """Synchronise and read the device status word. Returns (status, bits)."""
+    lib = load_library()
+    bits = ctypes.c_uint32(0)
+    rc = lib.orthros_check(_ptr(workspace), _stream(stream), ctypes.byref(bits))
+    return int(rc), int(bits.value)
+
+
+def orthros_profile_begin():
+    """Start recording per-kernel CUDA-event times of the library's launches."""
+    _raise_if(load_library().orthros_profile_begin(), load_library())
+
+
+def orthros_profile_end():
+    """Stop recording; returns {kernel name: (launches, total_ms)} in first-launch order."""
+    lib = load_library()
+    buf = (KernelTime * 64)()
+    n = lib.orthros_profile_end(buf, 64)
+    if n < 0:
+        raise OrthrosError(3, "orthros_profile_end: CUDA error while reading events")
+    return {buf[i].name.decode(): (buf[i].launches, buf[i].total_ms) for i in range(min(n, 64))}

@@ -1,0 +1,88 @@
+// internal.cuh -- declarations shared by the translation units of liborthros_attn.
+//
+// Nothing here is part of the public ABI (include/orthros_attn.h is).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "orthros_attn.h"
+
+namespace orthros {
+
+// ---------------------------------------------------------------------------
+// Workspace layout (every region 256-byte aligned)
+//   [0, 256)        status word (uint32 at offset 0) + spare
+//   then per-entry-point regions, sized by the *_workspace_size functions
+// ---------------------------------------------------------------------------
+constexpr size_t kStatusBytes = 256;
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+__device__ __forceinline__ void set_status(uint32_t *status, uint32_t bit) {
+    if (status) atomicOr(status, bit);
+}
+
+// Element loads / stores for the two supported element types.
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+// Arguments of the generic row kernels. Every pointer is a device pointer.
+struct RowsArgs {
+    const void *q;      // prefill [B,T,Hq,d] / decode [B,Hq,d]
+    const void *q_out;  // prefill [n_out,Hq,d] / decode [B,Hq,d] or nullptr
+    const void *k;      // prefill [B,T,Hkv,d] / decode cache [num_pages,P,Hkv,d]
+    const void *v;
+    const float *alpha_base, *beta_base, *alpha_out, *beta_out;
+    const int32_t *out_indptr;     // device copy [B+1] (prefill output rows)
+    const int32_t *out_positions;  // [n_out]
+    const int32_t *block_table;    // decode
+    const int32_t *cache_lens;     // decode
+    int n_out, max_pages, page_size, num_pages;
+    int B, T, Hq, Hkv, window;
+    float scale;
+    void *o_base;
+    float *lse_base;
+    void *o_out;
+    float *lse_out;
+    uint32_t *status;
+};
+
+enum RowKind { kPrefillBase = 0, kPrefillOut = 1, kDecodePair = 2 };
+
+// profile.cu: brackets one kernel launch with CUDA events while profiling is on.
+class ProfScope {
+  public:
+    ProfScope(const char *name, cudaStream_t s);
+    ~ProfScope();
+    ProfScope(const ProfScope &) = delete;
+    ProfScope &operator=(const ProfScope &) = delete;
+
+  private:
+    const char *name_;
+    cudaStream_t stream_;
+    void *a_;
+};
+
+// simt_rows.cu: one warp per (row, head); any element type; the fp32 path.
+cudaError_t launch_rows_simt(const RowsArgs &a, RowKind kind, int d, orthros_dtype dtype,
+                             cudaStream_t stream);
+
+// cache.cu
+cudaError_t launch_decode_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                                 const int32_t *block_table, const int32_t *cache_lens, int B, int Hkv,
+                                 int d, int max_pages, int page_size, int num_pages, int elem_bytes,
+                                 uint32_t *status, cudaStream_t stream);
+cudaError_t launch_prefill_cache_fill(const void *k, const void *v, void *k_cache, void *v_cache,
+                                      const int32_t *block_table, int B, int T, int Hkv, int d,
+                                      int max_pages, int page_size, int num_pages, int elem_bytes,
+                                      uint32_t *status, cudaStream_t stream);
+
+}  // namespace orthros

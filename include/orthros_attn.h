@@ -1,0 +1,199 @@
+/*
+ * orthros_attn.h -- C ABI of the Orthros attention hot path on one GPU.
+ *
+ * Orthros ("Orthros: Phase-Aware Heterogeneous Attention for Efficient
+ * Transformers", paperz.arrangedbits.com full text) runs, in every layer:
+ *   - a base stream: sliding-window attention of EVERY position t over the keys
+ *     max(0, t-w+1) .. t  (Sec. 3.1, Eq. 4; 0-indexed here), which also
+ *     produces the layer's K/V cache;
+ *   - an output stream: full causal cross-attention of the output positions
+ *     over keys 0 .. t of the same K/V (Sec. 3.1, Eq. 5).
+ * Both query streams come from one Q projection through their own
+ * per-channel scale-offset affine, q = alpha (.) q_raw + beta (Sec. 3.1,
+ * Alg. 1 line 5). The four regimes of Sec. 3.2 (pre-training, SFT,
+ * prefilling, decoding) differ only in which positions are output rows.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor arguments are DEVICE pointers unless marked HOST. The caller
+ *     owns every buffer, including the workspace and the cache pages; the
+ *     library never allocates, frees or synchronises on the compute path.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = default stream).
+ *   - Layouts are row-major and contiguous. Query heads h map to K/V heads
+ *     kv = h / (Hq / Hkv) (contiguous groups; Hq == Hkv is plain multi-head).
+ *   - Element type of q, k, v, q_out, k_new, v_new, caches and o_* is given by
+ *     `dtype`: ORTHROS_BF16 (bfloat16) or ORTHROS_F32 (float). alpha/beta and
+ *     lse are always float. lse is the natural log of sum_j exp(scale q.k_j).
+ *   - The logit is scale * (q_affined . k); scale is usually 1/sqrt(d)
+ *     (Sec. 2.1, Eq. 1).
+ *   - Tensors of element type bf16/f32 must be 16-byte aligned.
+ *   - Errors found on the host return before any launch (ORTHROS_EINVAL,
+ *     ORTHROS_EUNSUPPORTED, ORTHROS_EWORKSPACE); orthros_last_error() then
+ *     describes the problem. Launch failures return ORTHROS_ECUDA. Bad data
+ *     that only the GPU can see (a position out of range, a block-table entry
+ *     outside the page pool, a cache length past the block table, a key value
+ *     the fp16 tensor-core path cannot represent) sets a status word in the
+ *     workspace; the affected rows are skipped or their outputs are NaN, and
+ *     orthros_check() reports ORTHROS_EDEVICE. Nothing aborts or traps.
+ *   - Supported head sizes: d = 64 or 128.
+ */
+#ifndef ORTHROS_ATTN_H
+#define ORTHROS_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ORTHROS_API __attribute__((visibility("default")))
+#else
+#define ORTHROS_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *orthros_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    ORTHROS_OK = 0,
+    ORTHROS_EINVAL = 1,       /* bad argument, detected on the host */
+    ORTHROS_EUNSUPPORTED = 2, /* well-formed but not supported (e.g. d = 96) */
+    ORTHROS_ECUDA = 3,        /* a CUDA call or kernel launch failed */
+    ORTHROS_EWORKSPACE = 4,   /* workspace NULL or smaller than required */
+    ORTHROS_EDEVICE = 5,      /* a kernel flagged bad device-side data */
+    ORTHROS_ETIMEOUT = 6      /* a kernel's bounded wait ran out */
+} orthros_status;
+
+typedef enum { ORTHROS_BF16 = 0, ORTHROS_F32 = 1 } orthros_dtype;
+
+/* Bits of the device status word (see orthros_check). */
+#define ORTHROS_DEV_BAD_POSITION 0x1u  /* out_positions entry outside [0, T) */
+#define ORTHROS_DEV_BAD_PAGE 0x2u      /* block-table entry outside [0, num_pages) */
+#define ORTHROS_DEV_BAD_LENGTH 0x4u    /* cache_lens[b] < 0 or past the block table */
+#define ORTHROS_DEV_FP16_RANGE 0x8u    /* |k| or |affined q| beyond the fp16 range */
+#define ORTHROS_DEV_TIMEOUT 0x10u      /* a bounded wait inside a kernel ran out */
+
+/*
+ * Workspace bytes orthros_prefill needs for these sizes. n_out is the total
+ * number of output rows. Returns 0 for sizes orthros_prefill would reject.
+ */
+ORTHROS_API size_t orthros_prefill_workspace_size(int B, int T, int Hq, int Hkv, int d,
+                                      int n_out, int window, orthros_dtype dtype);
+
+/*
+ * Prefill (Sec. 3.2 regimes pre-training / SFT / prefilling): Eq. 4 at every
+ * position of B sequences of T tokens, Eq. 5 at the output rows, and
+ * optionally the paged K/V cache fill that the decoding phase reads.
+ *
+ * q            [B, T, Hq, d]   raw queries (the affines are applied inside)
+ * k, v         [B, T, Hkv, d]
+ * alpha_base, beta_base [Hq, d] float: base-stream affine (alpha, beta)
+ * alpha_out,  beta_out  [Hq, d] float: output-stream affine (alpha', beta');
+ *              may be NULL when n_out == 0
+ * out_indptr   HOST [B+1] int32, out_indptr[0] = 0, non-decreasing,
+ *              out_indptr[B] = n_out: output rows of sequence b are
+ *              r in [out_indptr[b], out_indptr[b+1])
+ * out_positions [n_out] int32: position t_r in [0, T) of output row r (any
+ *              order, repeats allowed; each row is independent)
+ * q_out        [n_out, Hq, d] raw output-stream queries, or NULL: then the raw
+ *              query of row r is q[b, t_r] (one shared Q projection; exact for
+ *              a first layer, whose output tokens duplicate the base tokens)
+ * window       w >= 1; w >= T gives full causal attention in the base stream
+ * scale        logit scale (finite)
+ * o_base [B, T, Hq, d], lse_base [B, Hq, T] float
+ * o_out  [n_out, Hq, d], lse_out [n_out, Hq] float  (may be NULL if n_out == 0)
+ * k_cache, v_cache [num_pages, page_size, Hkv, d], block_table [B, max_pages]
+ *              int32: optional (all NULL to skip). When given, token t of
+ *              sequence b is also written to page block_table[b*max_pages +
+ *              t/page_size], slot t % page_size, for t < T (needs
+ *              max_pages * page_size >= T). num_pages bounds the entries.
+ * workspace    device scratch of at least orthros_prefill_workspace_size()
+ *              bytes, 256-byte aligned; its contents on entry do not matter.
+ */
+ORTHROS_API orthros_status orthros_prefill(
+    const void *q, const void *k, const void *v,
+    const float *alpha_base, const float *beta_base,
+    const float *alpha_out, const float *beta_out,
+    const int32_t *out_indptr, const int32_t *out_positions, int n_out,
+    const void *q_out,
+    int B, int T, int Hq, int Hkv, int d, int window, float scale,
+    orthros_dtype dtype,
+    void *o_base, float *lse_base, void *o_out, float *lse_out,
+    void *k_cache, void *v_cache, const int32_t *block_table,
+    int max_pages, int page_size, int num_pages,
+    void *workspace, size_t workspace_bytes, orthros_stream_t stream);
+
+/* Workspace bytes orthros_decode needs for these sizes (0 if rejected). */
+ORTHROS_API size_t orthros_decode_workspace_size(int B, int Hq, int Hkv, int d,
+                                     int max_pages, int page_size,
+                                     orthros_dtype dtype);
+
+/*
+ * One decoding step for B sequences (Sec. 3.2 "Decoding"; the decoupled
+ * token pair of Sec. 3.1). For each sequence b with L = cache_lens[b]:
+ *   1. the base token's K/V (k_new[b], v_new[b]) is written at position L of
+ *      the paged cache (page block_table[b*max_pages + L/page_size], slot
+ *      L % page_size);
+ *   2. the base query (alpha/beta affine) attends keys max(0, L-w+1) .. L;
+ *   3. the output query (alpha'/beta' affine) attends keys 0 .. L.
+ * Both queries read the cache after the append.
+ *
+ * q            [B, Hq, d] raw query of the base token
+ * q_out        [B, Hq, d] raw query of the output token, or NULL (= q)
+ * k_new, v_new [B, Hkv, d]
+ * k_cache, v_cache [num_pages, page_size, Hkv, d]  (modified: one slot per b)
+ * block_table  [B, max_pages] int32 physical page ids
+ * cache_lens   [B] int32 lengths BEFORE this step (read only; the caller
+ *              increments them afterwards and provides a page for slot L)
+ * o_base, o_out [B, Hq, d]; lse_base, lse_out [B, Hq] float
+ * workspace    at least orthros_decode_workspace_size() bytes, 256-byte aligned
+ */
+ORTHROS_API orthros_status orthros_decode(
+    const void *q, const void *q_out, const void *k_new, const void *v_new,
+    void *k_cache, void *v_cache, const int32_t *block_table, int max_pages,
+    int page_size, int num_pages, const int32_t *cache_lens,
+    const float *alpha_base, const float *beta_base,
+    const float *alpha_out, const float *beta_out,
+    int B, int Hq, int Hkv, int d, int window, float scale, orthros_dtype dtype,
+    void *o_base, float *lse_base, void *o_out, float *lse_out,
+    void *workspace, size_t workspace_bytes, orthros_stream_t stream);
+
+/*
+ * Synchronises `stream`, reads the status word that the last call using
+ * `workspace` left there and returns ORTHROS_OK, ORTHROS_EDEVICE (data bits) or
+ * ORTHROS_ETIMEOUT (timeout bit). *bits (if not NULL) receives the raw
+ * ORTHROS_DEV_* bits. This is the one call that blocks the host.
+ */
+ORTHROS_API orthros_status orthros_check(const void *workspace, orthros_stream_t stream,
+                             uint32_t *bits);
+
+/*
+ * Per-kernel timing of the library's own launches (tracing aid).
+ * orthros_profile_begin() starts recording: every kernel the library launches
+ * afterwards is bracketed by two CUDA events recorded on its launch stream.
+ * orthros_profile_end() stops recording, waits for the recorded events and
+ * fills up to max_entries records, one per kernel name, in first-launch order.
+ * It returns the number of distinct kernels (may exceed max_entries), or -1 on
+ * a CUDA error. Recording is process-wide and not thread-safe; it adds two
+ * event records per launch and nothing else.
+ */
+typedef struct {
+    char name[48];   /* kernel family, e.g. "prefill_tc" */
+    int launches;    /* launches recorded */
+    double total_ms; /* summed event-to-event time of those launches */
+} orthros_kernel_time;
+
+ORTHROS_API orthros_status orthros_profile_begin(void);
+ORTHROS_API int orthros_profile_end(orthros_kernel_time *out, int max_entries);
+
+/* Static English name of a status code. */
+ORTHROS_API const char *orthros_status_string(orthros_status s);
+
+/* Description of the last host-side error on this thread ("" if none). */
+ORTHROS_API const char *orthros_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ORTHROS_ATTN_H */

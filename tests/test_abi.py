@@ -1,0 +1,120 @@
+"""The C-ABI library builds, loads and exports every symbol the header declares;
+host-side argument checks return their error codes without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import efficient_long_context_gb300 as ola
+from efficient_long_context_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return ola.load_library()
+
+
+def declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"ORTHROS_API\s+[\w\s\*]*?\b(orthros_\w+)\s*\(", src))
+    return names
+
+
+def test_header_declares_the_abi():
+    names = declared_symbols()
+    assert {"orthros_prefill", "orthros_decode", "orthros_check"} <= names
+    assert names == set(ola._binding.EXPORTS)
+
+
+def test_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    assert ola.orthros_status_string(0) == "ok"
+    assert "workspace" in ola.orthros_status_string(4)
+
+
+def test_workspace_size_rejects_bad_shapes(lib):
+    assert ola.orthros_prefill_workspace_size(1, 16, 4, 2, 128, 1, 8) > 0
+    assert ola.orthros_prefill_workspace_size(1, 16, 3, 2, 128, 1, 8) == 0  # Hq % Hkv
+    assert ola.orthros_prefill_workspace_size(1, 16, 4, 2, 96, 1, 8) == 0  # d
+    assert ola.orthros_prefill_workspace_size(1, 16, 4, 2, 128, 1, 0) == 0  # window
+    assert ola.orthros_decode_workspace_size(2, 4, 2, 64, 8, 64) > 0
+    assert ola.orthros_decode_workspace_size(2, 4, 2, 64, 0, 64) == 0
+
+
+def _call_prefill(lib, **over):
+    args = dict(q=1 << 12, k=1 << 12, v=1 << 12, ab=1 << 12, bb=1 << 12, ao=1 << 12, bo=1 << 12,
+                indptr=(ctypes.c_int32 * 2)(0, 1), pos=1 << 12, n_out=1, q_out=None,
+                B=1, T=16, Hq=4, Hkv=2, d=128, window=8, scale=0.1, dtype=0,
+                o_base=1 << 12, lse_base=1 << 12, o_out=1 << 12, lse_out=1 << 12,
+                k_cache=None, v_cache=None, bt=None, max_pages=0, page_size=0, num_pages=0,
+                ws=1 << 12, ws_bytes=1 << 30, stream=None)
+    args.update(over)
+    a = args
+    return lib.orthros_prefill(a["q"], a["k"], a["v"], a["ab"], a["bb"], a["ao"], a["bo"],
+                               a["indptr"], a["pos"], a["n_out"], a["q_out"], a["B"], a["T"], a["Hq"],
+                               a["Hkv"], a["d"], a["window"], a["scale"], a["dtype"], a["o_base"],
+                               a["lse_base"], a["o_out"], a["lse_out"], a["k_cache"], a["v_cache"],
+                               a["bt"], a["max_pages"], a["page_size"], a["num_pages"], a["ws"],
+                               a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(Hq=3), 1),
+    (dict(d=96), 2),
+    (dict(window=0), 1),
+    (dict(scale=float("inf")), 1),
+    (dict(q=None), 1),
+    (dict(q=(1 << 12) + 2), 1),  # misaligned
+    (dict(indptr=(ctypes.c_int32 * 2)(0, 2)), 1),  # indptr[B] != n_out
+    (dict(indptr=(ctypes.c_int32 * 2)(1, 1)), 1),  # indptr[0] != 0
+    (dict(pos=None), 1),
+    (dict(ws=None), 4),
+    (dict(ws_bytes=8), 4),
+    (dict(ws=(1 << 12) + 16), 1),  # workspace alignment
+    (dict(k_cache=1 << 12), 1),  # partial cache arguments
+    (dict(k_cache=1 << 12, v_cache=1 << 12, bt=1 << 12, max_pages=1, page_size=8, num_pages=4), 1),  # pages < T
+    (dict(dtype=7), 1),
+])
+def test_prefill_host_checks(lib, over, code):
+    assert _call_prefill(lib, **over) == code
+    assert ola.orthros_last_error() != ""
+
+
+def test_decode_host_checks(lib):
+    rc = lib.orthros_decode(1 << 12, None, 1 << 12, 1 << 12, 1 << 12, 1 << 12, 1 << 12, 0, 64, 4, 1 << 12,
+                            1 << 12, 1 << 12, 1 << 12, 1 << 12, 2, 4, 2, 128, 16, 0.1, 0,
+                            1 << 12, 1 << 12, 1 << 12, 1 << 12, 1 << 12, 1 << 20, None)
+    assert rc == 1  # max_pages = 0
+    rc = lib.orthros_decode(1 << 12, None, 1 << 12, 1 << 12, 1 << 12, 1 << 12, 1 << 12, 4, 64, 4, 1 << 12,
+                            1 << 12, 1 << 12, 1 << 12, 1 << 12, 2, 4, 2, 128, 16, 0.1, 0,
+                            1 << 12, 1 << 12, 1 << 12, 1 << 12, None, 0, None)
+    assert rc == 4  # no workspace
+
+
+def test_product_path_fails_loudly_without_library(tmp_path):
+    with pytest.raises(ola.OrthrosError):
+        ola.load_library(str(tmp_path / "missing.so"))
+
+
+def test_binding_does_not_import_oracle():
+    import sys
+
+    import efficient_long_context_gb300._binding  # noqa: F401
+    src = open(os.path.join(ROOT, "efficient_long_context_gb300", "_binding.py")).read()
+    assert "oracle" not in src
+    for fn in os.listdir(os.path.join(ROOT, "efficient_long_context_gb300", "csrc")):
+        assert "orthros_ref" not in open(os.path.join(ROOT, "efficient_long_context_gb300", "csrc", fn)).read()
+    assert torch is not None and sys is not None
