@@ -62,7 +62,68 @@ __global__ void prefill_cache_fill_kernel(const uint4 *__restrict__ k, const uin
     }
 }
 
+// One pass over the bf16 keys/values of a prefill: keys -> fp16 copy (exact in
+// the fp16 range; out-of-range magnitudes raise ORTHROS_DEV_FP16_RANGE), and,
+// when a block table is given, both tensors -> their cache pages.
+__global__ void prefill_prep_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
+                                    uint4 *__restrict__ k16, uint4 *__restrict__ k_cache,
+                                    uint4 *__restrict__ v_cache, const int32_t *__restrict__ block_table, int B,
+                                    int T, int vec_per_tok, int max_pages, int page_size, int num_pages,
+                                    uint32_t *status) {
+    const long long n = (long long)B * T * vec_per_tok;
+    bool over = false;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x) {
+        const uint4 kx = k[i];
+        const uint32_t *w = reinterpret_cast<const uint32_t *>(&kx);
+        uint4 h;
+        uint32_t *hw = reinterpret_cast<uint32_t *>(&h);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
+            over |= fabsf(lo) > 65504.f || fabsf(hi) > 65504.f;
+            const __half2 hv = __floats2half2_rn(lo, hi);
+            hw[e] = *reinterpret_cast<const uint32_t *>(&hv);
+        }
+        k16[i] = h;
+        if (k_cache) {
+            const long long tok = i / vec_per_tok;
+            const int wi = (int)(i % vec_per_tok);
+            const int b = (int)(tok / T);
+            const int t = (int)(tok % T);
+            const int pg = block_table[(long long)b * max_pages + t / page_size];
+            if (pg < 0 || pg >= num_pages) {
+                if (wi == 0) set_status(status, ORTHROS_DEV_BAD_PAGE);
+                continue;
+            }
+            const long long dst = ((long long)pg * page_size + t % page_size) * vec_per_tok + wi;
+            k_cache[dst] = kx;
+            v_cache[dst] = v[i];
+        }
+    }
+    if (over) set_status(status, ORTHROS_DEV_FP16_RANGE);
+}
+
+int grid_for(long long n, int threads, int per_sm) {
+    int sms = 152, dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    long long blocks = (n + threads - 1) / threads;
+    const long long cap = (long long)sms * per_sm;
+    return (int)(blocks < cap ? blocks : cap);
+}
+
 }  // namespace
+
+cudaError_t launch_prefill_prep(const void *k, const void *v, void *k16, void *k_cache, void *v_cache,
+                                const int32_t *block_table, int B, int T, int Hkv, int d, int max_pages,
+                                int page_size, int num_pages, uint32_t *status, cudaStream_t stream) {
+    const long long n = (long long)B * T * Hkv * d * 2 / 16;
+    if (n == 0) return cudaSuccess;
+    prefill_prep_kernel<<<grid_for(n, 256, 8), 256, 0, stream>>>(
+        (const uint4 *)k, (const uint4 *)v, (uint4 *)k16, (uint4 *)k_cache, (uint4 *)v_cache, block_table, B, T,
+        Hkv * d * 2 / 16, max_pages, page_size, num_pages, status);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_decode_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
                                  const int32_t *block_table, const int32_t *cache_lens, int B, int Hkv,

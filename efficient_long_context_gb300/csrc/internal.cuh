@@ -71,6 +71,51 @@ class ProfScope {
     void *a_;
 };
 
+// prefill_tc.cu: tensor-core banded prefill (bf16 inputs, d = 64 or 128).
+struct TcParams {
+    const __nv_bfloat16 *q;      // [B,T,Hq,d]
+    const __nv_bfloat16 *q_out;  // [n_out,Hq,d] or nullptr
+    const float *alpha_base, *beta_base, *alpha_out, *beta_out;
+    const int32_t *out_indptr;         // device [B+1]
+    const int32_t *out_positions;      // [n_out]
+    const int32_t *cross_unit_indptr;  // device [B+1]: output-row units per sequence (prefix sums)
+    int B, T, Hq, Hkv, window;
+    float scale, scale_log2;
+    int n_cross_units, n_base_units, base_nblk;
+    __nv_bfloat16 *o_base;
+    float *lse_base;
+    __nv_bfloat16 *o_out;
+    float *lse_out;
+    uint32_t *status;
+};
+// Work units of one (sequence, kv head) for nblk row blocks and group size g.
+int tc_units_per_kv(int nblk, int g);
+cudaError_t launch_prefill_tc(const TcParams &p, const void *k16, const void *v, int d, cudaStream_t stream);
+
+// splitkv.cu: split-KV attention for few rows over long key ranges + combine.
+enum SplitMode { kSplitPrefill = 0, kSplitDecode = 1 };
+struct SplitParams {
+    int mode;
+    const __nv_bfloat16 *q, *q_out;  // prefill [B,T,Hq,d] / [n_out,Hq,d]; decode [B,Hq,d] each
+    const __nv_bfloat16 *k, *v;      // prefill [B,T,Hkv,d]; decode caches [num_pages,P,Hkv,d]
+    const float *alpha_base, *beta_base, *alpha_out, *beta_out;
+    const int32_t *out_positions;    // prefill
+    const int32_t *group_info;       // prefill: 3 ints per group (b<<16 | kv, first row, positions)
+    const int32_t *block_table, *cache_lens;  // decode
+    int max_pages, page_size, num_pages;
+    int B, T, Hq, Hkv, window;
+    float scale, scale_log2;
+    int n_groups, chunk, max_chunks;
+    float *partial;  // [n_groups, max_chunks, 16, d + 2]
+    __nv_bfloat16 *o_base;
+    float *lse_base;
+    __nv_bfloat16 *o_out;
+    float *lse_out;
+    uint32_t *status;
+};
+size_t split_partial_bytes(int n_groups, int max_chunks, int d);
+cudaError_t launch_splitkv(const SplitParams &p, int d, int rows_per_group, cudaStream_t stream);
+
 // simt_rows.cu: one warp per (row, head); any element type; the fp32 path.
 cudaError_t launch_rows_simt(const RowsArgs &a, RowKind kind, int d, orthros_dtype dtype,
                              cudaStream_t stream);
@@ -80,6 +125,11 @@ cudaError_t launch_decode_append(const void *k_new, const void *v_new, void *k_c
                                  const int32_t *block_table, const int32_t *cache_lens, int B, int Hkv,
                                  int d, int max_pages, int page_size, int num_pages, int elem_bytes,
                                  uint32_t *status, cudaStream_t stream);
+// fp16 copy of the keys for the tensor-core prefill, optionally fused with the
+// paged cache fill (k_cache == nullptr skips it).
+cudaError_t launch_prefill_prep(const void *k, const void *v, void *k16, void *k_cache, void *v_cache,
+                                const int32_t *block_table, int B, int T, int Hkv, int d, int max_pages,
+                                int page_size, int num_pages, uint32_t *status, cudaStream_t stream);
 cudaError_t launch_prefill_cache_fill(const void *k, const void *v, void *k_cache, void *v_cache,
                                       const int32_t *block_table, int B, int T, int Hkv, int d,
                                       int max_pages, int page_size, int num_pages, int elem_bytes,

@@ -3,10 +3,12 @@
 // Every entry point validates everything the host can see before the first
 // launch, then enqueues its kernels on the caller's stream and returns. See
 // include/orthros_attn.h for the contract of each call.
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <string>
+#include <vector>
 
 #include "internal.cuh"
 
@@ -33,27 +35,48 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 int elem_bytes(orthros_dtype t) { return t == ORTHROS_F32 ? 4 : 2; }
 
+// Split-KV chunk sizes (keys per CTA; multiples of 64).
+constexpr int kPrefillChunk = 1024;
+constexpr int kDecodeChunk = 2048;
+// A sequence's output rows take the split-KV kernel when all of its rows fit
+// in at most this many 16-row groups per kv head; otherwise the tile kernel.
+constexpr int kSplitRowsMax = 256;
+
+int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
 // Workspace regions of orthros_prefill.
 struct PrefillLayout {
-    size_t indptr_off, total;
+    size_t blob_off, k16_off, part_off, total;
+    int max_groups, max_chunks;
 };
 
-PrefillLayout prefill_layout(int B) {
+PrefillLayout prefill_layout(int B, int T, int Hkv, int d, int n_out, orthros_dtype dtype) {
     PrefillLayout L{};
     size_t at = kStatusBytes;
-    L.indptr_off = at;
-    at += align_up(sizeof(int32_t) * (size_t)(B + 1), 256);
+    L.max_groups = dtype == ORTHROS_BF16 ? (int)std::min<long long>((long long)n_out, 16LL * B) * Hkv : 0;
+    L.max_chunks = ceil_div(T, kPrefillChunk);
+    L.blob_off = at;
+    at += align_up(sizeof(int32_t) * (size_t)(2 * (B + 1) + 3 * (size_t)L.max_groups), 256);
+    L.k16_off = at;
+    if (dtype == ORTHROS_BF16) at += align_up((size_t)B * T * Hkv * d * 2, 256);
+    L.part_off = at;
+    at += align_up(split_partial_bytes(L.max_groups, L.max_chunks, d), 256);
     L.total = at;
     return L;
 }
 
 struct DecodeLayout {
-    size_t total;
+    size_t part_off, total;
+    int max_chunks;
 };
 
-DecodeLayout decode_layout() {
+DecodeLayout decode_layout(int B, int Hkv, int d, int max_pages, int page_size, orthros_dtype dtype) {
     DecodeLayout L{};
-    L.total = kStatusBytes;
+    size_t at = kStatusBytes;
+    L.part_off = at;
+    L.max_chunks = ceil_div((long long)max_pages * page_size, kDecodeChunk);
+    if (dtype == ORTHROS_BF16) at += align_up(split_partial_bytes(B * Hkv, L.max_chunks, d), 256);
+    L.total = at;
     return L;
 }
 
@@ -94,7 +117,7 @@ size_t orthros_prefill_workspace_size(int B, int T, int Hq, int Hkv, int d, int 
                                       orthros_dtype dtype) {
     if (T < 0 || n_out < 0) return 0;
     if (check_shapes(B, Hq, Hkv, d, window, 1.0f, dtype) != ORTHROS_OK) return 0;
-    return prefill_layout(B).total;
+    return prefill_layout(B, T, Hkv, d, n_out, dtype).total;
 }
 
 orthros_status orthros_prefill(const void *q, const void *k, const void *v, const float *alpha_base,
@@ -119,6 +142,8 @@ orthros_status orthros_prefill(const void *q, const void *k, const void *v, cons
         if (!o_base || !lse_base) return fail(ORTHROS_EINVAL, "o_base and lse_base must not be NULL");
         if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o_base))
             return fail(ORTHROS_EINVAL, "q, k, v and o_base must be 16-byte aligned");
+        if (!aligned16(alpha_base) || !aligned16(beta_base))
+            return fail(ORTHROS_EINVAL, "alpha_base and beta_base must be 16-byte aligned");
     }
     if (B > 0 && !out_indptr) return fail(ORTHROS_EINVAL, "out_indptr (host) must not be NULL");
     if (B > 0) {
@@ -136,8 +161,8 @@ orthros_status orthros_prefill(const void *q, const void *k, const void *v, cons
         if (!out_positions) return fail(ORTHROS_EINVAL, "out_positions must not be NULL when n_out > 0");
         if (!alpha_out || !beta_out) return fail(ORTHROS_EINVAL, "alpha_out and beta_out must not be NULL when n_out > 0");
         if (!o_out || !lse_out) return fail(ORTHROS_EINVAL, "o_out and lse_out must not be NULL when n_out > 0");
-        if (!aligned16(o_out) || (q_out && !aligned16(q_out)))
-            return fail(ORTHROS_EINVAL, "o_out and q_out must be 16-byte aligned");
+        if (!aligned16(o_out) || (q_out && !aligned16(q_out)) || !aligned16(alpha_out) || !aligned16(beta_out))
+            return fail(ORTHROS_EINVAL, "o_out, q_out, alpha_out and beta_out must be 16-byte aligned");
     }
     const bool fill = k_cache || v_cache || block_table;
     if (fill) {
@@ -151,7 +176,7 @@ orthros_status orthros_prefill(const void *q, const void *k, const void *v, cons
         if (!aligned16(k_cache) || !aligned16(v_cache))
             return fail(ORTHROS_EINVAL, "k_cache and v_cache must be 16-byte aligned");
     }
-    const PrefillLayout lay = prefill_layout(B);
+    const PrefillLayout lay = prefill_layout(B, T, Hkv, d, n_out, dtype);
     if (!workspace || workspace_bytes < lay.total)
         return fail(ORTHROS_EWORKSPACE, "workspace needs %zu bytes, got %zu", lay.total,
                     workspace ? workspace_bytes : (size_t)0);
@@ -164,53 +189,160 @@ orthros_status orthros_prefill(const void *q, const void *k, const void *v, cons
     if (e != cudaSuccess) return cuda_fail(e, "status reset");
     if (rows == 0) return ORTHROS_OK;
 
-    int32_t *indptr_dev = reinterpret_cast<int32_t *>(ws + lay.indptr_off);
+    const int g = Hq / Hkv;
+    const bool tc = dtype == ORTHROS_BF16;
+
+    // Plan (host): which sequences' output rows take the split-KV kernel, the
+    // tile kernel's output-row units, and the split groups. One upload.
+    std::vector<int32_t> blob((size_t)2 * (B + 1), 0);
+    int n_cross_units = 0, n_groups = 0, rows_per_group = 0;
+    bool any_simt_out = false;
+    std::copy(out_indptr, out_indptr + B + 1, blob.begin());
+    for (int b = 0; b < B; ++b) {
+        const int nb = out_indptr[b + 1] - out_indptr[b];
+        blob[(size_t)B + 1 + b] = n_cross_units;
+        if (nb == 0) continue;
+        if (!tc) {
+            any_simt_out = true;
+        } else if (g <= 16 && (long long)nb * g <= kSplitRowsMax) {
+            const int per = 16 / g;  // positions per 16-row group
+            for (int kvh = 0; kvh < Hkv; ++kvh)
+                for (int r0 = 0; r0 < nb; r0 += per) {
+                    const int cnt = std::min(per, nb - r0);
+                    blob.push_back((b << 16) | kvh);
+                    blob.push_back(out_indptr[b] + r0);
+                    blob.push_back(cnt);
+                    rows_per_group = std::max(rows_per_group, cnt * g);
+                    ++n_groups;
+                }
+        } else {
+            n_cross_units += Hkv * tc_units_per_kv(ceil_div(nb, 128), g);
+        }
+    }
+    blob[(size_t)2 * B + 1] = n_cross_units;
+    if (n_groups > lay.max_groups) return fail(ORTHROS_EWORKSPACE, "internal: split groups exceed the workspace plan");
+    int32_t *blob_dev = reinterpret_cast<int32_t *>(ws + lay.blob_off);
+    const int32_t *indptr_dev = blob_dev;
+    const int32_t *cross_indptr_dev = blob_dev + B + 1;
+    const int32_t *groups_dev = blob_dev + 2 * (B + 1);
     if (n_out > 0) {
-        e = cudaMemcpyAsync(indptr_dev, out_indptr, sizeof(int32_t) * (size_t)(B + 1), cudaMemcpyHostToDevice,
-                            stream);
-        if (e != cudaSuccess) return cuda_fail(e, "out_indptr upload");
+        e = cudaMemcpyAsync(blob_dev, blob.data(), sizeof(int32_t) * blob.size(), cudaMemcpyHostToDevice, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "plan upload");
     }
 
-    if (fill) {
-        ProfScope ps("cache_fill", stream);
-        e = launch_prefill_cache_fill(k, v, k_cache, v_cache, block_table, B, T, Hkv, d, max_pages, page_size,
-                                      num_pages, elem_bytes(dtype), status, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "cache fill launch");
+    if (!tc) {
+        if (fill) {
+            ProfScope ps("cache_fill", stream);
+            e = launch_prefill_cache_fill(k, v, k_cache, v_cache, block_table, B, T, Hkv, d, max_pages, page_size,
+                                          num_pages, elem_bytes(dtype), status, stream);
+            if (e != cudaSuccess) return cuda_fail(e, "cache fill launch");
+        }
+        RowsArgs a{};
+        a.q = q;
+        a.q_out = q_out;
+        a.k = k;
+        a.v = v;
+        a.alpha_base = alpha_base;
+        a.beta_base = beta_base;
+        a.alpha_out = alpha_out;
+        a.beta_out = beta_out;
+        a.out_indptr = indptr_dev;
+        a.out_positions = out_positions;
+        a.n_out = n_out;
+        a.B = B;
+        a.T = T;
+        a.Hq = Hq;
+        a.Hkv = Hkv;
+        a.window = window;
+        a.scale = scale;
+        a.o_base = o_base;
+        a.lse_base = lse_base;
+        a.o_out = o_out;
+        a.lse_out = lse_out;
+        a.status = status;
+        {
+            ProfScope ps("rows_simt_base", stream);
+            e = launch_rows_simt(a, kPrefillBase, d, dtype, stream);
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "base-stream launch");
+        if (any_simt_out) {
+            ProfScope ps("rows_simt_out", stream);
+            e = launch_rows_simt(a, kPrefillOut, d, dtype, stream);
+            if (e != cudaSuccess) return cuda_fail(e, "output-stream launch");
+        }
+        return ORTHROS_OK;
     }
 
-    RowsArgs a{};
-    a.q = q;
-    a.q_out = q_out;
-    a.k = k;
-    a.v = v;
-    a.alpha_base = alpha_base;
-    a.beta_base = beta_base;
-    a.alpha_out = alpha_out;
-    a.beta_out = beta_out;
-    a.out_indptr = indptr_dev;
-    a.out_positions = out_positions;
-    a.n_out = n_out;
-    a.B = B;
-    a.T = T;
-    a.Hq = Hq;
-    a.Hkv = Hkv;
-    a.window = window;
-    a.scale = scale;
-    a.o_base = o_base;
-    a.lse_base = lse_base;
-    a.o_out = o_out;
-    a.lse_out = lse_out;
-    a.status = status;
+    // bf16: fp16 keys (+ cache fill) -> split-KV output rows -> tensor-core tiles
+    void *k16 = ws + lay.k16_off;
     {
-        ProfScope ps("rows_simt_base", stream);
-        e = launch_rows_simt(a, kPrefillBase, d, dtype, stream);
+        ProfScope ps("prefill_prep", stream);
+        e = launch_prefill_prep(k, v, k16, fill ? k_cache : nullptr, fill ? v_cache : nullptr, block_table, B, T, Hkv,
+                                d, max_pages, page_size, num_pages, status, stream);
     }
-    if (e != cudaSuccess) return cuda_fail(e, "base-stream launch");
-    if (n_out > 0) {
-        ProfScope ps("rows_simt_out", stream);
-        e = launch_rows_simt(a, kPrefillOut, d, dtype, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "output-stream launch");
+    if (e != cudaSuccess) return cuda_fail(e, "prep launch");
+    const float log2e = 1.4426950408889634f;
+    if (n_groups > 0) {
+        SplitParams sp{};
+        sp.mode = kSplitPrefill;
+        sp.q = static_cast<const __nv_bfloat16 *>(q);
+        sp.q_out = static_cast<const __nv_bfloat16 *>(q_out);
+        sp.k = static_cast<const __nv_bfloat16 *>(k);
+        sp.v = static_cast<const __nv_bfloat16 *>(v);
+        sp.alpha_base = alpha_base;
+        sp.beta_base = beta_base;
+        sp.alpha_out = alpha_out;
+        sp.beta_out = beta_out;
+        sp.out_positions = out_positions;
+        sp.group_info = groups_dev;
+        sp.B = B;
+        sp.T = T;
+        sp.Hq = Hq;
+        sp.Hkv = Hkv;
+        sp.window = window;
+        sp.scale = scale;
+        sp.scale_log2 = scale * log2e;
+        sp.n_groups = n_groups;
+        sp.chunk = kPrefillChunk;
+        sp.max_chunks = lay.max_chunks;
+        sp.partial = reinterpret_cast<float *>(ws + lay.part_off);
+        sp.o_out = static_cast<__nv_bfloat16 *>(o_out);
+        sp.lse_out = lse_out;
+        sp.status = status;
+        ProfScope ps("splitkv_prefill", stream);
+        e = launch_splitkv(sp, d, rows_per_group, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "split-KV launch");
     }
+    TcParams tp{};
+    tp.q = static_cast<const __nv_bfloat16 *>(q);
+    tp.q_out = static_cast<const __nv_bfloat16 *>(q_out);
+    tp.alpha_base = alpha_base;
+    tp.beta_base = beta_base;
+    tp.alpha_out = alpha_out;
+    tp.beta_out = beta_out;
+    tp.out_indptr = indptr_dev;
+    tp.out_positions = out_positions;
+    tp.cross_unit_indptr = cross_indptr_dev;
+    tp.B = B;
+    tp.T = T;
+    tp.Hq = Hq;
+    tp.Hkv = Hkv;
+    tp.window = window;
+    tp.scale = scale;
+    tp.scale_log2 = scale * log2e;
+    tp.base_nblk = ceil_div(T, 128);
+    tp.n_cross_units = n_cross_units;
+    tp.n_base_units = B * Hkv * tc_units_per_kv(tp.base_nblk, g);
+    tp.o_base = static_cast<__nv_bfloat16 *>(o_base);
+    tp.lse_base = lse_base;
+    tp.o_out = static_cast<__nv_bfloat16 *>(o_out);
+    tp.lse_out = lse_out;
+    tp.status = status;
+    {
+        ProfScope ps("prefill_tc", stream);
+        e = launch_prefill_tc(tp, k16, v, d, stream);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "tensor-core prefill launch");
     return ORTHROS_OK;
 }
 
@@ -218,7 +350,7 @@ size_t orthros_decode_workspace_size(int B, int Hq, int Hkv, int d, int max_page
                                      orthros_dtype dtype) {
     if (max_pages < 1 || page_size < 1) return 0;
     if (check_shapes(B, Hq, Hkv, d, 1, 1.0f, dtype) != ORTHROS_OK) return 0;
-    return decode_layout().total;
+    return decode_layout(B, Hkv, d, max_pages, page_size, dtype).total;
 }
 
 orthros_status orthros_decode(const void *q, const void *q_out, const void *k_new, const void *v_new,
@@ -239,13 +371,15 @@ orthros_status orthros_decode(const void *q, const void *q_out, const void *k_ne
             return fail(ORTHROS_EINVAL, "q, k_new, v_new, caches, block_table, cache_lens must not be NULL");
         if (!alpha_base || !beta_base || !alpha_out || !beta_out)
             return fail(ORTHROS_EINVAL, "the four affine vectors must not be NULL");
+        if (!aligned16(alpha_base) || !aligned16(beta_base) || !aligned16(alpha_out) || !aligned16(beta_out))
+            return fail(ORTHROS_EINVAL, "the four affine vectors must be 16-byte aligned");
         if (!o_base || !lse_base || !o_out || !lse_out)
             return fail(ORTHROS_EINVAL, "outputs must not be NULL");
         if (!aligned16(q) || (q_out && !aligned16(q_out)) || !aligned16(k_new) || !aligned16(v_new) ||
             !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o_base) || !aligned16(o_out))
             return fail(ORTHROS_EINVAL, "element tensors must be 16-byte aligned");
     }
-    const DecodeLayout lay = decode_layout();
+    const DecodeLayout lay = decode_layout(B, Hkv, d, max_pages, page_size, dtype);
     if (!workspace || workspace_bytes < lay.total)
         return fail(ORTHROS_EWORKSPACE, "workspace needs %zu bytes, got %zu", lay.total,
                     workspace ? workspace_bytes : (size_t)0);
@@ -262,6 +396,45 @@ orthros_status orthros_decode(const void *q, const void *q_out, const void *k_ne
                                  page_size, num_pages, elem_bytes(dtype), status, stream);
     }
     if (e != cudaSuccess) return cuda_fail(e, "append launch");
+
+    const int g = Hq / Hkv;
+    if (dtype == ORTHROS_BF16 && 2 * g <= 16) {
+        // both rows of every query head of a kv group share one pass over the cache
+        SplitParams sp{};
+        sp.mode = kSplitDecode;
+        sp.q = static_cast<const __nv_bfloat16 *>(q);
+        sp.q_out = static_cast<const __nv_bfloat16 *>(q_out);
+        sp.k = static_cast<const __nv_bfloat16 *>(k_cache);
+        sp.v = static_cast<const __nv_bfloat16 *>(v_cache);
+        sp.alpha_base = alpha_base;
+        sp.beta_base = beta_base;
+        sp.alpha_out = alpha_out;
+        sp.beta_out = beta_out;
+        sp.block_table = block_table;
+        sp.cache_lens = cache_lens;
+        sp.max_pages = max_pages;
+        sp.page_size = page_size;
+        sp.num_pages = num_pages;
+        sp.B = B;
+        sp.Hq = Hq;
+        sp.Hkv = Hkv;
+        sp.window = window;
+        sp.scale = scale;
+        sp.scale_log2 = scale * 1.4426950408889634f;
+        sp.n_groups = B * Hkv;
+        sp.chunk = kDecodeChunk;
+        sp.max_chunks = lay.max_chunks;
+        sp.partial = reinterpret_cast<float *>(static_cast<char *>(workspace) + lay.part_off);
+        sp.o_base = static_cast<__nv_bfloat16 *>(o_base);
+        sp.lse_base = lse_base;
+        sp.o_out = static_cast<__nv_bfloat16 *>(o_out);
+        sp.lse_out = lse_out;
+        sp.status = status;
+        ProfScope ps("splitkv_decode", stream);
+        e = launch_splitkv(sp, d, 2 * g, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "split-KV decode launch");
+        return ORTHROS_OK;
+    }
 
     RowsArgs a{};
     a.q = q;

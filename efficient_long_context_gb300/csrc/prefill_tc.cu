@@ -1,0 +1,571 @@
+// prefill_tc.cu -- banded sliding-window attention (base stream) and dense
+// output-stream rows on the 5th-generation tensor cores (tcgen05, TMEM, TMA).
+//
+// What it computes (Orthros paper, Sec. 3.1):
+//   Eq. 4: o_t  = softmax_j(scale * q_t . k_j)  v_j over j in [max(0, t-w+1), t]
+//   Eq. 5: o'_t = softmax_j(scale * q'_t . k_j) v_j over j in [0, t]
+// with q = alpha (.) q_raw + beta applied while the query tile is staged
+// (Alg. 1 line 5), for every base position and for output rows handed to this
+// kernel (those of sequences with many output rows; sequences with few output
+// rows take the split-KV kernel instead).
+//
+// Design (one CTA per SM, 320 threads):
+//   * A work unit is two 128-row query tiles that read the SAME key/value
+//     tiles: two query heads of one GQA group at the same positions, or (when
+//     the group size is odd, e.g. plain multi-head) two consecutive row blocks
+//     of one head. Key/value tiles of 128 tokens are visited only inside the
+//     union of the tiles' bands; tiles outside the band are never loaded.
+//   * warp 8 (one thread): TMA producer. Keys come from an fp16 copy made by
+//     the pre-pass kernel (3 stages), values in bf16 (2 stages), 128B swizzle.
+//   * warp 9 (one thread): tcgen05.mma issuer. S_s = Q_s K^T (M=128, N=128,
+//     fp16 operands from shared memory) into TMEM; O_s += P_s V (M=128, N=d,
+//     P read from TMEM as bf16, V from shared memory, MN-major).
+//   * warps 0-3 / 4-7: softmax of tile 0 / tile 1. Thread i owns row i (TMEM
+//     lane i): it reads its 128 logits with tcgen05.ld, masks the two band
+//     edge tiles, keeps a running max with lazy rescaling (O in TMEM is only
+//     rescaled when the max grows by more than 2^8), writes P as packed bf16
+//     back over its logits, and finally normalises O and stores o and lse.
+//   TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [384,384+d).
+//
+// Precision: the query affine runs in fp32 and is rounded to fp16 (11-bit
+// significand) rather than bf16 for the QK^T product; the pre-pass converts
+// keys bf16 -> fp16, which is exact in the fp16 range (the pre-pass flags any
+// key beyond it). P is rounded to bf16 for the PV product, accumulation fp32.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "ptx.cuh"
+
+namespace orthros {
+
+using namespace ptx;
+
+namespace {
+
+constexpr int kRowsPerTile = 128;  // M of every MMA, rows of a query tile
+constexpr int kKeysPerTile = 128;  // N of QK^T, K of PV
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kNumK = 3;  // key stages
+constexpr int kNumV = 2;  // value stages
+
+template <int D> struct Cfg {
+    static constexpr int kSub = D / 64;                                 // 128-byte swizzle atoms per row
+    static constexpr int kTileBytes = kRowsPerTile * D * 2;             // one 128 x D fp16/bf16 tile
+    static constexpr int kQ0 = 0;                                       // two query tiles
+    static constexpr int kK0 = kQ0 + 2 * kTileBytes;                    // key stages
+    static constexpr int kV0 = kK0 + kNumK * kTileBytes;                // value stages
+    static constexpr int kBar = kV0 + kNumV * kTileBytes;               // barriers + metadata
+    static constexpr int kSmem = kBar + 256 + 1024;                     // + alignment slack
+    static constexpr int kTmemO = 256;                                  // first O column
+};
+
+struct Meta {
+    uint64_t k_full[kNumK], k_empty[kNumK], v_full[kNumV], v_empty[kNumV];
+    uint64_t s_full[2], p_full[2], o_full[2], mma_done;
+    uint32_t tmem_base;
+    int abort;
+    int t_min[2], t_max[2];
+};
+
+struct Slot {
+    int kind;  // 0 base positions, 1 output rows, -1 empty
+    int b, h, row0, n;
+};
+
+// Work-unit decoding. Units [0, n_cross) are output-row units (heavier, so
+// they start first), then base units. Inside one (sequence, kv head) the order
+// is reversed so that late, fully populated row blocks start first.
+__device__ __forceinline__ int units_per_kv(int nblk, int g) {
+    return (g % 2 == 0) ? nblk * (g / 2) : g * ((nblk + 1) / 2);
+}
+
+__device__ void decode_unit(const TcParams &p, int u, Slot &s0, Slot &s1) {
+    const int g = p.Hq / p.Hkv;
+    int b, lu, rows, rowbase, kind;
+    if (u < p.n_cross_units) {
+        kind = 1;
+        int lo = 0, hi = p.B - 1;  // last b with cross_unit_indptr[b] <= u
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.cross_unit_indptr[mid] <= u) lo = mid; else hi = mid - 1;
+        }
+        b = lo;
+        lu = u - p.cross_unit_indptr[b];
+        rowbase = p.out_indptr[b];
+        rows = p.out_indptr[b + 1] - rowbase;
+    } else {
+        kind = 0;
+        lu = u - p.n_cross_units;
+        const int upb = p.Hkv * units_per_kv(p.base_nblk, g);
+        b = lu / upb;
+        lu -= b * upb;
+        rowbase = 0;
+        rows = p.T;
+    }
+    const int nblk = (rows + kRowsPerTile - 1) / kRowsPerTile;
+    const int upk = units_per_kv(nblk, g);
+    const int kv = lu / upk;
+    const int q = upk - 1 - (lu - kv * upk);
+    int blk0, blk1, h0, h1;
+    if (g % 2 == 0) {
+        blk0 = blk1 = q / (g / 2);
+        h0 = kv * g + 2 * (q % (g / 2));
+        h1 = h0 + 1;
+    } else {
+        const int per = (nblk + 1) / 2;
+        h0 = h1 = kv * g + q / per;
+        blk0 = 2 * (q % per);
+        blk1 = blk0 + 1;
+    }
+    s0.kind = kind;
+    s0.b = b;
+    s0.h = h0;
+    s0.row0 = rowbase + blk0 * kRowsPerTile;
+    s0.n = min(kRowsPerTile, rows - blk0 * kRowsPerTile);
+    s1.kind = blk1 < nblk ? kind : -1;
+    s1.b = b;
+    s1.h = h1;
+    s1.row0 = rowbase + blk1 * kRowsPerTile;
+    s1.n = blk1 < nblk ? min(kRowsPerTile, rows - blk1 * kRowsPerTile) : 0;
+}
+
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                   "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]),
+                   "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]),
+                   "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
+}
+
+// Byte offset of (row, 16-byte chunk c) inside a 128B-swizzled tile of D columns.
+template <int D>
+__device__ __forceinline__ uint32_t sw128_offset(int row, int c) {
+    const int sub = c >> 3;  // 64-column atom
+    const int cc = c & 7;
+    return sub * (kRowsPerTile * 128) + row * 128 + ((cc ^ (row & 7)) << 4);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                      const TcParams p) {
+    using C = Cfg<D>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Meta &mt = *reinterpret_cast<Meta *>(smem + C::kBar);
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    volatile int *abort = &mt.abort;
+
+    Slot sl0, sl1;
+    decode_unit(p, blockIdx.x, sl0, sl1);
+
+    if (tid == 0) {
+        for (int i = 0; i < kNumK; ++i) {
+            mbar_init(&mt.k_full[i], 1);
+            mbar_init(&mt.k_empty[i], 1);
+        }
+        for (int i = 0; i < kNumV; ++i) {
+            mbar_init(&mt.v_full[i], 1);
+            mbar_init(&mt.v_empty[i], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&mt.s_full[s], 1);
+            mbar_init(&mt.p_full[s], kRowsPerTile);
+            mbar_init(&mt.o_full[s], 1);
+            mt.t_min[s] = 0x7fffffff;
+            mt.t_max[s] = -1;
+        }
+        mbar_init(&mt.mma_done, 1);
+        mt.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+    }
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tmem_alloc(&mt.tmem_base, 512);
+        tmem_relinquish();
+    }
+
+    // ---------------- prologue: stage both query tiles (affine fused) ----------------
+    const int s_me = tid >> 7;  // softmax slot of this thread (valid for tid < 256)
+    const int row = tid & 127;
+    int my_t = 0;
+    bool my_valid = false, my_bad = false;
+    if (tid < 256) {
+        const Slot S = s_me ? sl1 : sl0;
+        if (S.kind >= 0 && row < S.n) {
+            my_t = S.kind == 0 ? S.row0 + row : p.out_positions[S.row0 + row];
+            my_valid = my_t >= 0 && my_t < p.T;
+            my_bad = !my_valid;
+            if (my_bad) set_status(p.status, ORTHROS_DEV_BAD_POSITION);
+        }
+        uint8_t *qs = smem + C::kQ0 + s_me * C::kTileBytes;
+        if (my_valid) {
+            const __nv_bfloat16 *src;
+            if (S.kind == 1 && p.q_out)
+                src = p.q_out + ((long long)S.row0 + row) * p.Hq * D + (long long)S.h * D;
+            else
+                src = p.q + (((long long)S.b * p.T + my_t) * p.Hq + S.h) * D;
+            const float *al = (S.kind == 0 ? p.alpha_base : p.alpha_out) + S.h * D;
+            const float *be = (S.kind == 0 ? p.beta_base : p.beta_out) + S.h * D;
+            bool over = false;
+#pragma unroll 4
+            for (int c = 0; c < D / 8; ++c) {
+                const uint4 raw = reinterpret_cast<const uint4 *>(src)[c];
+                const float4 a0 = reinterpret_cast<const float4 *>(al)[2 * c];
+                const float4 a1 = reinterpret_cast<const float4 *>(al)[2 * c + 1];
+                const float4 b0 = reinterpret_cast<const float4 *>(be)[2 * c];
+                const float4 b1 = reinterpret_cast<const float4 *>(be)[2 * c + 1];
+                const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+                float2 x0 = __bfloat1622float2(h2[0]), x1 = __bfloat1622float2(h2[1]);
+                float2 x2 = __bfloat1622float2(h2[2]), x3 = __bfloat1622float2(h2[3]);
+                float v[8] = {fmaf(a0.x, x0.x, b0.x), fmaf(a0.y, x0.y, b0.y), fmaf(a0.z, x1.x, b0.z),
+                              fmaf(a0.w, x1.y, b0.w), fmaf(a1.x, x2.x, b1.x), fmaf(a1.y, x2.y, b1.y),
+                              fmaf(a1.z, x3.x, b1.z), fmaf(a1.w, x3.y, b1.w)};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) over |= fabsf(v[e]) > 65504.f;
+                uint4 o;
+                o.x = pack_f16(v[0], v[1]);
+                o.y = pack_f16(v[2], v[3]);
+                o.z = pack_f16(v[4], v[5]);
+                o.w = pack_f16(v[6], v[7]);
+                *reinterpret_cast<uint4 *>(qs + sw128_offset<D>(row, c)) = o;
+            }
+            if (over) set_status(p.status, ORTHROS_DEV_FP16_RANGE);
+            atomicMin(&mt.t_min[s_me], my_t);
+            atomicMax(&mt.t_max[s_me], my_t);
+        } else {
+#pragma unroll 4
+            for (int c = 0; c < D / 8; ++c)
+                *reinterpret_cast<uint4 *>(qs + sw128_offset<D>(row, c)) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // ---------------- band of each tile, in key-tile units ----------------
+    // Band of each tile in key-tile units: [kt_lo, kt_hi]; lo_max = latest
+    // window start of its rows (key tiles before it need the window mask).
+    struct Band {
+        int kt_lo, kt_hi, lo_max, t_min, t_max;
+    };
+    auto band_of = [&](const Slot &S, int tmin, int tmax) {
+        Band bd;
+        bd.t_min = tmin;
+        bd.t_max = tmax;
+        if (S.kind < 0 || tmax < 0) {
+            bd.kt_lo = 1;
+            bd.kt_hi = 0;
+            bd.lo_max = 0;
+            return bd;
+        }
+        const int lo_min = S.kind == 0 ? max(0, tmin - p.window + 1) : 0;
+        bd.lo_max = S.kind == 0 ? max(0, tmax - p.window + 1) : 0;
+        bd.kt_lo = lo_min / kKeysPerTile;
+        bd.kt_hi = tmax / kKeysPerTile;
+        return bd;
+    };
+    const Band bd0 = band_of(sl0, mt.t_min[0], mt.t_max[0]);
+    const Band bd1 = band_of(sl1, mt.t_min[1], mt.t_max[1]);
+    const bool any0 = bd0.kt_lo <= bd0.kt_hi, any1 = bd1.kt_lo <= bd1.kt_hi;
+    const int kt_min = any0 && any1 ? min(bd0.kt_lo, bd1.kt_lo) : (any0 ? bd0.kt_lo : bd1.kt_lo);
+    const int kt_max = any0 && any1 ? max(bd0.kt_hi, bd1.kt_hi) : (any0 ? bd0.kt_hi : bd1.kt_hi);
+    const int n_it = (any0 || any1) ? kt_max - kt_min + 1 : 0;
+    const uint32_t tmem = mt.tmem_base;
+    const int kv = sl0.h / (p.Hq / p.Hkv);
+    const int bseq = sl0.b;
+
+    if (warp == kProducerWarp) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            for (int i = 0; i < n_it && !*abort; ++i) {
+                const int kt = kt_min + i;
+                const int sk = i % kNumK;
+                if (i >= kNumK && !mbar_wait(&mt.k_empty[sk], ((i / kNumK) - 1) & 1, abort, p.status)) break;
+                mbar_arrive_expect_tx(&mt.k_full[sk], C::kTileBytes);
+                for (int j = 0; j < C::kSub; ++j)
+                    tma_load_4d(smem + C::kK0 + sk * C::kTileBytes + j * (kKeysPerTile * 128), &tm_k,
+                                &mt.k_full[sk], 64 * j, kv, kt * kKeysPerTile, bseq);
+                const int sv = i % kNumV;
+                if (i >= kNumV && !mbar_wait(&mt.v_empty[sv], ((i / kNumV) - 1) & 1, abort, p.status)) break;
+                mbar_arrive_expect_tx(&mt.v_full[sv], C::kTileBytes);
+                for (int j = 0; j < C::kSub; ++j)
+                    tma_load_4d(smem + C::kV0 + sv * C::kTileBytes + j * (kKeysPerTile * 128), &tm_v,
+                                &mt.v_full[sv], 64 * j, kv, kt * kKeysPerTile, bseq);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ---------------- tcgen05.mma issuer ----------------
+        if (lane == 0 && n_it > 0) {
+            constexpr uint32_t kIdescS = idesc_f16(0, 0, 0, 0, kRowsPerTile, kKeysPerTile);  // fp16, K-major
+            constexpr uint32_t kIdescO = idesc_f16(1, 1, 0, 1, kRowsPerTile, D);             // bf16, V MN-major
+            const uint32_t q_base = smem_u32(smem + C::kQ0);
+            const uint32_t k_base = smem_u32(smem + C::kK0);
+            const uint32_t v_base = smem_u32(smem + C::kV0);
+            auto active = [&](int s, int kt) {
+                return s == 0 ? (kt >= bd0.kt_lo && kt <= bd0.kt_hi) : (kt >= bd1.kt_lo && kt <= bd1.kt_hi);
+            };
+            auto issue_s = [&](int s, int sk) {
+                // S_s = Q_s K^T: 16 channels per instruction; within a 128B atom the
+                // start address advances 32 bytes per step.
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks >> 2) * (kRowsPerTile * 128) + (ks & 3) * 32;
+                    const uint64_t a = desc_sw128(q_base + s * C::kTileBytes + off, 16, 1024);
+                    const uint64_t bdesc = desc_sw128(k_base + sk * C::kTileBytes + off, 16, 1024);
+                    mma_ss(tmem + s * 128, a, bdesc, kIdescS, ks > 0);
+                }
+            };
+            uint32_t pc[2] = {0, 0};
+            bool o_init[2] = {false, false};
+            bool ok = mbar_wait(&mt.k_full[0], 0, abort, p.status);
+            if (ok) {
+                tc_fence_after();
+                for (int s = 0; s < 2; ++s)
+                    if (active(s, kt_min)) {
+                        issue_s(s, 0);
+                        tc_commit(&mt.s_full[s]);
+                    }
+                tc_commit(&mt.k_empty[0]);
+            }
+            for (int i = 0; ok && i < n_it; ++i) {
+                const int kt = kt_min + i;
+                const int sv = i % kNumV;
+                if (!(ok = mbar_wait(&mt.v_full[sv], (i / kNumV) & 1, abort, p.status))) break;
+                // per tile: PV_s(i), then S_s(i+1) into the TMEM that held P_s(i)
+                // (tcgen05.mma from one thread execute in issue order)
+                auto step = [&](const int s) -> bool {
+                    if (active(s, kt)) {
+                        if (!mbar_wait(&mt.p_full[s], pc[s] & 1, abort, p.status)) return false;
+                        ++pc[s];
+                        tc_fence_after();
+                        // O_s += P_s V: 16 keys per instruction; P packed bf16x2 in the
+                        // S_s columns (8 columns per step), V rows 128 bytes apart.
+#pragma unroll
+                        for (int kk = 0; kk < kKeysPerTile / 16; ++kk) {
+                            const uint64_t bdesc =
+                                desc_sw128(v_base + sv * C::kTileBytes + kk * 16 * 128, kKeysPerTile * 128, 1024);
+                            mma_ts(tmem + C::kTmemO + s * 128, tmem + s * 128 + kk * 8, bdesc, kIdescO,
+                                   (o_init[s] || kk > 0) ? 1u : 0u);
+                        }
+                        o_init[s] = true;
+                    }
+                    if (i + 1 < n_it) {
+                        const int skn = (i + 1) % kNumK;
+                        if (s == 0) {
+                            if (!mbar_wait(&mt.k_full[skn], ((i + 1) / kNumK) & 1, abort, p.status)) return false;
+                            tc_fence_after();
+                        }
+                        if (active(s, kt + 1)) {
+                            issue_s(s, skn);
+                            tc_commit(&mt.s_full[s]);
+                        }
+                        if (s == 1) tc_commit(&mt.k_empty[skn]);
+                    }
+                    if (s == 1) tc_commit(&mt.v_empty[sv]);
+                    return true;
+                };
+                ok = step(0) && step(1);
+            }
+            tc_commit(&mt.o_full[0]);
+            tc_commit(&mt.o_full[1]);
+            tc_commit(&mt.mma_done);
+            mbar_wait(&mt.mma_done, 0, abort, p.status);
+        }
+    } else {
+        // ---------------- softmax warpgroups ----------------
+        const int s = s_me;
+        const Slot S = s ? sl1 : sl0;
+        const Band bd = s ? bd1 : bd0;
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t t_s = tmem + lane_off + s * 128;
+        const uint32_t t_o = tmem + lane_off + C::kTmemO + s * 128;
+        const int t_row = my_valid ? my_t : bd.t_max;
+        const int lo_row = S.kind == 0 ? max(0, t_row - p.window + 1) : 0;
+        const float c2 = p.scale_log2;
+        const int t_min_s = bd.t_min;
+        float m_ref = -INFINITY, l = 0.f;
+        uint32_t cnt = 0;
+        for (int i = 0; i < n_it; ++i) {
+            const int kt = kt_min + i;
+            if (kt < bd.kt_lo || kt > bd.kt_hi) continue;
+            const bool got = mbar_wait(&mt.s_full[s], cnt & 1, abort, p.status);
+            if (!__all_sync(0xffffffffu, got)) break;
+            tc_fence_after();
+            uint32_t r[4][32];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) tmem_ld32(t_s + 32 * j, r[j]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 4; ++j) reg_fence(r[j]);
+            float *x = reinterpret_cast<float *>(&r[0][0]);
+            const int key0 = kt * kKeysPerTile;
+            if (key0 + kKeysPerTile - 1 > t_min_s || key0 < bd.lo_max) {
+#pragma unroll
+                for (int c = 0; c < kKeysPerTile; ++c) {
+                    const int j = key0 + c;
+                    if (j > t_row || j < lo_row) x[c] = -INFINITY;
+                }
+            }
+            float mx = x[0];
+#pragma unroll
+            for (int c = 1; c < kKeysPerTile; ++c) mx = fmaxf(mx, x[c]);
+            const float m_new = fmaxf(m_ref, mx);
+            const bool resc = (m_new - m_ref) * c2 > 8.f;  // true on the first finite max
+            const bool any_resc = __any_sync(0xffffffffu, resc);
+            const float alpha = resc ? ex2((m_ref - m_new) * c2) : 1.f;
+            if (resc) {
+                l *= alpha;
+                m_ref = m_new;
+            }
+            const float mb = m_ref == -INFINITY ? 0.f : m_ref * c2;
+            // P in two 64-key halves (32 packed columns each), so that only
+            // half of the packed values are live next to the logits
+            float ls = 0.f;
+#pragma unroll
+            for (int hlf = 0; hlf < 2; ++hlf) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int c = 64 * hlf + 2 * e;
+                    const float p0 = ex2(fmaf(x[c], c2, -mb));
+                    const float p1 = ex2(fmaf(x[c + 1], c2, -mb));
+                    ls += p0 + p1;
+                    pk[e] = pack_bf16(p0, p1);
+                }
+                tmem_st32(t_s + 32 * hlf, pk);
+            }
+            l += ls;
+            // O_s is idle here (PV_s of the previous tile completed before S_s of
+            // this tile was signalled; the next PV_s waits for p_full), so the
+            // rescale of the running output can follow the P stores.
+            if (any_resc && cnt > 0) {
+#pragma unroll
+                for (int j = 0; j < D / 32; ++j) {
+                    uint32_t o[32];
+                    tmem_ld32(t_o + 32 * j, o);
+                    tmem_ld_wait();
+                    reg_fence(o);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tmem_st32(t_o + 32 * j, o);
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&mt.p_full[s]);
+            ++cnt;
+        }
+        // ---------------- epilogue: o = O / l, lse = scale*m + ln l ----------------
+        // tcgen05.ld is warp-collective: every lane of the warp runs the loads,
+        // padding rows of a ragged tile only skip the stores.
+        bool have = cnt > 0 && mbar_wait(&mt.o_full[s], 0, abort, p.status);
+        have = __all_sync(0xffffffffu, have);
+        if (have) {
+            tc_fence_after();
+            const bool store = S.kind >= 0 && row < S.n;
+            __nv_bfloat16 *dst = nullptr;
+            float *lse_dst = nullptr;
+            if (store && S.kind == 0) {
+                dst = p.o_base + (((long long)S.b * p.T + my_t) * p.Hq + S.h) * D;
+                lse_dst = p.lse_base + ((long long)S.b * p.Hq + S.h) * p.T + my_t;
+            } else if (store) {
+                dst = p.o_out + ((long long)(S.row0 + row) * p.Hq + S.h) * D;
+                lse_dst = p.lse_out + (long long)(S.row0 + row) * p.Hq + S.h;
+            }
+            const float inv = my_bad ? __int_as_float(0x7fc00000) : 1.f / l;
+#pragma unroll
+            for (int j = 0; j < D / 32; ++j) {
+                uint32_t o[32];
+                tmem_ld32(t_o + 32 * j, o);
+                tmem_ld_wait();
+                reg_fence(o);
+                if (store) {
+                    uint4 w[4];
+                    uint32_t *wp = reinterpret_cast<uint32_t *>(w);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        wp[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) reinterpret_cast<uint4 *>(dst + 32 * j)[e] = w[e];
+                }
+            }
+            if (store) *lse_dst = my_bad ? __int_as_float(0x7fc00000) : m_ref * p.scale + logf(l);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// [B, T, Hkv, D] 2-byte elements -> 4-D map (D, Hkv, T, B), box (64, 1, 128, 1).
+bool make_kv_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int B, int T, int Hkv, int D) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)T, (cuuint64_t)B};
+    cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2, (cuuint64_t)T * Hkv * D * 2};
+    cuuint32_t box[4] = {64, 1, kKeysPerTile, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(m, dt, 4, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_d(const TcParams &p, const void *k16, const void *v, int units, cudaStream_t stream) {
+    CUtensorMap tk, tv;
+    if (!make_kv_map(&tk, k16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.B, p.T, p.Hkv, D) ||
+        !make_kv_map(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.B, p.T, p.Hkv, D))
+        return cudaErrorInvalidValue;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Cfg<D>::kSmem);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    prefill_tc_kernel<D><<<units, kThreads, Cfg<D>::kSmem, stream>>>(tk, tv, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int tc_units_per_kv(int nblk, int g) { return (g % 2 == 0) ? nblk * (g / 2) : g * ((nblk + 1) / 2); }
+
+cudaError_t launch_prefill_tc(const TcParams &p, const void *k16, const void *v, int d, cudaStream_t stream) {
+    const int units = p.n_cross_units + p.n_base_units;
+    if (units == 0) return cudaSuccess;
+    return d == 128 ? launch_d<128>(p, k16, v, units, stream) : launch_d<64>(p, k16, v, units, stream);
+}
+
+}  // namespace orthros
