@@ -233,20 +233,29 @@ def run_reference(args, dist):
 # ----------------------------------------------------------------------------
 # the GPU arm
 # ----------------------------------------------------------------------------
-def run_ours(args, dist):
-    import torch
+def _timed(ola, torch, dist, stream, fn, steps):
+    """Run fn(i) for i < steps between two CUDA events on `stream`, with the
+    library's per-kernel event profiling on. Returns (max-over-ranks ms, profile)."""
+    dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ola.orthros_profile_begin()
+    ev0.record(stream)
+    for i in range(steps):
+        fn(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    prof = ola.orthros_profile_end()
+    dist.barrier()
+    return dist.max(ev0.elapsed_time(ev1)), prof
 
-    import efficient_long_context_gb300 as ola
-    from efficient_long_context_gb300 import build as B
-    from efficient_long_context_gb300 import workloads as W
 
-    B.build()
-    torch.cuda.set_device(dist.local)
-    dev = torch.device("cuda", dist.local)
-    peaks = load_peaks()
-
-    # ---------------- prefill workload, resident in HBM ----------------
+def bench_prefill(args, dist, dev, stream, peaks, ola, torch, W):
     wl = W.PREFILL_128K
+    if args.prefill_T:
+        import dataclasses
+
+        wl = dataclasses.replace(wl, T=args.prefill_T, name=f"{wl.name}@T{args.prefill_T}")
     inputs = W.make_prefill(wl)
     q, k, v = (inputs[n].to(dev) for n in ("q", "k", "v"))
     aff = [inputs[n].to(dev) for n in ("alpha_base", "beta_base", "alpha_out", "beta_out")]
@@ -259,55 +268,70 @@ def run_ours(args, dist):
     k_cache = torch.empty((num_pages, P, wl.Hkv, wl.d), dtype=wl.dtype, device=dev)
     v_cache = torch.empty_like(k_cache)
     block_table = torch.arange(num_pages, dtype=torch.int32, device=dev).view(wl.B, max_pages)
-    o_base = torch.empty_like(q)
-    lse_base = torch.empty((wl.B, wl.Hq, wl.T), dtype=torch.float32, device=dev)
-    o_out = torch.empty((n_out, wl.Hq, wl.d), dtype=wl.dtype, device=dev)
-    lse_out = torch.empty((n_out, wl.Hq), dtype=torch.float32, device=dev)
+    outs = (torch.empty_like(q), torch.empty((wl.B, wl.Hq, wl.T), dtype=torch.float32, device=dev),
+            torch.empty((n_out, wl.Hq, wl.d), dtype=wl.dtype, device=dev),
+            torch.empty((n_out, wl.Hq), dtype=torch.float32, device=dev))
     ws = torch.empty(ola.orthros_prefill_workspace_size(wl.B, wl.T, wl.Hq, wl.Hkv, wl.d, n_out, wl.window,
                                                         wl.dtype), dtype=torch.uint8, device=dev)
-    outs = (o_base, lse_base, o_out, lse_out)
-    stream = torch.cuda.current_stream(dev)
 
-    def prefill_step():
+    def step(_=0):
         ola.orthros_prefill(q, k, v, *aff, indptr, pos, wl.window, wl.scale, out=outs, k_cache=k_cache,
                             v_cache=v_cache, block_table=block_table, page_size=P, workspace=ws, stream=stream)
 
-    flops = prefill_flops(wl, [int(t) for t in inputs["out_positions"]])
+    positions = [int(t) for t in inputs["out_positions"]]
+    flops = prefill_flops(wl, positions)
     for _ in range(max(args.warmup, 3)):
-        prefill_step()
+        step()
     torch.cuda.synchronize()
     rc, bits = ola.orthros_check(ws)
     if rc != 0:
         raise RuntimeError(f"prefill flagged device status {rc} bits 0x{bits:x}")
+    ms, prof = _timed(ola, torch, dist, stream, step, args.steps)
+    ms_step = ms / args.steps
+    # dominant kernel and the useful FLOPs it alone performs: the base stream,
+    # plus output rows of sequences dense enough to go to the tile kernel
+    dom, (dom_n, dom_ms) = max(prof.items(), key=lambda kv: kv[1][1])
+    g = wl.Hq // wl.Hkv
+    per_seq = [positions[int(indptr[b]):int(indptr[b + 1])] for b in range(wl.B)]
+    tile_cross = sum(sum(t + 1 for t in ps) for ps in per_seq if len(ps) * g > 256) * 4 * wl.d * wl.Hq
+    dom_flops = flops["swa"] + tile_cross if dom == "prefill_tc" else flops["total"]
+    achieved = dom_flops / (dom_ms / dom_n * 1e-3) / 1e12
+    res = dict(wl=wl, inputs=inputs, flops=flops, ms_step=ms_step, prof=prof, P=P,
+               value=flops["total"] * dist.world / (ms_step * 1e-3) / 1e12,
+               roofline={"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peaks["bf16"],
+                         "unit": "TFLOP/s", "frac": achieved / peaks["bf16"], "traffic": None,
+                         "peak_source": f"{peaks['src']} bf16 dense (burst)", "avg_launch_ms": dom_ms / dom_n,
+                         "useful_tflop_per_launch": dom_flops / 1e12})
+    if args.only == "all":
+        # end to end: pinned host buffers, host<->device copies inside the timed region
+        h_in = {n: inputs[n].pin_memory() for n in ("q", "k", "v")}
+        h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
 
-    clocks = ClockSampler(dist.local)
-    clocks.start()
-    time.sleep(0.3)
-    dist.barrier()
-    torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ola.orthros_profile_begin()
-    ev0.record(stream)
-    for _ in range(args.steps):
-        prefill_step()
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    prof = ola.orthros_profile_end()
-    dist.barrier()
-    ms_local = ev0.elapsed_time(ev1)
-    ms_total = dist.max(ms_local)
-    ms_step = ms_total / args.steps
-    value = flops["total"] * dist.world / (ms_step * 1e-3) / 1e12
+        def e2e_step(_):
+            q.copy_(h_in["q"], non_blocking=True)
+            k.copy_(h_in["k"], non_blocking=True)
+            v.copy_(h_in["v"], non_blocking=True)
+            step()
+            for hbuf, dbuf in zip(h_out, outs):
+                hbuf.copy_(dbuf, non_blocking=True)
 
-    # dominant kernel: the banded base-stream kernel
-    dom_name, (dom_launches, dom_ms) = max(prof.items(), key=lambda kv: kv[1][1])
-    dom_avg_ms = dom_ms / dom_launches
-    dom_flops = flops["swa"] if "base" in dom_name or "prefill_tc" in dom_name else flops["total"]
-    achieved = dom_flops / (dom_avg_ms * 1e-3) / 1e12
-    launches = sum(n for n, _ in prof.values())
+        e2e_steps = max(1, min(args.steps, 3))
+        e2e_step(0)
+        ms_e2e, _ = _timed(ola, torch, dist, stream, e2e_step, e2e_steps)
+        ms_e2e /= e2e_steps
+        res["e2e"] = {"value": flops["total"] * dist.world / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+                      "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in h_in.values()),
+                      "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in h_out),
+                      "ms_per_step": ms_e2e, "steps": e2e_steps}
+    return res
 
-    # ---------------- decoding workload ----------------
+
+def bench_decode(args, dist, dev, stream, peaks, ola, torch, W):
+    import dataclasses
+
     dec = W.DECODE_32
+    if args.decode_B:
+        dec = dataclasses.replace(dec, B=args.decode_B, name=f"{dec.name}@B{args.decode_B}")
     st = W.make_decode(dec, steps=args.decode_steps)
     dm = st.meta
     kc, vc = st.k_cache.to(dev), st.v_cache.to(dev)
@@ -315,99 +339,86 @@ def run_ours(args, dist):
     lens_steps = (st.cache_lens[None, :].to(torch.int64) + torch.arange(dm["steps"])[:, None]).to(torch.int32).to(dev)
     dq, dk, dv = st.q.to(dev), st.k_new.to(dev), st.v_new.to(dev)
     daff = [a.to(dev) for a in (st.alpha_base, st.beta_base, st.alpha_out, st.beta_out)]
-    d_ob = torch.empty((dec.B, dec.Hq, dec.d), dtype=dec.dtype, device=dev)
-    d_oo = torch.empty_like(d_ob)
-    d_lb = torch.empty((dec.B, dec.Hq), dtype=torch.float32, device=dev)
-    d_lo = torch.empty_like(d_lb)
-    d_ws = torch.empty(ola.orthros_decode_workspace_size(dec.B, dec.Hq, dec.Hkv, dec.d, dm["max_pages"], dec.page_size,
-                                                         dec.dtype), dtype=torch.uint8, device=dev)
-    d_outs = (d_ob, d_lb, d_oo, d_lo)
+    outs = (torch.empty((dec.B, dec.Hq, dec.d), dtype=dec.dtype, device=dev),
+            torch.empty((dec.B, dec.Hq), dtype=torch.float32, device=dev),
+            torch.empty((dec.B, dec.Hq, dec.d), dtype=dec.dtype, device=dev),
+            torch.empty((dec.B, dec.Hq), dtype=torch.float32, device=dev))
+    ws = torch.empty(ola.orthros_decode_workspace_size(dec.B, dec.Hq, dec.Hkv, dec.d, dm["max_pages"], dec.page_size,
+                                                       dec.dtype), dtype=torch.uint8, device=dev)
 
-    def decode_step(s):
+    def step(s):
         ola.orthros_decode(dq[s], dk[s], dv[s], kc, vc, bt, lens_steps[s], *daff, dec.window, dec.scale,
-                           out=d_outs, workspace=d_ws, stream=stream)
+                           out=outs, workspace=ws, stream=stream)
 
-    for s in range(max(args.warmup, 3)):
-        decode_step(s)
+    for s in range(min(max(args.warmup, 3), dm["steps"])):
+        step(s)
     torch.cuda.synchronize()
-    rc, bits = ola.orthros_check(d_ws)
+    rc, bits = ola.orthros_check(ws)
     if rc != 0:
         raise RuntimeError(f"decode flagged device status {rc} bits 0x{bits:x}")
-    dist.barrier()
-    ola.orthros_profile_begin()
-    ev0.record(stream)
-    for s in range(dm["steps"]):
-        decode_step(s)
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    dprof = ola.orthros_profile_end()
-    clk = clocks.stop()
-    d_ms = dist.max(ev0.elapsed_time(ev1))
-    d_bytes = decode_bytes(st.cache_lens.tolist(), dm["steps"], dec.Hkv, dec.d)
-    d_gbs = d_bytes * dist.world / (d_ms * 1e-3) / 1e9
-    d_dom, (d_dom_n, d_dom_ms) = max(dprof.items(), key=lambda kv: kv[1][1])
-    d_achieved = d_bytes / (d_dom_ms * 1e-3) / 1e9  # bytes of all steps / summed time of that kernel
-    del kc, vc, dq, dk, dv
-
-    # ---------------- end to end: host buffers, copies inside the timed region ----------------
-    h_in = {n: inputs[n].pin_memory() for n in ("q", "k", "v")}
-    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
-    e2e_steps = max(1, min(args.steps, 3))
-    prefill_step()
-    torch.cuda.synchronize()
-    dist.barrier()
-    ev0.record(stream)
-    for _ in range(e2e_steps):
-        q.copy_(h_in["q"], non_blocking=True)
-        k.copy_(h_in["k"], non_blocking=True)
-        v.copy_(h_in["v"], non_blocking=True)
-        prefill_step()
-        for hbuf, dbuf in zip(h_out, outs):
-            hbuf.copy_(dbuf, non_blocking=True)
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = dist.max(ev0.elapsed_time(ev1)) / e2e_steps
-    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in h_out)
-    e2e_value = flops["total"] * dist.world / (e2e_ms * 1e-3) / 1e12
-
-    # ---------------- CPU baseline (rank 0, N = 1 only) ----------------
-    cpu = None
-    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
-        v_cpu, cores, desc = oracle_sample(inputs, wl, args.cpu_seconds)
-        cpu = {"value": v_cpu, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
-
-    if dist.rank == 0:
-        line = {
-            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": dist.world, "steps": args.steps,
-            "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic (seeded N(0,1) q/k/v, affines 1+0.1N / 0.1N; no dataset)",
-            "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
-                       "window": wl.window, "out_rows": "last position (prefill regime)", "page_size": P,
-                       "useful_tflop_per_step": flops["total"] / 1e12,
-                       "l2": "inputs larger than L2 (q 1 GiB, k/v 256 MiB each)",
-                       "parallelism": f"replicas x{dist.world}"},
-            "roofline": {"bound": "tensor", "kernel": dom_name, "achieved": achieved, "peak": peaks["bf16"],
-                         "unit": "TFLOP/s", "frac": achieved / peaks["bf16"], "traffic": None,
-                         "peak_source": f"{peaks['src']} bf16 dense (burst)",
-                         "avg_launch_ms": dom_avg_ms},
+    ms, prof = _timed(ola, torch, dist, stream, step, dm["steps"])
+    nbytes = decode_bytes(st.cache_lens.tolist(), dm["steps"], dec.Hkv, dec.d)
+    gbs = nbytes * dist.world / (ms * 1e-3) / 1e9
+    dom, (dom_n, dom_ms) = max(prof.items(), key=lambda kv: kv[1][1])
+    achieved = nbytes / (dom_ms * 1e-3) / 1e9  # bytes of all steps over that kernel's summed time
+    return {"value": gbs, "unit": "GB/s", "workload": dec.name, "steps": dm["steps"], "ms_per_step": ms / dm["steps"],
+            "bytes": nbytes, "frac_of_hbm": gbs / peaks["hbm"],
+            "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm"], "traffic": None, "peak_source": f"{peaks['src']} HBM copy",
+                         "avg_launch_ms": dom_ms / dom_n, "bytes_per_launch": nbytes / dm["steps"]},
             "kernels": {n: {"launches": c, "total_ms": t} for n, (c, t) in prof.items()},
-            "gpu_launches": launches,
-            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": e2e_ms, "steps": e2e_steps},
-            "decode": {"value": d_gbs, "unit": "GB/s", "workload": dec.name, "steps": dm["steps"],
-                       "ms_per_step": d_ms / dm["steps"], "bytes": d_bytes,
-                       "roofline": {"bound": "hbm", "kernel": d_dom, "achieved": d_achieved, "peak": peaks["hbm"],
-                                    "unit": "GB/s", "frac": d_achieved / peaks["hbm"], "traffic": None,
-                                    "peak_source": f"{peaks['src']} HBM copy"},
-                       "frac_of_hbm": d_gbs / peaks["hbm"],
-                       "kernels": {n: {"launches": c, "total_ms": t} for n, (c, t) in dprof.items()},
-                       "gpu_launches": sum(n for n, _ in dprof.values())},
-            "cpu_baseline": cpu,
-            "clocks": clk,
-        }
-        print(json.dumps(line), flush=True)
+            "gpu_launches": sum(n for n, _ in prof.values())}
+
+
+def run_ours(args, dist):
+    import torch
+
+    import efficient_long_context_gb300 as ola
+    from efficient_long_context_gb300 import build as B
+    from efficient_long_context_gb300 import workloads as W
+
+    B.build()
+    torch.cuda.set_device(dist.local)
+    dev = torch.device("cuda", dist.local)
+    stream = torch.cuda.current_stream(dev)
+    peaks = load_peaks()
+    clocks = ClockSampler(dist.local)
+    clocks.start()
+    pre = dec = None
+    if args.only in ("all", "prefill"):
+        pre = bench_prefill(args, dist, dev, stream, peaks, ola, torch, W)
+    if args.only in ("all", "decode"):
+        dec = bench_decode(args, dist, dev, stream, peaks, ola, torch, W)
+    clk = clocks.stop()
+    cpu = None
+    if pre is not None and dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        v_cpu, cores, desc = oracle_sample(pre["inputs"], pre["wl"], args.cpu_seconds)
+        cpu = {"value": v_cpu, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
+    if dist.rank != 0:
+        return
+    if pre is None:  # decode-only profiling run
+        print(json.dumps({"decode": dec, "clocks": clk}), flush=True)
+        return
+    wl = pre["wl"]
+    line = {
+        "metric": METRIC, "value": pre["value"], "unit": "TFLOP/s", "n_gpus": dist.world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": pre["ms_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/k/v, affines 1+0.1N / 0.1N; no dataset)",
+        "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
+                   "window": wl.window, "out_rows": "last position (prefill regime)", "page_size": pre["P"],
+                   "useful_tflop_per_step": pre["flops"]["total"] / 1e12,
+                   "l2": "inputs larger than L2 (q 1 GiB, k/v 256 MiB each); no flush",
+                   "parallelism": f"replicas x{dist.world}"},
+        "roofline": pre["roofline"],
+        "kernels": {n: {"launches": c, "total_ms": t} for n, (c, t) in pre["prof"].items()},
+        "gpu_launches": sum(n for n, _ in pre["prof"].values()),
+        "e2e": pre.get("e2e"),
+        "decode": dec,
+        "cpu_baseline": cpu,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
 
 
 def main():
@@ -418,6 +429,11 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--decode-steps", type=int, default=None,
                     help="decoding steps to time (default: the workload's 128)")
+    ap.add_argument("--only", choices=("all", "prefill", "decode"), default="all",
+                    help="run one part (profiling captures); the headline line needs 'all'")
+    ap.add_argument("--prefill-T", type=int, default=None,
+                    help="shorter prefill (a smaller case of the same kernels, for profiler captures)")
+    ap.add_argument("--decode-B", type=int, default=None, help="fewer decoding sequences (profiler captures)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target length of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

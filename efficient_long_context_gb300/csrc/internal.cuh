@@ -57,6 +57,10 @@ struct RowsArgs {
 
 enum RowKind { kPrefillBase = 0, kPrefillOut = 1, kDecodePair = 2 };
 
+// orthros_api.cu: records the message returned by orthros_last_error() and
+// passes the status through.
+orthros_status report_error(orthros_status s, const char *fmt, ...);
+
 // profile.cu: brackets one kernel launch with CUDA events while profiling is on.
 class ProfScope {
   public:

@@ -92,6 +92,17 @@ orthros_status check_shapes(int B, int Hq, int Hkv, int d, int window, float sca
 }
 
 }  // namespace
+
+orthros_status report_error(orthros_status s, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
 }  // namespace orthros
 
 using namespace orthros;
