@@ -14,6 +14,7 @@ from ._binding import (  # noqa: F401
     load_library,
     orthros_check,
     orthros_decode,
+    orthros_decode_static,
     orthros_decode_workspace_size,
     orthros_last_error,
     orthros_prefill,

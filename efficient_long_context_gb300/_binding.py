@@ -22,7 +22,7 @@ STATUS_NAMES = {0: "ORTHROS_OK", 1: "ORTHROS_EINVAL", 2: "ORTHROS_EUNSUPPORTED",
 
 # the public symbols of include/orthros_attn.h
 EXPORTS = ("orthros_prefill_workspace_size", "orthros_prefill", "orthros_decode_workspace_size",
-           "orthros_decode", "orthros_check", "orthros_profile_begin", "orthros_profile_end",
+           "orthros_decode", "orthros_decode_static", "orthros_check", "orthros_profile_begin", "orthros_profile_end",
            "orthros_status_string", "orthros_last_error")
 
 
@@ -65,6 +65,10 @@ def load_library(path: str | None = None):
         lib.orthros_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp,
                                        vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float, i32,
                                        vp, vp, vp, vp, vp, sz, vp]
+        lib.orthros_decode_static.restype = i32
+        lib.orthros_decode_static.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp,
+                                              vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float, i32,
+                                              vp, vp, vp, vp, vp]
         lib.orthros_check.restype = i32
         lib.orthros_check.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
         lib.orthros_profile_begin.restype = i32
@@ -204,6 +208,31 @@ def orthros_decode(q, k_new, v_new, k_cache, v_cache, block_table, cache_lens, a
         B, Hq, Hkv, d, int(window), float(scale), _dtype(q),
         _ptr(o_base), _ptr(lse_base), _ptr(o_out), _ptr(lse_out),
         _ptr(workspace), workspace.numel(), _stream(stream))
+    _raise_if(rc, lib)
+    return o_base, lse_base, o_out, lse_out
+
+
+def orthros_decode_static(q, k_new, v_new, k_cache, v_cache, block_table, cache_lens, alpha_base, beta_base,
+                          alpha_out, beta_out, window, scale=None, *, q_out=None, out=None, stream=None):
+    """orthros_decode_static of include/orthros_attn.h: orthros_decode with the
+    library's built-in scratch array instead of a caller workspace."""
+    lib = load_library()
+    B, Hq, d = q.shape
+    Hkv = k_new.shape[1]
+    num_pages, page_size = k_cache.shape[0], k_cache.shape[1]
+    max_pages = block_table.shape[1]
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = (torch.empty_like(q), torch.empty((B, Hq), dtype=torch.float32, device=q.device),
+               torch.empty_like(q), torch.empty((B, Hq), dtype=torch.float32, device=q.device))
+    o_base, lse_base, o_out, lse_out = out
+    rc = lib.orthros_decode_static(
+        _ptr(q), _ptr(q_out), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+        max_pages, page_size, num_pages, _ptr(cache_lens),
+        _ptr(alpha_base), _ptr(beta_base), _ptr(alpha_out), _ptr(beta_out),
+        B, Hq, Hkv, d, int(window), float(scale), _dtype(q),
+        _ptr(o_base), _ptr(lse_base), _ptr(o_out), _ptr(lse_out), _stream(stream))
     _raise_if(rc, lib)
     return o_base, lse_base, o_out, lse_out
 

@@ -159,6 +159,33 @@ ORTHROS_API orthros_status orthros_decode(
     void *workspace, size_t workspace_bytes, orthros_stream_t stream);
 
 /*
+ * orthros_decode without a workspace argument, for callers that cannot
+ * allocate device memory where they run a decoding step (for example a host
+ * framework whose operator interface passes only inputs and outputs, or a
+ * serving loop whose allocator must not grow). The paper has no counterpart:
+ * this is a deployment convenience, not part of the method.
+ *
+ * Same arguments, semantics and results as orthros_decode, minus workspace.
+ * Scratch comes from one 32 MiB device array inside the library (held by
+ * every GPU that loads it until the process exits); sizes whose
+ * orthros_decode_workspace_size() exceeds that return ORTHROS_EWORKSPACE
+ * before any launch. The first call on a device looks up the array's address
+ * (cudaGetSymbolAddress) with that device current: make it before any stream
+ * capture. All calls share the array: calls ordered on one stream are fine,
+ * calls that overlap on the GPU race. Device-side status bits of this entry
+ * point are not exposed; rows with bad data come back as NaN.
+ */
+ORTHROS_API orthros_status orthros_decode_static(
+    const void *q, const void *q_out, const void *k_new, const void *v_new,
+    void *k_cache, void *v_cache, const int32_t *block_table, int max_pages,
+    int page_size, int num_pages, const int32_t *cache_lens,
+    const float *alpha_base, const float *beta_base,
+    const float *alpha_out, const float *beta_out,
+    int B, int Hq, int Hkv, int d, int window, float scale, orthros_dtype dtype,
+    void *o_base, float *lse_base, void *o_out, float *lse_out,
+    orthros_stream_t stream);
+
+/*
  * Synchronises `stream`, reads the status word that the last call using
  * `workspace` left there and returns ORTHROS_OK, ORTHROS_EDEVICE (data bits) or
  * ORTHROS_ETIMEOUT (timeout bit). *bits (if not NULL) receives the raw
