@@ -9,7 +9,7 @@
 // kernel (those of sequences with many output rows; sequences with few output
 // rows take the split-KV kernel instead).
 //
-// Design (one CTA per SM, 320 threads):
+// Design (one CTA per SM, 384 threads):
 //   * A work unit is two 128-row query tiles that read the SAME key/value
 //     tiles: two query heads of one GQA group at the same positions, or (when
 //     the group size is odd, e.g. plain multi-head) two consecutive row blocks
@@ -20,6 +20,7 @@
 //   * warp 9 (one thread): tcgen05.mma issuer. S_s = Q_s K^T (M=128, N=128,
 //     fp16 operands from shared memory) into TMEM; O_s += P_s V (M=128, N=d,
 //     P read from TMEM as bf16, V from shared memory, MN-major).
+//   * warps 10-11 only fill the third warpgroup (setmaxnreg acts per warpgroup).
 //   * warps 0-3 / 4-7: softmax of tile 0 / tile 1. Thread i owns row i (TMEM
 //     lane i): it reads its 128 logits with tcgen05.ld, masks the two band
 //     edge tiles, keeps a running max with lazy rescaling (O in TMEM is only
@@ -46,9 +47,14 @@ namespace {
 
 constexpr int kRowsPerTile = 128;  // M of every MMA, rows of a query tile
 constexpr int kKeysPerTile = 128;  // N of QK^T, K of PV
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;  // 3 warpgroups: softmax 0, softmax 1, producer + MMA (+ 2 idle warps)
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+// Register split after the prologue. Launch: 384 threads x 168 = 64512 registers.
+// Softmax warpgroups 2 x 128 x 216 + control warpgroup 128 x 64 = 63488 <= 64512.
+constexpr int kRegsSoftmax = 216;
+constexpr int kRegsControl = 64;
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsControl <= kThreads * 168, "register split exceeds the launch");
 constexpr int kNumK = 3;  // key stages
 constexpr int kNumV = 2;  // value stages
 
@@ -287,6 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kv = sl0.h / (p.Hq / p.Hkv);
     const int bseq = sl0.b;
 
+    if (warp >= 8) {
+    regs_dec<kRegsControl>();
     if (warp == kProducerWarp) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
@@ -383,7 +391,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_commit(&mt.mma_done);
             mbar_wait(&mt.mma_done, 0, abort, p.status);
         }
+    }
+    regs_inc<168>();
     } else {
+        regs_inc<kRegsSoftmax>();
         // ---------------- softmax warpgroups ----------------
         const int s = s_me;
         const Slot S = s ? sl1 : sl0;
@@ -418,9 +429,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (j > t_row || j < lo_row) x[c] = -INFINITY;
                 }
             }
-            float mx = x[0];
+            // row max: 8 independent three-input max chains, then a short tree
+            float mq[8];
 #pragma unroll
-            for (int c = 1; c < kKeysPerTile; ++c) mx = fmaxf(mx, x[c]);
+            for (int j = 0; j < 8; ++j) mq[j] = fmaxf(x[2 * j], x[2 * j + 1]);
+#pragma unroll
+            for (int c = 16; c < kKeysPerTile; c += 16)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) mq[j] = max3(mq[j], x[c + 2 * j], x[c + 2 * j + 1]);
+            const float mx = max3(max3(mq[0], mq[1], mq[2]), max3(mq[3], mq[4], mq[5]), fmaxf(mq[6], mq[7]));
             const float m_new = fmaxf(m_ref, mx);
             const bool resc = (m_new - m_ref) * c2 > 8.f;  // true on the first finite max
             const bool any_resc = __any_sync(0xffffffffu, resc);
@@ -432,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float mb = m_ref == -INFINITY ? 0.f : m_ref * c2;
             // P in two 64-key halves (32 packed columns each), so that only
             // half of the packed values are live next to the logits
-            float ls = 0.f;
+            float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // independent partial sums
 #pragma unroll
             for (int hlf = 0; hlf < 2; ++hlf) {
                 uint32_t pk[32];
@@ -441,12 +458,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int c = 64 * hlf + 2 * e;
                     const float p0 = ex2(fmaf(x[c], c2, -mb));
                     const float p1 = ex2(fmaf(x[c + 1], c2, -mb));
-                    ls += p0 + p1;
+                    ls[e & 7] += p0 + p1;
                     pk[e] = pack_bf16(p0, p1);
                 }
                 tmem_st32(t_s + 32 * hlf, pk);
             }
-            l += ls;
+            l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
             // O_s is idle here (PV_s of the previous tile completed before S_s of
             // this tile was signalled; the next PV_s waits for p_full), so the
             // rescale of the running output can follow the P stores.
@@ -503,6 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (store) *lse_dst = my_bad ? __int_as_float(0x7fc00000) : m_ref * p.scale + logf(l);
         }
+        regs_dec<168>();
     }
 
     tc_fence_before();
@@ -552,6 +570,12 @@ cudaError_t launch_d(const TcParams &p, const void *k16, const void *v, int unit
         cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              Cfg<D>::kSmem);
         if (e != cudaSuccess) return e;
+        // setmaxnreg.inc waits for registers the CTA was launched with: refuse to
+        // launch a build whose per-thread count cannot cover the split.
+        cudaFuncAttributes fa{};
+        e = cudaFuncGetAttributes(&fa, prefill_tc_kernel<D>);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs * kThreads < 2 * 128 * kRegsSoftmax + 128 * kRegsControl) return cudaErrorInvalidConfiguration;
         attr_set = true;
     }
     prefill_tc_kernel<D><<<units, kThreads, Cfg<D>::kSmem, stream>>>(tk, tv, p);

@@ -1,0 +1,86 @@
+"""Bad device-side data is reported through the status word, never by a fault.
+
+Each case hands the library data that only the GPU can see is wrong; the
+kernels' own checks skip the affected rows and set a bit that orthros_check
+returns. All accesses stay in bounds (the kernels clamp before they read).
+"""
+import pytest
+import torch
+
+import efficient_long_context_gb300 as ola
+from efficient_long_context_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+DEV_BAD_POSITION, DEV_BAD_PAGE, DEV_BAD_LENGTH, DEV_FP16_RANGE = 0x1, 0x2, 0x4, 0x8
+
+
+def _prefill(wl, ws=None, **kw):
+    dev = "cuda"
+    q, k, v = (wl[n].to(dev) for n in ("q", "k", "v"))
+    aff = [wl[n].to(dev) for n in ("alpha_base", "beta_base", "alpha_out", "beta_out")]
+    if ws is None:
+        n_out = int(wl["out_indptr"][-1])
+        ws = torch.empty(ola.orthros_prefill_workspace_size(wl["B"], wl["T"], wl["Hq"], wl["Hkv"], wl["d"], n_out,
+                                                            wl["window"], wl["dtype"]), dtype=torch.uint8, device=dev)
+    out = ola.orthros_prefill(q, k, v, *aff, wl["out_indptr"], wl["out_positions"].to(dev), wl["window"],
+                              wl["scale"], workspace=ws, **kw)
+    return out, ws
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("mode", [("list", [[3, 200, 50]]), ("list", [list(range(40))])])
+def test_bad_output_position(dtype, mode):
+    wl = W.small_prefill(1, 200, 4, 2, 128, 32, dtype=dtype, out_mode=mode, seed=1)
+    wl["out_positions"][1] = 200  # == T: out of range
+    out, ws = _prefill(wl)
+    rc, bits = ola.orthros_check(ws)
+    assert rc == 5 and bits & DEV_BAD_POSITION, (rc, bits)
+    # the other rows are still right: row 0 equals a clean run's row 0
+    wl2 = dict(wl)
+    wl2["out_positions"] = wl["out_positions"].clone()
+    wl2["out_positions"][1] = 199
+    out2, ws2 = _prefill(wl2)
+    assert ola.orthros_check(ws2) == (0, 0)
+    torch.testing.assert_close(out[2][0].float(), out2[2][0].float(), rtol=0, atol=0)
+    torch.testing.assert_close(out[0].float(), out2[0].float(), rtol=0, atol=0)
+
+
+def test_key_beyond_fp16_range_is_flagged():
+    wl = W.small_prefill(1, 256, 2, 2, 128, 64, seed=2)
+    wl["k"][0, 100, 1, 5] = 70000.0
+    _, ws = _prefill(wl)
+    rc, bits = ola.orthros_check(ws)
+    assert rc == 5 and bits & DEV_FP16_RANGE, (rc, bits)
+
+
+def test_prefill_cache_fill_bad_page():
+    wl = W.small_prefill(1, 128, 2, 2, 128, 64, seed=3)
+    kc = torch.zeros((4, 64, 2, 128), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    bt = torch.tensor([[1, 9]], dtype=torch.int32, device="cuda")  # page 9 is outside the pool of 4
+    _, ws = _prefill(wl, k_cache=kc, v_cache=vc, block_table=bt, page_size=64)
+    rc, bits = ola.orthros_check(ws)
+    assert rc == 5 and bits & DEV_BAD_PAGE, (rc, bits)
+    assert torch.equal(kc[1].cpu(), wl["k"][0, :64])  # the good page was written
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_decode_bad_length_and_page(dtype):
+    wl = W.DecodeWorkload("bad", 3, 8, 2, 128, 16, 16, 0, 0, 1, dtype=dtype, seed=4)
+    st = W.make_decode(wl, lens=[5, 40, 70])
+    dev = "cuda"
+    kc, vc = st.k_cache.to(dev), st.v_cache.to(dev)
+    bt = st.block_table.clone()
+    bt[1, 1] = st.k_cache.shape[0] + 3  # a page id outside the pool, inside sequence 1's history
+    lens = st.cache_lens.clone()
+    lens[2] = bt.shape[1] * wl.page_size + 5  # past the block table
+    aff = [a.to(dev) for a in (st.alpha_base, st.beta_base, st.alpha_out, st.beta_out)]
+    ws = torch.empty(ola.orthros_decode_workspace_size(3, 8, 2, 128, bt.shape[1], 16, dtype), dtype=torch.uint8,
+                     device=dev)
+    out = ola.orthros_decode(st.q[0].to(dev), st.k_new[0].to(dev), st.v_new[0].to(dev), kc, vc, bt.to(dev),
+                             lens.to(dev), *aff, wl.window, wl.scale, workspace=ws)
+    rc, bits = ola.orthros_check(ws)
+    assert rc == 5 and bits & DEV_BAD_PAGE and bits & DEV_BAD_LENGTH, (rc, bits)
+    assert torch.isnan(out[2][2].float()).all()  # the sequence with a bad length: NaN output rows
+    assert torch.isfinite(out[0][0].float()).all()  # an untouched sequence is fine
