@@ -3,6 +3,7 @@
 // Nothing here is part of the public ABI (include/orthros_attn.h is).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -110,6 +111,7 @@ struct SplitParams {
     int B, T, Hq, Hkv, window;
     float scale, scale_log2;
     int n_groups, chunk, max_chunks;
+    long long kv_tokens;  // token rows behind k / v: prefill B*T, decode num_pages*page_size
     float *partial;  // [n_groups, max_chunks, 16, d + 2]
     __nv_bfloat16 *o_base;
     float *lse_base;
@@ -118,7 +120,14 @@ struct SplitParams {
     uint32_t *status;
 };
 size_t split_partial_bytes(int n_groups, int max_chunks, int d);
+// Runs the split kernel (the TMA-fed persistent one when eligible) and the combine.
 cudaError_t launch_splitkv(const SplitParams &p, int d, int rows_per_group, cudaStream_t stream);
+// splitkv_tma.cu
+bool splitkv_tma_eligible(const SplitParams &p);
+cudaError_t launch_splitkv_tma(const SplitParams &p, int d, int rows_per_group, cudaStream_t stream);
+// prefill_tc.cu: 3-D tensor map (d, Hkv, tokens) over bf16 [tokens, Hkv, d] rows,
+// box (64 channels, 1 head, box_tokens), 128-byte swizzle, zero fill.
+bool encode_kv_map_3d(CUtensorMap *m, const void *base, long long tokens, int Hkv, int d, int box_tokens);
 
 // simt_rows.cu: one warp per (row, head); any element type; the fp32 path.
 cudaError_t launch_rows_simt(const RowsArgs &a, RowKind kind, int d, orthros_dtype dtype,

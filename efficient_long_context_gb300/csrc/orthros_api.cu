@@ -316,6 +316,7 @@ orthros_status orthros_prefill(const void *q, const void *k, const void *v, cons
         sp.n_groups = n_groups;
         sp.chunk = kPrefillChunk;
         sp.max_chunks = lay.max_chunks;
+        sp.kv_tokens = (long long)B * T;
         sp.partial = reinterpret_cast<float *>(ws + lay.part_off);
         sp.o_out = static_cast<__nv_bfloat16 *>(o_out);
         sp.lse_out = lse_out;
@@ -435,6 +436,7 @@ orthros_status orthros_decode(const void *q, const void *q_out, const void *k_ne
         sp.n_groups = B * Hkv;
         sp.chunk = kDecodeChunk;
         sp.max_chunks = lay.max_chunks;
+        sp.kv_tokens = (long long)num_pages * page_size;
         sp.partial = reinterpret_cast<float *>(static_cast<char *>(workspace) + lay.part_off);
         sp.o_base = static_cast<__nv_bfloat16 *>(o_base);
         sp.lse_base = lse_base;

@@ -9,7 +9,7 @@
 // kernel (those of sequences with many output rows; sequences with few output
 // rows take the split-KV kernel instead).
 //
-// Design (one CTA per SM, 384 threads):
+// Design (one CTA per SM, 320 threads):
 //   * A work unit is two 128-row query tiles that read the SAME key/value
 //     tiles: two query heads of one GQA group at the same positions, or (when
 //     the group size is odd, e.g. plain multi-head) two consecutive row blocks
@@ -20,7 +20,6 @@
 //   * warp 9 (one thread): tcgen05.mma issuer. S_s = Q_s K^T (M=128, N=128,
 //     fp16 operands from shared memory) into TMEM; O_s += P_s V (M=128, N=d,
 //     P read from TMEM as bf16, V from shared memory, MN-major).
-//   * warps 10-11 only fill the third warpgroup (setmaxnreg acts per warpgroup).
 //   * warps 0-3 / 4-7: softmax of tile 0 / tile 1. Thread i owns row i (TMEM
 //     lane i): it reads its 128 logits with tcgen05.ld, masks the two band
 //     edge tiles, keeps a running max with lazy rescaling (O in TMEM is only
@@ -47,14 +46,9 @@ namespace {
 
 constexpr int kRowsPerTile = 128;  // M of every MMA, rows of a query tile
 constexpr int kKeysPerTile = 128;  // N of QK^T, K of PV
-constexpr int kThreads = 384;  // 3 warpgroups: softmax 0, softmax 1, producer + MMA (+ 2 idle warps)
+constexpr int kThreads = 320;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-// Register split after the prologue. Launch: 384 threads x 168 = 64512 registers.
-// Softmax warpgroups 2 x 128 x 216 + control warpgroup 128 x 64 = 63488 <= 64512.
-constexpr int kRegsSoftmax = 216;
-constexpr int kRegsControl = 64;
-static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsControl <= kThreads * 168, "register split exceeds the launch");
 constexpr int kNumK = 3;  // key stages
 constexpr int kNumV = 2;  // value stages
 
@@ -293,8 +287,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kv = sl0.h / (p.Hq / p.Hkv);
     const int bseq = sl0.b;
 
-    if (warp >= 8) {
-    regs_dec<kRegsControl>();
     if (warp == kProducerWarp) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
@@ -391,10 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_commit(&mt.mma_done);
             mbar_wait(&mt.mma_done, 0, abort, p.status);
         }
-    }
-    regs_inc<168>();
     } else {
-        regs_inc<kRegsSoftmax>();
         // ---------------- softmax warpgroups ----------------
         const int s = s_me;
         const Slot S = s ? sl1 : sl0;
@@ -414,29 +403,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool got = mbar_wait(&mt.s_full[s], cnt & 1, abort, p.status);
             if (!__all_sync(0xffffffffu, got)) break;
             tc_fence_after();
-            uint32_t r[4][32];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) tmem_ld32(t_s + 32 * j, r[j]);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 4; ++j) reg_fence(r[j]);
-            float *x = reinterpret_cast<float *>(&r[0][0]);
+            // Pass 1: row max from four 32-column loads (only the running maxima
+            // stay live). Pass 2 reloads the columns (one chunk prefetched) for
+            // exp / sum / bf16 pack / store, so at most two chunks are in registers.
             const int key0 = kt * kKeysPerTile;
-            if (key0 + kKeysPerTile - 1 > t_min_s || key0 < bd.lo_max) {
+            const bool edge = key0 + kKeysPerTile - 1 > t_min_s || key0 < bd.lo_max;
+            auto mask_chunk = [&](uint32_t (&r)[32], int j) {
 #pragma unroll
-                for (int c = 0; c < kKeysPerTile; ++c) {
-                    const int j = key0 + c;
-                    if (j > t_row || j < lo_row) x[c] = -INFINITY;
+                for (int c = 0; c < 32; ++c) {
+                    const int key = key0 + 32 * j + c;
+                    if (key > t_row || key < lo_row) r[c] = __float_as_uint(-INFINITY);
                 }
-            }
-            // row max: 8 independent three-input max chains, then a short tree
+            };
             float mq[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) mq[j] = fmaxf(x[2 * j], x[2 * j + 1]);
+            for (int j = 0; j < 4; ++j) {
+                uint32_t r[32];
+                tmem_ld32(t_s + 32 * j, r);
+                tmem_ld_wait();
+                reg_fence(r);
+                if (edge) mask_chunk(r, j);
+                const float *x = reinterpret_cast<const float *>(r);
 #pragma unroll
-            for (int c = 16; c < kKeysPerTile; c += 16)
-#pragma unroll
-                for (int j = 0; j < 8; ++j) mq[j] = max3(mq[j], x[c + 2 * j], x[c + 2 * j + 1]);
+                for (int q = 0; q < 8; ++q) {
+                    const float v = max3(x[4 * q], x[4 * q + 1], fmaxf(x[4 * q + 2], x[4 * q + 3]));
+                    mq[q] = j == 0 ? v : fmaxf(mq[q], v);
+                }
+            }
             const float mx = max3(max3(mq[0], mq[1], mq[2]), max3(mq[3], mq[4], mq[5]), fmaxf(mq[6], mq[7]));
             const float m_new = fmaxf(m_ref, mx);
             const bool resc = (m_new - m_ref) * c2 > 8.f;  // true on the first finite max
@@ -447,23 +440,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_ref = m_new;
             }
             const float mb = m_ref == -INFINITY ? 0.f : m_ref * c2;
-            // P in two 64-key halves (32 packed columns each), so that only
-            // half of the packed values are live next to the logits
-            float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // independent partial sums
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t ra[32], rb[32];
+            tmem_ld32(t_s, ra);
 #pragma unroll
-            for (int hlf = 0; hlf < 2; ++hlf) {
-                uint32_t pk[32];
+            for (int j = 0; j < 4; ++j) {
+                uint32_t(&cur)[32] = (j & 1) ? rb : ra;
+                uint32_t(&nxt)[32] = (j & 1) ? ra : rb;
+                tmem_ld_wait();
+                reg_fence(cur);
+                // the next chunk's columns lie above every column P has written so far
+                if (j < 3) tmem_ld32(t_s + 32 * (j + 1), nxt);
+                if (edge) mask_chunk(cur, j);
+                const float *x = reinterpret_cast<const float *>(cur);
+                uint32_t pk[16];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int c = 64 * hlf + 2 * e;
-                    const float p0 = ex2(fmaf(x[c], c2, -mb));
-                    const float p1 = ex2(fmaf(x[c + 1], c2, -mb));
-                    ls[e & 7] += p0 + p1;
+                for (int e = 0; e < 16; ++e) {
+                    const float p0 = ex2(fmaf(x[2 * e], c2, -mb));
+                    const float p1 = ex2(fmaf(x[2 * e + 1], c2, -mb));
+                    ls[e & 3] += p0 + p1;
                     pk[e] = pack_bf16(p0, p1);
                 }
-                tmem_st32(t_s + 32 * hlf, pk);
+                tmem_st16(t_s + 16 * j, pk);
             }
-            l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             // O_s is idle here (PV_s of the previous tile completed before S_s of
             // this tile was signalled; the next PV_s waits for p_full), so the
             // rescale of the running output can follow the P stores.
@@ -520,7 +520,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (store) *lse_dst = my_bad ? __int_as_float(0x7fc00000) : m_ref * p.scale + logf(l);
         }
-        regs_dec<168>();
     }
 
     tc_fence_before();
@@ -570,12 +569,6 @@ cudaError_t launch_d(const TcParams &p, const void *k16, const void *v, int unit
         cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              Cfg<D>::kSmem);
         if (e != cudaSuccess) return e;
-        // setmaxnreg.inc waits for registers the CTA was launched with: refuse to
-        // launch a build whose per-thread count cannot cover the split.
-        cudaFuncAttributes fa{};
-        e = cudaFuncGetAttributes(&fa, prefill_tc_kernel<D>);
-        if (e != cudaSuccess) return e;
-        if (fa.numRegs * kThreads < 2 * 128 * kRegsSoftmax + 128 * kRegsControl) return cudaErrorInvalidConfiguration;
         attr_set = true;
     }
     prefill_tc_kernel<D><<<units, kThreads, Cfg<D>::kSmem, stream>>>(tk, tv, p);
@@ -583,6 +576,18 @@ cudaError_t launch_d(const TcParams &p, const void *k16, const void *v, int unit
 }
 
 }  // namespace
+
+bool encode_kv_map_3d(CUtensorMap *m, const void *base, long long tokens, int Hkv, int d, int box_tokens) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)Hkv, (cuuint64_t)tokens};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)Hkv * d * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)box_tokens};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 int tc_units_per_kv(int nblk, int g) { return (g % 2 == 0) ? nblk * (g / 2) : g * ((nblk + 1) / 2); }
 

@@ -490,8 +490,11 @@ cudaError_t launch_split_t(const SplitParams &p, cudaStream_t stream) {
     const long long ctas = (long long)p.max_chunks * p.n_groups;
     if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     splitkv_kernel<D, NT><<<(unsigned)ctas, kThreads, kSmem, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_combine_t(const SplitParams &p, cudaStream_t stream) {
     const int warps = p.n_groups * kMaxRows;
     combine_kernel<D><<<(warps + 7) / 8, 256, 0, stream>>>(p);
     return cudaGetLastError();
@@ -505,9 +508,16 @@ size_t split_partial_bytes(int n_groups, int max_chunks, int d) {
 
 cudaError_t launch_splitkv(const SplitParams &p, int d, int rows_per_group, cudaStream_t stream) {
     if (p.n_groups == 0 || p.max_chunks == 0) return cudaSuccess;
-    const int nt = rows_per_group > 8 ? 2 : 1;
-    if (d == 128) return nt == 2 ? launch_split_t<128, 2>(p, stream) : launch_split_t<128, 1>(p, stream);
-    return nt == 2 ? launch_split_t<64, 2>(p, stream) : launch_split_t<64, 1>(p, stream);
+    cudaError_t e;
+    if (splitkv_tma_eligible(p)) {
+        e = launch_splitkv_tma(p, d, rows_per_group, stream);
+    } else {
+        const int nt = rows_per_group > 8 ? 2 : 1;
+        if (d == 128) e = nt == 2 ? launch_split_t<128, 2>(p, stream) : launch_split_t<128, 1>(p, stream);
+        else e = nt == 2 ? launch_split_t<64, 2>(p, stream) : launch_split_t<64, 1>(p, stream);
+    }
+    if (e != cudaSuccess) return e;
+    return d == 128 ? launch_combine_t<128>(p, stream) : launch_combine_t<64>(p, stream);
 }
 
 }  // namespace orthros
