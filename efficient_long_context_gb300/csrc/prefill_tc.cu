@@ -46,9 +46,10 @@ namespace {
 
 constexpr int kRowsPerTile = 128;  // M of every MMA, rows of a query tile
 constexpr int kKeysPerTile = 128;  // N of QK^T, K of PV
-constexpr int kThreads = 320;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kSoftmaxWarps = 16;  // 2 slots x 2 column halves x 4 lane quarters
+constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
+constexpr int kProducerWarp = 16;
+constexpr int kMmaWarp = 17;
 constexpr int kNumK = 3;  // key stages
 constexpr int kNumV = 2;  // value stages
 
@@ -59,16 +60,18 @@ template <int D> struct Cfg {
     static constexpr int kK0 = kQ0 + 2 * kTileBytes;                    // key stages
     static constexpr int kV0 = kK0 + kNumK * kTileBytes;                // value stages
     static constexpr int kBar = kV0 + kNumV * kTileBytes;               // barriers + metadata
-    static constexpr int kSmem = kBar + 256 + 1024;                     // + alignment slack
+    static constexpr int kSmem = kBar + 1536 + 1024;                    // + alignment slack
     static constexpr int kTmemO = 256;                                  // first O column
 };
 
 struct Meta {
     uint64_t k_full[kNumK], k_empty[kNumK], v_full[kNumV], v_empty[kNumV];
     uint64_t s_full[2], p_full[2], o_full[2], mma_done;
+    uint64_t xm_bar[2], lx_bar[2];  // per slot: row maxima / row sums exchanged between column halves
     uint32_t tmem_base;
     int abort;
     int t_min[2], t_max[2];
+    __nv_bfloat16 xmax[2][2][kRowsPerTile];  // [slot][half][row] tile maxima (a shared shift; rounding is harmless)
 };
 
 struct Slot {
@@ -177,8 +180,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&mt.s_full[s], 1);
-            mbar_init(&mt.p_full[s], kRowsPerTile);
+            mbar_init(&mt.p_full[s], 2 * kRowsPerTile);
             mbar_init(&mt.o_full[s], 1);
+            mbar_init(&mt.xm_bar[s], 2 * kRowsPerTile);
+            mbar_init(&mt.lx_bar[s], 2 * kRowsPerTile);
             mt.t_min[s] = 0x7fffffff;
             mt.t_max[s] = -1;
         }
@@ -197,19 +202,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---------------- prologue: stage both query tiles (affine fused) ----------------
-    const int s_me = tid >> 7;  // softmax slot of this thread (valid for tid < 256)
-    const int row = tid & 127;
+    // Softmax warp w: slot (w >> 2) & 1, column half w >> 3, rows 32 (w & 3) .. +31;
+    // each half stages its own D/2 channels of the row.
+    const bool softmax_thread = warp < kSoftmaxWarps;
+    const int s_me = (warp >> 2) & 1;
+    const int h_me = warp >> 3;
+    const int row = ((warp & 3) << 5) | lane;
     int my_t = 0;
     bool my_valid = false, my_bad = false;
-    if (tid < 256) {
+    if (softmax_thread) {
         const Slot S = s_me ? sl1 : sl0;
         if (S.kind >= 0 && row < S.n) {
             my_t = S.kind == 0 ? S.row0 + row : p.out_positions[S.row0 + row];
             my_valid = my_t >= 0 && my_t < p.T;
             my_bad = !my_valid;
-            if (my_bad) set_status(p.status, ORTHROS_DEV_BAD_POSITION);
+            if (my_bad && h_me == 0) set_status(p.status, ORTHROS_DEV_BAD_POSITION);
         }
         uint8_t *qs = smem + C::kQ0 + s_me * C::kTileBytes;
+        constexpr int kHalfChunks = D / 16;  // 16-byte chunks per half row
         if (my_valid) {
             const __nv_bfloat16 *src;
             if (S.kind == 1 && p.q_out)
@@ -220,7 +230,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float *be = (S.kind == 0 ? p.beta_base : p.beta_out) + S.h * D;
             bool over = false;
 #pragma unroll 4
-            for (int c = 0; c < D / 8; ++c) {
+            for (int cc = 0; cc < kHalfChunks; ++cc) {
+                const int c = h_me * kHalfChunks + cc;
                 const uint4 raw = reinterpret_cast<const uint4 *>(src)[c];
                 const float4 a0 = reinterpret_cast<const float4 *>(al)[2 * c];
                 const float4 a1 = reinterpret_cast<const float4 *>(al)[2 * c + 1];
@@ -242,12 +253,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<uint4 *>(qs + sw128_offset<D>(row, c)) = o;
             }
             if (over) set_status(p.status, ORTHROS_DEV_FP16_RANGE);
-            atomicMin(&mt.t_min[s_me], my_t);
-            atomicMax(&mt.t_max[s_me], my_t);
+            if (h_me == 0) {
+                atomicMin(&mt.t_min[s_me], my_t);
+                atomicMax(&mt.t_max[s_me], my_t);
+            }
         } else {
 #pragma unroll 4
-            for (int c = 0; c < D / 8; ++c)
-                *reinterpret_cast<uint4 *>(qs + sw128_offset<D>(row, c)) = make_uint4(0, 0, 0, 0);
+            for (int cc = 0; cc < kHalfChunks; ++cc)
+                *reinterpret_cast<uint4 *>(qs + sw128_offset<D>(row, h_me * kHalfChunks + cc)) = make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
     }
@@ -311,86 +324,101 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0 && n_it > 0) {
             constexpr uint32_t kIdescS = idesc_f16(0, 0, 0, 0, kRowsPerTile, kKeysPerTile);  // fp16, K-major
             constexpr uint32_t kIdescO = idesc_f16(1, 1, 0, 1, kRowsPerTile, D);             // bf16, V MN-major
-            const uint32_t q_base = smem_u32(smem + C::kQ0);
-            const uint32_t k_base = smem_u32(smem + C::kK0);
-            const uint32_t v_base = smem_u32(smem + C::kV0);
-            auto active = [&](int s, int kt) {
-                return s == 0 ? (kt >= bd0.kt_lo && kt <= bd0.kt_hi) : (kt >= bd1.kt_lo && kt <= bd1.kt_hi);
-            };
-            auto issue_s = [&](int s, int sk) {
-                // S_s = Q_s K^T: 16 channels per instruction; within a 128B atom the
-                // start address advances 32 bytes per step.
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks >> 2) * (kRowsPerTile * 128) + (ks & 3) * 32;
-                    const uint64_t a = desc_sw128(q_base + s * C::kTileBytes + off, 16, 1024);
-                    const uint64_t bdesc = desc_sw128(k_base + sk * C::kTileBytes + off, 16, 1024);
-                    mma_ss(tmem + s * 128, a, bdesc, kIdescS, ks > 0);
-                }
-            };
-            uint32_t pc[2] = {0, 0};
-            bool o_init[2] = {false, false};
+            // Descriptors are built once; the start-address field is the low 14 bits
+            // (byte address >> 4) and every operand lies below 256 KB of shared
+            // memory, so adding (byte offset >> 4) never carries out of the field.
+            constexpr uint32_t kTileU = C::kTileBytes >> 4;
+            const uint64_t dq = desc_sw128(smem_u32(smem + C::kQ0), 16, 1024);
+            const uint64_t dk = desc_sw128(smem_u32(smem + C::kK0), 16, 1024);
+            const uint64_t dv = desc_sw128(smem_u32(smem + C::kV0), kKeysPerTile * 128, 1024);
+            const uint32_t d_s0 = tmem, d_s1 = tmem + 128;
+            const uint32_t d_o0 = tmem + C::kTmemO, d_o1 = tmem + C::kTmemO + 128;
+            const int lo0 = bd0.kt_lo, hi0 = bd0.kt_hi, lo1 = bd1.kt_lo, hi1 = bd1.kt_hi;
+            // S = Q K^T: 16 channels per instruction; inside a 128B atom the start
+            // address advances 32 bytes per step.
+#define ORTHROS_ISSUE_S(D_TMEM, QDESC, KDESC)                                           \
+    _Pragma("unroll") for (int ks = 0; ks < D / 16; ++ks) {                            \
+        const uint32_t off = ((ks >> 2) * (kRowsPerTile * 128) + (ks & 3) * 32) >> 4; \
+        mma_ss((D_TMEM), (QDESC) + off, (KDESC) + off, kIdescS, ks > 0);             \
+    }
+            // O += P V: 16 keys per instruction; P packed bf16x2 in the S columns
+            // (8 columns per step), V rows 128 bytes apart.
+#define ORTHROS_ISSUE_PV(D_TMEM, P_TMEM, VDESC, ACC0)                                            \
+    _Pragma("unroll") for (int kk = 0; kk < kKeysPerTile / 16; ++kk)                            \
+        mma_ts((D_TMEM), (P_TMEM) + kk * 8, (VDESC) + (uint64_t)((kk * 16 * 128) >> 4), kIdescO, \
+               kk > 0 ? 1u : (ACC0));
+            uint32_t pc0 = 0, pc1 = 0, o_init0 = 0, o_init1 = 0;
             bool ok = mbar_wait(&mt.k_full[0], 0, abort, p.status);
             if (ok) {
                 tc_fence_after();
-                for (int s = 0; s < 2; ++s)
-                    if (active(s, kt_min)) {
-                        issue_s(s, 0);
-                        tc_commit(&mt.s_full[s]);
-                    }
+                if (kt_min >= lo0 && kt_min <= hi0) {
+                    ORTHROS_ISSUE_S(d_s0, dq, dk)
+                    tc_commit(&mt.s_full[0]);
+                }
+                if (kt_min >= lo1 && kt_min <= hi1) {
+                    ORTHROS_ISSUE_S(d_s1, dq + kTileU, dk)
+                    tc_commit(&mt.s_full[1]);
+                }
                 tc_commit(&mt.k_empty[0]);
             }
+            // per tile and slot: PV_s(i), then S_s(i+1) into the TMEM that held P_s(i)
+            // (tcgen05.mma from one thread execute in issue order)
             for (int i = 0; ok && i < n_it; ++i) {
                 const int kt = kt_min + i;
                 const int sv = i % kNumV;
+                const uint64_t vdesc = dv + (uint64_t)(sv * kTileU);
+                const bool more = i + 1 < n_it;
+                const int skn = (i + 1) % kNumK;
+                const uint64_t kdesc = dk + (uint64_t)(skn * kTileU);
                 if (!(ok = mbar_wait(&mt.v_full[sv], (i / kNumV) & 1, abort, p.status))) break;
-                // per tile: PV_s(i), then S_s(i+1) into the TMEM that held P_s(i)
-                // (tcgen05.mma from one thread execute in issue order)
-                auto step = [&](const int s) -> bool {
-                    if (active(s, kt)) {
-                        if (!mbar_wait(&mt.p_full[s], pc[s] & 1, abort, p.status)) return false;
-                        ++pc[s];
-                        tc_fence_after();
-                        // O_s += P_s V: 16 keys per instruction; P packed bf16x2 in the
-                        // S_s columns (8 columns per step), V rows 128 bytes apart.
-#pragma unroll
-                        for (int kk = 0; kk < kKeysPerTile / 16; ++kk) {
-                            const uint64_t bdesc =
-                                desc_sw128(v_base + sv * C::kTileBytes + kk * 16 * 128, kKeysPerTile * 128, 1024);
-                            mma_ts(tmem + C::kTmemO + s * 128, tmem + s * 128 + kk * 8, bdesc, kIdescO,
-                                   (o_init[s] || kk > 0) ? 1u : 0u);
-                        }
-                        o_init[s] = true;
+                // slot 0
+                if (kt >= lo0 && kt <= hi0) {
+                    if (!(ok = mbar_wait(&mt.p_full[0], pc0 & 1, abort, p.status))) break;
+                    ++pc0;
+                    tc_fence_after();
+                    ORTHROS_ISSUE_PV(d_o0, d_s0, vdesc, o_init0)
+                    o_init0 = 1;
+                }
+                if (more) {
+                    if (!(ok = mbar_wait(&mt.k_full[skn], ((i + 1) / kNumK) & 1, abort, p.status))) break;
+                    tc_fence_after();
+                    if (kt + 1 >= lo0 && kt + 1 <= hi0) {
+                        ORTHROS_ISSUE_S(d_s0, dq, kdesc)
+                        tc_commit(&mt.s_full[0]);
                     }
-                    if (i + 1 < n_it) {
-                        const int skn = (i + 1) % kNumK;
-                        if (s == 0) {
-                            if (!mbar_wait(&mt.k_full[skn], ((i + 1) / kNumK) & 1, abort, p.status)) return false;
-                            tc_fence_after();
-                        }
-                        if (active(s, kt + 1)) {
-                            issue_s(s, skn);
-                            tc_commit(&mt.s_full[s]);
-                        }
-                        if (s == 1) tc_commit(&mt.k_empty[skn]);
+                }
+                // slot 1
+                if (kt >= lo1 && kt <= hi1) {
+                    if (!(ok = mbar_wait(&mt.p_full[1], pc1 & 1, abort, p.status))) break;
+                    ++pc1;
+                    tc_fence_after();
+                    ORTHROS_ISSUE_PV(d_o1, d_s1, vdesc, o_init1)
+                    o_init1 = 1;
+                }
+                if (more) {
+                    if (kt + 1 >= lo1 && kt + 1 <= hi1) {
+                        ORTHROS_ISSUE_S(d_s1, dq + kTileU, kdesc)
+                        tc_commit(&mt.s_full[1]);
                     }
-                    if (s == 1) tc_commit(&mt.v_empty[sv]);
-                    return true;
-                };
-                ok = step(0) && step(1);
+                    tc_commit(&mt.k_empty[skn]);
+                }
+                tc_commit(&mt.v_empty[sv]);
             }
+#undef ORTHROS_ISSUE_S
+#undef ORTHROS_ISSUE_PV
             tc_commit(&mt.o_full[0]);
             tc_commit(&mt.o_full[1]);
             tc_commit(&mt.mma_done);
             mbar_wait(&mt.mma_done, 0, abort, p.status);
         }
     } else {
-        // ---------------- softmax warpgroups ----------------
-        const int s = s_me;
+        // ---------------- softmax: two threads per row (one per 64-key half) ----------------
+        const int s = s_me, hh = h_me;
         const Slot S = s ? sl1 : sl0;
         const Band bd = s ? bd1 : bd0;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t t_s = tmem + lane_off + s * 128;
-        const uint32_t t_o = tmem + lane_off + C::kTmemO + s * 128;
+        const uint32_t t_s = tmem + lane_off + s * 128;                // S_s columns of this lane quarter
+        const uint32_t t_o = tmem + lane_off + C::kTmemO + s * 128 + hh * (D / 2);  // this half of O_s
         const int t_row = my_valid ? my_t : bd.t_max;
         const int lo_row = S.kind == 0 ? max(0, t_row - p.window + 1) : 0;
         const float c2 = p.scale_log2;
@@ -403,35 +431,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool got = mbar_wait(&mt.s_full[s], cnt & 1, abort, p.status);
             if (!__all_sync(0xffffffffu, got)) break;
             tc_fence_after();
-            // Pass 1: row max from four 32-column loads (only the running maxima
-            // stay live). Pass 2 reloads the columns (one chunk prefetched) for
-            // exp / sum / bf16 pack / store, so at most two chunks are in registers.
-            const int key0 = kt * kKeysPerTile;
-            const bool edge = key0 + kKeysPerTile - 1 > t_min_s || key0 < bd.lo_max;
-            auto mask_chunk = [&](uint32_t (&r)[32], int j) {
+            // this half's 64 logits of the row, in two 32-column loads, one wait
+            uint32_t ra[32], rb[32];
+            tmem_ld32(t_s + 64 * hh, ra);
+            tmem_ld32(t_s + 64 * hh + 32, rb);
+            tmem_ld_wait();
+            reg_fence(ra);
+            reg_fence(rb);
+            const int key0 = kt * kKeysPerTile + 64 * hh;
+            if (kt * kKeysPerTile + kKeysPerTile - 1 > t_min_s || kt * kKeysPerTile < bd.lo_max) {
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
-                    const int key = key0 + 32 * j + c;
-                    if (key > t_row || key < lo_row) r[c] = __float_as_uint(-INFINITY);
-                }
-            };
-            float mq[8];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                uint32_t r[32];
-                tmem_ld32(t_s + 32 * j, r);
-                tmem_ld_wait();
-                reg_fence(r);
-                if (edge) mask_chunk(r, j);
-                const float *x = reinterpret_cast<const float *>(r);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const float v = max3(x[4 * q], x[4 * q + 1], fmaxf(x[4 * q + 2], x[4 * q + 3]));
-                    mq[q] = j == 0 ? v : fmaxf(mq[q], v);
+                    if (key0 + c > t_row || key0 + c < lo_row) ra[c] = __float_as_uint(-INFINITY);
+                    if (key0 + 32 + c > t_row || key0 + 32 + c < lo_row) rb[c] = __float_as_uint(-INFINITY);
                 }
             }
-            const float mx = max3(max3(mq[0], mq[1], mq[2]), max3(mq[3], mq[4], mq[5]), fmaxf(mq[6], mq[7]));
-            const float m_new = fmaxf(m_ref, mx);
+            const float *xa = reinterpret_cast<const float *>(ra);
+            const float *xb = reinterpret_cast<const float *>(rb);
+            float mq[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                mq[q] = max3(max3(xa[4 * q], xa[4 * q + 1], xa[4 * q + 2]), max3(xa[4 * q + 3], xb[4 * q], xb[4 * q + 1]),
+                             fmaxf(xb[4 * q + 2], xb[4 * q + 3]));
+            const float mine = max3(max3(mq[0], mq[1], mq[2]), max3(mq[3], mq[4], mq[5]), fmaxf(mq[6], mq[7]));
+            // both halves combine the same two bf16-rounded maxima, so they agree on the shift
+            const __nv_bfloat16 mine_b = __float2bfloat16_rn(mine);
+            mt.xmax[s][hh][row] = mine_b;
+            mbar_arrive(&mt.xm_bar[s]);
+            if (!__all_sync(0xffffffffu, mbar_wait(&mt.xm_bar[s], cnt & 1, abort, p.status))) break;
+            const float m_tile = fmaxf(__bfloat162float(mine_b), __bfloat162float(mt.xmax[s][hh ^ 1][row]));
+            const float m_new = fmaxf(m_ref, m_tile);
             const bool resc = (m_new - m_ref) * c2 > 8.f;  // true on the first finite max
             const bool any_resc = __any_sync(0xffffffffu, resc);
             const float alpha = resc ? ex2((m_ref - m_new) * c2) : 1.f;
@@ -441,18 +470,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float mb = m_ref == -INFINITY ? 0.f : m_ref * c2;
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
-            uint32_t ra[32], rb[32];
-            tmem_ld32(t_s, ra);
+            // P for keys 64 hh .. 64 hh + 63 -> packed columns 32 hh .. 32 hh + 31
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                uint32_t(&cur)[32] = (j & 1) ? rb : ra;
-                uint32_t(&nxt)[32] = (j & 1) ? ra : rb;
-                tmem_ld_wait();
-                reg_fence(cur);
-                // the next chunk's columns lie above every column P has written so far
-                if (j < 3) tmem_ld32(t_s + 32 * (j + 1), nxt);
-                if (edge) mask_chunk(cur, j);
-                const float *x = reinterpret_cast<const float *>(cur);
+            for (int j = 0; j < 2; ++j) {
+                const float *x = j ? xb : xa;
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
@@ -461,15 +482,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ls[e & 3] += p0 + p1;
                     pk[e] = pack_bf16(p0, p1);
                 }
-                tmem_st16(t_s + 16 * j, pk);
+                tmem_st16(t_s + 32 * hh + 16 * j, pk);
             }
             l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             // O_s is idle here (PV_s of the previous tile completed before S_s of
-            // this tile was signalled; the next PV_s waits for p_full), so the
-            // rescale of the running output can follow the P stores.
+            // this tile was signalled; the next PV_s waits for p_full): each half
+            // rescales its own D/2 columns of the running output.
             if (any_resc && cnt > 0) {
 #pragma unroll
-                for (int j = 0; j < D / 32; ++j) {
+                for (int j = 0; j < D / 64; ++j) {
                     uint32_t o[32];
                     tmem_ld32(t_o + 32 * j, o);
                     tmem_ld_wait();
@@ -485,25 +506,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++cnt;
         }
         // ---------------- epilogue: o = O / l, lse = scale*m + ln l ----------------
-        // tcgen05.ld is warp-collective: every lane of the warp runs the loads,
-        // padding rows of a ragged tile only skip the stores.
+        // Row sums are exchanged through the (now idle) query tile of this slot.
         bool have = cnt > 0 && mbar_wait(&mt.o_full[s], 0, abort, p.status);
         have = __all_sync(0xffffffffu, have);
         if (have) {
             tc_fence_after();
-            const bool store = S.kind >= 0 && row < S.n;
+            float *lx = reinterpret_cast<float *>(smem + C::kQ0 + s * C::kTileBytes);  // [2][128]
+            lx[hh * kRowsPerTile + row] = l;
+            mbar_arrive(&mt.lx_bar[s]);
+            have = __all_sync(0xffffffffu, mbar_wait(&mt.lx_bar[s], 0, abort, p.status));
+            const float l_all = l + lx[(hh ^ 1) * kRowsPerTile + row];
+            const bool store = have && S.kind >= 0 && row < S.n;
             __nv_bfloat16 *dst = nullptr;
             float *lse_dst = nullptr;
             if (store && S.kind == 0) {
-                dst = p.o_base + (((long long)S.b * p.T + my_t) * p.Hq + S.h) * D;
+                dst = p.o_base + (((long long)S.b * p.T + my_t) * p.Hq + S.h) * D + hh * (D / 2);
                 lse_dst = p.lse_base + ((long long)S.b * p.Hq + S.h) * p.T + my_t;
             } else if (store) {
-                dst = p.o_out + ((long long)(S.row0 + row) * p.Hq + S.h) * D;
+                dst = p.o_out + ((long long)(S.row0 + row) * p.Hq + S.h) * D + hh * (D / 2);
                 lse_dst = p.lse_out + (long long)(S.row0 + row) * p.Hq + S.h;
             }
-            const float inv = my_bad ? __int_as_float(0x7fc00000) : 1.f / l;
+            const float inv = my_bad ? __int_as_float(0x7fc00000) : 1.f / l_all;
 #pragma unroll
-            for (int j = 0; j < D / 32; ++j) {
+            for (int j = 0; j < D / 64; ++j) {
                 uint32_t o[32];
                 tmem_ld32(t_o + 32 * j, o);
                 tmem_ld_wait();
@@ -518,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int e = 0; e < 4; ++e) reinterpret_cast<uint4 *>(dst + 32 * j)[e] = w[e];
                 }
             }
-            if (store) *lse_dst = my_bad ? __int_as_float(0x7fc00000) : m_ref * p.scale + logf(l);
+            if (store && hh == 0) *lse_dst = my_bad ? __int_as_float(0x7fc00000) : m_ref * p.scale + logf(l_all);
         }
     }
 
