@@ -201,6 +201,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
 
+    // Base-position tiles know their band without reading any data, so the
+    // producer starts the first key/value loads now and they overlap the query
+    // staging below (tiles with output rows wait for their positions).
+    int pre_k = 0, pre_v = 0;
+    const bool closed_form = sl0.kind == 0 && sl1.kind != 1;
+    if (warp == kProducerWarp && lane == 0 && closed_form) {
+        const int lo0 = max(0, sl0.row0 - p.window + 1) / kKeysPerTile;
+        const int hi0 = (sl0.row0 + sl0.n - 1) / kKeysPerTile;
+        int lo = lo0, hi = hi0;
+        if (sl1.kind == 0) {
+            lo = min(lo, max(0, sl1.row0 - p.window + 1) / kKeysPerTile);
+            hi = max(hi, (sl1.row0 + sl1.n - 1) / kKeysPerTile);
+        }
+        const int n_cf = hi - lo + 1;
+        const int kvh = sl0.h / (p.Hq / p.Hkv);
+        pre_k = min(n_cf, kNumK);
+        pre_v = min(n_cf, kNumV);
+        for (int i = 0; i < pre_k; ++i) {
+            mbar_arrive_expect_tx(&mt.k_full[i], C::kTileBytes);
+            for (int j = 0; j < C::kSub; ++j)
+                tma_load_4d(smem + C::kK0 + i * C::kTileBytes + j * (kKeysPerTile * 128), &tm_k, &mt.k_full[i], 64 * j,
+                            kvh, (lo + i) * kKeysPerTile, sl0.b);
+        }
+        for (int i = 0; i < pre_v; ++i) {
+            mbar_arrive_expect_tx(&mt.v_full[i], C::kTileBytes);
+            for (int j = 0; j < C::kSub; ++j)
+                tma_load_4d(smem + C::kV0 + i * C::kTileBytes + j * (kKeysPerTile * 128), &tm_v, &mt.v_full[i], 64 * j,
+                            kvh, (lo + i) * kKeysPerTile, sl0.b);
+        }
+    }
+
     // ---------------- prologue: stage both query tiles (affine fused) ----------------
     // Softmax warp w: slot (w >> 2) & 1, column half w >> 3, rows 32 (w & 3) .. +31;
     // each half stages its own D/2 channels of the row.
@@ -229,10 +260,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float *al = (S.kind == 0 ? p.alpha_base : p.alpha_out) + S.h * D;
             const float *be = (S.kind == 0 ? p.beta_base : p.beta_out) + S.h * D;
             bool over = false;
-#pragma unroll 4
+            uint4 raws[kHalfChunks];  // every load of the half row in flight at once
+#pragma unroll
+            for (int cc = 0; cc < kHalfChunks; ++cc) raws[cc] = reinterpret_cast<const uint4 *>(src)[h_me * kHalfChunks + cc];
+#pragma unroll
             for (int cc = 0; cc < kHalfChunks; ++cc) {
                 const int c = h_me * kHalfChunks + cc;
-                const uint4 raw = reinterpret_cast<const uint4 *>(src)[c];
+                const uint4 raw = raws[cc];
                 const float4 a0 = reinterpret_cast<const float4 *>(al)[2 * c];
                 const float4 a1 = reinterpret_cast<const float4 *>(al)[2 * c + 1];
                 const float4 b0 = reinterpret_cast<const float4 *>(be)[2 * c];
@@ -306,17 +340,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < n_it && !*abort; ++i) {
                 const int kt = kt_min + i;
                 const int sk = i % kNumK;
-                if (i >= kNumK && !mbar_wait(&mt.k_empty[sk], ((i / kNumK) - 1) & 1, abort, p.status)) break;
-                mbar_arrive_expect_tx(&mt.k_full[sk], C::kTileBytes);
-                for (int j = 0; j < C::kSub; ++j)
-                    tma_load_4d(smem + C::kK0 + sk * C::kTileBytes + j * (kKeysPerTile * 128), &tm_k,
-                                &mt.k_full[sk], 64 * j, kv, kt * kKeysPerTile, bseq);
+                if (i >= pre_k) {
+                    if (i >= kNumK && !mbar_wait(&mt.k_empty[sk], ((i / kNumK) - 1) & 1, abort, p.status)) break;
+                    mbar_arrive_expect_tx(&mt.k_full[sk], C::kTileBytes);
+                    for (int j = 0; j < C::kSub; ++j)
+                        tma_load_4d(smem + C::kK0 + sk * C::kTileBytes + j * (kKeysPerTile * 128), &tm_k,
+                                    &mt.k_full[sk], 64 * j, kv, kt * kKeysPerTile, bseq);
+                }
                 const int sv = i % kNumV;
-                if (i >= kNumV && !mbar_wait(&mt.v_empty[sv], ((i / kNumV) - 1) & 1, abort, p.status)) break;
-                mbar_arrive_expect_tx(&mt.v_full[sv], C::kTileBytes);
-                for (int j = 0; j < C::kSub; ++j)
-                    tma_load_4d(smem + C::kV0 + sv * C::kTileBytes + j * (kKeysPerTile * 128), &tm_v,
-                                &mt.v_full[sv], 64 * j, kv, kt * kKeysPerTile, bseq);
+                if (i >= pre_v) {
+                    if (i >= kNumV && !mbar_wait(&mt.v_empty[sv], ((i / kNumV) - 1) & 1, abort, p.status)) break;
+                    mbar_arrive_expect_tx(&mt.v_full[sv], C::kTileBytes);
+                    for (int j = 0; j < C::kSub; ++j)
+                        tma_load_4d(smem + C::kV0 + sv * C::kTileBytes + j * (kKeysPerTile * 128), &tm_v,
+                                    &mt.v_full[sv], 64 * j, kv, kt * kKeysPerTile, bseq);
+                }
             }
         }
     } else if (warp == kMmaWarp) {
