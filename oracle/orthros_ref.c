@@ -19,6 +19,10 @@
  *   - Alg. 1, lines 6-7: heads are split after the affine, so alpha/beta hold
  *     one value per (query head, channel); grouped K/V heads follow the
  *     contiguous-group convention kv = h / (Hq / Hkv).
+ *   - The backward of Eq. 4 / Eq. 5 and of the affines (training on the
+ *     pre-training and fine-tuning regimes of Sec. 3.2 runs exactly these rows):
+ *     the chain rule through softmax attention, written out per row (recompute
+ *     p, then ds = p (dO.v - dO.o)); no formula for it is printed in the paper.
  *
  * Arithmetic: inputs are float (bf16 inputs are widened exactly by the caller);
  * every intermediate and every output is double. Softmax is the two-pass exact
@@ -366,6 +370,179 @@ int orthros_ref_decode(const float *q, const float *q_out, const float *k_new,
     }
     free(krow);
     free(vrow);
+    return err;
+}
+
+/*
+ * Gradient of one query row's output (Eq. 4 / Eq. 5) given dO: recomputes the
+ * row's exact softmax in double, then
+ *   D = dO . o,  dp_j = dO . v_j,  ds_j = p_j (dp_j - D),
+ *   dqa += scale sum_j ds_j k_j,  dk_j += scale ds_j qa,  dv_j += p_j dO.
+ * krow/vrow/dkrow/dvrow[j] point at key j's rows. w is scratch (hi-lo+1).
+ */
+static void attend_row_backward(const double *qa, const float *dO, const float *const *krow,
+                                const float *const *vrow, double *const *dkrow, double *const *dvrow,
+                                int lo, int hi, int d, double scale, double *dqa, double *w, double *o)
+{
+    double m = -INFINITY;
+    for (int j = lo; j <= hi; ++j) {
+        double dot = 0.0;
+        for (int c = 0; c < d; ++c)
+            dot += qa[c] * (double)krow[j][c];
+        w[j - lo] = scale * dot;
+        if (w[j - lo] > m)
+            m = w[j - lo];
+    }
+    double l = 0.0;
+    for (int j = lo; j <= hi; ++j) {
+        w[j - lo] = exp(w[j - lo] - m);
+        l += w[j - lo];
+    }
+    for (int c = 0; c < d; ++c)
+        o[c] = 0.0;
+    for (int j = lo; j <= hi; ++j) {
+        w[j - lo] /= l; /* p_j */
+        for (int c = 0; c < d; ++c)
+            o[c] += w[j - lo] * (double)vrow[j][c];
+    }
+    double D = 0.0;
+    for (int c = 0; c < d; ++c)
+        D += (double)dO[c] * o[c];
+    for (int c = 0; c < d; ++c)
+        dqa[c] = 0.0;
+    for (int j = lo; j <= hi; ++j) {
+        const double p = w[j - lo];
+        double dp = 0.0;
+        for (int c = 0; c < d; ++c)
+            dp += (double)dO[c] * (double)vrow[j][c];
+        const double ds = p * (dp - D);
+        for (int c = 0; c < d; ++c) {
+            dqa[c] += scale * ds * (double)krow[j][c];
+            dkrow[j][c] += scale * ds * qa[c];
+            dvrow[j][c] += p * (double)dO[c];
+        }
+    }
+}
+
+/*
+ * Backward of orthros_ref_prefill: gradients of a loss L given dL/do_base
+ * (do_base [B,T,Hq,d]) and dL/do_out (do_out [n_out,Hq,d]); lse is treated as
+ * an output the loss does not use.
+ *
+ * Outputs (double, overwritten): dq [B,T,Hq,d] (raw base queries; also
+ * receives the output rows' gradient when q_out is NULL, since those rows
+ * read q at their position), dk, dv [B,T,Hkv,d], dq_out [n_out,Hq,d] (only
+ * when q_out is given), d_alpha_base, d_beta_base, d_alpha_out, d_beta_out
+ * [Hq,d]. Through the affine q = alpha (.) q_raw + beta (Sec. 3.1):
+ * dq_raw = alpha (.) dqa, dalpha += dqa (.) q_raw, dbeta += dqa.
+ * Parallel over kv heads only (each owns its K/V, query heads and affine rows).
+ */
+int orthros_ref_prefill_backward(const float *q, const float *k, const float *v,
+                                 const float *alpha_base, const float *beta_base,
+                                 const float *alpha_out, const float *beta_out,
+                                 const int32_t *out_indptr, const int32_t *out_positions,
+                                 const float *q_out, int B, int T, int Hq, int Hkv,
+                                 int d, int window, double scale,
+                                 const float *do_base, const float *do_out,
+                                 double *dq, double *dk, double *dv, double *dq_out,
+                                 double *d_alpha_base, double *d_beta_base,
+                                 double *d_alpha_out, double *d_beta_out, int nthreads)
+{
+    if (check_common(B, T, Hq, Hkv, d, window) != REF_OK)
+        return REF_EINVAL;
+    const int g = Hq / Hkv;
+    const int n_out = out_indptr ? out_indptr[B] : 0;
+    for (int b = 0; out_indptr && b < B; ++b)
+        for (int r = out_indptr[b]; r < out_indptr[b + 1]; ++r)
+            if (out_positions[r] < 0 || out_positions[r] >= T)
+                return REF_EINVAL;
+    memset(dq, 0, sizeof(double) * (size_t)B * T * Hq * d);
+    memset(dk, 0, sizeof(double) * (size_t)B * T * Hkv * d);
+    memset(dv, 0, sizeof(double) * (size_t)B * T * Hkv * d);
+    if (dq_out)
+        memset(dq_out, 0, sizeof(double) * (size_t)n_out * Hq * d);
+    memset(d_alpha_base, 0, sizeof(double) * (size_t)Hq * d);
+    memset(d_beta_base, 0, sizeof(double) * (size_t)Hq * d);
+    memset(d_alpha_out, 0, sizeof(double) * (size_t)Hq * d);
+    memset(d_beta_out, 0, sizeof(double) * (size_t)Hq * d);
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int err = REF_OK;
+    const size_t tt = T > 0 ? (size_t)T : 1;
+#pragma omp parallel
+    {
+        const float **krow = (const float **)malloc(sizeof(*krow) * tt);
+        const float **vrow = (const float **)malloc(sizeof(*vrow) * tt);
+        double **dkrow = (double **)malloc(sizeof(*dkrow) * tt);
+        double **dvrow = (double **)malloc(sizeof(*dvrow) * tt);
+        double *qa = (double *)malloc(sizeof(double) * d);
+        double *dqa = (double *)malloc(sizeof(double) * d);
+        double *o = (double *)malloc(sizeof(double) * d);
+        double *w = (double *)malloc(sizeof(double) * tt);
+        const int ok = krow && vrow && dkrow && dvrow && qa && dqa && o && w;
+        if (!ok) {
+#pragma omp atomic write
+            err = REF_ENOMEM;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int kv = 0; kv < Hkv; ++kv) {
+            if (!ok)
+                continue;
+            for (int b = 0; b < B; ++b) {
+                for (int j = 0; j < T; ++j) {
+                    const size_t off = (((size_t)b * T + j) * Hkv + kv) * (size_t)d;
+                    krow[j] = k + off;
+                    vrow[j] = v + off;
+                    dkrow[j] = dk + off;
+                    dvrow[j] = dv + off;
+                }
+                for (int h = kv * g; h < (kv + 1) * g; ++h) {
+                    /* base stream, Eq. 4 */
+                    for (int t = 0; t < T; ++t) {
+                        const size_t qoff = (((size_t)b * T + t) * Hq + h) * (size_t)d;
+                        affine(q + qoff, alpha_base + (size_t)h * d, beta_base + (size_t)h * d, d, qa);
+                        const int lo = t - window + 1 > 0 ? t - window + 1 : 0;
+                        attend_row_backward(qa, do_base + qoff, krow, vrow, dkrow, dvrow, lo, t, d, scale, dqa, w, o);
+                        for (int c = 0; c < d; ++c) {
+                            dq[qoff + c] += (double)alpha_base[(size_t)h * d + c] * dqa[c];
+                            d_alpha_base[(size_t)h * d + c] += dqa[c] * (double)q[qoff + c];
+                            d_beta_base[(size_t)h * d + c] += dqa[c];
+                        }
+                    }
+                    /* output stream, Eq. 5 */
+                    for (int r = out_indptr ? out_indptr[b] : 0; out_indptr && r < out_indptr[b + 1]; ++r) {
+                        const int t = out_positions[r];
+                        const size_t roff = ((size_t)r * Hq + h) * (size_t)d;
+                        const size_t qoff = (((size_t)b * T + t) * Hq + h) * (size_t)d;
+                        const float *qraw = q_out ? q_out + roff : q + qoff;
+                        affine(qraw, alpha_out + (size_t)h * d, beta_out + (size_t)h * d, d, qa);
+                        attend_row_backward(qa, do_out + roff, krow, vrow, dkrow, dvrow, 0, t, d, scale, dqa, w, o);
+                        for (int c = 0; c < d; ++c) {
+                            const double gq = (double)alpha_out[(size_t)h * d + c] * dqa[c];
+                            if (q_out)
+                                dq_out[roff + c] += gq;
+                            else
+                                dq[qoff + c] += gq;
+                            d_alpha_out[(size_t)h * d + c] += dqa[c] * (double)qraw[c];
+                            d_beta_out[(size_t)h * d + c] += dqa[c];
+                        }
+                    }
+                }
+            }
+        }
+        free(krow);
+        free(vrow);
+        free(dkrow);
+        free(dvrow);
+        free(qa);
+        free(dqa);
+        free(o);
+        free(w);
+    }
     return err;
 }
 

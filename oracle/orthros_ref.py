@@ -67,6 +67,18 @@ def _bind(path):
         _f64p, _f64p, _f64p, _f64p,
         ctypes.c_int,
     ]
+    lib.orthros_ref_prefill_backward.restype = ctypes.c_int
+    lib.orthros_ref_prefill_backward.argtypes = [
+        _f32p, _f32p, _f32p,  # q k v
+        _f32p, _f32p, _f32p, _f32p,  # affines
+        _i32p, _i32p, _f32p,  # out_indptr out_positions q_out
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_int, ctypes.c_double,  # B T Hq Hkv d window scale
+        _f32p, _f32p,  # do_base do_out
+        _f64p, _f64p, _f64p, _f64p,  # dq dk dv dq_out
+        _f64p, _f64p, _f64p, _f64p,  # d alpha/beta base, d alpha/beta out
+        ctypes.c_int,
+    ]
     lib.orthros_ref_max_threads.restype = ctypes.c_int
     lib.orthros_ref_max_threads.argtypes = []
     return lib
@@ -92,6 +104,9 @@ class Oracle:
 
     def decode(self, *args, **kwargs):
         return decode(*args, _lib=self._lib, **kwargs)
+
+    def prefill_backward(self, *args, **kwargs):
+        return prefill_backward(*args, _lib=self._lib, **kwargs)
 
 
 def max_threads() -> int:
@@ -201,3 +216,54 @@ def decode(q, k_new, v_new, k_cache, v_cache, block_table, cache_lens,
     if rc != 0:
         raise ValueError(f"orthros_ref_decode failed with code {rc}")
     return o_base, lse_base, o_out, lse_out
+
+
+def prefill_backward(q, k, v, alpha_base, beta_base, alpha_out, beta_out, out_indptr,
+                     out_positions, window, scale, do_base, do_out, q_out=None,
+                     nthreads=0, _lib=None):
+    """Gradients of Eq. 4 (all T base rows) and Eq. 5 (the output rows) in float64.
+
+    do_base [B,T,Hq,d] and do_out [n_out,Hq,d] are dL/do of the two streams.
+    Returns a dict with dq [B,T,Hq,d], dk, dv [B,T,Hkv,d], dq_out [n_out,Hq,d]
+    (None when q_out is None: the output rows' gradient then lands in dq),
+    d_alpha_base, d_beta_base, d_alpha_out, d_beta_out [Hq,d].
+    """
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    B, T, Hq, d = q.shape
+    Hkv = k.shape[2]
+    assert k.shape == (B, T, Hkv, d) and v.shape == k.shape
+    ab, bb, ao, bo = (_f32(x) for x in (alpha_base, beta_base, alpha_out, beta_out))
+    out_indptr = _i32(out_indptr)
+    out_positions = _i32(out_positions if out_positions is not None else np.zeros(0, np.int32))
+    n_out = int(out_indptr[-1])
+    assert out_positions.shape == (n_out,)
+    q_out = _f32(q_out)
+    if q_out is not None:
+        assert q_out.shape == (n_out, Hq, d)
+    do_base = _f32(do_base)
+    assert do_base.shape == (B, T, Hq, d)
+    do_out = _f32(do_out if do_out is not None else np.zeros((n_out, Hq, d), np.float32))
+    assert do_out.shape == (n_out, Hq, d)
+    dq = np.zeros((B, T, Hq, d), np.float64)
+    dk = np.zeros((B, T, Hkv, d), np.float64)
+    dv = np.zeros((B, T, Hkv, d), np.float64)
+    dq_out = np.zeros((n_out, Hq, d), np.float64) if q_out is not None else None
+    grads = [np.zeros((Hq, d), np.float64) for _ in range(4)]
+    # zero-length arrays still need valid pointers
+    pos_arg = out_positions if out_positions.size else np.zeros(1, np.int32)
+    do_out_arg = do_out if do_out.size else np.zeros(1, np.float32)
+    rc = (_lib or _load()).orthros_ref_prefill_backward(
+        _ptr(q, _f32p), _ptr(k, _f32p), _ptr(v, _f32p),
+        _ptr(ab, _f32p), _ptr(bb, _f32p), _ptr(ao, _f32p), _ptr(bo, _f32p),
+        _ptr(out_indptr, _i32p), _ptr(pos_arg, _i32p), _ptr(q_out, _f32p),
+        B, T, Hq, Hkv, d, int(window), float(scale),
+        _ptr(do_base, _f32p), _ptr(do_out_arg, _f32p),
+        _ptr(dq, _f64p), _ptr(dk, _f64p), _ptr(dv, _f64p), _ptr(dq_out, _f64p),
+        *(_ptr(g, _f64p) for g in grads),
+        int(nthreads),
+    )
+    if rc != 0:
+        raise ValueError(f"orthros_ref_prefill_backward failed with code {rc}")
+    return {"dq": dq, "dk": dk, "dv": dv, "dq_out": dq_out,
+            "d_alpha_base": grads[0], "d_beta_base": grads[1],
+            "d_alpha_out": grads[2], "d_beta_out": grads[3]}

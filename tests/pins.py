@@ -376,6 +376,154 @@ def pin_hand_worked(orc):
     _close(lo[:, 0], np.log(np.array(g["exp_lse_out"])), 1e-12, "hand lse_out")
 
 
+# ---------------------------------------------------------------------------
+# Backward (gradients of Eq. 4 and Eq. 5 and of the query affines)
+# ---------------------------------------------------------------------------
+
+def torch_forward(q, k, v, ab, bb, ao, bo, indptr, pos, window, scale, q_out=None):
+    """Dense masked forward in torch float64 (library softmax), differentiable.
+
+    Arguments are float64 torch tensors; returns (o_base [B,T,Hq,d], o_out [n_out,Hq,d]).
+    The gradients that torch.autograd derives from it are what the oracle's
+    hand-derived backward is checked against.
+    """
+    B, T, Hq, d = q.shape
+    Hkv = k.shape[2]
+    g = Hq // Hkv
+    kr = k.repeat_interleave(g, dim=2)  # [B,T,Hq,d], kv = h // g
+    vr = v.repeat_interleave(g, dim=2)
+    i = torch.arange(T)[:, None]
+    j = torch.arange(T)[None, :]
+    band = (j <= i) & (j > i - window)
+    qa = q * ab + bb
+    S = scale * torch.einsum("bthc,bjhc->bhtj", qa, kr)
+    S = S.masked_fill(~band, float("-inf"))
+    o_base = torch.einsum("bhtj,bjhc->bthc", torch.softmax(S, dim=-1), vr)
+    outs = []
+    for b in range(B):
+        r0, r1 = int(indptr[b]), int(indptr[b + 1])
+        if r1 == r0:
+            continue
+        p = torch.as_tensor(pos[r0:r1], dtype=torch.long)
+        qr = q_out[r0:r1] if q_out is not None else q[b, p]
+        qo = qr * ao + bo  # [R,Hq,d]
+        So = scale * torch.einsum("rhc,jhc->rhj", qo, kr[b])
+        causal = torch.arange(T)[None, None, :] <= p[:, None, None]
+        So = So.masked_fill(~causal, float("-inf"))
+        outs.append(torch.einsum("rhj,jhc->rhc", torch.softmax(So, dim=-1), vr[b]))
+    o_out = torch.cat(outs, 0) if outs else torch.zeros((0, Hq, d), dtype=q.dtype)
+    return o_base, o_out
+
+
+BACKWARD_CASES = [
+    # (B, T, Hq, Hkv, d, window)
+    (1, 1, 1, 1, 4, 1),
+    (1, 13, 2, 1, 8, 1),
+    (1, 17, 4, 2, 8, 5),
+    (2, 21, 4, 1, 8, 21),
+    (2, 19, 6, 2, 4, 30),
+]
+
+
+def _backward_inputs(i, B, T, Hq, Hkv, d, with_q_out):
+    q, k, v, ab, bb, ao, bo = rng_inputs(101 + i, B, T, Hq, Hkv, d)
+    r = np.random.default_rng(101 + i)
+    lists = [sorted(r.choice(T, size=r.integers(0, T + 1), replace=False).tolist()) for _ in range(B)]
+    lists[-1] = sorted(set(lists[-1]) | {T - 1})
+    indptr, pos = csr(lists)
+    n_out = int(indptr[-1])
+    q_out = r.standard_normal((n_out, Hq, d)).astype(np.float32) if with_q_out else None
+    do_b = r.standard_normal((B, T, Hq, d)).astype(np.float32)
+    do_o = r.standard_normal((n_out, Hq, d)).astype(np.float32)
+    return q, k, v, ab, bb, ao, bo, indptr, pos, q_out, do_b, do_o
+
+
+def pin_backward_autograd(orc, cases=BACKWARD_CASES):
+    """Every gradient equals torch.autograd (float64) through the dense masked forward."""
+    for i, (B, T, Hq, Hkv, d, w) in enumerate(cases):
+        for with_q_out in (False, True):
+            q, k, v, ab, bb, ao, bo, indptr, pos, q_out, do_b, do_o = _backward_inputs(i, B, T, Hq, Hkv, d, with_q_out)
+            scale = 0.9 / math.sqrt(d)
+            got = orc.prefill_backward(q, k, v, ab, bb, ao, bo, indptr, pos, w, scale, do_b, do_o, q_out=q_out)
+            leaves = {n: torch.tensor(x, dtype=torch.float64, requires_grad=True)
+                      for n, x in (("q", q), ("k", k), ("v", v), ("ab", ab), ("bb", bb), ("ao", ao), ("bo", bo))}
+            qo_t = torch.tensor(q_out, dtype=torch.float64, requires_grad=True) if q_out is not None else None
+            ob, oo = torch_forward(leaves["q"], leaves["k"], leaves["v"], leaves["ab"], leaves["bb"],
+                                   leaves["ao"], leaves["bo"], indptr, pos, w, scale, qo_t)
+            loss = (ob * torch.from_numpy(do_b).double()).sum() + (oo * torch.from_numpy(do_o).double()).sum()
+            loss.backward()
+            tag = f"case {i} q_out={with_q_out}"
+            for name, leaf in (("dq", "q"), ("dk", "k"), ("dv", "v"), ("d_alpha_base", "ab"),
+                               ("d_beta_base", "bb"), ("d_alpha_out", "ao"), ("d_beta_out", "bo")):
+                _close(got[name], leaves[leaf].grad.numpy(), 1e-9, f"{tag} {name}")
+            if q_out is not None:
+                _close(got["dq_out"], qo_t.grad.numpy(), 1e-9, f"{tag} dq_out")
+            else:
+                assert got["dq_out"] is None
+
+
+def pin_backward_finite_difference(orc):
+    """Directional derivatives of L = <do_base, o_base> + <do_out, o_out>, taken
+    by central differences of the oracle's own (pinned) forward, equal the
+    gradients contracted with the same direction, one input at a time."""
+    B, T, Hq, Hkv, d, w = 2, 11, 4, 2, 8, 4
+    q, k, v, ab, bb, ao, bo, indptr, pos, q_out, do_b, do_o = _backward_inputs(7, B, T, Hq, Hkv, d, True)
+    scale = 0.4
+    got = orc.prefill_backward(q, k, v, ab, bb, ao, bo, indptr, pos, w, scale, do_b, do_o, q_out=q_out)
+    base = dict(q=q, k=k, v=v, ab=ab, bb=bb, ao=ao, bo=bo, q_out=q_out)
+    grad_of = dict(q="dq", k="dk", v="dv", ab="d_alpha_base", bb="d_beta_base",
+                   ao="d_alpha_out", bo="d_beta_out", q_out="dq_out")
+
+    def loss(x):
+        ob, _, oo, _ = orc.prefill(x["q"], x["k"], x["v"], x["ab"], x["bb"], x["ao"], x["bo"],
+                                   indptr, pos, w, scale, q_out=x["q_out"])
+        return float(np.sum(ob * do_b) + np.sum(oo * do_o))
+
+    r = np.random.default_rng(5)
+    h = 2.0 ** -9
+    for name, gname in grad_of.items():
+        u = r.standard_normal(base[name].shape)
+        xp, xm = dict(base), dict(base)
+        xp[name] = (base[name] + h * u).astype(np.float32)
+        xm[name] = (base[name] - h * u).astype(np.float32)
+        step = xp[name].astype(np.float64) - xm[name].astype(np.float64)  # the float32 step actually taken
+        fd = loss(xp) - loss(xm)
+        pred = float(np.sum(got[gname] * step))
+        assert abs(fd - pred) <= 1e-6 * max(1.0, abs(pred)), f"finite difference {name}: {fd} vs {pred}"
+
+
+def pin_backward_translation_sums(orc):
+    """Adding one vector c to every key of a (b, kv) sequence leaves every
+    output unchanged, so the keys' gradients sum to zero; adding c to every
+    value adds c to every output of that group, so the values' gradients sum
+    to the sum of all dO rows (both streams) of the group's query heads."""
+    B, T, Hq, Hkv, d, w = 2, 16, 6, 2, 8, 5
+    q, k, v, ab, bb, ao, bo, indptr, pos, q_out, do_b, do_o = _backward_inputs(11, B, T, Hq, Hkv, d, False)
+    got = orc.prefill_backward(q, k, v, ab, bb, ao, bo, indptr, pos, w, 0.3, do_b, do_o)
+    g = Hq // Hkv
+    for b in range(B):
+        r0, r1 = int(indptr[b]), int(indptr[b + 1])
+        for kv in range(Hkv):
+            hs = slice(kv * g, (kv + 1) * g)
+            _close(got["dk"][b, :, kv].sum(axis=0), np.zeros(d), 1e-11, "sum dk")
+            want = do_b[b, :, hs].astype(np.float64).sum(axis=(0, 1)) + do_o[r0:r1, hs].astype(np.float64).sum(axis=(0, 1))
+            _close(got["dv"][b, :, kv].sum(axis=0), want, 1e-11, "sum dv")
+
+
+def pin_backward_window_one(orc):
+    """w = 1 and no output rows: o_base[t] = v_t, so dv_t is the sum of dO over
+    the group's heads and every other gradient is zero."""
+    B, T, Hq, Hkv, d = 1, 9, 4, 2, 8
+    q, k, v, ab, bb, ao, bo = rng_inputs(41, B, T, Hq, Hkv, d)
+    indptr, pos = csr([[]])
+    do_b = np.random.default_rng(2).standard_normal((B, T, Hq, d)).astype(np.float32)
+    got = orc.prefill_backward(q, k, v, ab, bb, ao, bo, indptr, pos, 1, 0.5, do_b, None)
+    want = do_b.astype(np.float64).reshape(B, T, Hkv, Hq // Hkv, d).sum(axis=3)
+    _close(got["dv"], want, 1e-12, "w=1 dv")
+    for n in ("dq", "dk", "d_alpha_base", "d_beta_base", "d_alpha_out", "d_beta_out"):
+        _close(got[n], np.zeros_like(got[n]), 1e-12, f"w=1 {n}")
+
+
 ALL_PINS = [
     pin_brute_force_prefill,
     pin_row_subset,
@@ -389,4 +537,8 @@ ALL_PINS = [
     pin_decode_page_permutation,
     pin_prefill_decode_consistency,
     pin_hand_worked,
+    pin_backward_autograd,
+    pin_backward_finite_difference,
+    pin_backward_translation_sums,
+    pin_backward_window_one,
 ]

@@ -31,6 +31,18 @@ MUTANTS = {
     "values_are_keys": ("o[c] += p * (double)vj[c];", "o[c] += p * (double)krow[j][c];"),
     "no_normalisation": ("o[c] /= l;", "o[c] /= 1.0;"),
     "prefill_q_out_ignored": ("q_out ? q_out + ((size_t)r * Hq + h) * (size_t)d", "0 ? q_out + ((size_t)r * Hq + h) * (size_t)d"),
+    "bw_delta_dropped": ("const double ds = p * (dp - D);", "const double ds = p * dp;"),
+    "bw_dk_scale_dropped": ("dkrow[j][c] += scale * ds * qa[c];", "dkrow[j][c] += ds * qa[c];"),
+    "bw_dv_uses_ds": ("dvrow[j][c] += p * (double)dO[c];", "dvrow[j][c] += ds * (double)dO[c];"),
+    "bw_dp_uses_keys": ("dp += (double)dO[c] * (double)vrow[j][c];", "dp += (double)dO[c] * (double)krow[j][c];"),
+    "bw_dq_alpha_dropped": ("dq[qoff + c] += (double)alpha_base[(size_t)h * d + c] * dqa[c];", "dq[qoff + c] += dqa[c];"),
+    "bw_dalpha_uses_affined_q": ("d_alpha_base[(size_t)h * d + c] += dqa[c] * (double)q[qoff + c];",
+                                 "d_alpha_base[(size_t)h * d + c] += dqa[c] * qa[c];"),
+    "bw_out_rows_miss_dq": ("                            else\n                                dq[qoff + c] += gq;",
+                            "                            else\n                                (void)gq;"),
+    "bw_dbeta_out_to_base": ("d_beta_out[(size_t)h * d + c] += dqa[c];", "d_beta_base[(size_t)h * d + c] += dqa[c];"),
+    "bw_out_row_band": ("attend_row_backward(qa, do_out + roff, krow, vrow, dkrow, dvrow, 0, t,",
+                        "attend_row_backward(qa, do_out + roff, krow, vrow, dkrow, dvrow, t > 0 ? 1 : 0, t,"),
     "decode_append_wrong_slot": ("((size_t)pg * page_size + L % page_size) * tok;", "((size_t)pg * page_size + (L + 1) % page_size) * tok;"),
 }
 
