@@ -435,6 +435,10 @@ static void attend_row_backward(const double *qa, const float *dO, const float *
  * when q_out is given), d_alpha_base, d_beta_base, d_alpha_out, d_beta_out
  * [Hq,d]. Through the affine q = alpha (.) q_raw + beta (Sec. 3.1):
  * dq_raw = alpha (.) dqa, dalpha += dqa (.) q_raw, dbeta += dqa.
+ * Only rows (of either stream) at positions in [row_lo, row_hi) contribute:
+ * the full gradient is [0, T). A range [t0, T) still gives the exact dk, dv of
+ * every key j >= t0 (no row before t0 sees such a key) and the exact dq of the
+ * rows in the range, at a fraction of the cost on long sequences.
  * Parallel over kv heads only (each owns its K/V, query heads and affine rows).
  */
 int orthros_ref_prefill_backward(const float *q, const float *k, const float *v,
@@ -443,7 +447,7 @@ int orthros_ref_prefill_backward(const float *q, const float *k, const float *v,
                                  const int32_t *out_indptr, const int32_t *out_positions,
                                  const float *q_out, int B, int T, int Hq, int Hkv,
                                  int d, int window, double scale,
-                                 const float *do_base, const float *do_out,
+                                 const float *do_base, const float *do_out, int row_lo, int row_hi,
                                  double *dq, double *dk, double *dv, double *dq_out,
                                  double *d_alpha_base, double *d_beta_base,
                                  double *d_alpha_out, double *d_beta_out, int nthreads)
@@ -502,7 +506,7 @@ int orthros_ref_prefill_backward(const float *q, const float *k, const float *v,
                 }
                 for (int h = kv * g; h < (kv + 1) * g; ++h) {
                     /* base stream, Eq. 4 */
-                    for (int t = 0; t < T; ++t) {
+                    for (int t = row_lo > 0 ? row_lo : 0; t < T && t < row_hi; ++t) {
                         const size_t qoff = (((size_t)b * T + t) * Hq + h) * (size_t)d;
                         affine(q + qoff, alpha_base + (size_t)h * d, beta_base + (size_t)h * d, d, qa);
                         const int lo = t - window + 1 > 0 ? t - window + 1 : 0;
@@ -516,6 +520,8 @@ int orthros_ref_prefill_backward(const float *q, const float *k, const float *v,
                     /* output stream, Eq. 5 */
                     for (int r = out_indptr ? out_indptr[b] : 0; out_indptr && r < out_indptr[b + 1]; ++r) {
                         const int t = out_positions[r];
+                        if (t < row_lo || t >= row_hi)
+                            continue;
                         const size_t roff = ((size_t)r * Hq + h) * (size_t)d;
                         const size_t qoff = (((size_t)b * T + t) * Hq + h) * (size_t)d;
                         const float *qraw = q_out ? q_out + roff : q + qoff;

@@ -74,7 +74,7 @@ def _bind(path):
         _i32p, _i32p, _f32p,  # out_indptr out_positions q_out
         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
         ctypes.c_int, ctypes.c_double,  # B T Hq Hkv d window scale
-        _f32p, _f32p,  # do_base do_out
+        _f32p, _f32p, ctypes.c_int, ctypes.c_int,  # do_base do_out row_lo row_hi
         _f64p, _f64p, _f64p, _f64p,  # dq dk dv dq_out
         _f64p, _f64p, _f64p, _f64p,  # d alpha/beta base, d alpha/beta out
         ctypes.c_int,
@@ -220,10 +220,12 @@ def decode(q, k_new, v_new, k_cache, v_cache, block_table, cache_lens,
 
 def prefill_backward(q, k, v, alpha_base, beta_base, alpha_out, beta_out, out_indptr,
                      out_positions, window, scale, do_base, do_out, q_out=None,
-                     nthreads=0, _lib=None):
+                     row_range=None, nthreads=0, _lib=None):
     """Gradients of Eq. 4 (all T base rows) and Eq. 5 (the output rows) in float64.
 
     do_base [B,T,Hq,d] and do_out [n_out,Hq,d] are dL/do of the two streams.
+    row_range (lo, hi): only rows at positions in [lo, hi) contribute (default
+    all); [t0, T) still gives exact dk/dv for keys >= t0 and exact dq in range.
     Returns a dict with dq [B,T,Hq,d], dk, dv [B,T,Hkv,d], dq_out [n_out,Hq,d]
     (None when q_out is None: the output rows' gradient then lands in dq),
     d_alpha_base, d_beta_base, d_alpha_out, d_beta_out [Hq,d].
@@ -258,6 +260,7 @@ def prefill_backward(q, k, v, alpha_base, beta_base, alpha_out, beta_out, out_in
         _ptr(out_indptr, _i32p), _ptr(pos_arg, _i32p), _ptr(q_out, _f32p),
         B, T, Hq, Hkv, d, int(window), float(scale),
         _ptr(do_base, _f32p), _ptr(do_out_arg, _f32p),
+        int(row_range[0]) if row_range else 0, int(row_range[1]) if row_range else T,
         _ptr(dq, _f64p), _ptr(dk, _f64p), _ptr(dv, _f64p), _ptr(dq_out, _f64p),
         *(_ptr(g, _f64p) for g in grads),
         int(nthreads),

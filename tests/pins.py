@@ -510,6 +510,31 @@ def pin_backward_translation_sums(orc):
             _close(got["dv"][b, :, kv].sum(axis=0), want, 1e-11, "sum dv")
 
 
+def pin_backward_row_range(orc):
+    """Restricting the rows to positions [t0, T) leaves the gradients of every
+    key j >= t0 and of every row in the range unchanged (no earlier row sees
+    those keys); restricting to [0, t1) leaves dq of rows < t1 unchanged."""
+    B, T, Hq, Hkv, d, w = 1, 30, 4, 2, 8, 6
+    for with_q_out in (False, True):
+        q, k, v, ab, bb, ao, bo, indptr, pos, q_out, do_b, do_o = _backward_inputs(13, B, T, Hq, Hkv, d, with_q_out)
+        full = orc.prefill_backward(q, k, v, ab, bb, ao, bo, indptr, pos, w, 0.3, do_b, do_o, q_out=q_out)
+        t0, t1 = 17, 12
+        tail = orc.prefill_backward(q, k, v, ab, bb, ao, bo, indptr, pos, w, 0.3, do_b, do_o, q_out=q_out,
+                                    row_range=(t0, T))
+        head = orc.prefill_backward(q, k, v, ab, bb, ao, bo, indptr, pos, w, 0.3, do_b, do_o, q_out=q_out,
+                                    row_range=(0, t1))
+        _close(tail["dk"][:, t0:], full["dk"][:, t0:], 1e-12, "tail dk")
+        _close(tail["dv"][:, t0:], full["dv"][:, t0:], 1e-12, "tail dv")
+        if q_out is None:
+            _close(tail["dq"][:, t0:], full["dq"][:, t0:], 1e-12, "tail dq")
+            _close(head["dq"][:, :t1], full["dq"][:, :t1], 1e-12, "head dq")
+            _close(tail["dq"][:, :t0], np.zeros_like(full["dq"][:, :t0]), 0.0, "tail dq outside")
+        else:
+            sel = pos >= t0
+            _close(tail["dq_out"][sel], full["dq_out"][sel], 1e-12, "tail dq_out")
+            _close(tail["dq"][:, t0:], full["dq"][:, t0:], 1e-12, "tail dq")
+
+
 def pin_backward_window_one(orc):
     """w = 1 and no output rows: o_base[t] = v_t, so dv_t is the sum of dO over
     the group's heads and every other gradient is zero."""
@@ -540,5 +565,6 @@ ALL_PINS = [
     pin_backward_autograd,
     pin_backward_finite_difference,
     pin_backward_translation_sums,
+    pin_backward_row_range,
     pin_backward_window_one,
 ]
