@@ -18,6 +18,8 @@ from ._binding import (  # noqa: F401
     orthros_decode_workspace_size,
     orthros_last_error,
     orthros_prefill,
+    orthros_prefill_backward,
+    orthros_prefill_backward_workspace_size,
     orthros_prefill_workspace_size,
     orthros_profile_begin,
     orthros_profile_end,

@@ -21,7 +21,8 @@ STATUS_NAMES = {0: "ORTHROS_OK", 1: "ORTHROS_EINVAL", 2: "ORTHROS_EUNSUPPORTED",
                 4: "ORTHROS_EWORKSPACE", 5: "ORTHROS_EDEVICE", 6: "ORTHROS_ETIMEOUT"}
 
 # the public symbols of include/orthros_attn.h
-EXPORTS = ("orthros_prefill_workspace_size", "orthros_prefill", "orthros_decode_workspace_size",
+EXPORTS = ("orthros_prefill_workspace_size", "orthros_prefill", "orthros_prefill_backward_workspace_size",
+           "orthros_prefill_backward", "orthros_decode_workspace_size",
            "orthros_decode", "orthros_decode_static", "orthros_check", "orthros_profile_begin", "orthros_profile_end",
            "orthros_status_string", "orthros_last_error")
 
@@ -59,6 +60,13 @@ def load_library(path: str | None = None):
         lib.orthros_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32p, vp, i32, vp,
                                         i32, i32, i32, i32, i32, i32, ctypes.c_float, i32,
                                         vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp, sz, vp]
+        lib.orthros_prefill_backward_workspace_size.restype = sz
+        lib.orthros_prefill_backward_workspace_size.argtypes = [i32] * 8
+        lib.orthros_prefill_backward.restype = i32
+        lib.orthros_prefill_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32p, vp, i32, vp,
+                                                 i32, i32, i32, i32, i32, i32, ctypes.c_float, i32,
+                                                 vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                                 vp, sz, vp]
         lib.orthros_decode_workspace_size.restype = sz
         lib.orthros_decode_workspace_size.argtypes = [i32] * 7
         lib.orthros_decode.restype = i32
@@ -174,6 +182,52 @@ def orthros_prefill(q, k, v, alpha_base, beta_base, alpha_out, beta_out, out_ind
         _ptr(workspace), workspace.numel(), _stream(stream))
     _raise_if(rc, lib)
     return o_base, lse_base, o_out, lse_out
+
+
+def orthros_prefill_backward_workspace_size(B, T, Hq, Hkv, d, n_out, window, dtype=torch.bfloat16) -> int:
+    return int(load_library().orthros_prefill_backward_workspace_size(B, T, Hq, Hkv, d, n_out, window,
+                                                                      _DTYPES[dtype]))
+
+
+def orthros_prefill_backward(q, k, v, alpha_base, beta_base, alpha_out, beta_out, out_indptr, out_positions,
+                             window, scale, o_base, lse_base, o_out, lse_out, do_base, do_out, *, q_out=None,
+                             out=None, workspace=None, stream=None):
+    """orthros_prefill_backward of include/orthros_attn.h on torch CUDA tensors.
+
+    Returns a dict with dq, dk, dv, dq_out (None without q_out), d_alpha_base,
+    d_beta_base, d_alpha_out, d_beta_out; allocated here unless `out` (a dict
+    with the same keys) gives them.
+    """
+    lib = load_library()
+    B, T, Hq, d = q.shape
+    Hkv = k.shape[2]
+    indptr = np.ascontiguousarray(np.asarray(out_indptr.cpu() if isinstance(out_indptr, torch.Tensor)
+                                             else out_indptr, dtype=np.int32))
+    n_out = int(indptr[-1]) if indptr.size else 0
+    if scale is None:
+        scale = d ** -0.5
+    for name, t in (("q", q), ("k", k), ("v", v), ("q_out", q_out), ("out_positions", out_positions),
+                    ("o_base", o_base), ("o_out", o_out), ("do_base", do_base), ("do_out", do_out)):
+        _contig(name, t)
+    if out is None:
+        dev = q.device
+        out = {"dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v),
+               "dq_out": torch.empty_like(q_out) if q_out is not None else None}
+        for n in ("d_alpha_base", "d_beta_base", "d_alpha_out", "d_beta_out"):
+            out[n] = torch.empty((Hq, d), dtype=torch.float32, device=dev)
+    if workspace is None:
+        ws = orthros_prefill_backward_workspace_size(B, T, Hq, Hkv, d, n_out, window, q.dtype)
+        workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=q.device)
+    rc = lib.orthros_prefill_backward(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(alpha_base), _ptr(beta_base), _ptr(alpha_out), _ptr(beta_out),
+        indptr.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), _ptr(out_positions), n_out, _ptr(q_out),
+        B, T, Hq, Hkv, d, int(window), float(scale), _dtype(q),
+        _ptr(o_base), _ptr(lse_base), _ptr(o_out), _ptr(lse_out), _ptr(do_base), _ptr(do_out),
+        _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dq_out"]),
+        _ptr(out["d_alpha_base"]), _ptr(out["d_beta_base"]), _ptr(out["d_alpha_out"]), _ptr(out["d_beta_out"]),
+        _ptr(workspace), workspace.numel(), _stream(stream))
+    _raise_if(rc, lib)
+    return out
 
 
 def orthros_decode(q, k_new, v_new, k_cache, v_cache, block_table, cache_lens, alpha_base, beta_base,

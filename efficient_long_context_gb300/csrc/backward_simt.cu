@@ -1,0 +1,341 @@
+// backward_simt.cu -- gradients of the banded and cross rows on CUDA cores.
+//
+// The backward of Sec. 3.1 Eq. 4 (every position t over keys max(0,t-w+1)..t)
+// and Eq. 5 (every output row at position t_r over keys 0..t_r), both behind
+// the query affine q = alpha (.) q_raw + beta (Alg. 1 line 5). With the
+// forward's log-sum-exp L and D = dO . o of each row, each (row, key) pair
+// contributes
+//   p  = exp(scale * qa . k - L)
+//   ds = p * (dO . v - D)
+//   dv_key += p * dO,   dk_key += scale * ds * qa,   dqa_row += scale * ds * k
+// and, through the affine, dq_raw = alpha (.) dqa, dalpha += dqa (.) q_raw,
+// dbeta += dqa. Output rows that read q at their own position (no separate
+// q_out) add their dq_raw into that position's dq.
+//
+// Layout of the work, any element type, fp32 arithmetic:
+//   delta kernel  one warp per row: D = dO . o
+//   dk/dv kernel  one warp per (sequence, kv head, key): walks every query
+//                 row of the group's heads that sees the key, in both streams;
+//                 each key's dk and dv are written once, no atomics
+//   dq kernel     one warp per (row, head): walks the row's keys; a block of 8
+//                 warps shares one head and reduces its affine gradients in
+//                 shared memory before one atomic add per channel
+// Lane l holds channels [l*E, l*E+E), E = d/32, of every row it touches.
+#include "internal.cuh"
+
+namespace orthros {
+namespace {
+
+constexpr int kWarps = 8;
+
+template <typename T, int E>
+__device__ __forceinline__ void ld(const T *p, float (&x)[E]) {
+    if constexpr (sizeof(T) == 4) {
+#pragma unroll
+        for (int e = 0; e < E; e += 2) {
+            const float2 r = *reinterpret_cast<const float2 *>(p + e);
+            x[e] = r.x;
+            x[e + 1] = r.y;
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < E; e += 2) {
+            const __nv_bfloat162 r = *reinterpret_cast<const __nv_bfloat162 *>(p + e);
+            x[e] = __low2float(r);
+            x[e + 1] = __high2float(r);
+        }
+    }
+}
+
+template <typename T, int E>
+__device__ __forceinline__ void st(T *p, const float (&x)[E]) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) p[e] = from_f32<T>(x[e]);
+}
+
+__device__ __forceinline__ float wsum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+template <int E>
+__device__ __forceinline__ float dot(const float (&a)[E], const float (&b)[E]) {
+    float s = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) s = fmaf(a[e], b[e], s);
+    return s;
+}
+
+// Sequence of output row r: the last b with indptr[b] <= r.
+__device__ __forceinline__ int seq_of_row(const int32_t *indptr, int B, int r) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (indptr[mid] <= r) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(256) bwd_delta_kernel(BwdArgs a, long long n_base) {
+    constexpr int E = D / 32;
+    const int lane = threadIdx.x & 31;
+    const long long unit = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const long long n_units = n_base + (long long)a.n_out * a.Hq;
+    if (unit >= n_units) return;
+    float o[E], dO[E];
+    if (unit < n_base) {  // unit = (b, t, h) in [B,T,Hq] order
+        const int h = (int)(unit % a.Hq);
+        const long long bt = unit / a.Hq;
+        const int t = (int)(bt % a.T), b = (int)(bt / a.T);
+        ld<T, E>(static_cast<const T *>(a.o_base) + unit * D + lane * E, o);
+        ld<T, E>(static_cast<const T *>(a.do_base) + unit * D + lane * E, dO);
+        const float s = wsum(dot<E>(o, dO));
+        if (lane == 0) a.delta_base[((long long)b * a.Hq + h) * a.T + t] = s;
+    } else {
+        const long long u = unit - n_base;  // (r, h)
+        ld<T, E>(static_cast<const T *>(a.o_out) + u * D + lane * E, o);
+        ld<T, E>(static_cast<const T *>(a.do_out) + u * D + lane * E, dO);
+        const float s = wsum(dot<E>(o, dO));
+        if (lane == 0) a.delta_out[u] = s;
+    }
+}
+
+// Threads the output rows of each position into a list (positions may repeat):
+// pos_head[b*T + t] is the first row at (b, t), row_next[r] the next one, -1 ends.
+__global__ void bwd_row_lists_kernel(BwdArgs a) {
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= a.n_out) return;
+    const int b = seq_of_row(a.out_indptr, a.B, r);
+    const int t = a.out_positions[r];
+    if (t < 0 || t >= a.T) {
+        set_status(a.status, ORTHROS_DEV_BAD_POSITION);
+        a.row_next[r] = -1;
+        return;
+    }
+    a.row_next[r] = atomicExch(a.pos_head + (long long)b * a.T + t, r);
+}
+
+// One (row, key) pair seen from the key's side: accumulates dv and dk (unscaled).
+template <int E>
+__device__ __forceinline__ void key_pair(const float (&k)[E], const float (&v)[E], const float (&qa)[E],
+                                         const float (&dO)[E], float lse, float delta, float scale,
+                                         float (&dk)[E], float (&dv)[E]) {
+    const float s = wsum(dot<E>(qa, k)) * scale;
+    const float p = __expf(s - lse);
+    const float dp = wsum(dot<E>(dO, v));
+    const float ds = p * (dp - delta);
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        dv[e] = fmaf(p, dO[e], dv[e]);
+        dk[e] = fmaf(ds, qa[e], dk[e]);
+    }
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(256) bwd_dkdv_kernel(BwdArgs a) {
+    constexpr int E = D / 32;
+    const int lane = threadIdx.x & 31;
+    const long long unit = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5);  // (b, j, kv)
+    if (unit >= (long long)a.B * a.T * a.Hkv) return;
+    const int kv = (int)(unit % a.Hkv);
+    const long long bj = unit / a.Hkv;
+    const int j = (int)(bj % a.T), b = (int)(bj / a.T);
+    const int g = a.Hq / a.Hkv;
+    float k[E], v[E], dk[E], dv[E];
+    ld<T, E>(static_cast<const T *>(a.k) + unit * D + lane * E, k);
+    ld<T, E>(static_cast<const T *>(a.v) + unit * D + lane * E, v);
+#pragma unroll
+    for (int e = 0; e < E; ++e) dk[e] = dv[e] = 0.f;
+    const int t_hi = (int)min((long long)a.T - 1, (long long)j + a.window - 1);
+    const int r0 = a.n_out ? a.out_indptr[b] : 0, r1 = a.n_out ? a.out_indptr[b + 1] : 0;
+    for (int h = kv * g; h < (kv + 1) * g; ++h) {
+        float al[E], be[E], qa[E], dO[E];
+        ld<float, E>(a.alpha_base + h * D + lane * E, al);
+        ld<float, E>(a.beta_base + h * D + lane * E, be);
+        for (int t = j; t <= t_hi; ++t) {  // base rows that see key j
+            const long long row = ((long long)b * a.T + t) * a.Hq + h;
+            ld<T, E>(static_cast<const T *>(a.q) + row * D + lane * E, qa);
+#pragma unroll
+            for (int e = 0; e < E; ++e) qa[e] = fmaf(al[e], qa[e], be[e]);
+            ld<T, E>(static_cast<const T *>(a.do_base) + row * D + lane * E, dO);
+            const long long li = ((long long)b * a.Hq + h) * a.T + t;
+            key_pair<E>(k, v, qa, dO, a.lse_base[li], a.delta_base[li], a.scale, dk, dv);
+        }
+        if (r1 > r0) {
+            ld<float, E>(a.alpha_out + h * D + lane * E, al);
+            ld<float, E>(a.beta_out + h * D + lane * E, be);
+        }
+        for (int r = r0; r < r1; ++r) {  // output rows at positions >= j
+            const int t = a.out_positions[r];
+            if (t < j || t >= a.T) continue;
+            const long long ro = (long long)r * a.Hq + h;
+            const T *qraw = a.q_out ? static_cast<const T *>(a.q_out) + ro * D
+                                    : static_cast<const T *>(a.q) + (((long long)b * a.T + t) * a.Hq + h) * D;
+            ld<T, E>(qraw + lane * E, qa);
+#pragma unroll
+            for (int e = 0; e < E; ++e) qa[e] = fmaf(al[e], qa[e], be[e]);
+            ld<T, E>(static_cast<const T *>(a.do_out) + ro * D + lane * E, dO);
+            key_pair<E>(k, v, qa, dO, a.lse_out[ro], a.delta_out[ro], a.scale, dk, dv);
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) dk[e] *= a.scale;
+    st<T, E>(static_cast<T *>(a.dk) + unit * D + lane * E, dk);
+    st<T, E>(static_cast<T *>(a.dv) + unit * D + lane * E, dv);
+}
+
+// kind 0: base rows, grid (ceil(T/8), Hq, B); kind 1: output rows, grid (ceil(n_out/8), Hq).
+template <typename T, int D>
+__global__ void __launch_bounds__(256) bwd_dq_kernel(BwdArgs a, int kind) {
+    constexpr int E = D / 32;
+    __shared__ float red[2][kWarps][D];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int h = blockIdx.y;
+    const int kv = h / (a.Hq / a.Hkv);
+    float dqa[E], qraw[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) dqa[e] = qraw[e] = 0.f;
+    const float *alpha = kind == 0 ? a.alpha_base : a.alpha_out;
+    const float *beta = kind == 0 ? a.beta_base : a.beta_out;
+    int b = 0, t = -1, r = -1;
+    bool active;
+    if (kind == 0) {
+        b = blockIdx.z;
+        t = blockIdx.x * kWarps + warp;
+        active = t < a.T;
+    } else {
+        r = blockIdx.x * kWarps + warp;
+        active = r < a.n_out;
+        if (active) {
+            b = seq_of_row(a.out_indptr, a.B, r);
+            t = a.out_positions[r];
+            if (t < 0 || t >= a.T) {
+                set_status(a.status, ORTHROS_DEV_BAD_POSITION);
+                float nanv[E];
+#pragma unroll
+                for (int e = 0; e < E; ++e) nanv[e] = __int_as_float(0x7fc00000);
+                const long long ro = (long long)r * a.Hq + h;
+                if (a.q_out) st<T, E>(static_cast<T *>(a.dq_out) + ro * D + lane * E, nanv);
+                else st<float, E>(a.dq_rows + ro * D + lane * E, nanv);
+                active = false;
+            }
+        }
+    }
+    if (active) {
+        float al[E], be[E], qa[E], dO[E], k[E], v[E];
+        ld<float, E>(alpha + h * D + lane * E, al);
+        ld<float, E>(beta + h * D + lane * E, be);
+        const long long row = ((long long)b * a.T + t) * a.Hq + h;
+        const long long ro = (long long)r * a.Hq + h;
+        const T *qp = (kind == 1 && a.q_out) ? static_cast<const T *>(a.q_out) + ro * D
+                                             : static_cast<const T *>(a.q) + row * D;
+        ld<T, E>(qp + lane * E, qraw);
+#pragma unroll
+        for (int e = 0; e < E; ++e) qa[e] = fmaf(al[e], qraw[e], be[e]);
+        float lse, delta;
+        if (kind == 0) {
+            ld<T, E>(static_cast<const T *>(a.do_base) + row * D + lane * E, dO);
+            const long long li = ((long long)b * a.Hq + h) * a.T + t;
+            lse = a.lse_base[li];
+            delta = a.delta_base[li];
+        } else {
+            ld<T, E>(static_cast<const T *>(a.do_out) + ro * D + lane * E, dO);
+            lse = a.lse_out[ro];
+            delta = a.delta_out[ro];
+        }
+        const int lo = kind == 0 ? max(0, t - a.window + 1) : 0;
+        const T *kb = static_cast<const T *>(a.k) + ((long long)b * a.T * a.Hkv + kv) * D + lane * E;
+        const T *vb = static_cast<const T *>(a.v) + ((long long)b * a.T * a.Hkv + kv) * D + lane * E;
+        for (int j = lo; j <= t; ++j) {
+            ld<T, E>(kb + (long long)j * a.Hkv * D, k);
+            ld<T, E>(vb + (long long)j * a.Hkv * D, v);
+            const float s = wsum(dot<E>(qa, k)) * a.scale;
+            const float p = __expf(s - lse);
+            const float dp = wsum(dot<E>(dO, v));
+            const float ds = p * (dp - delta);
+#pragma unroll
+            for (int e = 0; e < E; ++e) dqa[e] = fmaf(ds, k[e], dqa[e]);
+        }
+        float dq[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            dqa[e] *= a.scale;
+            dq[e] = al[e] * dqa[e];
+        }
+        if (kind == 0) {
+            // output rows at this position that read this q add their share
+            int rr = (a.q_out || a.n_out == 0) ? -1 : a.pos_head[(long long)b * a.T + t];
+            for (int guard = 0; rr >= 0 && rr < a.n_out && guard < a.n_out; ++guard) {
+                float add[E];
+                ld<float, E>(a.dq_rows + ((long long)rr * a.Hq + h) * D + lane * E, add);
+#pragma unroll
+                for (int e = 0; e < E; ++e) dq[e] += add[e];
+                rr = a.row_next[rr];
+            }
+            st<T, E>(static_cast<T *>(a.dq) + row * D + lane * E, dq);
+        } else if (a.q_out) {
+            st<T, E>(static_cast<T *>(a.dq_out) + ro * D + lane * E, dq);
+        } else {
+            st<float, E>(a.dq_rows + ro * D + lane * E, dq);
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        red[0][warp][lane * E + e] = dqa[e] * qraw[e];  // zero for inactive warps
+        red[1][warp][lane * E + e] = dqa[e];
+    }
+    __syncthreads();
+    float *ga = kind == 0 ? a.d_alpha_base : a.d_alpha_out;
+    float *gb = kind == 0 ? a.d_beta_base : a.d_beta_out;
+    for (int i = threadIdx.x; i < 2 * D; i += blockDim.x) {
+        const int which = i / D, c = i % D;
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) s += red[which][w][c];
+        atomicAdd((which ? gb : ga) + h * D + c, s);
+    }
+}
+
+template <typename T, int D>
+cudaError_t launch_t(const BwdArgs &a, cudaStream_t stream, const char *const names[4]) {
+    const long long n_base = (long long)a.B * a.T * a.Hq;
+    const long long n_rows = n_base + (long long)a.n_out * a.Hq;
+    {
+        ProfScope ps(names[0], stream);
+        if (a.n_out > 0) {
+            bwd_row_lists_kernel<<<(a.n_out + 255) / 256, 256, 0, stream>>>(a);
+        }
+        bwd_delta_kernel<T, D><<<(unsigned)((n_rows + kWarps - 1) / kWarps), kWarps * 32, 0, stream>>>(a, n_base);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    {
+        ProfScope ps(names[1], stream);
+        const long long n = (long long)a.B * a.T * a.Hkv;
+        bwd_dkdv_kernel<T, D><<<(unsigned)((n + kWarps - 1) / kWarps), kWarps * 32, 0, stream>>>(a);
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (a.n_out > 0) {
+        ProfScope ps(names[2], stream);
+        bwd_dq_kernel<T, D><<<dim3((a.n_out + kWarps - 1) / kWarps, a.Hq), kWarps * 32, 0, stream>>>(a, 1);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    {
+        ProfScope ps(names[3], stream);
+        bwd_dq_kernel<T, D><<<dim3((a.T + kWarps - 1) / kWarps, a.Hq, a.B), kWarps * 32, 0, stream>>>(a, 0);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_backward_simt(const BwdArgs &a, int d, orthros_dtype dtype, cudaStream_t stream) {
+    static const char *const names[4] = {"bwd_delta", "bwd_dkdv_simt", "bwd_dq_out_simt", "bwd_dq_simt"};
+    if (dtype == ORTHROS_F32)
+        return d == 64 ? launch_t<float, 64>(a, stream, names) : launch_t<float, 128>(a, stream, names);
+    return d == 64 ? launch_t<__nv_bfloat16, 64>(a, stream, names) : launch_t<__nv_bfloat16, 128>(a, stream, names);
+}
+
+}  // namespace orthros

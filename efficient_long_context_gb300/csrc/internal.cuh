@@ -133,6 +133,27 @@ bool encode_kv_map_3d(CUtensorMap *m, const void *base, long long tokens, int Hk
 cudaError_t launch_rows_simt(const RowsArgs &a, RowKind kind, int d, orthros_dtype dtype,
                              cudaStream_t stream);
 
+// backward_simt.cu: gradients of the base and output rows (any element type).
+struct BwdArgs {
+    const void *q, *q_out, *k, *v;  // forward inputs, layouts as in orthros_prefill
+    const float *alpha_base, *beta_base, *alpha_out, *beta_out;
+    const int32_t *out_indptr;     // device [B+1]
+    const int32_t *out_positions;  // [n_out]
+    int32_t *pos_head;             // [B*T]: first output row at (b, t), or -1 (set to -1 by the caller)
+    int32_t *row_next;             // [n_out]: next output row at the same position, or -1
+    int n_out, B, T, Hq, Hkv, window;
+    float scale;
+    const void *o_base, *o_out, *do_base, *do_out;  // forward outputs and their gradients
+    const float *lse_base, *lse_out;
+    float *delta_base;  // [B,Hq,T]  dO . o of every base row
+    float *delta_out;   // [n_out,Hq]
+    float *dq_rows;     // [n_out,Hq,d] fp32 dq of output rows that read q (q_out == nullptr)
+    void *dq, *dk, *dv, *dq_out;
+    float *d_alpha_base, *d_beta_base, *d_alpha_out, *d_beta_out;  // zeroed by the caller
+    uint32_t *status;
+};
+cudaError_t launch_backward_simt(const BwdArgs &a, int d, orthros_dtype dtype, cudaStream_t stream);
+
 // cache.cu
 cudaError_t launch_decode_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
                                  const int32_t *block_table, const int32_t *cache_lens, int B, int Hkv,

@@ -80,6 +80,30 @@ DecodeLayout decode_layout(int B, int Hkv, int d, int max_pages, int page_size, 
     return L;
 }
 
+// Workspace regions of orthros_prefill_backward.
+struct BackwardLayout {
+    size_t indptr_off, head_off, next_off, delta_base_off, delta_out_off, dq_rows_off, total;
+};
+
+BackwardLayout backward_layout(int B, int T, int Hq, int d, int n_out) {
+    BackwardLayout L{};
+    size_t at = kStatusBytes;
+    L.indptr_off = at;
+    at += align_up(sizeof(int32_t) * (size_t)(B + 1), 256);
+    L.head_off = at;
+    at += align_up(sizeof(int32_t) * (size_t)B * T, 256);
+    L.next_off = at;
+    at += align_up(sizeof(int32_t) * (size_t)n_out, 256);
+    L.delta_base_off = at;
+    at += align_up(sizeof(float) * (size_t)B * Hq * T, 256);
+    L.delta_out_off = at;
+    at += align_up(sizeof(float) * (size_t)n_out * Hq, 256);
+    L.dq_rows_off = at;
+    at += align_up(sizeof(float) * (size_t)n_out * Hq * d, 256);
+    L.total = at;
+    return L;
+}
+
 orthros_status check_shapes(int B, int Hq, int Hkv, int d, int window, float scale, orthros_dtype dtype) {
     if (B < 0) return fail(ORTHROS_EINVAL, "B = %d must be >= 0", B);
     if (Hq < 1 || Hkv < 1) return fail(ORTHROS_EINVAL, "head counts Hq = %d, Hkv = %d must be >= 1", Hq, Hkv);
@@ -355,6 +379,132 @@ orthros_status orthros_prefill(const void *q, const void *k, const void *v, cons
         e = launch_prefill_tc(tp, k16, v, d, stream);
     }
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core prefill launch");
+    return ORTHROS_OK;
+}
+
+size_t orthros_prefill_backward_workspace_size(int B, int T, int Hq, int Hkv, int d, int n_out, int window,
+                                               orthros_dtype dtype) {
+    if (T < 0 || n_out < 0) return 0;
+    if (check_shapes(B, Hq, Hkv, d, window, 1.0f, dtype) != ORTHROS_OK) return 0;
+    return backward_layout(B, T, Hq, d, n_out).total;
+}
+
+orthros_status orthros_prefill_backward(const void *q, const void *k, const void *v, const float *alpha_base,
+                                        const float *beta_base, const float *alpha_out, const float *beta_out,
+                                        const int32_t *out_indptr, const int32_t *out_positions, int n_out,
+                                        const void *q_out, int B, int T, int Hq, int Hkv, int d, int window,
+                                        float scale, orthros_dtype dtype, const void *o_base,
+                                        const float *lse_base, const void *o_out, const float *lse_out,
+                                        const void *do_base, const void *do_out, void *dq, void *dk, void *dv,
+                                        void *dq_out, float *d_alpha_base, float *d_beta_base,
+                                        float *d_alpha_out, float *d_beta_out, void *workspace,
+                                        size_t workspace_bytes, orthros_stream_t stream_) {
+    g_last_error.clear();
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    orthros_status st = check_shapes(B, Hq, Hkv, d, window, scale, dtype);
+    if (st != ORTHROS_OK) return st;
+    if (T < 0) return fail(ORTHROS_EINVAL, "T = %d must be >= 0", T);
+    if (n_out < 0) return fail(ORTHROS_EINVAL, "n_out = %d must be >= 0", n_out);
+    const long long rows = (long long)B * T;
+    if (rows > (1LL << 31)) return fail(ORTHROS_EUNSUPPORTED, "B*T = %lld tokens exceeds 2^31", rows);
+    if (B > 65535) return fail(ORTHROS_EUNSUPPORTED, "B = %d exceeds 65535 sequences per call", B);
+    if (!d_alpha_base || !d_beta_base || !d_alpha_out || !d_beta_out)
+        return fail(ORTHROS_EINVAL, "the four affine gradients must not be NULL");
+    if (rows > 0) {
+        if (!q || !k || !v || !o_base || !lse_base || !do_base || !dq || !dk || !dv)
+            return fail(ORTHROS_EINVAL, "q, k, v, o_base, lse_base, do_base, dq, dk and dv must not be NULL");
+        if (!alpha_base || !beta_base) return fail(ORTHROS_EINVAL, "alpha_base and beta_base must not be NULL");
+        if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o_base) || !aligned16(do_base) ||
+            !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+            return fail(ORTHROS_EINVAL, "element tensors must be 16-byte aligned");
+        if (!aligned16(alpha_base) || !aligned16(beta_base))
+            return fail(ORTHROS_EINVAL, "alpha_base and beta_base must be 16-byte aligned");
+    }
+    if (B > 0 && !out_indptr) return fail(ORTHROS_EINVAL, "out_indptr (host) must not be NULL");
+    if (B > 0) {
+        if (out_indptr[0] != 0) return fail(ORTHROS_EINVAL, "out_indptr[0] = %d must be 0", out_indptr[0]);
+        for (int b = 0; b < B; ++b)
+            if (out_indptr[b + 1] < out_indptr[b])
+                return fail(ORTHROS_EINVAL, "out_indptr decreases at %d", b);
+        if (out_indptr[B] != n_out)
+            return fail(ORTHROS_EINVAL, "out_indptr[B] = %d differs from n_out = %d", out_indptr[B], n_out);
+    } else if (n_out != 0) {
+        return fail(ORTHROS_EINVAL, "n_out = %d with B = 0", n_out);
+    }
+    if (n_out > 0) {
+        if (T == 0) return fail(ORTHROS_EINVAL, "output rows with T = 0");
+        if (!out_positions || !alpha_out || !beta_out || !o_out || !lse_out || !do_out)
+            return fail(ORTHROS_EINVAL, "out_positions, alpha_out, beta_out, o_out, lse_out and do_out "
+                                        "must not be NULL when n_out > 0");
+        if (q_out && !dq_out) return fail(ORTHROS_EINVAL, "dq_out must not be NULL when q_out is given");
+        if (!aligned16(o_out) || !aligned16(do_out) || (q_out && (!aligned16(q_out) || !aligned16(dq_out))) ||
+            !aligned16(alpha_out) || !aligned16(beta_out))
+            return fail(ORTHROS_EINVAL, "output-row tensors and affines must be 16-byte aligned");
+    }
+    const BackwardLayout lay = backward_layout(B, T, Hq, d, n_out);
+    if (!workspace || workspace_bytes < lay.total)
+        return fail(ORTHROS_EWORKSPACE, "workspace needs %zu bytes, got %zu", lay.total,
+                    workspace ? workspace_bytes : (size_t)0);
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(ORTHROS_EINVAL, "workspace must be 256-byte aligned");
+
+    char *ws = static_cast<char *>(workspace);
+    uint32_t *status = reinterpret_cast<uint32_t *>(ws);
+    cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "status reset");
+    const size_t affine_bytes = sizeof(float) * (size_t)Hq * d;
+    for (float *g : {d_alpha_base, d_beta_base, d_alpha_out, d_beta_out})
+        if ((e = cudaMemsetAsync(g, 0, affine_bytes, stream)) != cudaSuccess) return cuda_fail(e, "gradient reset");
+    if (rows == 0) return ORTHROS_OK;
+    int32_t *indptr_dev = reinterpret_cast<int32_t *>(ws + lay.indptr_off);
+    int32_t *head = reinterpret_cast<int32_t *>(ws + lay.head_off);
+    if (n_out > 0) {
+        e = cudaMemcpyAsync(indptr_dev, out_indptr, sizeof(int32_t) * (size_t)(B + 1), cudaMemcpyHostToDevice,
+                            stream);
+        if (e != cudaSuccess) return cuda_fail(e, "indptr upload");
+        if ((e = cudaMemsetAsync(head, 0xff, sizeof(int32_t) * (size_t)rows, stream)) != cudaSuccess)
+            return cuda_fail(e, "row-list reset");
+    }
+    BwdArgs a{};
+    a.q = q;
+    a.q_out = q_out;
+    a.k = k;
+    a.v = v;
+    a.alpha_base = alpha_base;
+    a.beta_base = beta_base;
+    a.alpha_out = alpha_out;
+    a.beta_out = beta_out;
+    a.out_indptr = indptr_dev;
+    a.out_positions = out_positions;
+    a.pos_head = head;
+    a.row_next = reinterpret_cast<int32_t *>(ws + lay.next_off);
+    a.n_out = n_out;
+    a.B = B;
+    a.T = T;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.window = window;
+    a.scale = scale;
+    a.o_base = o_base;
+    a.o_out = o_out;
+    a.do_base = do_base;
+    a.do_out = do_out;
+    a.lse_base = lse_base;
+    a.lse_out = lse_out;
+    a.delta_base = reinterpret_cast<float *>(ws + lay.delta_base_off);
+    a.delta_out = reinterpret_cast<float *>(ws + lay.delta_out_off);
+    a.dq_rows = reinterpret_cast<float *>(ws + lay.dq_rows_off);
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.dq_out = q_out ? dq_out : nullptr;
+    a.d_alpha_base = d_alpha_base;
+    a.d_beta_base = d_beta_base;
+    a.d_alpha_out = d_alpha_out;
+    a.d_beta_out = d_beta_out;
+    a.status = status;
+    e = launch_backward_simt(a, d, dtype, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "backward launch");
     return ORTHROS_OK;
 }
 

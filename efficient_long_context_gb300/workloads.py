@@ -134,6 +134,18 @@ def make_prefill(w: PrefillWorkload, seed: int | None = None, out_mode=None, wit
                 B=B, T=T, Hq=Hq, Hkv=Hkv, d=d, window=w.window, scale=w.scale, dtype=w.dtype)
 
 
+def make_grad_outputs(wl: dict, seed: int):
+    """Seeded gradients dL/do for a prefill workload (the backward's inputs):
+    do_base [B,T,Hq,d] and do_out [n_out,Hq,d], N(0,1) in the workload's dtype."""
+    gen = torch.Generator()
+    gen.manual_seed(seed)
+    B, T, Hq, d = wl["B"], wl["T"], wl["Hq"], wl["d"]
+    n_out = int(wl["out_indptr"][-1])
+    do_base = _normal(gen, (B, T, Hq, d), wl["dtype"])
+    do_out = _normal(gen, (n_out, Hq, d), wl["dtype"])
+    return do_base, do_out
+
+
 def small_prefill(B, T, Hq, Hkv, d, window, dtype=torch.bfloat16, out_mode="last", seed=7,
                   with_q_out=False, k_offset_std=0.0):
     """A small prefill case for parity sweeps (same recipe as the named workloads)."""

@@ -123,6 +123,49 @@ ORTHROS_API orthros_status orthros_prefill(
     int max_pages, int page_size, int num_pages,
     void *workspace, size_t workspace_bytes, orthros_stream_t stream);
 
+/* Workspace bytes orthros_prefill_backward needs for these sizes (0 if rejected). */
+ORTHROS_API size_t orthros_prefill_backward_workspace_size(int B, int T, int Hq, int Hkv, int d,
+                                               int n_out, int window, orthros_dtype dtype);
+
+/*
+ * Backward of orthros_prefill for training in the pre-training and
+ * fine-tuning regimes (Sec. 3.2): the gradients of a loss L with respect to
+ * q, k, v, q_out and the four affine vectors, given dL/do of both streams.
+ * The paper prints no backward; it is the chain rule through Eq. 4 and Eq. 5
+ * (softmax attention) and through the affines q = alpha (.) q_raw + beta.
+ * lse is an output the loss is taken not to depend on.
+ *
+ * Forward arguments (q .. scale, dtype) exactly as given to orthros_prefill,
+ * except that out_positions must hold positions in [0, T) (repeats allowed).
+ * o_base, lse_base, o_out, lse_out  the outputs orthros_prefill returned for
+ *              them (o is used for D = dO . o, lse to recompute softmax weights)
+ * do_base [B, T, Hq, d], do_out [n_out, Hq, d]: dL/do_base, dL/do_out
+ * dq      [B, T, Hq, d]  dL/dq. When q_out is NULL the output rows read q at
+ *              their positions, and their share is included here.
+ * dk, dv  [B, T, Hkv, d] (both streams' shares)
+ * dq_out  [n_out, Hq, d] dL/dq_out; required when q_out is given, else ignored
+ * d_alpha_base, d_beta_base, d_alpha_out, d_beta_out [Hq, d] float
+ * All gradients are overwritten (not accumulated into). Element tensors have
+ * the dtype of q; lse and the affine gradients are float.
+ * workspace    at least orthros_prefill_backward_workspace_size() bytes,
+ *              256-byte aligned; contents on entry do not matter.
+ * Errors as for orthros_prefill; an output position outside [0, T) sets
+ * ORTHROS_DEV_BAD_POSITION and that row's dq_out (or share of dq) is NaN/absent.
+ */
+ORTHROS_API orthros_status orthros_prefill_backward(
+    const void *q, const void *k, const void *v,
+    const float *alpha_base, const float *beta_base,
+    const float *alpha_out, const float *beta_out,
+    const int32_t *out_indptr, const int32_t *out_positions, int n_out,
+    const void *q_out,
+    int B, int T, int Hq, int Hkv, int d, int window, float scale,
+    orthros_dtype dtype,
+    const void *o_base, const float *lse_base, const void *o_out, const float *lse_out,
+    const void *do_base, const void *do_out,
+    void *dq, void *dk, void *dv, void *dq_out,
+    float *d_alpha_base, float *d_beta_base, float *d_alpha_out, float *d_beta_out,
+    void *workspace, size_t workspace_bytes, orthros_stream_t stream);
+
 /* Workspace bytes orthros_decode needs for these sizes (0 if rejected). */
 ORTHROS_API size_t orthros_decode_workspace_size(int B, int Hq, int Hkv, int d,
                                      int max_pages, int page_size,

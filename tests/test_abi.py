@@ -104,6 +104,47 @@ def test_decode_host_checks(lib):
     assert rc == 4  # no workspace
 
 
+def _call_backward(lib, **over):
+    P = 1 << 12
+    a = dict(q=P, k=P, v=P, ab=P, bb=P, ao=P, bo=P, indptr=(ctypes.c_int32 * 2)(0, 1), pos=P, n_out=1,
+             q_out=None, B=1, T=16, Hq=4, Hkv=2, d=128, window=8, scale=0.1, dtype=0,
+             o_base=P, lse_base=P, o_out=P, lse_out=P, do_base=P, do_out=P,
+             dq=P, dk=P, dv=P, dq_out=None, dab=P, dbb=P, dao=P, dbo=P, ws=P, ws_bytes=1 << 30, stream=None)
+    a.update(over)
+    return lib.orthros_prefill_backward(
+        a["q"], a["k"], a["v"], a["ab"], a["bb"], a["ao"], a["bo"], a["indptr"], a["pos"], a["n_out"], a["q_out"],
+        a["B"], a["T"], a["Hq"], a["Hkv"], a["d"], a["window"], a["scale"], a["dtype"],
+        a["o_base"], a["lse_base"], a["o_out"], a["lse_out"], a["do_base"], a["do_out"],
+        a["dq"], a["dk"], a["dv"], a["dq_out"], a["dab"], a["dbb"], a["dao"], a["dbo"],
+        a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(Hq=3), 1),
+    (dict(d=96), 2),
+    (dict(window=0), 1),
+    (dict(do_base=None), 1),
+    (dict(dk=None), 1),
+    (dict(dab=None), 1),
+    (dict(q_out=1 << 12), 1),  # q_out without dq_out
+    (dict(dq=(1 << 12) + 4), 1),  # misaligned
+    (dict(indptr=(ctypes.c_int32 * 2)(0, 2)), 1),
+    (dict(do_out=None), 1),
+    (dict(ws=None), 4),
+    (dict(ws_bytes=8), 4),
+    (dict(ws=(1 << 12) + 16), 1),
+])
+def test_backward_host_checks(lib, over, code):
+    assert _call_backward(lib, **over) == code
+    assert ola.orthros_last_error() != ""
+
+
+def test_backward_workspace_size(lib):
+    assert ola.orthros_prefill_backward_workspace_size(2, 64, 4, 2, 128, 10, 16) > 0
+    assert ola.orthros_prefill_backward_workspace_size(2, 64, 4, 2, 96, 10, 16) == 0
+    assert ola.orthros_prefill_backward_workspace_size(2, 64, 4, 2, 128, -1, 16) == 0
+
+
 def test_product_path_fails_loudly_without_library(tmp_path):
     with pytest.raises(ola.OrthrosError):
         ola.load_library(str(tmp_path / "missing.so"))
