@@ -1,4 +1,5 @@
-// backward_simt.cu -- gradients of the banded and cross rows on CUDA cores.
+// backward.cu -- gradients of the banded and cross rows: the CUDA-core path
+// and the pre/post passes of the tensor-core path (backward_tc.cu).
 //
 // The backward of Sec. 3.1 Eq. 4 (every position t over keys max(0,t-w+1)..t)
 // and Eq. 5 (every output row at position t_r over keys 0..t_r), both behind
@@ -12,7 +13,7 @@
 // dbeta += dqa. Output rows that read q at their own position (no separate
 // q_out) add their dq_raw into that position's dq.
 //
-// Layout of the work, any element type, fp32 arithmetic:
+// CUDA-core path (any element type, fp32 arithmetic):
 //   delta kernel  one warp per row: D = dO . o
 //   dk/dv kernel  one warp per (sequence, kv head, key): walks every query
 //                 row of the group's heads that sees the key, in both streams;
@@ -21,6 +22,10 @@
 //                 warps shares one head and reduces its affine gradients in
 //                 shared memory before one atomic add per channel
 // Lane l holds channels [l*E, l*E+E), E = d/32, of every row it touches.
+//
+// Tensor-core path (bf16, d = 128): the delta kernel also writes qa in bf16,
+// backward_tc.cu computes dk, dv and accumulates dqa in fp32, and the dq
+// kernel (FromAcc) applies the affine and reduces the affine gradients.
 #include "internal.cuh"
 
 namespace orthros {
@@ -77,7 +82,9 @@ __device__ __forceinline__ int seq_of_row(const int32_t *indptr, int B, int r) {
     return lo;
 }
 
-template <typename T, int D>
+// D = dO . o of every row; with WriteQa (bf16 tensor-core path) also the
+// affined query of the row, qa = alpha (.) q_raw + beta, rounded to bf16.
+template <typename T, int D, bool WriteQa>
 __global__ void __launch_bounds__(256) bwd_delta_kernel(BwdArgs a, long long n_base) {
     constexpr int E = D / 32;
     const int lane = threadIdx.x & 31;
@@ -93,13 +100,54 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(BwdArgs a, long long n_b
         ld<T, E>(static_cast<const T *>(a.do_base) + unit * D + lane * E, dO);
         const float s = wsum(dot<E>(o, dO));
         if (lane == 0) a.delta_base[((long long)b * a.Hq + h) * a.T + t] = s;
+        if constexpr (WriteQa) {
+            float q[E], al[E], be[E];
+            ld<T, E>(static_cast<const T *>(a.q) + unit * D + lane * E, q);
+            ld<float, E>(a.alpha_base + h * D + lane * E, al);
+            ld<float, E>(a.beta_base + h * D + lane * E, be);
+#pragma unroll
+            for (int e = 0; e < E; ++e) q[e] = fmaf(al[e], q[e], be[e]);
+            st<__nv_bfloat16, E>(a.qa_base + unit * D + lane * E, q);
+        }
     } else {
         const long long u = unit - n_base;  // (r, h)
         ld<T, E>(static_cast<const T *>(a.o_out) + u * D + lane * E, o);
         ld<T, E>(static_cast<const T *>(a.do_out) + u * D + lane * E, dO);
         const float s = wsum(dot<E>(o, dO));
         if (lane == 0) a.delta_out[u] = s;
+        if constexpr (WriteQa) {
+            const int h = (int)(u % a.Hq), r = (int)(u / a.Hq);
+            float q[E], al[E], be[E];
+#pragma unroll
+            for (int e = 0; e < E; ++e) q[e] = 0.f;
+            bool ok = true;
+            if (a.q_out) {
+                ld<T, E>(static_cast<const T *>(a.q_out) + u * D + lane * E, q);
+            } else {
+                const int b = seq_of_row(a.out_indptr, a.B, r);
+                const int t = a.out_positions[r];
+                ok = t >= 0 && t < a.T;  // bad positions are flagged (and masked) elsewhere
+                if (ok) ld<T, E>(static_cast<const T *>(a.q) + (((long long)b * a.T + t) * a.Hq + h) * D + lane * E, q);
+            }
+            ld<float, E>(a.alpha_out + h * D + lane * E, al);
+            ld<float, E>(a.beta_out + h * D + lane * E, be);
+#pragma unroll
+            for (int e = 0; e < E; ++e) q[e] = ok ? fmaf(al[e], q[e], be[e]) : 0.f;
+            st<__nv_bfloat16, E>(a.qa_out + u * D + lane * E, q);
+        }
     }
+}
+
+// omax[r] = largest position among output rows r .. r+63 of r's sequence: the
+// tensor-core kernel skips a 64-row tile whose largest position precedes its keys.
+__global__ void bwd_omax_kernel(BwdArgs a) {
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= a.n_out) return;
+    const int b = seq_of_row(a.out_indptr, a.B, r);
+    const int end = min(r + 64, a.out_indptr[b + 1]);
+    int m = -1;
+    for (int i = r; i < end; ++i) m = max(m, a.out_positions[i]);
+    a.omax[r] = m;
 }
 
 // Threads the output rows of each position into a list (positions may repeat):
@@ -187,7 +235,10 @@ __global__ void __launch_bounds__(256) bwd_dkdv_kernel(BwdArgs a) {
 }
 
 // kind 0: base rows, grid (ceil(T/8), Hq, B); kind 1: output rows, grid (ceil(n_out/8), Hq).
-template <typename T, int D>
+// FromAcc: dqa (scale included) was accumulated by the tensor-core kernel
+// (dq_acc for base rows, dq_rows for output rows); only the affine step and
+// the affine gradients remain.
+template <typename T, int D, bool FromAcc>
 __global__ void __launch_bounds__(256) bwd_dq_kernel(BwdArgs a, int kind) {
     constexpr int E = D / 32;
     __shared__ float red[2][kWarps][D];
@@ -224,7 +275,8 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(BwdArgs a, int kind) {
         }
     }
     if (active) {
-        float al[E], be[E], qa[E], dO[E], k[E], v[E];
+        float al[E], be[E];
+        [[maybe_unused]] float qa[E], dO[E], k[E], v[E];
         ld<float, E>(alpha + h * D + lane * E, al);
         ld<float, E>(beta + h * D + lane * E, be);
         const long long row = ((long long)b * a.T + t) * a.Hq + h;
@@ -232,6 +284,9 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(BwdArgs a, int kind) {
         const T *qp = (kind == 1 && a.q_out) ? static_cast<const T *>(a.q_out) + ro * D
                                              : static_cast<const T *>(a.q) + row * D;
         ld<T, E>(qp + lane * E, qraw);
+        if constexpr (FromAcc) {
+            ld<float, E>((kind == 0 ? a.dq_acc + row * D : a.dq_rows + ro * D) + lane * E, dqa);
+        } else {
 #pragma unroll
         for (int e = 0; e < E; ++e) qa[e] = fmaf(al[e], qraw[e], be[e]);
         float lse, delta;
@@ -258,12 +313,12 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(BwdArgs a, int kind) {
 #pragma unroll
             for (int e = 0; e < E; ++e) dqa[e] = fmaf(ds, k[e], dqa[e]);
         }
+#pragma unroll
+        for (int e = 0; e < E; ++e) dqa[e] *= a.scale;
+        }
         float dq[E];
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-            dqa[e] *= a.scale;
-            dq[e] = al[e] * dqa[e];
-        }
+        for (int e = 0; e < E; ++e) dq[e] = al[e] * dqa[e];
         if (kind == 0) {
             // output rows at this position that read this q add their share
             int rr = (a.q_out || a.n_out == 0) ? -1 : a.pos_head[(long long)b * a.T + t];
@@ -298,44 +353,75 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(BwdArgs a, int kind) {
     }
 }
 
-template <typename T, int D>
-cudaError_t launch_t(const BwdArgs &a, cudaStream_t stream, const char *const names[4]) {
+template <typename T, int D, bool Tc>
+cudaError_t launch_t(const BwdArgs &a, cudaStream_t stream) {
     const long long n_base = (long long)a.B * a.T * a.Hq;
     const long long n_rows = n_base + (long long)a.n_out * a.Hq;
+    cudaError_t e;
     {
-        ProfScope ps(names[0], stream);
+        ProfScope ps("bwd_prep", stream);
         if (a.n_out > 0) {
             bwd_row_lists_kernel<<<(a.n_out + 255) / 256, 256, 0, stream>>>(a);
+            if constexpr (Tc) bwd_omax_kernel<<<(a.n_out + 255) / 256, 256, 0, stream>>>(a);
         }
-        bwd_delta_kernel<T, D><<<(unsigned)((n_rows + kWarps - 1) / kWarps), kWarps * 32, 0, stream>>>(a, n_base);
-    }
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    {
-        ProfScope ps(names[1], stream);
-        const long long n = (long long)a.B * a.T * a.Hkv;
-        bwd_dkdv_kernel<T, D><<<(unsigned)((n + kWarps - 1) / kWarps), kWarps * 32, 0, stream>>>(a);
+        bwd_delta_kernel<T, D, Tc><<<(unsigned)((n_rows + kWarps - 1) / kWarps), kWarps * 32, 0, stream>>>(a, n_base);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if constexpr (Tc) {
+        if ((e = cudaMemsetAsync(a.dq_acc, 0, sizeof(float) * (size_t)n_base * D, stream)) != cudaSuccess) return e;
+        if (a.n_out > 0 &&
+            (e = cudaMemsetAsync(a.dq_rows, 0, sizeof(float) * (size_t)a.n_out * a.Hq * D, stream)) != cudaSuccess)
+            return e;
+        BwdTcParams tp{};
+        tp.out_indptr = a.out_indptr;
+        tp.out_positions = a.out_positions;
+        tp.omax = a.omax;
+        tp.lse_base = a.lse_base;
+        tp.lse_out = a.lse_out;
+        tp.delta_base = a.delta_base;
+        tp.delta_out = a.delta_out;
+        tp.dq_acc = a.dq_acc;
+        tp.dq_out_acc = a.dq_rows;
+        tp.dk = static_cast<__nv_bfloat16 *>(a.dk);
+        tp.dv = static_cast<__nv_bfloat16 *>(a.dv);
+        tp.B = a.B;
+        tp.T = a.T;
+        tp.Hq = a.Hq;
+        tp.Hkv = a.Hkv;
+        tp.window = a.window;
+        tp.n_out = a.n_out;
+        tp.nkb = (a.T + 127) / 128;
+        tp.scale = a.scale;
+        tp.scale_log2 = a.scale * 1.4426950408889634f;
+        tp.status = a.status;
+        ProfScope ps("bwd_tc", stream);
+        e = launch_backward_tc(tp, a.k, a.v, a.qa_base, a.do_base, a.qa_out, a.do_out, stream);
+    } else {
+        ProfScope ps("bwd_dkdv_simt", stream);
+        const long long n = (long long)a.B * a.T * a.Hkv;
+        bwd_dkdv_kernel<T, D><<<(unsigned)((n + kWarps - 1) / kWarps), kWarps * 32, 0, stream>>>(a);
+        e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) return e;
     if (a.n_out > 0) {
-        ProfScope ps(names[2], stream);
-        bwd_dq_kernel<T, D><<<dim3((a.n_out + kWarps - 1) / kWarps, a.Hq), kWarps * 32, 0, stream>>>(a, 1);
+        ProfScope ps(Tc ? "bwd_finish_out" : "bwd_dq_out_simt", stream);
+        bwd_dq_kernel<T, D, Tc><<<dim3((a.n_out + kWarps - 1) / kWarps, a.Hq), kWarps * 32, 0, stream>>>(a, 1);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     {
-        ProfScope ps(names[3], stream);
-        bwd_dq_kernel<T, D><<<dim3((a.T + kWarps - 1) / kWarps, a.Hq, a.B), kWarps * 32, 0, stream>>>(a, 0);
+        ProfScope ps(Tc ? "bwd_finish" : "bwd_dq_simt", stream);
+        bwd_dq_kernel<T, D, Tc><<<dim3((a.T + kWarps - 1) / kWarps, a.Hq, a.B), kWarps * 32, 0, stream>>>(a, 0);
     }
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_backward_simt(const BwdArgs &a, int d, orthros_dtype dtype, cudaStream_t stream) {
-    static const char *const names[4] = {"bwd_delta", "bwd_dkdv_simt", "bwd_dq_out_simt", "bwd_dq_simt"};
+cudaError_t launch_backward(const BwdArgs &a, int d, orthros_dtype dtype, bool use_tc, cudaStream_t stream) {
     if (dtype == ORTHROS_F32)
-        return d == 64 ? launch_t<float, 64>(a, stream, names) : launch_t<float, 128>(a, stream, names);
-    return d == 64 ? launch_t<__nv_bfloat16, 64>(a, stream, names) : launch_t<__nv_bfloat16, 128>(a, stream, names);
+        return d == 64 ? launch_t<float, 64, false>(a, stream) : launch_t<float, 128, false>(a, stream);
+    if (use_tc && d == 128) return launch_t<__nv_bfloat16, 128, true>(a, stream);
+    return d == 64 ? launch_t<__nv_bfloat16, 64, false>(a, stream) : launch_t<__nv_bfloat16, 128, false>(a, stream);
 }
 
 }  // namespace orthros

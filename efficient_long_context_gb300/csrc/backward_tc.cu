@@ -1,0 +1,468 @@
+// backward_tc.cu -- gradients of the banded and cross rows on the 5th-generation
+// tensor cores (tcgen05, TMEM, TMA); bf16, head size 128.
+//
+// What it computes: the chain rule through Sec. 3.1 Eq. 4 (base rows, keys
+// max(0, t-w+1) .. t) and Eq. 5 (output rows, keys 0 .. t_r). With the
+// forward's log-sum-exp L and D = dO . o of each row (prepared by a pre-pass
+// together with the affined queries qa = alpha (.) q + beta in bf16):
+//   P  = exp(scale * qa k^T - L)          dP = dO v^T
+//   dS = scale * P (.) (dP - D)
+//   dV = P^T dO     dK = dS^T qa     dQa = dS K
+// dV and dK are complete per key; dQa is reduced over key blocks in fp32.
+//
+// Design: one CTA per (sequence, kv head, block of 128 keys), 320 threads.
+//   It visits every 64-row query tile that sees its keys: for each query head
+//   of the GQA group, the base-stream tiles of the band [j0, j0 + 127 + w - 1]
+//   and the output-row tiles whose largest position reaches j0.
+//   Keys are the M dimension of every product, so dK and dV accumulate in
+//   TMEM over all tiles and are written once:
+//     S^T  = K qa^T   (M 128 keys, N 64 rows, K = d)        TMEM [0, 64)
+//     dP^T = V dO^T                                          TMEM [64, 128)
+//     dV  += P^T dO   (N = d, K = 64 rows; dO read MN-major) TMEM [128, 256)
+//     dK  += dS^T qa                                         TMEM [256, 384)
+//     dQ^T = K^T dS^T (M = d channels, N = 64 rows, both operands MN-major)
+//                                                            TMEM [384, 512), two buffers
+//   warp 8: TMA producer (K, V once; qa and dO tiles, 2 stages) and the
+//           per-tile row metadata (positions, L, D).
+//   warp 9: one thread issues the MMAs in the order S_i, dP_i, dV_{i-1},
+//           dK_{i-1}, dQ_{i-1}, so the tensor core works on tile i while the
+//           softmax warps turn tile i-1's scores into P and dS.
+//   warps 0-7: thread (lane quarter q, half h) owns key 32 q + lane and 32 of
+//           the 64 rows: P and dS in fp32, stored to shared memory as bf16
+//           (the layout is K-major for dV/dK and MN-major for dQ^T at once);
+//           then they drain dQ^T of the previous tile into the fp32
+//           accumulator with coalesced reductions, and at the end store dK, dV.
+#include <cuda.h>
+
+#include <algorithm>
+
+#include "ptx.cuh"
+
+namespace orthros {
+
+using namespace ptx;
+
+namespace {
+
+constexpr int kD = 128;
+constexpr int kKeys = 128;
+constexpr int kRows = 64;
+constexpr int kStages = 2;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
+constexpr int kSoftThreads = 256;
+
+constexpr int kBoxK = kKeys * 128;     // one 64-channel box of 128 keys: 16 KB
+constexpr int kBoxQ = kRows * 128;     // one 64-channel box of 64 rows: 8 KB
+constexpr int kKBytes = 2 * kBoxK;     // 32 KB
+constexpr int kQBytes = 2 * kBoxQ;     // 16 KB
+constexpr int kPBytes = kKeys * kRows * 2;  // 16 KB
+constexpr int kOffK = 0;
+constexpr int kOffV = kOffK + kKBytes;
+constexpr int kOffQ = kOffV + kKBytes;            // stage s: qa at +s*2*kQBytes, dO after it
+constexpr int kOffP = kOffQ + kStages * 2 * kQBytes;
+constexpr int kOffDS = kOffP + 2 * kPBytes;
+constexpr int kOffMeta = kOffDS + 2 * kPBytes;
+
+struct StageMeta {
+    int pos[kRows];      // row position, -1 for rows past the tile's end
+    float lse2[kRows];   // L * log2(e), +inf for rows past the end
+    float delta[kRows];  // D = dO . o
+};
+
+struct Meta {
+    uint64_t kv_full, q_full[kStages], q_empty[kStages];
+    uint64_t s_full, s_free, p_full[2], pds_free[2], dq_full[2], dq_free[2], mma_done;
+    uint32_t tmem_base;
+    int abort;
+    int n_tiles;
+    int pad;
+    StageMeta st[kStages];
+    int2 tiles[kBwdMaxTiles];  // x = 2 * head + kind (0 base, 1 output rows), y = first row
+};
+
+constexpr int kSmem = kOffMeta + (int)sizeof(Meta) + 1024;
+
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                   "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]),
+                   "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]),
+                   "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    backward_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_qb, const __grid_constant__ CUtensorMap tm_db,
+                       const __grid_constant__ CUtensorMap tm_qo, const __grid_constant__ CUtensorMap tm_do,
+                       const BwdTcParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Meta &mt = *reinterpret_cast<Meta *>(smem + kOffMeta);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    volatile int *abort = &mt.abort;
+
+    // unit: key block (slowest, so blocks with the most output rows start first), sequence, kv head
+    const int per_jb = p.B * p.Hkv;
+    const int jb = blockIdx.x / per_jb;
+    const int b = (blockIdx.x % per_jb) / p.Hkv;
+    const int kv = blockIdx.x % p.Hkv;
+    const int j0 = jb * kKeys;
+    const int g = p.Hq / p.Hkv;
+    const int r0b = p.n_out ? p.out_indptr[b] : 0;
+    const int r1b = p.n_out ? p.out_indptr[b + 1] : 0;
+
+    if (tid == 0) {
+        mbar_init(&mt.kv_full, 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&mt.q_full[s], 1);
+            mbar_init(&mt.q_empty[s], 1);
+        }
+        mbar_init(&mt.s_full, 1);
+        mbar_init(&mt.s_free, kSoftThreads);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&mt.p_full[s], kSoftThreads);
+            mbar_init(&mt.pds_free[s], 1);
+            mbar_init(&mt.dq_full[s], 1);
+            mbar_init(&mt.dq_free[s], kSoftThreads);
+        }
+        mbar_init(&mt.mma_done, 1);
+        mt.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        // Tile list: base-stream tiles of the band, then output-row tiles that
+        // reach this key block, for each query head of the group.
+        const long long t_hi_ll = min((long long)p.T - 1, (long long)j0 + kKeys - 1 + (long long)p.window - 1);
+        const int n_base = (int)((t_hi_ll - j0) / kRows) + 1;
+        int n = 0;
+        for (int hh = 0; hh < g; ++hh) {
+            const int h = kv * g + hh;
+            for (int i = lane; i < n_base; i += 32)
+                if (n + i < kBwdMaxTiles) mt.tiles[n + i] = make_int2(2 * h, j0 + i * kRows);
+            n += n_base;
+            for (int r0 = r0b; r0 < r1b; r0 += 32 * kRows) {
+                const int r = r0 + lane * kRows;
+                const bool take = r < r1b && p.omax[r] >= j0;
+                const unsigned m = __ballot_sync(0xffffffffu, take);
+                const int at = n + __popc(m & ((1u << lane) - 1u));
+                if (take && at < kBwdMaxTiles) mt.tiles[at] = make_int2(2 * h + 1, r);
+                n += __popc(m);
+            }
+        }
+        // the host launches this kernel only when bwd_tc_max_tiles_bound() fits
+        if (lane == 0) mt.n_tiles = min(n, kBwdMaxTiles);
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_qb);
+        prefetch_tmap(&tm_db);
+    }
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tmem_alloc(&mt.tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = mt.tmem_base;
+    const int n_tiles = mt.n_tiles;
+    const long long seq_tok = (long long)b * p.T;
+
+    if (warp == kProducerWarp) {
+        // ---------------- TMA producer + row metadata ----------------
+        int issued = 0;
+        if (lane == 0 && n_tiles > 0) {
+            mbar_arrive_expect_tx(&mt.kv_full, 2 * kKBytes);
+            for (int j = 0; j < 2; ++j) {
+                tma_load_3d(smem + kOffK + j * kBoxK, &tm_k, &mt.kv_full, 64 * j, kv, (int)(seq_tok + j0));
+                tma_load_3d(smem + kOffV + j * kBoxK, &tm_v, &mt.kv_full, 64 * j, kv, (int)(seq_tok + j0));
+            }
+        }
+        const float log2e = 1.4426950408889634f;
+        for (int i = 0; i < n_tiles; ++i) {
+            const int s = i % kStages;
+            if (i >= kStages) {
+                const bool ok = mbar_wait(&mt.q_empty[s], ((i / kStages) - 1) & 1, abort, p.status);
+                if (!__all_sync(0xffffffffu, ok)) break;
+            }
+            const int2 tl = mt.tiles[i];
+            const int h = tl.x >> 1, kind = tl.x & 1, row0 = tl.y;
+            StageMeta &sm = mt.st[s];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int c = lane + 32 * u;
+                int pos = -1;
+                float l2 = INFINITY, dl = 0.f;
+                if (kind == 0) {
+                    const int t = row0 + c;
+                    if (t < p.T) {
+                        const long long idx = ((long long)b * p.Hq + h) * p.T + t;
+                        pos = t;
+                        l2 = p.lse_base[idx] * log2e;
+                        dl = p.delta_base[idx];
+                    }
+                } else {
+                    const int r = row0 + c;
+                    if (r < r1b) {
+                        const int t = p.out_positions[r];
+                        if (t >= 0 && t < p.T) {
+                            const long long idx = (long long)r * p.Hq + h;
+                            pos = t;
+                            l2 = p.lse_out[idx] * log2e;
+                            dl = p.delta_out[idx];
+                        }
+                    }
+                }
+                sm.pos[c] = pos;
+                sm.lse2[c] = l2;
+                sm.delta[c] = dl;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                uint8_t *qa = smem + kOffQ + s * 2 * kQBytes;
+                uint8_t *dO = qa + kQBytes;
+                mbar_arrive_expect_tx(&mt.q_full[s], 2 * kQBytes);
+                const int row_tok = kind == 0 ? (int)(seq_tok + row0) : row0;
+                const CUtensorMap *mq = kind == 0 ? &tm_qb : &tm_qo;
+                const CUtensorMap *md = kind == 0 ? &tm_db : &tm_do;
+                for (int j = 0; j < 2; ++j) {
+                    tma_load_3d(qa + j * kBoxQ, mq, &mt.q_full[s], 64 * j, h, row_tok);
+                    tma_load_3d(dO + j * kBoxQ, md, &mt.q_full[s], 64 * j, h, row_tok);
+                }
+            }
+            issued = i + 1;
+        }
+        // nothing may land in shared memory after the CTA exits
+        if (lane == 0) {
+            if (n_tiles > 0) mbar_wait_drain(&mt.kv_full, 0, p.status);
+            for (int i = max(0, issued - kStages); i < issued; ++i)
+                mbar_wait_drain(&mt.q_full[i % kStages], (i / kStages) & 1, p.status);
+        }
+    } else if (warp == kMmaWarp) {
+        // ---------------- tcgen05.mma issuer ----------------
+        if (lane == 0 && n_tiles > 0) {
+            constexpr uint32_t kIdS = idesc_f16(1, 1, 0, 0, kKeys, kRows);   // S^T, dP^T
+            constexpr uint32_t kIdKV = idesc_f16(1, 1, 0, 1, kKeys, kD);     // dV, dK: B MN-major
+            constexpr uint32_t kIdQ = idesc_f16(1, 1, 1, 1, kD, kRows);      // dQ^T: A and B MN-major
+            // start-address field is (byte address >> 4); all operands lie below
+            // 256 KB, so adding (offset >> 4) never carries out of the field
+            const uint64_t d_k = desc_sw128(smem_u32(smem + kOffK), 16, 1024);          // K-major
+            const uint64_t d_v = desc_sw128(smem_u32(smem + kOffV), 16, 1024);
+            const uint64_t d_kmn = desc_sw128(smem_u32(smem + kOffK), kBoxK, 1024);     // K as MN-major A
+            const uint64_t d_q0 = desc_sw128(smem_u32(smem + kOffQ), 16, 1024);         // qa stage 0, K-major
+            const uint64_t d_qmn0 = desc_sw128(smem_u32(smem + kOffQ), kBoxQ, 1024);    // qa stage 0, MN-major
+            const uint64_t d_p0 = desc_sw128(smem_u32(smem + kOffP), 16, 1024);
+            const uint64_t d_ds0 = desc_sw128(smem_u32(smem + kOffDS), 16, 1024);
+            const uint64_t d_dsmn0 = desc_sw128(smem_u32(smem + kOffDS), kBoxQ, 1024);
+            constexpr uint32_t kStageU = (2 * kQBytes) >> 4, kQU = kQBytes >> 4, kPU = kPBytes >> 4;
+            bool ok = mbar_wait(&mt.kv_full, 0, abort, p.status);
+            for (int i = 0; ok && i <= n_tiles; ++i) {
+                if (i < n_tiles) {
+                    const int s = i % kStages;
+                    if (!(ok = mbar_wait(&mt.q_full[s], (i / kStages) & 1, abort, p.status))) break;
+                    if (i >= 1 && !(ok = mbar_wait(&mt.s_free, (i - 1) & 1, abort, p.status))) break;
+                    tc_fence_after();
+                    const uint64_t dq = d_q0 + s * kStageU, ddo = dq + kQU;
+#pragma unroll
+                    for (int ks = 0; ks < kD / 16; ++ks) {
+                        const uint32_t ok_ = ((ks >> 2) * kBoxK + (ks & 3) * 32) >> 4;
+                        const uint32_t oq = ((ks >> 2) * kBoxQ + (ks & 3) * 32) >> 4;
+                        mma_ss(tmem, d_k + ok_, dq + oq, kIdS, ks > 0);
+                    }
+#pragma unroll
+                    for (int ks = 0; ks < kD / 16; ++ks) {
+                        const uint32_t ok_ = ((ks >> 2) * kBoxK + (ks & 3) * 32) >> 4;
+                        const uint32_t oq = ((ks >> 2) * kBoxQ + (ks & 3) * 32) >> 4;
+                        mma_ss(tmem + 64, d_v + ok_, ddo + oq, kIdS, ks > 0);
+                    }
+                    tc_commit(&mt.s_full);
+                }
+                if (i >= 1) {
+                    const int pi = i - 1, ps = pi % 2, qs = pi % kStages;
+                    if (!(ok = mbar_wait(&mt.p_full[ps], (pi / 2) & 1, abort, p.status))) break;
+                    tc_fence_after();
+                    const uint64_t dqmn = d_qmn0 + qs * kStageU, ddomn = dqmn + kQU;
+                    const uint64_t dp = d_p0 + ps * kPU, dds = d_ds0 + ps * kPU, ddsmn = d_dsmn0 + ps * kPU;
+#pragma unroll
+                    for (int kk = 0; kk < kRows / 16; ++kk)
+                        mma_ss(tmem + 128, dp + ((kk * 32) >> 4), ddomn + ((kk * 16 * 128) >> 4), kIdKV,
+                               (pi > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 0; kk < kRows / 16; ++kk)
+                        mma_ss(tmem + 256, dds + ((kk * 32) >> 4), dqmn + ((kk * 16 * 128) >> 4), kIdKV,
+                               (pi > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit(&mt.q_empty[qs]);
+                    if (pi >= 2 && !(ok = mbar_wait(&mt.dq_free[ps], ((pi / 2) - 1) & 1, abort, p.status))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < kKeys / 16; ++kk)
+                        mma_ss(tmem + 384 + 64 * ps, d_kmn + ((kk * 16 * 128) >> 4), ddsmn + ((kk * 16 * 128) >> 4),
+                               kIdQ, kk > 0);
+                    tc_commit(&mt.dq_full[ps]);
+                    tc_commit(&mt.pds_free[ps]);
+                }
+            }
+            tc_commit(&mt.mma_done);
+            mbar_wait_drain(&mt.mma_done, 0, p.status);
+        }
+    } else {
+        // ---------------- P, dS; dQ drain; dK, dV store ----------------
+        const int qd = warp & 3, hh = warp >> 2;
+        const int key = qd * 32 + lane;  // TMEM lane of this thread
+        const int j = j0 + key;
+        const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
+        const float c2 = p.scale_log2;
+        auto drain = [&](int pi) -> bool {
+            const int ps = pi % 2;
+            const bool got = mbar_wait(&mt.dq_full[ps], (pi / 2) & 1, abort, p.status);
+            if (!__all_sync(0xffffffffu, got)) return false;
+            tc_fence_after();
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_off + 384 + 64 * ps + 32 * hh, v);
+            tmem_ld_wait();
+            reg_fence(v);
+            tc_fence_before();
+            mbar_arrive(&mt.dq_free[ps]);
+            const int2 tl = mt.tiles[pi];
+            const int h = tl.x >> 1, kind = tl.x & 1, row0 = tl.y;
+            const int ch = key;  // dQ^T lanes are channels
+#pragma unroll 8
+            for (int e = 0; e < 32; ++e) {
+                const int col = 32 * hh + e;
+                if (kind == 0) {
+                    const int t = row0 + col;
+                    if (t < p.T) red_add_f32(p.dq_acc + ((seq_tok + t) * p.Hq + h) * kD + ch, __uint_as_float(v[e]));
+                } else {
+                    const int r = row0 + col;
+                    if (r < r1b) red_add_f32(p.dq_out_acc + ((long long)r * p.Hq + h) * kD + ch, __uint_as_float(v[e]));
+                }
+            }
+            return true;
+        };
+        bool ok = true;
+        for (int i = 0; i < n_tiles; ++i) {
+            const int s = i % kStages, ps = i % 2;
+            const bool got = mbar_wait(&mt.s_full, i & 1, abort, p.status);
+            if (!(ok = __all_sync(0xffffffffu, got))) break;
+            tc_fence_after();
+            uint32_t sv[32], dv[32];
+            tmem_ld32(tmem + lane_off + 32 * hh, sv);
+            tmem_ld32(tmem + lane_off + 64 + 32 * hh, dv);
+            tmem_ld_wait();
+            reg_fence(sv);
+            reg_fence(dv);
+            tc_fence_before();
+            mbar_arrive(&mt.s_free);
+            // the row metadata was written by the producer's threads before q_full
+            const bool meta = mbar_wait(&mt.q_full[s], (i / kStages) & 1, abort, p.status);
+            if (!(ok = __all_sync(0xffffffffu, meta))) break;
+            const int kind = mt.tiles[i].x & 1;
+            const StageMeta &sm = mt.st[s];
+            uint32_t pk[16], dk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                float pv[2], dsv[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int col = 32 * hh + 2 * e + u;
+                    const int t = sm.pos[col];
+                    const bool valid = t >= j && (kind == 1 || t - j < p.window);
+                    const float pr = ex2(fmaf(__uint_as_float(sv[2 * e + u]), c2, -sm.lse2[col]));
+                    const float pp = valid ? pr : 0.f;
+                    pv[u] = pp;
+                    dsv[u] = valid ? pp * (__uint_as_float(dv[2 * e + u]) - sm.delta[col]) * p.scale : 0.f;
+                }
+                pk[e] = pack_bf16(pv[0], pv[1]);
+                dk[e] = pack_bf16(dsv[0], dsv[1]);
+            }
+            if (i >= 2) {
+                const bool free_ = mbar_wait(&mt.pds_free[ps], ((i / 2) - 1) & 1, abort, p.status);
+                if (!(ok = __all_sync(0xffffffffu, free_))) break;
+            }
+            uint8_t *pb = smem + kOffP + ps * kPBytes + key * 128;
+            uint8_t *db = smem + kOffDS + ps * kPBytes + key * 128;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int phys = ((4 * hh + q) ^ (key & 7)) << 4;
+                *reinterpret_cast<uint4 *>(pb + phys) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                *reinterpret_cast<uint4 *>(db + phys) = make_uint4(dk[4 * q], dk[4 * q + 1], dk[4 * q + 2], dk[4 * q + 3]);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&mt.p_full[ps]);
+            if (i >= 1 && !(ok = drain(i - 1))) break;
+        }
+        if (ok && n_tiles > 0) ok = drain(n_tiles - 1);
+        // dK, dV of this thread's key: columns [64 hh, 64 hh + 64) of each
+        const bool done = n_tiles > 0 && ok && mbar_wait(&mt.mma_done, 0, abort, p.status);
+        if (__all_sync(0xffffffffu, done)) {
+            tc_fence_after();
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                __nv_bfloat16 *dst = (which ? p.dk : p.dv) + ((seq_tok + j) * p.Hkv + kv) * kD + 64 * hh;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + lane_off + 128 + 128 * which + 64 * hh + 32 * half, v);
+                    tmem_ld_wait();
+                    reg_fence(v);
+                    if (j < p.T) {
+                        uint4 w[4];
+                        uint32_t *wp = reinterpret_cast<uint32_t *>(w);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            wp[e] = pack_bf16(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) reinterpret_cast<uint4 *>(dst + 32 * half)[e] = w[e];
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace
+
+int bwd_tc_max_tiles_bound(int T, int window, int g, int max_rows_per_seq) {
+    const long long span = std::min<long long>((long long)T, (long long)kKeys + window - 1);
+    const long long n_base = (span - 1) / kRows + 1;
+    const long long n_out = ((long long)max_rows_per_seq + kRows - 1) / kRows;
+    const long long n = (long long)g * (n_base + n_out);
+    return n > (1LL << 30) ? (1 << 30) : (int)n;
+}
+
+cudaError_t launch_backward_tc(const BwdTcParams &p, const void *k, const void *v, const void *qa_base,
+                               const void *do_base, const void *qa_out, const void *do_out, cudaStream_t stream) {
+    const long long tokens = (long long)p.B * p.T;
+    CUtensorMap tk, tv, tqb, tdb, tqo, tdo;
+    const long long n_out_rows = p.n_out > 0 ? p.n_out : 1;
+    if (!encode_kv_map_3d(&tk, k, tokens, p.Hkv, kD, kKeys) || !encode_kv_map_3d(&tv, v, tokens, p.Hkv, kD, kKeys) ||
+        !encode_kv_map_3d(&tqb, qa_base, tokens, p.Hq, kD, kRows) ||
+        !encode_kv_map_3d(&tdb, do_base, tokens, p.Hq, kD, kRows) ||
+        !encode_kv_map_3d(&tqo, p.n_out > 0 ? qa_out : qa_base, n_out_rows, p.Hq, kD, kRows) ||
+        !encode_kv_map_3d(&tdo, p.n_out > 0 ? do_out : do_base, n_out_rows, p.Hq, kD, kRows))
+        return cudaErrorInvalidValue;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(backward_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const long long units = (long long)p.nkb * p.B * p.Hkv;
+    if (units == 0) return cudaSuccess;
+    backward_tc_kernel<<<(unsigned)units, kThreads, kSmem, stream>>>(tk, tv, tqb, tdb, tqo, tdo, p);
+    return cudaGetLastError();
+}
+
+}  // namespace orthros

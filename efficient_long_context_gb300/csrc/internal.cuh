@@ -147,12 +147,36 @@ struct BwdArgs {
     const float *lse_base, *lse_out;
     float *delta_base;  // [B,Hq,T]  dO . o of every base row
     float *delta_out;   // [n_out,Hq]
-    float *dq_rows;     // [n_out,Hq,d] fp32 dq of output rows that read q (q_out == nullptr)
+    float *dq_rows;     // [n_out,Hq,d] fp32 dq of output rows that read q (q_out == nullptr);
+                        // the tensor-core path first accumulates the rows' dqa here
     void *dq, *dk, *dv, *dq_out;
     float *d_alpha_base, *d_beta_base, *d_alpha_out, *d_beta_out;  // zeroed by the caller
     uint32_t *status;
+    // tensor-core path only (bf16, d = 128); nullptr otherwise
+    __nv_bfloat16 *qa_base;  // [B,T,Hq,d] affined base queries
+    __nv_bfloat16 *qa_out;   // [n_out,Hq,d] affined output-row queries
+    float *dq_acc;           // [B,T,Hq,d] fp32 dqa of base rows
+    int32_t *omax;           // [n_out]: largest position among rows r .. r+63 of r's sequence
 };
-cudaError_t launch_backward_simt(const BwdArgs &a, int d, orthros_dtype dtype, cudaStream_t stream);
+// Runs the whole backward; use_tc selects the tensor-core kernel (bf16, d = 128,
+// with the workspace regions above) for the dk/dv/dqa products.
+cudaError_t launch_backward(const BwdArgs &a, int d, orthros_dtype dtype, bool use_tc, cudaStream_t stream);
+
+// backward_tc.cu
+constexpr int kBwdMaxTiles = 1024;  // query tiles one key block may visit
+struct BwdTcParams {
+    const int32_t *out_indptr, *out_positions, *omax;
+    const float *lse_base, *lse_out, *delta_base, *delta_out;
+    float *dq_acc, *dq_out_acc;
+    __nv_bfloat16 *dk, *dv;
+    int B, T, Hq, Hkv, window, n_out, nkb;
+    float scale, scale_log2;
+    uint32_t *status;
+};
+// Upper bound on the query tiles of one key block (must not exceed kBwdMaxTiles).
+int bwd_tc_max_tiles_bound(int T, int window, int g, int max_rows_per_seq);
+cudaError_t launch_backward_tc(const BwdTcParams &p, const void *k, const void *v, const void *qa_base,
+                               const void *do_base, const void *qa_out, const void *do_out, cudaStream_t stream);
 
 // cache.cu
 cudaError_t launch_decode_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache,

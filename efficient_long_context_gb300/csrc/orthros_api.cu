@@ -82,10 +82,13 @@ DecodeLayout decode_layout(int B, int Hkv, int d, int max_pages, int page_size, 
 
 // Workspace regions of orthros_prefill_backward.
 struct BackwardLayout {
-    size_t indptr_off, head_off, next_off, delta_base_off, delta_out_off, dq_rows_off, total;
+    size_t indptr_off, head_off, next_off, delta_base_off, delta_out_off, dq_rows_off;
+    size_t qa_base_off, qa_out_off, dq_acc_off, omax_off, total;
 };
 
-BackwardLayout backward_layout(int B, int T, int Hq, int d, int n_out) {
+// The tensor-core backward (bf16, d = 128) also needs bf16 affined queries,
+// an fp32 dqa accumulator for the base rows and the output tiles' largest positions.
+BackwardLayout backward_layout(int B, int T, int Hq, int d, int n_out, orthros_dtype dtype) {
     BackwardLayout L{};
     size_t at = kStatusBytes;
     L.indptr_off = at;
@@ -100,6 +103,15 @@ BackwardLayout backward_layout(int B, int T, int Hq, int d, int n_out) {
     at += align_up(sizeof(float) * (size_t)n_out * Hq, 256);
     L.dq_rows_off = at;
     at += align_up(sizeof(float) * (size_t)n_out * Hq * d, 256);
+    const bool tc = dtype == ORTHROS_BF16 && d == 128;
+    L.qa_base_off = at;
+    if (tc) at += align_up((size_t)2 * B * T * Hq * d, 256);
+    L.qa_out_off = at;
+    if (tc) at += align_up((size_t)2 * n_out * Hq * d, 256);
+    L.dq_acc_off = at;
+    if (tc) at += align_up(sizeof(float) * (size_t)B * T * Hq * d, 256);
+    L.omax_off = at;
+    if (tc) at += align_up(sizeof(int32_t) * (size_t)n_out, 256);
     L.total = at;
     return L;
 }
@@ -386,7 +398,7 @@ size_t orthros_prefill_backward_workspace_size(int B, int T, int Hq, int Hkv, in
                                                orthros_dtype dtype) {
     if (T < 0 || n_out < 0) return 0;
     if (check_shapes(B, Hq, Hkv, d, window, 1.0f, dtype) != ORTHROS_OK) return 0;
-    return backward_layout(B, T, Hq, d, n_out).total;
+    return backward_layout(B, T, Hq, d, n_out, dtype).total;
 }
 
 orthros_status orthros_prefill_backward(const void *q, const void *k, const void *v, const float *alpha_base,
@@ -441,7 +453,7 @@ orthros_status orthros_prefill_backward(const void *q, const void *k, const void
             !aligned16(alpha_out) || !aligned16(beta_out))
             return fail(ORTHROS_EINVAL, "output-row tensors and affines must be 16-byte aligned");
     }
-    const BackwardLayout lay = backward_layout(B, T, Hq, d, n_out);
+    const BackwardLayout lay = backward_layout(B, T, Hq, d, n_out, dtype);
     if (!workspace || workspace_bytes < lay.total)
         return fail(ORTHROS_EWORKSPACE, "workspace needs %zu bytes, got %zu", lay.total,
                     workspace ? workspace_bytes : (size_t)0);
@@ -503,7 +515,19 @@ orthros_status orthros_prefill_backward(const void *q, const void *k, const void
     a.d_alpha_out = d_alpha_out;
     a.d_beta_out = d_beta_out;
     a.status = status;
-    e = launch_backward_simt(a, d, dtype, stream);
+    bool use_tc = dtype == ORTHROS_BF16 && d == 128;
+    if (use_tc) {
+        int max_rows = 0;
+        for (int b = 0; b < B && n_out > 0; ++b) max_rows = std::max(max_rows, out_indptr[b + 1] - out_indptr[b]);
+        use_tc = bwd_tc_max_tiles_bound(T, window, Hq / Hkv, max_rows) <= kBwdMaxTiles;
+    }
+    if (use_tc) {
+        a.qa_base = reinterpret_cast<__nv_bfloat16 *>(ws + lay.qa_base_off);
+        a.qa_out = reinterpret_cast<__nv_bfloat16 *>(ws + lay.qa_out_off);
+        a.dq_acc = reinterpret_cast<float *>(ws + lay.dq_acc_off);
+        a.omax = reinterpret_cast<int32_t *>(ws + lay.omax_off);
+    }
+    e = launch_backward(a, d, dtype, use_tc, stream);
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
     return ORTHROS_OK;
 }

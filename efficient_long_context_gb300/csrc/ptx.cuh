@@ -71,6 +71,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     }
 }
 
+// Bounded wait that ignores the abort flag: used while draining (waiting for
+// copies or MMAs this thread already issued) so that nothing is left in flight
+// when the CTA releases its shared and tensor memory.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity, uint32_t *status) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > kWaitLimitCycles) {
+            set_status(status, ORTHROS_DEV_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
 // ----------------------------------------------------------------------------
 // proxy fences
 // ----------------------------------------------------------------------------
@@ -227,6 +241,11 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// fp32 reduction into global memory (no return value).
+__device__ __forceinline__ void red_add_f32(float *addr, float v) {
+    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+}
 
 // ----------------------------------------------------------------------------
 // math
