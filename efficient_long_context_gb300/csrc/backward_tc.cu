@@ -187,8 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < n_tiles; ++i) {
             const int s = i % kStages;
             if (i >= kStages) {
-                const bool ok = mbar_wait(&mt.q_empty[s], ((i / kStages) - 1) & 1, abort, p.status);
-                if (!__all_sync(0xffffffffu, ok)) break;
+                if (!mbar_wait_warp(&mt.q_empty[s], ((i / kStages) - 1) & 1, abort, p.status)) break;
             }
             const int2 tl = mt.tiles[i];
             const int h = tl.x >> 1, kind = tl.x & 1, row0 = tl.y;
@@ -319,8 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float c2 = p.scale_log2;
         auto drain = [&](int pi) -> bool {
             const int ps = pi % 2;
-            const bool got = mbar_wait(&mt.dq_full[ps], (pi / 2) & 1, abort, p.status);
-            if (!__all_sync(0xffffffffu, got)) return false;
+            if (!mbar_wait_warp(&mt.dq_full[ps], (pi / 2) & 1, abort, p.status)) return false;
             tc_fence_after();
             uint32_t v[32];
             tmem_ld32(tmem + lane_off + 384 + 64 * ps + 32 * hh, v);
@@ -331,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int2 tl = mt.tiles[pi];
             const int h = tl.x >> 1, kind = tl.x & 1, row0 = tl.y;
             const int ch = key;  // dQ^T lanes are channels
-#pragma unroll 8
+#pragma unroll
             for (int e = 0; e < 32; ++e) {
                 const int col = 32 * hh + e;
                 if (kind == 0) {
@@ -347,8 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int i = 0; i < n_tiles; ++i) {
             const int s = i % kStages, ps = i % 2;
-            const bool got = mbar_wait(&mt.s_full, i & 1, abort, p.status);
-            if (!(ok = __all_sync(0xffffffffu, got))) break;
+            if (!(ok = mbar_wait_warp(&mt.s_full, i & 1, abort, p.status))) break;
             tc_fence_after();
             uint32_t sv[32], dv[32];
             tmem_ld32(tmem + lane_off + 32 * hh, sv);
@@ -359,8 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(&mt.s_free);
             // the row metadata was written by the producer's threads before q_full
-            const bool meta = mbar_wait(&mt.q_full[s], (i / kStages) & 1, abort, p.status);
-            if (!(ok = __all_sync(0xffffffffu, meta))) break;
+            if (!(ok = mbar_wait_warp(&mt.q_full[s], (i / kStages) & 1, abort, p.status))) break;
             const int kind = mt.tiles[i].x & 1;
             const StageMeta &sm = mt.st[s];
             uint32_t pk[16], dk[16];
@@ -381,8 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 dk[e] = pack_bf16(dsv[0], dsv[1]);
             }
             if (i >= 2) {
-                const bool free_ = mbar_wait(&mt.pds_free[ps], ((i / 2) - 1) & 1, abort, p.status);
-                if (!(ok = __all_sync(0xffffffffu, free_))) break;
+                if (!(ok = mbar_wait_warp(&mt.pds_free[ps], ((i / 2) - 1) & 1, abort, p.status))) break;
             }
             uint8_t *pb = smem + kOffP + ps * kPBytes + key * 128;
             uint8_t *db = smem + kOffDS + ps * kPBytes + key * 128;
@@ -398,8 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok && n_tiles > 0) ok = drain(n_tiles - 1);
         // dK, dV of this thread's key: columns [64 hh, 64 hh + 64) of each
-        const bool done = n_tiles > 0 && ok && mbar_wait(&mt.mma_done, 0, abort, p.status);
-        if (__all_sync(0xffffffffu, done)) {
+        const bool done = n_tiles > 0 && ok && mbar_wait_warp(&mt.mma_done, 0, abort, p.status);
+        if (done) {
             tc_fence_after();
 #pragma unroll
             for (int which = 0; which < 2; ++which) {

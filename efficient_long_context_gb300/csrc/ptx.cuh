@@ -71,6 +71,28 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     }
 }
 
+// Warp-converged form of mbar_wait for waits that every lane of a warp makes:
+// all lanes poll together and leave together, so the warp never splits into
+// lanes that were woken and lanes still suspended in try_wait (a split warp
+// reconverges only when the slowest lane's wait returns). Returns the same
+// value in every lane.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                               uint32_t *status) {
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+        if (__any_sync(0xffffffffu, *abort != 0)) return false;
+        if (__any_sync(0xffffffffu, clock64() - t0 > kWaitLimitCycles)) {
+            if ((threadIdx.x & 31) == 0) {
+                *abort = 1;
+                set_status(status, ORTHROS_DEV_TIMEOUT);
+            }
+            return false;
+        }
+    }
+}
+
 // Bounded wait that ignores the abort flag: used while draining (waiting for
 // copies or MMAs this thread already issued) so that nothing is left in flight
 // when the CTA releases its shared and tensor memory.
