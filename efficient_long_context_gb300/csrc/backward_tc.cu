@@ -18,20 +18,22 @@
 //   TMEM over all tiles and are written once:
 //     S^T  = K qa^T   (M 128 keys, N 64 rows, K = d)        TMEM [0, 64)
 //     dP^T = V dO^T                                          TMEM [64, 128)
-//     dV  += P^T dO   (N = d, K = 64 rows; dO read MN-major) TMEM [128, 256)
-//     dK  += dS^T qa                                         TMEM [256, 384)
+//     dV  += P^T dO   (P^T from TMEM; dO read MN-major)      TMEM [128, 256)
+//     dK  += dS^T qa  (dS^T from shared memory)              TMEM [256, 384)
 //     dQ^T = K^T dS^T (M = d channels, N = 64 rows, both operands MN-major)
-//                                                            TMEM [384, 512), two buffers
-//   warp 8: TMA producer (K, V once; qa and dO tiles, 2 stages) and the
-//           per-tile row metadata (positions, L, D).
+//                                                            TMEM [384, 448)
+//     P^T as packed bf16, two buffers                        TMEM [448, 512)
+//   warp 8: TMA producer (K, V once; qa and dO tiles, 3 stages) and the
+//           per-tile row metadata (positions, L, D), loaded while the tiles fly.
 //   warp 9: one thread issues the MMAs in the order S_i, dP_i, dV_{i-1},
 //           dK_{i-1}, dQ_{i-1}, so the tensor core works on tile i while the
 //           softmax warps turn tile i-1's scores into P and dS.
 //   warps 0-7: thread (lane quarter q, half h) owns key 32 q + lane and 32 of
-//           the 64 rows: P and dS in fp32, stored to shared memory as bf16
-//           (the layout is K-major for dV/dK and MN-major for dQ^T at once);
-//           then they drain dQ^T of the previous tile into the fp32
-//           accumulator with coalesced reductions, and at the end store dK, dV.
+//           the 64 rows: P and dS in fp32; P^T back to TMEM as bf16, dS^T to
+//           shared memory as bf16 in a swizzled layout that is K-major for
+//           dK and MN-major for dQ^T at once; then they drain dQ^T of the
+//           previous tile into the fp32 accumulator with coalesced
+//           reductions, and at the end store dK and dV.
 #include <cuda.h>
 
 #include <algorithm>
@@ -47,7 +49,7 @@ namespace {
 constexpr int kD = 128;
 constexpr int kKeys = 128;
 constexpr int kRows = 64;
-constexpr int kStages = 2;
+constexpr int kStages = 3;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kThreads = 320;
@@ -57,23 +59,24 @@ constexpr int kBoxK = kKeys * 128;     // one 64-channel box of 128 keys: 16 KB
 constexpr int kBoxQ = kRows * 128;     // one 64-channel box of 64 rows: 8 KB
 constexpr int kKBytes = 2 * kBoxK;     // 32 KB
 constexpr int kQBytes = 2 * kBoxQ;     // 16 KB
-constexpr int kPBytes = kKeys * kRows * 2;  // 16 KB
+constexpr int kDSBytes = kKeys * kRows * 2;  // 16 KB
 constexpr int kOffK = 0;
 constexpr int kOffV = kOffK + kKBytes;
 constexpr int kOffQ = kOffV + kKBytes;            // stage s: qa at +s*2*kQBytes, dO after it
-constexpr int kOffP = kOffQ + kStages * 2 * kQBytes;
-constexpr int kOffDS = kOffP + 2 * kPBytes;
-constexpr int kOffMeta = kOffDS + 2 * kPBytes;
+constexpr int kOffDS = kOffQ + kStages * 2 * kQBytes;
+constexpr int kOffMeta = kOffDS + 2 * kDSBytes;
+// TMEM columns
+constexpr uint32_t kTS = 0, kTdP = 64, kTdV = 128, kTdK = 256, kTdQ = 384, kTP = 448;
 
 struct StageMeta {
     int pos[kRows];      // row position, -1 for rows past the tile's end
     float lse2[kRows];   // L * log2(e), +inf for rows past the end
-    float delta[kRows];  // D = dO . o
+    float ndelta[kRows]; // -D * scale, D = dO . o
 };
 
 struct Meta {
     uint64_t kv_full, q_full[kStages], q_empty[kStages];
-    uint64_t s_full, s_free, p_full[2], pds_free[2], dq_full[2], dq_free[2], mma_done;
+    uint64_t s_full, s_free, p_full[2], pds_free[2], dq_full, dq_free, mma_done;
     uint32_t tmem_base;
     int abort;
     int n_tiles;
@@ -125,9 +128,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < 2; ++s) {
             mbar_init(&mt.p_full[s], kSoftThreads);
             mbar_init(&mt.pds_free[s], 1);
-            mbar_init(&mt.dq_full[s], 1);
-            mbar_init(&mt.dq_free[s], kSoftThreads);
         }
+        mbar_init(&mt.dq_full, 1);
+        mbar_init(&mt.dq_free, kSoftThreads);
         mbar_init(&mt.mma_done, 1);
         mt.abort = 0;
         fence_mbar_init();
@@ -191,6 +194,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int2 tl = mt.tiles[i];
             const int h = tl.x >> 1, kind = tl.x & 1, row0 = tl.y;
+            if (lane == 0) {
+                uint8_t *qa = smem + kOffQ + s * 2 * kQBytes;
+                uint8_t *dO = qa + kQBytes;
+                mbar_expect_tx(&mt.q_full[s], 2 * kQBytes);
+                const int row_tok = kind == 0 ? (int)(seq_tok + row0) : row0;
+                const CUtensorMap *mq = kind == 0 ? &tm_qb : &tm_qo;
+                const CUtensorMap *md = kind == 0 ? &tm_db : &tm_do;
+                for (int j = 0; j < 2; ++j) {
+                    tma_load_3d(qa + j * kBoxQ, mq, &mt.q_full[s], 64 * j, h, row_tok);
+                    tma_load_3d(dO + j * kBoxQ, md, &mt.q_full[s], 64 * j, h, row_tok);
+                }
+            }
+            // row metadata while the tiles are in flight; the arrive publishes it
             StageMeta &sm = mt.st[s];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
@@ -219,21 +235,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 sm.pos[c] = pos;
                 sm.lse2[c] = l2;
-                sm.delta[c] = dl;
+                sm.ndelta[c] = -dl * p.scale;
             }
             __syncwarp();
-            if (lane == 0) {
-                uint8_t *qa = smem + kOffQ + s * 2 * kQBytes;
-                uint8_t *dO = qa + kQBytes;
-                mbar_arrive_expect_tx(&mt.q_full[s], 2 * kQBytes);
-                const int row_tok = kind == 0 ? (int)(seq_tok + row0) : row0;
-                const CUtensorMap *mq = kind == 0 ? &tm_qb : &tm_qo;
-                const CUtensorMap *md = kind == 0 ? &tm_db : &tm_do;
-                for (int j = 0; j < 2; ++j) {
-                    tma_load_3d(qa + j * kBoxQ, mq, &mt.q_full[s], 64 * j, h, row_tok);
-                    tma_load_3d(dO + j * kBoxQ, md, &mt.q_full[s], 64 * j, h, row_tok);
-                }
-            }
+            if (lane == 0) mbar_arrive(&mt.q_full[s]);
             issued = i + 1;
         }
         // nothing may land in shared memory after the CTA exits
@@ -255,10 +260,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t d_kmn = desc_sw128(smem_u32(smem + kOffK), kBoxK, 1024);     // K as MN-major A
             const uint64_t d_q0 = desc_sw128(smem_u32(smem + kOffQ), 16, 1024);         // qa stage 0, K-major
             const uint64_t d_qmn0 = desc_sw128(smem_u32(smem + kOffQ), kBoxQ, 1024);    // qa stage 0, MN-major
-            const uint64_t d_p0 = desc_sw128(smem_u32(smem + kOffP), 16, 1024);
             const uint64_t d_ds0 = desc_sw128(smem_u32(smem + kOffDS), 16, 1024);
             const uint64_t d_dsmn0 = desc_sw128(smem_u32(smem + kOffDS), kBoxQ, 1024);
-            constexpr uint32_t kStageU = (2 * kQBytes) >> 4, kQU = kQBytes >> 4, kPU = kPBytes >> 4;
+            constexpr uint32_t kStageU = (2 * kQBytes) >> 4, kQU = kQBytes >> 4, kDSU = kDSBytes >> 4;
             bool ok = mbar_wait(&mt.kv_full, 0, abort, p.status);
             for (int i = 0; ok && i <= n_tiles; ++i) {
                 if (i < n_tiles) {
@@ -271,13 +275,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int ks = 0; ks < kD / 16; ++ks) {
                         const uint32_t ok_ = ((ks >> 2) * kBoxK + (ks & 3) * 32) >> 4;
                         const uint32_t oq = ((ks >> 2) * kBoxQ + (ks & 3) * 32) >> 4;
-                        mma_ss(tmem, d_k + ok_, dq + oq, kIdS, ks > 0);
+                        mma_ss(tmem + kTS, d_k + ok_, dq + oq, kIdS, ks > 0);
                     }
 #pragma unroll
                     for (int ks = 0; ks < kD / 16; ++ks) {
                         const uint32_t ok_ = ((ks >> 2) * kBoxK + (ks & 3) * 32) >> 4;
                         const uint32_t oq = ((ks >> 2) * kBoxQ + (ks & 3) * 32) >> 4;
-                        mma_ss(tmem + 64, d_v + ok_, ddo + oq, kIdS, ks > 0);
+                        mma_ss(tmem + kTdP, d_v + ok_, ddo + oq, kIdS, ks > 0);
                     }
                     tc_commit(&mt.s_full);
                 }
@@ -286,23 +290,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(ok = mbar_wait(&mt.p_full[ps], (pi / 2) & 1, abort, p.status))) break;
                     tc_fence_after();
                     const uint64_t dqmn = d_qmn0 + qs * kStageU, ddomn = dqmn + kQU;
-                    const uint64_t dp = d_p0 + ps * kPU, dds = d_ds0 + ps * kPU, ddsmn = d_dsmn0 + ps * kPU;
+                    const uint64_t dds = d_ds0 + ps * kDSU, ddsmn = d_dsmn0 + ps * kDSU;
+                    // dV += P^T dO: P^T packed bf16 in TMEM, 16 rows (8 columns) per step
 #pragma unroll
                     for (int kk = 0; kk < kRows / 16; ++kk)
-                        mma_ss(tmem + 128, dp + ((kk * 32) >> 4), ddomn + ((kk * 16 * 128) >> 4), kIdKV,
+                        mma_ts(tmem + kTdV, tmem + kTP + 32 * ps + 8 * kk, ddomn + ((kk * 16 * 128) >> 4), kIdKV,
                                (pi > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
                     for (int kk = 0; kk < kRows / 16; ++kk)
-                        mma_ss(tmem + 256, dds + ((kk * 32) >> 4), dqmn + ((kk * 16 * 128) >> 4), kIdKV,
+                        mma_ss(tmem + kTdK, dds + ((kk * 32) >> 4), dqmn + ((kk * 16 * 128) >> 4), kIdKV,
                                (pi > 0 || kk > 0) ? 1u : 0u);
                     tc_commit(&mt.q_empty[qs]);
-                    if (pi >= 2 && !(ok = mbar_wait(&mt.dq_free[ps], ((pi / 2) - 1) & 1, abort, p.status))) break;
+                    if (pi >= 1 && !(ok = mbar_wait(&mt.dq_free, (pi - 1) & 1, abort, p.status))) break;
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < kKeys / 16; ++kk)
-                        mma_ss(tmem + 384 + 64 * ps, d_kmn + ((kk * 16 * 128) >> 4), ddsmn + ((kk * 16 * 128) >> 4),
-                               kIdQ, kk > 0);
-                    tc_commit(&mt.dq_full[ps]);
+                        mma_ss(tmem + kTdQ, d_kmn + ((kk * 16 * 128) >> 4), ddsmn + ((kk * 16 * 128) >> 4), kIdQ,
+                               kk > 0);
+                    tc_commit(&mt.dq_full);
                     tc_commit(&mt.pds_free[ps]);
                 }
             }
@@ -317,28 +322,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
         const float c2 = p.scale_log2;
         auto drain = [&](int pi) -> bool {
-            const int ps = pi % 2;
-            if (!mbar_wait_warp(&mt.dq_full[ps], (pi / 2) & 1, abort, p.status)) return false;
+            if (!mbar_wait_warp(&mt.dq_full, pi & 1, abort, p.status)) return false;
             tc_fence_after();
             uint32_t v[32];
-            tmem_ld32(tmem + lane_off + 384 + 64 * ps + 32 * hh, v);
+            tmem_ld32(tmem + lane_off + kTdQ + 32 * hh, v);
             tmem_ld_wait();
             reg_fence(v);
             tc_fence_before();
-            mbar_arrive(&mt.dq_free[ps]);
+            mbar_arrive(&mt.dq_free);
             const int2 tl = mt.tiles[pi];
             const int h = tl.x >> 1, kind = tl.x & 1, row0 = tl.y;
             const int ch = key;  // dQ^T lanes are channels
+            if (kind == 0) {
+                float *dst = p.dq_acc + ((seq_tok + row0 + 32 * hh) * p.Hq + h) * kD + ch;
+                const long long stride = (long long)p.Hq * kD;
+                const int n = min(32, p.T - (row0 + 32 * hh));
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const int col = 32 * hh + e;
-                if (kind == 0) {
-                    const int t = row0 + col;
-                    if (t < p.T) red_add_f32(p.dq_acc + ((seq_tok + t) * p.Hq + h) * kD + ch, __uint_as_float(v[e]));
-                } else {
-                    const int r = row0 + col;
-                    if (r < r1b) red_add_f32(p.dq_out_acc + ((long long)r * p.Hq + h) * kD + ch, __uint_as_float(v[e]));
-                }
+                for (int e = 0; e < 32; ++e)
+                    if (e < n) red_add_f32(dst + e * stride, __uint_as_float(v[e]));
+            } else {
+                float *dst = p.dq_out_acc + ((long long)(row0 + 32 * hh) * p.Hq + h) * kD + ch;
+                const long long stride = (long long)p.Hq * kD;
+                const int n = min(32, r1b - (row0 + 32 * hh));
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    if (e < n) red_add_f32(dst + e * stride, __uint_as_float(v[e]));
             }
             return true;
         };
@@ -348,46 +356,54 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = mbar_wait_warp(&mt.s_full, i & 1, abort, p.status))) break;
             tc_fence_after();
             uint32_t sv[32], dv[32];
-            tmem_ld32(tmem + lane_off + 32 * hh, sv);
-            tmem_ld32(tmem + lane_off + 64 + 32 * hh, dv);
+            tmem_ld32(tmem + lane_off + kTS + 32 * hh, sv);
+            tmem_ld32(tmem + lane_off + kTdP + 32 * hh, dv);
             tmem_ld_wait();
             reg_fence(sv);
             reg_fence(dv);
             tc_fence_before();
             mbar_arrive(&mt.s_free);
-            // the row metadata was written by the producer's threads before q_full
+            // the row metadata was published with q_full (already complete for this tile)
             if (!(ok = mbar_wait_warp(&mt.q_full[s], (i / kStages) & 1, abort, p.status))) break;
             const int kind = mt.tiles[i].x & 1;
+            const unsigned wlim = kind ? 0x7fffffffu : (unsigned)p.window;  // valid: 0 <= t - j < wlim
             const StageMeta &sm = mt.st[s];
             uint32_t pk[16], dk[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                float pv[2], dsv[2];
+            for (int q4 = 0; q4 < 8; ++q4) {
+                const int col = 32 * hh + 4 * q4;
+                const int4 t4 = *reinterpret_cast<const int4 *>(&sm.pos[col]);
+                const float4 l4 = *reinterpret_cast<const float4 *>(&sm.lse2[col]);
+                const float4 d4 = *reinterpret_cast<const float4 *>(&sm.ndelta[col]);
+                const int tt[4] = {t4.x, t4.y, t4.z, t4.w};
+                const float ll[4] = {l4.x, l4.y, l4.z, l4.w};
+                const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
+                float pv[4], dsv[4];
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int col = 32 * hh + 2 * e + u;
-                    const int t = sm.pos[col];
-                    const bool valid = t >= j && (kind == 1 || t - j < p.window);
-                    const float pr = ex2(fmaf(__uint_as_float(sv[2 * e + u]), c2, -sm.lse2[col]));
-                    const float pp = valid ? pr : 0.f;
+                for (int u = 0; u < 4; ++u) {
+                    const int e = 4 * q4 + u;
+                    const float pr = ex2(fmaf(__uint_as_float(sv[e]), c2, -ll[u]));
+                    const float pp = (unsigned)(tt[u] - j) < wlim ? pr : 0.f;
                     pv[u] = pp;
-                    dsv[u] = valid ? pp * (__uint_as_float(dv[2 * e + u]) - sm.delta[col]) * p.scale : 0.f;
+                    dsv[u] = pp * fmaf(__uint_as_float(dv[e]), p.scale, dd[u]);
                 }
-                pk[e] = pack_bf16(pv[0], pv[1]);
-                dk[e] = pack_bf16(dsv[0], dsv[1]);
+                pk[2 * q4] = pack_bf16(pv[0], pv[1]);
+                pk[2 * q4 + 1] = pack_bf16(pv[2], pv[3]);
+                dk[2 * q4] = pack_bf16(dsv[0], dsv[1]);
+                dk[2 * q4 + 1] = pack_bf16(dsv[2], dsv[3]);
             }
-            if (i >= 2) {
-                if (!(ok = mbar_wait_warp(&mt.pds_free[ps], ((i / 2) - 1) & 1, abort, p.status))) break;
-            }
-            uint8_t *pb = smem + kOffP + ps * kPBytes + key * 128;
-            uint8_t *db = smem + kOffDS + ps * kPBytes + key * 128;
+            if (i >= 2 && !(ok = mbar_wait_warp(&mt.pds_free[ps], ((i / 2) - 1) & 1, abort, p.status))) break;
+            // P^T rows 32 hh .. +31 of this key -> 16 packed columns of this P buffer
+            tmem_st16(tmem + lane_off + kTP + 32 * ps + 16 * hh, pk);
+            uint8_t *db = smem + kOffDS + ps * kDSBytes + key * 128;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int phys = ((4 * hh + q) ^ (key & 7)) << 4;
-                *reinterpret_cast<uint4 *>(pb + phys) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
                 *reinterpret_cast<uint4 *>(db + phys) = make_uint4(dk[4 * q], dk[4 * q + 1], dk[4 * q + 2], dk[4 * q + 3]);
             }
+            tmem_st_wait();
             fence_proxy_async_smem();
+            tc_fence_before();
             mbar_arrive(&mt.p_full[ps]);
             if (i >= 1 && !(ok = drain(i - 1))) break;
         }
@@ -402,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     uint32_t v[32];
-                    tmem_ld32(tmem + lane_off + 128 + 128 * which + 64 * hh + 32 * half, v);
+                    tmem_ld32(tmem + lane_off + kTdV + 128 * which + 64 * hh + 32 * half, v);
                     tmem_ld_wait();
                     reg_fence(v);
                     if (j < p.T) {
