@@ -187,6 +187,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         const float log2e = 1.4426950408889634f;
+        // Row metadata of tile i (2 rows per lane) is loaded into registers one
+        // tile ahead, so its global-memory latency overlaps the wait for a stage.
+        int m_pos[2];
+        float m_l2[2], m_dl[2];
+        auto fetch = [&](int i) {
+            const int2 tl = mt.tiles[i];
+            const int h = tl.x >> 1, kind = tl.x & 1, row0 = tl.y;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int c = lane + 32 * u;
+                m_pos[u] = -1;
+                m_l2[u] = INFINITY;
+                m_dl[u] = 0.f;
+                if (kind == 0) {
+                    const int t = row0 + c;
+                    if (t < p.T) {
+                        const long long idx = ((long long)b * p.Hq + h) * p.T + t;
+                        m_pos[u] = t;
+                        m_l2[u] = p.lse_base[idx];
+                        m_dl[u] = p.delta_base[idx];
+                    }
+                } else {
+                    const int r = row0 + c;
+                    if (r < r1b) {
+                        const long long idx = (long long)r * p.Hq + h;
+                        m_pos[u] = p.out_positions[r];
+                        m_l2[u] = p.lse_out[idx];
+                        m_dl[u] = p.delta_out[idx];
+                    }
+                }
+            }
+        };
+        if (n_tiles > 0) fetch(0);
         for (int i = 0; i < n_tiles; ++i) {
             const int s = i % kStages;
             if (i >= kStages) {
@@ -206,39 +239,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_3d(dO + j * kBoxQ, md, &mt.q_full[s], 64 * j, h, row_tok);
                 }
             }
-            // row metadata while the tiles are in flight; the arrive publishes it
             StageMeta &sm = mt.st[s];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int c = lane + 32 * u;
-                int pos = -1;
-                float l2 = INFINITY, dl = 0.f;
-                if (kind == 0) {
-                    const int t = row0 + c;
-                    if (t < p.T) {
-                        const long long idx = ((long long)b * p.Hq + h) * p.T + t;
-                        pos = t;
-                        l2 = p.lse_base[idx] * log2e;
-                        dl = p.delta_base[idx];
-                    }
-                } else {
-                    const int r = row0 + c;
-                    if (r < r1b) {
-                        const int t = p.out_positions[r];
-                        if (t >= 0 && t < p.T) {
-                            const long long idx = (long long)r * p.Hq + h;
-                            pos = t;
-                            l2 = p.lse_out[idx] * log2e;
-                            dl = p.delta_out[idx];
-                        }
-                    }
-                }
-                sm.pos[c] = pos;
-                sm.lse2[c] = l2;
-                sm.ndelta[c] = -dl * p.scale;
+                const int t = m_pos[u];
+                const bool valid = t >= 0 && t < p.T;  // rows past the end carry -1
+                sm.pos[c] = valid ? t : -1;
+                sm.lse2[c] = valid ? m_l2[u] * log2e : INFINITY;
+                sm.ndelta[c] = valid ? -m_dl[u] * p.scale : 0.f;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&mt.q_full[s]);
+            if (i + 1 < n_tiles) fetch(i + 1);
             issued = i + 1;
         }
         // nothing may land in shared memory after the CTA exits
