@@ -406,6 +406,54 @@ def bench_decode(args, dist, dev, stream, peaks, ola, torch, W):
             "gpu_launches": sum(n for n, _ in prof.values())}
 
 
+def bench_backward(args, dist, dev, stream, peaks, ola, torch, W):
+    """Backward of the fine-tuning workload (Llama-8B attention shape, 8K,
+    answer span of 1024 output rows): one forward for o and lse, then K timed
+    calls of orthros_prefill_backward. Algorithmic FLOPs: 5 products of 2d per
+    useful (query, key) pair, i.e. 2.5x the forward's 4d."""
+    wl = W.SFT_8K
+    inputs = W.make_prefill(wl)
+    q, k, v = (inputs[n].to(dev) for n in ("q", "k", "v"))
+    aff = [inputs[n].to(dev) for n in ("alpha_base", "beta_base", "alpha_out", "beta_out")]
+    indptr = inputs["out_indptr"]
+    pos = inputs["out_positions"].to(dev)
+    n_out = int(indptr[-1])
+    fwd = ola.orthros_prefill(q, k, v, *aff, indptr, pos, wl.window, wl.scale, stream=stream)
+    do_b, do_o = (t.to(dev) for t in W.make_grad_outputs(inputs, seed=wl.seed + 7))
+    ws = torch.empty(ola.orthros_prefill_backward_workspace_size(wl.B, wl.T, wl.Hq, wl.Hkv, wl.d, n_out, wl.window,
+                                                                 wl.dtype), dtype=torch.uint8, device=dev)
+    grads = None
+
+    def step(_=0):
+        nonlocal grads
+        grads = ola.orthros_prefill_backward(q, k, v, *aff, indptr, pos, wl.window, wl.scale, *fwd, do_b, do_o,
+                                             out=grads, workspace=ws, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    rc, bits = ola.orthros_check(ws)
+    if rc != 0:
+        raise RuntimeError(f"backward flagged device status {rc} bits 0x{bits:x}")
+    steps = args.steps
+    ms, prof = _timed(ola, torch, dist, stream, step, steps)
+    positions = [int(t) for t in inputs["out_positions"]]
+    fwd_flops = prefill_flops(wl, positions)
+    flops = 2.5 * fwd_flops["total"]
+    dom, (dom_n, dom_ms) = max(prof.items(), key=lambda kv: kv[1][1])
+    achieved = flops / (dom_ms / dom_n * 1e-3) / 1e12
+    return {"value": flops * dist.world / (ms / steps * 1e-3) / 1e12, "unit": "TFLOP/s", "workload": wl.name,
+            "steps": steps, "ms_per_step": ms / steps, "useful_tflop_per_step": flops / 1e12,
+            "flop_model": "10 d per useful (query, key) pair: recomputed S, dP, dV, dK, dQ",
+            "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peaks["bf16"],
+                         "unit": "TFLOP/s", "frac": achieved / peaks["bf16"],
+                         "traffic": captured_traffic("bwd_tc") if dom == "bwd_tc" else None,
+                         "peak_source": f"{peaks['src']} bf16 dense (burst)", "avg_launch_ms": dom_ms / dom_n,
+                         "useful_tflop_per_launch": flops / 1e12},
+            "kernels": {n: {"launches": c, "total_ms": t} for n, (c, t) in prof.items()},
+            "gpu_launches": sum(n for n, _ in prof.values())}
+
+
 def run_ours(args, dist):
     import torch
 
@@ -420,11 +468,13 @@ def run_ours(args, dist):
     peaks = load_peaks()
     clocks = ClockSampler(dist.local)
     clocks.start()
-    pre = dec = None
+    pre = dec = bwd = None
     if args.only in ("all", "prefill"):
         pre = bench_prefill(args, dist, dev, stream, peaks, ola, torch, W)
     if args.only in ("all", "decode"):
         dec = bench_decode(args, dist, dev, stream, peaks, ola, torch, W)
+    if args.only in ("all", "backward"):
+        bwd = bench_backward(args, dist, dev, stream, peaks, ola, torch, W)
     clk = clocks.stop()
     cpu = None
     if pre is not None and dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
@@ -432,8 +482,8 @@ def run_ours(args, dist):
         cpu = {"value": v_cpu, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
     if dist.rank != 0:
         return
-    if pre is None:  # decode-only profiling run
-        print(json.dumps({"decode": dec, "clocks": clk}), flush=True)
+    if pre is None:  # decode- or backward-only profiling run
+        print(json.dumps({"decode": dec, "backward": bwd, "clocks": clk}), flush=True)
         return
     wl = pre["wl"]
     line = {
@@ -451,6 +501,7 @@ def run_ours(args, dist):
         "gpu_launches": sum(n for n, _ in pre["prof"].values()),
         "e2e": pre.get("e2e"),
         "decode": dec,
+        "backward": bwd,
         "cpu_baseline": cpu,
         "clocks": clk,
     }
@@ -465,7 +516,7 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--decode-steps", type=int, default=None,
                     help="decoding steps to time (default: the workload's 128)")
-    ap.add_argument("--only", choices=("all", "prefill", "decode"), default="all",
+    ap.add_argument("--only", choices=("all", "prefill", "decode", "backward"), default="all",
                     help="run one part (profiling captures); the headline line needs 'all'")
     ap.add_argument("--prefill-T", type=int, default=None,
                     help="shorter prefill (a smaller case of the same kernels, for profiler captures)")

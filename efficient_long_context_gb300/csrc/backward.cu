@@ -33,29 +33,47 @@ namespace {
 
 constexpr int kWarps = 8;
 
+// E consecutive elements of this lane as one vector load (E = 2 or 4).
 template <typename T, int E>
 __device__ __forceinline__ void ld(const T *p, float (&x)[E]) {
     if constexpr (sizeof(T) == 4) {
-#pragma unroll
-        for (int e = 0; e < E; e += 2) {
-            const float2 r = *reinterpret_cast<const float2 *>(p + e);
-            x[e] = r.x;
-            x[e + 1] = r.y;
+        if constexpr (E == 4) {
+            const float4 r = *reinterpret_cast<const float4 *>(p);
+            x[0] = r.x; x[1] = r.y; x[2] = r.z; x[3] = r.w;
+        } else {
+            const float2 r = *reinterpret_cast<const float2 *>(p);
+            x[0] = r.x; x[1] = r.y;
         }
     } else {
-#pragma unroll
-        for (int e = 0; e < E; e += 2) {
-            const __nv_bfloat162 r = *reinterpret_cast<const __nv_bfloat162 *>(p + e);
-            x[e] = __low2float(r);
-            x[e + 1] = __high2float(r);
+        if constexpr (E == 4) {
+            const uint2 r = *reinterpret_cast<const uint2 *>(p);
+            const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(&r.x);
+            const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&r.y);
+            x[0] = __low2float(a); x[1] = __high2float(a); x[2] = __low2float(b); x[3] = __high2float(b);
+        } else {
+            const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(p);
+            x[0] = __low2float(a); x[1] = __high2float(a);
         }
     }
 }
 
 template <typename T, int E>
 __device__ __forceinline__ void st(T *p, const float (&x)[E]) {
-#pragma unroll
-    for (int e = 0; e < E; ++e) p[e] = from_f32<T>(x[e]);
+    if constexpr (sizeof(T) == 4) {
+        if constexpr (E == 4) *reinterpret_cast<float4 *>(p) = make_float4(x[0], x[1], x[2], x[3]);
+        else *reinterpret_cast<float2 *>(p) = make_float2(x[0], x[1]);
+    } else {
+        const __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]);
+        if constexpr (E == 4) {
+            const __nv_bfloat162 b = __floats2bfloat162_rn(x[2], x[3]);
+            uint2 r;
+            r.x = *reinterpret_cast<const uint32_t *>(&a);
+            r.y = *reinterpret_cast<const uint32_t *>(&b);
+            *reinterpret_cast<uint2 *>(p) = r;
+        } else {
+            *reinterpret_cast<__nv_bfloat162 *>(p) = a;
+        }
+    }
 }
 
 __device__ __forceinline__ float wsum(float x) {
@@ -234,30 +252,37 @@ __global__ void __launch_bounds__(256) bwd_dkdv_kernel(BwdArgs a) {
     st<T, E>(static_cast<T *>(a.dv) + unit * D + lane * E, dv);
 }
 
-// kind 0: base rows, grid (ceil(T/8), Hq, B); kind 1: output rows, grid (ceil(n_out/8), Hq).
-// FromAcc: dqa (scale included) was accumulated by the tensor-core kernel
-// (dq_acc for base rows, dq_rows for output rows); only the affine step and
-// the affine gradients remain.
-template <typename T, int D, bool FromAcc>
+// kind 0: base rows, grid (ceil(T/(8 RPW)), Hq, B); kind 1: output rows,
+// grid (ceil(n_out/(8 RPW)), Hq). Each warp handles RPW rows of one head and
+// keeps its share of the affine gradients in registers; the block reduces
+// them once. FromAcc: dqa (scale included) was accumulated by the tensor-core
+// kernel (dq_acc for base rows, dq_rows for output rows); only the affine
+// step and the affine gradients remain.
+template <typename T, int D, bool FromAcc, int RPW>
 __global__ void __launch_bounds__(256) bwd_dq_kernel(BwdArgs a, int kind) {
     constexpr int E = D / 32;
     __shared__ float red[2][kWarps][D];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int h = blockIdx.y;
     const int kv = h / (a.Hq / a.Hkv);
+    float acc_a[E], acc_b[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc_a[e] = acc_b[e] = 0.f;
+    const float *alpha = kind == 0 ? a.alpha_base : a.alpha_out;
+    const float *beta = kind == 0 ? a.beta_base : a.beta_out;
+    for (int it = 0; it < RPW; ++it) {
+    const int row_id = (blockIdx.x * RPW + it) * kWarps + warp;
     float dqa[E], qraw[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) dqa[e] = qraw[e] = 0.f;
-    const float *alpha = kind == 0 ? a.alpha_base : a.alpha_out;
-    const float *beta = kind == 0 ? a.beta_base : a.beta_out;
     int b = 0, t = -1, r = -1;
     bool active;
     if (kind == 0) {
         b = blockIdx.z;
-        t = blockIdx.x * kWarps + warp;
+        t = row_id;
         active = t < a.T;
     } else {
-        r = blockIdx.x * kWarps + warp;
+        r = row_id;
         active = r < a.n_out;
         if (active) {
             b = seq_of_row(a.out_indptr, a.B, r);
@@ -338,8 +363,14 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(BwdArgs a, int kind) {
     }
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-        red[0][warp][lane * E + e] = dqa[e] * qraw[e];  // zero for inactive warps
-        red[1][warp][lane * E + e] = dqa[e];
+        acc_a[e] = fmaf(dqa[e], qraw[e], acc_a[e]);  // zero for inactive rows
+        acc_b[e] += dqa[e];
+    }
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        red[0][warp][lane * E + e] = acc_a[e];
+        red[1][warp][lane * E + e] = acc_b[e];
     }
     __syncthreads();
     float *ga = kind == 0 ? a.d_alpha_base : a.d_alpha_out;
@@ -358,12 +389,18 @@ cudaError_t launch_t(const BwdArgs &a, cudaStream_t stream) {
     const long long n_base = (long long)a.B * a.T * a.Hq;
     const long long n_rows = n_base + (long long)a.n_out * a.Hq;
     cudaError_t e;
+    if (a.n_out > 0) {
+        {
+            ProfScope ps("bwd_row_lists", stream);
+            bwd_row_lists_kernel<<<(a.n_out + 255) / 256, 256, 0, stream>>>(a);
+        }
+        if constexpr (Tc) {
+            ProfScope ps("bwd_omax", stream);
+            bwd_omax_kernel<<<(a.n_out + 255) / 256, 256, 0, stream>>>(a);
+        }
+    }
     {
         ProfScope ps("bwd_prep", stream);
-        if (a.n_out > 0) {
-            bwd_row_lists_kernel<<<(a.n_out + 255) / 256, 256, 0, stream>>>(a);
-            if constexpr (Tc) bwd_omax_kernel<<<(a.n_out + 255) / 256, 256, 0, stream>>>(a);
-        }
         bwd_delta_kernel<T, D, Tc><<<(unsigned)((n_rows + kWarps - 1) / kWarps), kWarps * 32, 0, stream>>>(a, n_base);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -403,14 +440,19 @@ cudaError_t launch_t(const BwdArgs &a, cudaStream_t stream) {
         e = cudaGetLastError();
     }
     if (e != cudaSuccess) return e;
+    // the tensor-core path's finishing pass is light per row: 8 rows per warp
+    constexpr int kRpw = Tc ? 8 : 1;
+    constexpr int kRowsPerBlock = kWarps * kRpw;
     if (a.n_out > 0) {
         ProfScope ps(Tc ? "bwd_finish_out" : "bwd_dq_out_simt", stream);
-        bwd_dq_kernel<T, D, Tc><<<dim3((a.n_out + kWarps - 1) / kWarps, a.Hq), kWarps * 32, 0, stream>>>(a, 1);
+        bwd_dq_kernel<T, D, Tc, kRpw><<<dim3((a.n_out + kRowsPerBlock - 1) / kRowsPerBlock, a.Hq), kWarps * 32, 0,
+                                         stream>>>(a, 1);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     {
         ProfScope ps(Tc ? "bwd_finish" : "bwd_dq_simt", stream);
-        bwd_dq_kernel<T, D, Tc><<<dim3((a.T + kWarps - 1) / kWarps, a.Hq, a.B), kWarps * 32, 0, stream>>>(a, 0);
+        bwd_dq_kernel<T, D, Tc, kRpw><<<dim3((a.T + kRowsPerBlock - 1) / kRowsPerBlock, a.Hq, a.B), kWarps * 32, 0,
+                                         stream>>>(a, 0);
     }
     return cudaGetLastError();
 }
