@@ -374,6 +374,144 @@ int orthros_ref_decode(const float *q, const float *q_out, const float *k_new,
 }
 
 /*
+ * One continuous-batching step over the paged cache: Sec. 3.2 runs every
+ * regime as the same computation (prefill then decoding agree exactly with
+ * one longer prefill), so a step may append several tokens to a sequence (a
+ * prefill chunk) or one (a decoding step) or none. Sequence b appends
+ * n_b = new_indptr[b+1] - new_indptr[b] tokens (rows new_indptr[b] .. of
+ * k_new/v_new/q) at positions L_b .. L_b + n_b - 1, L_b = cache_lens[b]; then
+ *   - every new token's base row attends keys max(0, t-w+1) .. t (Eq. 4);
+ *   - every output row r of sequence b (out_indptr, out_positions) at a
+ *     position t in [0, L_b + n_b) attends keys 0 .. t (Eq. 5), with raw
+ *     query q_out[r], or, when q_out is NULL, the q of the new token at t
+ *     (t must then be a new position).
+ * q [n_new,Hq,d], k_new/v_new [n_new,Hkv,d]; outputs o_base [n_new,Hq,d],
+ * lse_base [n_new,Hq], o_out [n_out,Hq,d], lse_out [n_out,Hq]. The caches are
+ * modified (the appends).
+ */
+int orthros_ref_extend(const float *q, const float *q_out, const float *k_new,
+                       const float *v_new, float *k_cache, float *v_cache,
+                       const int32_t *block_table, int max_pages, int page_size,
+                       int num_pages, const int32_t *cache_lens,
+                       const int32_t *new_indptr, const int32_t *out_indptr,
+                       const int32_t *out_positions,
+                       const float *alpha_base, const float *beta_base,
+                       const float *alpha_out, const float *beta_out, int B,
+                       int Hq, int Hkv, int d, int window, double scale,
+                       double *o_base, double *lse_base, double *o_out,
+                       double *lse_out, int nthreads)
+{
+    if (check_common(B, 1, Hq, Hkv, d, window) != REF_OK || page_size < 1 ||
+        max_pages < 1 || num_pages < 1)
+        return REF_EINVAL;
+    const int g = Hq / Hkv;
+    const size_t tok = (size_t)Hkv * d;
+    int maxlen = 1;
+    for (int b = 0; b < B; ++b) {
+        const int L = cache_lens[b], n = new_indptr[b + 1] - new_indptr[b];
+        if (L < 0 || n < 0 || (long long)L + n > (long long)max_pages * page_size)
+            return REF_EINVAL;
+        for (int p = 0; p * page_size < L + n; ++p) {
+            const int pg = block_table[(size_t)b * max_pages + p];
+            if (pg < 0 || pg >= num_pages)
+                return REF_EINVAL;
+        }
+        for (int r = out_indptr[b]; r < out_indptr[b + 1]; ++r) {
+            const int t = out_positions[r];
+            if (t < 0 || t >= L + n || (!q_out && t < L))
+                return REF_EINVAL;
+        }
+        if (L + n > maxlen)
+            maxlen = L + n;
+    }
+    /* append first: the base tokens update the KV cache */
+    for (int b = 0; b < B; ++b)
+        for (int i = new_indptr[b]; i < new_indptr[b + 1]; ++i) {
+            const int t = cache_lens[b] + (i - new_indptr[b]);
+            const int pg = block_table[(size_t)b * max_pages + t / page_size];
+            const size_t off = ((size_t)pg * page_size + t % page_size) * tok;
+            memcpy(k_cache + off, k_new + (size_t)i * tok, sizeof(float) * tok);
+            memcpy(v_cache + off, v_new + (size_t)i * tok, sizeof(float) * tok);
+        }
+    const float **krow = (const float **)malloc(sizeof(*krow) * (size_t)B * Hkv * maxlen);
+    const float **vrow = (const float **)malloc(sizeof(*vrow) * (size_t)B * Hkv * maxlen);
+    if (!krow || !vrow) {
+        free(krow);
+        free(vrow);
+        return REF_ENOMEM;
+    }
+    for (int b = 0; b < B; ++b) {
+        const int len = cache_lens[b] + new_indptr[b + 1] - new_indptr[b];
+        for (int kv = 0; kv < Hkv; ++kv)
+            for (int j = 0; j < len; ++j) {
+                const int pg = block_table[(size_t)b * max_pages + j / page_size];
+                const size_t off = ((size_t)pg * page_size + j % page_size) * tok + (size_t)kv * d;
+                krow[((size_t)b * Hkv + kv) * maxlen + j] = k_cache + off;
+                vrow[((size_t)b * Hkv + kv) * maxlen + j] = v_cache + off;
+            }
+    }
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    const int n_new = new_indptr[B], n_out = out_indptr[B];
+    const long long nunits = ((long long)n_new + n_out) * Hq;
+    int err = REF_OK;
+#pragma omp parallel
+    {
+        double *qa = (double *)malloc(sizeof(double) * d);
+        double *w = (double *)malloc(sizeof(double) * maxlen);
+        const int ok = qa && w;
+        if (!ok) {
+#pragma omp atomic write
+            err = REF_ENOMEM;
+        }
+#pragma omp for schedule(dynamic, 8)
+        for (long long u = 0; u < nunits; ++u) {
+            if (!ok)
+                continue;
+            const int h = (int)(u % Hq);
+            const long long row = u / Hq;
+            const int kv = h / g;
+            double lse;
+            if (row < n_new) { /* base row of a new token */
+                const int i = (int)row;
+                int b = 0;
+                while (new_indptr[b + 1] <= i)
+                    ++b;
+                const int t = cache_lens[b] + (i - new_indptr[b]);
+                const size_t qoff = ((size_t)i * Hq + h) * (size_t)d;
+                const size_t tab = ((size_t)b * Hkv + kv) * maxlen;
+                affine(q + qoff, alpha_base + (size_t)h * d, beta_base + (size_t)h * d, d, qa);
+                const int lo = t - window + 1 > 0 ? t - window + 1 : 0;
+                attend_row(qa, krow + tab, vrow + tab, lo, t, d, scale, o_base + qoff, &lse, w);
+                lse_base[(size_t)i * Hq + h] = lse;
+            } else { /* output row */
+                const int r = (int)(row - n_new);
+                int b = 0;
+                while (out_indptr[b + 1] <= r)
+                    ++b;
+                const int t = out_positions[r];
+                const size_t roff = ((size_t)r * Hq + h) * (size_t)d;
+                const size_t tab = ((size_t)b * Hkv + kv) * maxlen;
+                const float *qraw = q_out ? q_out + roff
+                                          : q + ((size_t)(new_indptr[b] + t - cache_lens[b]) * Hq + h) * (size_t)d;
+                affine(qraw, alpha_out + (size_t)h * d, beta_out + (size_t)h * d, d, qa);
+                attend_row(qa, krow + tab, vrow + tab, 0, t, d, scale, o_out + roff, &lse, w);
+                lse_out[(size_t)r * Hq + h] = lse;
+            }
+        }
+        free(qa);
+        free(w);
+    }
+    free(krow);
+    free(vrow);
+    return err;
+}
+
+/*
  * Gradient of one query row's output (Eq. 4 / Eq. 5) given dO: recomputes the
  * row's exact softmax in double, then
  *   D = dO . o,  dp_j = dO . v_j,  ds_j = p_j (dp_j - D),

@@ -67,6 +67,17 @@ def _bind(path):
         _f64p, _f64p, _f64p, _f64p,
         ctypes.c_int,
     ]
+    lib.orthros_ref_extend.restype = ctypes.c_int
+    lib.orthros_ref_extend.argtypes = [
+        _f32p, _f32p, _f32p, _f32p,  # q q_out k_new v_new
+        _f32p, _f32p,  # caches
+        _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,  # block_table max_pages page_size num_pages
+        _i32p, _i32p, _i32p, _i32p,  # cache_lens new_indptr out_indptr out_positions
+        _f32p, _f32p, _f32p, _f32p,
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+        _f64p, _f64p, _f64p, _f64p,
+        ctypes.c_int,
+    ]
     lib.orthros_ref_prefill_backward.restype = ctypes.c_int
     lib.orthros_ref_prefill_backward.argtypes = [
         _f32p, _f32p, _f32p,  # q k v
@@ -107,6 +118,9 @@ class Oracle:
 
     def prefill_backward(self, *args, **kwargs):
         return prefill_backward(*args, _lib=self._lib, **kwargs)
+
+    def extend(self, *args, **kwargs):
+        return extend(*args, _lib=self._lib, **kwargs)
 
 
 def max_threads() -> int:
@@ -270,3 +284,46 @@ def prefill_backward(q, k, v, alpha_base, beta_base, alpha_out, beta_out, out_in
     return {"dq": dq, "dk": dk, "dv": dv, "dq_out": dq_out,
             "d_alpha_base": grads[0], "d_beta_base": grads[1],
             "d_alpha_out": grads[2], "d_beta_out": grads[3]}
+
+
+def extend(q, k_new, v_new, k_cache, v_cache, block_table, cache_lens, new_indptr, out_indptr, out_positions,
+           alpha_base, beta_base, alpha_out, beta_out, window, scale, q_out=None, nthreads=0, _lib=None):
+    """One continuous-batching step (appends, then Eq. 4 rows of the new tokens
+    and Eq. 5 output rows) in float64; k_cache / v_cache are MODIFIED in place.
+    q [n_new,Hq,d], k_new/v_new [n_new,Hkv,d], new_indptr/out_indptr [B+1],
+    out_positions [n_out] absolute positions. Returns (o_base [n_new,Hq,d],
+    lse_base [n_new,Hq], o_out [n_out,Hq,d], lse_out [n_out,Hq])."""
+    q, k_new, v_new = _f32(q), _f32(k_new), _f32(v_new)
+    n_new, Hq, d = q.shape
+    Hkv = k_new.shape[1]
+    assert k_cache.dtype == np.float32 and k_cache.flags.c_contiguous
+    assert v_cache.dtype == np.float32 and v_cache.flags.c_contiguous
+    num_pages, page_size = k_cache.shape[0], k_cache.shape[1]
+    block_table = _i32(block_table)
+    max_pages = block_table.shape[1]
+    new_indptr, out_indptr = _i32(new_indptr), _i32(out_indptr)
+    B = new_indptr.shape[0] - 1
+    assert out_indptr.shape == (B + 1,) and int(new_indptr[-1]) == n_new
+    n_out = int(out_indptr[-1])
+    out_positions = _i32(out_positions if out_positions is not None else np.zeros(0, np.int32))
+    cache_lens = _i32(cache_lens)
+    ab, bb, ao, bo = (_f32(x) for x in (alpha_base, beta_base, alpha_out, beta_out))
+    q_out = _f32(q_out)
+    o_base = np.zeros((n_new, Hq, d), np.float64)
+    lse_base = np.zeros((n_new, Hq), np.float64)
+    o_out = np.zeros((n_out, Hq, d), np.float64)
+    lse_out = np.zeros((n_out, Hq), np.float64)
+    dummy_f = np.zeros(1, np.float32)
+    dummy_i = np.zeros(1, np.int32)
+    rc = (_lib or _load()).orthros_ref_extend(
+        _ptr(q if n_new else dummy_f, _f32p), _ptr(q_out, _f32p), _ptr(k_new if n_new else dummy_f, _f32p),
+        _ptr(v_new if n_new else dummy_f, _f32p), _ptr(k_cache, _f32p), _ptr(v_cache, _f32p),
+        _ptr(block_table, _i32p), max_pages, page_size, num_pages,
+        _ptr(cache_lens, _i32p), _ptr(new_indptr, _i32p), _ptr(out_indptr, _i32p),
+        _ptr(out_positions if n_out else dummy_i, _i32p),
+        _ptr(ab, _f32p), _ptr(bb, _f32p), _ptr(ao, _f32p), _ptr(bo, _f32p),
+        B, Hq, Hkv, d, int(window), float(scale),
+        _ptr(o_base, _f64p), _ptr(lse_base, _f64p), _ptr(o_out, _f64p), _ptr(lse_out, _f64p), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"orthros_ref_extend failed with code {rc}")
+    return o_base, lse_base, o_out, lse_out

@@ -377,6 +377,121 @@ def pin_hand_worked(orc):
 
 
 # ---------------------------------------------------------------------------
+# Continuous-batching step (appends of several tokens per sequence)
+# ---------------------------------------------------------------------------
+
+def _extend_setup(seed, B, Hq, Hkv, d, P, lens, news, extra=0):
+    """Random history of lens[b] tokens per sequence in a shuffled page pool
+    with room for news[b] more; returns the logical per-sequence K/V too."""
+    rng = np.random.default_rng(seed)
+    k_hist = [rng.standard_normal((int(L), Hkv, d)).astype(np.float32) for L in lens]
+    v_hist = [rng.standard_normal((int(L), Hkv, d)).astype(np.float32) for L in lens]
+    kc, vc, bt = _paged_from_seq(k_hist, v_hist, np.asarray(lens), P, max(news) + extra, rng)
+    new_indptr = np.zeros(B + 1, np.int32)
+    new_indptr[1:] = np.cumsum(news)
+    n_new = int(new_indptr[-1])
+    q = rng.standard_normal((n_new, Hq, d)).astype(np.float32)
+    kn = rng.standard_normal((n_new, Hkv, d)).astype(np.float32)
+    vn = rng.standard_normal((n_new, Hkv, d)).astype(np.float32)
+    return rng, k_hist, v_hist, kc, vc, bt, new_indptr, q, kn, vn
+
+
+def pin_extend_brute_force(orc):
+    """Base rows of the new tokens and output rows anywhere in the sequence,
+    against dense brute force over the logical sequence (history + new)."""
+    B, Hq, Hkv, d, P, w = 3, 4, 2, 8, 4, 5
+    lens, news = [0, 6, 13], [4, 1, 0]
+    rng, k_hist, v_hist, kc, vc, bt, new_indptr, q, kn, vn = _extend_setup(41, B, Hq, Hkv, d, P, lens, news, extra=1)
+    ab, bb, ao, bo = (x.numpy() for x in make_affines(torch.Generator().manual_seed(8), Hq, d))
+    scale = 0.37
+    for with_q_out in (False, True):
+        if with_q_out:  # output rows may sit in the history when their query is given
+            lists = [[3, 0], [2, 6], [12, 5]]
+        else:  # otherwise only at new positions
+            lists = [[0, 3, 2], [6], []]
+        out_indptr, pos = csr(lists)
+        q_out = rng.standard_normal((int(out_indptr[-1]), Hq, d)).astype(np.float32) if with_q_out else None
+        kc2, vc2 = kc.copy(), vc.copy()
+        ob, lb, oo, lo = orc.extend(q, kn, vn, kc2, vc2, bt, np.asarray(lens, np.int32), new_indptr, out_indptr, pos,
+                                    ab, bb, ao, bo, w, scale, q_out=q_out)
+        for b in range(B):
+            i0, i1 = int(new_indptr[b]), int(new_indptr[b + 1])
+            K = np.concatenate([k_hist[b], kn[i0:i1]], 0)
+            V = np.concatenate([v_hist[b], vn[i0:i1]], 0)
+            L = lens[b]
+            for h in range(Hq):
+                kv = h // (Hq // Hkv)
+                if i1 > i0:
+                    o, l = brute_rows(q[i0:i1, h], ab[h], bb[h], K[:, kv], V[:, kv], np.arange(L, L + i1 - i0),
+                                      lambda t: max(0, t - w + 1), scale)
+                    _close(ob[i0:i1, h], o, what="extend base o")
+                    _close(lb[i0:i1, h], l, what="extend base lse")
+                r0, r1 = int(out_indptr[b]), int(out_indptr[b + 1])
+                if r1 > r0:
+                    p = pos[r0:r1]
+                    qr = q_out[r0:r1, h] if q_out is not None else q[i0 + p - L, h]
+                    o, l = brute_rows(qr, ao[h], bo[h], K[:, kv], V[:, kv], p, lambda t: 0, scale)
+                    _close(oo[r0:r1, h], o, what="extend out o")
+                    _close(lo[r0:r1, h], l, what="extend out lse")
+            for i in range(i0, i1):  # the appends landed where the block table says
+                t = L + i - i0
+                assert np.array_equal(kc2[bt[b, t // P], t % P], kn[i])
+                assert np.array_equal(vc2[bt[b, t // P], t % P], vn[i])
+
+
+def pin_extend_chunked_consistency(orc):
+    """Sec. 3.2: a prefill of T0 tokens followed by steps that append chunks of
+    3, 0, 5, 1 and 7 tokens gives every new token the base row of one prefill
+    over all tokens, and the output rows (last token of each chunk) its output rows."""
+    B, T0, Hq, Hkv, d, w, P = 2, 6, 4, 2, 8, 4, 4
+    chunks = [3, 0, 5, 1, 7]
+    T = T0 + sum(chunks)
+    q, k, v, ab, bb, ao, bo = rng_inputs(43, B, T, Hq, Hkv, d)
+    ends = np.cumsum([T0] + chunks) - 1
+    out_pos = sorted(set(int(e) for e in ends[1:]))
+    indptr, pos = csr([out_pos] * B)
+    full = orc.prefill(q, k, v, ab, bb, ao, bo, indptr, pos, w, 0.3)
+    rng = np.random.default_rng(4)
+    lens = np.full(B, T0, np.int32)
+    kc, vc, bt = _paged_from_seq([k[b, :T0] for b in range(B)], [v[b, :T0] for b in range(B)], lens, P, T - T0, rng)
+    at = T0
+    for c in chunks:
+        new_indptr = np.arange(B + 1, dtype=np.int32) * c
+        qn = np.concatenate([q[b, at:at + c] for b in range(B)], 0)
+        kn = np.concatenate([k[b, at:at + c] for b in range(B)], 0)
+        vn = np.concatenate([v[b, at:at + c] for b in range(B)], 0)
+        lists = [[at + c - 1] if c else [] for _ in range(B)]
+        oi, op = csr(lists)
+        ob, lb, oo, lo = orc.extend(qn.reshape(B * c, Hq, d), kn.reshape(B * c, Hkv, d), vn.reshape(B * c, Hkv, d),
+                                    kc, vc, bt, lens, new_indptr, oi, op, ab, bb, ao, bo, w, 0.3)
+        for b in range(B):
+            _close(ob[b * c:(b + 1) * c], full[0][b, at:at + c], 1e-12, f"chunk base o at {at}")
+            _close(lb[b * c:(b + 1) * c].T, full[1][b, :, at:at + c], 1e-12, f"chunk base lse at {at}")
+            if c:
+                r = int(indptr[b]) + out_pos.index(at + c - 1)
+                _close(oo[b], full[2][r], 1e-12, f"chunk out o at {at}")
+                _close(lo[b], full[3][r], 1e-12, f"chunk out lse at {at}")
+        lens = lens + c
+        at += c
+
+
+def pin_extend_single_token_is_decode(orc):
+    """One new token per sequence with an output row at it is a decoding step."""
+    rng = np.random.default_rng(47)
+    B, Hq, Hkv, d, P, w = 3, 4, 2, 8, 4, 6
+    lens = [0, 5, 11]
+    _, k_hist, v_hist, kc, vc, bt, new_indptr, q, kn, vn = _extend_setup(47, B, Hq, Hkv, d, P, lens, [1, 1, 1])
+    ab, bb, ao, bo = (x.numpy() for x in make_affines(torch.Generator().manual_seed(9), Hq, d))
+    qo = rng.standard_normal((B, Hq, d)).astype(np.float32)
+    out_indptr, pos = csr([[L] for L in lens])
+    a = orc.extend(q, kn, vn, kc.copy(), vc.copy(), bt, np.asarray(lens, np.int32), new_indptr, out_indptr, pos,
+                   ab, bb, ao, bo, w, 0.5, q_out=qo)
+    b_ = orc.decode(q, kn, vn, kc.copy(), vc.copy(), bt, np.asarray(lens, np.int32), ab, bb, ao, bo, w, 0.5, q_out=qo)
+    for x, y, n in zip(a, b_, ("o_base", "lse_base", "o_out", "lse_out")):
+        _close(x, y, 1e-12, "extend as decode " + n)
+
+
+# ---------------------------------------------------------------------------
 # Backward (gradients of Eq. 4 and Eq. 5 and of the query affines)
 # ---------------------------------------------------------------------------
 
@@ -562,6 +677,9 @@ ALL_PINS = [
     pin_decode_page_permutation,
     pin_prefill_decode_consistency,
     pin_hand_worked,
+    pin_extend_brute_force,
+    pin_extend_chunked_consistency,
+    pin_extend_single_token_is_decode,
     pin_backward_autograd,
     pin_backward_finite_difference,
     pin_backward_translation_sums,

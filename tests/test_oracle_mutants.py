@@ -43,6 +43,12 @@ MUTANTS = {
     "bw_dbeta_out_to_base": ("d_beta_out[(size_t)h * d + c] += dqa[c];", "d_beta_base[(size_t)h * d + c] += dqa[c];"),
     "bw_out_row_band": ("attend_row_backward(qa, do_out + roff, krow, vrow, dkrow, dvrow, 0, t,",
                         "attend_row_backward(qa, do_out + roff, krow, vrow, dkrow, dvrow, t > 0 ? 1 : 0, t,"),
+    "extend_position_shift": ("const int t = cache_lens[b] + (i - new_indptr[b]);",
+                              "const int t = cache_lens[b] + (i - new_indptr[b]) - (i > new_indptr[b] ? 1 : 0);"),
+    "extend_out_query_first_token": ("q + ((size_t)(new_indptr[b] + t - cache_lens[b]) * Hq + h)",
+                                     "q + ((size_t)(new_indptr[b] + 0 * (t - cache_lens[b])) * Hq + h)"),
+    "extend_base_sees_next_token": ("attend_row(qa, krow + tab, vrow + tab, lo, t, d, scale, o_base + qoff, &lse, w);\n                lse_base[(size_t)i * Hq + h] = lse;",
+                                    "attend_row(qa, krow + tab, vrow + tab, lo, t + (i + 1 < new_indptr[b + 1] ? 1 : 0), d, scale, o_base + qoff, &lse, w);\n                lse_base[(size_t)i * Hq + h] = lse;"),
     "decode_append_wrong_slot": ("((size_t)pg * page_size + L % page_size) * tok;", "((size_t)pg * page_size + (L + 1) % page_size) * tok;"),
 }
 
