@@ -454,6 +454,51 @@ def bench_backward(args, dist, dev, stream, peaks, ola, torch, W):
             "gpu_launches": sum(n for n, _ in prof.values())}
 
 
+def bench_extend(args, dist, dev, stream, peaks, ola, torch, W):
+    """A continuous-batching step (MIXED_32: 28 sequences decode one token, 4
+    append a 16-token prefill chunk, 16K-32K cached tokens each), timed over K
+    calls with the same inputs. Algorithmic bytes: every sequence's cached K
+    and V (L_b + n_b tokens) read once per step."""
+    wl = W.make_extend(W.MIXED_32)
+    w = W.MIXED_32
+    kc, vc = wl["k_cache"].to(dev), wl["v_cache"].to(dev)
+    bt, lens = wl["block_table"].to(dev), wl["cache_lens"].to(dev)
+    q, kn, vn = (wl[n].to(dev) for n in ("q", "k_new", "v_new"))
+    pos = wl["out_positions"].to(dev)
+    aff = [wl[n].to(dev) for n in ("alpha_base", "beta_base", "alpha_out", "beta_out")]
+    n_new, n_out = int(wl["new_indptr"][-1]), int(wl["out_indptr"][-1])
+    outs = (torch.empty_like(q), torch.empty((n_new, w.Hq), dtype=torch.float32, device=dev),
+            torch.empty((n_out, w.Hq, w.d), dtype=w.dtype, device=dev),
+            torch.empty((n_out, w.Hq), dtype=torch.float32, device=dev))
+    ws = torch.empty(ola.orthros_extend_workspace_size(w.B, n_new, n_out, w.Hq, w.Hkv, w.d, wl["max_pages"],
+                                                       w.page_size, w.dtype), dtype=torch.uint8, device=dev)
+
+    def step(_=0):
+        ola.orthros_extend(q, kn, vn, kc, vc, bt, lens, wl["new_indptr"], wl["out_indptr"], pos, *aff, w.window,
+                           w.scale, out=outs, workspace=ws, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    rc, bits = ola.orthros_check(ws)
+    if rc != 0:
+        raise RuntimeError(f"extend flagged device status {rc} bits 0x{bits:x}")
+    steps = max(args.steps, 20)
+    ms, prof = _timed(ola, torch, dist, stream, step, steps)
+    news = list(w.news)
+    nbytes = sum((int(L) + n) * w.Hkv * w.d * 2 * 2 for L, n in zip(wl["cache_lens"].tolist(), news))
+    dom, (dom_n, dom_ms) = max(prof.items(), key=lambda kv: kv[1][1])
+    achieved = nbytes / (dom_ms / dom_n * 1e-3) / 1e9
+    return {"value": nbytes * dist.world / (ms / steps * 1e-3) / 1e9, "unit": "GB/s", "workload": w.name,
+            "steps": steps, "ms_per_step": ms / steps, "bytes_per_step": nbytes,
+            "new_tokens_per_step": n_new, "output_rows_per_step": n_out,
+            "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm"], "traffic": None,
+                         "peak_source": f"{peaks['src']} HBM copy", "avg_launch_ms": dom_ms / dom_n},
+            "kernels": {n: {"launches": c, "total_ms": t} for n, (c, t) in prof.items()},
+            "gpu_launches": sum(n for n, _ in prof.values())}
+
+
 def run_ours(args, dist):
     import torch
 
@@ -468,13 +513,15 @@ def run_ours(args, dist):
     peaks = load_peaks()
     clocks = ClockSampler(dist.local)
     clocks.start()
-    pre = dec = bwd = None
+    pre = dec = bwd = ext = None
     if args.only in ("all", "prefill"):
         pre = bench_prefill(args, dist, dev, stream, peaks, ola, torch, W)
     if args.only in ("all", "decode"):
         dec = bench_decode(args, dist, dev, stream, peaks, ola, torch, W)
     if args.only in ("all", "backward"):
         bwd = bench_backward(args, dist, dev, stream, peaks, ola, torch, W)
+    if args.only in ("all", "extend"):
+        ext = bench_extend(args, dist, dev, stream, peaks, ola, torch, W)
     clk = clocks.stop()
     cpu = None
     if pre is not None and dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
@@ -483,7 +530,7 @@ def run_ours(args, dist):
     if dist.rank != 0:
         return
     if pre is None:  # decode- or backward-only profiling run
-        print(json.dumps({"decode": dec, "backward": bwd, "clocks": clk}), flush=True)
+        print(json.dumps({"decode": dec, "backward": bwd, "extend": ext, "clocks": clk}), flush=True)
         return
     wl = pre["wl"]
     line = {
@@ -502,6 +549,7 @@ def run_ours(args, dist):
         "e2e": pre.get("e2e"),
         "decode": dec,
         "backward": bwd,
+        "extend": ext,
         "cpu_baseline": cpu,
         "clocks": clk,
     }
@@ -516,7 +564,7 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--decode-steps", type=int, default=None,
                     help="decoding steps to time (default: the workload's 128)")
-    ap.add_argument("--only", choices=("all", "prefill", "decode", "backward"), default="all",
+    ap.add_argument("--only", choices=("all", "prefill", "decode", "backward", "extend"), default="all",
                     help="run one part (profiling captures); the headline line needs 'all'")
     ap.add_argument("--prefill-T", type=int, default=None,
                     help="shorter prefill (a smaller case of the same kernels, for profiler captures)")

@@ -16,6 +16,8 @@ from ._binding import (  # noqa: F401
     orthros_decode,
     orthros_decode_static,
     orthros_decode_workspace_size,
+    orthros_extend,
+    orthros_extend_workspace_size,
     orthros_last_error,
     orthros_prefill,
     orthros_prefill_backward,

@@ -22,7 +22,8 @@ STATUS_NAMES = {0: "ORTHROS_OK", 1: "ORTHROS_EINVAL", 2: "ORTHROS_EUNSUPPORTED",
 
 # the public symbols of include/orthros_attn.h
 EXPORTS = ("orthros_prefill_workspace_size", "orthros_prefill", "orthros_prefill_backward_workspace_size",
-           "orthros_prefill_backward", "orthros_decode_workspace_size",
+           "orthros_prefill_backward", "orthros_extend_workspace_size", "orthros_extend",
+           "orthros_decode_workspace_size",
            "orthros_decode", "orthros_decode_static", "orthros_check", "orthros_profile_begin", "orthros_profile_end",
            "orthros_status_string", "orthros_last_error")
 
@@ -67,6 +68,12 @@ def load_library(path: str | None = None):
                                                  i32, i32, i32, i32, i32, i32, ctypes.c_float, i32,
                                                  vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                                  vp, sz, vp]
+        lib.orthros_extend_workspace_size.restype = sz
+        lib.orthros_extend_workspace_size.argtypes = [i32] * 9
+        lib.orthros_extend.restype = i32
+        lib.orthros_extend.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp, i32p, i32p, vp,
+                                       vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float, i32,
+                                       vp, vp, vp, vp, vp, sz, vp]
         lib.orthros_decode_workspace_size.restype = sz
         lib.orthros_decode_workspace_size.argtypes = [i32] * 7
         lib.orthros_decode.restype = i32
@@ -228,6 +235,52 @@ def orthros_prefill_backward(q, k, v, alpha_base, beta_base, alpha_out, beta_out
         _ptr(workspace), workspace.numel(), _stream(stream))
     _raise_if(rc, lib)
     return out
+
+
+def orthros_extend_workspace_size(B, n_new, n_out, Hq, Hkv, d, max_pages, page_size, dtype=torch.bfloat16) -> int:
+    return int(load_library().orthros_extend_workspace_size(B, n_new, n_out, Hq, Hkv, d, max_pages, page_size,
+                                                            _DTYPES[dtype]))
+
+
+def orthros_extend(q, k_new, v_new, k_cache, v_cache, block_table, cache_lens, new_indptr, out_indptr,
+                   out_positions, alpha_base, beta_base, alpha_out, beta_out, window, scale=None, *, q_out=None,
+                   out=None, workspace=None, stream=None):
+    """orthros_extend of include/orthros_attn.h on torch CUDA tensors.
+
+    new_indptr / out_indptr are HOST int32 array-likes [B+1]; k_cache /
+    v_cache are updated in place. Returns (o_base [n_new,Hq,d], lse_base
+    [n_new,Hq], o_out [n_out,Hq,d], lse_out [n_out,Hq]).
+    """
+    lib = load_library()
+    n_new, Hq, d = q.shape
+    Hkv = k_new.shape[1]
+    num_pages, page_size = k_cache.shape[0], k_cache.shape[1]
+    max_pages = block_table.shape[1]
+    ni = np.ascontiguousarray(np.asarray(new_indptr, dtype=np.int32))
+    oi = np.ascontiguousarray(np.asarray(out_indptr, dtype=np.int32))
+    B = ni.shape[0] - 1
+    n_out = int(oi[-1]) if oi.size else 0
+    if scale is None:
+        scale = d ** -0.5
+    for name, t in (("q", q), ("q_out", q_out), ("k_new", k_new), ("v_new", v_new), ("out_positions", out_positions)):
+        _contig(name, t)
+    if out is None:
+        out = (torch.empty_like(q), torch.empty((n_new, Hq), dtype=torch.float32, device=q.device),
+               torch.empty((n_out, Hq, d), dtype=q.dtype, device=q.device),
+               torch.empty((n_out, Hq), dtype=torch.float32, device=q.device))
+    o_base, lse_base, o_out, lse_out = out
+    if workspace is None:
+        ws = orthros_extend_workspace_size(B, n_new, n_out, Hq, Hkv, d, max_pages, page_size, q.dtype)
+        workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=q.device)
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    rc = lib.orthros_extend(
+        _ptr(q), _ptr(q_out), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+        max_pages, page_size, num_pages, _ptr(cache_lens), ni.ctypes.data_as(i32p), oi.ctypes.data_as(i32p),
+        _ptr(out_positions), _ptr(alpha_base), _ptr(beta_base), _ptr(alpha_out), _ptr(beta_out),
+        B, Hq, Hkv, d, int(window), float(scale), _dtype(q),
+        _ptr(o_base), _ptr(lse_base), _ptr(o_out), _ptr(lse_out), _ptr(workspace), workspace.numel(), _stream(stream))
+    _raise_if(rc, lib)
+    return o_base, lse_base, o_out, lse_out
 
 
 def orthros_decode(q, k_new, v_new, k_cache, v_cache, block_table, cache_lens, alpha_base, beta_base,

@@ -38,6 +38,40 @@ __global__ void decode_append_kernel(const uint4 *__restrict__ k_new, const uint
     v_cache[dst] = v_new[i];
 }
 
+// Continuous-batching step: new token i of sequence b (rows new_indptr[b] ..)
+// goes to position cache_lens[b] + (i - new_indptr[b]).
+__global__ void extend_append_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
+                                     uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                                     const int32_t *__restrict__ block_table,
+                                     const int32_t *__restrict__ cache_lens, const int32_t *__restrict__ new_indptr,
+                                     int B, int n_new, int vec_per_tok, int max_pages, int page_size, int num_pages,
+                                     uint32_t *status) {
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (long long)n_new * vec_per_tok) return;
+    const int row = (int)(i / vec_per_tok);
+    const int w = (int)(i % vec_per_tok);
+    int lo = 0, hi = B - 1;  // sequence of the row: last b with new_indptr[b] <= row
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (new_indptr[mid] <= row) lo = mid; else hi = mid - 1;
+    }
+    const int b = lo;
+    const int L = cache_lens[b];
+    const long long t = (long long)L + (row - new_indptr[b]);
+    if (L < 0 || t >= (long long)max_pages * page_size) {
+        if (w == 0) set_status(status, ORTHROS_DEV_BAD_LENGTH);
+        return;
+    }
+    const int pg = block_table[(long long)b * max_pages + t / page_size];
+    if (pg < 0 || pg >= num_pages) {
+        if (w == 0) set_status(status, ORTHROS_DEV_BAD_PAGE);
+        return;
+    }
+    const long long dst = ((long long)pg * page_size + t % page_size) * vec_per_tok + w;
+    k_cache[dst] = k_new[i];
+    v_cache[dst] = v_new[i];
+}
+
 // Prefill: token t of sequence b goes to page block_table[b][t / P], slot t % P.
 __global__ void prefill_cache_fill_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
                                           uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
@@ -136,6 +170,21 @@ cudaError_t launch_decode_append(const void *k_new, const void *v_new, void *k_c
     decode_append_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, stream>>>(
         (const uint4 *)k_new, (const uint4 *)v_new, (uint4 *)k_cache, (uint4 *)v_cache, block_table,
         cache_lens, B, vec_per_tok, max_pages, page_size, num_pages, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_extend_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                                 const int32_t *block_table, const int32_t *cache_lens, const int32_t *new_indptr,
+                                 int B, int n_new, int Hkv, int d, int max_pages, int page_size, int num_pages,
+                                 int elem_bytes, uint32_t *status, cudaStream_t stream) {
+    if (n_new == 0) return cudaSuccess;
+    const int vec_per_tok = Hkv * d * elem_bytes / 16;
+    const long long n = (long long)n_new * vec_per_tok;
+    const int threads = 256;
+    if ((n + threads - 1) / threads > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    extend_append_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, stream>>>(
+        (const uint4 *)k_new, (const uint4 *)v_new, (uint4 *)k_cache, (uint4 *)v_cache, block_table, cache_lens,
+        new_indptr, B, n_new, vec_per_tok, max_pages, page_size, num_pages, status);
     return cudaGetLastError();
 }
 

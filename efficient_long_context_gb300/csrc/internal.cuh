@@ -44,9 +44,11 @@ struct RowsArgs {
     const float *alpha_base, *beta_base, *alpha_out, *beta_out;
     const int32_t *out_indptr;     // device copy [B+1] (prefill output rows)
     const int32_t *out_positions;  // [n_out]
-    const int32_t *block_table;    // decode
-    const int32_t *cache_lens;     // decode
+    const int32_t *block_table;    // decode / extend
+    const int32_t *cache_lens;     // decode / extend
+    const int32_t *new_indptr;     // extend: device [B+1], new tokens of each sequence
     int n_out, max_pages, page_size, num_pages;
+    int n_new;                     // extend
     int B, T, Hq, Hkv, window;
     float scale;
     void *o_base;
@@ -56,7 +58,7 @@ struct RowsArgs {
     uint32_t *status;
 };
 
-enum RowKind { kPrefillBase = 0, kPrefillOut = 1, kDecodePair = 2 };
+enum RowKind { kPrefillBase = 0, kPrefillOut = 1, kDecodePair = 2, kExtendBase = 3, kExtendOut = 4 };
 
 // orthros_api.cu: records the message returned by orthros_last_error() and
 // passes the status through.
@@ -98,15 +100,18 @@ int tc_units_per_kv(int nblk, int g);
 cudaError_t launch_prefill_tc(const TcParams &p, const void *k16, const void *v, int d, cudaStream_t stream);
 
 // splitkv.cu: split-KV attention for few rows over long key ranges + combine.
-enum SplitMode { kSplitPrefill = 0, kSplitDecode = 1 };
+enum SplitMode { kSplitPrefill = 0, kSplitDecode = 1, kSplitExtend = 2 };
 struct SplitParams {
     int mode;
     const __nv_bfloat16 *q, *q_out;  // prefill [B,T,Hq,d] / [n_out,Hq,d]; decode [B,Hq,d] each
     const __nv_bfloat16 *k, *v;      // prefill [B,T,Hkv,d]; decode caches [num_pages,P,Hkv,d]
     const float *alpha_base, *beta_base, *alpha_out, *beta_out;
     const int32_t *out_positions;    // prefill
-    const int32_t *group_info;       // prefill: 3 ints per group (b<<16 | kv, first row, positions)
-    const int32_t *block_table, *cache_lens;  // decode
+    const int32_t *group_info;       // prefill / extend: 3 ints per group (b<<16 | kv, first row,
+                                     // positions | kind << 30; kind (extend): 0 new-token base rows, 1 output rows)
+    const int32_t *block_table, *cache_lens;  // decode / extend
+    const int32_t *new_indptr;                // extend: device [B+1]
+    int n_new;                                // extend: rows of q / k_new / v_new
     int max_pages, page_size, num_pages;
     int B, T, Hq, Hkv, window;
     float scale, scale_log2;
@@ -119,6 +124,10 @@ struct SplitParams {
     float *lse_out;
     uint32_t *status;
 };
+// Row of an extend-mode group: position and whether it may be computed.
+__device__ __forceinline__ int extend_seq_len(const SplitParams &p, int b) {
+    return p.cache_lens[b] + (p.new_indptr[b + 1] - p.new_indptr[b]);
+}
 size_t split_partial_bytes(int n_groups, int max_chunks, int d);
 // Runs the split kernel (the TMA-fed persistent one when eligible) and the combine.
 cudaError_t launch_splitkv(const SplitParams &p, int d, int rows_per_group, cudaStream_t stream);
@@ -179,6 +188,12 @@ cudaError_t launch_backward_tc(const BwdTcParams &p, const void *k, const void *
                                const void *do_base, const void *qa_out, const void *do_out, cudaStream_t stream);
 
 // cache.cu
+// Writes new token i of sequence b (rows new_indptr[b] ..) at position
+// cache_lens[b] + (i - new_indptr[b]) of its pages.
+cudaError_t launch_extend_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                                 const int32_t *block_table, const int32_t *cache_lens, const int32_t *new_indptr,
+                                 int B, int n_new, int Hkv, int d, int max_pages, int page_size, int num_pages,
+                                 int elem_bytes, uint32_t *status, cudaStream_t stream);
 cudaError_t launch_decode_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
                                  const int32_t *block_table, const int32_t *cache_lens, int B, int Hkv,
                                  int d, int max_pages, int page_size, int num_pages, int elem_bytes,

@@ -116,6 +116,32 @@ BackwardLayout backward_layout(int B, int T, int Hq, int d, int n_out, orthros_d
     return L;
 }
 
+// Workspace regions of orthros_extend.
+struct ExtendLayout {
+    size_t blob_off, part_off, total;
+    int max_groups, max_chunks;
+};
+
+// Rows per split group: P positions of a sequence x the g query heads of a kv head.
+int extend_positions_per_group(int g) { return g <= 16 ? std::max(1, 16 / g) : 1; }
+
+ExtendLayout extend_layout(int B, int n_new, int n_out, int Hq, int Hkv, int d, int max_pages, int page_size,
+                           orthros_dtype dtype) {
+    ExtendLayout L{};
+    const int P = extend_positions_per_group(Hq / Hkv);
+    size_t at = kStatusBytes;
+    // every sequence's rows are cut into groups of P positions, per kv head
+    const long long groups = ((long long)(n_new + P - 1) / P + (long long)(n_out + P - 1) / P + 2LL * B) * Hkv;
+    L.max_groups = dtype == ORTHROS_BF16 ? (int)std::min<long long>(groups, 1LL << 30) : 0;
+    L.max_chunks = ceil_div((long long)max_pages * page_size, kDecodeChunk);
+    L.blob_off = at;
+    at += align_up(sizeof(int32_t) * (size_t)(2 * (B + 1) + 3 * (size_t)L.max_groups), 256);
+    L.part_off = at;
+    at += align_up(split_partial_bytes(L.max_groups, L.max_chunks, d), 256);
+    L.total = at;
+    return L;
+}
+
 orthros_status check_shapes(int B, int Hq, int Hkv, int d, int window, float scale, orthros_dtype dtype) {
     if (B < 0) return fail(ORTHROS_EINVAL, "B = %d must be >= 0", B);
     if (Hq < 1 || Hkv < 1) return fail(ORTHROS_EINVAL, "head counts Hq = %d, Hkv = %d must be >= 1", Hq, Hkv);
@@ -529,6 +555,184 @@ orthros_status orthros_prefill_backward(const void *q, const void *k, const void
     }
     e = launch_backward(a, d, dtype, use_tc, stream);
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+    return ORTHROS_OK;
+}
+
+size_t orthros_extend_workspace_size(int B, int n_new, int n_out, int Hq, int Hkv, int d, int max_pages,
+                                     int page_size, orthros_dtype dtype) {
+    if (n_new < 0 || n_out < 0 || max_pages < 1 || page_size < 1) return 0;
+    if (check_shapes(B, Hq, Hkv, d, 1, 1.0f, dtype) != ORTHROS_OK) return 0;
+    return extend_layout(B, n_new, n_out, Hq, Hkv, d, max_pages, page_size, dtype).total;
+}
+
+orthros_status orthros_extend(const void *q, const void *q_out, const void *k_new, const void *v_new, void *k_cache,
+                              void *v_cache, const int32_t *block_table, int max_pages, int page_size, int num_pages,
+                              const int32_t *cache_lens, const int32_t *new_indptr, const int32_t *out_indptr,
+                              const int32_t *out_positions, const float *alpha_base, const float *beta_base,
+                              const float *alpha_out, const float *beta_out, int B, int Hq, int Hkv, int d,
+                              int window, float scale, orthros_dtype dtype, void *o_base, float *lse_base,
+                              void *o_out, float *lse_out, void *workspace, size_t workspace_bytes,
+                              orthros_stream_t stream_) {
+    g_last_error.clear();
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    orthros_status st = check_shapes(B, Hq, Hkv, d, window, scale, dtype);
+    if (st != ORTHROS_OK) return st;
+    if (B > 32767) return fail(ORTHROS_EUNSUPPORTED, "B = %d exceeds 32767 sequences per step", B);
+    if (page_size < 1 || max_pages < 1 || num_pages < 1)
+        return fail(ORTHROS_EINVAL, "page_size, max_pages and num_pages must be >= 1");
+    if (B > 0 && (!new_indptr || !out_indptr)) return fail(ORTHROS_EINVAL, "new_indptr and out_indptr (host) must not be NULL");
+    for (const int32_t *ip : {new_indptr, out_indptr}) {
+        if (B == 0) break;
+        if (ip[0] != 0) return fail(ORTHROS_EINVAL, "indptr[0] = %d must be 0", ip[0]);
+        for (int b = 0; b < B; ++b)
+            if (ip[b + 1] < ip[b]) return fail(ORTHROS_EINVAL, "indptr decreases at %d", b);
+    }
+    const int n_new = B > 0 ? new_indptr[B] : 0;
+    const int n_out = B > 0 ? out_indptr[B] : 0;
+    if (B > 0) {
+        if (!k_cache || !v_cache || !block_table || !cache_lens)
+            return fail(ORTHROS_EINVAL, "k_cache, v_cache, block_table and cache_lens must not be NULL");
+        if (!aligned16(k_cache) || !aligned16(v_cache)) return fail(ORTHROS_EINVAL, "caches must be 16-byte aligned");
+    }
+    if (n_new > 0) {
+        if (!q || !k_new || !v_new || !alpha_base || !beta_base || !o_base || !lse_base)
+            return fail(ORTHROS_EINVAL, "q, k_new, v_new, alpha_base, beta_base, o_base, lse_base must not be NULL");
+        if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(o_base) ||
+            !aligned16(alpha_base) || !aligned16(beta_base))
+            return fail(ORTHROS_EINVAL, "new-token tensors and base affines must be 16-byte aligned");
+    }
+    if (n_out > 0) {
+        if (!out_positions || !alpha_out || !beta_out || !o_out || !lse_out)
+            return fail(ORTHROS_EINVAL, "out_positions, alpha_out, beta_out, o_out, lse_out must not be NULL");
+        if (!q_out && !q) return fail(ORTHROS_EINVAL, "output rows need q_out or the new tokens' q");
+        if (!aligned16(o_out) || (q_out && !aligned16(q_out)) || !aligned16(alpha_out) || !aligned16(beta_out))
+            return fail(ORTHROS_EINVAL, "output-row tensors and affines must be 16-byte aligned");
+    }
+    const ExtendLayout lay = extend_layout(B, n_new, n_out, Hq, Hkv, d, max_pages, page_size, dtype);
+    if (!workspace || workspace_bytes < lay.total)
+        return fail(ORTHROS_EWORKSPACE, "workspace needs %zu bytes, got %zu", lay.total,
+                    workspace ? workspace_bytes : (size_t)0);
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(ORTHROS_EINVAL, "workspace must be 256-byte aligned");
+    char *ws = static_cast<char *>(workspace);
+    uint32_t *status = reinterpret_cast<uint32_t *>(ws);
+    cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "status reset");
+    if (n_new + n_out == 0) return ORTHROS_OK;
+
+    // plan: both indptrs, then the split groups (bf16 fast path)
+    const int g = Hq / Hkv;
+    const long long kv_tokens = (long long)num_pages * page_size;
+    const bool fast = dtype == ORTHROS_BF16 && g <= 16 && page_size % 64 == 0 && kv_tokens < 0x7fffffffLL;
+    std::vector<int32_t> blob((size_t)2 * (B + 1));
+    std::copy(new_indptr, new_indptr + B + 1, blob.begin());
+    std::copy(out_indptr, out_indptr + B + 1, blob.begin() + B + 1);
+    int n_groups = 0, rows_per_group = 0;
+    if (fast) {
+        const int P = extend_positions_per_group(g);
+        for (int kind = 0; kind < 2; ++kind) {
+            const int32_t *ip = kind == 0 ? new_indptr : out_indptr;
+            for (int b = 0; b < B; ++b)
+                for (int kvh = 0; kvh < Hkv; ++kvh)
+                    for (int r0 = ip[b]; r0 < ip[b + 1]; r0 += P) {
+                        const int cnt = std::min(P, ip[b + 1] - r0);
+                        blob.push_back((b << 16) | kvh);
+                        blob.push_back(r0);
+                        blob.push_back(cnt | (kind << 30));
+                        rows_per_group = std::max(rows_per_group, cnt * g);
+                        ++n_groups;
+                    }
+        }
+        if (n_groups > lay.max_groups) return fail(ORTHROS_EWORKSPACE, "internal: extend groups exceed the plan");
+    }
+    int32_t *blob_dev = reinterpret_cast<int32_t *>(ws + lay.blob_off);
+    e = cudaMemcpyAsync(blob_dev, blob.data(), sizeof(int32_t) * blob.size(), cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "plan upload");
+    const int32_t *new_dev = blob_dev, *out_dev = blob_dev + B + 1, *groups_dev = blob_dev + 2 * (B + 1);
+    {
+        ProfScope ps("extend_append", stream);
+        e = launch_extend_append(k_new, v_new, k_cache, v_cache, block_table, cache_lens, new_dev, B, n_new, Hkv, d,
+                                 max_pages, page_size, num_pages, elem_bytes(dtype), status, stream);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "append launch");
+    if (fast) {
+        SplitParams sp{};
+        sp.mode = kSplitExtend;
+        sp.q = static_cast<const __nv_bfloat16 *>(q);
+        sp.q_out = static_cast<const __nv_bfloat16 *>(q_out);
+        sp.k = static_cast<const __nv_bfloat16 *>(k_cache);
+        sp.v = static_cast<const __nv_bfloat16 *>(v_cache);
+        sp.alpha_base = alpha_base;
+        sp.beta_base = beta_base;
+        sp.alpha_out = alpha_out;
+        sp.beta_out = beta_out;
+        sp.out_positions = out_positions;
+        sp.group_info = groups_dev;
+        sp.block_table = block_table;
+        sp.cache_lens = cache_lens;
+        sp.new_indptr = new_dev;
+        sp.n_new = n_new;
+        sp.max_pages = max_pages;
+        sp.page_size = page_size;
+        sp.num_pages = num_pages;
+        sp.B = B;
+        sp.Hq = Hq;
+        sp.Hkv = Hkv;
+        sp.window = window;
+        sp.scale = scale;
+        sp.scale_log2 = scale * 1.4426950408889634f;
+        sp.n_groups = n_groups;
+        sp.chunk = kDecodeChunk;
+        sp.max_chunks = lay.max_chunks;
+        sp.kv_tokens = kv_tokens;
+        sp.partial = reinterpret_cast<float *>(ws + lay.part_off);
+        sp.o_base = static_cast<__nv_bfloat16 *>(o_base);
+        sp.lse_base = lse_base;
+        sp.o_out = static_cast<__nv_bfloat16 *>(o_out);
+        sp.lse_out = lse_out;
+        sp.status = status;
+        ProfScope ps("splitkv_extend", stream);
+        e = launch_splitkv(sp, d, rows_per_group, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "split-KV extend launch");
+        return ORTHROS_OK;
+    }
+    RowsArgs a{};
+    a.q = q;
+    a.q_out = q_out;
+    a.k = k_cache;
+    a.v = v_cache;
+    a.alpha_base = alpha_base;
+    a.beta_base = beta_base;
+    a.alpha_out = alpha_out;
+    a.beta_out = beta_out;
+    a.out_indptr = out_dev;
+    a.out_positions = out_positions;
+    a.block_table = block_table;
+    a.cache_lens = cache_lens;
+    a.new_indptr = new_dev;
+    a.n_new = n_new;
+    a.n_out = n_out;
+    a.max_pages = max_pages;
+    a.page_size = page_size;
+    a.num_pages = num_pages;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.window = window;
+    a.scale = scale;
+    a.o_base = o_base;
+    a.lse_base = lse_base;
+    a.o_out = o_out;
+    a.lse_out = lse_out;
+    a.status = status;
+    if (n_new > 0) {
+        ProfScope ps("rows_simt_extend", stream);
+        if ((e = launch_rows_simt(a, kExtendBase, d, dtype, stream)) != cudaSuccess) return cuda_fail(e, "extend rows");
+    }
+    if (n_out > 0) {
+        ProfScope ps("rows_simt_extend_out", stream);
+        if ((e = launch_rows_simt(a, kExtendOut, d, dtype, stream)) != cudaSuccess) return cuda_fail(e, "extend rows");
+    }
     return ORTHROS_OK;
 }
 

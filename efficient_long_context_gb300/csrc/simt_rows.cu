@@ -125,6 +125,46 @@ __global__ void __launch_bounds__(256) rows_simt_kernel(RowsArgs a, int kind, lo
         lo = 0;
         hi = t;
         ka.base = (long long)b * a.T * a.Hkv * D + (long long)(h / g) * D;
+    } else if (kind == kExtendBase || kind == kExtendOut) {
+        // unit = (row, h): rows are new tokens (base) or output rows
+        h = (int)(unit % a.Hq);
+        const int r = (int)(unit / a.Hq);
+        const int32_t *ip = kind == kExtendBase ? a.new_indptr : a.out_indptr;
+        int lo_b = 0, hi_b = a.B - 1;  // sequence of row r
+        while (lo_b < hi_b) {
+            const int mid = (lo_b + hi_b + 1) >> 1;
+            if (ip[mid] <= r) lo_b = mid; else hi_b = mid - 1;
+        }
+        b = lo_b;
+        const int L = a.cache_lens[b];
+        const int len = L + (a.new_indptr[b + 1] - a.new_indptr[b]);
+        const long long row = (long long)r * a.Hq + h;
+        const bool base = kind == kExtendBase;
+        orow = reinterpret_cast<T *>(base ? a.o_base : a.o_out) + row * D;
+        lse_ptr = (base ? a.lse_base : a.lse_out) + row;
+        t = base ? L + (r - a.new_indptr[b]) : a.out_positions[r];
+        const bool bad_len = L < 0 || (long long)len > (long long)a.max_pages * a.page_size;
+        const bool bad_pos = !base && (t < 0 || t >= len || (!a.q_out && t < L));
+        if (bad_len || bad_pos) {
+            set_status(a.status, bad_len ? ORTHROS_DEV_BAD_LENGTH : ORTHROS_DEV_BAD_POSITION);
+            float nanv[E];
+#pragma unroll
+            for (int e = 0; e < E; ++e) nanv[e] = __int_as_float(0x7fc00000);
+            store_vec<T, E>(orow + lane * E, nanv);
+            if (lane == 0) *lse_ptr = __int_as_float(0x7fc00000);
+            return;
+        }
+        if (base) qrow = reinterpret_cast<const T *>(a.q) + row * D;
+        else if (a.q_out) qrow = reinterpret_cast<const T *>(a.q_out) + row * D;
+        else qrow = reinterpret_cast<const T *>(a.q) + ((long long)(a.new_indptr[b] + t - L) * a.Hq + h) * D;
+        alpha = (base ? a.alpha_base : a.alpha_out) + (long long)h * D;
+        beta = (base ? a.beta_base : a.beta_out) + (long long)h * D;
+        lo = base ? max(0, t - a.window + 1) : 0;
+        hi = t;
+        ka.bt = a.block_table + (long long)b * a.max_pages;
+        ka.page_size = a.page_size;
+        ka.num_pages = a.num_pages;
+        ka.base = (long long)(h / g) * D;
     } else {  // decoding pair: unit = (b, h, stream)
         const int stream = (int)(unit & 1);
         h = (int)((unit >> 1) % a.Hq);
@@ -204,7 +244,8 @@ template <typename T>
 cudaError_t launch_t(const RowsArgs &a, RowKind kind, int d, cudaStream_t stream) {
     long long n_units;
     if (kind == kPrefillBase) n_units = (long long)a.B * a.T * a.Hq;
-    else if (kind == kPrefillOut) n_units = (long long)a.n_out * a.Hq;
+    else if (kind == kPrefillOut || kind == kExtendOut) n_units = (long long)a.n_out * a.Hq;
+    else if (kind == kExtendBase) n_units = (long long)a.n_new * a.Hq;
     else n_units = (long long)a.B * a.Hq * 2;
     if (n_units == 0) return cudaSuccess;
     constexpr int kWarps = 8;

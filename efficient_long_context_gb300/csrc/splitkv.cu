@@ -411,7 +411,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const SplitParams p) {
     if (gw >= p.n_groups * kMaxRows) return;
     const int group = gw / kMaxRows, r = gw % kMaxRows;
     const int gsz = p.Hq / p.Hkv;
-    int b, kv, nrows, pos_base = 0;
+    int b, kv, nrows, pos_base = 0, kind = 0;
     if (p.mode == kSplitDecode) {
         b = group / p.Hkv;
         kv = group % p.Hkv;
@@ -421,13 +421,33 @@ __global__ void __launch_bounds__(256) combine_kernel(const SplitParams p) {
         b = gi >> 16;
         kv = gi & 0xffff;
         pos_base = p.group_info[3 * group + 1];
-        nrows = p.group_info[3 * group + 2] * gsz;
+        const int raw = p.group_info[3 * group + 2];
+        nrows = (raw & 0x3fffffff) * gsz;
+        kind = raw >> 30;
     }
     if (r >= nrows) return;
     int hi;
     __nv_bfloat16 *dst;
     float *lse_dst;
-    if (p.mode == kSplitDecode) {
+    if (p.mode == kSplitExtend) {
+        // the same validity rule as the split kernel's rows
+        const int pi = pos_base + r / gsz;
+        const int h = kv * gsz + r % gsz;
+        const int L = p.cache_lens[b];
+        const int len = extend_seq_len(p, b);
+        int t;
+        if (L < 0 || len > p.max_pages * p.page_size) {
+            t = -1;
+        } else if (kind == 0) {
+            t = L + (pi - p.new_indptr[b]);
+        } else {
+            t = p.out_positions[pi];
+            if (t < 0 || t >= len || (!p.q_out && t < L)) t = -1;
+        }
+        hi = t;
+        dst = (kind == 0 ? p.o_base : p.o_out) + ((long long)pi * p.Hq + h) * D;
+        lse_dst = (kind == 0 ? p.lse_base : p.lse_out) + (long long)pi * p.Hq + h;
+    } else if (p.mode == kSplitDecode) {
         const int L = p.cache_lens[b];
         hi = (L >= 0 && L / p.page_size < p.max_pages) ? L : -1;
         const bool base = r < gsz;
@@ -509,6 +529,7 @@ size_t split_partial_bytes(int n_groups, int max_chunks, int d) {
 cudaError_t launch_splitkv(const SplitParams &p, int d, int rows_per_group, cudaStream_t stream) {
     if (p.n_groups == 0 || p.max_chunks == 0) return cudaSuccess;
     cudaError_t e;
+    if (p.mode == kSplitExtend && !splitkv_tma_eligible(p)) return cudaErrorInvalidValue;  // TMA kernel only
     if (splitkv_tma_eligible(p)) {
         e = launch_splitkv_tma(p, d, rows_per_group, stream);
     } else {

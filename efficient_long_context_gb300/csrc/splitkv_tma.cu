@@ -64,8 +64,21 @@ __device__ __forceinline__ uint32_t stage_off(int r, int c) {
 // Rows of one work item (group): key range per row and where its query lives.
 struct ItemInfo {
     int b, kv, nrows, pos_base, L;
+    int kind;      // extend: 0 base rows of new tokens, 1 output rows
     int union_hi;  // last key any row needs (-1: none)
 };
+
+// Extend mode: position of row r of the item (-1 when the data make it impossible).
+__device__ __forceinline__ int extend_row_pos(const SplitParams &p, const ItemInfo &it, int r) {
+    const int gsz = p.Hq / p.Hkv;
+    const int pi = it.pos_base + r / gsz;
+    const int len = extend_seq_len(p, it.b);
+    if (it.L < 0 || len > p.max_pages * p.page_size) return -1;
+    if (it.kind == 0) return it.L + (pi - p.new_indptr[it.b]);
+    const int t = p.out_positions[pi];
+    if (t < 0 || t >= len || (!p.q_out && t < it.L)) return -1;
+    return t;
+}
 
 __device__ __forceinline__ ItemInfo item_info(const SplitParams &p, int group) {
     ItemInfo it{};
@@ -81,12 +94,19 @@ __device__ __forceinline__ ItemInfo item_info(const SplitParams &p, int group) {
         it.b = gi >> 16;
         it.kv = gi & 0xffff;
         it.pos_base = p.group_info[3 * group + 1];
-        const int npos = p.group_info[3 * group + 2];
+        const int raw = p.group_info[3 * group + 2];
+        const int npos = raw & 0x3fffffff;
+        it.kind = raw >> 30;
         it.nrows = npos * gsz;
         int hi = -1;
-        for (int i = 0; i < npos; ++i) {
-            const int t = p.out_positions[it.pos_base + i];
-            if (t >= 0 && t < p.T) hi = max(hi, t);
+        if (p.mode == kSplitExtend) {
+            it.L = p.cache_lens[it.b];
+            for (int i = 0; i < npos; ++i) hi = max(hi, extend_row_pos(p, it, i * gsz));
+        } else {
+            for (int i = 0; i < npos; ++i) {
+                const int t = p.out_positions[it.pos_base + i];
+                if (t >= 0 && t < p.T) hi = max(hi, t);
+            }
         }
         it.union_hi = hi;
     }
@@ -103,6 +123,12 @@ __device__ __forceinline__ void row_range(const SplitParams &p, const ItemInfo &
         if (it.union_hi < 0) return;
         hi = it.L;
         lo = r < gsz ? max(0, it.L - p.window + 1) : 0;
+    } else if (p.mode == kSplitExtend) {
+        const int t = extend_row_pos(p, it, r);
+        if (t >= 0) {
+            hi = t;
+            lo = it.kind == 0 ? max(0, t - p.window + 1) : 0;
+        }
     } else {
         const int t = p.out_positions[it.pos_base + r / gsz];
         if (t >= 0 && t < p.T) {
@@ -163,7 +189,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
             const int key_lo = chunk * p.chunk;
             const int key_hi = min(it.union_hi, key_lo + p.chunk - 1);
             if (key_lo > key_hi) continue;
-            const int32_t *bt = p.mode == kSplitDecode ? p.block_table + (long long)it.b * p.max_pages : nullptr;
+            const int32_t *bt = p.mode != kSplitPrefill ? p.block_table + (long long)it.b * p.max_pages : nullptr;
             for (int j0 = key_lo; j0 <= key_hi; j0 += kStageKeys, ++sc) {
                 const int st = sc % C::kStages;
                 if (sc >= (uint32_t)C::kStages &&
@@ -222,6 +248,9 @@ __global__ void __launch_bounds__(kThreadsT, 1)
             // report rows the data makes impossible (their combined outputs are NaN)
             if (p.mode == kSplitDecode) {
                 if (it.union_hi < 0 && tid == 0) set_status(p.status, ORTHROS_DEV_BAD_LENGTH);
+            } else if (p.mode == kSplitExtend) {
+                if (tid % gsz == 0 && extend_row_pos(p, it, tid) < 0)
+                    set_status(p.status, it.kind == 0 ? ORTHROS_DEV_BAD_LENGTH : ORTHROS_DEV_BAD_POSITION);
             } else if (tid % gsz == 0) {
                 const int t = p.out_positions[it.pos_base + tid / gsz];
                 if (t < 0 || t >= p.T) set_status(p.status, ORTHROS_DEV_BAD_POSITION);
@@ -251,6 +280,20 @@ __global__ void __launch_bounds__(kThreadsT, 1)
                     qrow = src + ((long long)it.b * p.Hq + h) * D;
                     al = (base ? p.alpha_base : p.alpha_out) + h * D;
                     be = (base ? p.beta_base : p.beta_out) + h * D;
+                } else if (p.mode == kSplitExtend) {
+                    const int pi = it.pos_base + r / gsz;
+                    const int h = it.kv * gsz + r % gsz;
+                    if (it.kind == 0) {
+                        qrow = p.q + ((long long)pi * p.Hq + h) * D;
+                    } else if (p.q_out) {
+                        qrow = p.q_out + ((long long)pi * p.Hq + h) * D;
+                    } else {  // the new token at the row's position (its first new token if the row is invalid)
+                        const int t = extend_row_pos(p, it, r);
+                        const int i = p.new_indptr[it.b] + (t >= 0 ? t - it.L : 0);
+                        qrow = p.q + ((long long)min(i, max(p.n_new - 1, 0)) * p.Hq + h) * D;
+                    }
+                    al = (it.kind == 0 ? p.alpha_base : p.alpha_out) + h * D;
+                    be = (it.kind == 0 ? p.beta_base : p.beta_out) + h * D;
                 } else {
                     const int pi = it.pos_base + r / gsz;
                     const int h = it.kv * gsz + r % gsz;
@@ -446,7 +489,7 @@ cudaError_t launch_t(const SplitParams &p, cudaStream_t stream) {
 }  // namespace
 
 bool splitkv_tma_eligible(const SplitParams &p) {
-    return p.chunk % kStageKeys == 0 && (p.mode != kSplitDecode || p.page_size % kBoxTokens == 0) &&
+    return p.chunk % kStageKeys == 0 && (p.mode == kSplitPrefill || p.page_size % kBoxTokens == 0) &&
            p.kv_tokens > 0 && p.kv_tokens < 0x7fffffffLL;
 }
 

@@ -210,3 +210,81 @@ def make_decode(w: DecodeWorkload, steps: int | None = None, seed: int | None = 
                        meta=dict(B=B, Hq=w.Hq, Hkv=w.Hkv, d=w.d, window=w.window, page_size=P,
                                  max_pages=max_pages, num_pages=num_pages, steps=steps,
                                  scale=w.scale, dtype=w.dtype))
+
+
+@dataclass(frozen=True)
+class ExtendWorkload:
+    """A continuous-batching step: histories in a paged cache, then per
+    sequence a number of new tokens (a prefill chunk, one decoding token or
+    none). Output rows: the last new token of every sequence that has one,
+    plus `history_rows` rows at earlier positions (these need q_out)."""
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    d: int
+    window: int
+    len_lo: int
+    len_hi: int
+    news: tuple
+    page_size: int = 64
+    dtype: torch.dtype = torch.bfloat16
+    history_rows: int = 0
+    seed: int = 0
+
+    @property
+    def scale(self) -> float:
+        return self.d ** -0.5
+
+
+# 32 sequences with 16K-32K cached tokens: 28 decode one token, 4 append a 16-token prefill chunk
+MIXED_32 = ExtendWorkload("mixed_b32_L16k-32k_gqa32x8_w4096_4x16+28x1", 32, 32, 8, 128, 4096, 16384, 32768,
+                          tuple([16] * 4 + [1] * 28), seed=1005)
+
+
+def make_extend(w: ExtendWorkload, with_q_out: bool = False, seed: int | None = None) -> dict:
+    """Draw one continuous-batching step (CPU tensors). Draw order: lengths,
+    page permutation, k_cache, v_cache, affines, q, k_new, v_new, history-row
+    positions, q_out."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(w.seed if seed is None else seed)
+    B, P = w.B, w.page_size
+    news = list(w.news)
+    assert len(news) == B
+    lens = torch.randint(w.len_lo, w.len_hi + 1, (B,), generator=gen, dtype=torch.int64)
+    pages_per = [max(1, (int(L) + n + P - 1) // P) for L, n in zip(lens, news)]
+    max_pages = max(pages_per)
+    num_pages = sum(pages_per)
+    perm = torch.randperm(num_pages, generator=gen).to(torch.int32)
+    block_table = torch.full((B, max_pages), -1, dtype=torch.int32)
+    at = 0
+    for b, n in enumerate(pages_per):
+        block_table[b, :n] = perm[at:at + n]
+        at += n
+    k_cache = _normal(gen, (num_pages, P, w.Hkv, w.d), w.dtype)
+    v_cache = _normal(gen, (num_pages, P, w.Hkv, w.d), w.dtype)
+    ab, bb, ao, bo = make_affines(gen, w.Hq, w.d)
+    new_indptr = torch.zeros(B + 1, dtype=torch.int32)
+    new_indptr[1:] = torch.cumsum(torch.tensor(news), 0)
+    n_new = int(new_indptr[-1])
+    q = _normal(gen, (n_new, w.Hq, w.d), w.dtype)
+    k_new = _normal(gen, (n_new, w.Hkv, w.d), w.dtype)
+    v_new = _normal(gen, (n_new, w.Hkv, w.d), w.dtype)
+    lists = []
+    for b in range(B):
+        L, n = int(lens[b]), news[b]
+        rows = [L + n - 1] if n else []
+        if w.history_rows and with_q_out:
+            hist = torch.randint(0, max(L + n, 1), (w.history_rows,), generator=gen).tolist()
+            rows = sorted(rows + hist)
+        lists.append(rows)
+    out_indptr = torch.zeros(B + 1, dtype=torch.int32)
+    out_indptr[1:] = torch.cumsum(torch.tensor([len(r) for r in lists]), 0)
+    out_positions = torch.tensor([t for r in lists for t in r], dtype=torch.int32)
+    n_out = int(out_indptr[-1])
+    q_out = _normal(gen, (n_out, w.Hq, w.d), w.dtype) if with_q_out else None
+    return dict(k_cache=k_cache, v_cache=v_cache, block_table=block_table, cache_lens=lens.to(torch.int32),
+                new_indptr=new_indptr, out_indptr=out_indptr, out_positions=out_positions, q=q, k_new=k_new,
+                v_new=v_new, q_out=q_out, alpha_base=ab, beta_base=bb, alpha_out=ao, beta_out=bo,
+                B=B, Hq=w.Hq, Hkv=w.Hkv, d=w.d, window=w.window, scale=w.scale, dtype=w.dtype,
+                page_size=P, max_pages=max_pages, num_pages=num_pages)

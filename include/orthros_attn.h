@@ -201,6 +201,52 @@ ORTHROS_API orthros_status orthros_decode(
     void *o_base, float *lse_base, void *o_out, float *lse_out,
     void *workspace, size_t workspace_bytes, orthros_stream_t stream);
 
+/* Workspace bytes orthros_extend needs for these sizes (0 if rejected). */
+ORTHROS_API size_t orthros_extend_workspace_size(int B, int n_new, int n_out, int Hq, int Hkv, int d,
+                                     int max_pages, int page_size, orthros_dtype dtype);
+
+/*
+ * One continuous-batching step over the paged cache: a batch in which some
+ * sequences append a prefill chunk, others decode one token, others nothing.
+ * Sec. 3.2 runs every regime as the same computation (a prefill followed by
+ * decoding steps agrees exactly with one longer prefill), so one call serves
+ * them all; orthros_decode is the case of one new token per sequence.
+ *
+ * Sequence b (L = cache_lens[b]) appends its n_b = new_indptr[b+1] -
+ * new_indptr[b] new tokens (rows new_indptr[b] .. of q, k_new, v_new) at
+ * positions L .. L + n_b - 1 of its pages, then
+ *   - every new token's base row attends keys max(0, t-w+1) .. t (Eq. 4);
+ *   - every output row r (out_indptr[b] <= r < out_indptr[b+1]) at position
+ *     out_positions[r] = t in [0, L + n_b) attends keys 0 .. t (Eq. 5), with
+ *     raw query q_out[r], or, when q_out is NULL, the q of the new token at
+ *     position t (t must then be a new position).
+ *
+ * q            [n_new, Hq, d] raw base queries of the new tokens
+ * q_out        [n_out, Hq, d] raw output queries, or NULL (see above)
+ * k_new, v_new [n_new, Hkv, d]
+ * k_cache, v_cache [num_pages, page_size, Hkv, d] (modified: the appends)
+ * block_table  [B, max_pages] int32; pages for positions < L + n_b must exist
+ * cache_lens   [B] int32 device, lengths BEFORE the step (read only)
+ * new_indptr, out_indptr  HOST [B+1] int32, start at 0, non-decreasing
+ * out_positions [n_out] int32 device, absolute positions
+ * o_base [n_new, Hq, d], lse_base [n_new, Hq], o_out [n_out, Hq, d],
+ * lse_out [n_out, Hq] float
+ * workspace    at least orthros_extend_workspace_size() bytes, 256-byte aligned
+ * Rows whose data are impossible (a position outside its sequence, a length
+ * past the block table) set ORTHROS_DEV_BAD_POSITION / _BAD_LENGTH and come
+ * back as NaN; a page id outside [0, num_pages) sets ORTHROS_DEV_BAD_PAGE.
+ */
+ORTHROS_API orthros_status orthros_extend(
+    const void *q, const void *q_out, const void *k_new, const void *v_new,
+    void *k_cache, void *v_cache, const int32_t *block_table, int max_pages,
+    int page_size, int num_pages, const int32_t *cache_lens,
+    const int32_t *new_indptr, const int32_t *out_indptr, const int32_t *out_positions,
+    const float *alpha_base, const float *beta_base,
+    const float *alpha_out, const float *beta_out,
+    int B, int Hq, int Hkv, int d, int window, float scale, orthros_dtype dtype,
+    void *o_base, float *lse_base, void *o_out, float *lse_out,
+    void *workspace, size_t workspace_bytes, orthros_stream_t stream);
+
 /*
  * orthros_decode without a workspace argument, for callers that cannot
  * allocate device memory where they run a decoding step (for example a host

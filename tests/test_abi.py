@@ -145,6 +145,35 @@ def test_backward_workspace_size(lib):
     assert ola.orthros_prefill_backward_workspace_size(2, 64, 4, 2, 128, -1, 16) == 0
 
 
+def test_extend_host_checks(lib):
+    P = 1 << 12
+    ni = (ctypes.c_int32 * 3)(0, 2, 3)
+    oi = (ctypes.c_int32 * 3)(0, 1, 1)
+
+    def call(**over):
+        a = dict(q=P, q_out=None, kn=P, vn=P, kc=P, vc=P, bt=P, max_pages=4, page_size=64, num_pages=8, lens=P,
+                 ni=ni, oi=oi, pos=P, ab=P, bb=P, ao=P, bo=P, B=2, Hq=4, Hkv=2, d=128, w=16, scale=0.1, dtype=0,
+                 ob=P, lb=P, oo=P, lo=P, ws=P, ws_bytes=1 << 30, stream=None)
+        a.update(over)
+        return lib.orthros_extend(a["q"], a["q_out"], a["kn"], a["vn"], a["kc"], a["vc"], a["bt"], a["max_pages"],
+                                  a["page_size"], a["num_pages"], a["lens"], a["ni"], a["oi"], a["pos"], a["ab"],
+                                  a["bb"], a["ao"], a["bo"], a["B"], a["Hq"], a["Hkv"], a["d"], a["w"], a["scale"],
+                                  a["dtype"], a["ob"], a["lb"], a["oo"], a["lo"], a["ws"], a["ws_bytes"], a["stream"])
+
+    assert call(Hq=3) == 1
+    assert call(d=96) == 2
+    assert call(max_pages=0) == 1
+    assert call(ni=(ctypes.c_int32 * 3)(1, 2, 3)) == 1  # indptr[0] != 0
+    assert call(oi=(ctypes.c_int32 * 3)(0, 2, 1)) == 1  # decreasing
+    assert call(kn=None) == 1
+    assert call(pos=None) == 1
+    assert call(q=(1 << 12) + 2) == 1
+    assert call(ws=None) == 4
+    assert call(ws_bytes=8) == 4
+    assert ola.orthros_extend_workspace_size(2, 3, 1, 4, 2, 128, 4, 64) > 0
+    assert ola.orthros_extend_workspace_size(2, 3, 1, 4, 2, 96, 4, 64) == 0
+
+
 def test_product_path_fails_loudly_without_library(tmp_path):
     with pytest.raises(ola.OrthrosError):
         ola.load_library(str(tmp_path / "missing.so"))
