@@ -107,11 +107,14 @@ struct SplitParams {
     const __nv_bfloat16 *k, *v;      // prefill [B,T,Hkv,d]; decode caches [num_pages,P,Hkv,d]
     const float *alpha_base, *beta_base, *alpha_out, *beta_out;
     const int32_t *out_positions;    // prefill
-    const int32_t *group_info;       // prefill / extend: 3 ints per group (b<<16 | kv, first row,
-                                     // positions | kind << 30; kind (extend): 0 new-token base rows, 1 output rows)
+    const int32_t *group_info;       // prefill: 3 ints per group (b<<16 | kv, first row, positions)
+    const int32_t *ext_info;         // extend: 4 ints per group (b<<16 | kv, first new-token row,
+                                     // first output row, n_base | n_out << 16): positions of the group are
+                                     // its n_base new tokens' base rows, then its n_out output rows
     const int32_t *block_table, *cache_lens;  // decode / extend
     const int32_t *new_indptr;                // extend: device [B+1]
     int n_new;                                // extend: rows of q / k_new / v_new
+    int group_offset;                         // first group of this launch (the partial buffer is shared)
     int max_pages, page_size, num_pages;
     int B, T, Hq, Hkv, window;
     float scale, scale_log2;
@@ -124,13 +127,30 @@ struct SplitParams {
     float *lse_out;
     uint32_t *status;
 };
-// Row of an extend-mode group: position and whether it may be computed.
-__device__ __forceinline__ int extend_seq_len(const SplitParams &p, int b) {
-    return p.cache_lens[b] + (p.new_indptr[b + 1] - p.new_indptr[b]);
+// Position index pidx of an extend-mode group (b, L = cache_lens[b]): sets
+// kind (0 base row of a new token, 1 output row) and idx (new-token row or
+// output row) and returns the position, or -1 when the data make the row
+// impossible (length past the block table, output position outside the
+// sequence, or a history position without q_out).
+__device__ __forceinline__ int extend_position(const SplitParams &p, int group, int b, int L, int pidx, int &kind,
+                                               int &idx) {
+    const int *e = p.ext_info + 4 * group;
+    const int n_base = e[3] & 0xffff;
+    const int len = L + (p.new_indptr[b + 1] - p.new_indptr[b]);
+    kind = pidx < n_base ? 0 : 1;
+    idx = kind == 0 ? e[1] + pidx : e[2] + (pidx - n_base);
+    if (L < 0 || (long long)len > (long long)p.max_pages * p.page_size) return -1;
+    if (kind == 0) return L + (idx - p.new_indptr[b]);
+    const int t = p.out_positions[idx];
+    if (t < 0 || t >= len || (!p.q_out && t < L)) return -1;
+    return t;
 }
 size_t split_partial_bytes(int n_groups, int max_chunks, int d);
 // Runs the split kernel (the TMA-fed persistent one when eligible) and the combine.
 cudaError_t launch_splitkv(const SplitParams &p, int d, int rows_per_group, cudaStream_t stream);
+// Extend mode: groups [0, n_small) have at most 8 rows, the rest at most 16;
+// one TMA launch for each class, then the combine over all p.n_groups groups.
+cudaError_t launch_splitkv_extend(const SplitParams &p, int d, int n_small, cudaStream_t stream);
 // splitkv_tma.cu
 bool splitkv_tma_eligible(const SplitParams &p);
 cudaError_t launch_splitkv_tma(const SplitParams &p, int d, int rows_per_group, cudaStream_t stream);

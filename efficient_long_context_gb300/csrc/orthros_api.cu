@@ -122,20 +122,17 @@ struct ExtendLayout {
     int max_groups, max_chunks;
 };
 
-// Rows per split group: P positions of a sequence x the g query heads of a kv head.
-int extend_positions_per_group(int g) { return g <= 16 ? std::max(1, 16 / g) : 1; }
-
 ExtendLayout extend_layout(int B, int n_new, int n_out, int Hq, int Hkv, int d, int max_pages, int page_size,
                            orthros_dtype dtype) {
     ExtendLayout L{};
-    const int P = extend_positions_per_group(Hq / Hkv);
+    (void)Hq;
     size_t at = kStatusBytes;
-    // every sequence's rows are cut into groups of P positions, per kv head
-    const long long groups = ((long long)(n_new + P - 1) / P + (long long)(n_out + P - 1) / P + 2LL * B) * Hkv;
+    // at most one group per position of each (sequence, kv head), plus one partial group per class
+    const long long groups = ((long long)n_new + n_out + 2LL * B) * Hkv;
     L.max_groups = dtype == ORTHROS_BF16 ? (int)std::min<long long>(groups, 1LL << 30) : 0;
     L.max_chunks = ceil_div((long long)max_pages * page_size, kDecodeChunk);
     L.blob_off = at;
-    at += align_up(sizeof(int32_t) * (size_t)(2 * (B + 1) + 3 * (size_t)L.max_groups), 256);
+    at += align_up(sizeof(int32_t) * (size_t)(2 * (B + 1) + 4 * (size_t)L.max_groups), 256);
     L.part_off = at;
     at += align_up(split_partial_bytes(L.max_groups, L.max_chunks, d), 256);
     L.total = at;
@@ -627,22 +624,39 @@ orthros_status orthros_extend(const void *q, const void *q_out, const void *k_ne
     std::vector<int32_t> blob((size_t)2 * (B + 1));
     std::copy(new_indptr, new_indptr + B + 1, blob.begin());
     std::copy(out_indptr, out_indptr + B + 1, blob.begin() + B + 1);
-    int n_groups = 0, rows_per_group = 0;
+    // Groups of one (sequence, kv head): all its positions in one group when
+    // they fit 8 rows (a decoding token's base and output rows then share one
+    // pass over the cache); otherwise new-token base rows in groups of up to
+    // 16 rows (neighbouring windows overlap) and output rows in groups of up
+    // to 8. Groups of <= 8 rows come first (their own launch).
+    int n_groups = 0, n_small = 0;
     if (fast) {
-        const int P = extend_positions_per_group(g);
-        for (int kind = 0; kind < 2; ++kind) {
-            const int32_t *ip = kind == 0 ? new_indptr : out_indptr;
-            for (int b = 0; b < B; ++b)
-                for (int kvh = 0; kvh < Hkv; ++kvh)
-                    for (int r0 = ip[b]; r0 < ip[b + 1]; r0 += P) {
-                        const int cnt = std::min(P, ip[b + 1] - r0);
-                        blob.push_back((b << 16) | kvh);
-                        blob.push_back(r0);
-                        blob.push_back(cnt | (kind << 30));
-                        rows_per_group = std::max(rows_per_group, cnt * g);
-                        ++n_groups;
-                    }
+        std::vector<int32_t> small, big;
+        auto add = [&](std::vector<int32_t> &v, int b, int kvh, int base0, int nb, int out0, int no) {
+            v.push_back((b << 16) | kvh);
+            v.push_back(base0);
+            v.push_back(out0);
+            v.push_back(nb | (no << 16));
+        };
+        const int p8 = std::max(1, 8 / g), p16 = 16 / g;
+        for (int b = 0; b < B; ++b) {
+            const int nb = new_indptr[b + 1] - new_indptr[b], no = out_indptr[b + 1] - out_indptr[b];
+            for (int kvh = 0; kvh < Hkv; ++kvh) {
+                if (nb + no == 0) continue;
+                if (g <= 8 && (nb + no) * g <= 8) {
+                    add(small, b, kvh, new_indptr[b], nb, out_indptr[b], no);
+                    continue;
+                }
+                for (int i = 0; i < nb; i += p16)
+                    add(big, b, kvh, new_indptr[b] + i, std::min(p16, nb - i), out_indptr[b], 0);
+                for (int i = 0; i < no; i += p8)
+                    add(g <= 8 ? small : big, b, kvh, new_indptr[b], 0, out_indptr[b] + i, std::min(p8, no - i));
+            }
         }
+        n_small = (int)small.size() / 4;
+        n_groups = n_small + (int)big.size() / 4;
+        blob.insert(blob.end(), small.begin(), small.end());
+        blob.insert(blob.end(), big.begin(), big.end());
         if (n_groups > lay.max_groups) return fail(ORTHROS_EWORKSPACE, "internal: extend groups exceed the plan");
     }
     int32_t *blob_dev = reinterpret_cast<int32_t *>(ws + lay.blob_off);
@@ -667,7 +681,7 @@ orthros_status orthros_extend(const void *q, const void *q_out, const void *k_ne
         sp.alpha_out = alpha_out;
         sp.beta_out = beta_out;
         sp.out_positions = out_positions;
-        sp.group_info = groups_dev;
+        sp.ext_info = groups_dev;
         sp.block_table = block_table;
         sp.cache_lens = cache_lens;
         sp.new_indptr = new_dev;
@@ -692,7 +706,7 @@ orthros_status orthros_extend(const void *q, const void *q_out, const void *k_ne
         sp.lse_out = lse_out;
         sp.status = status;
         ProfScope ps("splitkv_extend", stream);
-        e = launch_splitkv(sp, d, rows_per_group, stream);
+        e = launch_splitkv_extend(sp, d, n_small, stream);
         if (e != cudaSuccess) return cuda_fail(e, "split-KV extend launch");
         return ORTHROS_OK;
     }

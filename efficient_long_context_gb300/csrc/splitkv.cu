@@ -411,19 +411,22 @@ __global__ void __launch_bounds__(256) combine_kernel(const SplitParams p) {
     if (gw >= p.n_groups * kMaxRows) return;
     const int group = gw / kMaxRows, r = gw % kMaxRows;
     const int gsz = p.Hq / p.Hkv;
-    int b, kv, nrows, pos_base = 0, kind = 0;
+    int b, kv, nrows, pos_base = 0;
     if (p.mode == kSplitDecode) {
         b = group / p.Hkv;
         kv = group % p.Hkv;
         nrows = 2 * gsz;
+    } else if (p.mode == kSplitExtend) {
+        const int *e = p.ext_info + 4 * group;
+        b = e[0] >> 16;
+        kv = e[0] & 0xffff;
+        nrows = ((e[3] & 0xffff) + (e[3] >> 16)) * gsz;
     } else {
         const int gi = p.group_info[3 * group];
         b = gi >> 16;
         kv = gi & 0xffff;
         pos_base = p.group_info[3 * group + 1];
-        const int raw = p.group_info[3 * group + 2];
-        nrows = (raw & 0x3fffffff) * gsz;
-        kind = raw >> 30;
+        nrows = p.group_info[3 * group + 2] * gsz;
     }
     if (r >= nrows) return;
     int hi;
@@ -431,22 +434,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const SplitParams p) {
     float *lse_dst;
     if (p.mode == kSplitExtend) {
         // the same validity rule as the split kernel's rows
-        const int pi = pos_base + r / gsz;
         const int h = kv * gsz + r % gsz;
-        const int L = p.cache_lens[b];
-        const int len = extend_seq_len(p, b);
-        int t;
-        if (L < 0 || len > p.max_pages * p.page_size) {
-            t = -1;
-        } else if (kind == 0) {
-            t = L + (pi - p.new_indptr[b]);
-        } else {
-            t = p.out_positions[pi];
-            if (t < 0 || t >= len || (!p.q_out && t < L)) t = -1;
-        }
-        hi = t;
-        dst = (kind == 0 ? p.o_base : p.o_out) + ((long long)pi * p.Hq + h) * D;
-        lse_dst = (kind == 0 ? p.lse_base : p.lse_out) + (long long)pi * p.Hq + h;
+        int kind, idx;
+        hi = extend_position(p, group, b, p.cache_lens[b], r / gsz, kind, idx);
+        dst = (kind == 0 ? p.o_base : p.o_out) + ((long long)idx * p.Hq + h) * D;
+        lse_dst = (kind == 0 ? p.lse_base : p.lse_out) + (long long)idx * p.Hq + h;
     } else if (p.mode == kSplitDecode) {
         const int L = p.cache_lens[b];
         hi = (L >= 0 && L / p.page_size < p.max_pages) ? L : -1;
@@ -522,6 +514,24 @@ cudaError_t launch_combine_t(const SplitParams &p, cudaStream_t stream) {
 
 }  // namespace
 
+cudaError_t launch_splitkv_extend(const SplitParams &p, int d, int n_small, cudaStream_t stream) {
+    if (p.n_groups == 0 || p.max_chunks == 0) return cudaSuccess;
+    if (!splitkv_tma_eligible(p)) return cudaErrorInvalidValue;
+    cudaError_t e;
+    SplitParams q = p;
+    if (n_small > 0) {
+        q.group_offset = 0;
+        q.n_groups = n_small;
+        if ((e = launch_splitkv_tma(q, d, 8, stream)) != cudaSuccess) return e;
+    }
+    if (p.n_groups > n_small) {
+        q.group_offset = n_small;
+        q.n_groups = p.n_groups - n_small;
+        if ((e = launch_splitkv_tma(q, d, 16, stream)) != cudaSuccess) return e;
+    }
+    return d == 128 ? launch_combine_t<128>(p, stream) : launch_combine_t<64>(p, stream);
+}
+
 size_t split_partial_bytes(int n_groups, int max_chunks, int d) {
     return (size_t)n_groups * max_chunks * kMaxRows * (d + 2) * sizeof(float);
 }
@@ -529,7 +539,7 @@ size_t split_partial_bytes(int n_groups, int max_chunks, int d) {
 cudaError_t launch_splitkv(const SplitParams &p, int d, int rows_per_group, cudaStream_t stream) {
     if (p.n_groups == 0 || p.max_chunks == 0) return cudaSuccess;
     cudaError_t e;
-    if (p.mode == kSplitExtend && !splitkv_tma_eligible(p)) return cudaErrorInvalidValue;  // TMA kernel only
+    if (p.mode == kSplitExtend) return cudaErrorInvalidValue;  // launch_splitkv_extend
     if (splitkv_tma_eligible(p)) {
         e = launch_splitkv_tma(p, d, rows_per_group, stream);
     } else {

@@ -64,49 +64,41 @@ __device__ __forceinline__ uint32_t stage_off(int r, int c) {
 // Rows of one work item (group): key range per row and where its query lives.
 struct ItemInfo {
     int b, kv, nrows, pos_base, L;
-    int kind;      // extend: 0 base rows of new tokens, 1 output rows
+    int group;     // global group index (extend rows are looked up through it)
     int union_hi;  // last key any row needs (-1: none)
 };
-
-// Extend mode: position of row r of the item (-1 when the data make it impossible).
-__device__ __forceinline__ int extend_row_pos(const SplitParams &p, const ItemInfo &it, int r) {
-    const int gsz = p.Hq / p.Hkv;
-    const int pi = it.pos_base + r / gsz;
-    const int len = extend_seq_len(p, it.b);
-    if (it.L < 0 || len > p.max_pages * p.page_size) return -1;
-    if (it.kind == 0) return it.L + (pi - p.new_indptr[it.b]);
-    const int t = p.out_positions[pi];
-    if (t < 0 || t >= len || (!p.q_out && t < it.L)) return -1;
-    return t;
-}
 
 __device__ __forceinline__ ItemInfo item_info(const SplitParams &p, int group) {
     ItemInfo it{};
     const int gsz = p.Hq / p.Hkv;
+    it.group = group;
     if (p.mode == kSplitDecode) {
         it.b = group / p.Hkv;
         it.kv = group % p.Hkv;
         it.nrows = 2 * gsz;
         it.L = p.cache_lens[it.b];
         it.union_hi = (it.L >= 0 && it.L / p.page_size < p.max_pages) ? it.L : -1;
+    } else if (p.mode == kSplitExtend) {
+        const int *e = p.ext_info + 4 * group;
+        it.b = e[0] >> 16;
+        it.kv = e[0] & 0xffff;
+        const int npos = (e[3] & 0xffff) + (e[3] >> 16);
+        it.nrows = npos * gsz;
+        it.L = p.cache_lens[it.b];
+        int hi = -1, kind, idx;
+        for (int i = 0; i < npos; ++i) hi = max(hi, extend_position(p, group, it.b, it.L, i, kind, idx));
+        it.union_hi = hi;
     } else {
         const int gi = p.group_info[3 * group];
         it.b = gi >> 16;
         it.kv = gi & 0xffff;
         it.pos_base = p.group_info[3 * group + 1];
-        const int raw = p.group_info[3 * group + 2];
-        const int npos = raw & 0x3fffffff;
-        it.kind = raw >> 30;
+        const int npos = p.group_info[3 * group + 2];
         it.nrows = npos * gsz;
         int hi = -1;
-        if (p.mode == kSplitExtend) {
-            it.L = p.cache_lens[it.b];
-            for (int i = 0; i < npos; ++i) hi = max(hi, extend_row_pos(p, it, i * gsz));
-        } else {
-            for (int i = 0; i < npos; ++i) {
-                const int t = p.out_positions[it.pos_base + i];
-                if (t >= 0 && t < p.T) hi = max(hi, t);
-            }
+        for (int i = 0; i < npos; ++i) {
+            const int t = p.out_positions[it.pos_base + i];
+            if (t >= 0 && t < p.T) hi = max(hi, t);
         }
         it.union_hi = hi;
     }
@@ -124,10 +116,11 @@ __device__ __forceinline__ void row_range(const SplitParams &p, const ItemInfo &
         hi = it.L;
         lo = r < gsz ? max(0, it.L - p.window + 1) : 0;
     } else if (p.mode == kSplitExtend) {
-        const int t = extend_row_pos(p, it, r);
+        int kind, idx;
+        const int t = extend_position(p, it.group, it.b, it.L, r / gsz, kind, idx);
         if (t >= 0) {
             hi = t;
-            lo = it.kind == 0 ? max(0, t - p.window + 1) : 0;
+            lo = kind == 0 ? max(0, t - p.window + 1) : 0;
         }
     } else {
         const int t = p.out_positions[it.pos_base + r / gsz];
@@ -184,7 +177,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         if (lane != 0) return;
         uint32_t sc = 0;  // stages issued so far
         for (int item = blockIdx.x; item < total_items && !*abort; item += gridDim.x) {
-            const int group = item / p.max_chunks, chunk = item % p.max_chunks;
+            const int group = p.group_offset + item / p.max_chunks, chunk = item % p.max_chunks;
             const ItemInfo it = item_info(p, group);
             const int key_lo = chunk * p.chunk;
             const int key_hi = min(it.union_hi, key_lo + p.chunk - 1);
@@ -239,7 +232,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         return __all_sync(0xffffffffu, got);
     };
     for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
-        const int group = item / p.max_chunks, chunk = item % p.max_chunks;
+        const int group = p.group_offset + item / p.max_chunks, chunk = item % p.max_chunks;
         const ItemInfo it = item_info(p, group);
         const int key_lo = chunk * p.chunk;
         const int key_hi = min(it.union_hi, key_lo + p.chunk - 1);
@@ -249,8 +242,9 @@ __global__ void __launch_bounds__(kThreadsT, 1)
             if (p.mode == kSplitDecode) {
                 if (it.union_hi < 0 && tid == 0) set_status(p.status, ORTHROS_DEV_BAD_LENGTH);
             } else if (p.mode == kSplitExtend) {
-                if (tid % gsz == 0 && extend_row_pos(p, it, tid) < 0)
-                    set_status(p.status, it.kind == 0 ? ORTHROS_DEV_BAD_LENGTH : ORTHROS_DEV_BAD_POSITION);
+                int kind, idx;
+                if (tid % gsz == 0 && extend_position(p, group, it.b, it.L, tid / gsz, kind, idx) < 0)
+                    set_status(p.status, (it.L < 0 || kind == 0) ? ORTHROS_DEV_BAD_LENGTH : ORTHROS_DEV_BAD_POSITION);
             } else if (tid % gsz == 0) {
                 const int t = p.out_positions[it.pos_base + tid / gsz];
                 if (t < 0 || t >= p.T) set_status(p.status, ORTHROS_DEV_BAD_POSITION);
@@ -281,19 +275,19 @@ __global__ void __launch_bounds__(kThreadsT, 1)
                     al = (base ? p.alpha_base : p.alpha_out) + h * D;
                     be = (base ? p.beta_base : p.beta_out) + h * D;
                 } else if (p.mode == kSplitExtend) {
-                    const int pi = it.pos_base + r / gsz;
                     const int h = it.kv * gsz + r % gsz;
-                    if (it.kind == 0) {
-                        qrow = p.q + ((long long)pi * p.Hq + h) * D;
+                    int kind, idx;
+                    const int t = extend_position(p, it.group, it.b, it.L, r / gsz, kind, idx);
+                    if (kind == 0) {
+                        qrow = p.q + ((long long)idx * p.Hq + h) * D;
                     } else if (p.q_out) {
-                        qrow = p.q_out + ((long long)pi * p.Hq + h) * D;
+                        qrow = p.q_out + ((long long)idx * p.Hq + h) * D;
                     } else {  // the new token at the row's position (its first new token if the row is invalid)
-                        const int t = extend_row_pos(p, it, r);
                         const int i = p.new_indptr[it.b] + (t >= 0 ? t - it.L : 0);
                         qrow = p.q + ((long long)min(i, max(p.n_new - 1, 0)) * p.Hq + h) * D;
                     }
-                    al = (it.kind == 0 ? p.alpha_base : p.alpha_out) + h * D;
-                    be = (it.kind == 0 ? p.beta_base : p.beta_out) + h * D;
+                    al = (kind == 0 ? p.alpha_base : p.alpha_out) + h * D;
+                    be = (kind == 0 ? p.beta_base : p.beta_out) + h * D;
                 } else {
                     const int pi = it.pos_base + r / gsz;
                     const int h = it.kv * gsz + r % gsz;
