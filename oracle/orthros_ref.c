@@ -512,6 +512,83 @@ int orthros_ref_extend(const float *q, const float *q_out, const float *k_new,
 }
 
 /*
+ * The projection feeding the hot path (Alg. 1 lines 4-5; Sec. 3.1): the base
+ * tokens' hidden rows x and the output tokens' rows x' go through one shared
+ * Q/K/V weight, y = x W (W [d_model, (Hq + 2 Hkv) d] stored transposed as
+ * w_t [(Hq + 2 Hkv) d, d_model]); the query part gets its stream's affine,
+ * q = alpha (.) y_Q + beta, and the base tokens' K/V parts are the cache
+ * entries (only the base stream writes the cache). Rows 0 .. n_base-1 of x
+ * are base tokens, rows n_base .. n_base+n_out-1 output tokens.
+ * Outputs (double): q_base [n_base,Hq,d], q_out [n_out,Hq,d], k, v
+ * [n_base,Hkv,d]; when k_cache is given, base row i is also written (as float)
+ * to page block_table[token_seq[i]][token_pos[i] / page_size], slot
+ * token_pos[i] % page_size.
+ */
+int orthros_ref_qkv_project(const float *x, int n_base, int n_out, int d_model,
+                            const float *w_t, int Hq, int Hkv, int d,
+                            const float *alpha_base, const float *beta_base,
+                            const float *alpha_out, const float *beta_out,
+                            double *q_base, double *q_out, double *k, double *v,
+                            float *k_cache, float *v_cache, const int32_t *block_table,
+                            int max_pages, int page_size, int num_pages,
+                            const int32_t *token_seq, const int32_t *token_pos, int nthreads)
+{
+    if (n_base < 0 || n_out < 0 || d_model < 1 || Hq < 1 || Hkv < 1 || d < 1)
+        return REF_EINVAL;
+    const int Nq = Hq * d, Nkv = Hkv * d, N = Nq + 2 * Nkv;
+    if (k_cache) {
+        for (int i = 0; i < n_base; ++i) {
+            const int t = token_pos[i];
+            if (t < 0 || t / page_size >= max_pages)
+                return REF_EINVAL;
+            const int pg = block_table[(size_t)token_seq[i] * max_pages + t / page_size];
+            if (pg < 0 || pg >= num_pages)
+                return REF_EINVAL;
+        }
+    }
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    const long long rows = (long long)n_base + n_out;
+#pragma omp parallel for schedule(dynamic, 4)
+    for (long long r = 0; r < rows; ++r) {
+        const int base = r < n_base;
+        const float *xr = x + (size_t)r * d_model;
+        for (int j = 0; j < (base ? N : Nq); ++j) {
+            const float *wj = w_t + (size_t)j * d_model;
+            double y = 0.0;
+            for (int c = 0; c < d_model; ++c)
+                y += (double)xr[c] * (double)wj[c];
+            if (j < Nq) {
+                if (base)
+                    q_base[(size_t)r * Nq + j] = (double)alpha_base[j] * y + (double)beta_base[j];
+                else
+                    q_out[(size_t)(r - n_base) * Nq + j] = (double)alpha_out[j] * y + (double)beta_out[j];
+            } else if (j < Nq + Nkv) {
+                k[(size_t)r * Nkv + (j - Nq)] = y;
+            } else {
+                v[(size_t)r * Nkv + (j - Nq - Nkv)] = y;
+            }
+        }
+    }
+    if (k_cache) {
+        for (int i = 0; i < n_base; ++i) {
+            const int t = token_pos[i];
+            const int pg = block_table[(size_t)token_seq[i] * max_pages + t / page_size];
+            const size_t off = ((size_t)pg * page_size + t % page_size) * (size_t)Nkv;
+            for (int c = 0; c < Nkv; ++c) {
+                k_cache[off + c] = (float)k[(size_t)i * Nkv + c];
+                v_cache[off + c] = (float)v[(size_t)i * Nkv + c];
+            }
+        }
+    }
+    return REF_OK;
+}
+
+/*
  * Gradient of one query row's output (Eq. 4 / Eq. 5) given dO: recomputes the
  * row's exact softmax in double, then
  *   D = dO . o,  dp_j = dO . v_j,  ds_j = p_j (dp_j - D),

@@ -67,6 +67,14 @@ def _bind(path):
         _f64p, _f64p, _f64p, _f64p,
         ctypes.c_int,
     ]
+    lib.orthros_ref_qkv_project.restype = ctypes.c_int
+    lib.orthros_ref_qkv_project.argtypes = [
+        _f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        _f32p, _f32p, _f32p, _f32p,
+        _f64p, _f64p, _f64p, _f64p,
+        _f32p, _f32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _i32p, _i32p,
+        ctypes.c_int,
+    ]
     lib.orthros_ref_extend.restype = ctypes.c_int
     lib.orthros_ref_extend.argtypes = [
         _f32p, _f32p, _f32p, _f32p,  # q q_out k_new v_new
@@ -121,6 +129,9 @@ class Oracle:
 
     def extend(self, *args, **kwargs):
         return extend(*args, _lib=self._lib, **kwargs)
+
+    def qkv_project(self, *args, **kwargs):
+        return qkv_project(*args, _lib=self._lib, **kwargs)
 
 
 def max_threads() -> int:
@@ -327,3 +338,39 @@ def extend(q, k_new, v_new, k_cache, v_cache, block_table, cache_lens, new_indpt
     if rc != 0:
         raise ValueError(f"orthros_ref_extend failed with code {rc}")
     return o_base, lse_base, o_out, lse_out
+
+
+def qkv_project(x, n_base, w_t, Hq, Hkv, d, alpha_base, beta_base, alpha_out, beta_out,
+                k_cache=None, v_cache=None, block_table=None, token_seq=None, token_pos=None,
+                nthreads=0, _lib=None):
+    """Shared Q/K/V projection of base rows x[:n_base] and output rows
+    x[n_base:] with the stream affines on the query part (float64). The
+    caches (float32, [num_pages, page_size, Hkv, d]) are MODIFIED when given.
+    Returns (q_base [n_base,Hq,d], q_out [n_out,Hq,d], k, v [n_base,Hkv,d])."""
+    x, w_t = _f32(x), _f32(w_t)
+    rows, d_model = x.shape
+    n_out = rows - n_base
+    Nq, Nkv = Hq * d, Hkv * d
+    assert w_t.shape == (Nq + 2 * Nkv, d_model)
+    ab, bb, ao, bo = (_f32(a).reshape(-1) for a in (alpha_base, beta_base, alpha_out, beta_out))
+    qb = np.zeros((n_base, Hq, d), np.float64)
+    qo = np.zeros((n_out, Hq, d), np.float64)
+    k = np.zeros((n_base, Hkv, d), np.float64)
+    v = np.zeros((n_base, Hkv, d), np.float64)
+    if k_cache is not None:
+        assert k_cache.dtype == np.float32 and k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+        bt = _i32(block_table)
+        max_pages, page_size, num_pages = bt.shape[1], k_cache.shape[1], k_cache.shape[0]
+        ts, tp = _i32(token_seq), _i32(token_pos)
+    else:
+        bt = ts = tp = None
+        max_pages = page_size = num_pages = 1
+    rc = (_lib or _load()).orthros_ref_qkv_project(
+        _ptr(x, _f32p), int(n_base), int(n_out), int(d_model), _ptr(w_t, _f32p), Hq, Hkv, d,
+        _ptr(ab, _f32p), _ptr(bb, _f32p), _ptr(ao, _f32p), _ptr(bo, _f32p),
+        _ptr(qb, _f64p), _ptr(qo, _f64p), _ptr(k, _f64p), _ptr(v, _f64p),
+        _ptr(k_cache, _f32p), _ptr(v_cache, _f32p), _ptr(bt, _i32p), max_pages, page_size, num_pages,
+        _ptr(ts, _i32p), _ptr(tp, _i32p), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"orthros_ref_qkv_project failed with code {rc}")
+    return qb, qo, k, v

@@ -377,6 +377,84 @@ def pin_hand_worked(orc):
 
 
 # ---------------------------------------------------------------------------
+# Shared Q/K/V projection (the step upstream of the hot path)
+# ---------------------------------------------------------------------------
+
+def pin_project_selection_weight(orc):
+    """A weight whose every output column selects one input column times a
+    power of two: each projection output is that input times the factor, so q
+    is alpha * (s x_c) + beta and k, v are s x_c, exactly."""
+    rng = np.random.default_rng(51)
+    n_base, n_out, d_model, Hq, Hkv, d = 3, 2, 24, 4, 2, 4
+    N = (Hq + 2 * Hkv) * d
+    x = rng.standard_normal((n_base + n_out, d_model)).astype(np.float32)
+    sel = rng.integers(0, d_model, N)
+    fac = (2.0 ** rng.integers(-2, 3, N)).astype(np.float32)
+    w_t = np.zeros((N, d_model), np.float32)
+    w_t[np.arange(N), sel] = fac
+    ab, bb, ao, bo = (a.numpy() for a in make_affines(torch.Generator().manual_seed(3), Hq, d))
+    qb, qo, k, v = orc.qkv_project(x, n_base, w_t, Hq, Hkv, d, ab, bb, ao, bo)
+    y = x.astype(np.float64)[:, sel] * fac.astype(np.float64)
+    Nq, Nkv = Hq * d, Hkv * d
+    _close(qb.reshape(n_base, Nq), ab.reshape(-1) * y[:n_base, :Nq] + bb.reshape(-1), 1e-15, "select q_base")
+    _close(qo.reshape(n_out, Nq), ao.reshape(-1) * y[n_base:, :Nq] + bo.reshape(-1), 1e-15, "select q_out")
+    _close(k.reshape(n_base, Nkv), y[:n_base, Nq:Nq + Nkv], 0.0, "select k")
+    _close(v.reshape(n_base, Nkv), y[:n_base, Nq + Nkv:], 0.0, "select v")
+
+
+def pin_project_rank_one(orc):
+    """w_t[j, c] = a_j b_c: every output is a_j (x . b), with the dot product
+    taken by numpy; values on a binary grid so all products are exact."""
+    rng = np.random.default_rng(53)
+    n_base, n_out, d_model, Hq, Hkv, d = 2, 1, 40, 2, 1, 8
+    N = (Hq + 2 * Hkv) * d
+    x = (np.round(rng.standard_normal((n_base + n_out, d_model)) * 8) / 8).astype(np.float32)
+    a = (np.round(rng.standard_normal(N) * 4) / 4).astype(np.float32)
+    b = (np.round(rng.standard_normal(d_model) * 4) / 4).astype(np.float32)
+    w_t = np.outer(a, b).astype(np.float32)
+    one = np.ones((Hq, d), np.float32)
+    zero = np.zeros((Hq, d), np.float32)
+    qb, qo, k, v = orc.qkv_project(x, n_base, w_t, Hq, Hkv, d, one, zero, one, zero)
+    y = np.outer(x.astype(np.float64) @ b.astype(np.float64), a.astype(np.float64))
+    Nq, Nkv = Hq * d, Hkv * d
+    _close(qb.reshape(n_base, Nq), y[:n_base, :Nq], 1e-12, "rank-1 q_base")
+    _close(qo.reshape(n_out, Nq), y[n_base:, :Nq], 1e-12, "rank-1 q_out")
+    _close(k.reshape(n_base, Nkv), y[:n_base, Nq:Nq + Nkv], 1e-12, "rank-1 k")
+    _close(v.reshape(n_base, Nkv), y[:n_base, Nq + Nkv:], 1e-12, "rank-1 v")
+
+
+def pin_project_feeds_decode(orc):
+    """Alg. 1 line 5 applies each stream's affine once: projecting a decoding
+    pair with the affines in the projection and then decoding with identity
+    affines equals decoding the raw projections with the stream affines; the
+    projection's cache writes are the decoding step's appends."""
+    rng = np.random.default_rng(57)
+    B, Hq, Hkv, d, P, w, d_model = 3, 4, 2, 8, 4, 5, 16
+    lens = np.array([2, 7, 0], np.int32)
+    k_hist = [rng.standard_normal((int(L), Hkv, d)).astype(np.float32) for L in lens]
+    v_hist = [rng.standard_normal((int(L), Hkv, d)).astype(np.float32) for L in lens]
+    kc, vc, bt = _paged_from_seq(k_hist, v_hist, lens, P, 1, rng)
+    x = rng.standard_normal((2 * B, d_model)).astype(np.float32)
+    w_t = (0.25 * rng.standard_normal(((Hq + 2 * Hkv) * d, d_model))).astype(np.float32)
+    ab, bb, ao, bo = (a.numpy() for a in make_affines(torch.Generator().manual_seed(6), Hq, d))
+    one = np.ones((Hq, d), np.float32)
+    zero = np.zeros((Hq, d), np.float32)
+    kc1, vc1 = kc.copy(), vc.copy()
+    qb, qo, k, v = orc.qkv_project(x, B, w_t, Hq, Hkv, d, ab, bb, ao, bo, k_cache=kc1, v_cache=vc1,
+                                   block_table=bt, token_seq=np.arange(B, dtype=np.int32), token_pos=lens)
+    raw = orc.qkv_project(x, B, w_t, Hq, Hkv, d, one, zero, one, zero)
+    kc2, vc2 = kc.copy(), vc.copy()
+    a = orc.decode(qb.astype(np.float32), k.astype(np.float32), v.astype(np.float32), kc2, vc2, bt, lens,
+                   one, zero, one, zero, w, 0.4, q_out=qo.astype(np.float32))
+    kc3, vc3 = kc.copy(), vc.copy()
+    b_ = orc.decode(raw[0].astype(np.float32), raw[2].astype(np.float32), raw[3].astype(np.float32), kc3, vc3, bt,
+                    lens, ab, bb, ao, bo, w, 0.4, q_out=raw[1].astype(np.float32))
+    for x1, x2, n in zip(a, b_, ("o_base", "lse_base", "o_out", "lse_out")):
+        _close(x1, x2, 2e-6, "projection affine " + n)  # the affine runs in float32 on one side
+    assert np.array_equal(kc1, kc2) and np.array_equal(vc1, vc2), "projection cache writes != decode appends"
+
+
+# ---------------------------------------------------------------------------
 # Continuous-batching step (appends of several tokens per sequence)
 # ---------------------------------------------------------------------------
 
@@ -677,6 +755,9 @@ ALL_PINS = [
     pin_decode_page_permutation,
     pin_prefill_decode_consistency,
     pin_hand_worked,
+    pin_project_selection_weight,
+    pin_project_rank_one,
+    pin_project_feeds_decode,
     pin_extend_brute_force,
     pin_extend_chunked_consistency,
     pin_extend_single_token_is_decode,

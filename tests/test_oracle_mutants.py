@@ -49,6 +49,13 @@ MUTANTS = {
                                      "q + ((size_t)(new_indptr[b] + 0 * (t - cache_lens[b])) * Hq + h)"),
     "extend_base_sees_next_token": ("attend_row(qa, krow + tab, vrow + tab, lo, t, d, scale, o_base + qoff, &lse, w);\n                lse_base[(size_t)i * Hq + h] = lse;",
                                     "attend_row(qa, krow + tab, vrow + tab, lo, t + (i + 1 < new_indptr[b + 1] ? 1 : 0), d, scale, o_base + qoff, &lse, w);\n                lse_base[(size_t)i * Hq + h] = lse;"),
+    "proj_out_rows_base_affine": ("q_out[(size_t)(r - n_base) * Nq + j] = (double)alpha_out[j] * y + (double)beta_out[j];",
+                                  "q_out[(size_t)(r - n_base) * Nq + j] = (double)alpha_base[j] * y + (double)beta_out[j];"),
+    "proj_k_v_swapped": ("k[(size_t)r * Nkv + (j - Nq)] = y;", "v[(size_t)r * Nkv + (j - Nq)] = y;"),
+    "proj_beta_dropped": ("q_base[(size_t)r * Nq + j] = (double)alpha_base[j] * y + (double)beta_base[j];",
+                          "q_base[(size_t)r * Nq + j] = (double)alpha_base[j] * y;"),
+    "proj_cache_slot_off": ("const size_t off = ((size_t)pg * page_size + t % page_size) * (size_t)Nkv;",
+                            "const size_t off = ((size_t)pg * page_size + (t + 1) % page_size) * (size_t)Nkv;"),
     "decode_append_wrong_slot": ("((size_t)pg * page_size + L % page_size) * tok;", "((size_t)pg * page_size + (L + 1) % page_size) * tok;"),
 }
 
