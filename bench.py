@@ -499,6 +499,57 @@ def bench_extend(args, dist, dev, stream, peaks, ola, torch, W):
             "gpu_launches": sum(n for n, _ in prof.values())}
 
 
+def bench_project(args, dist, dev, stream, peaks, ola, torch, W):
+    """The shared Q/K/V projection at the Llama-8B shape: a 32-sequence decoding
+    pair (64 rows share one read of the 50 MB weight; HBM-bound, reported in
+    GB/s of weight + rows + outputs) and an 8192-token prefill chunk
+    (tensor-bound, 2 * rows * d_model * N FLOP), with the K/V written to pages."""
+    res = {}
+    for wdef, key in ((W.PROJ_DECODE_32, "decode"), (W.PROJ_PREFILL_8K, "prefill")):
+        wl = W.make_projection(wdef)
+        nb, no, dm, Hq, Hkv, d = wdef.n_base, wdef.n_out, wdef.d_model, wdef.Hq, wdef.Hkv, wdef.d
+        x, w_t = wl["x"].to(dev), wl["w_t"].to(dev)
+        aff = [wl[n].to(dev) for n in ("alpha_base", "beta_base", "alpha_out", "beta_out")]
+        P = 64
+        max_pages = (nb + P - 1) // P
+        kc = torch.empty((max_pages, P, Hkv, d), dtype=torch.bfloat16, device=dev)
+        vc = torch.empty_like(kc)
+        bt = torch.arange(max_pages, dtype=torch.int32, device=dev).view(1, max_pages)
+        seq = torch.zeros(nb, dtype=torch.int32, device=dev)
+        pos = torch.arange(nb, dtype=torch.int32, device=dev)
+        out = (torch.empty((nb, Hq, d), dtype=torch.bfloat16, device=dev),
+               torch.empty((no, Hq, d), dtype=torch.bfloat16, device=dev), None, None)
+        ws = torch.empty(256, dtype=torch.uint8, device=dev)
+
+        def step(_=0):
+            ola.orthros_qkv_project(x, nb, w_t, Hq, Hkv, d, *aff, k_cache=kc, v_cache=vc, block_table=bt,
+                                    token_seq=seq, token_pos=pos, out=out, workspace=ws, stream=stream)
+
+        for _ in range(max(args.warmup, 3)):
+            step()
+        torch.cuda.synchronize()
+        steps = max(args.steps, 20)
+        ms, prof = _timed(ola, torch, dist, stream, step, steps)
+        N = (Hq + 2 * Hkv) * d
+        nbytes = (N * dm + (nb + no) * dm + (nb + no) * Hq * d + nb * 2 * Hkv * d) * 2
+        flops = 2.0 * (nb * N + no * Hq * d) * dm
+        n_, t_ = prof["project_tc"]
+        avg = t_ / n_
+        if key == "decode":
+            ach = nbytes / (avg * 1e-3) / 1e9
+            roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm"], "unit": "GB/s", "frac": ach / peaks["hbm"],
+                    "bytes_per_launch": nbytes}
+        else:
+            ach = flops / (avg * 1e-3) / 1e12
+            roof = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16"], "unit": "TFLOP/s",
+                    "frac": ach / peaks["bf16"], "flop_per_launch": flops}
+        roof.update({"kernel": "project_tc", "avg_launch_ms": avg, "traffic": None,
+                     "peak_source": f"{peaks['src']} " + ("HBM copy" if key == "decode" else "bf16 dense (burst)")})
+        res[key] = {"workload": wdef.name, "ms_per_step": ms / steps, "steps": steps, "roofline": roof,
+                    "gpu_launches": sum(c for c, _ in prof.values())}
+    return res
+
+
 def run_ours(args, dist):
     import torch
 
@@ -513,7 +564,7 @@ def run_ours(args, dist):
     peaks = load_peaks()
     clocks = ClockSampler(dist.local)
     clocks.start()
-    pre = dec = bwd = ext = None
+    pre = dec = bwd = ext = prj = None
     if args.only in ("all", "prefill"):
         pre = bench_prefill(args, dist, dev, stream, peaks, ola, torch, W)
     if args.only in ("all", "decode"):
@@ -522,6 +573,8 @@ def run_ours(args, dist):
         bwd = bench_backward(args, dist, dev, stream, peaks, ola, torch, W)
     if args.only in ("all", "extend"):
         ext = bench_extend(args, dist, dev, stream, peaks, ola, torch, W)
+    if args.only in ("all", "project"):
+        prj = bench_project(args, dist, dev, stream, peaks, ola, torch, W)
     clk = clocks.stop()
     cpu = None
     if pre is not None and dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
@@ -530,7 +583,7 @@ def run_ours(args, dist):
     if dist.rank != 0:
         return
     if pre is None:  # decode- or backward-only profiling run
-        print(json.dumps({"decode": dec, "backward": bwd, "extend": ext, "clocks": clk}), flush=True)
+        print(json.dumps({"decode": dec, "backward": bwd, "extend": ext, "project": prj, "clocks": clk}), flush=True)
         return
     wl = pre["wl"]
     line = {
@@ -550,6 +603,7 @@ def run_ours(args, dist):
         "decode": dec,
         "backward": bwd,
         "extend": ext,
+        "project": prj,
         "cpu_baseline": cpu,
         "clocks": clk,
     }
@@ -564,7 +618,7 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--decode-steps", type=int, default=None,
                     help="decoding steps to time (default: the workload's 128)")
-    ap.add_argument("--only", choices=("all", "prefill", "decode", "backward", "extend"), default="all",
+    ap.add_argument("--only", choices=("all", "prefill", "decode", "backward", "extend", "project"), default="all",
                     help="run one part (profiling captures); the headline line needs 'all'")
     ap.add_argument("--prefill-T", type=int, default=None,
                     help="shorter prefill (a smaller case of the same kernels, for profiler captures)")

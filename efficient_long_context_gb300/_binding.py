@@ -22,7 +22,7 @@ STATUS_NAMES = {0: "ORTHROS_OK", 1: "ORTHROS_EINVAL", 2: "ORTHROS_EUNSUPPORTED",
 
 # the public symbols of include/orthros_attn.h
 EXPORTS = ("orthros_prefill_workspace_size", "orthros_prefill", "orthros_prefill_backward_workspace_size",
-           "orthros_prefill_backward", "orthros_extend_workspace_size", "orthros_extend",
+           "orthros_prefill_backward", "orthros_extend_workspace_size", "orthros_extend", "orthros_qkv_project",
            "orthros_decode_workspace_size",
            "orthros_decode", "orthros_decode_static", "orthros_check", "orthros_profile_begin", "orthros_profile_end",
            "orthros_status_string", "orthros_last_error")
@@ -74,6 +74,10 @@ def load_library(path: str | None = None):
         lib.orthros_extend.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp, i32p, i32p, vp,
                                        vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float, i32,
                                        vp, vp, vp, vp, vp, sz, vp]
+        lib.orthros_qkv_project.restype = i32
+        lib.orthros_qkv_project.argtypes = [vp, i32, i32, i32, vp, i32, i32, i32, vp, vp, vp, vp,
+                                            vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, i32,
+                                            vp, sz, vp]
         lib.orthros_decode_workspace_size.restype = sz
         lib.orthros_decode_workspace_size.argtypes = [i32] * 7
         lib.orthros_decode.restype = i32
@@ -281,6 +285,43 @@ def orthros_extend(q, k_new, v_new, k_cache, v_cache, block_table, cache_lens, n
         _ptr(o_base), _ptr(lse_base), _ptr(o_out), _ptr(lse_out), _ptr(workspace), workspace.numel(), _stream(stream))
     _raise_if(rc, lib)
     return o_base, lse_base, o_out, lse_out
+
+
+def orthros_qkv_project(x, n_base, w_qkv, Hq, Hkv, d, alpha_base, beta_base, alpha_out, beta_out, *,
+                        kv_out=False, k_cache=None, v_cache=None, block_table=None, token_seq=None,
+                        token_pos=None, out=None, workspace=None, stream=None):
+    """orthros_qkv_project of include/orthros_attn.h on torch CUDA tensors.
+
+    x [n_base + n_out, d_model] (base rows first), w_qkv [(Hq+2Hkv) d, d_model].
+    Returns (q_base [n_base,Hq,d], q_out [n_out,Hq,d], k [n_base,Hkv,d] or None,
+    v or None); the caches are written in place when given.
+    """
+    lib = load_library()
+    rows, d_model = x.shape
+    n_out = rows - int(n_base)
+    for name, t in (("x", x), ("w_qkv", w_qkv)):
+        _contig(name, t)
+    if out is None:
+        dev = x.device
+        out = (torch.empty((n_base, Hq, d), dtype=x.dtype, device=dev),
+               torch.empty((n_out, Hq, d), dtype=x.dtype, device=dev),
+               torch.empty((n_base, Hkv, d), dtype=x.dtype, device=dev) if kv_out else None,
+               torch.empty((n_base, Hkv, d), dtype=x.dtype, device=dev) if kv_out else None)
+    q_b, q_o, k_o, v_o = out
+    if workspace is None:
+        workspace = torch.empty(256, dtype=torch.uint8, device=x.device)
+    max_pages = block_table.shape[1] if block_table is not None else 0
+    B = block_table.shape[0] if block_table is not None else 0
+    page_size = k_cache.shape[1] if k_cache is not None else 0
+    num_pages = k_cache.shape[0] if k_cache is not None else 0
+    rc = lib.orthros_qkv_project(
+        _ptr(x), int(n_base), n_out, d_model, _ptr(w_qkv), Hq, Hkv, d,
+        _ptr(alpha_base), _ptr(beta_base), _ptr(alpha_out), _ptr(beta_out),
+        _ptr(q_b), _ptr(q_o), _ptr(k_o), _ptr(v_o), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), B,
+        max_pages, page_size, num_pages, _ptr(token_seq), _ptr(token_pos), _dtype(x),
+        _ptr(workspace), workspace.numel(), _stream(stream))
+    _raise_if(rc, lib)
+    return out
 
 
 def orthros_decode(q, k_new, v_new, k_cache, v_cache, block_table, cache_lens, alpha_base, beta_base,

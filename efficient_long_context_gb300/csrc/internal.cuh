@@ -207,6 +207,21 @@ int bwd_tc_max_tiles_bound(int T, int window, int g, int max_rows_per_seq);
 cudaError_t launch_backward_tc(const BwdTcParams &p, const void *k, const void *v, const void *qa_base,
                                const void *do_base, const void *qa_out, const void *do_out, cudaStream_t stream);
 
+// project_tc.cu: shared Q/K/V projection (bf16) with the query affines and
+// the cache writes in the epilogue.
+struct ProjParams {
+    const __nv_bfloat16 *x;    // [n_base + n_out, d_model]
+    const __nv_bfloat16 *w_t;  // [(Hq + 2 Hkv) d, d_model]
+    int n_base, n_out, d_model, Hq, Hkv, d;
+    const float *alpha_base, *beta_base, *alpha_out, *beta_out;
+    __nv_bfloat16 *q_base, *q_out, *k_out, *v_out;  // k_out / v_out may be null
+    __nv_bfloat16 *k_cache, *v_cache;               // null: no cache writes
+    const int32_t *block_table, *token_seq, *token_pos;
+    int B, max_pages, page_size, num_pages;
+    uint32_t *status;
+};
+cudaError_t launch_project_tc(const ProjParams &p, cudaStream_t stream);
+
 // cache.cu
 // Writes new token i of sequence b (rows new_indptr[b] ..) at position
 // cache_lens[b] + (i - new_indptr[b]) of its pages.

@@ -750,6 +750,85 @@ orthros_status orthros_extend(const void *q, const void *q_out, const void *k_ne
     return ORTHROS_OK;
 }
 
+orthros_status orthros_qkv_project(const void *x, int n_base, int n_out, int d_model, const void *w_qkv, int Hq,
+                                   int Hkv, int d, const float *alpha_base, const float *beta_base,
+                                   const float *alpha_out, const float *beta_out, void *q_base, void *q_out,
+                                   void *k_out, void *v_out, void *k_cache, void *v_cache,
+                                   const int32_t *block_table, int B, int max_pages, int page_size, int num_pages,
+                                   const int32_t *token_seq, const int32_t *token_pos, orthros_dtype dtype,
+                                   void *workspace, size_t workspace_bytes, orthros_stream_t stream_) {
+    g_last_error.clear();
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (dtype != ORTHROS_BF16) return fail(ORTHROS_EUNSUPPORTED, "the projection takes bf16 only");
+    if (n_base < 0 || n_out < 0) return fail(ORTHROS_EINVAL, "n_base = %d, n_out = %d must be >= 0", n_base, n_out);
+    if (Hq < 1 || Hkv < 1) return fail(ORTHROS_EINVAL, "head counts must be >= 1");
+    if (d != 64 && d != 128) return fail(ORTHROS_EUNSUPPORTED, "head size d = %d (supported: 64, 128)", d);
+    if (d_model < 64 || d_model % 64 != 0)
+        return fail(ORTHROS_EUNSUPPORTED, "d_model = %d must be a positive multiple of 64", d_model);
+    if ((long long)n_base + n_out > (1LL << 31) - 1) return fail(ORTHROS_EUNSUPPORTED, "too many rows");
+    if (!workspace || workspace_bytes < kStatusBytes)
+        return fail(ORTHROS_EWORKSPACE, "workspace needs %zu bytes", kStatusBytes);
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(ORTHROS_EINVAL, "workspace must be 256-byte aligned");
+    if (n_base + n_out > 0) {
+        if (!x || !w_qkv) return fail(ORTHROS_EINVAL, "x and w_qkv must not be NULL");
+        if (!aligned16(x) || !aligned16(w_qkv)) return fail(ORTHROS_EINVAL, "x and w_qkv must be 16-byte aligned");
+    }
+    if (n_base > 0) {
+        if (!q_base || !alpha_base || !beta_base) return fail(ORTHROS_EINVAL, "q_base and the base affine must not be NULL");
+        if ((k_out == nullptr) != (v_out == nullptr)) return fail(ORTHROS_EINVAL, "k_out and v_out: both or neither");
+        const bool cache = k_cache || v_cache || block_table;
+        if (cache && (!k_cache || !v_cache || !block_table || !token_seq || !token_pos))
+            return fail(ORTHROS_EINVAL, "cache writes need k_cache, v_cache, block_table, token_seq and token_pos");
+        if (cache && (page_size < 1 || max_pages < 1 || num_pages < 1 || B < 1))
+            return fail(ORTHROS_EINVAL, "B, page_size, max_pages and num_pages must be >= 1 for cache writes");
+        if (!aligned16(q_base) || (k_out && (!aligned16(k_out) || !aligned16(v_out))) ||
+            (k_cache && (!aligned16(k_cache) || !aligned16(v_cache))))
+            return fail(ORTHROS_EINVAL, "outputs must be 16-byte aligned");
+    }
+    if (n_out > 0) {
+        if (!q_out || !alpha_out || !beta_out) return fail(ORTHROS_EINVAL, "q_out and the output affine must not be NULL");
+        if (!aligned16(q_out)) return fail(ORTHROS_EINVAL, "q_out must be 16-byte aligned");
+    }
+    uint32_t *status = static_cast<uint32_t *>(workspace);
+    cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "status reset");
+    if (n_base + n_out == 0) return ORTHROS_OK;
+    ProjParams pp{};
+    pp.x = static_cast<const __nv_bfloat16 *>(x);
+    pp.w_t = static_cast<const __nv_bfloat16 *>(w_qkv);
+    pp.n_base = n_base;
+    pp.n_out = n_out;
+    pp.d_model = d_model;
+    pp.Hq = Hq;
+    pp.Hkv = Hkv;
+    pp.d = d;
+    pp.alpha_base = alpha_base;
+    pp.beta_base = beta_base;
+    pp.alpha_out = alpha_out;
+    pp.beta_out = beta_out;
+    pp.q_base = static_cast<__nv_bfloat16 *>(q_base);
+    pp.q_out = static_cast<__nv_bfloat16 *>(q_out);
+    pp.k_out = static_cast<__nv_bfloat16 *>(k_out);
+    pp.v_out = static_cast<__nv_bfloat16 *>(v_out);
+    pp.k_cache = static_cast<__nv_bfloat16 *>(k_cache);
+    pp.v_cache = static_cast<__nv_bfloat16 *>(v_cache);
+    pp.block_table = block_table;
+    pp.token_seq = token_seq;
+    pp.token_pos = token_pos;
+    pp.B = B;
+    pp.max_pages = max_pages;
+    pp.page_size = page_size;
+    pp.num_pages = num_pages;
+    pp.status = status;
+    {
+        ProfScope ps("project_tc", stream);
+        e = launch_project_tc(pp, stream);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "projection launch");
+    return ORTHROS_OK;
+}
+
 size_t orthros_decode_workspace_size(int B, int Hq, int Hkv, int d, int max_pages, int page_size,
                                      orthros_dtype dtype) {
     if (max_pages < 1 || page_size < 1) return 0;

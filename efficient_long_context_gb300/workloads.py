@@ -288,3 +288,36 @@ def make_extend(w: ExtendWorkload, with_q_out: bool = False, seed: int | None = 
                 v_new=v_new, q_out=q_out, alpha_base=ab, beta_base=bb, alpha_out=ao, beta_out=bo,
                 B=B, Hq=w.Hq, Hkv=w.Hkv, d=w.d, window=w.window, scale=w.scale, dtype=w.dtype,
                 page_size=P, max_pages=max_pages, num_pages=num_pages)
+
+
+@dataclass(frozen=True)
+class ProjectionWorkload:
+    """The shared Q/K/V projection: n_base base-token rows and n_out output
+    rows of width d_model through one weight of (Hq + 2 Hkv) d columns."""
+    name: str
+    n_base: int
+    n_out: int
+    d_model: int
+    Hq: int
+    Hkv: int
+    d: int
+    seed: int = 0
+
+
+# Llama-3.1-8B attention projection: a 32-sequence decoding step (32 base +
+# 32 output tokens share the weight read) and an 8192-token prefill chunk.
+PROJ_DECODE_32 = ProjectionWorkload("proj_decode_b32x2_d4096_gqa32x8", 32, 32, 4096, 32, 8, 128, seed=1006)
+PROJ_PREFILL_8K = ProjectionWorkload("proj_prefill_8192_d4096_gqa32x8", 8192, 0, 4096, 32, 8, 128, seed=1007)
+
+
+def make_projection(w: ProjectionWorkload, seed: int | None = None) -> dict:
+    """Hidden rows ~ N(0,1), weights ~ N(0,1)/sqrt(d_model) (unit-variance
+    outputs), affines as elsewhere; bf16. Draw order: x, w_t, affines."""
+    gen = torch.Generator()
+    gen.manual_seed(w.seed if seed is None else seed)
+    N = (w.Hq + 2 * w.Hkv) * w.d
+    x = _normal(gen, (w.n_base + w.n_out, w.d_model), torch.bfloat16)
+    w_t = (torch.randn((N, w.d_model), generator=gen) * w.d_model ** -0.5).to(torch.bfloat16)
+    ab, bb, ao, bo = make_affines(gen, w.Hq, w.d)
+    return dict(x=x, w_t=w_t, alpha_base=ab, beta_base=bb, alpha_out=ao, beta_out=bo, n_base=w.n_base,
+                n_out=w.n_out, d_model=w.d_model, Hq=w.Hq, Hkv=w.Hkv, d=w.d)

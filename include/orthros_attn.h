@@ -248,6 +248,44 @@ ORTHROS_API orthros_status orthros_extend(
     void *workspace, size_t workspace_bytes, orthros_stream_t stream);
 
 /*
+ * The shared Q/K/V projection that feeds the hot path (Alg. 1 lines 4-5,
+ * Sec. 3.1): base-token rows x[0 .. n_base) and output-token rows
+ * x[n_base .. n_base+n_out) are multiplied by ONE weight (in decoding, a
+ * step's base and output tokens share its read), y = x W, and
+ *   q_base = alpha_base (.) y_Q + beta_base   for base rows,
+ *   q_out  = alpha_out  (.) y_Q + beta_out    for output rows,
+ *   k, v   = y_K, y_V                         for base rows only (only the
+ *            base stream writes the cache), to k_out / v_out and/or to the
+ *            page slot of (token_seq[i], token_pos[i]).
+ * The queries leave with their affine applied: pass identity affines
+ * (alpha = 1, beta = 0) to the attention calls that read them.
+ *
+ * x        [n_base + n_out, d_model] bf16, d_model a multiple of 64
+ * w_qkv    [(Hq + 2 Hkv) d, d_model] bf16: row j holds the weights of output
+ *          column j (W transposed); columns are Q heads, then K, then V heads
+ * alpha_*, beta_* [Hq, d] float
+ * q_base [n_base, Hq, d], q_out [n_out, Hq, d] bf16 (q_out NULL if n_out = 0)
+ * k_out, v_out [n_base, Hkv, d] bf16, or both NULL
+ * k_cache, v_cache [num_pages, page_size, Hkv, d], block_table [B, max_pages],
+ * token_seq, token_pos [n_base] device int32: all NULL for no cache writes
+ * workspace at least 256 bytes (status word), 256-byte aligned
+ * Errors: bf16 only (EUNSUPPORTED otherwise); a row whose page does not exist
+ * sets ORTHROS_DEV_BAD_PAGE / _BAD_POSITION and its cache write is skipped.
+ * The paper has no kernel for this step; it is the step upstream of the
+ * attention that the decoding pair's shared weight read makes worth fusing.
+ */
+ORTHROS_API orthros_status orthros_qkv_project(
+    const void *x, int n_base, int n_out, int d_model, const void *w_qkv,
+    int Hq, int Hkv, int d,
+    const float *alpha_base, const float *beta_base,
+    const float *alpha_out, const float *beta_out,
+    void *q_base, void *q_out, void *k_out, void *v_out,
+    void *k_cache, void *v_cache, const int32_t *block_table, int B,
+    int max_pages, int page_size, int num_pages,
+    const int32_t *token_seq, const int32_t *token_pos, orthros_dtype dtype,
+    void *workspace, size_t workspace_bytes, orthros_stream_t stream);
+
+/*
  * orthros_decode without a workspace argument, for callers that cannot
  * allocate device memory where they run a decoding step (for example a host
  * framework whose operator interface passes only inputs and outputs, or a

@@ -174,6 +174,30 @@ def test_extend_host_checks(lib):
     assert ola.orthros_extend_workspace_size(2, 3, 1, 4, 2, 96, 4, 64) == 0
 
 
+def test_projection_host_checks(lib):
+    P = 1 << 12
+
+    def call(**over):
+        a = dict(x=P, nb=2, no=1, dm=128, w=P, Hq=4, Hkv=2, d=64, ab=P, bb=P, ao=P, bo=P, qb=P, qo=P, ko=None,
+                 vo=None, kc=None, vc=None, bt=None, B=0, mp=0, ps=0, np_=0, ts=None, tp=None, dtype=0, ws=P,
+                 wsb=256, stream=None)
+        a.update(over)
+        return lib.orthros_qkv_project(a["x"], a["nb"], a["no"], a["dm"], a["w"], a["Hq"], a["Hkv"], a["d"], a["ab"],
+                                       a["bb"], a["ao"], a["bo"], a["qb"], a["qo"], a["ko"], a["vo"], a["kc"], a["vc"],
+                                       a["bt"], a["B"], a["mp"], a["ps"], a["np_"], a["ts"], a["tp"], a["dtype"],
+                                       a["ws"], a["wsb"], a["stream"])
+
+    assert call(dtype=1) == 2  # bf16 only
+    assert call(d=96) == 2
+    assert call(dm=100) == 2
+    assert call(x=None) == 1
+    assert call(ko=P) == 1  # k_out without v_out
+    assert call(kc=P, vc=P, bt=P) == 1  # cache writes without token positions
+    assert call(qo=None) == 1
+    assert call(qb=P + 8) == 1
+    assert call(ws=None) == 4
+
+
 def test_product_path_fails_loudly_without_library(tmp_path):
     with pytest.raises(ola.OrthrosError):
         ola.load_library(str(tmp_path / "missing.so"))

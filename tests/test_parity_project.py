@@ -1,0 +1,103 @@
+"""GPU parity of orthros_qkv_project (shared Q/K/V projection with the stream
+affines and the cache writes in the epilogue) against the oracle.
+
+Tolerance per element: |gpu - ref| <= 5e-3 * (rms(ref) + |ref|). The products
+are exact bf16 x bf16 in fp32 and accumulate in fp32, so the error is the
+final bf16 rounding, at most 2^-9 relative (2.5x margin).
+"""
+import numpy as np
+import pytest
+import torch
+
+from efficient_long_context_gb300 import workloads as W
+from tests.parity_util import f32
+
+pytestmark = pytest.mark.gpu
+
+TOL = 5e-3
+
+
+def rel_err(gpu, ref):
+    g = gpu.float().cpu().numpy().astype(np.float64)
+    r = np.asarray(ref, np.float64)
+    assert g.shape == r.shape and np.all(np.isfinite(g))
+    if r.size == 0:
+        return 0.0
+    return float(np.max(np.abs(g - r) / (np.sqrt(np.mean(r * r)) + np.abs(r) + 1e-30)))
+
+
+def run(wdef, rows=None, cache=True):
+    import efficient_long_context_gb300 as ola
+    import oracle
+
+    wl = W.make_projection(wdef)
+    dev = "cuda"
+    nb, no = wl["n_base"], wl["n_out"]
+    Hq, Hkv, d = wl["Hq"], wl["Hkv"], wl["d"]
+    aff = [wl[n].to(dev) for n in ("alpha_base", "beta_base", "alpha_out", "beta_out")]
+    kw = {}
+    if cache and nb:
+        P = 64
+        B = 3
+        # base rows spread over 3 sequences at scattered positions of a shuffled page pool
+        g = torch.Generator().manual_seed(9)
+        seq = torch.randint(0, B, (nb,), generator=g).to(torch.int32)
+        pos = torch.zeros(nb, dtype=torch.int32)
+        for b in range(B):
+            idx = torch.nonzero(seq == b).flatten()
+            pos[idx] = torch.randperm(max(len(idx) * 2, 1), generator=g)[:len(idx)].to(torch.int32)
+        max_pages = int(pos.max()) // P + 1
+        num_pages = B * max_pages
+        bt = torch.randperm(num_pages, generator=g).to(torch.int32).view(B, max_pages)
+        kc = torch.zeros((num_pages, P, Hkv, d), dtype=torch.bfloat16)
+        vc = torch.zeros_like(kc)
+        kw = dict(k_cache=kc.to(dev), v_cache=vc.to(dev), block_table=bt.to(dev), token_seq=seq.to(dev),
+                  token_pos=pos.to(dev))
+    qb, qo, k, v = ola.orthros_qkv_project(wl["x"].to(dev), nb, wl["w_t"].to(dev), Hq, Hkv, d, *aff, kv_out=True,
+                                           **kw)
+    torch.cuda.synchronize()
+    x = f32(wl["x"])
+    sel_b = np.arange(nb) if rows is None else np.asarray([r for r in rows if r < nb])
+    sel_o = np.arange(no) if rows is None else np.asarray([r - nb for r in rows if r >= nb], dtype=np.int64)
+    xs = np.concatenate([x[sel_b], x[nb + sel_o]], 0)
+    ref = oracle.qkv_project(xs, len(sel_b), f32(wl["w_t"]), Hq, Hkv, d,
+                             *(f32(wl[n]) for n in ("alpha_base", "beta_base", "alpha_out", "beta_out")))
+    errs = dict(q_base=rel_err(qb[sel_b], ref[0]), q_out=rel_err(qo[sel_o], ref[1]),
+                k=rel_err(k[sel_b], ref[2]), v=rel_err(v[sel_b], ref[3]))
+    if kw:
+        P = kw["k_cache"].shape[1]
+        kc, vc = kw["k_cache"].cpu(), kw["v_cache"].cpu()
+        seq, pos, bt = kw["token_seq"].cpu(), kw["token_pos"].cpu(), kw["block_table"].cpu()
+        pg = bt[seq[sel_b].long(), (pos[sel_b] // P).long()]
+        slot = (pos[sel_b] % P).long()
+        # the cache holds exactly the bf16 values the call returned in k_out / v_out
+        assert torch.equal(kc[pg.long(), slot], k[sel_b].cpu()) and torch.equal(vc[pg.long(), slot], v[sel_b].cpu())
+    bad = {n: e for n, e in errs.items() if e > TOL}
+    assert not bad, f"{wdef.name}: {errs}"
+    return errs
+
+
+SMALL = [
+    W.ProjectionWorkload("tiny", 3, 2, 64, 2, 1, 64, seed=1),
+    W.ProjectionWorkload("decode_pair", 5, 5, 256, 4, 2, 128, seed=2),
+    W.ProjectionWorkload("rows_past_tile", 130, 7, 192, 4, 2, 64, seed=3),
+    W.ProjectionWorkload("wide", 300, 0, 512, 8, 2, 128, seed=4),   # 256-wide tiles once enough rows
+    W.ProjectionWorkload("no_base", 0, 9, 128, 4, 4, 64, seed=5),
+]
+
+
+@pytest.mark.parametrize("wdef", SMALL, ids=lambda w: w.name)
+def test_projection_small(wdef):
+    run(wdef)
+
+
+def test_projection_decode_shape_full():
+    """The 32-sequence decoding pair at the Llama-8B projection shape, all rows."""
+    run(W.PROJ_DECODE_32)
+
+
+def test_projection_prefill_shape_sampled():
+    """8192 base rows at the Llama-8B shape (256-wide tiles), checked on sampled rows."""
+    rng = np.random.default_rng(0)
+    rows = sorted(set([0, 1, 127, 128, 4095, 8191]) | set(rng.choice(8192, 40, replace=False).tolist()))
+    run(W.PROJ_PREFILL_8K, rows=rows)
