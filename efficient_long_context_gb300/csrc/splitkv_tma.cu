@@ -66,6 +66,7 @@ struct ItemInfo {
     int b, kv, nrows, pos_base, L;
     int group;     // global group index (extend rows are looked up through it)
     int union_hi;  // last key any row needs (-1: none)
+    int union_lo;  // first key any row needs, rounded down to a whole stage (keys before it are skipped)
 };
 
 __device__ __forceinline__ ItemInfo item_info(const SplitParams &p, int group) {
@@ -85,9 +86,16 @@ __device__ __forceinline__ ItemInfo item_info(const SplitParams &p, int group) {
         const int npos = (e[3] & 0xffff) + (e[3] >> 16);
         it.nrows = npos * gsz;
         it.L = p.cache_lens[it.b];
-        int hi = -1, kind, idx;
-        for (int i = 0; i < npos; ++i) hi = max(hi, extend_position(p, group, it.b, it.L, i, kind, idx));
+        int hi = -1, lo = 0x7fffffff, kind, idx;
+        for (int i = 0; i < npos; ++i) {
+            const int t = extend_position(p, group, it.b, it.L, i, kind, idx);
+            if (t < 0) continue;
+            hi = max(hi, t);
+            lo = min(lo, kind == 0 ? max(0, t - p.window + 1) : 0);
+        }
         it.union_hi = hi;
+        // base rows of a prefill chunk need only their windows
+        it.union_lo = hi >= 0 ? (lo / kStageKeys) * kStageKeys : 0;
     } else {
         const int gi = p.group_info[3 * group];
         it.b = gi >> 16;
@@ -179,8 +187,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         for (int item = blockIdx.x; item < total_items && !*abort; item += gridDim.x) {
             const int group = p.group_offset + item / p.max_chunks, chunk = item % p.max_chunks;
             const ItemInfo it = item_info(p, group);
-            const int key_lo = chunk * p.chunk;
-            const int key_hi = min(it.union_hi, key_lo + p.chunk - 1);
+            const int key_lo = max(chunk * p.chunk, it.union_lo);
+            const int key_hi = min(it.union_hi, chunk * p.chunk + p.chunk - 1);
             if (key_lo > key_hi) continue;
             const int32_t *bt = p.mode != kSplitPrefill ? p.block_table + (long long)it.b * p.max_pages : nullptr;
             for (int j0 = key_lo; j0 <= key_hi; j0 += kStageKeys, ++sc) {
@@ -234,8 +242,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
         const int group = p.group_offset + item / p.max_chunks, chunk = item % p.max_chunks;
         const ItemInfo it = item_info(p, group);
-        const int key_lo = chunk * p.chunk;
-        const int key_hi = min(it.union_hi, key_lo + p.chunk - 1);
+        const int key_lo = max(chunk * p.chunk, it.union_lo);
+        const int key_hi = min(it.union_hi, chunk * p.chunk + p.chunk - 1);
         float *part = p.partial + ((long long)group * p.max_chunks + chunk) * kMaxRowsT * kRowStride;
         if (chunk == 0 && tid < kMaxRowsT && tid < it.nrows) {
             // report rows the data makes impossible (their combined outputs are NaN)
