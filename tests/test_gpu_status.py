@@ -84,3 +84,73 @@ def test_decode_bad_length_and_page(dtype):
     assert rc == 5 and bits & DEV_BAD_PAGE and bits & DEV_BAD_LENGTH, (rc, bits)
     assert torch.isnan(out[2][2].float()).all()  # the sequence with a bad length: NaN output rows
     assert torch.isfinite(out[0][0].float()).all()  # an untouched sequence is fine
+
+
+@pytest.mark.parametrize("page_size,dtype", [(64, torch.bfloat16), (16, torch.bfloat16), (16, torch.float32)])
+def test_extend_bad_rows_are_flagged(page_size, dtype):
+    """A history output row without q_out and a sequence whose length runs past
+    its block table are flagged; their rows come back NaN, the others are
+    those of a clean call."""
+    wdef = W.ExtendWorkload("bad_ext", 3, 8, 2, 128, 32, 10, 200, (3, 1, 2), page_size=page_size, dtype=dtype,
+                            seed=6)
+    wl = W.make_extend(wdef)
+    dev = "cuda"
+
+    def call(lens, pos):
+        kc, vc = wl["k_cache"].to(dev), wl["v_cache"].to(dev)
+        aff = [wl[n].to(dev) for n in ("alpha_base", "beta_base", "alpha_out", "beta_out")]
+        ws = torch.empty(ola.orthros_extend_workspace_size(3, 6, 3, 8, 2, 128, wl["max_pages"], page_size, dtype),
+                         dtype=torch.uint8, device=dev)
+        out = ola.orthros_extend(wl["q"].to(dev), wl["k_new"].to(dev), wl["v_new"].to(dev), kc, vc,
+                                 wl["block_table"].to(dev), lens.to(dev), wl["new_indptr"], wl["out_indptr"],
+                                 pos.to(dev), *aff, wdef.window, wdef.scale, workspace=ws)
+        return out, ola.orthros_check(ws)
+
+    clean, st = call(wl["cache_lens"], wl["out_positions"])
+    assert st == (0, 0)
+    pos = wl["out_positions"].clone()
+    pos[0] = 0  # a history position of sequence 0, but no q_out: no query for it
+    lens = wl["cache_lens"].clone()
+    lens[2] = wl["max_pages"] * page_size  # sequence 2's appends fall past its block table
+    bad, (rc, bits) = call(lens, pos)
+    assert rc == 5 and bits & DEV_BAD_POSITION and bits & (DEV_BAD_LENGTH | DEV_BAD_PAGE), (rc, bits)
+    assert torch.isnan(bad[2][0].float()).all() and torch.isnan(bad[3][0]).all()  # the flagged output row
+    assert torch.isnan(bad[1][4:6]).all()  # sequence 2's base rows
+    torch.testing.assert_close(bad[0][:4].float(), clean[0][:4].float(), rtol=0, atol=0)
+    torch.testing.assert_close(bad[2][1].float(), clean[2][1].float(), rtol=0, atol=0)
+
+
+def test_backward_bad_output_position():
+    wl = W.small_prefill(1, 200, 4, 2, 128, 32, out_mode=("list", [[3, 150, 50]]), seed=7)
+    dev = "cuda"
+    q, k, v = (wl[n].to(dev) for n in ("q", "k", "v"))
+    aff = [wl[n].to(dev) for n in ("alpha_base", "beta_base", "alpha_out", "beta_out")]
+    fwd = ola.orthros_prefill(q, k, v, *aff, wl["out_indptr"], wl["out_positions"].to(dev), wl["window"],
+                              wl["scale"])
+    do_b, do_o = (t.to(dev) for t in W.make_grad_outputs(wl, 3))
+    pos = wl["out_positions"].clone()
+    pos[1] = 200  # == T
+    ws = torch.empty(ola.orthros_prefill_backward_workspace_size(1, 200, 4, 2, 128, 3, 32), dtype=torch.uint8,
+                     device=dev)
+    ola.orthros_prefill_backward(q, k, v, *aff, wl["out_indptr"], pos.to(dev), wl["window"], wl["scale"], *fwd, do_b,
+                                 do_o, workspace=ws)
+    rc, bits = ola.orthros_check(ws)
+    assert rc == 5 and bits & DEV_BAD_POSITION, (rc, bits)
+
+
+def test_projection_bad_page():
+    wdef = W.ProjectionWorkload("bad_proj", 4, 0, 128, 4, 2, 64, seed=8)
+    wl = W.make_projection(wdef)
+    dev = "cuda"
+    kc = torch.zeros((2, 16, 2, 64), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    bt = torch.tensor([[1, 5]], dtype=torch.int32, device=dev)  # page 5 is outside the pool of 2
+    seq = torch.zeros(4, dtype=torch.int32, device=dev)
+    pos = torch.tensor([0, 1, 16, 17], dtype=torch.int32, device=dev)  # the last two rows land on page 5
+    aff = [wl[n].to(dev) for n in ("alpha_base", "beta_base", "alpha_out", "beta_out")]
+    ws = torch.empty(256, dtype=torch.uint8, device=dev)
+    out = ola.orthros_qkv_project(wl["x"].to(dev), 4, wl["w_t"].to(dev), 4, 2, 64, *aff, kv_out=True, k_cache=kc,
+                                  v_cache=vc, block_table=bt, token_seq=seq, token_pos=pos, workspace=ws)
+    rc, bits = ola.orthros_check(ws)
+    assert rc == 5 and bits & DEV_BAD_PAGE, (rc, bits)
+    assert torch.equal(kc[1, :2].cpu(), out[2][:2].cpu())  # the rows with a page were written
