@@ -765,7 +765,8 @@ orthros_status orthros_qkv_project(const void *x, int n_base, int n_out, int d_m
     if (d != 64 && d != 128) return fail(ORTHROS_EUNSUPPORTED, "head size d = %d (supported: 64, 128)", d);
     if (d_model < 64 || d_model % 64 != 0)
         return fail(ORTHROS_EUNSUPPORTED, "d_model = %d must be a positive multiple of 64", d_model);
-    if ((long long)n_base + n_out > (1LL << 31) - 1) return fail(ORTHROS_EUNSUPPORTED, "too many rows");
+    if ((long long)n_base + n_out > 65535LL * 128)
+        return fail(ORTHROS_EUNSUPPORTED, "%lld rows exceed 65535 tiles of 128", (long long)n_base + n_out);
     if (!workspace || workspace_bytes < kStatusBytes)
         return fail(ORTHROS_EWORKSPACE, "workspace needs %zu bytes", kStatusBytes);
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
