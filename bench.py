@@ -380,9 +380,9 @@ def bench_decode(args, dist, dev, stream, peaks, ola, torch, W):
     ws = torch.empty(ola.orthros_decode_workspace_size(dec.B, dec.Hq, dec.Hkv, dec.d, dm["max_pages"], dec.page_size,
                                                        dec.dtype), dtype=torch.uint8, device=dev)
 
-    def step(s):
+    def step(s, strm=stream):
         ola.orthros_decode(dq[s], dk[s], dv[s], kc, vc, bt, lens_steps[s], *daff, dec.window, dec.scale,
-                           out=outs, workspace=ws, stream=stream)
+                           out=outs, workspace=ws, stream=strm)
 
     for s in range(min(max(args.warmup, 3), dm["steps"])):
         step(s)
@@ -392,6 +392,29 @@ def bench_decode(args, dist, dev, stream, peaks, ola, torch, W):
         raise RuntimeError(f"decode flagged device status {rc} bits 0x{bits:x}")
     ms, prof = _timed(ola, torch, dist, stream, step, dm["steps"])
     nbytes = decode_bytes(st.cache_lens.tolist(), dm["steps"], dec.Hkv, dec.d)
+    # the same steps captured once in a CUDA graph and replayed (no host work or
+    # launch gaps between steps, as in a captured serving loop)
+    graph = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for s in range(dm["steps"]):
+                step(s, None)  # the capture stream
+        torch.cuda.synchronize()
+        g.replay()  # warm
+        dist.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ms_g = dist.max(e0.elapsed_time(e1))
+        graph = {"ms_per_step": ms_g / dm["steps"], "value": nbytes * dist.world / (ms_g * 1e-3) / 1e9,
+                 "unit": "GB/s", "frac_of_hbm": nbytes / (ms_g * 1e-3) / 1e9 / peaks["hbm"]}
+        del g
+    except RuntimeError as exc:  # capture is optional for the measurement
+        graph = {"error": str(exc)[:200]}
     gbs = nbytes * dist.world / (ms * 1e-3) / 1e9
     dom, (dom_n, dom_ms) = max(prof.items(), key=lambda kv: kv[1][1])
     achieved = nbytes / (dom_ms * 1e-3) / 1e9  # bytes of all steps over that kernel's summed time
@@ -403,7 +426,8 @@ def bench_decode(args, dist, dev, stream, peaks, ola, torch, W):
                          "peak_source": f"{peaks['src']} HBM copy",
                          "avg_launch_ms": dom_ms / dom_n, "bytes_per_launch": nbytes / dm["steps"]},
             "kernels": {n: {"launches": c, "total_ms": t} for n, (c, t) in prof.items()},
-            "gpu_launches": sum(n for n, _ in prof.values())}
+            "gpu_launches": sum(n for n, _ in prof.values()),
+            "graph_replay": graph}
 
 
 def bench_backward(args, dist, dev, stream, peaks, ola, torch, W):

@@ -98,3 +98,51 @@ def test_decode_workload_sampled():
     r = np.random.default_rng(1)
     seqs = sorted({int(np.argmin(lens)), int(np.argmax(lens)), *map(int, r.choice(len(lens), 2, replace=False))})
     run_and_compare(st, 3, seqs=seqs, what="decode workload")
+
+
+def test_decode_steps_replayed_from_a_cuda_graph():
+    """Several decoding steps captured once in a CUDA graph (a serving loop's
+    form: no host work per step) and replayed give the oracle's results; the
+    call does nothing on the host that capture forbids."""
+    import oracle
+
+    wl = W.DecodeWorkload("graph", 3, 8, 2, 128, 64, 64, 0, 0, 3, seed=12)
+    st = W.make_decode(wl, lens=[5, 70, 300])
+    m = st.meta
+    dev = "cuda"
+    kc0, vc0 = st.k_cache.to(dev), st.v_cache.to(dev)
+    kc, vc = kc0.clone(), vc0.clone()
+    bt = st.block_table.to(dev)
+    steps = 3
+    lens = (st.cache_lens[None, :].long() + torch.arange(steps)[:, None]).to(torch.int32).to(dev)
+    aff = [a.to(dev) for a in (st.alpha_base, st.beta_base, st.alpha_out, st.beta_out)]
+    q, kn, vn = st.q.to(dev), st.k_new.to(dev), st.v_new.to(dev)
+    ws = torch.empty(ola.orthros_decode_workspace_size(3, 8, 2, 128, m["max_pages"], m["page_size"]),
+                     dtype=torch.uint8, device=dev)
+    outs = [(torch.empty_like(q[0]), torch.empty((3, 8), dtype=torch.float32, device=dev), torch.empty_like(q[0]),
+             torch.empty((3, 8), dtype=torch.float32, device=dev)) for _ in range(steps)]
+    # warm up outside capture (first calls set kernel attributes), then restore the cache
+    ola.orthros_decode(q[0], kn[0], vn[0], kc, vc, bt, lens[0], *aff, wl.window, wl.scale, out=outs[0], workspace=ws)
+    torch.cuda.synchronize()
+    kc.copy_(kc0)
+    vc.copy_(vc0)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for s in range(steps):
+            ola.orthros_decode(q[s], kn[s], vn[s], kc, vc, bt, lens[s], *aff, wl.window, wl.scale, out=outs[s],
+                               workspace=ws)
+    kc.copy_(kc0)  # capture ran nothing; start from the initial cache anyway
+    vc.copy_(vc0)
+    g.replay()
+    torch.cuda.synchronize()
+    assert ola.orthros_check(ws) == (0, 0)
+    okc, ovc = f32(st.k_cache).copy(), f32(st.v_cache).copy()
+    olens = st.cache_lens.numpy().copy()
+    tol_o, tol_l = TOL[torch.bfloat16]
+    for s in range(steps):
+        ref = oracle.decode(f32(st.q[s]), f32(st.k_new[s]), f32(st.v_new[s]), okc, ovc, st.block_table.numpy(),
+                            olens, *(f32(a) for a in (st.alpha_base, st.beta_base, st.alpha_out, st.beta_out)),
+                            wl.window, wl.scale)
+        olens += 1
+        errs = [max_err(gg, r) for gg, r in zip(outs[s], ref)]
+        assert errs[0] <= tol_o and errs[2] <= tol_o and errs[1] <= tol_l and errs[3] <= tol_l, (s, errs)
