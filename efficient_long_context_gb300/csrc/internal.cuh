@@ -89,6 +89,7 @@ struct TcParams {
     int B, T, Hq, Hkv, window;
     float scale, scale_log2;
     int n_cross_units, n_base_units, base_nblk;
+    int n_out;  // rows of q_out (its tensor map)
     __nv_bfloat16 *o_base;
     float *lse_base;
     __nv_bfloat16 *o_out;

@@ -403,6 +403,7 @@ orthros_status orthros_prefill(const void *q, const void *k, const void *v, cons
     tp.scale_log2 = scale * log2e;
     tp.base_nblk = ceil_div(T, 128);
     tp.n_cross_units = n_cross_units;
+    tp.n_out = n_out;
     tp.n_base_units = B * Hkv * tc_units_per_kv(tp.base_nblk, g);
     tp.o_base = static_cast<__nv_bfloat16 *>(o_base);
     tp.lse_base = lse_base;

@@ -67,6 +67,7 @@ template <int D> struct Cfg {
 struct Meta {
     uint64_t k_full[kNumK], k_empty[kNumK], v_full[kNumV], v_empty[kNumV];
     uint64_t s_full[2], p_full[2], o_full[2], mma_done;
+    uint64_t q_full[2];  // per slot: raw query tile landed (TMA; rows contiguous in q or q_out)
     uint64_t xm_bar[2], lx_bar[2];  // per slot: row maxima / row sums exchanged between column halves
     uint32_t tmem_base;
     int abort;
@@ -156,6 +157,7 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int c) {
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qo,
                       const TcParams p) {
     using C = Cfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -184,6 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&mt.o_full[s], 1);
             mbar_init(&mt.xm_bar[s], 2 * kRowsPerTile);
             mbar_init(&mt.lx_bar[s], 2 * kRowsPerTile);
+            mbar_init(&mt.q_full[s], 1);
             mt.t_min[s] = 0x7fffffff;
             mt.t_max[s] = -1;
         }
@@ -199,6 +202,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kMmaWarp) {
         tmem_alloc(&mt.tmem_base, 512);
         tmem_relinquish();
+    }
+
+    // Query tiles whose rows are contiguous (base positions; output rows with
+    // their own q_out) arrive by TMA as raw bf16 and are turned into affined
+    // fp16 in place below; output rows that read q at their positions are
+    // gathered by the softmax threads.
+    auto q_by_tma = [&](const Slot &S) { return S.kind == 0 || (S.kind == 1 && p.q_out != nullptr); };
+    if (warp == kProducerWarp && lane == 0) {
+        for (int s = 0; s < 2; ++s) {
+            const Slot S = s ? sl1 : sl0;
+            if (S.kind < 0 || !q_by_tma(S)) continue;
+            mbar_arrive_expect_tx(&mt.q_full[s], C::kTileBytes);
+            const int row = S.kind == 0 ? S.b * p.T + S.row0 : S.row0;
+            for (int j = 0; j < C::kSub; ++j)
+                tma_load_3d(smem + C::kQ0 + s * C::kTileBytes + j * (kRowsPerTile * 128), S.kind == 0 ? &tm_q : &tm_qo,
+                            &mt.q_full[s], 64 * j, S.h, row);
+        }
     }
 
     // Base-position tiles know their band without reading any data, so the
@@ -251,18 +271,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         uint8_t *qs = smem + C::kQ0 + s_me * C::kTileBytes;
         constexpr int kHalfChunks = D / 16;  // 16-byte chunks per half row
+        const bool tma = S.kind >= 0 && q_by_tma(S);
+        if (tma && !mbar_wait_warp(&mt.q_full[s_me], 0, abort, p.status)) my_valid = false;
         if (my_valid) {
-            const __nv_bfloat16 *src;
-            if (S.kind == 1 && p.q_out)
-                src = p.q_out + ((long long)S.row0 + row) * p.Hq * D + (long long)S.h * D;
-            else
-                src = p.q + (((long long)S.b * p.T + my_t) * p.Hq + S.h) * D;
             const float *al = (S.kind == 0 ? p.alpha_base : p.alpha_out) + S.h * D;
             const float *be = (S.kind == 0 ? p.beta_base : p.beta_out) + S.h * D;
             bool over = false;
             uint4 raws[kHalfChunks];  // every load of the half row in flight at once
+            if (tma) {
 #pragma unroll
-            for (int cc = 0; cc < kHalfChunks; ++cc) raws[cc] = reinterpret_cast<const uint4 *>(src)[h_me * kHalfChunks + cc];
+                for (int cc = 0; cc < kHalfChunks; ++cc)
+                    raws[cc] = *reinterpret_cast<const uint4 *>(qs + sw128_offset<D>(row, h_me * kHalfChunks + cc));
+            } else {
+                const __nv_bfloat16 *src = p.q + (((long long)S.b * p.T + my_t) * p.Hq + S.h) * D;
+#pragma unroll
+                for (int cc = 0; cc < kHalfChunks; ++cc)
+                    raws[cc] = reinterpret_cast<const uint4 *>(src)[h_me * kHalfChunks + cc];
+            }
 #pragma unroll
             for (int cc = 0; cc < kHalfChunks; ++cc) {
                 const int c = h_me * kHalfChunks + cc;
@@ -623,9 +648,12 @@ bool make_kv_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int B
 
 template <int D>
 cudaError_t launch_d(const TcParams &p, const void *k16, const void *v, int units, cudaStream_t stream) {
-    CUtensorMap tk, tv;
+    CUtensorMap tk, tv, tq, tqo;
     if (!make_kv_map(&tk, k16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.B, p.T, p.Hkv, D) ||
-        !make_kv_map(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.B, p.T, p.Hkv, D))
+        !make_kv_map(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.B, p.T, p.Hkv, D) ||
+        !encode_kv_map_3d(&tq, p.q, (long long)p.B * p.T, p.Hq, D, kRowsPerTile) ||
+        !encode_kv_map_3d(&tqo, p.q_out ? (const void *)p.q_out : (const void *)p.q,
+                          p.q_out ? (long long)p.n_out : (long long)p.B * p.T, p.Hq, D, kRowsPerTile))
         return cudaErrorInvalidValue;
     static bool attr_set = false;
     if (!attr_set) {
@@ -634,7 +662,7 @@ cudaError_t launch_d(const TcParams &p, const void *k16, const void *v, int unit
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    prefill_tc_kernel<D><<<units, kThreads, Cfg<D>::kSmem, stream>>>(tk, tv, p);
+    prefill_tc_kernel<D><<<units, kThreads, Cfg<D>::kSmem, stream>>>(tk, tv, tq, tqo, p);
     return cudaGetLastError();
 }
 
