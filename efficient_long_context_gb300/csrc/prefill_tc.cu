@@ -68,6 +68,7 @@ struct Meta {
     uint64_t k_full[kNumK], k_empty[kNumK], v_full[kNumV], v_empty[kNumV];
     uint64_t s_full[2], p_full[2], o_full[2], mma_done;
     uint64_t q_full[2];  // per slot: raw query tile landed (TMA; rows contiguous in q or q_out)
+    uint64_t os_bar[2];  // per slot: normalised output tile staged for the TMA store
     uint64_t xm_bar[2], lx_bar[2];  // per slot: row maxima / row sums exchanged between column halves
     uint32_t tmem_base;
     int abort;
@@ -158,7 +159,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qo,
-                      const TcParams p) {
+                      const __grid_constant__ CUtensorMap tm_ob, const TcParams p) {
     using C = Cfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -187,6 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&mt.xm_bar[s], 2 * kRowsPerTile);
             mbar_init(&mt.lx_bar[s], 2 * kRowsPerTile);
             mbar_init(&mt.q_full[s], 1);
+            mbar_init(&mt.os_bar[s], 2 * kRowsPerTile);
             mt.t_min[s] = 0x7fffffff;
             mt.t_max[s] = -1;
         }
@@ -569,21 +571,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++cnt;
         }
         // ---------------- epilogue: o = O / l, lse = scale*m + ln l ----------------
-        // Row sums are exchanged through the (now idle) query tile of this slot.
+        // Every MMA has completed once o_full fires, so the key stages and the
+        // query tile are idle: row sums are exchanged through the first key
+        // stage; a base-position tile's normalised output is staged in its
+        // query tile (128-byte swizzle) and leaves by one TMA store (rows past
+        // T fall outside the map); output-row tiles store row by row.
         bool have = cnt > 0 && mbar_wait(&mt.o_full[s], 0, abort, p.status);
         have = __all_sync(0xffffffffu, have);
         if (have) {
             tc_fence_after();
-            float *lx = reinterpret_cast<float *>(smem + C::kQ0 + s * C::kTileBytes);  // [2][128]
+            float *lx = reinterpret_cast<float *>(smem + C::kK0 + s * 1024);  // [2][128]
             lx[hh * kRowsPerTile + row] = l;
             mbar_arrive(&mt.lx_bar[s]);
             have = __all_sync(0xffffffffu, mbar_wait(&mt.lx_bar[s], 0, abort, p.status));
             const float l_all = l + lx[(hh ^ 1) * kRowsPerTile + row];
+            const bool tile_store = S.kind == 0;  // warp-uniform
             const bool store = have && S.kind >= 0 && row < S.n;
+            uint8_t *stage = smem + C::kQ0 + s * C::kTileBytes;
             __nv_bfloat16 *dst = nullptr;
             float *lse_dst = nullptr;
             if (store && S.kind == 0) {
-                dst = p.o_base + (((long long)S.b * p.T + my_t) * p.Hq + S.h) * D + hh * (D / 2);
                 lse_dst = p.lse_base + ((long long)S.b * p.Hq + S.h) * p.T + my_t;
             } else if (store) {
                 dst = p.o_out + ((long long)(S.row0 + row) * p.Hq + S.h) * D + hh * (D / 2);
@@ -596,17 +603,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld32(t_o + 32 * j, o);
                 tmem_ld_wait();
                 reg_fence(o);
-                if (store) {
-                    uint4 w[4];
-                    uint32_t *wp = reinterpret_cast<uint32_t *>(w);
+                uint4 w[4];
+                uint32_t *wp = reinterpret_cast<uint32_t *>(w);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        wp[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+                for (int e = 0; e < 16; ++e)
+                    wp[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+                if (tile_store) {
+                    const int c0 = (hh * (D / 2) + 32 * j) / 8;  // first 16-byte chunk of these 32 channels
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) *reinterpret_cast<uint4 *>(stage + sw128_offset<D>(row, c0 + e)) = w[e];
+                } else if (store) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) reinterpret_cast<uint4 *>(dst + 32 * j)[e] = w[e];
                 }
             }
             if (store && hh == 0) *lse_dst = my_bad ? __int_as_float(0x7fc00000) : m_ref * p.scale + logf(l_all);
+            if (tile_store && have) {
+                fence_proxy_async_smem();
+                mbar_arrive(&mt.os_bar[s]);
+                const bool staged = __all_sync(0xffffffffu, mbar_wait(&mt.os_bar[s], 0, abort, p.status));
+                if (staged && row == 0 && hh == 0 && lane == 0) {
+                    for (int j = 0; j < C::kSub; ++j)
+                        tma_store_4d(&tm_ob, stage + j * (kRowsPerTile * 128), 64 * j, S.h, S.row0, S.b);
+                    bulk_commit();
+                    bulk_wait_read();
+                }
+            }
         }
     }
 
@@ -648,9 +670,10 @@ bool make_kv_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int B
 
 template <int D>
 cudaError_t launch_d(const TcParams &p, const void *k16, const void *v, int units, cudaStream_t stream) {
-    CUtensorMap tk, tv, tq, tqo;
+    CUtensorMap tk, tv, tq, tqo, tob;
     if (!make_kv_map(&tk, k16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.B, p.T, p.Hkv, D) ||
         !make_kv_map(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.B, p.T, p.Hkv, D) ||
+        !make_kv_map(&tob, p.o_base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.B, p.T, p.Hq, D) ||
         !encode_kv_map_3d(&tq, p.q, (long long)p.B * p.T, p.Hq, D, kRowsPerTile) ||
         !encode_kv_map_3d(&tqo, p.q_out ? (const void *)p.q_out : (const void *)p.q,
                           p.q_out ? (long long)p.n_out : (long long)p.B * p.T, p.Hq, D, kRowsPerTile))
@@ -662,7 +685,7 @@ cudaError_t launch_d(const TcParams &p, const void *k16, const void *v, int unit
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    prefill_tc_kernel<D><<<units, kThreads, Cfg<D>::kSmem, stream>>>(tk, tv, tq, tqo, p);
+    prefill_tc_kernel<D><<<units, kThreads, Cfg<D>::kSmem, stream>>>(tk, tv, tq, tqo, tob, p);
     return cudaGetLastError();
 }
 
