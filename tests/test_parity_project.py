@@ -81,8 +81,10 @@ SMALL = [
     W.ProjectionWorkload("tiny", 3, 2, 64, 2, 1, 64, seed=1),
     W.ProjectionWorkload("decode_pair", 5, 5, 256, 4, 2, 128, seed=2),
     W.ProjectionWorkload("rows_past_tile", 130, 7, 192, 4, 2, 64, seed=3),
-    W.ProjectionWorkload("wide", 300, 0, 512, 8, 2, 128, seed=4),   # 256-wide tiles once enough rows
+    W.ProjectionWorkload("wide", 300, 0, 512, 8, 2, 128, seed=4),
     W.ProjectionWorkload("no_base", 0, 9, 128, 4, 4, 64, seed=5),
+    W.ProjectionWorkload("short_tile_edge", 33, 31, 320, 4, 2, 64, seed=6),  # 64 rows: the 64-row x slices
+    W.ProjectionWorkload("one_full_tile", 40, 41, 256, 4, 2, 128, seed=7),   # 81 rows: 128-row x slices
 ]
 
 
