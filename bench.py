@@ -284,7 +284,7 @@ def _timed(ola, torch, dist, stream, fn, steps):
 
 
 def bench_prefill(args, dist, dev, stream, peaks, ola, torch, W):
-    wl = W.PREFILL_128K
+    wl = {"128k": W.PREFILL_128K, "pt": W.PT_2K, "sft": W.SFT_8K}[args.prefill_workload]
     if args.prefill_T:
         import dataclasses
 
@@ -307,7 +307,14 @@ def bench_prefill(args, dist, dev, stream, peaks, ola, torch, W):
     ws = torch.empty(ola.orthros_prefill_workspace_size(wl.B, wl.T, wl.Hq, wl.Hkv, wl.d, n_out, wl.window,
                                                         wl.dtype), dtype=torch.uint8, device=dev)
 
+    # training-shape workloads fit in L2: a buffer twice its size is rewritten before each step
+    in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v))
+    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev) if in_bytes < 2 * l2_bytes else None
+
     def step(_=0):
+        if flush is not None:
+            flush.fill_(1)
         ola.orthros_prefill(q, k, v, *aff, indptr, pos, wl.window, wl.scale, out=outs, k_cache=k_cache,
                             v_cache=v_cache, block_table=block_table, page_size=P, workspace=ws, stream=stream)
 
@@ -330,10 +337,13 @@ def bench_prefill(args, dist, dev, stream, peaks, ola, torch, W):
     dom_flops = flops["swa"] + tile_cross if dom == "prefill_tc" else flops["total"]
     achieved = dom_flops / (dom_ms / dom_n * 1e-3) / 1e12
     res = dict(wl=wl, inputs=inputs, flops=flops, ms_step=ms_step, prof=prof, P=P,
+               l2=(f"L2 flushed before each step ({2 * l2_bytes >> 20} MiB written, inside the step time)"
+                   if flush is not None else "inputs larger than L2; no flush"),
                value=flops["total"] * dist.world / (ms_step * 1e-3) / 1e12,
                roofline={"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peaks["bf16"],
                          "unit": "TFLOP/s", "frac": achieved / peaks["bf16"],
-                         "traffic": captured_traffic("prefill_tc") if dom == "prefill_tc" and wl.T == 131072 else None,
+                         "traffic": captured_traffic("prefill_tc")
+                         if dom == "prefill_tc" and wl.name == W.PREFILL_128K.name else None,
                          "peak_source": f"{peaks['src']} bf16 dense (burst)", "avg_launch_ms": dom_ms / dom_n,
                          "useful_tflop_per_launch": dom_flops / 1e12})
     if args.only == "all":
@@ -624,9 +634,12 @@ def run_ours(args, dist):
         "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) q/k/v, affines 1+0.1N / 0.1N; no dataset)",
         "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
-                   "window": wl.window, "out_rows": "last position (prefill regime)", "page_size": pre["P"],
+                   "window": wl.window, "page_size": pre["P"],
+                   "out_rows": ("last position (prefill regime)" if wl.out_mode == "last" else
+                                "every position (pre-training)" if wl.out_mode == "all" else
+                                f"last {wl.out_mode[1]} positions of each sequence (fine-tuning answer span)"),
                    "useful_tflop_per_step": pre["flops"]["total"] / 1e12,
-                   "l2": "inputs larger than L2 (q 1 GiB, k/v 256 MiB each); no flush",
+                   "l2": pre["l2"],
                    "parallelism": f"replicas x{dist.world}"},
         "roofline": pre["roofline"],
         "kernels": {n: {"launches": c, "total_ms": t} for n, (c, t) in pre["prof"].items()},
@@ -652,6 +665,8 @@ def main():
                     help="decoding steps to time (default: the workload's 128)")
     ap.add_argument("--only", choices=("all", "prefill", "decode", "backward", "extend", "project"), default="all",
                     help="run one part (profiling captures); the headline line needs 'all'")
+    ap.add_argument("--prefill-workload", choices=("128k", "pt", "sft"), default="128k",
+                    help="prefill workload: the 128K headline, or the pre-training / fine-tuning shapes")
     ap.add_argument("--prefill-T", type=int, default=None,
                     help="shorter prefill (a smaller case of the same kernels, for profiler captures)")
     ap.add_argument("--decode-B", type=int, default=None, help="fewer decoding sequences (profiler captures)")
