@@ -33,20 +33,23 @@ constexpr int kThreadsP = 192;
 constexpr int kProducerWarpP = 4;
 constexpr int kMmaWarpP = 5;
 
-template <int BN> struct PCfg {
-    static constexpr int kStages = BN == 256 ? 4 : 8;
-    static constexpr int kABytes = kBM * kBK * 2;  // 16 KB
-    static constexpr int kBBytes = BN * kBK * 2;   // 32 KB or 8 KB
+// KS = 128-byte swizzle atoms of K per stage (one stage = KS * 64 channels).
+template <int BN, int KS> struct PCfg {
+    static constexpr int kStages = (BN == 256 ? 4 : 8) / KS;
+    static constexpr int kASub = kBM * kBK * 2;  // 16 KB per atom
+    static constexpr int kBSub = BN * kBK * 2;   // 32 KB or 8 KB per atom
+    static constexpr int kABytes = KS * kASub;
+    static constexpr int kBBytes = KS * kBSub;
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kBar = kStages * kStageBytes;
     static constexpr int kSmem = kBar + 256 + 1024;
 };
 
-template <int BN>
+template <int BN, int KS>
 __global__ void __launch_bounds__(kThreadsP, 1)
     project_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                       const ProjParams p) {
-    using C = PCfg<BN>;
+    using C = PCfg<BN, KS>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBar);
@@ -57,7 +60,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     volatile int *abort = abort_flag;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n0 = blockIdx.x * BN, m0 = blockIdx.y * kBM;
-    const int k_tiles = p.d_model / kBK;
+    const int k_tiles = p.d_model / (kBK * KS);
 
     if (tid == 0) {
         for (int s = 0; s < C::kStages; ++s) {
@@ -90,8 +93,11 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                 if (kt >= C::kStages && !mbar_wait(&empty[s], ((kt / C::kStages) - 1) & 1, abort, p.status)) break;
                 uint8_t *a = smem + s * C::kStageBytes;
                 mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-                tma_load_3d(a, &tm_x, &full[s], kt * kBK, 0, m0);
-                tma_load_3d(a + C::kABytes, &tm_w, &full[s], kt * kBK, 0, n0);
+#pragma unroll
+                for (int j = 0; j < KS; ++j) {
+                    tma_load_3d(a + j * C::kASub, &tm_x, &full[s], (kt * KS + j) * kBK, 0, m0);
+                    tma_load_3d(a + C::kABytes + j * C::kBSub, &tm_w, &full[s], (kt * KS + j) * kBK, 0, n0);
+                }
                 issued = kt + 1;
             }
             // nothing may land in shared memory after the CTA exits
@@ -109,9 +115,12 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                 if (!mbar_wait(&full[s], (kt / C::kStages) & 1, abort, p.status)) break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk)
-                    mma_ss(tmem, da + s * kStageU + ((kk * 32) >> 4), db + s * kStageU + ((kk * 32) >> 4), kId,
-                           (kt > 0 || kk > 0) ? 1u : 0u);
+                for (int j = 0; j < KS; ++j)
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        mma_ss(tmem, da + s * kStageU + ((j * C::kASub + kk * 32) >> 4),
+                               db + s * kStageU + ((j * C::kBSub + kk * 32) >> 4), kId,
+                               (kt > 0 || j > 0 || kk > 0) ? 1u : 0u);
                 tc_commit(&empty[s]);
             }
             tc_commit(acc_full);
@@ -185,8 +194,9 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     }
 }
 
-template <int BN>
+template <int BN, int KS>
 cudaError_t launch_bn(const ProjParams &p, cudaStream_t stream) {
+    using C = PCfg<BN, KS>;
     CUtensorMap tx, tw;
     const int N = (p.Hq + 2 * p.Hkv) * p.d;
     if (!encode_kv_map_3d(&tx, p.x, (long long)p.n_base + p.n_out, 1, p.d_model, kBM) ||
@@ -194,13 +204,13 @@ cudaError_t launch_bn(const ProjParams &p, cudaStream_t stream) {
         return cudaErrorInvalidValue;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(project_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             PCfg<BN>::kSmem);
+        cudaError_t e =
+            cudaFuncSetAttribute(project_tc_kernel<BN, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
         if (e != cudaSuccess) return e;
         attr = true;
     }
     const dim3 grid(N / BN, (p.n_base + p.n_out + kBM - 1) / kBM);
-    project_tc_kernel<BN><<<grid, kThreadsP, PCfg<BN>::kSmem, stream>>>(tx, tw, p);
+    project_tc_kernel<BN, KS><<<grid, kThreadsP, C::kSmem, stream>>>(tx, tw, p);
     return cudaGetLastError();
 }
 
@@ -213,8 +223,9 @@ cudaError_t launch_project_tc(const ProjParams &p, cudaStream_t stream) {
     int dev = 0, sms = 152;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     // wide tiles when they already fill the GPU, narrow ones for few rows
-    if (N % 256 == 0 && m_tiles * (N / 256) >= sms) return launch_bn<256>(p, stream);
-    return launch_bn<64>(p, stream);
+    if (N % 256 == 0 && m_tiles * (N / 256) >= sms) return launch_bn<256, 1>(p, stream);
+    if (p.d_model % (2 * kBK) == 0) return launch_bn<64, 2>(p, stream);
+    return launch_bn<64, 1>(p, stream);
 }
 
 }  // namespace orthros
