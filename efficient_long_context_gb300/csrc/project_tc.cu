@@ -9,12 +9,13 @@
 // entries (the output stream never writes the cache). In decoding the base
 // and output token of every sequence share one read of the weight.
 //
-// Design: a CTA computes a 128-row x BN-column tile of y (BN = 256, or 64 when
-// there are few rows, so that enough CTAs stream the weight). Warp 4 streams
-// 64-wide K slices of x and of the weight (stored K-major, one output column
-// per row) with TMA, 128-byte swizzle; warp 5 issues tcgen05.mma (M=128,
-// N=BN, K=16) into a TMEM accumulator; warps 0-3 (thread = tile row = TMEM
-// lane) read the accumulator 32 columns at a time, apply the affine to query
+// Design: a CTA computes a BM-row x BN-column tile of y (BN = 256, or 64 when
+// there are few rows, so that enough CTAs stream the weight; BM = 128, or 64
+// when the call has at most 64 rows). Warp 4 streams K slices of x and of the
+// weight (stored K-major, one output column per row) with TMA, 128-byte
+// swizzle, one or two 64-channel atoms per stage; warp 5 issues tcgen05.mma
+// (M=BM, N=BN, K=16) into a TMEM accumulator; warps 0-3 read the accumulator
+// 32 columns at a time (one thread per tile row), apply the affine to query
 // columns, round to bf16 and store: queries to q_base / q_out, keys and values
 // to k_out / v_out and/or straight into the row's page slot.
 #include <cuda.h>
@@ -34,9 +35,12 @@ constexpr int kProducerWarpP = 4;
 constexpr int kMmaWarpP = 5;
 
 // KS = 128-byte swizzle atoms of K per stage (one stage = KS * 64 channels).
-template <int BN, int KS> struct PCfg {
-    static constexpr int kStages = (BN == 256 ? 4 : 8) / KS;
-    static constexpr int kASub = kBM * kBK * 2;  // 16 KB per atom
+// BM = rows per tile: 128, or 64 when the whole call has at most 64 rows (a
+// decoding step); an M=64 accumulator puts rows 16q .. 16q+15 in TMEM lanes
+// 32q .. 32q+15, so epilogue warp q owns 16 rows in its lanes 0-15.
+template <int BN, int KS, int BM> struct PCfg {
+    static constexpr int kStages = (BN == 256 ? 4 : (BM == 64 ? 12 : 8)) / KS;
+    static constexpr int kASub = BM * kBK * 2;   // 16 KB (8 KB) per atom
     static constexpr int kBSub = BN * kBK * 2;   // 32 KB or 8 KB per atom
     static constexpr int kABytes = KS * kASub;
     static constexpr int kBBytes = KS * kBSub;
@@ -45,11 +49,11 @@ template <int BN, int KS> struct PCfg {
     static constexpr int kSmem = kBar + 256 + 1024;
 };
 
-template <int BN, int KS>
+template <int BN, int KS, int BM>
 __global__ void __launch_bounds__(kThreadsP, 1)
     project_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                       const ProjParams p) {
-    using C = PCfg<BN, KS>;
+    using C = PCfg<BN, KS, BM>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBar);
@@ -59,7 +63,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
     volatile int *abort = abort_flag;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n0 = blockIdx.x * BN, m0 = blockIdx.y * kBM;
+    const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
     const int k_tiles = p.d_model / (kBK * KS);
 
     if (tid == 0) {
@@ -106,7 +110,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         }
     } else if (warp == kMmaWarpP) {
         if (lane == 0) {
-            constexpr uint32_t kId = idesc_f16(1, 1, 0, 0, kBM, BN);
+            constexpr uint32_t kId = idesc_f16(1, 1, 0, 0, BM, BN);
             const uint64_t da = desc_sw128(smem_u32(smem), 16, 1024);
             const uint64_t db = desc_sw128(smem_u32(smem + C::kABytes), 16, 1024);
             constexpr uint32_t kStageU = C::kStageBytes >> 4;
@@ -128,14 +132,14 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         }
     } else {
         // ---------------- epilogue: thread = tile row ----------------
-        const int r = m0 + warp * 32 + lane;
+        const int r = m0 + warp * (BM / 4) + lane;
         const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
         const bool got = mbar_wait_warp(acc_full, 0, abort, p.status);
         if (got) {
             tc_fence_after();
             const int Nq = p.Hq * p.d, Nkv = p.Hkv * p.d;
             const bool base = r < p.n_base;
-            const bool live = r < p.n_base + p.n_out;
+            const bool live = lane < BM / 4 && r < p.n_base + p.n_out;
             // the page slot of a base row's K/V
             long long slot = -1;
             if (live && base && p.k_cache) {
@@ -194,23 +198,23 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     }
 }
 
-template <int BN, int KS>
+template <int BN, int KS, int BM>
 cudaError_t launch_bn(const ProjParams &p, cudaStream_t stream) {
-    using C = PCfg<BN, KS>;
+    using C = PCfg<BN, KS, BM>;
     CUtensorMap tx, tw;
     const int N = (p.Hq + 2 * p.Hkv) * p.d;
-    if (!encode_kv_map_3d(&tx, p.x, (long long)p.n_base + p.n_out, 1, p.d_model, kBM) ||
+    if (!encode_kv_map_3d(&tx, p.x, (long long)p.n_base + p.n_out, 1, p.d_model, BM) ||
         !encode_kv_map_3d(&tw, p.w_t, N, 1, p.d_model, BN))
         return cudaErrorInvalidValue;
     static bool attr = false;
     if (!attr) {
         cudaError_t e =
-            cudaFuncSetAttribute(project_tc_kernel<BN, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+            cudaFuncSetAttribute(project_tc_kernel<BN, KS, BM>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    const dim3 grid(N / BN, (p.n_base + p.n_out + kBM - 1) / kBM);
-    project_tc_kernel<BN, KS><<<grid, kThreadsP, C::kSmem, stream>>>(tx, tw, p);
+    const dim3 grid(N / BN, (p.n_base + p.n_out + BM - 1) / BM);
+    project_tc_kernel<BN, KS, BM><<<grid, kThreadsP, C::kSmem, stream>>>(tx, tw, p);
     return cudaGetLastError();
 }
 
@@ -223,9 +227,10 @@ cudaError_t launch_project_tc(const ProjParams &p, cudaStream_t stream) {
     int dev = 0, sms = 152;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     // wide tiles when they already fill the GPU, narrow ones for few rows
-    if (N % 256 == 0 && m_tiles * (N / 256) >= sms) return launch_bn<256, 1>(p, stream);
-    if (p.d_model % (2 * kBK) == 0) return launch_bn<64, 2>(p, stream);
-    return launch_bn<64, 1>(p, stream);
+    if (N % 256 == 0 && m_tiles * (N / 256) >= sms) return launch_bn<256, 1, kBM>(p, stream);
+    const bool k2 = p.d_model % (2 * kBK) == 0;
+    if ((long long)p.n_base + p.n_out <= 64) return k2 ? launch_bn<64, 2, 64>(p, stream) : launch_bn<64, 1, 64>(p, stream);
+    return k2 ? launch_bn<64, 2, kBM>(p, stream) : launch_bn<64, 1, kBM>(p, stream);
 }
 
 }  // namespace orthros
