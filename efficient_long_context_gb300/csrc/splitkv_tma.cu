@@ -5,7 +5,7 @@
 // per step (Orthros paper, Sec. 3.3: decoding is I/O-bound; Sec. 3.2
 // "Decoding": the base and the output token of a step read the same cache).
 // This version keeps the memory system busy without per-thread address work:
-//   * one CTA per SM loops over work items (row group, 2048-key chunk);
+//   * one CTA per SM loops over work items (row group, key chunk), chunk-major;
 //   * one producer thread streams 128-key stages with TMA (64-token boxes,
 //     128-byte swizzle) through a 3-stage ring (6 for d = 64) and keeps
 //     streaming across item boundaries, so no pipeline refill between items;
@@ -163,6 +163,10 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     volatile int *abort = abort_flag;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gsz = p.Hq / p.Hkv;
+    // Items run chunk-major: CTAs that run at the same time read the same
+    // token range of every group (all kv heads of a token row, 2 KB of
+    // contiguous cache for GQA 32/8), not distant ranges of one head.
+    const int n_groups = total_items / p.max_chunks;
 
     if (tid == 0) {
         for (int s = 0; s < C::kStages; ++s) {
@@ -185,7 +189,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         if (lane != 0) return;
         uint32_t sc = 0;  // stages issued so far
         for (int item = blockIdx.x; item < total_items && !*abort; item += gridDim.x) {
-            const int group = p.group_offset + item / p.max_chunks, chunk = item % p.max_chunks;
+            const int group = p.group_offset + item % n_groups, chunk = item / n_groups;
             const ItemInfo it = item_info(p, group);
             const int key_lo = max(chunk * p.chunk, it.union_lo);
             const int key_hi = min(it.union_hi, chunk * p.chunk + p.chunk - 1);
@@ -240,7 +244,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         return __all_sync(0xffffffffu, got);
     };
     for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
-        const int group = p.group_offset + item / p.max_chunks, chunk = item % p.max_chunks;
+        const int group = p.group_offset + item % n_groups, chunk = item / n_groups;
         const ItemInfo it = item_info(p, group);
         const int key_lo = max(chunk * p.chunk, it.union_lo);
         const int key_hi = min(it.union_hi, chunk * p.chunk + p.chunk - 1);
