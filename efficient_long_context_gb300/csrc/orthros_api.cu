@@ -35,9 +35,37 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 int elem_bytes(orthros_dtype t) { return t == ORTHROS_F32 ? 4 : 2; }
 
-// Split-KV chunk sizes (keys per CTA; multiples of 64).
-constexpr int kPrefillChunk = 1024;
-constexpr int kDecodeChunk = 2048;
+// Split-KV work items cover `chunk` keys of one row group: the longest of
+// 8192 .. 512 keys (multiples of the kernels' 128-key stages) that still gives
+// every SM three items. Long items amortise each item's query load and state
+// merge; short ones keep small batches spread over the GPU.
+constexpr int kChunkMax = 8192;
+constexpr int kChunkMin = 512;
+
+int device_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+        n > 0)
+        return n;
+    return 152;
+}
+
+int split_chunk(long long n_groups, long long keys) {
+    const long long want = 3LL * device_sms();
+    for (int c = kChunkMax; c > kChunkMin; c /= 2)
+        if (n_groups * ((keys + c - 1) / c) >= want) return c;
+    return kChunkMin;
+}
+
+// Partial slots (group x chunk) that a launch with at most max_groups groups
+// can use: with the largest chunk, n * ceil(keys / 8192); otherwise the chosen
+// chunk c was taken because 2c gave fewer than 3 items per SM, so
+// n * ceil(keys / c) <= 2 n * ceil(keys / 2c) < 6 items per SM.
+long long split_slots_bound(long long max_groups, long long keys) {
+    const long long lo = max_groups * ((keys + kChunkMax - 1) / kChunkMax);
+    const long long hi = max_groups * ((keys + kChunkMin - 1) / kChunkMin);
+    return std::min(hi, std::max(lo, 6LL * device_sms()));
+}
 // A sequence's output rows take the split-KV kernel when all of its rows fit
 // in at most this many 16-row groups per kv head; otherwise the tile kernel.
 constexpr int kSplitRowsMax = 256;
@@ -47,34 +75,36 @@ int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 // Workspace regions of orthros_prefill.
 struct PrefillLayout {
     size_t blob_off, k16_off, part_off, total;
-    int max_groups, max_chunks;
+    int max_groups;
+    long long part_slots;
 };
 
 PrefillLayout prefill_layout(int B, int T, int Hkv, int d, int n_out, orthros_dtype dtype) {
     PrefillLayout L{};
     size_t at = kStatusBytes;
     L.max_groups = dtype == ORTHROS_BF16 ? (int)std::min<long long>((long long)n_out, 16LL * B) * Hkv : 0;
-    L.max_chunks = ceil_div(T, kPrefillChunk);
+    L.part_slots = split_slots_bound(L.max_groups, T);
     L.blob_off = at;
     at += align_up(sizeof(int32_t) * (size_t)(2 * (B + 1) + 3 * (size_t)L.max_groups), 256);
     L.k16_off = at;
     if (dtype == ORTHROS_BF16) at += align_up((size_t)B * T * Hkv * d * 2, 256);
     L.part_off = at;
-    at += align_up(split_partial_bytes(L.max_groups, L.max_chunks, d), 256);
+    at += align_up((size_t)L.part_slots * split_partial_bytes(1, 1, d), 256);
     L.total = at;
     return L;
 }
 
 struct DecodeLayout {
     size_t part_off, total;
-    int max_chunks;
+    int chunk, max_chunks;
 };
 
 DecodeLayout decode_layout(int B, int Hkv, int d, int max_pages, int page_size, orthros_dtype dtype) {
     DecodeLayout L{};
     size_t at = kStatusBytes;
     L.part_off = at;
-    L.max_chunks = ceil_div((long long)max_pages * page_size, kDecodeChunk);
+    L.chunk = split_chunk((long long)B * Hkv, (long long)max_pages * page_size);
+    L.max_chunks = ceil_div((long long)max_pages * page_size, L.chunk);
     if (dtype == ORTHROS_BF16) at += align_up(split_partial_bytes(B * Hkv, L.max_chunks, d), 256);
     L.total = at;
     return L;
@@ -119,7 +149,8 @@ BackwardLayout backward_layout(int B, int T, int Hq, int d, int n_out, orthros_d
 // Workspace regions of orthros_extend.
 struct ExtendLayout {
     size_t blob_off, part_off, total;
-    int max_groups, max_chunks;
+    int max_groups;
+    long long part_slots;
 };
 
 ExtendLayout extend_layout(int B, int n_new, int n_out, int Hq, int Hkv, int d, int max_pages, int page_size,
@@ -130,11 +161,11 @@ ExtendLayout extend_layout(int B, int n_new, int n_out, int Hq, int Hkv, int d, 
     // at most one group per position of each (sequence, kv head), plus one partial group per class
     const long long groups = ((long long)n_new + n_out + 2LL * B) * Hkv;
     L.max_groups = dtype == ORTHROS_BF16 ? (int)std::min<long long>(groups, 1LL << 30) : 0;
-    L.max_chunks = ceil_div((long long)max_pages * page_size, kDecodeChunk);
+    L.part_slots = split_slots_bound(L.max_groups, (long long)max_pages * page_size);
     L.blob_off = at;
     at += align_up(sizeof(int32_t) * (size_t)(2 * (B + 1) + 4 * (size_t)L.max_groups), 256);
     L.part_off = at;
-    at += align_up(split_partial_bytes(L.max_groups, L.max_chunks, d), 256);
+    at += align_up((size_t)L.part_slots * split_partial_bytes(1, 1, d), 256);
     L.total = at;
     return L;
 }
@@ -373,8 +404,10 @@ orthros_status orthros_prefill(const void *q, const void *k, const void *v, cons
         sp.scale = scale;
         sp.scale_log2 = scale * log2e;
         sp.n_groups = n_groups;
-        sp.chunk = kPrefillChunk;
-        sp.max_chunks = lay.max_chunks;
+        sp.chunk = split_chunk(n_groups, T);
+        sp.max_chunks = ceil_div(T, sp.chunk);
+        if ((long long)n_groups * sp.max_chunks > lay.part_slots)
+            return fail(ORTHROS_EWORKSPACE, "internal: split partials exceed the workspace plan");
         sp.kv_tokens = (long long)B * T;
         sp.partial = reinterpret_cast<float *>(ws + lay.part_off);
         sp.o_out = static_cast<__nv_bfloat16 *>(o_out);
@@ -697,8 +730,10 @@ orthros_status orthros_extend(const void *q, const void *q_out, const void *k_ne
         sp.scale = scale;
         sp.scale_log2 = scale * 1.4426950408889634f;
         sp.n_groups = n_groups;
-        sp.chunk = kDecodeChunk;
-        sp.max_chunks = lay.max_chunks;
+        sp.chunk = split_chunk(n_groups, (long long)max_pages * page_size);
+        sp.max_chunks = ceil_div((long long)max_pages * page_size, sp.chunk);
+        if ((long long)n_groups * sp.max_chunks > lay.part_slots)
+            return fail(ORTHROS_EWORKSPACE, "internal: split partials exceed the workspace plan");
         sp.kv_tokens = kv_tokens;
         sp.partial = reinterpret_cast<float *>(ws + lay.part_off);
         sp.o_base = static_cast<__nv_bfloat16 *>(o_base);
@@ -907,7 +942,7 @@ orthros_status orthros_decode(const void *q, const void *q_out, const void *k_ne
         sp.scale = scale;
         sp.scale_log2 = scale * 1.4426950408889634f;
         sp.n_groups = B * Hkv;
-        sp.chunk = kDecodeChunk;
+        sp.chunk = lay.chunk;
         sp.max_chunks = lay.max_chunks;
         sp.kv_tokens = (long long)num_pages * page_size;
         sp.partial = reinterpret_cast<float *>(static_cast<char *>(workspace) + lay.part_off);
