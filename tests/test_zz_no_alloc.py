@@ -55,9 +55,14 @@ def test_static_decode_refuses_sizes_beyond_the_array():
     # host-side refusal: no launch happens, so this also runs without a GPU
     lib = ola.load_library()
     fake = ctypes.c_void_p(1 << 12)
-    # 32 sequences x 8 kv heads with 600 pages of 64 tokens need ~40 MB of partials
-    rc = lib.orthros_decode_static(fake, None, fake, fake, fake, fake, fake, 600, 64, 20000, fake,
-                                   fake, fake, fake, fake, 32, 32, 8, 128, 4096, 0.088, 0,
+    B, Hq, Hkv, d, max_pages, page_size = 128, 32, 8, 128, 600, 64
+    # 128 sequences x 8 kv heads over 600 pages of 64 tokens need ~43 MB of
+    # partials; the fake pointers below are only safe because the host refuses
+    # the call before any launch, so make sure first that the size is refused
+    need = ola.orthros_decode_workspace_size(B, Hq, Hkv, d, max_pages, page_size)
+    assert need > 32 << 20, need
+    rc = lib.orthros_decode_static(fake, None, fake, fake, fake, fake, fake, max_pages, page_size, 20000, fake,
+                                   fake, fake, fake, fake, B, Hq, Hkv, d, 4096, 0.088, 0,
                                    fake, fake, fake, fake, None)
     assert rc == 4, rc
     assert "static array" in ola.orthros_last_error()
