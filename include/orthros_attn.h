@@ -35,6 +35,10 @@
  *     workspace; the affected rows are skipped or their outputs are NaN, and
  *     orthros_check() reports ORTHROS_EDEVICE. Nothing aborts or traps.
  *   - Supported head sizes: d = 64 or 128.
+ *   - The *_workspace_size functions size the scratch for the CUDA device that
+ *     is current when they are called (the split-KV partials depend on its SM
+ *     count); call them with the device that will run the call current. A
+ *     workspace smaller than the call then needs returns ORTHROS_EWORKSPACE.
  */
 #ifndef ORTHROS_ATTN_H
 #define ORTHROS_ATTN_H
