@@ -118,9 +118,15 @@ def _raise_if(rc: int, lib):
 
 
 def _ptr(t):
+    """Device address of a tensor argument. Every tensor the library reads or
+    writes must live on the current CUDA device: a host tensor's address
+    handed to a kernel would make it read host memory. Raised here, while the
+    call's arguments are marshalled, so nothing is launched."""
     if t is None:
         return None
     if isinstance(t, torch.Tensor):
+        if not t.is_cuda or t.device.index != torch.cuda.current_device():
+            raise OrthrosError(1, f"tensor on {t.device}: every tensor argument must be on the current CUDA device")
         return ctypes.c_void_p(t.data_ptr()) if t.numel() else ctypes.c_void_p(0)
     return t
 

@@ -212,3 +212,13 @@ def test_binding_does_not_import_oracle():
     for fn in os.listdir(os.path.join(ROOT, "efficient_long_context_gb300", "csrc")):
         assert "orthros_ref" not in open(os.path.join(ROOT, "efficient_long_context_gb300", "csrc", fn)).read()
     assert torch is not None and sys is not None
+
+
+def test_host_tensors_are_refused_before_any_call():
+    """A host tensor's address must never reach a kernel: the marshalling
+    helper refuses it (checked on the helper itself, so no call is made)."""
+    from efficient_long_context_gb300 import _binding
+
+    with pytest.raises(_binding.OrthrosError, match="current CUDA device"):
+        _binding._ptr(torch.zeros(4))
+    assert _binding._ptr(None) is None
