@@ -15,16 +15,17 @@ stays in the library's kernels:
 * output rows (Eq. 5): a row at position t attends keys 0 .. t, spread over
   every rank whose chunk starts at or before t. Each such rank computes the
   row over its own keys only (an output row of a separate call on its chunk),
-  giving a partial (o_r, lse_r); the owner of position t merges them exactly:
+  giving a partial (o_r, lse_r), and sends it point to point to the owner of
+  position t, which merges them exactly:
   lse = log sum_r exp(lse_r), o = sum_r exp(lse_r - lse) o_r.
 
 ``attend`` is the single-device attention call (``orthros_prefill`` on a GPU);
 it receives torch tensors of one rank and returns (o_base, lse_base, o_out,
 lse_out). The exchange uses torch.distributed (NCCL between GPUs, gloo for
-CPU tensors). Partials of every output row are all-gathered, which suits the
-prefill and fine-tuning regimes (one row / an answer span per sequence); a
-pre-training regime with every position an output row would reduce-scatter
-them to their owners instead.
+CPU tensors). A rank receives only the partials of the rows it owns, from the
+ranks before it, so the output-row exchange moves each partial once however
+many rows there are (one per sequence when prefilling, an answer span when
+fine-tuning, every position when pre-training).
 """
 from __future__ import annotations
 
@@ -78,6 +79,38 @@ def _exchange_halo(k, v, T, window, world, rank, group):
         k_halo[:, a:a + kb.shape[1]] = kb
         v_halo[:, a:a + vb.shape[1]] = vb
     return k_halo, v_halo
+
+
+def _partials_to_owners(o_part, lse_part, pos, rows, T, world, rank, group):
+    """Send this rank's partials of rows owned by later ranks to their owners
+    and receive, from every earlier rank, its partials of the rows this rank
+    owns (a rank holds a partial of every row at or after its chunk start).
+    Returns the partials of this rank's rows, [rank + 1, len(rows), ...]:
+    its own first, then those of ranks 0 .. rank-1."""
+    owner = torch.full_like(pos, -1)
+    for s in range(world):
+        s0, s1 = chunk_bounds(T, world, s)
+        owner[(pos >= s0) & (pos < s1)] = s
+    ops = []
+    for s in range(rank + 1, world):
+        sel = torch.nonzero(owner == s).flatten().to(o_part.device)
+        if len(sel):
+            ops.append(dist.P2POp(dist.isend, o_part[sel].contiguous(), s, group))
+            ops.append(dist.P2POp(dist.isend, lse_part[sel].contiguous(), s, group))
+    rd = rows.to(o_part.device)
+    o_in, l_in = [o_part[rd]], [lse_part[rd]]
+    if len(rows):
+        for r in range(rank):
+            ob = o_part.new_empty((len(rows),) + tuple(o_part.shape[1:]))
+            lb = lse_part.new_empty((len(rows),) + tuple(lse_part.shape[1:]))
+            ops.append(dist.P2POp(dist.irecv, ob, r, group))
+            ops.append(dist.P2POp(dist.irecv, lb, r, group))
+            o_in.append(ob)
+            l_in.append(lb)
+    if ops:
+        for req in dist.batch_isend_irecv(ops):
+            req.wait()
+    return torch.stack(o_in), torch.stack(l_in)
 
 
 def sp_prefill(q, k, v, alpha_base, beta_base, alpha_out, beta_out, out_indptr, out_positions, window, scale,
@@ -150,17 +183,11 @@ def sp_prefill(q, k, v, alpha_base, beta_base, alpha_out, beta_out, out_indptr, 
         o_part[sel.to(q.device)] = o_r.float()
         lse_part[sel.to(q.device)] = lse_r.float()
     if world > 1:
-        o_all = [torch.empty_like(o_part) for _ in range(world)]
-        l_all = [torch.empty_like(lse_part) for _ in range(world)]
-        dist.all_gather(o_all, o_part, group=group)
-        dist.all_gather(l_all, lse_part, group=group)
-        o_all = torch.stack(o_all)
-        l_all = torch.stack(l_all)
+        o_rows, l_rows = _partials_to_owners(o_part, lse_part, pos, rows, T, world, rank, group)
     else:
-        o_all, l_all = o_part[None], lse_part[None]
-    rd = rows.to(q.device)
-    l_rows = l_all[:, rd]                      # [world, rows, Hq]
-    lse = torch.logsumexp(l_rows, dim=0)       # ranks without keys carry -inf
-    wgt = torch.exp(l_rows - lse[None])        # [world, rows, Hq]
-    o_out = (wgt[..., None] * o_all[:, rd]).sum(0)
+        rd = rows.to(q.device)
+        o_rows, l_rows = o_part[rd][None], lse_part[rd][None]
+    lse = torch.logsumexp(l_rows, dim=0)       # [rows, Hq]; a partial without keys carries -inf
+    wgt = torch.exp(l_rows - lse[None])        # [ranks, rows, Hq]
+    o_out = (wgt[..., None] * o_rows).sum(0)
     return o_base, lse_base, rows, o_out.to(q.dtype), lse

@@ -1,7 +1,7 @@
 """Sequence-parallel prefill (token axis sharded over ranks) against the oracle
 on the whole sequence.
 
-CPU: 2 and 3 gloo ranks, each rank's single-device attention done by the
+CPU: 1, 2 and 3 gloo ranks, each rank's single-device attention done by the
 oracle (test infrastructure), so what is checked is the decomposition: the
 halo exchange (including halos that span several ranks), the discarded halo
 rows, and the exact LSE merge of the output rows' partials. GPU: one rank
@@ -87,7 +87,7 @@ def _worker(rank, world, port, case, out_q):
         dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("world", [2, 3])
+@pytest.mark.parametrize("world", [1, 2, 3])
 @pytest.mark.parametrize("case", CASES, ids=lambda c: f"B{c[0]}T{c[1]}w{c[5]}{'qo' if c[7] else ''}")
 def test_sequence_parallel_matches_whole_sequence(world, case, oracle_mod):
     ctx = mp.get_context("spawn")
