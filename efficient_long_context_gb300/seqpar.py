@@ -23,9 +23,11 @@ stays in the library's kernels:
 it receives torch tensors of one rank and returns (o_base, lse_base, o_out,
 lse_out). The exchange uses torch.distributed (NCCL between GPUs, gloo for
 CPU tensors). A rank receives only the partials of the rows it owns, from the
-ranks before it, so the output-row exchange moves each partial once however
-many rows there are (one per sequence when prefilling, an answer span when
-fine-tuning, every position when pre-training).
+ranks before it, and (without q_out) the raw queries of later ranks' rows,
+from their owners, so the output-row exchange moves each partial and each
+query only to where it is used, however many rows there are (one per
+sequence when prefilling, an answer span when fine-tuning, every position
+when pre-training).
 """
 from __future__ import annotations
 
@@ -81,16 +83,46 @@ def _exchange_halo(k, v, T, window, world, rank, group):
     return k_halo, v_halo
 
 
+def _owners(pos, T, world):
+    """Rank that owns each position (-1 for positions outside [0, T))."""
+    owner = torch.full_like(pos, -1)
+    for s in range(world):
+        s0, s1 = chunk_bounds(T, world, s)
+        owner[(pos >= s0) & (pos < s1)] = s
+    return owner
+
+
+def _queries_from_owners(qo, pos, rows, T, world, rank, group):
+    """Fill qo's rows owned by later ranks with their raw queries: the owner of
+    a row sends it to every earlier rank (each of those holds keys the row
+    attends); this rank's own rows are already in qo."""
+    owner = _owners(pos, T, world)
+    ops = []
+    if len(rows):
+        mine = qo[rows.to(qo.device)].contiguous()
+        for r in range(rank):
+            ops.append(dist.P2POp(dist.isend, mine, r, group))
+    recv = []
+    for s in range(rank + 1, world):
+        sel = torch.nonzero(owner == s).flatten().to(qo.device)
+        if len(sel):
+            buf = qo.new_empty((len(sel),) + tuple(qo.shape[1:]))
+            ops.append(dist.P2POp(dist.irecv, buf, s, group))
+            recv.append((sel, buf))
+    if ops:
+        for req in dist.batch_isend_irecv(ops):
+            req.wait()
+    for sel, buf in recv:
+        qo[sel] = buf
+
+
 def _partials_to_owners(o_part, lse_part, pos, rows, T, world, rank, group):
     """Send this rank's partials of rows owned by later ranks to their owners
     and receive, from every earlier rank, its partials of the rows this rank
     owns (a rank holds a partial of every row at or after its chunk start).
     Returns the partials of this rank's rows, [rank + 1, len(rows), ...]:
     its own first, then those of ranks 0 .. rank-1."""
-    owner = torch.full_like(pos, -1)
-    for s in range(world):
-        s0, s1 = chunk_bounds(T, world, s)
-        owner[(pos >= s0) & (pos < s1)] = s
+    owner = _owners(pos, T, world)
     ops = []
     for s in range(rank + 1, world):
         sel = torch.nonzero(owner == s).flatten().to(o_part.device)
@@ -157,13 +189,13 @@ def sp_prefill(q, k, v, alpha_base, beta_base, alpha_out, beta_out, out_indptr, 
     if n_out == 0:
         return o_base, lse_base, rows, q.new_zeros((0, Hq, d)), lse_base.new_zeros((0, Hq))
     if q_out is None:
-        # raw queries of all output rows: each owner contributes its rows
-        qo = q.new_zeros((n_out, Hq, d), dtype=torch.float32)
+        # raw queries of the output rows this rank attends: its own, and those
+        # of later ranks' rows, sent by their owners
+        qo = q.new_zeros((n_out, Hq, d))
         if len(rows):
-            qo[rows] = q[seq[rows], pos[rows] - start].float()
+            qo[rows.to(q.device)] = q[seq[rows], pos[rows] - start]
         if world > 1:
-            dist.all_reduce(qo, group=group)
-        qo = qo.to(q.dtype)
+            _queries_from_owners(qo, pos, rows, T, world, rank, group)
     else:
         qo = q_out
     mine = torch.nonzero(pos >= start).flatten()  # rows that see at least one key of this chunk
