@@ -24,6 +24,7 @@ CASES = [
     (1, 37, 4, 2, 8, 20, [[36, 5, 13, 24, 25]], True),   # halo wider than one chunk
     (2, 29, 2, 1, 8, 40, [[28], [7, 28]], False),        # window >= T: full causal
     (1, 30, 4, 4, 8, 3, [[]], False),                    # no output rows
+    (2, 25, 4, 2, 8, 6, [list(range(25))] * 2, False),   # pre-training: every position an output row
 ]
 
 
