@@ -109,6 +109,40 @@ def test_sequence_parallel_matches_whole_sequence(world, case, oracle_mod):
             assert e <= 2e-5, f"rank {rank} {name}: {e}"
 
 
+def _random_case(seed):
+    """A seeded shape with halos that span several of four ranks and output
+    rows (repeats included) spread over every owner."""
+    import random
+
+    r = random.Random(seed)
+    B, T = r.choice([1, 2]), r.randint(9, 41)
+    Hkv = r.choice([1, 2])
+    Hq = Hkv * r.choice([1, 2, 3])
+    w = r.choice([1, 2, r.randint(3, T), T + 3])
+    lists = [sorted(r.choice(range(T)) for _ in range(r.randint(0, 6))) for _ in range(B)]
+    return (B, T, Hq, Hkv, 8, w, lists, r.random() < 0.5)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_sequence_parallel_random_shapes_four_ranks(seed, oracle_mod):
+    case = _random_case(seed)
+    ctx = mp.get_context("spawn")
+    out_q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 4, port, case, out_q)) for r in range(4)]
+    for p in procs:
+        p.start()
+    got = [out_q.get(timeout=180) for _ in procs]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    owned = sorted(r for _, _, rows in got for r in rows)
+    assert owned == list(range(sum(len(x) for x in case[6]))), case
+    for rank, errs, _ in got:
+        for name, e in errs.items():
+            assert e <= 2e-5, f"{case} rank {rank} {name}: {e}"
+
+
 @pytest.mark.gpu
 def test_single_rank_on_gpu_matches_oracle(oracle_mod):
     sys.path.insert(0, ROOT)
