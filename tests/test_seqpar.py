@@ -88,19 +88,33 @@ def _worker(rank, world, port, case, out_q):
         dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("world", [1, 2, 3])
-@pytest.mark.parametrize("case", CASES, ids=lambda c: f"B{c[0]}T{c[1]}w{c[5]}{'qo' if c[7] else ''}")
-def test_sequence_parallel_matches_whole_sequence(world, case, oracle_mod):
+def _run_ranks(world, case):
+    """Run `world` gloo ranks on one case; returns their (rank, errors, rows).
+    Ranks still running when the results are in (or after a failure) are
+    ended here, so a broken exchange cannot leave processes behind."""
     ctx = mp.get_context("spawn")
     out_q = ctx.Queue()
     port = _free_port()
     procs = [ctx.Process(target=_worker, args=(r, world, port, case, out_q)) for r in range(world)]
     for p in procs:
         p.start()
-    got = [out_q.get(timeout=180) for _ in procs]
-    for p in procs:
-        p.join(timeout=60)
-        assert p.exitcode == 0
+    try:
+        got = [out_q.get(timeout=180) for _ in procs]
+        for p in procs:
+            p.join(timeout=60)
+            assert p.exitcode == 0
+        return got
+    finally:
+        for p in procs:
+            if p.is_alive():
+                p.terminate()
+                p.join(timeout=10)
+
+
+@pytest.mark.parametrize("world", [1, 2, 3])
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"B{c[0]}T{c[1]}w{c[5]}{'qo' if c[7] else ''}")
+def test_sequence_parallel_matches_whole_sequence(world, case, oracle_mod):
+    got = _run_ranks(world, case)
     owned = sorted(r for _, _, rows in got for r in rows)
     n_out = sum(len(x) for x in case[6])
     assert owned == list(range(n_out))  # every output row has exactly one owner
@@ -126,16 +140,7 @@ def _random_case(seed):
 @pytest.mark.parametrize("seed", range(6))
 def test_sequence_parallel_random_shapes_four_ranks(seed, oracle_mod):
     case = _random_case(seed)
-    ctx = mp.get_context("spawn")
-    out_q = ctx.Queue()
-    port = _free_port()
-    procs = [ctx.Process(target=_worker, args=(r, 4, port, case, out_q)) for r in range(4)]
-    for p in procs:
-        p.start()
-    got = [out_q.get(timeout=180) for _ in procs]
-    for p in procs:
-        p.join(timeout=60)
-        assert p.exitcode == 0
+    got = _run_ranks(4, case)
     owned = sorted(r for _, _, rows in got for r in rows)
     assert owned == list(range(sum(len(x) for x in case[6]))), case
     for rank, errs, _ in got:
