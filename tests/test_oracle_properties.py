@@ -5,7 +5,9 @@
   length, group size, head size, window (from 1 to beyond T), output-row sets
   (empty or any positions) and the optional raw queries of the output stream;
 * a prefill followed by decoding steps against one longer prefill, over page
-  sizes and windows.
+  sizes and windows;
+* continuous-batching steps (every sequence appends its own chunk) against a
+  prefill of each sequence over all its tokens.
 """
 import math
 
@@ -90,3 +92,67 @@ def test_prefill_then_decode_equals_longer_prefill(orc, case):
         for a, b_ in ((ob, full[0][:, t]), (lb, full[1][:, :, t]), (oo, full[2][rows]), (lo, full[3][rows])):
             assert float(np.max(np.abs(np.asarray(a, np.float64) - np.asarray(b_, np.float64)))) <= 1e-12
         lens = lens + 1
+
+
+@st.composite
+def batching_case(draw):
+    B = draw(st.integers(1, 3))
+    t0 = [draw(st.integers(1, 8)) for _ in range(B)]
+    steps = draw(st.integers(1, 4))
+    chunks = [[draw(st.integers(0, 4)) for _ in range(B)] for _ in range(steps)]
+    Hkv = draw(st.integers(1, 2))
+    g = draw(st.integers(1, 2))
+    window = draw(st.integers(1, 12))
+    page = draw(st.sampled_from([1, 2, 4]))
+    seed = draw(st.integers(0, 2**16))
+    return t0, chunks, Hkv * g, Hkv, 8, window, page, seed
+
+
+@hypothesis.settings(max_examples=40, deadline=None)
+@hypothesis.given(batching_case())
+def test_continuous_batching_equals_per_sequence_prefill(orc, case):
+    """Continuous batching: steps in which every sequence appends its own chunk
+    (0 to 4 tokens) give each new token the base row, and each chunk's last
+    token the output row, of one prefill of that sequence over all its tokens."""
+    t0, chunks, Hq, Hkv, d, window, page, seed = case
+    B = len(t0)
+    total = [t0[b] + sum(c[b] for c in chunks) for b in range(B)]
+    seqs = [pins.rng_inputs(seed + b, 1, total[b], Hq, Hkv, d) for b in range(B)]
+    ab, bb, ao, bo = seqs[0][3:]
+    ends = []
+    for b in range(B):
+        at, e = t0[b], []
+        for c in chunks:
+            at += c[b]
+            if c[b]:
+                e.append(at - 1)
+        ends.append(e)
+    full = []
+    for b in range(B):
+        q, k, v = seqs[b][:3]
+        ip, ps = pins.csr([ends[b]])
+        full.append(orc.prefill(q, k, v, ab, bb, ao, bo, ip, ps, window, 0.3))
+    rng = np.random.default_rng(seed)
+    lens = np.array(t0, np.int32)
+    kc, vc, bt = pins._paged_from_seq([seqs[b][1][0, :t0[b]] for b in range(B)],
+                                      [seqs[b][2][0, :t0[b]] for b in range(B)], lens, page,
+                                      max(total[b] - t0[b] for b in range(B)), rng)
+    for c in chunks:
+        new_indptr = np.concatenate([[0], np.cumsum(c)]).astype(np.int32)
+        pick = lambda x, b: x[0, lens[b]:lens[b] + c[b]]  # noqa: E731
+        qn = np.concatenate([pick(seqs[b][0], b) for b in range(B)], 0).reshape(-1, Hq, d)
+        kn = np.concatenate([pick(seqs[b][1], b) for b in range(B)], 0).reshape(-1, Hkv, d)
+        vn = np.concatenate([pick(seqs[b][2], b) for b in range(B)], 0).reshape(-1, Hkv, d)
+        oi, op = pins.csr([[int(lens[b]) + c[b] - 1] if c[b] else [] for b in range(B)])
+        ob, lb, oo, lo = orc.extend(qn, kn, vn, kc, vc, bt, lens, new_indptr, oi, op, ab, bb, ao, bo, window, 0.3)
+        for b in range(B):
+            r0, r1 = int(new_indptr[b]), int(new_indptr[b + 1])
+            L = int(lens[b])
+            assert np.max(np.abs(ob[r0:r1] - full[b][0][0, L:L + c[b]]), initial=0.0) <= 1e-12
+            assert np.max(np.abs(lb[r0:r1].T - full[b][1][0, :, L:L + c[b]]), initial=0.0) <= 1e-12
+            if c[b]:
+                r = ends[b].index(L + c[b] - 1)
+                o_row = int(oi[b])
+                assert np.max(np.abs(oo[o_row] - full[b][2][r])) <= 1e-12
+                assert np.max(np.abs(lo[o_row] - full[b][3][r])) <= 1e-12
+        lens = lens + np.asarray(c, np.int32)
