@@ -7,7 +7,9 @@
 * a prefill followed by decoding steps against one longer prefill, over page
   sizes and windows;
 * continuous-batching steps (every sequence appends its own chunk) against a
-  prefill of each sequence over all its tokens.
+  prefill of each sequence over all its tokens;
+* every gradient of the backward against torch.autograd through the dense
+  masked forward, output rows at repeated positions included.
 """
 import math
 
@@ -156,3 +158,50 @@ def test_continuous_batching_equals_per_sequence_prefill(orc, case):
                 assert np.max(np.abs(oo[o_row] - full[b][2][r])) <= 1e-12
                 assert np.max(np.abs(lo[o_row] - full[b][3][r])) <= 1e-12
         lens = lens + np.asarray(c, np.int32)
+
+
+@st.composite
+def backward_case(draw):
+    B = draw(st.integers(1, 2))
+    T = draw(st.integers(1, 14))
+    Hkv = draw(st.integers(1, 2))
+    g = draw(st.integers(1, 3))
+    d = draw(st.sampled_from([4, 8]))
+    window = draw(st.integers(1, T + 2))
+    # output rows may repeat a position (their query and gradient add up)
+    lists = [sorted(draw(st.lists(st.integers(0, T - 1), max_size=T + 2))) for _ in range(B)]
+    with_q_out = draw(st.booleans())
+    seed = draw(st.integers(0, 2**16))
+    return B, T, Hkv * g, Hkv, d, window, lists, with_q_out, seed
+
+
+@hypothesis.settings(max_examples=30, deadline=None)
+@hypothesis.given(backward_case())
+def test_backward_matches_autograd(orc, case):
+    """Every gradient of the oracle's backward equals torch.autograd (float64)
+    through the dense masked forward of tests/pins.py."""
+    B, T, Hq, Hkv, d, window, lists, with_q_out, seed = case
+    q, k, v, ab, bb, ao, bo = pins.rng_inputs(seed, B, T, Hq, Hkv, d)
+    indptr, pos = pins.csr(lists)
+    n_out = int(indptr[-1])
+    r = np.random.default_rng(seed)
+    q_out = r.standard_normal((n_out, Hq, d)).astype(np.float32) if with_q_out else None
+    do_b = r.standard_normal((B, T, Hq, d)).astype(np.float32)
+    do_o = r.standard_normal((n_out, Hq, d)).astype(np.float32)
+    scale = 0.9 / math.sqrt(d)
+    got = orc.prefill_backward(q, k, v, ab, bb, ao, bo, indptr, pos, window, scale, do_b, do_o, q_out=q_out)
+    leaves = {n: torch.tensor(x, dtype=torch.float64, requires_grad=True)
+              for n, x in (("q", q), ("k", k), ("v", v), ("ab", ab), ("bb", bb), ("ao", ao), ("bo", bo))}
+    qo_t = torch.tensor(q_out, dtype=torch.float64, requires_grad=True) if q_out is not None else None
+    ob, oo = pins.torch_forward(leaves["q"], leaves["k"], leaves["v"], leaves["ab"], leaves["bb"], leaves["ao"],
+                                leaves["bo"], indptr, pos, window, scale, qo_t)
+    loss = (ob * torch.from_numpy(do_b).double()).sum() + (oo * torch.from_numpy(do_o).double()).sum()
+    loss.backward()
+    for name, leaf in (("dq", "q"), ("dk", "k"), ("dv", "v"), ("d_alpha_base", "ab"), ("d_beta_base", "bb"),
+                       ("d_alpha_out", "ao"), ("d_beta_out", "bo")):
+        grad = leaves[leaf].grad
+        ref = grad.numpy() if grad is not None else np.zeros_like(np.asarray(got[name]))
+        assert float(np.max(np.abs(np.asarray(got[name], np.float64) - ref), initial=0.0)) <= 1e-9, name
+    if q_out is not None:
+        ref = qo_t.grad.numpy() if qo_t.grad is not None else np.zeros((0, Hq, d))
+        assert float(np.max(np.abs(np.asarray(got["dq_out"], np.float64) - ref), initial=0.0)) <= 1e-9
