@@ -9,7 +9,8 @@
 * continuous-batching steps (every sequence appends its own chunk) against a
   prefill of each sequence over all its tokens;
 * every gradient of the backward against torch.autograd through the dense
-  masked forward, output rows at repeated positions included.
+  masked forward, output rows at repeated positions included;
+* the projection against a dense float64 product with the stream affines.
 """
 import math
 
@@ -205,3 +206,37 @@ def test_backward_matches_autograd(orc, case):
     if q_out is not None:
         ref = qo_t.grad.numpy() if qo_t.grad is not None else np.zeros((0, Hq, d))
         assert float(np.max(np.abs(np.asarray(got["dq_out"], np.float64) - ref), initial=0.0)) <= 1e-9
+
+
+@st.composite
+def projection_case(draw):
+    n_base = draw(st.integers(0, 6))
+    n_out = draw(st.integers(0, 6))
+    d_model = draw(st.integers(1, 24))
+    Hkv = draw(st.integers(1, 2))
+    g = draw(st.integers(1, 3))
+    d = draw(st.sampled_from([2, 4, 8]))
+    seed = draw(st.integers(0, 2**16))
+    return n_base, n_out, d_model, Hkv * g, Hkv, d, seed
+
+
+@hypothesis.settings(max_examples=40, deadline=None)
+@hypothesis.given(projection_case())
+def test_projection_matches_a_dense_product(orc, case):
+    """The projection (Orthros paper, Alg. 1 lines 4-5) equals x W^T in float64
+    with each stream's affine on the query columns and K/V from base rows only."""
+    n_base, n_out, d_model, Hq, Hkv, d, seed = case
+    r = np.random.default_rng(seed)
+    N = (Hq + 2 * Hkv) * d
+    x = r.standard_normal((n_base + n_out, d_model)).astype(np.float32)
+    w_t = r.standard_normal((N, d_model)).astype(np.float32)
+    ab, bb, ao, bo = (r.standard_normal((Hq, d)).astype(np.float32) for _ in range(4))
+    qb, qo, k, v = orc.qkv_project(x, n_base, w_t, Hq, Hkv, d, ab, bb, ao, bo)
+    y = x.astype(np.float64) @ w_t.astype(np.float64).T
+    Nq, Nkv = Hq * d, Hkv * d
+    want_qb = y[:n_base, :Nq].reshape(n_base, Hq, d) * ab + bb
+    want_qo = y[n_base:, :Nq].reshape(n_out, Hq, d) * ao + bo
+    for got, want in ((qb, want_qb), (qo, want_qo), (k, y[:n_base, Nq:Nq + Nkv].reshape(n_base, Hkv, d)),
+                      (v, y[:n_base, Nq + Nkv:].reshape(n_base, Hkv, d))):
+        assert np.asarray(got).shape == want.shape
+        assert float(np.max(np.abs(np.asarray(got, np.float64) - want), initial=0.0)) <= 1e-9
