@@ -19,9 +19,12 @@ from ._binding import (  # noqa: F401
     orthros_extend,
     orthros_extend_workspace_size,
     orthros_last_error,
+    orthros_merge_partials,
     orthros_prefill,
     orthros_prefill_backward,
     orthros_prefill_backward_workspace_size,
+    orthros_prefill_shard,
+    orthros_prefill_shard_workspace_size,
     orthros_prefill_workspace_size,
     orthros_profile_begin,
     orthros_qkv_project,

@@ -21,7 +21,8 @@ STATUS_NAMES = {0: "ORTHROS_OK", 1: "ORTHROS_EINVAL", 2: "ORTHROS_EUNSUPPORTED",
                 4: "ORTHROS_EWORKSPACE", 5: "ORTHROS_EDEVICE", 6: "ORTHROS_ETIMEOUT"}
 
 # the public symbols of include/orthros_attn.h
-EXPORTS = ("orthros_prefill_workspace_size", "orthros_prefill", "orthros_prefill_backward_workspace_size",
+EXPORTS = ("orthros_prefill_workspace_size", "orthros_prefill", "orthros_prefill_shard_workspace_size",
+           "orthros_prefill_shard", "orthros_merge_partials", "orthros_prefill_backward_workspace_size",
            "orthros_prefill_backward", "orthros_extend_workspace_size", "orthros_extend", "orthros_qkv_project",
            "orthros_decode_workspace_size",
            "orthros_decode", "orthros_decode_static", "orthros_check", "orthros_profile_begin", "orthros_profile_end",
@@ -61,6 +62,14 @@ def load_library(path: str | None = None):
         lib.orthros_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32p, vp, i32, vp,
                                         i32, i32, i32, i32, i32, i32, ctypes.c_float, i32,
                                         vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp, sz, vp]
+        lib.orthros_prefill_shard_workspace_size.restype = sz
+        lib.orthros_prefill_shard_workspace_size.argtypes = [i32] * 9
+        lib.orthros_prefill_shard.restype = i32
+        lib.orthros_prefill_shard.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32p, vp, i32, vp,
+                                              i32, i32, i32, i32, i32, i32, i32, ctypes.c_float, i32,
+                                              vp, vp, vp, vp, vp, sz, vp]
+        lib.orthros_merge_partials.restype = i32
+        lib.orthros_merge_partials.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
         lib.orthros_prefill_backward_workspace_size.restype = sz
         lib.orthros_prefill_backward_workspace_size.argtypes = [i32] * 8
         lib.orthros_prefill_backward.restype = i32
@@ -199,6 +208,66 @@ def orthros_prefill(q, k, v, alpha_base, beta_base, alpha_out, beta_out, out_ind
         _ptr(workspace), workspace.numel(), _stream(stream))
     _raise_if(rc, lib)
     return o_base, lse_base, o_out, lse_out
+
+
+def orthros_prefill_shard_workspace_size(B, Tq, Tkv, Hq, Hkv, d, n_rows, window, dtype=torch.bfloat16) -> int:
+    return int(load_library().orthros_prefill_shard_workspace_size(B, Tq, Tkv, Hq, Hkv, d, n_rows, window,
+                                                                   _DTYPES[dtype]))
+
+
+def orthros_prefill_shard(q, k, v, alpha_base, beta_base, alpha_out, beta_out, row_indptr, row_positions,
+                          window, scale=None, *, q_rows=None, out=None, workspace=None, stream=None):
+    """orthros_prefill_shard of include/orthros_attn.h on torch CUDA tensors.
+
+    q [B, Tq, Hq, d] (the chunk's queries), k, v [B, Tkv, Hkv, d] (halo then
+    chunk); row_indptr is a HOST int32 array-like [B+1], row_positions [n_rows]
+    int32 in the K/V buffer's coordinates, q_rows [n_rows, Hq, d]. Returns
+    (o_base [B,Tq,Hq,d], lse_base [B,Hq,Tq], o_part [n_rows,Hq,d] float,
+    lse_part [n_rows,Hq] float), allocated here unless `out` gives all four.
+    """
+    lib = load_library()
+    B, Tq, Hq, d = q.shape
+    Tkv, Hkv = k.shape[1], k.shape[2]
+    indptr = np.ascontiguousarray(np.asarray(row_indptr.cpu() if isinstance(row_indptr, torch.Tensor)
+                                             else row_indptr, dtype=np.int32))
+    n_rows = int(indptr[-1]) if indptr.size else 0
+    if scale is None:
+        scale = d ** -0.5
+    for name, t in (("q", q), ("k", k), ("v", v), ("q_rows", q_rows), ("row_positions", row_positions)):
+        _contig(name, t)
+    if out is None:
+        out = (torch.empty_like(q), torch.empty((B, Hq, Tq), dtype=torch.float32, device=q.device),
+               torch.empty((n_rows, Hq, d), dtype=torch.float32, device=q.device),
+               torch.empty((n_rows, Hq), dtype=torch.float32, device=q.device))
+    o_base, lse_base, o_part, lse_part = out
+    if workspace is None:
+        ws = orthros_prefill_shard_workspace_size(B, Tq, Tkv, Hq, Hkv, d, n_rows, window, q.dtype)
+        workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=q.device)
+    rc = lib.orthros_prefill_shard(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(alpha_base), _ptr(beta_base), _ptr(alpha_out), _ptr(beta_out),
+        indptr.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), _ptr(row_positions), n_rows, _ptr(q_rows),
+        B, Tq, Tkv, Hq, Hkv, d, int(window), float(scale), _dtype(q),
+        _ptr(o_base), _ptr(lse_base), _ptr(o_part), _ptr(lse_part), _ptr(workspace), workspace.numel(),
+        _stream(stream))
+    _raise_if(rc, lib)
+    return o_base, lse_base, o_part, lse_part
+
+
+def orthros_merge_partials(o_parts, lse_parts, dtype=torch.bfloat16, *, out=None, stream=None):
+    """orthros_merge_partials of include/orthros_attn.h: o_parts [P, n, Hq, d]
+    float, lse_parts [P, n, Hq] float -> (o [n, Hq, d] of `dtype`, lse [n, Hq])."""
+    lib = load_library()
+    P, n, Hq, d = o_parts.shape
+    for name, t in (("o_parts", o_parts), ("lse_parts", lse_parts)):
+        _contig(name, t)
+    if out is None:
+        out = (torch.empty((n, Hq, d), dtype=dtype, device=o_parts.device),
+               torch.empty((n, Hq), dtype=torch.float32, device=o_parts.device))
+    o, lse = out
+    rc = lib.orthros_merge_partials(_ptr(o_parts), _ptr(lse_parts), P, n, Hq, d, _DTYPES[o.dtype], _ptr(o), _ptr(lse),
+                                    _stream(stream))
+    _raise_if(rc, lib)
+    return o, lse
 
 
 def orthros_prefill_backward_workspace_size(B, T, Hq, Hkv, d, n_out, window, dtype=torch.bfloat16) -> int:

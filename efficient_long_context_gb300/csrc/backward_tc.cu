@@ -477,12 +477,8 @@ cudaError_t launch_backward_tc(const BwdTcParams &p, const void *k, const void *
         !encode_kv_map_3d(&tqo, p.n_out > 0 ? qa_out : qa_base, n_out_rows, p.Hq, kD, kRows) ||
         !encode_kv_map_3d(&tdo, p.n_out > 0 ? do_out : do_base, n_out_rows, p.Hq, kD, kRows))
         return cudaErrorInvalidValue;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(backward_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static SmemLimit limit;
+    if (cudaError_t e = limit.ensure((const void *)backward_tc_kernel, kSmem); e != cudaSuccess) return e;
     const long long units = (long long)p.nkb * p.B * p.Hkv;
     if (units == 0) return cudaSuccess;
     backward_tc_kernel<<<(unsigned)units, kThreads, kSmem, stream>>>(tk, tv, tqb, tdb, tqo, tdo, p);

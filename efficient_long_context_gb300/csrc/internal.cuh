@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "orthros_attn.h"
 
 namespace orthros {
@@ -21,6 +23,27 @@ namespace orthros {
 constexpr size_t kStatusBytes = 256;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// A kernel's dynamic shared-memory limit is a per-device attribute: raise it
+// once on every device that launches the kernel (the first 64 devices are
+// remembered; later ones set it on every launch). Concurrent first launches
+// may both set it, which is harmless.
+class SmemLimit {
+  public:
+    cudaError_t ensure(const void *func, int bytes) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
+        if (bit && (done_.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+        e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e == cudaSuccess && bit) done_.fetch_or(bit, std::memory_order_acq_rel);
+        return e;
+    }
+
+  private:
+    std::atomic<uint64_t> done_{0};
+};
 
 __device__ __forceinline__ void set_status(uint32_t *status, uint32_t bit) {
     if (status) atomicOr(status, bit);
@@ -86,13 +109,18 @@ struct TcParams {
     const int32_t *out_indptr;         // device [B+1]
     const int32_t *out_positions;      // [n_out]
     const int32_t *cross_unit_indptr;  // device [B+1]: output-row units per sequence (prefix sums)
-    int B, T, Hq, Hkv, window;
+    int B, T, Hq, Hkv, window;  // T: key positions per sequence
+    int Tq;     // query rows per sequence; query i sits at key position q_off + i
+    int q_off;  // T - Tq (0 for a whole-sequence prefill)
+    int shard;  // output rows are partials over keys key_lo .. min(t, T - 1)
+    int key_lo; // first key of every output row (0 unless shard)
     float scale, scale_log2;
     int n_cross_units, n_base_units, base_nblk;
     int n_out;  // rows of q_out (its tensor map)
     __nv_bfloat16 *o_base;
     float *lse_base;
     __nv_bfloat16 *o_out;
+    float *o_out_f32;  // when set, output rows are written here as float instead of o_out
     float *lse_out;
     uint32_t *status;
 };
@@ -118,6 +146,8 @@ struct SplitParams {
     int group_offset;                         // first group of this launch (the partial buffer is shared)
     int max_pages, page_size, num_pages;
     int B, T, Hq, Hkv, window;
+    int Tq, q_off;       // prefill: query rows per sequence; query i sits at key position q_off + i
+    int shard, key_lo;   // prefill: output rows are partials over keys key_lo .. min(t, T - 1)
     float scale, scale_log2;
     int n_groups, chunk, max_chunks;
     long long kv_tokens;  // token rows behind k / v: prefill B*T, decode num_pages*page_size
@@ -125,6 +155,7 @@ struct SplitParams {
     __nv_bfloat16 *o_base;
     float *lse_base;
     __nv_bfloat16 *o_out;
+    float *o_out_f32;  // prefill: when set, output rows are written here as float instead of o_out
     float *lse_out;
     uint32_t *status;
 };
@@ -145,6 +176,15 @@ __device__ __forceinline__ int extend_position(const SplitParams &p, int group, 
     const int t = p.out_positions[idx];
     if (t < 0 || t >= len || (!p.q_out && t < L)) return -1;
     return t;
+}
+// Prefill mode: the last key of an output row at position t (a shard's rows
+// past its keys read them all), or -1 when the position is impossible (before
+// 0; past the keys outside a shard; without q_out, outside the query rows).
+__device__ __forceinline__ int prefill_row_end(const SplitParams &p, int t) {
+    if (t < 0 || (!p.shard && t >= p.T)) return -1;
+    const int te = min(t, p.T - 1);
+    if (!p.q_out && (te < p.q_off || te - p.q_off >= p.Tq)) return -1;
+    return te;
 }
 size_t split_partial_bytes(int n_groups, int max_chunks, int d);
 // Runs the split kernel (the TMA-fed persistent one when eligible) and the combine.
@@ -222,6 +262,10 @@ struct ProjParams {
     uint32_t *status;
 };
 cudaError_t launch_project_tc(const ProjParams &p, cudaStream_t stream);
+
+// merge.cu: exact merge of normalised partials over disjoint key sets.
+cudaError_t launch_merge_partials(const float *o_parts, const float *lse_parts, int n_parts, int n_rows, int Hq, int d,
+                                  bool f32_out, void *o_out, float *lse_out, cudaStream_t stream);
 
 // cache.cu
 // Writes new token i of sequence b (rows new_indptr[b] ..) at position

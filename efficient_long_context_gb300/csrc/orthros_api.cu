@@ -181,63 +181,27 @@ orthros_status check_shapes(int B, int Hq, int Hkv, int d, int window, float sca
     return ORTHROS_OK;
 }
 
-}  // namespace
-
-orthros_status report_error(orthros_status s, const char *fmt, ...) {
-    char buf[512];
-    va_list ap;
-    va_start(ap, fmt);
-    vsnprintf(buf, sizeof buf, fmt, ap);
-    va_end(ap);
-    g_last_error = buf;
-    return s;
-}
-
-}  // namespace orthros
-
-using namespace orthros;
-
-extern "C" {
-
-const char *orthros_status_string(orthros_status s) {
-    switch (s) {
-        case ORTHROS_OK: return "ok";
-        case ORTHROS_EINVAL: return "invalid argument";
-        case ORTHROS_EUNSUPPORTED: return "unsupported configuration";
-        case ORTHROS_ECUDA: return "CUDA error";
-        case ORTHROS_EWORKSPACE: return "workspace missing or too small";
-        case ORTHROS_EDEVICE: return "bad device-side data flagged by a kernel";
-        case ORTHROS_ETIMEOUT: return "bounded wait inside a kernel ran out";
-    }
-    return "unknown status";
-}
-
-const char *orthros_last_error(void) { return g_last_error.c_str(); }
-
-size_t orthros_prefill_workspace_size(int B, int T, int Hq, int Hkv, int d, int n_out, int window,
-                                      orthros_dtype dtype) {
-    if (T < 0 || n_out < 0) return 0;
-    if (check_shapes(B, Hq, Hkv, d, window, 1.0f, dtype) != ORTHROS_OK) return 0;
-    return prefill_layout(B, T, Hkv, d, n_out, dtype).total;
-}
-
-orthros_status orthros_prefill(const void *q, const void *k, const void *v, const float *alpha_base,
-                               const float *beta_base, const float *alpha_out, const float *beta_out,
-                               const int32_t *out_indptr, const int32_t *out_positions, int n_out,
-                               const void *q_out, int B, int T, int Hq, int Hkv, int d, int window,
-                               float scale, orthros_dtype dtype, void *o_base, float *lse_base,
-                               void *o_out, float *lse_out, void *k_cache, void *v_cache,
-                               const int32_t *block_table, int max_pages, int page_size, int num_pages,
-                               void *workspace, size_t workspace_bytes, orthros_stream_t stream_) {
-    g_last_error.clear();
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+// orthros_prefill (Tq == T, whole sequences) and orthros_prefill_shard (Tq <=
+// T: the queries are the last Tq key positions; with `shard` the output rows
+// are float partials over the last Tq keys) share this body. T counts keys.
+orthros_status prefill_core(const void *q, const void *k, const void *v, const float *alpha_base,
+                            const float *beta_base, const float *alpha_out, const float *beta_out,
+                            const int32_t *out_indptr, const int32_t *out_positions, int n_out,
+                            const void *q_out, int B, int T, int Tq, bool shard, int Hq, int Hkv, int d,
+                            int window, float scale, orthros_dtype dtype, void *o_base, float *lse_base,
+                            void *o_out, float *o_out_f32, float *lse_out, void *k_cache, void *v_cache,
+                            const int32_t *block_table, int max_pages, int page_size, int num_pages,
+                            void *workspace, size_t workspace_bytes, cudaStream_t stream) {
     orthros_status st = check_shapes(B, Hq, Hkv, d, window, scale, dtype);
     if (st != ORTHROS_OK) return st;
     if (T < 0) return fail(ORTHROS_EINVAL, "T = %d must be >= 0", T);
+    if (Tq < 0 || Tq > T) return fail(ORTHROS_EINVAL, "Tq = %d must lie in [0, T = %d]", Tq, T);
     if (n_out < 0) return fail(ORTHROS_EINVAL, "n_out = %d must be >= 0", n_out);
     const long long rows = (long long)B * T;
     if (rows > (1LL << 31)) return fail(ORTHROS_EUNSUPPORTED, "B*T = %lld tokens exceeds 2^31", rows);
-    if (rows > 0) {
+    if (shard && dtype != ORTHROS_BF16) return fail(ORTHROS_EUNSUPPORTED, "shards take bf16 only");
+    if (shard && n_out > 0 && !q_out) return fail(ORTHROS_EINVAL, "a shard's output rows need q_out");
+    if ((long long)B * Tq > 0) {
         if (!q || !k || !v) return fail(ORTHROS_EINVAL, "q, k and v must not be NULL");
         if (!alpha_base || !beta_base) return fail(ORTHROS_EINVAL, "alpha_base and beta_base must not be NULL");
         if (!o_base || !lse_base) return fail(ORTHROS_EINVAL, "o_base and lse_base must not be NULL");
@@ -261,8 +225,10 @@ orthros_status orthros_prefill(const void *q, const void *k, const void *v, cons
         if (T == 0) return fail(ORTHROS_EINVAL, "output rows with T = 0");
         if (!out_positions) return fail(ORTHROS_EINVAL, "out_positions must not be NULL when n_out > 0");
         if (!alpha_out || !beta_out) return fail(ORTHROS_EINVAL, "alpha_out and beta_out must not be NULL when n_out > 0");
-        if (!o_out || !lse_out) return fail(ORTHROS_EINVAL, "o_out and lse_out must not be NULL when n_out > 0");
-        if (!aligned16(o_out) || (q_out && !aligned16(q_out)) || !aligned16(alpha_out) || !aligned16(beta_out))
+        if (!(shard ? (void *)o_out_f32 : o_out) || !lse_out)
+            return fail(ORTHROS_EINVAL, "o_out and lse_out must not be NULL when n_out > 0");
+        if (!aligned16(shard ? (void *)o_out_f32 : o_out) || (q_out && !aligned16(q_out)) || !aligned16(alpha_out) ||
+            !aligned16(beta_out))
             return fail(ORTHROS_EINVAL, "o_out, q_out, alpha_out and beta_out must be 16-byte aligned");
     }
     const bool fill = k_cache || v_cache || block_table;
@@ -398,6 +364,10 @@ orthros_status orthros_prefill(const void *q, const void *k, const void *v, cons
         sp.group_info = groups_dev;
         sp.B = B;
         sp.T = T;
+        sp.Tq = Tq;
+        sp.q_off = T - Tq;
+        sp.shard = shard;
+        sp.key_lo = shard ? T - Tq : 0;
         sp.Hq = Hq;
         sp.Hkv = Hkv;
         sp.window = window;
@@ -411,6 +381,7 @@ orthros_status orthros_prefill(const void *q, const void *k, const void *v, cons
         sp.kv_tokens = (long long)B * T;
         sp.partial = reinterpret_cast<float *>(ws + lay.part_off);
         sp.o_out = static_cast<__nv_bfloat16 *>(o_out);
+        sp.o_out_f32 = shard ? o_out_f32 : nullptr;
         sp.lse_out = lse_out;
         sp.status = status;
         ProfScope ps("splitkv_prefill", stream);
@@ -429,18 +400,23 @@ orthros_status orthros_prefill(const void *q, const void *k, const void *v, cons
     tp.cross_unit_indptr = cross_indptr_dev;
     tp.B = B;
     tp.T = T;
+    tp.Tq = Tq;
+    tp.q_off = T - Tq;
+    tp.shard = shard;
+    tp.key_lo = shard ? T - Tq : 0;
     tp.Hq = Hq;
     tp.Hkv = Hkv;
     tp.window = window;
     tp.scale = scale;
     tp.scale_log2 = scale * log2e;
-    tp.base_nblk = ceil_div(T, 128);
+    tp.base_nblk = ceil_div(Tq, 128);
     tp.n_cross_units = n_cross_units;
     tp.n_out = n_out;
     tp.n_base_units = B * Hkv * tc_units_per_kv(tp.base_nblk, g);
     tp.o_base = static_cast<__nv_bfloat16 *>(o_base);
     tp.lse_base = lse_base;
     tp.o_out = static_cast<__nv_bfloat16 *>(o_out);
+    tp.o_out_f32 = shard ? o_out_f32 : nullptr;
     tp.lse_out = lse_out;
     tp.status = status;
     {
@@ -448,6 +424,106 @@ orthros_status orthros_prefill(const void *q, const void *k, const void *v, cons
         e = launch_prefill_tc(tp, k16, v, d, stream);
     }
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core prefill launch");
+    return ORTHROS_OK;
+}
+
+}  // namespace
+
+orthros_status report_error(orthros_status s, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+}  // namespace orthros
+
+using namespace orthros;
+
+extern "C" {
+
+const char *orthros_status_string(orthros_status s) {
+    switch (s) {
+        case ORTHROS_OK: return "ok";
+        case ORTHROS_EINVAL: return "invalid argument";
+        case ORTHROS_EUNSUPPORTED: return "unsupported configuration";
+        case ORTHROS_ECUDA: return "CUDA error";
+        case ORTHROS_EWORKSPACE: return "workspace missing or too small";
+        case ORTHROS_EDEVICE: return "bad device-side data flagged by a kernel";
+        case ORTHROS_ETIMEOUT: return "bounded wait inside a kernel ran out";
+    }
+    return "unknown status";
+}
+
+const char *orthros_last_error(void) { return g_last_error.c_str(); }
+
+size_t orthros_prefill_workspace_size(int B, int T, int Hq, int Hkv, int d, int n_out, int window,
+                                      orthros_dtype dtype) {
+    if (T < 0 || n_out < 0) return 0;
+    if (check_shapes(B, Hq, Hkv, d, window, 1.0f, dtype) != ORTHROS_OK) return 0;
+    return prefill_layout(B, T, Hkv, d, n_out, dtype).total;
+}
+
+orthros_status orthros_prefill(const void *q, const void *k, const void *v, const float *alpha_base,
+                               const float *beta_base, const float *alpha_out, const float *beta_out,
+                               const int32_t *out_indptr, const int32_t *out_positions, int n_out,
+                               const void *q_out, int B, int T, int Hq, int Hkv, int d, int window,
+                               float scale, orthros_dtype dtype, void *o_base, float *lse_base,
+                               void *o_out, float *lse_out, void *k_cache, void *v_cache,
+                               const int32_t *block_table, int max_pages, int page_size, int num_pages,
+                               void *workspace, size_t workspace_bytes, orthros_stream_t stream) {
+    g_last_error.clear();
+    return prefill_core(q, k, v, alpha_base, beta_base, alpha_out, beta_out, out_indptr, out_positions, n_out, q_out,
+                        B, T, T, false, Hq, Hkv, d, window, scale, dtype, o_base, lse_base, o_out, nullptr, lse_out,
+                        k_cache, v_cache, block_table, max_pages, page_size, num_pages, workspace, workspace_bytes,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t orthros_prefill_shard_workspace_size(int B, int Tq, int Tkv, int Hq, int Hkv, int d, int n_rows, int window,
+                                            orthros_dtype dtype) {
+    if (Tkv < 0 || Tq < 0 || Tq > Tkv || n_rows < 0 || dtype != ORTHROS_BF16) return 0;
+    if (check_shapes(B, Hq, Hkv, d, window, 1.0f, dtype) != ORTHROS_OK) return 0;
+    return prefill_layout(B, Tkv, Hkv, d, n_rows, dtype).total;
+}
+
+orthros_status orthros_prefill_shard(const void *q, const void *k, const void *v, const float *alpha_base,
+                                     const float *beta_base, const float *alpha_out, const float *beta_out,
+                                     const int32_t *row_indptr, const int32_t *row_positions, int n_rows,
+                                     const void *q_rows, int B, int Tq, int Tkv, int Hq, int Hkv, int d, int window,
+                                     float scale, orthros_dtype dtype, void *o_base, float *lse_base,
+                                     float *o_part, float *lse_part, void *workspace, size_t workspace_bytes,
+                                     orthros_stream_t stream) {
+    g_last_error.clear();
+    if (Tq < 1) return fail(ORTHROS_EINVAL, "Tq = %d: a shard holds at least one query row", Tq);
+    return prefill_core(q, k, v, alpha_base, beta_base, alpha_out, beta_out, row_indptr, row_positions, n_rows,
+                        q_rows, B, Tkv, Tq, true, Hq, Hkv, d, window, scale, dtype, o_base, lse_base, nullptr,
+                        o_part, lse_part, nullptr, nullptr, nullptr, 0, 0, 0, workspace, workspace_bytes,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+orthros_status orthros_merge_partials(const float *o_parts, const float *lse_parts, int n_parts, int n_rows, int Hq,
+                                      int d, orthros_dtype dtype, void *o_out, float *lse_out,
+                                      orthros_stream_t stream_) {
+    g_last_error.clear();
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (n_parts < 1 || n_rows < 0 || Hq < 1) return fail(ORTHROS_EINVAL, "n_parts >= 1, n_rows >= 0, Hq >= 1");
+    if (d != 64 && d != 128) return fail(ORTHROS_EUNSUPPORTED, "head size d = %d (supported: 64, 128)", d);
+    if (dtype != ORTHROS_BF16 && dtype != ORTHROS_F32) return fail(ORTHROS_EINVAL, "unknown dtype %d", (int)dtype);
+    if ((long long)n_rows * Hq > (1LL << 31) / 32)
+        return fail(ORTHROS_EUNSUPPORTED, "n_rows * Hq = %lld exceeds the launch grid", (long long)n_rows * Hq);
+    if (n_rows == 0) return ORTHROS_OK;
+    if (!o_parts || !lse_parts || !o_out || !lse_out) return fail(ORTHROS_EINVAL, "pointers must not be NULL");
+    if (!aligned16(o_parts) || !aligned16(o_out)) return fail(ORTHROS_EINVAL, "o_parts and o_out must be 16-byte aligned");
+    cudaError_t e;
+    {
+        ProfScope ps("merge_partials", stream);
+        e = launch_merge_partials(o_parts, lse_parts, n_parts, n_rows, Hq, d, dtype == ORTHROS_F32, o_out, lse_out,
+                                  stream);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
     return ORTHROS_OK;
 }
 

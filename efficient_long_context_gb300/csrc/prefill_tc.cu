@@ -9,22 +9,25 @@
 // kernel (those of sequences with many output rows; sequences with few output
 // rows take the split-KV kernel instead).
 //
-// Design (one CTA per SM, 320 threads):
+// Design (one CTA per SM, 576 threads):
 //   * A work unit is two 128-row query tiles that read the SAME key/value
 //     tiles: two query heads of one GQA group at the same positions, or (when
 //     the group size is odd, e.g. plain multi-head) two consecutive row blocks
 //     of one head. Key/value tiles of 128 tokens are visited only inside the
 //     union of the tiles' bands; tiles outside the band are never loaded.
-//   * warp 8 (one thread): TMA producer. Keys come from an fp16 copy made by
+//   * warp 16 (one thread): TMA producer. Keys come from an fp16 copy made by
 //     the pre-pass kernel (3 stages), values in bf16 (2 stages), 128B swizzle.
-//   * warp 9 (one thread): tcgen05.mma issuer. S_s = Q_s K^T (M=128, N=128,
+//   * warp 17 (one thread): tcgen05.mma issuer. S_s = Q_s K^T (M=128, N=128,
 //     fp16 operands from shared memory) into TMEM; O_s += P_s V (M=128, N=d,
 //     P read from TMEM as bf16, V from shared memory, MN-major).
-//   * warps 0-3 / 4-7: softmax of tile 0 / tile 1. Thread i owns row i (TMEM
-//     lane i): it reads its 128 logits with tcgen05.ld, masks the two band
-//     edge tiles, keeps a running max with lazy rescaling (O in TMEM is only
-//     rescaled when the max grows by more than 2^8), writes P as packed bf16
-//     back over its logits, and finally normalises O and stores o and lse.
+//   * warps 0-15: softmax, two threads per row. Warp w serves slot
+//     (w >> 2) & 1, key half w >> 3 of each 128-key tile, rows 32 (w & 3) ..
+//     +31 (TMEM lane quarter w & 3). A thread reads its 64 logits with
+//     tcgen05.ld, masks the two band edge tiles, agrees with its partner on
+//     the row's shift, keeps a running max with lazy rescaling (O in TMEM is
+//     only rescaled when the max grows by more than 2^8), writes P as packed
+//     bf16 back over its logits, and finally normalises its half of O and
+//     stores o and lse.
 //   TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [384,384+d).
 //
 // Precision: the query affine runs in fp32 and is rounded to fp16 (11-bit
@@ -109,7 +112,7 @@ __device__ void decode_unit(const TcParams &p, int u, Slot &s0, Slot &s1) {
         b = lu / upb;
         lu -= b * upb;
         rowbase = 0;
-        rows = p.T;
+        rows = p.Tq;
     }
     const int nblk = (rows + kRowsPerTile - 1) / kRowsPerTile;
     const int upk = units_per_kv(nblk, g);
@@ -216,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Slot S = s ? sl1 : sl0;
             if (S.kind < 0 || !q_by_tma(S)) continue;
             mbar_arrive_expect_tx(&mt.q_full[s], C::kTileBytes);
-            const int row = S.kind == 0 ? S.b * p.T + S.row0 : S.row0;
+            const int row = S.kind == 0 ? S.b * p.Tq + S.row0 : S.row0;
             for (int j = 0; j < C::kSub; ++j)
                 tma_load_3d(smem + C::kQ0 + s * C::kTileBytes + j * (kRowsPerTile * 128), S.kind == 0 ? &tm_q : &tm_qo,
                             &mt.q_full[s], 64 * j, S.h, row);
@@ -229,12 +232,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     int pre_k = 0, pre_v = 0;
     const bool closed_form = sl0.kind == 0 && sl1.kind != 1;
     if (warp == kProducerWarp && lane == 0 && closed_form) {
-        const int lo0 = max(0, sl0.row0 - p.window + 1) / kKeysPerTile;
-        const int hi0 = (sl0.row0 + sl0.n - 1) / kKeysPerTile;
+        const int t0 = sl0.row0 + p.q_off;
+        const int lo0 = max(0, t0 - p.window + 1) / kKeysPerTile;
+        const int hi0 = (t0 + sl0.n - 1) / kKeysPerTile;
         int lo = lo0, hi = hi0;
         if (sl1.kind == 0) {
-            lo = min(lo, max(0, sl1.row0 - p.window + 1) / kKeysPerTile);
-            hi = max(hi, (sl1.row0 + sl1.n - 1) / kKeysPerTile);
+            const int t1 = sl1.row0 + p.q_off;
+            lo = min(lo, max(0, t1 - p.window + 1) / kKeysPerTile);
+            hi = max(hi, (t1 + sl1.n - 1) / kKeysPerTile);
         }
         const int n_cf = hi - lo + 1;
         const int kvh = sl0.h / (p.Hq / p.Hkv);
@@ -261,13 +266,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int s_me = (warp >> 2) & 1;
     const int h_me = warp >> 3;
     const int row = ((warp & 3) << 5) | lane;
-    int my_t = 0;
+    int my_t = 0;  // the row's position in key coordinates
     bool my_valid = false, my_bad = false;
     if (softmax_thread) {
         const Slot S = s_me ? sl1 : sl0;
         if (S.kind >= 0 && row < S.n) {
-            my_t = S.kind == 0 ? S.row0 + row : p.out_positions[S.row0 + row];
-            my_valid = my_t >= 0 && my_t < p.T;
+            if (S.kind == 0) {
+                my_t = S.row0 + row + p.q_off;
+                my_valid = true;
+            } else {
+                const int t = p.out_positions[S.row0 + row];
+                // a shard's output rows may sit past its keys (they read them all)
+                my_t = p.shard ? min(t, p.T - 1) : t;
+                my_valid = t >= 0 && (p.shard || t < p.T);
+                // without q_out the row's query is the base query at its position
+                if (!p.q_out && (my_t < p.q_off || my_t - p.q_off >= p.Tq)) my_valid = false;
+            }
             my_bad = !my_valid;
             if (my_bad && h_me == 0) set_status(p.status, ORTHROS_DEV_BAD_POSITION);
         }
@@ -285,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int cc = 0; cc < kHalfChunks; ++cc)
                     raws[cc] = *reinterpret_cast<const uint4 *>(qs + sw128_offset<D>(row, h_me * kHalfChunks + cc));
             } else {
-                const __nv_bfloat16 *src = p.q + (((long long)S.b * p.T + my_t) * p.Hq + S.h) * D;
+                const __nv_bfloat16 *src = p.q + (((long long)S.b * p.Tq + (my_t - p.q_off)) * p.Hq + S.h) * D;
 #pragma unroll
                 for (int cc = 0; cc < kHalfChunks; ++cc)
                     raws[cc] = reinterpret_cast<const uint4 *>(src)[h_me * kHalfChunks + cc];
@@ -345,8 +359,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             bd.lo_max = 0;
             return bd;
         }
-        const int lo_min = S.kind == 0 ? max(0, tmin - p.window + 1) : 0;
-        bd.lo_max = S.kind == 0 ? max(0, tmax - p.window + 1) : 0;
+        const int lo_min = S.kind == 0 ? max(0, tmin - p.window + 1) : p.key_lo;
+        bd.lo_max = S.kind == 0 ? max(0, tmax - p.window + 1) : p.key_lo;
         bd.kt_lo = lo_min / kKeysPerTile;
         bd.kt_hi = tmax / kKeysPerTile;
         return bd;
@@ -485,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t t_s = tmem + lane_off + s * 128;                // S_s columns of this lane quarter
         const uint32_t t_o = tmem + lane_off + C::kTmemO + s * 128 + hh * (D / 2);  // this half of O_s
         const int t_row = my_valid ? my_t : bd.t_max;
-        const int lo_row = S.kind == 0 ? max(0, t_row - p.window + 1) : 0;
+        const int lo_row = S.kind == 0 ? max(0, t_row - p.window + 1) : p.key_lo;
         const float c2 = p.scale_log2;
         const int t_min_s = bd.t_min;
         float m_ref = -INFINITY, l = 0.f;
@@ -589,14 +603,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool store = have && S.kind >= 0 && row < S.n;
             uint8_t *stage = smem + C::kQ0 + s * C::kTileBytes;
             __nv_bfloat16 *dst = nullptr;
+            float *dst32 = nullptr;  // output rows written as float (shard partials)
             float *lse_dst = nullptr;
             if (store && S.kind == 0) {
-                lse_dst = p.lse_base + ((long long)S.b * p.Hq + S.h) * p.T + my_t;
+                lse_dst = p.lse_base + ((long long)S.b * p.Hq + S.h) * p.Tq + (my_t - p.q_off);
             } else if (store) {
-                dst = p.o_out + ((long long)(S.row0 + row) * p.Hq + S.h) * D + hh * (D / 2);
+                const long long o_off = ((long long)(S.row0 + row) * p.Hq + S.h) * D + hh * (D / 2);
+                if (p.o_out_f32) dst32 = p.o_out_f32 + o_off;
+                else dst = p.o_out + o_off;
                 lse_dst = p.lse_out + (long long)(S.row0 + row) * p.Hq + S.h;
             }
-            const float inv = my_bad ? __int_as_float(0x7fc00000) : 1.f / l_all;
+            // a shard's output row before the shard's first key has no keys: o = 0, lse = -inf
+            const float inv = my_bad ? __int_as_float(0x7fc00000) : (l_all > 0.f ? 1.f / l_all : 0.f);
 #pragma unroll
             for (int j = 0; j < D / 64; ++j) {
                 uint32_t o[32];
@@ -612,12 +630,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int c0 = (hh * (D / 2) + 32 * j) / 8;  // first 16-byte chunk of these 32 channels
 #pragma unroll
                     for (int e = 0; e < 4; ++e) *reinterpret_cast<uint4 *>(stage + sw128_offset<D>(row, c0 + e)) = w[e];
+                } else if (dst32) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        reinterpret_cast<float4 *>(dst32 + 32 * j)[e] =
+                            make_float4(__uint_as_float(o[4 * e]) * inv, __uint_as_float(o[4 * e + 1]) * inv,
+                                        __uint_as_float(o[4 * e + 2]) * inv, __uint_as_float(o[4 * e + 3]) * inv);
                 } else if (store) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) reinterpret_cast<uint4 *>(dst + 32 * j)[e] = w[e];
                 }
             }
-            if (store && hh == 0) *lse_dst = my_bad ? __int_as_float(0x7fc00000) : m_ref * p.scale + logf(l_all);
+            if (store && hh == 0)
+                *lse_dst = my_bad ? __int_as_float(0x7fc00000)
+                                  : (l_all > 0.f ? m_ref * p.scale + logf(l_all) : -INFINITY);
             if (tile_store && have) {
                 fence_proxy_async_smem();
                 mbar_arrive(&mt.os_bar[s]);
@@ -629,6 +655,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     bulk_wait_read();
                 }
             }
+        } else if (cnt == 0 && !*abort && S.kind == 1 && row < S.n && my_valid) {
+            // no key tile in the slot's band (a shard's rows that all precede its keys)
+            const long long o_off = ((long long)(S.row0 + row) * p.Hq + S.h) * D + hh * (D / 2);
+            for (int c = 0; c < D / 2; ++c) {
+                if (p.o_out_f32) p.o_out_f32[o_off + c] = 0.f;
+                else p.o_out[o_off + c] = __float2bfloat16_rn(0.f);
+            }
+            if (hh == 0) p.lse_out[(long long)(S.row0 + row) * p.Hq + S.h] = -INFINITY;
         }
     }
 
@@ -673,18 +707,13 @@ cudaError_t launch_d(const TcParams &p, const void *k16, const void *v, int unit
     CUtensorMap tk, tv, tq, tqo, tob;
     if (!make_kv_map(&tk, k16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.B, p.T, p.Hkv, D) ||
         !make_kv_map(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.B, p.T, p.Hkv, D) ||
-        !make_kv_map(&tob, p.o_base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.B, p.T, p.Hq, D) ||
-        !encode_kv_map_3d(&tq, p.q, (long long)p.B * p.T, p.Hq, D, kRowsPerTile) ||
+        !make_kv_map(&tob, p.o_base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.B, p.Tq, p.Hq, D) ||
+        !encode_kv_map_3d(&tq, p.q, (long long)p.B * p.Tq, p.Hq, D, kRowsPerTile) ||
         !encode_kv_map_3d(&tqo, p.q_out ? (const void *)p.q_out : (const void *)p.q,
-                          p.q_out ? (long long)p.n_out : (long long)p.B * p.T, p.Hq, D, kRowsPerTile))
+                          p.q_out ? (long long)p.n_out : (long long)p.B * p.Tq, p.Hq, D, kRowsPerTile))
         return cudaErrorInvalidValue;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             Cfg<D>::kSmem);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static SmemLimit limit;
+    if (cudaError_t e = limit.ensure((const void *)prefill_tc_kernel<D>, Cfg<D>::kSmem); e != cudaSuccess) return e;
     prefill_tc_kernel<D><<<units, kThreads, Cfg<D>::kSmem, stream>>>(tk, tv, tq, tqo, tob, p);
     return cudaGetLastError();
 }

@@ -206,13 +206,9 @@ cudaError_t launch_bn(const ProjParams &p, cudaStream_t stream) {
     if (!encode_kv_map_3d(&tx, p.x, (long long)p.n_base + p.n_out, 1, p.d_model, BM) ||
         !encode_kv_map_3d(&tw, p.w_t, N, 1, p.d_model, BN))
         return cudaErrorInvalidValue;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e =
-            cudaFuncSetAttribute(project_tc_kernel<BN, KS, BM>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static SmemLimit limit;
+    if (cudaError_t e = limit.ensure((const void *)project_tc_kernel<BN, KS, BM>, C::kSmem); e != cudaSuccess)
+        return e;
     const dim3 grid(N / BN, (p.n_base + p.n_out + BM - 1) / BM);
     project_tc_kernel<BN, KS, BM><<<grid, kThreadsP, C::kSmem, stream>>>(tx, tw, p);
     return cudaGetLastError();

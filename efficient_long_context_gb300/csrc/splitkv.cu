@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(kThreads) splitkv_kernel(const SplitParams p) 
     uint8_t *vs = smem + kStages * kTileBytes;
     __shared__ RowInfo rows[kMaxRows];
     __shared__ int grp_lo, grp_hi, grp_ok;
+    __shared__ int grp_bad;  // a block-table entry of this chunk's keys lay outside the page pool
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g4 = lane >> 2, t4 = lane & 3;  // mma fragment coordinates
@@ -134,9 +135,9 @@ __global__ void __launch_bounds__(kThreads) splitkv_kernel(const SplitParams p) 
                     set_status(p.status, ORTHROS_DEV_BAD_LENGTH);
                 }
             } else {
-                const int t = p.out_positions[pos_base + tid / gsz];
-                if (t >= 0 && t < p.T) {
-                    ri.lo = 0;
+                const int t = prefill_row_end(p, p.out_positions[pos_base + tid / gsz]);
+                if (t >= 0) {
+                    ri.lo = p.key_lo;
                     ri.hi = t;
                 } else if (chunk_id == 0 && tid % gsz == 0) {
                     set_status(p.status, ORTHROS_DEV_BAD_POSITION);
@@ -157,6 +158,7 @@ __global__ void __launch_bounds__(kThreads) splitkv_kernel(const SplitParams p) 
         grp_lo = max(lo, c0);
         grp_hi = min(hi, c1);
         grp_ok = grp_lo <= grp_hi;
+        grp_bad = 0;
     }
     __syncthreads();
     float *part = p.partial + ((long long)group * p.max_chunks + chunk_id) * kMaxRows * (D + 2);
@@ -193,10 +195,9 @@ __global__ void __launch_bounds__(kThreads) splitkv_kernel(const SplitParams p) 
             } else {
                 const int pi = pos_base + r / gsz;
                 const int h = kv * gsz + r % gsz;
-                int t = p.out_positions[pi];
-                t = min(max(t, 0), p.T - 1);
+                const int i = min(max(p.out_positions[pi] - p.q_off, 0), p.Tq - 1);  // query row of the position
                 qrow = p.q_out ? p.q_out + ((long long)pi * p.Hq + h) * D
-                               : p.q + (((long long)b * p.T + t) * p.Hq + h) * D;
+                               : p.q + (((long long)b * p.Tq + i) * p.Hq + h) * D;
                 al = p.alpha_out + h * D;
                 be = p.beta_out + h * D;
             }
@@ -249,6 +250,7 @@ __global__ void __launch_bounds__(kThreads) splitkv_kernel(const SplitParams p) 
                 int pg = bt[j / p.page_size];
                 if (pg < 0 || pg >= p.num_pages) {
                     set_status(p.status, ORTHROS_DEV_BAD_PAGE);
+                    grp_bad = 1;
                     pg = 0;
                 }
                 off = ((long long)pg * p.page_size + j % p.page_size) * tok_stride;
@@ -399,6 +401,9 @@ __global__ void __launch_bounds__(kThreads) splitkv_kernel(const SplitParams p) 
             if (c < D) acc += wgt * src[c];
             else if (c == D + 1) acc += wgt * src[D + 1];
         }
+        // rows that read keys loaded from a substituted page: a NaN row sum
+        // makes the combined row NaN
+        if (c == D + 1 && grp_bad && rows[r].lo <= key_hi && rows[r].hi >= key_lo) acc = __int_as_float(0x7fc00000);
         part[r * kRowStride + c] = c == D ? M : acc;
     }
 }
@@ -431,6 +436,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const SplitParams p) {
     if (r >= nrows) return;
     int hi;
     __nv_bfloat16 *dst;
+    float *dst32 = nullptr;
     float *lse_dst;
     if (p.mode == kSplitExtend) {
         // the same validity rule as the split kernel's rows
@@ -449,14 +455,23 @@ __global__ void __launch_bounds__(256) combine_kernel(const SplitParams p) {
     } else {
         const int pi = pos_base + r / gsz;
         const int h = kv * gsz + r % gsz;
-        const int t = p.out_positions[pi];
-        hi = (t >= 0 && t < p.T) ? t : -1;
+        hi = prefill_row_end(p, p.out_positions[pi]);
         dst = p.o_out + ((long long)pi * p.Hq + h) * D;
         lse_dst = p.lse_out + (long long)pi * p.Hq + h;
+        if (p.o_out_f32) {  // float output rows (a shard's partials)
+            dst = nullptr;
+            dst32 = p.o_out_f32 + ((long long)pi * p.Hq + h) * D;
+        }
     }
     const float nanv = __int_as_float(0x7fc00000);
+    // a split kernel that gave up on a bounded wait left some partials
+    // unwritten (they may hold an earlier call's values): every row is NaN
+    if (p.status && (*reinterpret_cast<volatile uint32_t *>(p.status) & ORTHROS_DEV_TIMEOUT)) hi = -1;
     if (hi < 0) {
-        for (int c = lane; c < D; c += 32) dst[c] = __float2bfloat16_rn(nanv);
+        for (int c = lane; c < D; c += 32) {
+            if (dst32) dst32[c] = nanv;
+            else dst[c] = __float2bfloat16_rn(nanv);
+        }
         if (lane == 0) *lse_dst = nanv;
         return;
     }
@@ -483,22 +498,23 @@ __global__ void __launch_bounds__(256) combine_kernel(const SplitParams p) {
 #pragma unroll
         for (int e = 0; e < E; ++e) acc[e] += w * src[lane + 32 * e];
     }
-    const float inv = 1.f / Lsum;
+    // a row without keys (a shard's row before its first key): o = 0, lse = -inf
+    const bool empty = M == -INFINITY;
+    const float inv = empty ? 0.f : 1.f / Lsum;
 #pragma unroll
-    for (int e = 0; e < E; ++e) dst[lane + 32 * e] = __float2bfloat16_rn(acc[e] * inv);
-    if (lane == 0) *lse_dst = M * p.scale + logf(Lsum);
+    for (int e = 0; e < E; ++e) {
+        if (dst32) dst32[lane + 32 * e] = acc[e] * inv;
+        else dst[lane + 32 * e] = __float2bfloat16_rn(acc[e] * inv);
+    }
+    if (lane == 0) *lse_dst = empty ? -INFINITY : M * p.scale + logf(Lsum);
 }
 
 template <int D, int NT>
 cudaError_t launch_split_t(const SplitParams &p, cudaStream_t stream) {
     constexpr int kSmem = 2 * kStages * kBlockKeys * D * 2;
     static_assert(kSmem >= kWarps * kMaxRows * (D + 2) * 4, "reduction scratch must fit the stage buffers");
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(splitkv_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static SmemLimit limit;
+    if (cudaError_t e = limit.ensure((const void *)splitkv_kernel<D, NT>, kSmem); e != cudaSuccess) return e;
     const long long ctas = (long long)p.max_chunks * p.n_groups;
     if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     splitkv_kernel<D, NT><<<(unsigned)ctas, kThreads, kSmem, stream>>>(p);

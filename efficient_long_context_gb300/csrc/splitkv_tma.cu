@@ -105,10 +105,11 @@ __device__ __forceinline__ ItemInfo item_info(const SplitParams &p, int group) {
         it.nrows = npos * gsz;
         int hi = -1;
         for (int i = 0; i < npos; ++i) {
-            const int t = p.out_positions[it.pos_base + i];
-            if (t >= 0 && t < p.T) hi = max(hi, t);
+            const int t = prefill_row_end(p, p.out_positions[it.pos_base + i]);
+            if (t >= p.key_lo) hi = max(hi, t);
         }
         it.union_hi = hi;
+        it.union_lo = (p.key_lo / kStageKeys) * kStageKeys;
     }
     return it;
 }
@@ -131,9 +132,9 @@ __device__ __forceinline__ void row_range(const SplitParams &p, const ItemInfo &
             lo = kind == 0 ? max(0, t - p.window + 1) : 0;
         }
     } else {
-        const int t = p.out_positions[it.pos_base + r / gsz];
-        if (t >= 0 && t < p.T) {
-            lo = 0;
+        const int t = prefill_row_end(p, p.out_positions[it.pos_base + r / gsz]);
+        if (t >= 0) {
+            lo = p.key_lo;
             hi = t;
         }
     }
@@ -145,6 +146,9 @@ template <int D> struct TCfg {
     static constexpr int kStageBytes = 2 * kTile;  // K + V
     static constexpr int kScratch = kConsumers * kMaxRowsT * (D + 2) * 4;
     static constexpr int kBar = kStages * kStageBytes + kScratch;
+    // barriers (2 kStages + 2) x 8 B, the abort flag and kStages stage flags
+    static constexpr int kMetaBytes = (2 * kStages + 2) * 8 + 4 + 4 * kStages;
+    static_assert(kMetaBytes <= 192, "stage metadata must fit its region");
     static constexpr int kSmem = kBar + 192 + 1024;
 };
 
@@ -161,6 +165,10 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     uint64_t *merge_bar = empty + C::kStages;  // [2]: states written / partial written (one arrive per consumer warp)
     int *abort_flag = reinterpret_cast<int *>(merge_bar + 2);
     volatile int *abort = abort_flag;
+    // per stage: 1 when a block-table entry of its keys was outside the page
+    // pool (the producer then loaded page 0 in its place); written before the
+    // stage's full barrier is armed, read by the consumers after it completes
+    volatile int *stage_bad = abort_flag + 1;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gsz = p.Hq / p.Hkv;
     // Items run chunk-major: CTAs that run at the same time read the same
@@ -188,6 +196,12 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         // ---------------- producer: one thread streams every stage of every item ----------------
         if (lane != 0) return;
         uint32_t sc = 0;  // stages issued so far
+        // Before leaving (normally or on abort) wait, bounded, for the copies of
+        // the last stages issued, so that none is in flight when the CTA exits.
+        auto drain = [&]() {
+            for (uint32_t i = sc > (uint32_t)C::kStages ? sc - C::kStages : 0; i < sc; ++i)
+                mbar_wait_drain(&full[i % C::kStages], (i / C::kStages) & 1, p.status);
+        };
         for (int item = blockIdx.x; item < total_items && !*abort; item += gridDim.x) {
             const int group = p.group_offset + item % n_groups, chunk = item / n_groups;
             const ItemInfo it = item_info(p, group);
@@ -198,35 +212,43 @@ __global__ void __launch_bounds__(kThreadsT, 1)
             for (int j0 = key_lo; j0 <= key_hi; j0 += kStageKeys, ++sc) {
                 const int st = sc % C::kStages;
                 if (sc >= (uint32_t)C::kStages &&
-                    !mbar_wait(&empty[st], ((sc / C::kStages) - 1) & 1, abort, p.status))
+                    !mbar_wait(&empty[st], ((sc / C::kStages) - 1) & 1, abort, p.status)) {
+                    drain();
                     return;
-                mbar_arrive_expect_tx(&full[st], C::kStageBytes);
-                uint8_t *ks = smem + st * C::kStageBytes;
-                uint8_t *vs = ks + C::kTile;
+                }
+                int tok[2], bad = 0;
 #pragma unroll
                 for (int tb = 0; tb < 2; ++tb) {
                     const int j = j0 + tb * kBoxTokens;
-                    int tok = (int)p.kv_tokens;  // past the end: TMA fills zeros
+                    tok[tb] = (int)p.kv_tokens;  // past the end: TMA fills zeros
                     if (j <= key_hi) {
                         if (bt) {
                             int pg = bt[j / p.page_size];
                             if (pg < 0 || pg >= p.num_pages) {
                                 set_status(p.status, ORTHROS_DEV_BAD_PAGE);
+                                bad = 1;
                                 pg = 0;
                             }
-                            tok = pg * p.page_size + j % p.page_size;
+                            tok[tb] = pg * p.page_size + j % p.page_size;
                         } else {
-                            tok = it.b * p.T + j;
+                            tok[tb] = it.b * p.T + j;
                         }
                     }
+                }
+                stage_bad[st] = bad;  // released to the consumers by the arrive below
+                mbar_arrive_expect_tx(&full[st], C::kStageBytes);
+                uint8_t *ks = smem + st * C::kStageBytes;
+                uint8_t *vs = ks + C::kTile;
+#pragma unroll
+                for (int tb = 0; tb < 2; ++tb)
 #pragma unroll
                     for (int h = 0; h < D / 64; ++h) {
-                        tma_load_3d(ks + (h * 2 + tb) * kBoxBytes, &tm_k, &full[st], 64 * h, it.kv, tok);
-                        tma_load_3d(vs + (h * 2 + tb) * kBoxBytes, &tm_v, &full[st], 64 * h, it.kv, tok);
+                        tma_load_3d(ks + (h * 2 + tb) * kBoxBytes, &tm_k, &full[st], 64 * h, it.kv, tok[tb]);
+                        tma_load_3d(vs + (h * 2 + tb) * kBoxBytes, &tm_v, &full[st], 64 * h, it.kv, tok[tb]);
                     }
-                }
             }
         }
+        drain();
         return;
     }
 
@@ -258,8 +280,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
                 if (tid % gsz == 0 && extend_position(p, group, it.b, it.L, tid / gsz, kind, idx) < 0)
                     set_status(p.status, (it.L < 0 || kind == 0) ? ORTHROS_DEV_BAD_LENGTH : ORTHROS_DEV_BAD_POSITION);
             } else if (tid % gsz == 0) {
-                const int t = p.out_positions[it.pos_base + tid / gsz];
-                if (t < 0 || t >= p.T) set_status(p.status, ORTHROS_DEV_BAD_POSITION);
+                if (prefill_row_end(p, p.out_positions[it.pos_base + tid / gsz]) < 0)
+                    set_status(p.status, ORTHROS_DEV_BAD_POSITION);
             }
         }
         if (key_lo > key_hi) {
@@ -303,9 +325,9 @@ __global__ void __launch_bounds__(kThreadsT, 1)
                 } else {
                     const int pi = it.pos_base + r / gsz;
                     const int h = it.kv * gsz + r % gsz;
-                    const int t = min(max(p.out_positions[pi], 0), p.T - 1);
+                    const int i = min(max(p.out_positions[pi] - p.q_off, 0), p.Tq - 1);  // query row of the position
                     qrow = p.q_out ? p.q_out + ((long long)pi * p.Hq + h) * D
-                                   : p.q + (((long long)it.b * p.T + t) * p.Hq + h) * D;
+                                   : p.q + (((long long)it.b * p.Tq + i) * p.Hq + h) * D;
                     al = p.alpha_out + h * D;
                     be = p.beta_out + h * D;
                 }
@@ -340,10 +362,18 @@ __global__ void __launch_bounds__(kThreadsT, 1)
                 for (int e = 0; e < 4; ++e) o[nt][cm][e] = 0.f;
         }
         bool ok = true;
+        uint32_t bad_rows = 0;  // bit 2 nt + e: a row of this thread read a stage loaded from a bad page
         for (int j0 = key_lo; j0 <= key_hi; j0 += kStageKeys, ++sc) {
             const int st = sc % C::kStages;
             ok = __all_sync(0xffffffffu, mbar_wait(&full[st], (sc / C::kStages) & 1, abort, p.status));
             if (!ok) break;
+            if (stage_bad[st]) {
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e)
+                        if (rlo[nt][e] <= j0 + kStageKeys - 1 && rhi[nt][e] >= j0) bad_rows |= 1u << (2 * nt + e);
+            }
             const uint32_t kt = smem_u32(smem + st * C::kStageBytes);
             const uint32_t vt = kt + C::kTile;
             const int r0 = warp * 32;  // this warp's 32 keys of the stage
@@ -444,8 +474,9 @@ __global__ void __launch_bounds__(kThreadsT, 1)
                     dst[16 * cm + g4 + 8] = o[nt][cm][2 + e];
                 }
                 if (g4 == 0) {
+                    // a NaN row sum makes the combined row NaN (the data behind it is not the row's)
                     dst[D] = m[nt][e];
-                    dst[D + 1] = l[nt][e];
+                    dst[D + 1] = (bad_rows >> (2 * nt + e)) & 1u ? __int_as_float(0x7fc00000) : l[nt][e];
                 }
             }
         if (!consumer_sync(0)) return;
@@ -476,13 +507,9 @@ cudaError_t launch_t(const SplitParams &p, cudaStream_t stream) {
     if (!encode_kv_map_3d(&tk, p.k, p.kv_tokens, p.Hkv, D, kBoxTokens) ||
         !encode_kv_map_3d(&tv, p.v, p.kv_tokens, p.Hkv, D, kBoxTokens))
         return cudaErrorInvalidValue;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(splitkv_tma_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             TCfg<D>::kSmem);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static SmemLimit limit;
+    if (cudaError_t e = limit.ensure((const void *)splitkv_tma_kernel<D, NT>, TCfg<D>::kSmem); e != cudaSuccess)
+        return e;
     int dev = 0, sms = 152;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const long long items = (long long)p.n_groups * p.max_chunks;

@@ -127,6 +127,64 @@ ORTHROS_API orthros_status orthros_prefill(
     int max_pages, int page_size, int num_pages,
     void *workspace, size_t workspace_bytes, orthros_stream_t stream);
 
+/* Workspace bytes orthros_prefill_shard needs for these sizes (0 if rejected). */
+ORTHROS_API size_t orthros_prefill_shard_workspace_size(int B, int Tq, int Tkv, int Hq, int Hkv, int d,
+                                                       int n_rows, int window, orthros_dtype dtype);
+
+/*
+ * One rank's share of a prefill whose token axis is cut into contiguous chunks
+ * across devices (sequence parallelism: the paper runs its 64K-1M-token
+ * prefills on 8 GPUs, Sec. 4.5 and the appendix's training/inference setup,
+ * without describing the split). Eq. 4 needs only a halo of the w - 1 keys
+ * before a chunk; Eq. 5 of an output row spans every chunk up to its position,
+ * so each chunk contributes a normalised partial that orthros_merge_partials
+ * combines exactly.
+ *
+ * The chunk holds Tq tokens at global positions P0 .. P0 + Tq - 1. Its keys
+ * and values come with the H = Tkv - Tq tokens before it (the halo, received
+ * from the ranks that own them; H >= min(w - 1, P0) makes the band rows exact):
+ * k, v [B, Tkv, Hkv, d] hold positions P0 - H .. P0 + Tq - 1. Positions below
+ * are in this buffer's coordinates (global position - P0 + H).
+ *   - base rows (Eq. 4): q [B, Tq, Hq, d] are the chunk's raw queries; query
+ *     i sits at position H + i and attends keys max(0, H + i - w + 1) .. H + i.
+ *     o_base [B, Tq, Hq, d] (dtype), lse_base [B, Hq, Tq] float.
+ *   - partial output rows (Eq. 5 over the chunk's own keys): row r of sequence b
+ *     (row_indptr as out_indptr of orthros_prefill, HOST) at position t_r >= 0
+ *     attends keys H .. min(t_r, Tkv - 1): rows owned by later ranks have
+ *     t_r >= Tkv and read the whole chunk; a row with t_r < H reads nothing and
+ *     gets o = 0, lse = -inf. q_rows [n_rows, Hq, d] are their raw
+ *     output-stream queries (required when n_rows > 0).
+ *     o_part [n_rows, Hq, d] float, lse_part [n_rows, Hq] float.
+ * bf16 only (ORTHROS_EUNSUPPORTED otherwise); 1 <= Tq <= Tkv. A negative
+ * row position sets ORTHROS_DEV_BAD_POSITION and that row is NaN. Workspace
+ * and errors as for orthros_prefill.
+ */
+ORTHROS_API orthros_status orthros_prefill_shard(
+    const void *q, const void *k, const void *v,
+    const float *alpha_base, const float *beta_base,
+    const float *alpha_out, const float *beta_out,
+    const int32_t *row_indptr, const int32_t *row_positions, int n_rows,
+    const void *q_rows,
+    int B, int Tq, int Tkv, int Hq, int Hkv, int d, int window, float scale,
+    orthros_dtype dtype,
+    void *o_base, float *lse_base, float *o_part, float *lse_part,
+    void *workspace, size_t workspace_bytes, orthros_stream_t stream);
+
+/*
+ * Exact merge of normalised attention partials of the same rows over disjoint
+ * key sets: lse = log sum_p exp(lse_p), o = sum_p exp(lse_p - lse) o_p (each
+ * set's share of the softmax denominator is exp(lse_p)). Merges the chunk
+ * partials of orthros_prefill_shard into the rows of Eq. 5.
+ * o_parts [n_parts, n_rows, Hq, d] float, lse_parts [n_parts, n_rows, Hq] float
+ * o_out [n_rows, Hq, d] of element type dtype, lse_out [n_rows, Hq] float.
+ * A partial with lse = -inf holds no keys and weighs nothing; a row whose
+ * partials are all empty comes back empty (o = 0, lse = -inf), so partials
+ * may be merged in any grouping. Needs no workspace.
+ */
+ORTHROS_API orthros_status orthros_merge_partials(const float *o_parts, const float *lse_parts, int n_parts,
+                                                  int n_rows, int Hq, int d, orthros_dtype dtype,
+                                                  void *o_out, float *lse_out, orthros_stream_t stream);
+
 /* Workspace bytes orthros_prefill_backward needs for these sizes (0 if rejected). */
 ORTHROS_API size_t orthros_prefill_backward_workspace_size(int B, int T, int Hq, int Hkv, int d,
                                                int n_out, int window, orthros_dtype dtype);

@@ -93,6 +93,55 @@ def test_prefill_host_checks(lib, over, code):
     assert ola.orthros_last_error() != ""
 
 
+def _call_shard(lib, **over):
+    args = dict(q=1 << 12, k=1 << 12, v=1 << 12, ab=1 << 12, bb=1 << 12, ao=1 << 12, bo=1 << 12,
+                indptr=(ctypes.c_int32 * 2)(0, 1), pos=1 << 12, n_rows=1, q_rows=1 << 12,
+                B=1, Tq=16, Tkv=40, Hq=4, Hkv=2, d=128, window=8, scale=0.1, dtype=0,
+                o_base=1 << 12, lse_base=1 << 12, o_part=1 << 12, lse_part=1 << 12,
+                ws=1 << 12, ws_bytes=1 << 30, stream=None)
+    args.update(over)
+    a = args
+    return lib.orthros_prefill_shard(a["q"], a["k"], a["v"], a["ab"], a["bb"], a["ao"], a["bo"], a["indptr"],
+                                     a["pos"], a["n_rows"], a["q_rows"], a["B"], a["Tq"], a["Tkv"], a["Hq"],
+                                     a["Hkv"], a["d"], a["window"], a["scale"], a["dtype"], a["o_base"],
+                                     a["lse_base"], a["o_part"], a["lse_part"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(Tq=0), 1),             # a shard holds at least one query row
+    (dict(Tq=41), 1),            # more queries than keys
+    (dict(dtype=1), 2),          # bf16 only
+    (dict(q_rows=None), 1),      # output rows need their queries
+    (dict(o_part=None), 1),
+    (dict(o_part=(1 << 12) + 4), 1),  # misaligned
+    (dict(indptr=(ctypes.c_int32 * 2)(0, 2)), 1),
+    (dict(ws_bytes=8), 4),
+    (dict(Hq=3), 1),
+])
+def test_shard_host_checks(lib, over, code):
+    assert _call_shard(lib, **over) == code
+    assert ola.orthros_last_error() != ""
+
+
+def test_shard_workspace_size(lib):
+    assert ola.orthros_prefill_shard_workspace_size(1, 16, 40, 4, 2, 128, 1, 8) > 0
+    assert ola.orthros_prefill_shard_workspace_size(1, 41, 40, 4, 2, 128, 1, 8) == 0  # Tq > Tkv
+    assert ola.orthros_prefill_shard_workspace_size(1, 16, 40, 4, 2, 128, 1, 8, torch.float32) == 0
+
+
+@pytest.mark.parametrize("args,code", [
+    ((0, 4, 8, 128, 0), 1),   # no partials
+    ((2, -1, 8, 128, 0), 1),  # negative row count
+    ((2, 4, 8, 96, 0), 2),    # head size
+    ((2, 4, 8, 128, 5), 1),   # dtype
+])
+def test_merge_host_checks(lib, args, code):
+    n_parts, n_rows, Hq, d, dtype = args
+    rc = lib.orthros_merge_partials(1 << 12, 1 << 12, n_parts, n_rows, Hq, d, dtype, 1 << 12, 1 << 12, None)
+    assert rc == code
+    assert ola.orthros_last_error() != ""
+
+
 def test_decode_host_checks(lib):
     rc = lib.orthros_decode(1 << 12, None, 1 << 12, 1 << 12, 1 << 12, 1 << 12, 1 << 12, 0, 64, 4, 1 << 12,
                             1 << 12, 1 << 12, 1 << 12, 1 << 12, 2, 4, 2, 128, 16, 0.1, 0,

@@ -86,6 +86,38 @@ def test_decode_bad_length_and_page(dtype):
     assert torch.isfinite(out[0][0].float()).all()  # an untouched sequence is fine
 
 
+def bad_page_decode_case():
+    """Three sequences on 64-token pages (the TMA-fed split-KV path); sequence
+    1 (300 cached tokens) has a block-table entry outside the pool for its
+    tokens 64..127. Its output row reads them, its 64-key window does not."""
+    wl = W.DecodeWorkload("bad_page64", 3, 8, 2, 128, 64, 64, 0, 0, 1, seed=12)
+    st = W.make_decode(wl, lens=[100, 300, 500])
+    bt = st.block_table.clone()
+    bt[1, 1] = st.k_cache.shape[0] + 7
+    return wl, st, bt
+
+
+def check_bad_page_rows(out):
+    o_base, _, o_out, lse_out = (t.float() for t in out)
+    assert torch.isnan(o_out[1]).all() and torch.isnan(lse_out[1]).all()  # reads the bad page
+    assert torch.isfinite(o_base[1]).all()  # its window lies past the bad page
+    for b in (0, 2):  # untouched sequences
+        assert torch.isfinite(o_out[b]).all() and torch.isfinite(o_base[b]).all()
+
+
+def test_decode_bad_page_on_tma_path_gives_nan_rows():
+    wl, st, bt = bad_page_decode_case()
+    dev = "cuda"
+    aff = [a.to(dev) for a in (st.alpha_base, st.beta_base, st.alpha_out, st.beta_out)]
+    ws = torch.empty(ola.orthros_decode_workspace_size(3, 8, 2, 128, bt.shape[1], 64), dtype=torch.uint8, device=dev)
+    out = ola.orthros_decode(st.q[0].to(dev), st.k_new[0].to(dev), st.v_new[0].to(dev), st.k_cache.to(dev),
+                             st.v_cache.to(dev), bt.to(dev), st.cache_lens.to(dev), *aff, wl.window, wl.scale,
+                             workspace=ws)
+    rc, bits = ola.orthros_check(ws)
+    assert rc == 5 and bits & DEV_BAD_PAGE, (rc, bits)
+    check_bad_page_rows(out)
+
+
 @pytest.mark.parametrize("page_size,dtype", [(64, torch.bfloat16), (16, torch.bfloat16), (16, torch.float32)])
 def test_extend_bad_rows_are_flagged(page_size, dtype):
     """A history output row without q_out and a sequence whose length runs past

@@ -20,6 +20,7 @@ import torch
 import efficient_long_context_gb300 as ola
 from efficient_long_context_gb300 import workloads as W
 from tests.parity_util import TOL, max_err
+from tests.test_gpu_status import bad_page_decode_case, check_bad_page_rows
 
 
 @pytest.mark.gpu
@@ -49,6 +50,20 @@ def test_static_decode_matches_workspace_decode():
             err = max_err(g, r.float().cpu().numpy())
             assert err <= tol, f"step {s} {name}: {err}"
         assert torch.equal(kc_a, kc_b) and torch.equal(vc_a, vc_b), "the appends differ"
+
+
+@pytest.mark.gpu
+def test_static_decode_bad_page_gives_nan_rows():
+    # the status word of this entry point is not exposed, so rows that read a
+    # block-table entry outside the page pool must come back as NaN
+    wl, st, bt = bad_page_decode_case()
+    dev = "cuda"
+    aff = [a.to(dev) for a in (st.alpha_base, st.beta_base, st.alpha_out, st.beta_out)]
+    out = ola.orthros_decode_static(st.q[0].to(dev), st.k_new[0].to(dev), st.v_new[0].to(dev), st.k_cache.to(dev),
+                                    st.v_cache.to(dev), bt.to(dev), st.cache_lens.to(dev), *aff, wl.window,
+                                    wl.scale)
+    torch.cuda.synchronize()
+    check_bad_page_rows(out)
 
 
 def test_static_decode_refuses_sizes_beyond_the_array():
