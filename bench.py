@@ -229,6 +229,85 @@ def oracle_sample(wl_inputs, wl, target_s: float, seed: int = 0):
     return flops / dt / 1e12, nthreads, desc
 
 
+def oracle_prefill_sample(inputs, wl, target_s: float, seed: int = 0):
+    """Time the oracle on a sample of the workload's own rows: random base
+    positions of every sequence (their true windows) and random output rows
+    (their whole causal prefix), growing the sample until it takes about
+    target_s seconds. Returns (TFLOP/s of the sampled rows' useful work,
+    threads, description)."""
+    import numpy as np
+
+    import oracle
+
+    f32 = inputs.get("_f32")
+    if f32 is None:
+        f32 = {n: inputs[n].float().numpy() for n in ("q", "k", "v", "alpha_base", "beta_base", "alpha_out",
+                                                      "beta_out")}
+        inputs["_f32"] = f32
+    nthreads = len(os.sched_getaffinity(0))
+    indptr = inputs["out_indptr"].numpy().astype(np.int64)
+    pos = inputs["out_positions"].numpy()
+    n_out = int(indptr[-1])
+    rng = np.random.default_rng(seed)
+    n = 1
+    while True:
+        rows = np.sort(rng.choice(wl.T, size=min(n, wl.T), replace=False)).astype(np.int32)
+        orow = np.sort(rng.choice(n_out, size=min(n, n_out), replace=False)) if n_out else np.zeros(0, np.int64)
+        seq = np.searchsorted(indptr, orow, side="right") - 1
+        s_indptr = np.concatenate([[0], np.cumsum(np.bincount(seq, minlength=wl.B))]).astype(np.int32)
+        s_pos = pos[orow].astype(np.int32)
+        t0 = time.perf_counter()
+        oracle.prefill(f32["q"], f32["k"], f32["v"], f32["alpha_base"], f32["beta_base"], f32["alpha_out"],
+                       f32["beta_out"], s_indptr, s_pos, wl.window, wl.scale, base_rows=rows, nthreads=nthreads)
+        dt = time.perf_counter() - t0
+        pairs = wl.B * int(np.minimum(rows.astype(np.int64) + 1, wl.window).sum()) + int((s_pos.astype(np.int64) + 1).sum())
+        flops = pairs * 4 * wl.d * wl.Hq
+        if dt >= target_s or (n >= wl.T and n >= n_out):
+            break
+        n = max(n * 2, int(n * target_s / max(dt, 1e-3) * 1.05))
+    desc = (f"{len(rows)} base positions of each of {wl.B} sequences and {len(orow)} output rows of the "
+            f"{wl.name} workload ({flops / 1e9:.1f} GFLOP useful, {dt:.1f} s)")
+    return flops / dt / 1e12, nthreads, desc
+
+
+def oracle_decode_sample(st, target_s: float, n_seq: int = 4):
+    """Time the oracle on decoding steps of the first n_seq sequences of the
+    decoding workload (their caches copied to a compact float pool), repeating
+    steps until about target_s seconds. Returns (GB/s of algorithmic cache
+    bytes, threads, description)."""
+    import numpy as np
+
+    import oracle
+
+    nthreads = len(os.sched_getaffinity(0))
+    seqs = np.arange(min(n_seq, st.meta["B"]))
+    bt = st.block_table[seqs].numpy()
+    used = np.unique(bt[bt >= 0])
+    remap = np.full(st.k_cache.shape[0], -1, np.int64)
+    remap[used] = np.arange(len(used))
+    obt = np.where(bt >= 0, remap[np.maximum(bt, 0)], -1).astype(np.int32)
+    import torch
+
+    okc = st.k_cache[torch.as_tensor(used)].float().numpy()
+    ovc = st.v_cache[torch.as_tensor(used)].float().numpy()
+    lens = st.cache_lens.numpy()[seqs].astype(np.int32).copy()
+    aff = [a.float().numpy() for a in (st.alpha_base, st.beta_base, st.alpha_out, st.beta_out)]
+    m = st.meta
+    nbytes, steps, t_all = 0, 0, 0.0
+    while t_all < target_s and steps < m["steps"]:
+        t0 = time.perf_counter()
+        oracle.decode(st.q[steps][seqs].float().numpy(), st.k_new[steps][seqs].float().numpy(),
+                      st.v_new[steps][seqs].float().numpy(), okc, ovc, obt, lens, *aff, m["window"], m["scale"],
+                      nthreads=nthreads)
+        t_all += time.perf_counter() - t0
+        nbytes += int((lens.astype(np.int64) + 1).sum()) * m["Hkv"] * m["d"] * 2 * 2
+        lens += 1
+        steps += 1
+    desc = (f"{steps} decoding steps of {len(seqs)} of the {m['B']} sequences ({nbytes / 1e9:.2f} GB of cache "
+            f"read, {t_all:.1f} s)")
+    return nbytes / t_all / 1e9, nthreads, desc
+
+
 def run_reference(args, dist):
     """The reference arm: the CPU oracle as it stands, same metric and config."""
     if dist.rank != 0:
@@ -283,12 +362,16 @@ def _timed(ola, torch, dist, stream, fn, steps):
     return dist.max(ev0.elapsed_time(ev1)), prof
 
 
-def bench_prefill(args, dist, dev, stream, peaks, ola, torch, W):
+def headline_workload(args, W):
     wl = {"128k": W.PREFILL_128K, "pt": W.PT_2K, "sft": W.SFT_8K}[args.prefill_workload]
     if args.prefill_T:
         import dataclasses
 
         wl = dataclasses.replace(wl, T=args.prefill_T, name=f"{wl.name}@T{args.prefill_T}")
+    return wl
+
+
+def bench_prefill(args, dist, dev, stream, peaks, ola, torch, W, wl, e2e=False):
     inputs = W.make_prefill(wl)
     q, k, v = (inputs[n].to(dev) for n in ("q", "k", "v"))
     aff = [inputs[n].to(dev) for n in ("alpha_base", "beta_base", "alpha_out", "beta_out")]
@@ -342,11 +425,12 @@ def bench_prefill(args, dist, dev, stream, peaks, ola, torch, W):
                value=flops["total"] * dist.world / (ms_step * 1e-3) / 1e12,
                roofline={"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peaks["bf16"],
                          "unit": "TFLOP/s", "frac": achieved / peaks["bf16"],
-                         "traffic": captured_traffic("prefill_tc")
-                         if dom == "prefill_tc" and wl.name == W.PREFILL_128K.name else None,
+                         "traffic": captured_traffic({W.PREFILL_128K.name: "prefill_tc", W.PT_2K.name: "prefill_tc_pt",
+                                                      W.SFT_8K.name: "prefill_tc_sft"}.get(wl.name, ""))
+                         if dom == "prefill_tc" else None,
                          "peak_source": f"{peaks['src']} bf16 dense (burst)", "avg_launch_ms": dom_ms / dom_n,
                          "useful_tflop_per_launch": dom_flops / 1e12})
-    if args.only == "all":
+    if e2e:
         # end to end: pinned host buffers, host<->device copies inside the timed region
         h_in = {n: inputs[n].pin_memory() for n in ("q", "k", "v")}
         h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
@@ -428,6 +512,31 @@ def bench_decode(args, dist, dev, stream, peaks, ola, torch, W):
     gbs = nbytes * dist.world / (ms * 1e-3) / 1e9
     dom, (dom_n, dom_ms) = max(prof.items(), key=lambda kv: kv[1][1])
     achieved = nbytes / (dom_ms * 1e-3) / 1e9  # bytes of all steps over that kernel's summed time
+    # end to end through the public call: every step's inputs (queries, new
+    # keys/values, lengths) copied from pinned host memory and its outputs read
+    # back, inside the timed region; the cache stays resident as serving state
+    e2e = None
+    if args.only == "all":
+        h_in = [t.pin_memory() for t in (st.q, st.k_new, st.v_new)]
+        h_lens = lens_steps.cpu().pin_memory()
+        d_in = [torch.empty_like(dq[0]), torch.empty_like(dk[0]), torch.empty_like(dv[0])]
+        d_len = torch.empty_like(lens_steps[0])
+        h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+
+        def e2e_step(s):
+            for hb, db in zip(h_in, d_in):
+                db.copy_(hb[s], non_blocking=True)
+            d_len.copy_(h_lens[s], non_blocking=True)
+            ola.orthros_decode(d_in[0], d_in[1], d_in[2], kc, vc, bt, d_len, *daff, dec.window, dec.scale, out=outs,
+                               workspace=ws, stream=stream)
+            for hb, db in zip(h_out, outs):
+                hb.copy_(db, non_blocking=True)
+
+        ms_e2e, _ = _timed(ola, torch, dist, stream, e2e_step, dm["steps"])
+        e2e = {"value": nbytes * dist.world / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": sum(t[0].numel() * t.element_size() for t in h_in) + h_lens[0].numel() * 4,
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in h_out),
+               "ms_per_step": ms_e2e / dm["steps"], "steps": dm["steps"]}
     return {"value": gbs, "unit": "GB/s", "workload": dec.name, "steps": dm["steps"], "ms_per_step": ms / dm["steps"],
             "bytes": nbytes, "frac_of_hbm": gbs / peaks["hbm"],
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s",
@@ -437,7 +546,7 @@ def bench_decode(args, dist, dev, stream, peaks, ola, torch, W):
                          "avg_launch_ms": dom_ms / dom_n, "bytes_per_launch": nbytes / dm["steps"]},
             "kernels": {n: {"launches": c, "total_ms": t} for n, (c, t) in prof.items()},
             "gpu_launches": sum(n for n, _ in prof.values()),
-            "graph_replay": graph}
+            "graph_replay": graph, "e2e": e2e, "_state": st}
 
 
 def bench_backward(args, dist, dev, stream, peaks, ola, torch, W):
@@ -607,8 +716,13 @@ def run_ours(args, dist):
     clocks = ClockSampler(dist.local)
     clocks.start()
     pre = dec = bwd = ext = prj = None
+    shapes = {}  # the pre-training and fine-tuning forward workloads
     if args.only in ("all", "prefill"):
-        pre = bench_prefill(args, dist, dev, stream, peaks, ola, torch, W)
+        pre = bench_prefill(args, dist, dev, stream, peaks, ola, torch, W, headline_workload(args, W),
+                            e2e=args.only == "all")
+    if args.only == "all":
+        for key, wl in (("pt", W.PT_2K), ("sft", W.SFT_8K)):
+            shapes[key] = bench_prefill(args, dist, dev, stream, peaks, ola, torch, W, wl)
     if args.only in ("all", "decode"):
         dec = bench_decode(args, dist, dev, stream, peaks, ola, torch, W)
     if args.only in ("all", "backward"):
@@ -619,9 +733,27 @@ def run_ours(args, dist):
         prj = bench_project(args, dist, dev, stream, peaks, ola, torch, W)
     clk = clocks.stop()
     cpu = None
-    if pre is not None and dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+    base_on = dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline
+    if pre is not None and base_on:
         v_cpu, cores, desc = oracle_sample(pre["inputs"], pre["wl"], args.cpu_seconds)
         cpu = {"value": v_cpu, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
+    shape_lines = {}
+    for key, r in shapes.items():
+        line_r = {"value": r["value"], "unit": "TFLOP/s", "workload": r["wl"].name, "ms_per_step": r["ms_step"],
+                  "useful_tflop_per_step": r["flops"]["total"] / 1e12, "l2": r["l2"], "roofline": r["roofline"],
+                  "kernels": {n: {"launches": c, "total_ms": t} for n, (c, t) in r["prof"].items()},
+                  "gpu_launches": sum(n for n, _ in r["prof"].values()), "cpu_baseline": None}
+        if base_on:
+            v_cpu, cores, desc = oracle_prefill_sample(r["inputs"], r["wl"], args.cpu_seconds / 3)
+            line_r["cpu_baseline"] = {"value": v_cpu, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                      "sample": desc}
+        shape_lines[key] = line_r
+    if dec is not None:
+        st = dec.pop("_state")
+        dec["cpu_baseline"] = None
+        if base_on:
+            v_cpu, cores, desc = oracle_decode_sample(st, args.cpu_seconds / 3)
+            dec["cpu_baseline"] = {"value": v_cpu, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc}
     if dist.rank != 0:
         return
     if pre is None:  # decode- or backward-only profiling run
@@ -645,6 +777,8 @@ def run_ours(args, dist):
         "kernels": {n: {"launches": c, "total_ms": t} for n, (c, t) in pre["prof"].items()},
         "gpu_launches": sum(n for n, _ in pre["prof"].values()),
         "e2e": pre.get("e2e"),
+        "pt": shape_lines.get("pt"),
+        "sft": shape_lines.get("sft"),
         "decode": dec,
         "backward": bwd,
         "extend": ext,

@@ -13,6 +13,22 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "slow: long-running case")
 
 
+def pytest_sessionfinish(session, exitstatus):
+    """Write the parity margins the GPU tests recorded (largest error per named
+    workload and output, beside its tolerance) when ORTHROS_PARITY_JSON names a file."""
+    path = os.environ.get("ORTHROS_PARITY_JSON")
+    if not path:
+        return
+    from tests.parity_util import MARGINS
+
+    if MARGINS:
+        import json
+
+        with open(path, "w") as f:
+            json.dump(MARGINS, f, indent=1, sort_keys=True)
+            f.write("\n")
+
+
 @pytest.fixture(scope="session")
 def oracle_mod():
     import oracle

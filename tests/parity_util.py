@@ -9,6 +9,17 @@ import torch
 # abs; the fp32 path 1e-3 on both.
 TOL = {torch.bfloat16: (2e-2, 2e-3), torch.float32: (1e-3, 1e-3)}
 
+# Largest errors seen per named workload and output in this test session
+# (written out at the end of the session when ORTHROS_PARITY_JSON is set).
+MARGINS: dict = {}
+
+
+def record_margin(workload: str, errs: dict, tol: dict, what: str = "max abs error vs the oracle"):
+    ent = MARGINS.setdefault(workload, {"measure": what, "errors": {}, "tolerance": {}})
+    for k, v in errs.items():
+        ent["errors"][k] = max(float(v), ent["errors"].get(k, 0.0))
+        ent["tolerance"][k] = float(tol[k])
+
 
 def f32(t: torch.Tensor) -> np.ndarray:
     """Exact widening of bf16 / fp32 CPU tensors for the oracle."""
@@ -84,6 +95,11 @@ def compare_prefill(w, gpu, base_rows=None, out_rows=None, what=""):
     assert errs["o_base"] <= tol_o and errs["o_out"] <= tol_o, f"{what} {errs}"
     assert errs["lse_base"] <= tol_l and errs["lse_out"] <= tol_l, f"{what} {errs}"
     return errs
+
+
+def prefill_tolerances(dtype):
+    tol_o, tol_l = TOL[dtype]
+    return {"o_base": tol_o, "lse_base": tol_l, "o_out": tol_o, "lse_out": tol_l}
 
 
 def sample_positions(T, window, n_random, seed):

@@ -24,7 +24,7 @@ import pytest
 import torch
 
 from efficient_long_context_gb300 import workloads as W
-from tests.parity_util import f32, run_gpu_prefill
+from tests.parity_util import f32, record_margin, run_gpu_prefill
 
 pytestmark = pytest.mark.gpu
 
@@ -166,3 +166,23 @@ def test_backward_named_workload_sampled(work):
     errs.update(compare_backward(one, {"dq": g1["dq"]}, {"dq": head["dq"]}, do_b1, what=f"{work.name} head",
                                  select={"dq": (slice(None), slice(0, 64))}))
     assert errs
+    record_margin(f"{work.name} backward", errs, {n: GRAD_TOL[work.dtype] for n in errs},
+                  "largest |gpu - ref| / (rms(ref) + |ref| + floor) on the last sequence's last 96 and first 64 rows")
+
+
+@pytest.mark.parametrize("work", [W.PT_2K, W.SFT_8K], ids=lambda x: x.name)
+def test_backward_one_full_sequence_every_gradient(work):
+    """One whole sequence of a training workload (its full length, all of its
+    output rows) through the GPU backward, against the oracle's full backward
+    of it: every gradient, the affine gradients summed over all its rows
+    included."""
+    wl = W.make_prefill(work)
+    do_b, do_o = W.make_grad_outputs(wl, seed=work.seed + 7)
+    one, r0, r1 = _one_sequence(wl, wl["B"] - 1)
+    do_b1 = do_b[wl["B"] - 1:].contiguous()
+    do_o1 = do_o[r0:r1].contiguous()
+    gpu = run_gpu_backward(one, do_b1, do_o1)
+    ref = run_oracle_backward(one, do_b1, do_o1)
+    errs = compare_backward(one, gpu, ref, do_b1, what=f"{work.name} one sequence")
+    record_margin(f"{work.name} backward, one full sequence", errs, {n: GRAD_TOL[work.dtype] for n in errs},
+                  "largest |gpu - ref| / (rms(ref) + |ref| + floor), every row of one sequence")

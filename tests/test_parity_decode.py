@@ -10,7 +10,7 @@ import torch
 
 import efficient_long_context_gb300 as ola
 from efficient_long_context_gb300 import workloads as W
-from tests.parity_util import TOL, f32, max_err
+from tests.parity_util import TOL, f32, max_err, record_margin
 
 pytestmark = pytest.mark.gpu
 
@@ -91,13 +91,18 @@ def test_small_decode(case):
 
 
 def test_decode_workload_sampled():
-    """The 32-sequence paged decoding workload at full size, 3 steps, checked
+    """The 32-sequence paged decoding workload at full size over all of its
+    128 steps (every append, including those that open fresh pages), checked
     on a sample of sequences (shortest, longest and two random)."""
-    st = W.make_decode(W.DECODE_32, steps=3)
+    steps = W.DECODE_32.steps
+    st = W.make_decode(W.DECODE_32, steps=steps)
     lens = st.cache_lens.numpy()
     r = np.random.default_rng(1)
     seqs = sorted({int(np.argmin(lens)), int(np.argmax(lens)), *map(int, r.choice(len(lens), 2, replace=False))})
-    run_and_compare(st, 3, seqs=seqs, what="decode workload")
+    worst = run_and_compare(st, steps, seqs=seqs, what="decode workload")
+    tol_o, tol_l = TOL[torch.bfloat16]
+    record_margin(W.DECODE_32.name, worst, {"o_base": tol_o, "lse_base": tol_l, "o_out": tol_o, "lse_out": tol_l},
+                  f"max abs error vs the oracle over {steps} steps of {len(seqs)} sampled sequences")
 
 
 def test_decode_steps_replayed_from_a_cuda_graph():

@@ -9,7 +9,7 @@ import pytest
 import torch
 
 from efficient_long_context_gb300 import workloads as W
-from tests.parity_util import compare_prefill, run_gpu_prefill, sample_positions
+from tests.parity_util import compare_prefill, prefill_tolerances, record_margin, run_gpu_prefill, sample_positions
 
 pytestmark = pytest.mark.gpu
 
@@ -46,7 +46,8 @@ def test_key_offsets_small():
 
 def test_tiny_fp32_full():
     wl = W.make_prefill(W.TINY_FP32)
-    compare_prefill(wl, run_gpu_prefill(wl), what=W.TINY_FP32.name)
+    errs = compare_prefill(wl, run_gpu_prefill(wl), what=W.TINY_FP32.name)
+    record_margin(W.TINY_FP32.name, errs, prefill_tolerances(torch.float32), "max abs error vs the oracle, every row")
 
 
 @pytest.mark.parametrize("work", [W.PT_2K, W.SFT_8K, W.PREFILL_128K], ids=lambda x: x.name)
@@ -57,4 +58,7 @@ def test_named_workload_sampled(work):
     n_out = int(wl["out_indptr"][-1])
     r = np.random.default_rng(work.seed)
     out_rows = np.unique(np.concatenate([[0, n_out - 1], r.choice(n_out, size=min(24, n_out), replace=False)]))
-    compare_prefill(wl, gpu, base_rows=rows, out_rows=out_rows, what=work.name)
+    errs = compare_prefill(wl, gpu, base_rows=rows, out_rows=out_rows, what=work.name)
+    record_margin(work.name, errs, prefill_tolerances(work.dtype),
+                  f"max abs error vs the oracle on {len(rows)} sampled positions x {work.B} sequences and "
+                  f"{len(out_rows)} sampled output rows")
