@@ -123,6 +123,7 @@ struct TcParams {
     float *o_out_f32;  // when set, output rows are written here as float instead of o_out
     float *lse_out;
     uint32_t *status;
+    int *unit_counter;  // zero before the launch: the next work unit to take (persistent CTAs)
 };
 // Work units of one (sequence, kv head) for nblk row blocks and group size g.
 int tc_units_per_kv(int nblk, int g);

@@ -252,7 +252,8 @@ orthros_status prefill_core(const void *q, const void *k, const void *v, const f
 
     char *ws = static_cast<char *>(workspace);
     uint32_t *status = reinterpret_cast<uint32_t *>(ws);
-    cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), stream);
+    // the status word and, next to it, the tile kernel's work-unit counter
+    cudaError_t e = cudaMemsetAsync(status, 0, 2 * sizeof(uint32_t), stream);
     if (e != cudaSuccess) return cuda_fail(e, "status reset");
     if (rows == 0) return ORTHROS_OK;
 
@@ -419,6 +420,7 @@ orthros_status prefill_core(const void *q, const void *k, const void *v, const f
     tp.o_out_f32 = shard ? o_out_f32 : nullptr;
     tp.lse_out = lse_out;
     tp.status = status;
+    tp.unit_counter = reinterpret_cast<int *>(ws + sizeof(uint32_t));
     {
         ProfScope ps("prefill_tc", stream);
         e = launch_prefill_tc(tp, k16, v, d, stream);

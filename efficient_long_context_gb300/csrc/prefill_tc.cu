@@ -67,22 +67,44 @@ template <int D> struct Cfg {
     static constexpr int kTmemO = 256;                                  // first O column
 };
 
-struct Meta {
-    uint64_t k_full[kNumK], k_empty[kNumK], v_full[kNumV], v_empty[kNumV];
-    uint64_t s_full[2], p_full[2], o_full[2], mma_done;
-    uint64_t q_full[2];  // per slot: raw query tile landed (TMA; rows contiguous in q or q_out)
-    uint64_t os_bar[2];  // per slot: normalised output tile staged for the TMA store
-    uint64_t xm_bar[2], lx_bar[2];  // per slot: row maxima / row sums exchanged between column halves
-    uint32_t tmem_base;
-    int abort;
-    int t_min[2], t_max[2];
-    __nv_bfloat16 xmax[2][2][kRowsPerTile];  // [slot][half][row] tile maxima (a shared shift; rounding is harmless)
-};
-
 struct Slot {
     int kind;  // 0 base positions, 1 output rows, -1 empty
     int b, h, row0, n;
 };
+
+// Band of a slot in key-tile units: [kt_lo, kt_hi]; lo_max = latest window
+// start of its rows (key tiles before it need the window mask); t_min / t_max
+// = first / last position of its usable rows.
+struct Band {
+    int kt_lo, kt_hi, lo_max, t_min, t_max;
+};
+
+// What every role needs to know about one work unit (written by the
+// producer, read by the MMA issuer and the softmax warps).
+struct UnitDesc {
+    Slot sl[2];
+    Band bd[2];
+    int kt_min, n_it;  // key tiles kt_min .. kt_min + n_it - 1: the union of the two bands
+    int end;           // no more units: every role leaves its loop
+};
+
+constexpr int kDescRing = 2;  // unit descriptors in flight
+
+struct Meta {
+    uint64_t k_full[kNumK], k_empty[kNumK], v_full[kNumV], v_empty[kNumV];
+    uint64_t s_full[2], p_full[2], o_full[2], mma_done;
+    uint64_t q_full[2];   // per slot: raw query tile landed (TMA) or nothing to land (gathered / empty)
+    uint64_t q_ready[2];  // per slot: affined query tile staged for the products
+    uint64_t q_free[2];   // per slot: the unit is done with its query tile (epilogue stored)
+    uint64_t os_bar[2];   // per slot: normalised output tile staged for the TMA store
+    uint64_t xm_bar[2], lx_bar[2];  // per slot: row maxima / row sums exchanged between column halves
+    uint64_t u_full[kDescRing], u_empty[kDescRing];  // unit descriptor ring
+    uint32_t tmem_base;
+    int abort;
+    UnitDesc desc[kDescRing];
+    __nv_bfloat16 xmax[2][2][kRowsPerTile];  // [slot][half][row] tile maxima (a shared shift; rounding is harmless)
+};
+static_assert(sizeof(Meta) <= 1536, "barriers and metadata must fit their shared-memory region");
 
 // Work-unit decoding. Units [0, n_cross) are output-row units (heavier, so
 // they start first), then base units. Inside one (sequence, kv head) the order
@@ -158,6 +180,80 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int c) {
     return sub * (kRowsPerTile * 128) + row * 128 + ((cc ^ (row & 7)) << 4);
 }
 
+// Position (in key coordinates) of output row r and whether the row is usable:
+// its position lies in [0, T) (a shard's rows past its keys read them all), and
+// without q_out the base query at that position exists.
+__device__ __forceinline__ bool out_row_position(const TcParams &p, int r, int &te) {
+    const int t = p.out_positions[r];
+    te = p.shard ? min(t, p.T - 1) : t;
+    bool ok = t >= 0 && (p.shard || t < p.T);
+    if (!p.q_out && (te < p.q_off || te - p.q_off >= p.Tq)) ok = false;
+    return ok;
+}
+
+__device__ __forceinline__ Band band_of(const TcParams &p, const Slot &S, int tmin, int tmax) {
+    Band bd;
+    bd.t_min = tmin;
+    bd.t_max = tmax;
+    if (S.kind < 0 || tmax < 0) {
+        bd.kt_lo = 1;
+        bd.kt_hi = 0;
+        bd.lo_max = 0;
+        return bd;
+    }
+    const int lo_min = S.kind == 0 ? max(0, tmin - p.window + 1) : p.key_lo;
+    bd.lo_max = S.kind == 0 ? max(0, tmax - p.window + 1) : p.key_lo;
+    bd.kt_lo = lo_min / kKeysPerTile;
+    bd.kt_hi = tmax / kKeysPerTile;
+    return bd;
+}
+
+// Descriptor of unit u (u < 0: the end marker). Called by all 32 lanes of the
+// producer warp, which read an output-row slot's positions together; every
+// lane returns the same descriptor.
+__device__ void make_desc(const TcParams &p, int u, int lane, UnitDesc &D) {
+    D.end = u < 0;
+    D.kt_min = 0;
+    D.n_it = 0;
+    if (D.end) {
+        for (int s = 0; s < 2; ++s) {
+            D.sl[s] = Slot{-1, 0, 0, 0, 0};
+            D.bd[s] = Band{1, 0, 0, 0, -1};
+        }
+        return;
+    }
+    decode_unit(p, u, D.sl[0], D.sl[1]);
+    for (int s = 0; s < 2; ++s) {
+        const Slot S = D.sl[s];
+        int tmin = 0x7fffffff, tmax = -1;
+        if (S.kind == 0) {
+            tmin = S.row0 + p.q_off;
+            tmax = S.row0 + S.n - 1 + p.q_off;
+        } else if (S.kind == 1) {
+            for (int r = lane; r < S.n; r += 32) {
+                int te;
+                if (out_row_position(p, S.row0 + r, te)) {
+                    tmin = min(tmin, te);
+                    tmax = max(tmax, te);
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                tmin = min(tmin, __shfl_xor_sync(0xffffffffu, tmin, o));
+                tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+            }
+        }
+        D.bd[s] = band_of(p, S, tmin, tmax);
+    }
+    const Band &b0 = D.bd[0], &b1 = D.bd[1];
+    const bool any0 = b0.kt_lo <= b0.kt_hi, any1 = b1.kt_lo <= b1.kt_hi;
+    if (any0 || any1) {
+        D.kt_min = any0 && any1 ? min(b0.kt_lo, b1.kt_lo) : (any0 ? b0.kt_lo : b1.kt_lo);
+        const int kt_max = any0 && any1 ? max(b0.kt_hi, b1.kt_hi) : (any0 ? b0.kt_hi : b1.kt_hi);
+        D.n_it = kt_max - D.kt_min + 1;
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -171,9 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = tid >> 5;
     const int lane = tid & 31;
     volatile int *abort = &mt.abort;
-
-    Slot sl0, sl1;
-    decode_unit(p, blockIdx.x, sl0, sl1);
+    const int total_units = p.n_cross_units + p.n_base_units;
 
     if (tid == 0) {
         for (int i = 0; i < kNumK; ++i) {
@@ -191,9 +285,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&mt.xm_bar[s], 2 * kRowsPerTile);
             mbar_init(&mt.lx_bar[s], 2 * kRowsPerTile);
             mbar_init(&mt.q_full[s], 1);
+            mbar_init(&mt.q_ready[s], 2 * kRowsPerTile);
+            mbar_init(&mt.q_free[s], 2 * kRowsPerTile);
             mbar_init(&mt.os_bar[s], 2 * kRowsPerTile);
-            mt.t_min[s] = 0x7fffffff;
-            mt.t_max[s] = -1;
+        }
+        for (int r = 0; r < kDescRing; ++r) {
+            mbar_init(&mt.u_full[r], 1);
+            mbar_init(&mt.u_empty[r], kSoftmaxWarps + 1);
         }
         mbar_init(&mt.mma_done, 1);
         mt.abort = 0;
@@ -202,205 +300,111 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kProducerWarp && lane == 0) {
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_qo);
+        prefetch_tmap(&tm_ob);
     }
     __syncthreads();
     if (warp == kMmaWarp) {
         tmem_alloc(&mt.tmem_base, 512);
         tmem_relinquish();
     }
-
-    // Query tiles whose rows are contiguous (base positions; output rows with
-    // their own q_out) arrive by TMA as raw bf16 and are turned into affined
-    // fp16 in place below; output rows that read q at their positions are
-    // gathered by the softmax threads.
-    auto q_by_tma = [&](const Slot &S) { return S.kind == 0 || (S.kind == 1 && p.q_out != nullptr); };
-    if (warp == kProducerWarp && lane == 0) {
-        for (int s = 0; s < 2; ++s) {
-            const Slot S = s ? sl1 : sl0;
-            if (S.kind < 0 || !q_by_tma(S)) continue;
-            mbar_arrive_expect_tx(&mt.q_full[s], C::kTileBytes);
-            const int row = S.kind == 0 ? S.b * p.Tq + S.row0 : S.row0;
-            for (int j = 0; j < C::kSub; ++j)
-                tma_load_3d(smem + C::kQ0 + s * C::kTileBytes + j * (kRowsPerTile * 128), S.kind == 0 ? &tm_q : &tm_qo,
-                            &mt.q_full[s], 64 * j, S.h, row);
-        }
-    }
-
-    // Base-position tiles know their band without reading any data, so the
-    // producer starts the first key/value loads now and they overlap the query
-    // staging below (tiles with output rows wait for their positions).
-    int pre_k = 0, pre_v = 0;
-    const bool closed_form = sl0.kind == 0 && sl1.kind != 1;
-    if (warp == kProducerWarp && lane == 0 && closed_form) {
-        const int t0 = sl0.row0 + p.q_off;
-        const int lo0 = max(0, t0 - p.window + 1) / kKeysPerTile;
-        const int hi0 = (t0 + sl0.n - 1) / kKeysPerTile;
-        int lo = lo0, hi = hi0;
-        if (sl1.kind == 0) {
-            const int t1 = sl1.row0 + p.q_off;
-            lo = min(lo, max(0, t1 - p.window + 1) / kKeysPerTile);
-            hi = max(hi, (t1 + sl1.n - 1) / kKeysPerTile);
-        }
-        const int n_cf = hi - lo + 1;
-        const int kvh = sl0.h / (p.Hq / p.Hkv);
-        pre_k = min(n_cf, kNumK);
-        pre_v = min(n_cf, kNumV);
-        for (int i = 0; i < pre_k; ++i) {
-            mbar_arrive_expect_tx(&mt.k_full[i], C::kTileBytes);
-            for (int j = 0; j < C::kSub; ++j)
-                tma_load_4d(smem + C::kK0 + i * C::kTileBytes + j * (kKeysPerTile * 128), &tm_k, &mt.k_full[i], 64 * j,
-                            kvh, (lo + i) * kKeysPerTile, sl0.b);
-        }
-        for (int i = 0; i < pre_v; ++i) {
-            mbar_arrive_expect_tx(&mt.v_full[i], C::kTileBytes);
-            for (int j = 0; j < C::kSub; ++j)
-                tma_load_4d(smem + C::kV0 + i * C::kTileBytes + j * (kKeysPerTile * 128), &tm_v, &mt.v_full[i], 64 * j,
-                            kvh, (lo + i) * kKeysPerTile, sl0.b);
-        }
-    }
-
-    // ---------------- prologue: stage both query tiles (affine fused) ----------------
-    // Softmax warp w: slot (w >> 2) & 1, column half w >> 3, rows 32 (w & 3) .. +31;
-    // each half stages its own D/2 channels of the row.
-    const bool softmax_thread = warp < kSoftmaxWarps;
-    const int s_me = (warp >> 2) & 1;
-    const int h_me = warp >> 3;
-    const int row = ((warp & 3) << 5) | lane;
-    int my_t = 0;  // the row's position in key coordinates
-    bool my_valid = false, my_bad = false;
-    if (softmax_thread) {
-        const Slot S = s_me ? sl1 : sl0;
-        if (S.kind >= 0 && row < S.n) {
-            if (S.kind == 0) {
-                my_t = S.row0 + row + p.q_off;
-                my_valid = true;
-            } else {
-                const int t = p.out_positions[S.row0 + row];
-                // a shard's output rows may sit past its keys (they read them all)
-                my_t = p.shard ? min(t, p.T - 1) : t;
-                my_valid = t >= 0 && (p.shard || t < p.T);
-                // without q_out the row's query is the base query at its position
-                if (!p.q_out && (my_t < p.q_off || my_t - p.q_off >= p.Tq)) my_valid = false;
-            }
-            my_bad = !my_valid;
-            if (my_bad && h_me == 0) set_status(p.status, ORTHROS_DEV_BAD_POSITION);
-        }
-        uint8_t *qs = smem + C::kQ0 + s_me * C::kTileBytes;
-        constexpr int kHalfChunks = D / 16;  // 16-byte chunks per half row
-        const bool tma = S.kind >= 0 && q_by_tma(S);
-        if (tma && !mbar_wait_warp(&mt.q_full[s_me], 0, abort, p.status)) my_valid = false;
-        if (my_valid) {
-            const float *al = (S.kind == 0 ? p.alpha_base : p.alpha_out) + S.h * D;
-            const float *be = (S.kind == 0 ? p.beta_base : p.beta_out) + S.h * D;
-            bool over = false;
-            uint4 raws[kHalfChunks];  // every load of the half row in flight at once
-            if (tma) {
-#pragma unroll
-                for (int cc = 0; cc < kHalfChunks; ++cc)
-                    raws[cc] = *reinterpret_cast<const uint4 *>(qs + sw128_offset<D>(row, h_me * kHalfChunks + cc));
-            } else {
-                const __nv_bfloat16 *src = p.q + (((long long)S.b * p.Tq + (my_t - p.q_off)) * p.Hq + S.h) * D;
-#pragma unroll
-                for (int cc = 0; cc < kHalfChunks; ++cc)
-                    raws[cc] = reinterpret_cast<const uint4 *>(src)[h_me * kHalfChunks + cc];
-            }
-#pragma unroll
-            for (int cc = 0; cc < kHalfChunks; ++cc) {
-                const int c = h_me * kHalfChunks + cc;
-                const uint4 raw = raws[cc];
-                const float4 a0 = reinterpret_cast<const float4 *>(al)[2 * c];
-                const float4 a1 = reinterpret_cast<const float4 *>(al)[2 * c + 1];
-                const float4 b0 = reinterpret_cast<const float4 *>(be)[2 * c];
-                const float4 b1 = reinterpret_cast<const float4 *>(be)[2 * c + 1];
-                const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
-                float2 x0 = __bfloat1622float2(h2[0]), x1 = __bfloat1622float2(h2[1]);
-                float2 x2 = __bfloat1622float2(h2[2]), x3 = __bfloat1622float2(h2[3]);
-                float v[8] = {fmaf(a0.x, x0.x, b0.x), fmaf(a0.y, x0.y, b0.y), fmaf(a0.z, x1.x, b0.z),
-                              fmaf(a0.w, x1.y, b0.w), fmaf(a1.x, x2.x, b1.x), fmaf(a1.y, x2.y, b1.y),
-                              fmaf(a1.z, x3.x, b1.z), fmaf(a1.w, x3.y, b1.w)};
-#pragma unroll
-                for (int e = 0; e < 8; ++e) over |= fabsf(v[e]) > 65504.f;
-                uint4 o;
-                o.x = pack_f16(v[0], v[1]);
-                o.y = pack_f16(v[2], v[3]);
-                o.z = pack_f16(v[4], v[5]);
-                o.w = pack_f16(v[6], v[7]);
-                *reinterpret_cast<uint4 *>(qs + sw128_offset<D>(row, c)) = o;
-            }
-            if (over) set_status(p.status, ORTHROS_DEV_FP16_RANGE);
-            if (h_me == 0) {
-                atomicMin(&mt.t_min[s_me], my_t);
-                atomicMax(&mt.t_max[s_me], my_t);
-            }
-        } else {
-#pragma unroll 4
-            for (int cc = 0; cc < kHalfChunks; ++cc)
-                *reinterpret_cast<uint4 *>(qs + sw128_offset<D>(row, h_me * kHalfChunks + cc)) = make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-
-    // ---------------- band of each tile, in key-tile units ----------------
-    // Band of each tile in key-tile units: [kt_lo, kt_hi]; lo_max = latest
-    // window start of its rows (key tiles before it need the window mask).
-    struct Band {
-        int kt_lo, kt_hi, lo_max, t_min, t_max;
-    };
-    auto band_of = [&](const Slot &S, int tmin, int tmax) {
-        Band bd;
-        bd.t_min = tmin;
-        bd.t_max = tmax;
-        if (S.kind < 0 || tmax < 0) {
-            bd.kt_lo = 1;
-            bd.kt_hi = 0;
-            bd.lo_max = 0;
-            return bd;
-        }
-        const int lo_min = S.kind == 0 ? max(0, tmin - p.window + 1) : p.key_lo;
-        bd.lo_max = S.kind == 0 ? max(0, tmax - p.window + 1) : p.key_lo;
-        bd.kt_lo = lo_min / kKeysPerTile;
-        bd.kt_hi = tmax / kKeysPerTile;
-        return bd;
-    };
-    const Band bd0 = band_of(sl0, mt.t_min[0], mt.t_max[0]);
-    const Band bd1 = band_of(sl1, mt.t_min[1], mt.t_max[1]);
-    const bool any0 = bd0.kt_lo <= bd0.kt_hi, any1 = bd1.kt_lo <= bd1.kt_hi;
-    const int kt_min = any0 && any1 ? min(bd0.kt_lo, bd1.kt_lo) : (any0 ? bd0.kt_lo : bd1.kt_lo);
-    const int kt_max = any0 && any1 ? max(bd0.kt_hi, bd1.kt_hi) : (any0 ? bd0.kt_hi : bd1.kt_hi);
-    const int n_it = (any0 || any1) ? kt_max - kt_min + 1 : 0;
     const uint32_t tmem = mt.tmem_base;
-    const int kv = sl0.h / (p.Hq / p.Hkv);
-    const int bseq = sl0.b;
+
+    // Query tiles whose rows are contiguous (base positions; output rows with
+    // their own q_out) arrive by TMA as raw bf16 and are turned into affined
+    // fp16 in place; output rows that read q at their positions are gathered
+    // by the softmax threads.
+    auto q_by_tma = [&](const Slot &S) { return S.kind == 0 || (S.kind == 1 && p.q_out != nullptr); };
 
     if (warp == kProducerWarp) {
-        // ---------------- TMA producer ----------------
-        if (lane == 0) {
-            for (int i = 0; i < n_it && !*abort; ++i) {
-                const int kt = kt_min + i;
-                const int sk = i % kNumK;
-                if (i >= pre_k) {
-                    if (i >= kNumK && !mbar_wait(&mt.k_empty[sk], ((i / kNumK) - 1) & 1, abort, p.status)) break;
+        // ---------------- producer: unit descriptors, then TMA loads ----------------
+        // Takes units from a device-wide counter (heaviest first: the numbering
+        // puts output-row units and late row blocks first), publishes each
+        // unit's descriptor, and streams its K/V tiles through the rings with
+        // phases that run on across units. The first K/V tiles of a unit go
+        // out before its query tiles, which wait for the previous unit's
+        // epilogue to release the query buffers.
+        uint32_t gk = 0;            // K/V iterations issued (all units so far)
+        uint32_t nq[2] = {0, 0};    // per slot: units whose query phase was armed
+        bool alive = true;
+        for (int i = 0; alive; ++i) {
+            int u = 0;
+            if (lane == 0) u = atomicAdd(p.unit_counter, 1);
+            u = __shfl_sync(0xffffffffu, u, 0);
+            UnitDesc dsc;
+            make_desc(p, u < total_units ? u : -1, lane, dsc);
+            const int r = i % kDescRing;
+            if (i >= kDescRing && !mbar_wait_warp(&mt.u_empty[r], ((i / kDescRing) - 1) & 1, abort, p.status)) break;
+            if (lane == 0) {
+                mt.desc[r] = dsc;
+                mbar_arrive(&mt.u_full[r]);  // releases the descriptor to the other roles
+            }
+            __syncwarp();
+            if (dsc.end) break;
+            if (lane == 0) {
+                const int kvh = dsc.sl[0].h / (p.Hq / p.Hkv);
+                const int bseq = dsc.sl[0].b;
+                auto issue_kv = [&](int it) -> bool {
+                    const uint32_t g = gk + it;
+                    const int kt = dsc.kt_min + it;
+                    const int sk = g % kNumK, sv = g % kNumV;
+                    if (g >= (uint32_t)kNumK && !mbar_wait(&mt.k_empty[sk], ((g / kNumK) - 1) & 1, abort, p.status))
+                        return false;
                     mbar_arrive_expect_tx(&mt.k_full[sk], C::kTileBytes);
                     for (int j = 0; j < C::kSub; ++j)
                         tma_load_4d(smem + C::kK0 + sk * C::kTileBytes + j * (kKeysPerTile * 128), &tm_k,
-                                    &mt.k_full[sk], 64 * j, kv, kt * kKeysPerTile, bseq);
-                }
-                const int sv = i % kNumV;
-                if (i >= pre_v) {
-                    if (i >= kNumV && !mbar_wait(&mt.v_empty[sv], ((i / kNumV) - 1) & 1, abort, p.status)) break;
+                                    &mt.k_full[sk], 64 * j, kvh, kt * kKeysPerTile, bseq);
+                    if (g >= (uint32_t)kNumV && !mbar_wait(&mt.v_empty[sv], ((g / kNumV) - 1) & 1, abort, p.status))
+                        return false;
                     mbar_arrive_expect_tx(&mt.v_full[sv], C::kTileBytes);
                     for (int j = 0; j < C::kSub; ++j)
                         tma_load_4d(smem + C::kV0 + sv * C::kTileBytes + j * (kKeysPerTile * 128), &tm_v,
-                                    &mt.v_full[sv], 64 * j, kv, kt * kKeysPerTile, bseq);
-                }
+                                    &mt.v_full[sv], 64 * j, kvh, kt * kKeysPerTile, bseq);
+                    return true;
+                };
+                auto issue_q = [&](int s) -> bool {
+                    if (i >= 1 && !mbar_wait(&mt.q_free[s], (i - 1) & 1, abort, p.status)) return false;
+                    const Slot &S = dsc.sl[s];
+                    nq[s] = i + 1;
+                    if (S.kind >= 0 && q_by_tma(S)) {
+                        mbar_arrive_expect_tx(&mt.q_full[s], C::kTileBytes);
+                        const int row = S.kind == 0 ? S.b * p.Tq + S.row0 : S.row0;
+                        for (int j = 0; j < C::kSub; ++j)
+                            tma_load_3d(smem + C::kQ0 + s * C::kTileBytes + j * (kRowsPerTile * 128),
+                                        S.kind == 0 ? &tm_q : &tm_qo, &mt.q_full[s], 64 * j, S.h, row);
+                    } else {
+                        mbar_arrive(&mt.q_full[s]);  // nothing to copy (gathered rows or an empty slot)
+                    }
+                    return true;
+                };
+                const int pre = min(dsc.n_it, 2);
+                bool ok = true;
+                for (int it = 0; ok && it < pre; ++it) ok = issue_kv(it);
+                ok = ok && issue_q(0);
+                ok = ok && issue_q(1);
+                for (int it = pre; ok && it < dsc.n_it; ++it) ok = issue_kv(it);
+                gk += dsc.n_it;
+                alive = ok;
             }
+            alive = __shfl_sync(0xffffffffu, alive, 0);
+        }
+        if (lane == 0) {
+            // nothing may be in flight when the CTA leaves: wait (bounded) for the
+            // copies of the last stages and query tiles issued
+            for (uint32_t g = gk > (uint32_t)kNumK ? gk - kNumK : 0; g < gk; ++g)
+                mbar_wait_drain(&mt.k_full[g % kNumK], (g / kNumK) & 1, p.status);
+            for (uint32_t g = gk > (uint32_t)kNumV ? gk - kNumV : 0; g < gk; ++g)
+                mbar_wait_drain(&mt.v_full[g % kNumV], (g / kNumV) & 1, p.status);
+            for (int s = 0; s < 2; ++s)
+                if (nq[s] > 0) mbar_wait_drain(&mt.q_full[s], (nq[s] - 1) & 1, p.status);
         }
     } else if (warp == kMmaWarp) {
         // ---------------- tcgen05.mma issuer ----------------
-        if (lane == 0 && n_it > 0) {
+        if (lane == 0) {
             constexpr uint32_t kIdescS = idesc_f16(0, 0, 0, 0, kRowsPerTile, kKeysPerTile);  // fp16, K-major
             constexpr uint32_t kIdescO = idesc_f16(1, 1, 0, 1, kRowsPerTile, D);             // bf16, V MN-major
             // Descriptors are built once; the start-address field is the low 14 bits
@@ -412,7 +416,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dv = desc_sw128(smem_u32(smem + C::kV0), kKeysPerTile * 128, 1024);
             const uint32_t d_s0 = tmem, d_s1 = tmem + 128;
             const uint32_t d_o0 = tmem + C::kTmemO, d_o1 = tmem + C::kTmemO + 128;
-            const int lo0 = bd0.kt_lo, hi0 = bd0.kt_hi, lo1 = bd1.kt_lo, hi1 = bd1.kt_hi;
             // S = Q K^T: 16 channels per instruction; inside a 128B atom the start
             // address advances 32 bytes per step.
 #define ORTHROS_ISSUE_S(D_TMEM, QDESC, KDESC)                                           \
@@ -426,244 +429,368 @@ __global__ void __launch_bounds__(kThreads, 1)
     _Pragma("unroll") for (int kk = 0; kk < kKeysPerTile / 16; ++kk)                            \
         mma_ts((D_TMEM), (P_TMEM) + kk * 8, (VDESC) + (uint64_t)((kk * 16 * 128) >> 4), kIdescO, \
                kk > 0 ? 1u : (ACC0));
-            uint32_t pc0 = 0, pc1 = 0, o_init0 = 0, o_init1 = 0;
-            bool ok = mbar_wait(&mt.k_full[0], 0, abort, p.status);
-            if (ok) {
+            uint32_t g = 0;              // K/V iterations consumed (all units so far)
+            uint32_t pc0 = 0, pc1 = 0;   // P tiles consumed per slot
+            bool ok = true;
+            for (int i = 0; ok; ++i) {
+                const int r = i % kDescRing;
+                if (!(ok = mbar_wait(&mt.u_full[r], (i / kDescRing) & 1, abort, p.status))) break;
+                const UnitDesc &dr = mt.desc[r];
+                const int end = dr.end;
+                const int lo0 = dr.bd[0].kt_lo, hi0 = dr.bd[0].kt_hi, lo1 = dr.bd[1].kt_lo, hi1 = dr.bd[1].kt_hi;
+                const int kt_min = dr.kt_min, n_it = dr.n_it;
+                mbar_arrive(&mt.u_empty[r]);
+                if (end) break;
+                // both query tiles of this unit staged (this also orders the unit's
+                // first products after the previous unit's epilogue)
+                if (!(ok = mbar_wait(&mt.q_ready[0], i & 1, abort, p.status))) break;
+                if (!(ok = mbar_wait(&mt.q_ready[1], i & 1, abort, p.status))) break;
+                if (n_it == 0) continue;
+                if (!(ok = mbar_wait(&mt.k_full[g % kNumK], (g / kNumK) & 1, abort, p.status))) break;
                 tc_fence_after();
+                const uint64_t dk0 = dk + (uint64_t)((g % kNumK) * kTileU);
                 if (kt_min >= lo0 && kt_min <= hi0) {
-                    ORTHROS_ISSUE_S(d_s0, dq, dk)
+                    ORTHROS_ISSUE_S(d_s0, dq, dk0)
                     tc_commit(&mt.s_full[0]);
                 }
                 if (kt_min >= lo1 && kt_min <= hi1) {
-                    ORTHROS_ISSUE_S(d_s1, dq + kTileU, dk)
+                    ORTHROS_ISSUE_S(d_s1, dq + kTileU, dk0)
                     tc_commit(&mt.s_full[1]);
                 }
-                tc_commit(&mt.k_empty[0]);
-            }
-            // per tile and slot: PV_s(i), then S_s(i+1) into the TMEM that held P_s(i)
-            // (tcgen05.mma from one thread execute in issue order)
-            for (int i = 0; ok && i < n_it; ++i) {
-                const int kt = kt_min + i;
-                const int sv = i % kNumV;
-                const uint64_t vdesc = dv + (uint64_t)(sv * kTileU);
-                const bool more = i + 1 < n_it;
-                const int skn = (i + 1) % kNumK;
-                const uint64_t kdesc = dk + (uint64_t)(skn * kTileU);
-                if (!(ok = mbar_wait(&mt.v_full[sv], (i / kNumV) & 1, abort, p.status))) break;
-                // slot 0
-                if (kt >= lo0 && kt <= hi0) {
-                    if (!(ok = mbar_wait(&mt.p_full[0], pc0 & 1, abort, p.status))) break;
-                    ++pc0;
-                    tc_fence_after();
-                    ORTHROS_ISSUE_PV(d_o0, d_s0, vdesc, o_init0)
-                    o_init0 = 1;
-                }
-                if (more) {
-                    if (!(ok = mbar_wait(&mt.k_full[skn], ((i + 1) / kNumK) & 1, abort, p.status))) break;
-                    tc_fence_after();
-                    if (kt + 1 >= lo0 && kt + 1 <= hi0) {
-                        ORTHROS_ISSUE_S(d_s0, dq, kdesc)
-                        tc_commit(&mt.s_full[0]);
+                tc_commit(&mt.k_empty[g % kNumK]);
+                // per tile and slot: PV_s(i), then S_s(i+1) into the TMEM that held P_s(i)
+                // (tcgen05.mma from one thread execute in issue order)
+                uint32_t o_init0 = 0, o_init1 = 0;
+                for (int it = 0; ok && it < n_it; ++it) {
+                    const uint32_t gi = g + it;
+                    const int kt = kt_min + it;
+                    const int sv = gi % kNumV;
+                    const uint64_t vdesc = dv + (uint64_t)(sv * kTileU);
+                    const bool more = it + 1 < n_it;
+                    const int skn = (gi + 1) % kNumK;
+                    const uint64_t kdesc = dk + (uint64_t)(skn * kTileU);
+                    if (!(ok = mbar_wait(&mt.v_full[sv], (gi / kNumV) & 1, abort, p.status))) break;
+                    // slot 0
+                    if (kt >= lo0 && kt <= hi0) {
+                        if (!(ok = mbar_wait(&mt.p_full[0], pc0 & 1, abort, p.status))) break;
+                        ++pc0;
+                        tc_fence_after();
+                        ORTHROS_ISSUE_PV(d_o0, d_s0, vdesc, o_init0)
+                        o_init0 = 1;
                     }
-                }
-                // slot 1
-                if (kt >= lo1 && kt <= hi1) {
-                    if (!(ok = mbar_wait(&mt.p_full[1], pc1 & 1, abort, p.status))) break;
-                    ++pc1;
-                    tc_fence_after();
-                    ORTHROS_ISSUE_PV(d_o1, d_s1, vdesc, o_init1)
-                    o_init1 = 1;
-                }
-                if (more) {
-                    if (kt + 1 >= lo1 && kt + 1 <= hi1) {
-                        ORTHROS_ISSUE_S(d_s1, dq + kTileU, kdesc)
-                        tc_commit(&mt.s_full[1]);
+                    if (more) {
+                        if (!(ok = mbar_wait(&mt.k_full[skn], ((gi + 1) / kNumK) & 1, abort, p.status))) break;
+                        tc_fence_after();
+                        if (kt + 1 >= lo0 && kt + 1 <= hi0) {
+                            ORTHROS_ISSUE_S(d_s0, dq, kdesc)
+                            tc_commit(&mt.s_full[0]);
+                        }
                     }
-                    tc_commit(&mt.k_empty[skn]);
+                    // slot 1
+                    if (kt >= lo1 && kt <= hi1) {
+                        if (!(ok = mbar_wait(&mt.p_full[1], pc1 & 1, abort, p.status))) break;
+                        ++pc1;
+                        tc_fence_after();
+                        ORTHROS_ISSUE_PV(d_o1, d_s1, vdesc, o_init1)
+                        o_init1 = 1;
+                    }
+                    if (more) {
+                        if (kt + 1 >= lo1 && kt + 1 <= hi1) {
+                            ORTHROS_ISSUE_S(d_s1, dq + kTileU, kdesc)
+                            tc_commit(&mt.s_full[1]);
+                        }
+                        tc_commit(&mt.k_empty[skn]);
+                    }
+                    tc_commit(&mt.v_empty[sv]);
                 }
-                tc_commit(&mt.v_empty[sv]);
+                if (!ok) break;
+                if (lo0 <= hi0) tc_commit(&mt.o_full[0]);
+                if (lo1 <= hi1) tc_commit(&mt.o_full[1]);
+                g += n_it;
             }
 #undef ORTHROS_ISSUE_S
 #undef ORTHROS_ISSUE_PV
-            tc_commit(&mt.o_full[0]);
-            tc_commit(&mt.o_full[1]);
+            // every product issued must be complete before tensor memory is freed
             tc_commit(&mt.mma_done);
-            mbar_wait(&mt.mma_done, 0, abort, p.status);
+            mbar_wait_drain(&mt.mma_done, 0, p.status);
         }
     } else {
         // ---------------- softmax: two threads per row (one per 64-key half) ----------------
-        const int s = s_me, hh = h_me;
-        const Slot S = s ? sl1 : sl0;
-        const Band bd = s ? bd1 : bd0;
+        // Softmax warp w: slot (w >> 2) & 1, column half w >> 3, rows 32 (w & 3) .. +31;
+        // each half stages its own D/2 channels of the row.
+        const int s = (warp >> 2) & 1;
+        const int hh = warp >> 3;
+        const int row = ((warp & 3) << 5) | lane;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t t_s = tmem + lane_off + s * 128;                // S_s columns of this lane quarter
+        const uint32_t t_s = tmem + lane_off + s * 128;                     // S_s columns of this lane quarter
         const uint32_t t_o = tmem + lane_off + C::kTmemO + s * 128 + hh * (D / 2);  // this half of O_s
-        const int t_row = my_valid ? my_t : bd.t_max;
-        const int lo_row = S.kind == 0 ? max(0, t_row - p.window + 1) : p.key_lo;
         const float c2 = p.scale_log2;
-        const int t_min_s = bd.t_min;
-        float m_ref = -INFINITY, l = 0.f;
-        uint32_t cnt = 0;
-        for (int i = 0; i < n_it; ++i) {
-            const int kt = kt_min + i;
-            if (kt < bd.kt_lo || kt > bd.kt_hi) continue;
-            const bool got = mbar_wait(&mt.s_full[s], cnt & 1, abort, p.status);
-            if (!__all_sync(0xffffffffu, got)) break;
-            tc_fence_after();
-            // this half's 64 logits of the row, in two 32-column loads, one wait
-            uint32_t ra[32], rb[32];
-            tmem_ld32(t_s + 64 * hh, ra);
-            tmem_ld32(t_s + 64 * hh + 32, rb);
-            tmem_ld_wait();
-            reg_fence(ra);
-            reg_fence(rb);
-            const int key0 = kt * kKeysPerTile + 64 * hh;
-            if (kt * kKeysPerTile + kKeysPerTile - 1 > t_min_s || kt * kKeysPerTile < bd.lo_max) {
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    if (key0 + c > t_row || key0 + c < lo_row) ra[c] = __float_as_uint(-INFINITY);
-                    if (key0 + 32 + c > t_row || key0 + 32 + c < lo_row) rb[c] = __float_as_uint(-INFINITY);
+        uint8_t *qs = smem + C::kQ0 + s * C::kTileBytes;
+        uint32_t cnt = 0;    // S tiles of this slot handled (all units so far)
+        uint32_t ucnt = 0;   // units in which this slot had tiles
+        uint32_t bcnt = 0;   // base-position tiles stored
+        bool stored = false; // this thread issued TMA stores
+        for (int i = 0;; ++i) {
+            const int r = i % kDescRing;
+            if (!mbar_wait_warp(&mt.u_full[r], (i / kDescRing) & 1, abort, p.status)) break;
+            const UnitDesc &dr = mt.desc[r];
+            const int end = dr.end;
+            const Slot S = dr.sl[s];
+            const Band bd = dr.bd[s];
+            const int kt_min = dr.kt_min, n_it = dr.n_it;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&mt.u_empty[r]);
+            if (end) break;
+
+            // ---- the row's position and its query, affine fused ----
+            int my_t = 0;  // the row's position in key coordinates
+            bool my_valid = false, my_bad = false;
+            if (S.kind >= 0 && row < S.n) {
+                if (S.kind == 0) {
+                    my_t = S.row0 + row + p.q_off;
+                    my_valid = true;
+                } else {
+                    my_valid = out_row_position(p, S.row0 + row, my_t);
                 }
+                my_bad = !my_valid;
+                if (my_bad && hh == 0) set_status(p.status, ORTHROS_DEV_BAD_POSITION);
             }
-            const float *xa = reinterpret_cast<const float *>(ra);
-            const float *xb = reinterpret_cast<const float *>(rb);
-            float mq[8];
+            const bool tma = S.kind >= 0 && q_by_tma(S);
+            if (!mbar_wait_warp(&mt.q_full[s], i & 1, abort, p.status)) break;
+            if (S.kind >= 0) {
+                constexpr int kHalfChunks = D / 16;  // 16-byte chunks per half row
+                if (my_valid) {
+                    const float *al = (S.kind == 0 ? p.alpha_base : p.alpha_out) + S.h * D;
+                    const float *be = (S.kind == 0 ? p.beta_base : p.beta_out) + S.h * D;
+                    bool over = false;
+                    uint4 raws[kHalfChunks];  // every load of the half row in flight at once
+                    if (tma) {
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-                mq[q] = max3(max3(xa[4 * q], xa[4 * q + 1], xa[4 * q + 2]), max3(xa[4 * q + 3], xb[4 * q], xb[4 * q + 1]),
-                             fmaxf(xb[4 * q + 2], xb[4 * q + 3]));
-            const float mine = max3(max3(mq[0], mq[1], mq[2]), max3(mq[3], mq[4], mq[5]), fmaxf(mq[6], mq[7]));
-            // both halves combine the same two bf16-rounded maxima, so they agree on the shift
-            const __nv_bfloat16 mine_b = __float2bfloat16_rn(mine);
-            mt.xmax[s][hh][row] = mine_b;
-            mbar_arrive(&mt.xm_bar[s]);
-            if (!__all_sync(0xffffffffu, mbar_wait(&mt.xm_bar[s], cnt & 1, abort, p.status))) break;
-            const float m_tile = fmaxf(__bfloat162float(mine_b), __bfloat162float(mt.xmax[s][hh ^ 1][row]));
-            const float m_new = fmaxf(m_ref, m_tile);
-            const bool resc = (m_new - m_ref) * c2 > 8.f;  // true on the first finite max
-            const bool any_resc = __any_sync(0xffffffffu, resc);
-            const float alpha = resc ? ex2((m_ref - m_new) * c2) : 1.f;
-            if (resc) {
-                l *= alpha;
-                m_ref = m_new;
-            }
-            const float mb = m_ref == -INFINITY ? 0.f : m_ref * c2;
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
-            // P for keys 64 hh .. 64 hh + 63 -> packed columns 32 hh .. 32 hh + 31
+                        for (int cc = 0; cc < kHalfChunks; ++cc)
+                            raws[cc] = *reinterpret_cast<const uint4 *>(qs + sw128_offset<D>(row, hh * kHalfChunks + cc));
+                    } else {
+                        const __nv_bfloat16 *src =
+                            p.q + (((long long)S.b * p.Tq + (my_t - p.q_off)) * p.Hq + S.h) * D;
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const float *x = j ? xb : xa;
-                uint32_t pk[16];
+                        for (int cc = 0; cc < kHalfChunks; ++cc)
+                            raws[cc] = reinterpret_cast<const uint4 *>(src)[hh * kHalfChunks + cc];
+                    }
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float p0 = ex2(fmaf(x[2 * e], c2, -mb));
-                    const float p1 = ex2(fmaf(x[2 * e + 1], c2, -mb));
-                    ls[e & 3] += p0 + p1;
-                    pk[e] = pack_bf16(p0, p1);
+                    for (int cc = 0; cc < kHalfChunks; ++cc) {
+                        const int c = hh * kHalfChunks + cc;
+                        const uint4 raw = raws[cc];
+                        const float4 a0 = reinterpret_cast<const float4 *>(al)[2 * c];
+                        const float4 a1 = reinterpret_cast<const float4 *>(al)[2 * c + 1];
+                        const float4 b0 = reinterpret_cast<const float4 *>(be)[2 * c];
+                        const float4 b1 = reinterpret_cast<const float4 *>(be)[2 * c + 1];
+                        const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+                        float2 x0 = __bfloat1622float2(h2[0]), x1 = __bfloat1622float2(h2[1]);
+                        float2 x2 = __bfloat1622float2(h2[2]), x3 = __bfloat1622float2(h2[3]);
+                        float v[8] = {fmaf(a0.x, x0.x, b0.x), fmaf(a0.y, x0.y, b0.y), fmaf(a0.z, x1.x, b0.z),
+                                      fmaf(a0.w, x1.y, b0.w), fmaf(a1.x, x2.x, b1.x), fmaf(a1.y, x2.y, b1.y),
+                                      fmaf(a1.z, x3.x, b1.z), fmaf(a1.w, x3.y, b1.w)};
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) over |= fabsf(v[e]) > 65504.f;
+                        uint4 o;
+                        o.x = pack_f16(v[0], v[1]);
+                        o.y = pack_f16(v[2], v[3]);
+                        o.z = pack_f16(v[4], v[5]);
+                        o.w = pack_f16(v[6], v[7]);
+                        *reinterpret_cast<uint4 *>(qs + sw128_offset<D>(row, c)) = o;
+                    }
+                    if (over) set_status(p.status, ORTHROS_DEV_FP16_RANGE);
+                } else {
+#pragma unroll 4
+                    for (int cc = 0; cc < kHalfChunks; ++cc)
+                        *reinterpret_cast<uint4 *>(qs + sw128_offset<D>(row, hh * kHalfChunks + cc)) =
+                            make_uint4(0, 0, 0, 0);
                 }
-                tmem_st16(t_s + 32 * hh + 16 * j, pk);
+                fence_proxy_async_smem();
             }
-            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            // O_s is idle here (PV_s of the previous tile completed before S_s of
-            // this tile was signalled; the next PV_s waits for p_full): each half
-            // rescales its own D/2 columns of the running output.
-            if (any_resc && cnt > 0) {
+            mbar_arrive(&mt.q_ready[s]);
+
+            // ---- tiles: S -> P (online softmax), band mask on edge tiles only ----
+            const int t_row = my_valid ? my_t : bd.t_max;
+            const int lo_row = S.kind == 0 ? max(0, t_row - p.window + 1) : p.key_lo;
+            const int t_min_s = bd.t_min;
+            float m_ref = -INFINITY, l = 0.f;
+            bool ok = true;
+            uint32_t tiles = 0;
+            for (int it = 0; it < n_it; ++it) {
+                const int kt = kt_min + it;
+                if (kt < bd.kt_lo || kt > bd.kt_hi) continue;
+                const bool got = mbar_wait(&mt.s_full[s], cnt & 1, abort, p.status);
+                if (!(ok = __all_sync(0xffffffffu, got))) break;
+                tc_fence_after();
+                // this half's 64 logits of the row, in two 32-column loads, one wait
+                uint32_t ra[32], rb[32];
+                tmem_ld32(t_s + 64 * hh, ra);
+                tmem_ld32(t_s + 64 * hh + 32, rb);
+                tmem_ld_wait();
+                reg_fence(ra);
+                reg_fence(rb);
+                const int key0 = kt * kKeysPerTile + 64 * hh;
+                if (kt * kKeysPerTile + kKeysPerTile - 1 > t_min_s || kt * kKeysPerTile < bd.lo_max) {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        if (key0 + c > t_row || key0 + c < lo_row) ra[c] = __float_as_uint(-INFINITY);
+                        if (key0 + 32 + c > t_row || key0 + 32 + c < lo_row) rb[c] = __float_as_uint(-INFINITY);
+                    }
+                }
+                const float *xa = reinterpret_cast<const float *>(ra);
+                const float *xb = reinterpret_cast<const float *>(rb);
+                float mq[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    mq[q] = max3(max3(xa[4 * q], xa[4 * q + 1], xa[4 * q + 2]),
+                                 max3(xa[4 * q + 3], xb[4 * q], xb[4 * q + 1]), fmaxf(xb[4 * q + 2], xb[4 * q + 3]));
+                const float mine = max3(max3(mq[0], mq[1], mq[2]), max3(mq[3], mq[4], mq[5]), fmaxf(mq[6], mq[7]));
+                // both halves combine the same two bf16-rounded maxima, so they agree on the shift
+                const __nv_bfloat16 mine_b = __float2bfloat16_rn(mine);
+                mt.xmax[s][hh][row] = mine_b;
+                mbar_arrive(&mt.xm_bar[s]);
+                if (!(ok = __all_sync(0xffffffffu, mbar_wait(&mt.xm_bar[s], cnt & 1, abort, p.status)))) break;
+                const float m_tile = fmaxf(__bfloat162float(mine_b), __bfloat162float(mt.xmax[s][hh ^ 1][row]));
+                const float m_new = fmaxf(m_ref, m_tile);
+                const bool resc = (m_new - m_ref) * c2 > 8.f;  // true on the first finite max
+                const bool any_resc = __any_sync(0xffffffffu, resc);
+                const float alpha = resc ? ex2((m_ref - m_new) * c2) : 1.f;
+                if (resc) {
+                    l *= alpha;
+                    m_ref = m_new;
+                }
+                const float mb = m_ref == -INFINITY ? 0.f : m_ref * c2;
+                float ls[4] = {0.f, 0.f, 0.f, 0.f};
+                // P for keys 64 hh .. 64 hh + 63 -> packed columns 32 hh .. 32 hh + 31
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const float *x = j ? xb : xa;
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float p0 = ex2(fmaf(x[2 * e], c2, -mb));
+                        const float p1 = ex2(fmaf(x[2 * e + 1], c2, -mb));
+                        ls[e & 3] += p0 + p1;
+                        pk[e] = pack_bf16(p0, p1);
+                    }
+                    tmem_st16(t_s + 32 * hh + 16 * j, pk);
+                }
+                l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                // O_s is idle here (PV_s of the previous tile completed before S_s of
+                // this tile was signalled; the next PV_s waits for p_full): each half
+                // rescales its own D/2 columns of the running output.
+                if (any_resc && tiles > 0) {
+#pragma unroll
+                    for (int j = 0; j < D / 64; ++j) {
+                        uint32_t o[32];
+                        tmem_ld32(t_o + 32 * j, o);
+                        tmem_ld_wait();
+                        reg_fence(o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st32(t_o + 32 * j, o);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&mt.p_full[s]);
+                ++cnt;
+                ++tiles;
+            }
+            if (!ok) break;
+
+            // ---- epilogue: o = O / l, lse = scale*m + ln l ----
+            // o_full fires once every product of the slot's unit has completed, so
+            // the slot's S columns and its query tile are idle: the two halves of a
+            // row exchange their row sums through two S columns of their TMEM lane;
+            // a base-position tile's normalised output is staged in its query tile
+            // (128-byte swizzle) and leaves by one TMA store (rows past the query
+            // rows fall outside the map); output-row tiles store row by row.
+            if (tiles > 0) {
+                if (!mbar_wait_warp(&mt.o_full[s], ucnt & 1, abort, p.status)) break;
+                tc_fence_after();
+                tmem_st1(t_s + 96 + hh, __float_as_uint(l));
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&mt.lx_bar[s]);
+                if (!mbar_wait_warp(&mt.lx_bar[s], ucnt & 1, abort, p.status)) break;
+                tc_fence_after();
+                uint32_t l_other = tmem_ld1(t_s + 96 + (hh ^ 1));
+                tmem_ld_wait();
+                asm volatile("" : "+r"(l_other));  // not read before the wait
+                const float l_all = l + __uint_as_float(l_other);
+                ++ucnt;
+                const bool tile_store = S.kind == 0;  // warp-uniform
+                const bool store = S.kind >= 0 && row < S.n;
+                __nv_bfloat16 *dst = nullptr;
+                float *dst32 = nullptr;  // output rows written as float (shard partials)
+                float *lse_dst = nullptr;
+                if (store && S.kind == 0) {
+                    lse_dst = p.lse_base + ((long long)S.b * p.Hq + S.h) * p.Tq + (my_t - p.q_off);
+                } else if (store) {
+                    const long long o_off = ((long long)(S.row0 + row) * p.Hq + S.h) * D + hh * (D / 2);
+                    if (p.o_out_f32) dst32 = p.o_out_f32 + o_off;
+                    else dst = p.o_out + o_off;
+                    lse_dst = p.lse_out + (long long)(S.row0 + row) * p.Hq + S.h;
+                }
+                // a shard's output row before the shard's first key has no keys: o = 0, lse = -inf
+                const float inv = my_bad ? __int_as_float(0x7fc00000) : (l_all > 0.f ? 1.f / l_all : 0.f);
 #pragma unroll
                 for (int j = 0; j < D / 64; ++j) {
                     uint32_t o[32];
                     tmem_ld32(t_o + 32 * j, o);
                     tmem_ld_wait();
                     reg_fence(o);
+                    uint4 w[4];
+                    uint32_t *wp = reinterpret_cast<uint32_t *>(w);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                    tmem_st32(t_o + 32 * j, o);
+                    for (int e = 0; e < 16; ++e)
+                        wp[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+                    if (tile_store) {
+                        const int c0 = (hh * (D / 2) + 32 * j) / 8;  // first 16-byte chunk of these 32 channels
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            *reinterpret_cast<uint4 *>(qs + sw128_offset<D>(row, c0 + e)) = w[e];
+                    } else if (dst32) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            reinterpret_cast<float4 *>(dst32 + 32 * j)[e] =
+                                make_float4(__uint_as_float(o[4 * e]) * inv, __uint_as_float(o[4 * e + 1]) * inv,
+                                            __uint_as_float(o[4 * e + 2]) * inv, __uint_as_float(o[4 * e + 3]) * inv);
+                    } else if (store) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) reinterpret_cast<uint4 *>(dst + 32 * j)[e] = w[e];
+                    }
                 }
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(&mt.p_full[s]);
-            ++cnt;
-        }
-        // ---------------- epilogue: o = O / l, lse = scale*m + ln l ----------------
-        // Every MMA has completed once o_full fires, so the key stages and the
-        // query tile are idle: row sums are exchanged through the first key
-        // stage; a base-position tile's normalised output is staged in its
-        // query tile (128-byte swizzle) and leaves by one TMA store (rows past
-        // T fall outside the map); output-row tiles store row by row.
-        bool have = cnt > 0 && mbar_wait(&mt.o_full[s], 0, abort, p.status);
-        have = __all_sync(0xffffffffu, have);
-        if (have) {
-            tc_fence_after();
-            float *lx = reinterpret_cast<float *>(smem + C::kK0 + s * 1024);  // [2][128]
-            lx[hh * kRowsPerTile + row] = l;
-            mbar_arrive(&mt.lx_bar[s]);
-            have = __all_sync(0xffffffffu, mbar_wait(&mt.lx_bar[s], 0, abort, p.status));
-            const float l_all = l + lx[(hh ^ 1) * kRowsPerTile + row];
-            const bool tile_store = S.kind == 0;  // warp-uniform
-            const bool store = have && S.kind >= 0 && row < S.n;
-            uint8_t *stage = smem + C::kQ0 + s * C::kTileBytes;
-            __nv_bfloat16 *dst = nullptr;
-            float *dst32 = nullptr;  // output rows written as float (shard partials)
-            float *lse_dst = nullptr;
-            if (store && S.kind == 0) {
-                lse_dst = p.lse_base + ((long long)S.b * p.Hq + S.h) * p.Tq + (my_t - p.q_off);
-            } else if (store) {
-                const long long o_off = ((long long)(S.row0 + row) * p.Hq + S.h) * D + hh * (D / 2);
-                if (p.o_out_f32) dst32 = p.o_out_f32 + o_off;
-                else dst = p.o_out + o_off;
-                lse_dst = p.lse_out + (long long)(S.row0 + row) * p.Hq + S.h;
-            }
-            // a shard's output row before the shard's first key has no keys: o = 0, lse = -inf
-            const float inv = my_bad ? __int_as_float(0x7fc00000) : (l_all > 0.f ? 1.f / l_all : 0.f);
-#pragma unroll
-            for (int j = 0; j < D / 64; ++j) {
-                uint32_t o[32];
-                tmem_ld32(t_o + 32 * j, o);
-                tmem_ld_wait();
-                reg_fence(o);
-                uint4 w[4];
-                uint32_t *wp = reinterpret_cast<uint32_t *>(w);
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    wp[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+                if (store && hh == 0)
+                    *lse_dst = my_bad ? __int_as_float(0x7fc00000)
+                                      : (l_all > 0.f ? m_ref * p.scale + logf(l_all) : -INFINITY);
                 if (tile_store) {
-                    const int c0 = (hh * (D / 2) + 32 * j) / 8;  // first 16-byte chunk of these 32 channels
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) *reinterpret_cast<uint4 *>(stage + sw128_offset<D>(row, c0 + e)) = w[e];
-                } else if (dst32) {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        reinterpret_cast<float4 *>(dst32 + 32 * j)[e] =
-                            make_float4(__uint_as_float(o[4 * e]) * inv, __uint_as_float(o[4 * e + 1]) * inv,
-                                        __uint_as_float(o[4 * e + 2]) * inv, __uint_as_float(o[4 * e + 3]) * inv);
-                } else if (store) {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) reinterpret_cast<uint4 *>(dst + 32 * j)[e] = w[e];
+                    fence_proxy_async_smem();
+                    mbar_arrive(&mt.os_bar[s]);
+                    if (!mbar_wait_warp(&mt.os_bar[s], bcnt & 1, abort, p.status)) break;
+                    ++bcnt;
+                    if (row == 0 && hh == 0) {
+                        for (int j = 0; j < C::kSub; ++j)
+                            tma_store_4d(&tm_ob, qs + j * (kRowsPerTile * 128), 64 * j, S.h, S.row0, S.b);
+                        bulk_commit();
+                        bulk_wait_read();  // the query tile is free again once the store has read it
+                        stored = true;
+                    }
                 }
-            }
-            if (store && hh == 0)
-                *lse_dst = my_bad ? __int_as_float(0x7fc00000)
-                                  : (l_all > 0.f ? m_ref * p.scale + logf(l_all) : -INFINITY);
-            if (tile_store && have) {
-                fence_proxy_async_smem();
-                mbar_arrive(&mt.os_bar[s]);
-                const bool staged = __all_sync(0xffffffffu, mbar_wait(&mt.os_bar[s], 0, abort, p.status));
-                if (staged && row == 0 && hh == 0 && lane == 0) {
-                    for (int j = 0; j < C::kSub; ++j)
-                        tma_store_4d(&tm_ob, stage + j * (kRowsPerTile * 128), 64 * j, S.h, S.row0, S.b);
-                    bulk_commit();
-                    bulk_wait_read();
+            } else if (S.kind == 1 && row < S.n && my_valid) {
+                // no key tile in the slot's band (a shard's rows that all precede its keys)
+                const long long o_off = ((long long)(S.row0 + row) * p.Hq + S.h) * D + hh * (D / 2);
+                for (int c = 0; c < D / 2; ++c) {
+                    if (p.o_out_f32) p.o_out_f32[o_off + c] = 0.f;
+                    else p.o_out[o_off + c] = __float2bfloat16_rn(0.f);
                 }
+                if (hh == 0) p.lse_out[(long long)(S.row0 + row) * p.Hq + S.h] = -INFINITY;
             }
-        } else if (cnt == 0 && !*abort && S.kind == 1 && row < S.n && my_valid) {
-            // no key tile in the slot's band (a shard's rows that all precede its keys)
-            const long long o_off = ((long long)(S.row0 + row) * p.Hq + S.h) * D + hh * (D / 2);
-            for (int c = 0; c < D / 2; ++c) {
-                if (p.o_out_f32) p.o_out_f32[o_off + c] = 0.f;
-                else p.o_out[o_off + c] = __float2bfloat16_rn(0.f);
-            }
-            if (hh == 0) p.lse_out[(long long)(S.row0 + row) * p.Hq + S.h] = -INFINITY;
+            tc_fence_before();
+            mbar_arrive(&mt.q_free[s]);
         }
+        if (stored) bulk_wait_all();
     }
 
     tc_fence_before();
@@ -714,7 +841,11 @@ cudaError_t launch_d(const TcParams &p, const void *k16, const void *v, int unit
         return cudaErrorInvalidValue;
     static SmemLimit limit;
     if (cudaError_t e = limit.ensure((const void *)prefill_tc_kernel<D>, Cfg<D>::kSmem); e != cudaSuccess) return e;
-    prefill_tc_kernel<D><<<units, kThreads, Cfg<D>::kSmem, stream>>>(tk, tv, tq, tqo, tob, p);
+    // persistent: one CTA per SM takes units from the counter until none is left
+    int dev = 0, sms = 152;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int grid = units < sms ? units : sms;
+    prefill_tc_kernel<D><<<grid, kThreads, Cfg<D>::kSmem, stream>>>(tk, tv, tq, tqo, tob, p);
     return cudaGetLastError();
 }
 
