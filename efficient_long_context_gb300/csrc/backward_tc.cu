@@ -68,10 +68,52 @@ constexpr int kOffMeta = kOffDS + 2 * kDSBytes;
 // TMEM columns
 constexpr uint32_t kTS = 0, kTdP = 64, kTdV = 128, kTdK = 256, kTdQ = 384, kTP = 448;
 
-struct StageMeta {
+// 16-byte aligned: the softmax warps read pos / lse2 / ndelta four at a time
+struct __align__(16) StageMeta {
     int pos[kRows];      // row position, -1 for rows past the tile's end
     float lse2[kRows];   // L * log2(e), +inf for rows past the end
     float ndelta[kRows]; // -D * scale, D = dO . o
+    int2 tile;           // x = 2 * head + kind (0 base, 1 output rows), y = first row
+};
+static_assert(sizeof(StageMeta) % 16 == 0, "stage metadata must keep every stage 16-byte aligned");
+
+// The query tiles one key block visits, in order: for each query head of the
+// GQA group, the base-stream tiles of the band [j0, j0 + 127 + w - 1], then
+// the output-row tiles whose largest position reaches j0. Produced one at a
+// time by the (warp-uniform) producer warp, so a key block may visit any
+// number of tiles.
+struct TileGen {
+    int hh = 0, bi = 0, mbase = 0, phase = 0;
+    unsigned mask = 0;
+    // next tile (x = -1 when none is left); every lane of the warp calls it
+    __device__ int2 next(const BwdTcParams &p, int kv, int g, int j0, int n_base, int r0b, int r1b, int lane) {
+        const int n_cand = (r1b - r0b + kRows - 1) / kRows;
+        while (hh < g) {
+            const int h = kv * g + hh;
+            if (phase == 0) {
+                if (bi < n_base) return make_int2(2 * h, j0 + kRows * bi++);
+                phase = 1;
+                mbase = 0;
+                mask = 0;
+            }
+            if (mask) {
+                const int k = __ffs(mask) - 1;
+                mask &= mask - 1;
+                return make_int2(2 * h + 1, r0b + (mbase - 32 + k) * kRows);
+            }
+            if (mbase >= n_cand) {
+                ++hh;
+                phase = 0;
+                bi = 0;
+                continue;
+            }
+            const int m = mbase + lane;
+            const int r = r0b + m * kRows;
+            mask = __ballot_sync(0xffffffffu, m < n_cand && p.omax[r] >= j0);
+            mbase += 32;
+        }
+        return make_int2(-1, 0);
+    }
 };
 
 struct Meta {
@@ -82,7 +124,6 @@ struct Meta {
     int n_tiles;
     int pad;
     StageMeta st[kStages];
-    int2 tiles[kBwdMaxTiles];  // x = 2 * head + kind (0 base, 1 output rows), y = first row
 };
 
 constexpr int kSmem = kOffMeta + (int)sizeof(Meta) + 1024;
@@ -107,11 +148,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     volatile int *abort = &mt.abort;
 
-    // unit: key block (slowest, so blocks with the most output rows start first), sequence, kv head
-    const int per_jb = p.B * p.Hkv;
-    const int jb = blockIdx.x / per_jb;
-    const int b = (blockIdx.x % per_jb) / p.Hkv;
-    const int kv = blockIdx.x % p.Hkv;
+    // unit: (sequence, kv head) slowest, key block fastest: the CTAs running at
+    // one time reduce into the dQ rows of a few (sequence, kv head) pairs,
+    // which then stay in L2; inside a pair the early key blocks (those that
+    // the most output rows reach) start first
+    const int jb = blockIdx.x % p.nkb;
+    const int b = blockIdx.x / p.nkb / p.Hkv;
+    const int kv = (blockIdx.x / p.nkb) % p.Hkv;
     const int j0 = jb * kKeys;
     const int g = p.Hq / p.Hkv;
     const int r0b = p.n_out ? p.out_indptr[b] : 0;
@@ -135,28 +178,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         mt.abort = 0;
         fence_mbar_init();
     }
+    // base tiles of the band of one head: rows j0 .. min(T - 1, j0 + 127 + w - 1)
+    const long long t_hi_ll = min((long long)p.T - 1, (long long)j0 + kKeys - 1 + (long long)p.window - 1);
+    const int n_base = (int)((t_hi_ll - j0) / kRows) + 1;
     if (warp == 0) {
-        // Tile list: base-stream tiles of the band, then output-row tiles that
-        // reach this key block, for each query head of the group.
-        const long long t_hi_ll = min((long long)p.T - 1, (long long)j0 + kKeys - 1 + (long long)p.window - 1);
-        const int n_base = (int)((t_hi_ll - j0) / kRows) + 1;
-        int n = 0;
-        for (int hh = 0; hh < g; ++hh) {
-            const int h = kv * g + hh;
-            for (int i = lane; i < n_base; i += 32)
-                if (n + i < kBwdMaxTiles) mt.tiles[n + i] = make_int2(2 * h, j0 + i * kRows);
-            n += n_base;
-            for (int r0 = r0b; r0 < r1b; r0 += 32 * kRows) {
-                const int r = r0 + lane * kRows;
-                const bool take = r < r1b && p.omax[r] >= j0;
-                const unsigned m = __ballot_sync(0xffffffffu, take);
-                const int at = n + __popc(m & ((1u << lane) - 1u));
-                if (take && at < kBwdMaxTiles) mt.tiles[at] = make_int2(2 * h + 1, r);
-                n += __popc(m);
-            }
+        // tiles to visit: the same output-row tiles reach this key block for every head
+        int n_out_tiles = 0;
+        for (int r0 = r0b; r0 < r1b; r0 += 32 * kRows) {
+            const int r = r0 + lane * kRows;
+            n_out_tiles += __popc(__ballot_sync(0xffffffffu, r < r1b && p.omax[r] >= j0));
         }
-        // the host launches this kernel only when bwd_tc_max_tiles_bound() fits
-        if (lane == 0) mt.n_tiles = min(n, kBwdMaxTiles);
+        if (lane == 0) mt.n_tiles = g * (n_base + n_out_tiles);
     }
     if (warp == kProducerWarp && lane == 0) {
         prefetch_tmap(&tm_k);
@@ -191,8 +223,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // tile ahead, so its global-memory latency overlaps the wait for a stage.
         int m_pos[2];
         float m_l2[2], m_dl[2];
-        auto fetch = [&](int i) {
-            const int2 tl = mt.tiles[i];
+        TileGen gen;
+        auto fetch = [&](int2 tl) {
             const int h = tl.x >> 1, kind = tl.x & 1, row0 = tl.y;
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
@@ -219,13 +251,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         };
-        if (n_tiles > 0) fetch(0);
+        int2 tl_next = make_int2(-1, 0);
+        if (n_tiles > 0) {
+            tl_next = gen.next(p, kv, g, j0, n_base, r0b, r1b, lane);
+            fetch(tl_next);
+        }
         for (int i = 0; i < n_tiles; ++i) {
             const int s = i % kStages;
             if (i >= kStages) {
                 if (!mbar_wait_warp(&mt.q_empty[s], ((i / kStages) - 1) & 1, abort, p.status)) break;
             }
-            const int2 tl = mt.tiles[i];
+            const int2 tl = tl_next;
             const int h = tl.x >> 1, kind = tl.x & 1, row0 = tl.y;
             if (lane == 0) {
                 uint8_t *qa = smem + kOffQ + s * 2 * kQBytes;
@@ -249,9 +285,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sm.lse2[c] = valid ? m_l2[u] * log2e : INFINITY;
                 sm.ndelta[c] = valid ? -m_dl[u] * p.scale : 0.f;
             }
+            if (lane == 0) sm.tile = tl;
             __syncwarp();
             if (lane == 0) mbar_arrive(&mt.q_full[s]);
-            if (i + 1 < n_tiles) fetch(i + 1);
+            if (i + 1 < n_tiles) {
+                tl_next = gen.next(p, kv, g, j0, n_base, r0b, r1b, lane);
+                fetch(tl_next);
+            }
             issued = i + 1;
         }
         // nothing may land in shared memory after the CTA exits
@@ -334,6 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int j = j0 + key;
         const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
         const float c2 = p.scale_log2;
+        int2 prev_tile = make_int2(0, 0);  // the tile whose dQ is drained next
         auto drain = [&](int pi) -> bool {
             if (!mbar_wait_warp(&mt.dq_full, pi & 1, abort, p.status)) return false;
             tc_fence_after();
@@ -343,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             reg_fence(v);
             tc_fence_before();
             mbar_arrive(&mt.dq_free);
-            const int2 tl = mt.tiles[pi];
+            const int2 tl = prev_tile;
             const int h = tl.x >> 1, kind = tl.x & 1, row0 = tl.y;
             const int ch = key;  // dQ^T lanes are channels
             if (kind == 0) {
@@ -378,7 +419,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&mt.s_free);
             // the row metadata was published with q_full (already complete for this tile)
             if (!(ok = mbar_wait_warp(&mt.q_full[s], (i / kStages) & 1, abort, p.status))) break;
-            const int kind = mt.tiles[i].x & 1;
+            const int2 cur_tile = mt.st[s].tile;
+            const int kind = cur_tile.x & 1;
             const unsigned wlim = kind ? 0x7fffffffu : (unsigned)p.window;  // valid: 0 <= t - j < wlim
             const StageMeta &sm = mt.st[s];
             uint32_t pk[16], dk[16];
@@ -419,6 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(&mt.p_full[ps]);
             if (i >= 1 && !(ok = drain(i - 1))) break;
+            prev_tile = cur_tile;
         }
         if (ok && n_tiles > 0) ok = drain(n_tiles - 1);
         // dK, dV of this thread's key: columns [64 hh, 64 hh + 64) of each
@@ -457,14 +500,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 }  // namespace
-
-int bwd_tc_max_tiles_bound(int T, int window, int g, int max_rows_per_seq) {
-    const long long span = std::min<long long>((long long)T, (long long)kKeys + window - 1);
-    const long long n_base = (span - 1) / kRows + 1;
-    const long long n_out = ((long long)max_rows_per_seq + kRows - 1) / kRows;
-    const long long n = (long long)g * (n_base + n_out);
-    return n > (1LL << 30) ? (1 << 30) : (int)n;
-}
 
 cudaError_t launch_backward_tc(const BwdTcParams &p, const void *k, const void *v, const void *qa_base,
                                const void *do_base, const void *qa_out, const void *do_out, cudaStream_t stream) {

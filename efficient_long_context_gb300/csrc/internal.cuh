@@ -130,7 +130,10 @@ int tc_units_per_kv(int nblk, int g);
 cudaError_t launch_prefill_tc(const TcParams &p, const void *k16, const void *v, int d, cudaStream_t stream);
 
 // splitkv.cu: split-KV attention for few rows over long key ranges + combine.
-enum SplitMode { kSplitPrefill = 0, kSplitDecode = 1, kSplitExtend = 2 };
+// kSplitDecodeSplit: a decoding step whose GQA group is too large for one
+// 16-row group (8 < g <= 16): group 2 * (b * Hkv + kv) + 0 holds the base rows
+// of (sequence b, kv head kv), + 1 its output rows (TMA kernel only).
+enum SplitMode { kSplitPrefill = 0, kSplitDecode = 1, kSplitExtend = 2, kSplitDecodeSplit = 3 };
 struct SplitParams {
     int mode;
     const __nv_bfloat16 *q, *q_out;  // prefill [B,T,Hq,d] / [n_out,Hq,d]; decode [B,Hq,d] each
@@ -234,7 +237,6 @@ struct BwdArgs {
 cudaError_t launch_backward(const BwdArgs &a, int d, orthros_dtype dtype, bool use_tc, cudaStream_t stream);
 
 // backward_tc.cu
-constexpr int kBwdMaxTiles = 1024;  // query tiles one key block may visit
 struct BwdTcParams {
     const int32_t *out_indptr, *out_positions, *omax;
     const float *lse_base, *lse_out, *delta_base, *delta_out;
@@ -244,8 +246,6 @@ struct BwdTcParams {
     float scale, scale_log2;
     uint32_t *status;
 };
-// Upper bound on the query tiles of one key block (must not exceed kBwdMaxTiles).
-int bwd_tc_max_tiles_bound(int T, int window, int g, int max_rows_per_seq);
 cudaError_t launch_backward_tc(const BwdTcParams &p, const void *k, const void *v, const void *qa_base,
                                const void *do_base, const void *qa_out, const void *do_out, cudaStream_t stream);
 

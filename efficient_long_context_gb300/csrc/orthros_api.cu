@@ -99,13 +99,24 @@ struct DecodeLayout {
     int chunk, max_chunks;
 };
 
-DecodeLayout decode_layout(int B, int Hkv, int d, int max_pages, int page_size, orthros_dtype dtype) {
+// Row groups of a decoding step on the split-KV path: one per (sequence, kv
+// head) when its g base and g output rows fit 16 rows, else two (base rows,
+// output rows) for groups of up to 16 query heads on 64-token-multiple pages.
+int decode_groups(int B, int Hq, int Hkv, int page_size) {
+    const int g = Hq / Hkv;
+    if (2 * g <= 16) return B * Hkv;
+    if (g <= 16 && page_size % 64 == 0) return 2 * B * Hkv;
+    return 0;  // CUDA-core rows
+}
+
+DecodeLayout decode_layout(int B, int Hq, int Hkv, int d, int max_pages, int page_size, orthros_dtype dtype) {
     DecodeLayout L{};
     size_t at = kStatusBytes;
     L.part_off = at;
-    L.chunk = split_chunk((long long)B * Hkv, (long long)max_pages * page_size);
+    const int groups = decode_groups(B, Hq, Hkv, page_size);
+    L.chunk = split_chunk(groups > 0 ? groups : 1, (long long)max_pages * page_size);
     L.max_chunks = ceil_div((long long)max_pages * page_size, L.chunk);
-    if (dtype == ORTHROS_BF16) at += align_up(split_partial_bytes(B * Hkv, L.max_chunks, d), 256);
+    if (dtype == ORTHROS_BF16 && groups > 0) at += align_up(split_partial_bytes(groups, L.max_chunks, d), 256);
     L.total = at;
     return L;
 }
@@ -650,12 +661,7 @@ orthros_status orthros_prefill_backward(const void *q, const void *k, const void
     a.d_alpha_out = d_alpha_out;
     a.d_beta_out = d_beta_out;
     a.status = status;
-    bool use_tc = dtype == ORTHROS_BF16 && d == 128;
-    if (use_tc) {
-        int max_rows = 0;
-        for (int b = 0; b < B && n_out > 0; ++b) max_rows = std::max(max_rows, out_indptr[b + 1] - out_indptr[b]);
-        use_tc = bwd_tc_max_tiles_bound(T, window, Hq / Hkv, max_rows) <= kBwdMaxTiles;
-    }
+    const bool use_tc = dtype == ORTHROS_BF16 && d == 128;
     if (use_tc) {
         a.qa_base = reinterpret_cast<__nv_bfloat16 *>(ws + lay.qa_base_off);
         a.qa_out = reinterpret_cast<__nv_bfloat16 *>(ws + lay.qa_out_off);
@@ -948,7 +954,7 @@ size_t orthros_decode_workspace_size(int B, int Hq, int Hkv, int d, int max_page
                                      orthros_dtype dtype) {
     if (max_pages < 1 || page_size < 1) return 0;
     if (check_shapes(B, Hq, Hkv, d, 1, 1.0f, dtype) != ORTHROS_OK) return 0;
-    return decode_layout(B, Hkv, d, max_pages, page_size, dtype).total;
+    return decode_layout(B, Hq, Hkv, d, max_pages, page_size, dtype).total;
 }
 
 orthros_status orthros_decode(const void *q, const void *q_out, const void *k_new, const void *v_new,
@@ -977,7 +983,7 @@ orthros_status orthros_decode(const void *q, const void *q_out, const void *k_ne
             !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o_base) || !aligned16(o_out))
             return fail(ORTHROS_EINVAL, "element tensors must be 16-byte aligned");
     }
-    const DecodeLayout lay = decode_layout(B, Hkv, d, max_pages, page_size, dtype);
+    const DecodeLayout lay = decode_layout(B, Hq, Hkv, d, max_pages, page_size, dtype);
     if (!workspace || workspace_bytes < lay.total)
         return fail(ORTHROS_EWORKSPACE, "workspace needs %zu bytes, got %zu", lay.total,
                     workspace ? workspace_bytes : (size_t)0);
@@ -996,10 +1002,13 @@ orthros_status orthros_decode(const void *q, const void *q_out, const void *k_ne
     if (e != cudaSuccess) return cuda_fail(e, "append launch");
 
     const int g = Hq / Hkv;
-    if (dtype == ORTHROS_BF16 && 2 * g <= 16) {
-        // both rows of every query head of a kv group share one pass over the cache
+    const int groups = decode_groups(B, Hq, Hkv, page_size);
+    if (dtype == ORTHROS_BF16 && groups > 0) {
+        // both rows of every query head of a kv group share one pass over the
+        // cache; groups of more than 8 query heads read it once per row kind
+        // (the base rows only their window)
         SplitParams sp{};
-        sp.mode = kSplitDecode;
+        sp.mode = groups == B * Hkv ? kSplitDecode : kSplitDecodeSplit;
         sp.q = static_cast<const __nv_bfloat16 *>(q);
         sp.q_out = static_cast<const __nv_bfloat16 *>(q_out);
         sp.k = static_cast<const __nv_bfloat16 *>(k_cache);
@@ -1019,7 +1028,7 @@ orthros_status orthros_decode(const void *q, const void *q_out, const void *k_ne
         sp.window = window;
         sp.scale = scale;
         sp.scale_log2 = scale * 1.4426950408889634f;
-        sp.n_groups = B * Hkv;
+        sp.n_groups = groups;
         sp.chunk = lay.chunk;
         sp.max_chunks = lay.max_chunks;
         sp.kv_tokens = (long long)num_pages * page_size;
@@ -1030,7 +1039,7 @@ orthros_status orthros_decode(const void *q, const void *q_out, const void *k_ne
         sp.lse_out = lse_out;
         sp.status = status;
         ProfScope ps("splitkv_decode", stream);
-        e = launch_splitkv(sp, d, 2 * g, stream);
+        e = launch_splitkv(sp, d, sp.mode == kSplitDecode ? 2 * g : g, stream);
         if (e != cudaSuccess) return cuda_fail(e, "split-KV decode launch");
         return ORTHROS_OK;
     }

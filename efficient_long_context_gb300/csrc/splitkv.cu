@@ -421,6 +421,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const SplitParams p) {
         b = group / p.Hkv;
         kv = group % p.Hkv;
         nrows = 2 * gsz;
+    } else if (p.mode == kSplitDecodeSplit) {
+        b = (group >> 1) / p.Hkv;
+        kv = (group >> 1) % p.Hkv;
+        nrows = gsz;
     } else if (p.mode == kSplitExtend) {
         const int *e = p.ext_info + 4 * group;
         b = e[0] >> 16;
@@ -445,11 +449,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const SplitParams p) {
         hi = extend_position(p, group, b, p.cache_lens[b], r / gsz, kind, idx);
         dst = (kind == 0 ? p.o_base : p.o_out) + ((long long)idx * p.Hq + h) * D;
         lse_dst = (kind == 0 ? p.lse_base : p.lse_out) + (long long)idx * p.Hq + h;
-    } else if (p.mode == kSplitDecode) {
+    } else if (p.mode == kSplitDecode || p.mode == kSplitDecodeSplit) {
         const int L = p.cache_lens[b];
         hi = (L >= 0 && L / p.page_size < p.max_pages) ? L : -1;
-        const bool base = r < gsz;
-        const int h = kv * gsz + (base ? r : r - gsz);
+        const bool base = p.mode == kSplitDecode ? r < gsz : (group & 1) == 0;
+        const int h = kv * gsz + (r < gsz ? r : r - gsz);
         dst = (base ? p.o_base : p.o_out) + ((long long)b * p.Hq + h) * D;
         lse_dst = (base ? p.lse_base : p.lse_out) + (long long)b * p.Hq + h;
     } else {
@@ -556,6 +560,7 @@ cudaError_t launch_splitkv(const SplitParams &p, int d, int rows_per_group, cuda
     if (p.n_groups == 0 || p.max_chunks == 0) return cudaSuccess;
     cudaError_t e;
     if (p.mode == kSplitExtend) return cudaErrorInvalidValue;  // launch_splitkv_extend
+    if (p.mode == kSplitDecodeSplit && !splitkv_tma_eligible(p)) return cudaErrorInvalidValue;  // TMA kernel only
     if (splitkv_tma_eligible(p)) {
         e = launch_splitkv_tma(p, d, rows_per_group, stream);
     } else {

@@ -79,6 +79,15 @@ __device__ __forceinline__ ItemInfo item_info(const SplitParams &p, int group) {
         it.nrows = 2 * gsz;
         it.L = p.cache_lens[it.b];
         it.union_hi = (it.L >= 0 && it.L / p.page_size < p.max_pages) ? it.L : -1;
+    } else if (p.mode == kSplitDecodeSplit) {
+        const int pair = group >> 1;
+        it.b = pair / p.Hkv;
+        it.kv = pair % p.Hkv;
+        it.nrows = gsz;
+        it.L = p.cache_lens[it.b];
+        it.union_hi = (it.L >= 0 && it.L / p.page_size < p.max_pages) ? it.L : -1;
+        // the base rows' group reads only the window
+        it.union_lo = (group & 1) == 0 && it.union_hi >= 0 ? (max(0, it.L - p.window + 1) / kStageKeys) * kStageKeys : 0;
     } else if (p.mode == kSplitExtend) {
         const int *e = p.ext_info + 4 * group;
         it.b = e[0] >> 16;
@@ -120,10 +129,11 @@ __device__ __forceinline__ void row_range(const SplitParams &p, const ItemInfo &
     lo = 1;
     hi = 0;
     if (r >= it.nrows) return;
-    if (p.mode == kSplitDecode) {
+    if (p.mode == kSplitDecode || p.mode == kSplitDecodeSplit) {
         if (it.union_hi < 0) return;
         hi = it.L;
-        lo = r < gsz ? max(0, it.L - p.window + 1) : 0;
+        const bool base = p.mode == kSplitDecode ? r < gsz : (it.group & 1) == 0;
+        lo = base ? max(0, it.L - p.window + 1) : 0;
     } else if (p.mode == kSplitExtend) {
         int kind, idx;
         const int t = extend_position(p, it.group, it.b, it.L, r / gsz, kind, idx);
@@ -273,7 +283,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         float *part = p.partial + ((long long)group * p.max_chunks + chunk) * kMaxRowsT * kRowStride;
         if (chunk == 0 && tid < kMaxRowsT && tid < it.nrows) {
             // report rows the data makes impossible (their combined outputs are NaN)
-            if (p.mode == kSplitDecode) {
+            if (p.mode == kSplitDecode || p.mode == kSplitDecodeSplit) {
                 if (it.union_hi < 0 && tid == 0) set_status(p.status, ORTHROS_DEV_BAD_LENGTH);
             } else if (p.mode == kSplitExtend) {
                 int kind, idx;
@@ -301,9 +311,9 @@ __global__ void __launch_bounds__(kThreadsT, 1)
             const __nv_bfloat16 *qrow = nullptr;
             const float *al = nullptr, *be = nullptr;
             if (valid) {
-                if (p.mode == kSplitDecode) {
-                    const bool base = r < gsz;
-                    const int h = it.kv * gsz + (base ? r : r - gsz);
+                if (p.mode == kSplitDecode || p.mode == kSplitDecodeSplit) {
+                    const bool base = p.mode == kSplitDecode ? r < gsz : (it.group & 1) == 0;
+                    const int h = it.kv * gsz + (r < gsz ? r : r - gsz);
                     const __nv_bfloat16 *src = (!base && p.q_out) ? p.q_out : p.q;
                     qrow = src + ((long long)it.b * p.Hq + h) * D;
                     al = (base ? p.alpha_base : p.alpha_out) + h * D;

@@ -121,6 +121,16 @@ def test_backward_small(case, with_q_out):
     compare_backward(wl, gpu, ref, do_b, what=str(case))
 
 
+def test_backward_many_tiles_per_key_block():
+    """GQA 16/1 with every position an output row: the first key block visits
+    16 x (3 band + 64 output-row) = 1072 query tiles on the tensor-core path
+    (the tile list is generated while the tiles stream, with no cap)."""
+    wl = W.small_prefill(1, 4096, 16, 1, 128, 64, out_mode="all", seed=21)
+    do_b, do_o = W.make_grad_outputs(wl, seed=22)
+    compare_backward(wl, run_gpu_backward(wl, do_b, do_o), run_oracle_backward(wl, do_b, do_o), do_b,
+                     what="1072 tiles per key block")
+
+
 def test_backward_key_offsets():
     wl = W.small_prefill(1, 400, 8, 2, 128, 100, out_mode=("span", 150), seed=9, k_offset_std=0.5)
     do_b, do_o = W.make_grad_outputs(wl, seed=4)

@@ -78,6 +78,10 @@ SMALL = [
     (2, 4, 1, 128, 5000, 64, [2000, 4500], torch.bfloat16, 2, True),
     (5, 8, 2, 128, 128, 32, [0, 127, 128, 129, 3000], torch.bfloat16, 3, False),
     (2, 4, 2, 64, 30, 16, [7, 400], torch.float32, 3, True),
+    # GQA groups of 9-16 query heads (e.g. 64/4): base and output rows in separate groups on the TMA path
+    (3, 32, 2, 128, 300, 64, [5, 700, 5000], torch.bfloat16, 3, True),
+    (2, 24, 2, 128, 64, 128, [129, 2000], torch.bfloat16, 2, False),
+    (2, 64, 4, 128, 4096, 64, [10000, 20000], torch.bfloat16, 2, False),
     (1, 2, 2, 128, 100, 64, [0], torch.float32, 2, False),
 ]
 
