@@ -28,6 +28,7 @@ from ._binding import (  # noqa: F401
     orthros_prefill_workspace_size,
     orthros_profile_begin,
     orthros_qkv_project,
+    orthros_selftest_wait_timeout,
     orthros_profile_end,
     orthros_status_string,
 )

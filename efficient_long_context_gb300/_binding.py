@@ -26,7 +26,7 @@ EXPORTS = ("orthros_prefill_workspace_size", "orthros_prefill", "orthros_prefill
            "orthros_prefill_backward", "orthros_extend_workspace_size", "orthros_extend", "orthros_qkv_project",
            "orthros_decode_workspace_size",
            "orthros_decode", "orthros_decode_static", "orthros_check", "orthros_profile_begin", "orthros_profile_end",
-           "orthros_status_string", "orthros_last_error")
+           "orthros_selftest_wait_timeout", "orthros_status_string", "orthros_last_error")
 
 
 class KernelTime(ctypes.Structure):
@@ -97,6 +97,8 @@ def load_library(path: str | None = None):
         lib.orthros_decode_static.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp,
                                               vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float, i32,
                                               vp, vp, vp, vp, vp]
+        lib.orthros_selftest_wait_timeout.restype = i32
+        lib.orthros_selftest_wait_timeout.argtypes = [ctypes.c_longlong, vp, sz, vp]
         lib.orthros_check.restype = i32
         lib.orthros_check.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
         lib.orthros_profile_begin.restype = i32
@@ -458,6 +460,14 @@ def orthros_decode_static(q, k_new, v_new, k_cache, v_cache, block_table, cache_
         _ptr(o_base), _ptr(lse_base), _ptr(o_out), _ptr(lse_out), _stream(stream))
     _raise_if(rc, lib)
     return o_base, lse_base, o_out, lse_out
+
+
+def orthros_selftest_wait_timeout(limit_cycles, workspace, stream=None):
+    """orthros_selftest_wait_timeout of include/orthros_attn.h: one kernel whose
+    bounded wait on a barrier nothing arms runs out after limit_cycles."""
+    lib = load_library()
+    rc = lib.orthros_selftest_wait_timeout(int(limit_cycles), _ptr(workspace), workspace.numel(), _stream(stream))
+    _raise_if(rc, lib)
 
 
 def orthros_check(workspace, stream=None):

@@ -25,7 +25,11 @@
 //     threads without ordering between them) race on the array.
 //   * Device-side data errors (bad block-table entries or cache lengths) land
 //     in the shared status word, which this entry point does not expose; the
-//     affected rows come back as NaN.
+//     affected rows come back as NaN, and so do all rows when a kernel gave
+//     up on a bounded wait.
+//   * The array's address is resolved once per device and kept for the life
+//     of the process, so resetting a device after its first call is not
+//     supported.
 #include <mutex>
 
 #include "internal.cuh"

@@ -63,13 +63,13 @@ constexpr long long kWaitLimitCycles = 4000000000LL;
 // raises *abort plus the status bit) if the limit runs out or another thread
 // of the CTA already aborted.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                          uint32_t *status) {
+                                          uint32_t *status, long long limit = kWaitLimitCycles) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
-        if (clock64() - t0 > kWaitLimitCycles) {
+        if (clock64() - t0 > limit) {
             *abort = 1;
             set_status(status, ORTHROS_DEV_TIMEOUT);
             return false;

@@ -362,7 +362,10 @@ ORTHROS_API orthros_status orthros_qkv_project(
  * (cudaGetSymbolAddress) with that device current: make it before any stream
  * capture. All calls share the array: calls ordered on one stream are fine,
  * calls that overlap on the GPU race. Device-side status bits of this entry
- * point are not exposed; rows with bad data come back as NaN.
+ * point are not exposed; rows with bad data (or whose kernel gave up on a
+ * bounded wait) come back as NaN. The array's address is kept per device for
+ * the life of the process: resetting a device (cudaDeviceReset) after its
+ * first call is not supported.
  */
 ORTHROS_API orthros_status orthros_decode_static(
     const void *q, const void *q_out, const void *k_new, const void *v_new,
@@ -401,6 +404,19 @@ typedef struct {
 
 ORTHROS_API orthros_status orthros_profile_begin(void);
 ORTHROS_API int orthros_profile_end(orthros_kernel_time *out, int max_entries);
+
+/*
+ * Self-test of the failure path (no counterpart in the paper): launches one
+ * small kernel whose only wait is on an mbarrier that nothing arrives on,
+ * bounded by limit_cycles SM clock cycles (1 .. about 4e9). The wait runs out,
+ * the kernel raises ORTHROS_DEV_TIMEOUT in the workspace's status word and
+ * returns; orthros_check(workspace, ...) then reports ORTHROS_ETIMEOUT. Every
+ * kernel of the library that waits on a barrier uses the same bounded wait
+ * (with a limit of about 2 s), so a stalled pipeline ends with this status
+ * instead of a hang. workspace: at least 256 bytes, 256-byte aligned.
+ */
+ORTHROS_API orthros_status orthros_selftest_wait_timeout(long long limit_cycles, void *workspace,
+                                                         size_t workspace_bytes, orthros_stream_t stream);
 
 /* Static English name of a status code. */
 ORTHROS_API const char *orthros_status_string(orthros_status s);

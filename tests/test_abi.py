@@ -142,6 +142,12 @@ def test_merge_host_checks(lib, args, code):
     assert ola.orthros_last_error() != ""
 
 
+def test_selftest_host_checks(lib):
+    assert lib.orthros_selftest_wait_timeout(0, 1 << 12, 256, None) == 1  # limit must be >= 1
+    assert lib.orthros_selftest_wait_timeout(1000, None, 256, None) == 4  # no workspace
+    assert lib.orthros_selftest_wait_timeout(1000, (1 << 12) + 16, 256, None) == 1  # alignment
+
+
 def test_decode_host_checks(lib):
     rc = lib.orthros_decode(1 << 12, None, 1 << 12, 1 << 12, 1 << 12, 1 << 12, 1 << 12, 0, 64, 4, 1 << 12,
                             1 << 12, 1 << 12, 1 << 12, 1 << 12, 2, 4, 2, 128, 16, 0.1, 0,

@@ -186,3 +186,23 @@ def test_projection_bad_page():
     rc, bits = ola.orthros_check(ws)
     assert rc == 5 and bits & DEV_BAD_PAGE, (rc, bits)
     assert torch.equal(kc[1, :2].cpu(), out[2][:2].cpu())  # the rows with a page were written
+
+
+def test_bounded_wait_runs_out_and_reports_a_timeout():
+    """The failure path of every TMA / tensor-core kernel: a wait on a barrier
+    that nothing arms runs out (here after 1e5 SM cycles), the kernel raises
+    the timeout bit and returns, and the context stays usable."""
+    import time
+
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    ola.orthros_selftest_wait_timeout(100_000, ws)
+    rc, bits = ola.orthros_check(ws)
+    elapsed = time.perf_counter() - t0
+    assert rc == 6 and bits == 0x10, (rc, bits)  # ORTHROS_ETIMEOUT, ORTHROS_DEV_TIMEOUT only
+    assert elapsed < 1.0, elapsed  # the other threads left on the abort flag, not on their own 2 s limit
+    # the context still works: a normal call afterwards succeeds
+    wl = W.small_prefill(1, 64, 2, 2, 128, 16, seed=13)
+    _, ws2 = _prefill(wl)
+    assert ola.orthros_check(ws2) == (0, 0)

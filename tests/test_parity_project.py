@@ -85,6 +85,8 @@ SMALL = [
     W.ProjectionWorkload("no_base", 0, 9, 128, 4, 4, 64, seed=5),
     W.ProjectionWorkload("short_tile_edge", 33, 31, 320, 4, 2, 64, seed=6),  # 64 rows: the 64-row x slices
     W.ProjectionWorkload("one_full_tile", 40, 41, 256, 4, 2, 128, seed=7),   # 81 rows: 128-row x slices
+    W.ProjectionWorkload("ragged_columns", 6, 6, 192, 3, 1, 64, seed=8),    # 320 columns: a half-empty last tile
+    W.ProjectionWorkload("one_row", 1, 0, 4096, 4, 1, 128, seed=10),
 ]
 
 
