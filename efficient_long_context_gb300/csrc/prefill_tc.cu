@@ -70,6 +70,7 @@ template <int D> struct Cfg {
 struct Slot {
     int kind;  // 0 base positions, 1 output rows, -1 empty
     int b, h, row0, n;
+    int qrow;  // first row of the raw query tile in q (or q_out) when its rows are contiguous there, else -1
 };
 
 // Band of a slot in key-tile units: [kt_lo, kt_hi]; lo_max = latest window
@@ -161,6 +162,10 @@ __device__ void decode_unit(const TcParams &p, int u, Slot &s0, Slot &s1) {
     s1.h = h1;
     s1.row0 = rowbase + blk1 * kRowsPerTile;
     s1.n = blk1 < nblk ? min(kRowsPerTile, rows - blk1 * kRowsPerTile) : 0;
+    // base rows are contiguous in q, output rows in q_out; output rows that
+    // read q at their positions are checked for contiguity by make_desc
+    for (Slot *S : {&s0, &s1})
+        S->qrow = S->kind == 0 ? S->b * p.Tq + S->row0 : (S->kind == 1 && p.q_out ? S->row0 : -1);
 }
 
 __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
@@ -217,7 +222,7 @@ __device__ void make_desc(const TcParams &p, int u, int lane, UnitDesc &D) {
     D.n_it = 0;
     if (D.end) {
         for (int s = 0; s < 2; ++s) {
-            D.sl[s] = Slot{-1, 0, 0, 0, 0};
+            D.sl[s] = Slot{-1, 0, 0, 0, 0, -1};
             D.bd[s] = Band{1, 0, 0, 0, -1};
         }
         return;
@@ -230,18 +235,26 @@ __device__ void make_desc(const TcParams &p, int u, int lane, UnitDesc &D) {
             tmin = S.row0 + p.q_off;
             tmax = S.row0 + S.n - 1 + p.q_off;
         } else if (S.kind == 1) {
+            // output rows at consecutive positions (an answer span, every position)
+            // have their raw queries contiguous in q: one TMA tile instead of a gather
+            const int t_first = p.out_positions[S.row0];
+            bool contig = !p.q_out;
             for (int r = lane; r < S.n; r += 32) {
                 int te;
-                if (out_row_position(p, S.row0 + r, te)) {
+                const bool ok = out_row_position(p, S.row0 + r, te);
+                if (ok) {
                     tmin = min(tmin, te);
                     tmax = max(tmax, te);
                 }
+                contig = contig && ok && p.out_positions[S.row0 + r] == t_first + r;
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
                 tmin = min(tmin, __shfl_xor_sync(0xffffffffu, tmin, o));
                 tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
             }
+            contig = __all_sync(0xffffffffu, contig);
+            if (contig) D.sl[s].qrow = S.b * p.Tq + (t_first - p.q_off);
         }
         D.bd[s] = band_of(p, S, tmin, tmax);
     }
@@ -314,11 +327,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = mt.tmem_base;
 
-    // Query tiles whose rows are contiguous (base positions; output rows with
-    // their own q_out) arrive by TMA as raw bf16 and are turned into affined
-    // fp16 in place; output rows that read q at their positions are gathered
-    // by the softmax threads.
-    auto q_by_tma = [&](const Slot &S) { return S.kind == 0 || (S.kind == 1 && p.q_out != nullptr); };
+    // Query tiles whose rows are contiguous in q or q_out (base positions;
+    // output rows with their own q_out or at consecutive positions) arrive by
+    // TMA as raw bf16 and are turned into affined fp16 in place; other output
+    // rows are gathered by the softmax threads.
 
     if (warp == kProducerWarp) {
         // ---------------- producer: unit descriptors, then TMA loads ----------------
@@ -330,21 +342,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         // epilogue to release the query buffers.
         uint32_t gk = 0;            // K/V iterations issued (all units so far)
         uint32_t nq[2] = {0, 0};    // per slot: units whose query phase was armed
-        bool alive = true;
-        for (int i = 0; alive; ++i) {
+        // Descriptors run one unit ahead of the loads, so the other roles never
+        // wait for the next unit's counter fetch and position reads.
+        auto next_desc = [&](UnitDesc &ud) {
             int u = 0;
             if (lane == 0) u = atomicAdd(p.unit_counter, 1);
             u = __shfl_sync(0xffffffffu, u, 0);
-            UnitDesc dsc;
-            make_desc(p, u < total_units ? u : -1, lane, dsc);
+            make_desc(p, u < total_units ? u : -1, lane, ud);
+        };
+        auto publish = [&](int i, const UnitDesc &ud) -> bool {
             const int r = i % kDescRing;
-            if (i >= kDescRing && !mbar_wait_warp(&mt.u_empty[r], ((i / kDescRing) - 1) & 1, abort, p.status)) break;
+            if (i >= kDescRing && !mbar_wait_warp(&mt.u_empty[r], ((i / kDescRing) - 1) & 1, abort, p.status))
+                return false;
             if (lane == 0) {
-                mt.desc[r] = dsc;
+                mt.desc[r] = ud;
                 mbar_arrive(&mt.u_full[r]);  // releases the descriptor to the other roles
             }
             __syncwarp();
-            if (dsc.end) break;
+            return true;
+        };
+        UnitDesc dsc;
+        next_desc(dsc);
+        bool alive = publish(0, dsc);
+        for (int i = 0; alive && !dsc.end; ++i) {
+            UnitDesc nxt;
+            next_desc(nxt);
+            if (!publish(i + 1, nxt)) break;
             if (lane == 0) {
                 const int kvh = dsc.sl[0].h / (p.Hq / p.Hkv);
                 const int bseq = dsc.sl[0].b;
@@ -370,27 +393,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (i >= 1 && !mbar_wait(&mt.q_free[s], (i - 1) & 1, abort, p.status)) return false;
                     const Slot &S = dsc.sl[s];
                     nq[s] = i + 1;
-                    if (S.kind >= 0 && q_by_tma(S)) {
+                    if (S.qrow >= 0) {
                         mbar_arrive_expect_tx(&mt.q_full[s], C::kTileBytes);
-                        const int row = S.kind == 0 ? S.b * p.Tq + S.row0 : S.row0;
                         for (int j = 0; j < C::kSub; ++j)
                             tma_load_3d(smem + C::kQ0 + s * C::kTileBytes + j * (kRowsPerTile * 128),
-                                        S.kind == 0 ? &tm_q : &tm_qo, &mt.q_full[s], 64 * j, S.h, row);
+                                        S.kind == 1 && p.q_out ? &tm_qo : &tm_q, &mt.q_full[s], 64 * j, S.h, S.qrow);
                     } else {
                         mbar_arrive(&mt.q_full[s]);  // nothing to copy (gathered rows or an empty slot)
                     }
                     return true;
                 };
-                const int pre = min(dsc.n_it, 2);
-                bool ok = true;
-                for (int it = 0; ok && it < pre; ++it) ok = issue_kv(it);
+                // the first tile's key/value loads need only stages the previous
+                // unit has released; the query tiles wait for its epilogue
+                bool ok = dsc.n_it == 0 || issue_kv(0);
                 ok = ok && issue_q(0);
                 ok = ok && issue_q(1);
-                for (int it = pre; ok && it < dsc.n_it; ++it) ok = issue_kv(it);
+                for (int it = 1; ok && it < dsc.n_it; ++it) ok = issue_kv(it);
                 gk += dsc.n_it;
                 alive = ok;
             }
             alive = __shfl_sync(0xffffffffu, alive, 0);
+            dsc = nxt;
         }
         if (lane == 0) {
             // nothing may be in flight when the CTA leaves: wait (bounded) for the
@@ -441,11 +464,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int kt_min = dr.kt_min, n_it = dr.n_it;
                 mbar_arrive(&mt.u_empty[r]);
                 if (end) break;
-                // both query tiles of this unit staged (this also orders the unit's
-                // first products after the previous unit's epilogue)
+                // each slot's query tile staged before its first product (this also
+                // orders the product after that slot's previous epilogue)
                 if (!(ok = mbar_wait(&mt.q_ready[0], i & 1, abort, p.status))) break;
-                if (!(ok = mbar_wait(&mt.q_ready[1], i & 1, abort, p.status))) break;
-                if (n_it == 0) continue;
+                if (n_it == 0) {
+                    if (!(ok = mbar_wait(&mt.q_ready[1], i & 1, abort, p.status))) break;
+                    continue;
+                }
                 if (!(ok = mbar_wait(&mt.k_full[g % kNumK], (g / kNumK) & 1, abort, p.status))) break;
                 tc_fence_after();
                 const uint64_t dk0 = dk + (uint64_t)((g % kNumK) * kTileU);
@@ -453,6 +478,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ORTHROS_ISSUE_S(d_s0, dq, dk0)
                     tc_commit(&mt.s_full[0]);
                 }
+                if (!(ok = mbar_wait(&mt.q_ready[1], i & 1, abort, p.status))) break;
+                tc_fence_after();
                 if (kt_min >= lo1 && kt_min <= hi1) {
                     ORTHROS_ISSUE_S(d_s1, dq + kTileU, dk0)
                     tc_commit(&mt.s_full[1]);
@@ -477,6 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_fence_after();
                         ORTHROS_ISSUE_PV(d_o0, d_s0, vdesc, o_init0)
                         o_init0 = 1;
+                        if (kt == hi0) tc_commit(&mt.o_full[0]);  // slot 0's epilogue may start
                     }
                     if (more) {
                         if (!(ok = mbar_wait(&mt.k_full[skn], ((gi + 1) / kNumK) & 1, abort, p.status))) break;
@@ -493,6 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_fence_after();
                         ORTHROS_ISSUE_PV(d_o1, d_s1, vdesc, o_init1)
                         o_init1 = 1;
+                        if (kt == hi1) tc_commit(&mt.o_full[1]);
                     }
                     if (more) {
                         if (kt + 1 >= lo1 && kt + 1 <= hi1) {
@@ -504,8 +533,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_commit(&mt.v_empty[sv]);
                 }
                 if (!ok) break;
-                if (lo0 <= hi0) tc_commit(&mt.o_full[0]);
-                if (lo1 <= hi1) tc_commit(&mt.o_full[1]);
                 g += n_it;
             }
 #undef ORTHROS_ISSUE_S
@@ -555,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 my_bad = !my_valid;
                 if (my_bad && hh == 0) set_status(p.status, ORTHROS_DEV_BAD_POSITION);
             }
-            const bool tma = S.kind >= 0 && q_by_tma(S);
+            const bool tma = S.qrow >= 0;
             if (!mbar_wait_warp(&mt.q_full[s], i & 1, abort, p.status)) break;
             if (S.kind >= 0) {
                 constexpr int kHalfChunks = D / 16;  // 16-byte chunks per half row
