@@ -701,6 +701,66 @@ def bench_project(args, dist, dev, stream, peaks, ola, torch, W):
     return res
 
 
+def bench_seqpar(args, dist, dev, stream, ola, torch, W, pre, world=8):
+    """Sequence-parallel split of the 128K prefill over `world` ranks, each
+    rank's arithmetic timed on this GPU: its orthros_prefill_shard call
+    (band rows of its chunk over [halo ; chunk], the output row's partial over
+    its chunk) and the owner's orthros_merge_partials. The halo and partial
+    transfers between GPUs are not part of it (one GPU here)."""
+    from efficient_long_context_gb300 import seqpar as SP
+
+    wl = pre["wl"]
+    inputs = pre["inputs"]
+    q, k, v = (inputs[n].to(dev) for n in ("q", "k", "v"))
+    aff = [inputs[n].to(dev) for n in ("alpha_base", "beta_base", "alpha_out", "beta_out")]
+    indptr, pos_all = inputs["out_indptr"], inputs["out_positions"]
+    B, T = wl.B, wl.T
+    pos = pos_all.long()
+    seq = torch.repeat_interleave(torch.arange(B), (indptr[1:] - indptr[:-1]).long())
+    q_rows_all = q[seq.to(dev), pos.to(dev)]
+    rank_ms, parts = [], []
+    for r in range(world):
+        start, end = SP.chunk_bounds(T, world, r)
+        H = SP.halo_len(T, wl.window, world, r)
+        k_ext, v_ext = k[:, start - H:end].contiguous(), v[:, start - H:end].contiguous()
+        qc = q[:, start:end].contiguous()
+        sel, r_indptr, r_pos = SP.shard_rows(pos, seq, B, start, H)
+        q_rows = q_rows_all[sel.to(dev)].contiguous()
+        r_pos = r_pos.to(dev)
+        ws = torch.empty(ola.orthros_prefill_shard_workspace_size(B, end - start, H + end - start, wl.Hq, wl.Hkv,
+                                                                  wl.d, len(sel), wl.window), dtype=torch.uint8,
+                         device=dev)
+        out = None
+
+        def call(_=0):
+            nonlocal out
+            out = ola.orthros_prefill_shard(qc, k_ext, v_ext, *aff, r_indptr, r_pos, wl.window, wl.scale,
+                                            q_rows=q_rows, out=out, workspace=ws, stream=stream)
+
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        ms, _ = _timed(ola, torch, dist, stream, call, 5)
+        rank_ms.append(ms / 5)
+        parts.append((out[2].clone(), out[3].clone()))
+    o_parts = torch.stack([p[0] for p in parts])
+    l_parts = torch.stack([p[1] for p in parts])
+    merged = None
+
+    def merge(_=0):
+        nonlocal merged
+        merged = ola.orthros_merge_partials(o_parts, l_parts, wl.dtype, out=merged, stream=stream)
+
+    for _ in range(3):
+        merge()
+    torch.cuda.synchronize()
+    ms_m, _ = _timed(ola, torch, dist, stream, merge, 10)
+    return {"workload": wl.name, "world": world, "rank_ms": rank_ms, "max_rank_ms": max(rank_ms),
+            "merge_ms": ms_m / 10, "single_gpu_step_ms": pre["ms_step"],
+            "projected_speedup": pre["ms_step"] / (max(rank_ms) + ms_m / 10),
+            "note": "ranks emulated one after the other on one GPU; halo and partial transfers not timed"}
+
+
 def run_ours(args, dist):
     import torch
 
@@ -720,6 +780,9 @@ def run_ours(args, dist):
     if args.only in ("all", "prefill"):
         pre = bench_prefill(args, dist, dev, stream, peaks, ola, torch, W, headline_workload(args, W),
                             e2e=args.only == "all")
+    seqpar = None
+    if args.only == "all" and pre is not None and pre["wl"].name == W.PREFILL_128K.name:
+        seqpar = bench_seqpar(args, dist, dev, stream, ola, torch, W, pre)
     if args.only == "all":
         for key, wl in (("pt", W.PT_2K), ("sft", W.SFT_8K)):
             shapes[key] = bench_prefill(args, dist, dev, stream, peaks, ola, torch, W, wl)
@@ -777,6 +840,7 @@ def run_ours(args, dist):
         "kernels": {n: {"launches": c, "total_ms": t} for n, (c, t) in pre["prof"].items()},
         "gpu_launches": sum(n for n, _ in pre["prof"].values()),
         "e2e": pre.get("e2e"),
+        "seqpar": seqpar,
         "pt": shape_lines.get("pt"),
         "sft": shape_lines.get("sft"),
         "decode": dec,
