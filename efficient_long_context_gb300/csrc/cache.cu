@@ -97,15 +97,17 @@ __global__ void prefill_cache_fill_kernel(const uint4 *__restrict__ k, const uin
 }
 
 // One pass over the bf16 keys/values of a prefill: keys -> fp16 copy (exact in
-// the fp16 range; out-of-range magnitudes raise ORTHROS_DEV_FP16_RANGE), and,
-// when a block table is given, both tensors -> their cache pages.
+// the fp16 range) while recording the largest |k| of the call, and, when a
+// block table is given, both tensors -> their cache pages. Also zeroes the
+// tile kernel's n_zero-word bitmap of row blocks to compute again.
 __global__ void prefill_prep_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
                                     uint4 *__restrict__ k16, uint4 *__restrict__ k_cache,
                                     uint4 *__restrict__ v_cache, const int32_t *__restrict__ block_table, int B,
                                     int T, int vec_per_tok, int max_pages, int page_size, int num_pages,
-                                    uint32_t *status) {
+                                    uint32_t *status, unsigned *kmax_bits, uint32_t *zero_words, int n_zero) {
     const long long n = (long long)B * T * vec_per_tok;
-    bool over = false;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_zero; i += gridDim.x * blockDim.x) zero_words[i] = 0;
+    float amax = 0.f;
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
          i += (long long)gridDim.x * blockDim.x) {
         const uint4 kx = k[i];
@@ -115,7 +117,7 @@ __global__ void prefill_prep_kernel(const uint4 *__restrict__ k, const uint4 *__
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
-            over |= fabsf(lo) > 65504.f || fabsf(hi) > 65504.f;
+            amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
             const __half2 hv = __floats2half2_rn(lo, hi);
             hw[e] = *reinterpret_cast<const uint32_t *>(&hv);
         }
@@ -135,7 +137,47 @@ __global__ void prefill_prep_kernel(const uint4 *__restrict__ k, const uint4 *__
             v_cache[dst] = v[i];
         }
     }
-    if (over) set_status(status, ORTHROS_DEV_FP16_RANGE);
+    // largest |k| of the call (non-negative floats order like their bit patterns)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if ((threadIdx.x & 31) == 0 && amax > 0.f) atomicMax(kmax_bits, __float_as_uint(amax));
+}
+
+// Keys beyond the fp16 range. s = 0 unless the largest |k| of the call
+// exceeds 65504; then s is the smallest shift that brings it below 2^15, and
+// the fp16 copy is rewritten as k * 2^-s (a power of two: exact for every key
+// whose scaled magnitude stays a normal fp16 number). Either way the four query
+// affines are copied scaled by 2^s (exact), so the tile kernel's staged
+// queries are qa * 2^s and its products are the logits unchanged.
+__global__ void prefill_key_rescale_kernel(const uint4 *__restrict__ k, uint4 *__restrict__ k16, long long n,
+                                           const unsigned *__restrict__ kmax_bits, AffineSet src,
+                                           float *__restrict__ aff, int n_aff) {
+    const unsigned bits = *kmax_bits;
+    const float kmax = __uint_as_float(bits);
+    // in range, or inf / NaN (not scalable): s = 0
+    const int sft = (kmax > 65504.f && bits < 0x7f800000u) ? (int)((bits >> 23) & 0xff) - 127 - 14 : 0;
+    const float up = __uint_as_float((uint32_t)(127 + sft) << 23);
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    for (long long i = tid; i < 4LL * n_aff; i += stride) {
+        const float *sp = src.p[i / n_aff];
+        aff[i] = sp ? sp[i % n_aff] * up : 0.f;
+    }
+    if (sft == 0) return;  // the common case
+    const float down = __uint_as_float((uint32_t)(127 - sft) << 23);
+    for (long long i = tid; i < n; i += stride) {
+        const uint4 kx = k[i];
+        const uint32_t *w = reinterpret_cast<const uint32_t *>(&kx);
+        uint4 h;
+        uint32_t *hw = reinterpret_cast<uint32_t *>(&h);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const __half2 hv =
+                __floats2half2_rn(__uint_as_float(w[e] << 16) * down, __uint_as_float(w[e] & 0xffff0000u) * down);
+            hw[e] = *reinterpret_cast<const uint32_t *>(&hv);
+        }
+        k16[i] = h;
+    }
 }
 
 int grid_for(long long n, int threads, int per_sm) {
@@ -150,12 +192,22 @@ int grid_for(long long n, int threads, int per_sm) {
 
 cudaError_t launch_prefill_prep(const void *k, const void *v, void *k16, void *k_cache, void *v_cache,
                                 const int32_t *block_table, int B, int T, int Hkv, int d, int max_pages,
-                                int page_size, int num_pages, uint32_t *status, cudaStream_t stream) {
+                                int page_size, int num_pages, uint32_t *status, unsigned *kmax_bits,
+                                uint32_t *zero_words, int n_zero, cudaStream_t stream) {
     const long long n = (long long)B * T * Hkv * d * 2 / 16;
-    if (n == 0) return cudaSuccess;
-    prefill_prep_kernel<<<grid_for(n, 256, 8), 256, 0, stream>>>(
+    if (n == 0 && n_zero == 0) return cudaSuccess;
+    prefill_prep_kernel<<<grid_for(n > n_zero ? n : n_zero, 256, 8), 256, 0, stream>>>(
         (const uint4 *)k, (const uint4 *)v, (uint4 *)k16, (uint4 *)k_cache, (uint4 *)v_cache, block_table, B, T,
-        Hkv * d * 2 / 16, max_pages, page_size, num_pages, status);
+        Hkv * d * 2 / 16, max_pages, page_size, num_pages, status, kmax_bits, zero_words, n_zero);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_key_rescale(const void *k, void *k16, int B, int T, int Hkv, int d,
+                                       const unsigned *kmax_bits, AffineSet src, float *aff, int n_aff,
+                                       cudaStream_t stream) {
+    const long long n = (long long)B * T * Hkv * d * 2 / 16;
+    prefill_key_rescale_kernel<<<grid_for(n > 4LL * n_aff ? n : 4LL * n_aff, 256, 8), 256, 0, stream>>>(
+        (const uint4 *)k, (uint4 *)k16, n, kmax_bits, src, aff, n_aff);
     return cudaGetLastError();
 }
 

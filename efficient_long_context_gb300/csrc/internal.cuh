@@ -124,6 +124,16 @@ struct TcParams {
     float *lse_out;
     uint32_t *status;
     int *unit_counter;  // zero before the launch: the next work unit to take (persistent CTAs)
+    // Second launch (rows whose staged query left the fp16 range): row blocks
+    // are numbered base blocks first (B * Hq * base_nblk), then the output-row
+    // blocks of the sequences whose output rows take this kernel
+    // (out_blk_indptr[b] of them before sequence b, device [B+1]); n_blocks in
+    // all. redo_bits: bitmap of n_blocks bits, zero before the first launch;
+    // redo_list: B * Hq * Tq + n_out * Hq ints of scratch.
+    const int32_t *out_blk_indptr;
+    int n_blocks;
+    uint32_t *redo_bits;
+    int *redo_list;
 };
 // Work units of one (sequence, kv head) for nblk row blocks and group size g.
 int tc_units_per_kv(int nblk, int g);
@@ -280,10 +290,24 @@ cudaError_t launch_decode_append(const void *k_new, const void *v_new, void *k_c
                                  int d, int max_pages, int page_size, int num_pages, int elem_bytes,
                                  uint32_t *status, cudaStream_t stream);
 // fp16 copy of the keys for the tensor-core prefill, optionally fused with the
-// paged cache fill (k_cache == nullptr skips it).
+// paged cache fill (k_cache == nullptr skips it); records the largest |k| in
+// *kmax_bits (atomic max of the float bits; zeroed by the caller).
 cudaError_t launch_prefill_prep(const void *k, const void *v, void *k16, void *k_cache, void *v_cache,
                                 const int32_t *block_table, int B, int T, int Hkv, int d, int max_pages,
-                                int page_size, int num_pages, uint32_t *status, cudaStream_t stream);
+                                int page_size, int num_pages, uint32_t *status, unsigned *kmax_bits,
+                                uint32_t *zero_words, int n_zero, cudaStream_t stream);
+// The four query affines (alpha_base, beta_base, alpha_out, beta_out; a null
+// pointer gives zeros), each of n_aff floats, as consecutive scaled copies in
+// aff.
+struct AffineSet {
+    const float *p[4];
+};
+// s = 0 unless the largest |k| (*kmax_bits) exceeds the fp16 range; then the
+// fp16 keys are rewritten as k * 2^-s. The affines are copied to aff scaled by
+// 2^s, so that queries staged with them meet the keys at unchanged logits.
+cudaError_t launch_prefill_key_rescale(const void *k, void *k16, int B, int T, int Hkv, int d,
+                                       const unsigned *kmax_bits, AffineSet src, float *aff, int n_aff,
+                                       cudaStream_t stream);
 cudaError_t launch_prefill_cache_fill(const void *k, const void *v, void *k_cache, void *v_cache,
                                       const int32_t *block_table, int B, int T, int Hkv, int d,
                                       int max_pages, int page_size, int num_pages, int elem_bytes,

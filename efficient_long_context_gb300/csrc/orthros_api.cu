@@ -74,22 +74,40 @@ int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 
 // Workspace regions of orthros_prefill.
 struct PrefillLayout {
-    size_t blob_off, k16_off, part_off, total;
+    size_t blob_off, k16_off, part_off, redo_bits_off, redo_list_off, aff_off, total;
     int max_groups;
     long long part_slots;
+    int redo_cap;  // row blocks of the tile kernel a call can have (bound)
 };
 
-PrefillLayout prefill_layout(int B, int T, int Hkv, int d, int n_out, orthros_dtype dtype) {
+PrefillLayout prefill_layout(int B, int T, int Hq, int Hkv, int d, int n_out, orthros_dtype dtype) {
     PrefillLayout L{};
     size_t at = kStatusBytes;
     L.max_groups = dtype == ORTHROS_BF16 ? (int)std::min<long long>((long long)n_out, 16LL * B) * Hkv : 0;
     L.part_slots = split_slots_bound(L.max_groups, T);
     L.blob_off = at;
-    at += align_up(sizeof(int32_t) * (size_t)(2 * (B + 1) + 3 * (size_t)L.max_groups), 256);
+    at += align_up(sizeof(int32_t) * (size_t)(3 * (B + 1) + 3 * (size_t)L.max_groups), 256);
     L.k16_off = at;
     if (dtype == ORTHROS_BF16) at += align_up((size_t)B * T * Hkv * d * 2, 256);
     L.part_off = at;
     at += align_up((size_t)L.part_slots * split_partial_bytes(1, 1, d), 256);
+    // the tile kernel's second launch: a bitmap over its row blocks (at most
+    // B * Hq * ceil(T / 128) base blocks and Hq * (ceil(n_out / 128) + B)
+    // output-row blocks, bounded generously below) and a list with one entry
+    // per log-sum-exp it scans
+    L.redo_bits_off = at;
+    L.redo_list_off = at;
+    if (dtype == ORTHROS_BF16) {
+        const long long cap =
+            (long long)Hq * ((long long)B * (ceil_div(T, 128) + 1) + ceil_div(n_out, 128) + 2LL * B);
+        L.redo_cap = (int)std::min<long long>(cap, 1LL << 30);
+        at += align_up(sizeof(uint32_t) * (size_t)((L.redo_cap + 31) / 32), 256);
+        L.redo_list_off = at;
+        at += align_up(sizeof(int32_t) * ((size_t)B * Hq * T + (size_t)n_out * Hq), 256);
+    }
+    // the tile kernel's copies of the four query affines (scaled with the keys)
+    L.aff_off = at;
+    if (dtype == ORTHROS_BF16) at += align_up(sizeof(float) * 4 * (size_t)Hq * d, 256);
     L.total = at;
     return L;
 }
@@ -254,7 +272,7 @@ orthros_status prefill_core(const void *q, const void *k, const void *v, const f
         if (!aligned16(k_cache) || !aligned16(v_cache))
             return fail(ORTHROS_EINVAL, "k_cache and v_cache must be 16-byte aligned");
     }
-    const PrefillLayout lay = prefill_layout(B, T, Hkv, d, n_out, dtype);
+    const PrefillLayout lay = prefill_layout(B, T, Hq, Hkv, d, n_out, dtype);
     if (!workspace || workspace_bytes < lay.total)
         return fail(ORTHROS_EWORKSPACE, "workspace needs %zu bytes, got %zu", lay.total,
                     workspace ? workspace_bytes : (size_t)0);
@@ -263,8 +281,9 @@ orthros_status prefill_core(const void *q, const void *k, const void *v, const f
 
     char *ws = static_cast<char *>(workspace);
     uint32_t *status = reinterpret_cast<uint32_t *>(ws);
-    // the status word and, next to it, the tile kernel's work-unit counter
-    cudaError_t e = cudaMemsetAsync(status, 0, 2 * sizeof(uint32_t), stream);
+    // the status word and, next to it, the tile kernel's work-unit counter, a
+    // spare word and the keys' largest magnitude
+    cudaError_t e = cudaMemsetAsync(status, 0, 4 * sizeof(uint32_t), stream);
     if (e != cudaSuccess) return cuda_fail(e, "status reset");
     if (rows == 0) return ORTHROS_OK;
 
@@ -273,13 +292,15 @@ orthros_status prefill_core(const void *q, const void *k, const void *v, const f
 
     // Plan (host): which sequences' output rows take the split-KV kernel, the
     // tile kernel's output-row units, and the split groups. One upload.
-    std::vector<int32_t> blob((size_t)2 * (B + 1), 0);
-    int n_cross_units = 0, n_groups = 0, rows_per_group = 0;
+    // blob: out_indptr, cross_unit_indptr, out_blk_indptr (B + 1 each), split groups
+    std::vector<int32_t> blob((size_t)3 * (B + 1), 0);
+    int n_cross_units = 0, n_groups = 0, rows_per_group = 0, n_out_blocks = 0;
     bool any_simt_out = false;
     std::copy(out_indptr, out_indptr + B + 1, blob.begin());
     for (int b = 0; b < B; ++b) {
         const int nb = out_indptr[b + 1] - out_indptr[b];
         blob[(size_t)B + 1 + b] = n_cross_units;
+        blob[(size_t)2 * (B + 1) + b] = n_out_blocks;
         if (nb == 0) continue;
         if (!tc) {
             any_simt_out = true;
@@ -296,14 +317,17 @@ orthros_status prefill_core(const void *q, const void *k, const void *v, const f
                 }
         } else {
             n_cross_units += Hkv * tc_units_per_kv(ceil_div(nb, 128), g);
+            n_out_blocks += Hq * ceil_div(nb, 128);
         }
     }
     blob[(size_t)2 * B + 1] = n_cross_units;
+    blob[(size_t)3 * B + 2] = n_out_blocks;
     if (n_groups > lay.max_groups) return fail(ORTHROS_EWORKSPACE, "internal: split groups exceed the workspace plan");
     int32_t *blob_dev = reinterpret_cast<int32_t *>(ws + lay.blob_off);
     const int32_t *indptr_dev = blob_dev;
     const int32_t *cross_indptr_dev = blob_dev + B + 1;
-    const int32_t *groups_dev = blob_dev + 2 * (B + 1);
+    const int32_t *out_blk_dev = blob_dev + 2 * (B + 1);
+    const int32_t *groups_dev = blob_dev + 3 * (B + 1);
     if (n_out > 0) {
         e = cudaMemcpyAsync(blob_dev, blob.data(), sizeof(int32_t) * blob.size(), cudaMemcpyHostToDevice, stream);
         if (e != cudaSuccess) return cuda_fail(e, "plan upload");
@@ -357,9 +381,18 @@ orthros_status prefill_core(const void *q, const void *k, const void *v, const f
     {
         ProfScope ps("prefill_prep", stream);
         e = launch_prefill_prep(k, v, k16, fill ? k_cache : nullptr, fill ? v_cache : nullptr, block_table, B, T, Hkv,
-                                d, max_pages, page_size, num_pages, status, stream);
+                                d, max_pages, page_size, num_pages, status, reinterpret_cast<unsigned *>(ws) + 3,
+                                reinterpret_cast<uint32_t *>(ws + lay.redo_bits_off), (lay.redo_cap + 31) / 32,
+                                stream);
     }
     if (e != cudaSuccess) return cuda_fail(e, "prep launch");
+    {
+        ProfScope ps("prefill_key_rescale", stream);
+        const AffineSet src{{alpha_base, beta_base, alpha_out, beta_out}};
+        e = launch_prefill_key_rescale(k, k16, B, T, Hkv, d, reinterpret_cast<const unsigned *>(ws) + 3, src,
+                                       reinterpret_cast<float *>(ws + lay.aff_off), Hq * d, stream);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "key rescale launch");
     const float log2e = 1.4426950408889634f;
     if (n_groups > 0) {
         SplitParams sp{};
@@ -403,10 +436,15 @@ orthros_status prefill_core(const void *q, const void *k, const void *v, const f
     TcParams tp{};
     tp.q = static_cast<const __nv_bfloat16 *>(q);
     tp.q_out = static_cast<const __nv_bfloat16 *>(q_out);
-    tp.alpha_base = alpha_base;
-    tp.beta_base = beta_base;
-    tp.alpha_out = alpha_out;
-    tp.beta_out = beta_out;
+    {
+        // the affines scaled with the keys (copies written by the rescale pass)
+        const float *aff = reinterpret_cast<const float *>(ws + lay.aff_off);
+        const size_t n_aff = (size_t)Hq * d;
+        tp.alpha_base = aff;
+        tp.beta_base = aff + n_aff;
+        tp.alpha_out = aff + 2 * n_aff;
+        tp.beta_out = aff + 3 * n_aff;
+    }
     tp.out_indptr = indptr_dev;
     tp.out_positions = out_positions;
     tp.cross_unit_indptr = cross_indptr_dev;
@@ -432,6 +470,11 @@ orthros_status prefill_core(const void *q, const void *k, const void *v, const f
     tp.lse_out = lse_out;
     tp.status = status;
     tp.unit_counter = reinterpret_cast<int *>(ws + sizeof(uint32_t));
+    tp.out_blk_indptr = out_blk_dev;
+    tp.n_blocks = B * Hq * tp.base_nblk + n_out_blocks;
+    tp.redo_bits = reinterpret_cast<uint32_t *>(ws + lay.redo_bits_off);
+    tp.redo_list = reinterpret_cast<int *>(ws + lay.redo_list_off);
+    if (tp.n_blocks > lay.redo_cap) return fail(ORTHROS_EWORKSPACE, "internal: row blocks exceed the workspace plan");
     {
         ProfScope ps("prefill_tc", stream);
         e = launch_prefill_tc(tp, k16, v, d, stream);
@@ -477,7 +520,7 @@ size_t orthros_prefill_workspace_size(int B, int T, int Hq, int Hkv, int d, int 
                                       orthros_dtype dtype) {
     if (T < 0 || n_out < 0) return 0;
     if (check_shapes(B, Hq, Hkv, d, window, 1.0f, dtype) != ORTHROS_OK) return 0;
-    return prefill_layout(B, T, Hkv, d, n_out, dtype).total;
+    return prefill_layout(B, T, Hq, Hkv, d, n_out, dtype).total;
 }
 
 orthros_status orthros_prefill(const void *q, const void *k, const void *v, const float *alpha_base,
@@ -499,7 +542,7 @@ size_t orthros_prefill_shard_workspace_size(int B, int Tq, int Tkv, int Hq, int 
                                             orthros_dtype dtype) {
     if (Tkv < 0 || Tq < 0 || Tq > Tkv || n_rows < 0 || dtype != ORTHROS_BF16) return 0;
     if (check_shapes(B, Hq, Hkv, d, window, 1.0f, dtype) != ORTHROS_OK) return 0;
-    return prefill_layout(B, Tkv, Hkv, d, n_rows, dtype).total;
+    return prefill_layout(B, Tkv, Hq, Hkv, d, n_rows, dtype).total;
 }
 
 orthros_status orthros_prefill_shard(const void *q, const void *k, const void *v, const float *alpha_base,

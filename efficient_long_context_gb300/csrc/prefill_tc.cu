@@ -67,6 +67,9 @@ template <int D> struct Cfg {
     static constexpr int kTmemO = 256;                                  // first O column
 };
 
+// 2^e for an integer e in [-126, 127] (exact).
+__device__ __forceinline__ float exp2_int(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
+
 struct Slot {
     int kind;  // 0 base positions, 1 output rows, -1 empty
     int b, h, row0, n;
@@ -99,9 +102,11 @@ struct Meta {
     uint64_t q_free[2];   // per slot: the unit is done with its query tile (epilogue stored)
     uint64_t os_bar[2];   // per slot: normalised output tile staged for the TMA store
     uint64_t xm_bar[2], lx_bar[2];  // per slot: row maxima / row sums exchanged between column halves
+                                    // (xm_bar completes one phase per s_full phase)
     uint64_t u_full[kDescRing], u_empty[kDescRing];  // unit descriptor ring
     uint32_t tmem_base;
     int abort;
+    int n_redo;  // second launch: row blocks this CTA lists to compute again
     UnitDesc desc[kDescRing];
     __nv_bfloat16 xmax[2][2][kRowsPerTile];  // [slot][half][row] tile maxima (a shared shift; rounding is harmless)
 };
@@ -168,6 +173,39 @@ __device__ void decode_unit(const TcParams &p, int u, Slot &s0, Slot &s1) {
         S->qrow = S->kind == 0 ? S->b * p.Tq + S->row0 : (S->kind == 1 && p.q_out ? S->row0 : -1);
 }
 
+// Second launch: row block idx as slot 0 of a unit. Blocks [0, B Hq nblk) are
+// base-position blocks (b, h, blk); the rest are output-row blocks of the
+// sequences whose output rows take this kernel, out_blk_indptr[b] of them
+// before sequence b, head-major within a sequence.
+__device__ void decode_block(const TcParams &p, int idx, Slot &S) {
+    const int nb_base = p.B * p.Hq * p.base_nblk;
+    if (idx < nb_base) {
+        const int b = idx / (p.Hq * p.base_nblk), rem = idx % (p.Hq * p.base_nblk);
+        S.kind = 0;
+        S.b = b;
+        S.h = rem / p.base_nblk;
+        S.row0 = (rem % p.base_nblk) * kRowsPerTile;
+        S.n = min(kRowsPerTile, p.Tq - S.row0);
+        S.qrow = b * p.Tq + S.row0;
+        return;
+    }
+    const int o = idx - nb_base;
+    int lo = 0, hi = p.B - 1;  // last b with out_blk_indptr[b] <= o
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.out_blk_indptr[mid] <= o) lo = mid; else hi = mid - 1;
+    }
+    const int b = lo, local = o - p.out_blk_indptr[b];
+    const int rows = p.out_indptr[b + 1] - p.out_indptr[b];
+    const int nbb = (rows + kRowsPerTile - 1) / kRowsPerTile;
+    S.kind = 1;
+    S.b = b;
+    S.h = local / nbb;
+    S.row0 = p.out_indptr[b] + (local % nbb) * kRowsPerTile;
+    S.n = min(kRowsPerTile, p.out_indptr[b + 1] - S.row0);
+    S.qrow = p.q_out ? S.row0 : -1;
+}
+
 __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
     asm volatile(""
                  : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
@@ -216,7 +254,7 @@ __device__ __forceinline__ Band band_of(const TcParams &p, const Slot &S, int tm
 // Descriptor of unit u (u < 0: the end marker). Called by all 32 lanes of the
 // producer warp, which read an output-row slot's positions together; every
 // lane returns the same descriptor.
-__device__ void make_desc(const TcParams &p, int u, int lane, UnitDesc &D) {
+__device__ void make_desc(const TcParams &p, int u, int lane, UnitDesc &D, bool block_unit) {
     D.end = u < 0;
     D.kt_min = 0;
     D.n_it = 0;
@@ -227,7 +265,12 @@ __device__ void make_desc(const TcParams &p, int u, int lane, UnitDesc &D) {
         }
         return;
     }
-    decode_unit(p, u, D.sl[0], D.sl[1]);
+    if (block_unit) {
+        decode_block(p, u, D.sl[0]);
+        D.sl[1] = Slot{-1, 0, 0, 0, 0, -1};
+    } else {
+        decode_unit(p, u, D.sl[0], D.sl[1]);
+    }
     for (int s = 0; s < 2; ++s) {
         const Slot S = D.sl[s];
         int tmin = 0x7fffffff, tmax = -1;
@@ -267,7 +310,12 @@ __device__ void make_desc(const TcParams &p, int u, int lane, UnitDesc &D) {
     }
 }
 
-template <int D>
+// kRedo: the second launch. Each CTA scans a slice of the log-sum-exps for
+// rows that came out non-finite although they have keys (a staged query value
+// past the fp16 range gives such rows) and computes their row blocks again,
+// every row staged with its own power-of-two shift and the inverse shift on
+// its logit scale. Without such rows every CTA leaves after the scan.
+template <int D, bool kRedo>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qo,
@@ -281,6 +329,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = tid & 31;
     volatile int *abort = &mt.abort;
     const int total_units = p.n_cross_units + p.n_base_units;
+    // The second launch is a programmatic dependent launch: its CTAs may start
+    // as the first launch's leave, and wait here until all of it has finished.
+    if constexpr (kRedo) asm volatile("griddepcontrol.wait;" ::: "memory");
+    else asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (tid == 0) {
         for (int i = 0; i < kNumK; ++i) {
@@ -308,6 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(&mt.mma_done, 1);
         mt.abort = 0;
+        mt.n_redo = 0;
         fence_mbar_init();
     }
     if (warp == kProducerWarp && lane == 0) {
@@ -318,6 +371,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tm_ob);
     }
     __syncthreads();
+    // Second launch: this CTA scans its slice of the log-sum-exps (lse_base,
+    // then lse_out, as one flat range; coalesced) for rows that have keys but a
+    // non-finite value. The first CTA to find a row block claims it in the
+    // bitmap redo_bits (zeroed before the first launch) and lists it in its own
+    // part of redo_list (one entry per scanned value at most), so every block is
+    // computed again once, by the CTA that found it.
+    long long redo_lo = 0;
+    if constexpr (kRedo) {
+        const long long fb = (long long)p.B * p.Hq * p.Tq, ft = fb + (long long)p.n_out * p.Hq;
+        const long long per = (ft + gridDim.x - 1) / gridDim.x;
+        redo_lo = min((long long)blockIdx.x * per, ft);
+        const long long redo_hi = min(redo_lo + per, ft);
+        const int nb_base = p.B * p.Hq * p.base_nblk;
+        auto claim = [&](long long f) {
+            int idx;
+            if (f < fb) {
+                idx = (int)(f / p.Tq) * p.base_nblk + (int)(f % p.Tq) / kRowsPerTile;
+            } else {
+                const int row = (int)((f - fb) / p.Hq), h = (int)((f - fb) % p.Hq);
+                int te;
+                if (!out_row_position(p, row, te) || te < p.key_lo) return;  // NaN by design / no keys
+                int lo = 0, hi = p.B - 1;  // the row's sequence: last b with out_indptr[b] <= row
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (p.out_indptr[mid] <= row) lo = mid; else hi = mid - 1;
+                }
+                const int b = lo;
+                if (p.out_blk_indptr[b + 1] == p.out_blk_indptr[b]) return;  // rows of the split-KV kernel
+                const int nbb = (p.out_indptr[b + 1] - p.out_indptr[b] + kRowsPerTile - 1) / kRowsPerTile;
+                idx = nb_base + p.out_blk_indptr[b] + h * nbb + (row - p.out_indptr[b]) / kRowsPerTile;
+            }
+            const uint32_t m = 1u << (idx & 31);
+            if (!(atomicOr(&p.redo_bits[idx >> 5], m) & m)) p.redo_list[redo_lo + atomicAdd(&mt.n_redo, 1)] = idx;
+        };
+        constexpr int kBatch = 8;  // loads in flight per thread
+        for (long long f0 = redo_lo + tid; f0 < redo_hi; f0 += (long long)kBatch * kThreads) {
+            float x[kBatch];
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                const long long f = f0 + (long long)j * kThreads;
+                x[j] = f >= redo_hi ? 0.f : __ldcg(f < fb ? p.lse_base + f : p.lse_out + (f - fb));
+            }
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j)
+                if (!(fabsf(x[j]) <= 3.4e38f)) claim(f0 + (long long)j * kThreads);
+        }
+        __syncthreads();
+        if (mt.n_redo == 0) return;  // the common case: nothing to compute again
+    }
     if (warp == kMmaWarp) {
         tmem_alloc(&mt.tmem_base, 512);
         tmem_relinquish();
@@ -344,11 +446,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t nq[2] = {0, 0};    // per slot: units whose query phase was armed
         // Descriptors run one unit ahead of the loads, so the other roles never
         // wait for the next unit's counter fetch and position reads.
+        int taken = 0;  // second launch: blocks of this CTA's list taken so far
         auto next_desc = [&](UnitDesc &ud) {
             int u = 0;
-            if (lane == 0) u = atomicAdd(p.unit_counter, 1);
-            u = __shfl_sync(0xffffffffu, u, 0);
-            make_desc(p, u < total_units ? u : -1, lane, ud);
+            if constexpr (kRedo) {
+                u = taken < mt.n_redo ? __ldcg(p.redo_list + redo_lo + taken) : -1;
+                ++taken;
+            } else {
+                if (lane == 0) u = atomicAdd(p.unit_counter, 1);
+                u = __shfl_sync(0xffffffffu, u, 0);
+                u = u < total_units ? u : -1;
+            }
+            make_desc(p, u, lane, ud, kRedo);
         };
         auto publish = [&](int i, const UnitDesc &ud) -> bool {
             const int r = i % kDescRing;
@@ -454,6 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                kk > 0 ? 1u : (ACC0));
             uint32_t g = 0;              // K/V iterations consumed (all units so far)
             uint32_t pc0 = 0, pc1 = 0;   // P tiles consumed per slot
+            uint32_t qr0 = 0, qr1 = 0;   // second launch: q_ready phases consumed per slot
             bool ok = true;
             for (int i = 0; ok; ++i) {
                 const int r = i % kDescRing;
@@ -464,13 +574,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int kt_min = dr.kt_min, n_it = dr.n_it;
                 mbar_arrive(&mt.u_empty[r]);
                 if (end) break;
+                // Second launch: a slot with key tiles gets, in place of its first
+                // product, a go-ahead on s_full to stage its rows again with per-row
+                // shifts; the products wait for that second staging (two q_ready
+                // phases per unit there, one in the first launch).
+                auto restage = [&](int sl, int lo, int hi, uint32_t &qr) -> bool {
+                    if (!kRedo || max(lo, kt_min) > min(hi, kt_min + n_it - 1)) return true;
+                    mbar_arrive(&mt.s_full[sl]);
+                    if (!mbar_wait(&mt.q_ready[sl], qr & 1, abort, p.status)) return false;
+                    ++qr;
+                    return true;
+                };
                 // each slot's query tile staged before its first product (this also
                 // orders the product after that slot's previous epilogue)
-                if (!(ok = mbar_wait(&mt.q_ready[0], i & 1, abort, p.status))) break;
+                if (!(ok = mbar_wait(&mt.q_ready[0], (kRedo ? qr0 : (uint32_t)i) & 1, abort, p.status))) break;
+                if (kRedo) ++qr0;
                 if (n_it == 0) {
-                    if (!(ok = mbar_wait(&mt.q_ready[1], i & 1, abort, p.status))) break;
+                    if (!(ok = mbar_wait(&mt.q_ready[1], (kRedo ? qr1 : (uint32_t)i) & 1, abort, p.status))) break;
+                    if (kRedo) ++qr1;
                     continue;
                 }
+                if (!(ok = restage(0, lo0, hi0, qr0))) break;
                 if (!(ok = mbar_wait(&mt.k_full[g % kNumK], (g / kNumK) & 1, abort, p.status))) break;
                 tc_fence_after();
                 const uint64_t dk0 = dk + (uint64_t)((g % kNumK) * kTileU);
@@ -478,7 +602,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ORTHROS_ISSUE_S(d_s0, dq, dk0)
                     tc_commit(&mt.s_full[0]);
                 }
-                if (!(ok = mbar_wait(&mt.q_ready[1], i & 1, abort, p.status))) break;
+                if (!(ok = mbar_wait(&mt.q_ready[1], (kRedo ? qr1 : (uint32_t)i) & 1, abort, p.status))) break;
+                if (kRedo) ++qr1;
+                if (!(ok = restage(1, lo1, hi1, qr1))) break;
                 tc_fence_after();
                 if (kt_min >= lo1 && kt_min <= hi1) {
                     ORTHROS_ISSUE_S(d_s1, dq + kTileU, dk0)
@@ -589,7 +715,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (my_valid) {
                     const float *al = (S.kind == 0 ? p.alpha_base : p.alpha_out) + S.h * D;
                     const float *be = (S.kind == 0 ? p.beta_base : p.beta_out) + S.h * D;
-                    bool over = false;
                     uint4 raws[kHalfChunks];  // every load of the half row in flight at once
                     if (tma) {
 #pragma unroll
@@ -616,8 +741,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float v[8] = {fmaf(a0.x, x0.x, b0.x), fmaf(a0.y, x0.y, b0.y), fmaf(a0.z, x1.x, b0.z),
                                       fmaf(a0.w, x1.y, b0.w), fmaf(a1.x, x2.x, b1.x), fmaf(a1.y, x2.y, b1.y),
                                       fmaf(a1.z, x3.x, b1.z), fmaf(a1.w, x3.y, b1.w)};
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) over |= fabsf(v[e]) > 65504.f;
                         uint4 o;
                         o.x = pack_f16(v[0], v[1]);
                         o.y = pack_f16(v[2], v[3]);
@@ -625,7 +748,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         o.w = pack_f16(v[6], v[7]);
                         *reinterpret_cast<uint4 *>(qs + sw128_offset<D>(row, c)) = o;
                     }
-                    if (over) set_status(p.status, ORTHROS_DEV_FP16_RANGE);
                 } else {
 #pragma unroll 4
                     for (int cc = 0; cc < kHalfChunks; ++cc)
@@ -643,11 +765,68 @@ __global__ void __launch_bounds__(kThreads, 1)
             float m_ref = -INFINITY, l = 0.f;
             bool ok = true;
             uint32_t tiles = 0;
+            int row_shift = 0;  // second launch: the products give this row's logits times 2^-row_shift
+            if (kRedo && max(bd.kt_lo, kt_min) <= min(bd.kt_hi, kt_min + n_it - 1)) {
+                // The issuer's go-ahead comes in place of the first product: each row is
+                // staged again as qa * 2^-r, r the smallest shift that brings its largest
+                // value below 2^15. The two halves of a row combine the same two rounded
+                // maxima (exchanged like a tile's maxima, one xm_bar phase for the one
+                // s_full phase), so they agree on r.
+                ok = __all_sync(0xffffffffu, mbar_wait(&mt.s_full[s], cnt & 1, abort, p.status));
+                if (ok) {
+                    constexpr int kHalfChunks = D / 16;
+                    const float *al = (S.kind == 0 ? p.alpha_base : p.alpha_out) + S.h * D;
+                    const float *be = (S.kind == 0 ? p.beta_base : p.beta_out) + S.h * D;
+                    float qa[D / 2];  // this half row, affined (re-read: the tile holds the first staging)
+                    float amax = 0.f;
+                    if (my_valid) {
+                        const __nv_bfloat16 *src =
+                            S.qrow >= 0
+                                ? (S.kind == 1 && p.q_out ? p.q_out : p.q) + ((long long)(S.qrow + row) * p.Hq + S.h) * D
+                                : p.q + (((long long)S.b * p.Tq + (my_t - p.q_off)) * p.Hq + S.h) * D;
+#pragma unroll
+                        for (int c = 0; c < D / 2; ++c) {
+                            const int ch = hh * (D / 2) + c;
+                            qa[c] = fmaf(al[ch], __bfloat162float(src[ch]), be[ch]);
+                            amax = fmaxf(amax, fabsf(qa[c]));
+                        }
+                    }
+                    const __nv_bfloat16 amax_b = __float2bfloat16_ru(amax);
+                    mt.xmax[s][hh][row] = amax_b;
+                    mbar_arrive(&mt.xm_bar[s]);
+                    ok = __all_sync(0xffffffffu, mbar_wait(&mt.xm_bar[s], cnt & 1, abort, p.status));
+                    ++cnt;
+                    if (ok) {
+                        const float rmax = fmaxf(__bfloat162float(amax_b), __bfloat162float(mt.xmax[s][hh ^ 1][row]));
+                        if (rmax > 65504.f && __float_as_uint(rmax) < 0x7f800000u)
+                            row_shift = min((int)((__float_as_uint(rmax) >> 23) & 0xff) - 127 - 14, 126);
+                        if (my_valid && row_shift > 0) {
+                            const float f = exp2_int(-row_shift);
+#pragma unroll
+                            for (int cc = 0; cc < kHalfChunks; ++cc) {
+                                uint4 o;
+                                o.x = pack_f16(qa[8 * cc] * f, qa[8 * cc + 1] * f);
+                                o.y = pack_f16(qa[8 * cc + 2] * f, qa[8 * cc + 3] * f);
+                                o.z = pack_f16(qa[8 * cc + 4] * f, qa[8 * cc + 5] * f);
+                                o.w = pack_f16(qa[8 * cc + 6] * f, qa[8 * cc + 7] * f);
+                                *reinterpret_cast<uint4 *>(qs + sw128_offset<D>(row, hh * kHalfChunks + cc)) = o;
+                            }
+                        }
+                        fence_proxy_async_smem();
+                        mbar_arrive(&mt.q_ready[s]);
+                        ok = __all_sync(0xffffffffu, mbar_wait(&mt.s_full[s], cnt & 1, abort, p.status));
+                    }
+                }
+                if (!ok) break;
+            }
+            const float c2u = kRedo ? c2 * exp2_int(row_shift) : c2;  // the row's logit scale
             for (int it = 0; it < n_it; ++it) {
                 const int kt = kt_min + it;
                 if (kt < bd.kt_lo || kt > bd.kt_hi) continue;
-                const bool got = mbar_wait(&mt.s_full[s], cnt & 1, abort, p.status);
-                if (!(ok = __all_sync(0xffffffffu, got))) break;
+                if (!kRedo || tiles > 0) {  // (second launch: the first tile's wait came above)
+                    const bool got = mbar_wait(&mt.s_full[s], cnt & 1, abort, p.status);
+                    if (!(ok = __all_sync(0xffffffffu, got))) break;
+                }
                 tc_fence_after();
                 // this half's 64 logits of the row, in two 32-column loads, one wait
                 uint32_t ra[32], rb[32];
@@ -679,14 +858,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!(ok = __all_sync(0xffffffffu, mbar_wait(&mt.xm_bar[s], cnt & 1, abort, p.status)))) break;
                 const float m_tile = fmaxf(__bfloat162float(mine_b), __bfloat162float(mt.xmax[s][hh ^ 1][row]));
                 const float m_new = fmaxf(m_ref, m_tile);
-                const bool resc = (m_new - m_ref) * c2 > 8.f;  // true on the first finite max
+                const bool resc = (m_new - m_ref) * c2u > 8.f;  // true on the first finite max
                 const bool any_resc = __any_sync(0xffffffffu, resc);
-                const float alpha = resc ? ex2((m_ref - m_new) * c2) : 1.f;
+                const float alpha = resc ? ex2((m_ref - m_new) * c2u) : 1.f;
                 if (resc) {
                     l *= alpha;
                     m_ref = m_new;
                 }
-                const float mb = m_ref == -INFINITY ? 0.f : m_ref * c2;
+                const float mb = m_ref == -INFINITY ? 0.f : m_ref * c2u;
                 float ls[4] = {0.f, 0.f, 0.f, 0.f};
                 // P for keys 64 hh .. 64 hh + 63 -> packed columns 32 hh .. 32 hh + 31
 #pragma unroll
@@ -695,8 +874,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
-                        const float p0 = ex2(fmaf(x[2 * e], c2, -mb));
-                        const float p1 = ex2(fmaf(x[2 * e + 1], c2, -mb));
+                        const float p0 = ex2(fmaf(x[2 * e], c2u, -mb));
+                        const float p1 = ex2(fmaf(x[2 * e + 1], c2u, -mb));
                         ls[e & 3] += p0 + p1;
                         pk[e] = pack_bf16(p0, p1);
                     }
@@ -725,6 +904,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++tiles;
             }
             if (!ok) break;
+            if (kRedo) m_ref *= exp2_int(row_shift);  // back to logit units for the epilogue
 
             // ---- epilogue: o = O / l, lse = scale*m + ln l ----
             // o_full fires once every product of the slot's unit has completed, so
@@ -866,13 +1046,31 @@ cudaError_t launch_d(const TcParams &p, const void *k16, const void *v, int unit
         !encode_kv_map_3d(&tqo, p.q_out ? (const void *)p.q_out : (const void *)p.q,
                           p.q_out ? (long long)p.n_out : (long long)p.B * p.Tq, p.Hq, D, kRowsPerTile))
         return cudaErrorInvalidValue;
-    static SmemLimit limit;
-    if (cudaError_t e = limit.ensure((const void *)prefill_tc_kernel<D>, Cfg<D>::kSmem); e != cudaSuccess) return e;
+    static SmemLimit limit, limit_redo;
+    if (cudaError_t e = limit.ensure((const void *)prefill_tc_kernel<D, false>, Cfg<D>::kSmem); e != cudaSuccess)
+        return e;
+    if (cudaError_t e = limit_redo.ensure((const void *)prefill_tc_kernel<D, true>, Cfg<D>::kSmem); e != cudaSuccess)
+        return e;
     // persistent: one CTA per SM takes units from the counter until none is left
     int dev = 0, sms = 152;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int grid = units < sms ? units : sms;
-    prefill_tc_kernel<D><<<grid, kThreads, Cfg<D>::kSmem, stream>>>(tk, tv, tq, tqo, tob, p);
+    prefill_tc_kernel<D, false><<<grid, kThreads, Cfg<D>::kSmem, stream>>>(tk, tv, tq, tqo, tob, p);
+    if (cudaError_t e = cudaGetLastError(); e != cudaSuccess) return e;
+    // second launch: scans the log-sum-exps for rows with a query past the fp16
+    // range and computes their blocks again (none: every CTA leaves after the scan)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(sms);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Cfg<D>::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D, true>, tk, tv, tq, tqo, tob, p); e != cudaSuccess)
+        return e;
     return cudaGetLastError();
 }
 

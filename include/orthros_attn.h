@@ -30,8 +30,8 @@
  *     ORTHROS_EUNSUPPORTED, ORTHROS_EWORKSPACE); orthros_last_error() then
  *     describes the problem. Launch failures return ORTHROS_ECUDA. Bad data
  *     that only the GPU can see (a position out of range, a block-table entry
- *     outside the page pool, a cache length past the block table, a key value
- *     the fp16 tensor-core path cannot represent) sets a status word in the
+ *     outside the page pool, a cache length past the block table) sets a
+ *     status word in the
  *     workspace; the affected rows are skipped or their outputs are NaN, and
  *     orthros_check() reports ORTHROS_EDEVICE. Nothing aborts or traps.
  *   - Supported head sizes: d = 64 or 128.
@@ -74,7 +74,10 @@ typedef enum { ORTHROS_BF16 = 0, ORTHROS_F32 = 1 } orthros_dtype;
 #define ORTHROS_DEV_BAD_POSITION 0x1u  /* out_positions entry outside [0, T) */
 #define ORTHROS_DEV_BAD_PAGE 0x2u      /* block-table entry outside [0, num_pages) */
 #define ORTHROS_DEV_BAD_LENGTH 0x4u    /* cache_lens[b] < 0 or past the block table */
-#define ORTHROS_DEV_FP16_RANGE 0x8u    /* |k| or |affined q| beyond the fp16 range */
+/* 0x8u is never raised: keys and affined queries beyond the fp16 range of the
+ * tensor-core prefill are scaled by exact powers of two (the logit scale
+ * takes the inverse), so any finite bf16 input is served. */
+#define ORTHROS_DEV_FP16_RANGE 0x8u
 #define ORTHROS_DEV_TIMEOUT 0x10u      /* a bounded wait inside a kernel ran out */
 
 /*

@@ -44,6 +44,44 @@ def test_key_offsets_small():
     compare_prefill(wl, run_gpu_prefill(wl), what="offsets")
 
 
+@pytest.mark.parametrize("mode", ["all", ("span", 70)], ids=["all", "span"])
+def test_key_beyond_fp16_range(mode):
+    """Single keys of 7e4 and -9e4 (fp16 stops at 65504): the fp16 key copy is
+    scaled by 2^-2 and the logit scale by 2^2. The query channel that meets
+    them is small (subnormal in fp16), so every logit stays moderate and the
+    usual tolerances hold."""
+    wl = W.small_prefill(2, 300, 4, 2, 128, 200, out_mode=mode, seed=11)
+    c = 5
+    wl["k"][0, 100, 1, c] = 70000.0
+    wl["k"][1, 7, 0, c] = -90000.0
+    for a, b in (("alpha_base", "beta_base"), ("alpha_out", "beta_out")):
+        wl[a][:, c] = 2e-5
+        wl[b][:, c] = 0.0
+    compare_prefill(wl, run_gpu_prefill(wl), what="keys beyond fp16")
+
+
+@pytest.mark.parametrize("mode", ["all", ("span", 70)], ids=["all", "span"])
+def test_query_beyond_fp16_range(mode):
+    """Affine weights of +-1e5 on one channel lift about half of the rows of a
+    base head and of an output head past 65504; those rows are staged as
+    q * 2^-r and their logit scale takes 2^r, the other rows of the same tiles
+    keep r = 0. The keys' values in that channel are small multiples of 2^-16
+    (exact in bf16 and fp16), so the logits stay moderate. One query sits just
+    below 2^17 (130781.25), where rounding the row maximum up crosses the
+    power of two: both column halves must still pick the same shift."""
+    wl = W.small_prefill(2, 300, 4, 2, 128, 200, out_mode=mode, seed=12)
+    c = 9
+    wl["alpha_base"][0, c] = 1e5
+    wl["beta_base"][0, c] = 0.0
+    wl["alpha_out"][3, c] = -1e5
+    wl["beta_out"][3, c] = 3e4
+    wl["q"][0, 299, 3, c] = -1.0078125  # affined: 130781.25
+    g = torch.Generator().manual_seed(3)
+    m = torch.randint(-2, 3, wl["k"].shape[:-1] + (1,), generator=g).float()
+    wl["k"][..., c:c + 1] = (m * 2.0 ** -16).to(wl["k"].dtype)
+    compare_prefill(wl, run_gpu_prefill(wl), what="queries beyond fp16")
+
+
 def test_tiny_fp32_full():
     wl = W.make_prefill(W.TINY_FP32)
     errs = compare_prefill(wl, run_gpu_prefill(wl), what=W.TINY_FP32.name)

@@ -77,6 +77,9 @@ def test_decode_chunk_choice_at_the_benchmark_shapes():
 def test_prefill_workspace_follows_the_rule(B, T, Hkv, n_out):
     d, Hq = 128, 4 * Hkv
     max_groups = min(n_out, 16 * B) * Hkv
-    want = (STATUS_BYTES + align(4 * (2 * (B + 1) + 3 * max_groups)) + align(B * T * Hkv * d * 2)
-            + align(slots_bound(max_groups, T, sms()) * slot_bytes(d)))
+    blocks = Hq * (B * (cdiv(T, 128) + 1) + cdiv(n_out, 128) + 2 * B)  # bound on the tile kernel's row blocks
+    want = (STATUS_BYTES + align(4 * (3 * (B + 1) + 3 * max_groups)) + align(B * T * Hkv * d * 2)
+            + align(slots_bound(max_groups, T, sms()) * slot_bytes(d))
+            + align(4 * cdiv(blocks, 32)) + align(4 * (B * Hq * T + n_out * Hq))  # second-pass bitmap and list
+            + align(4 * 4 * Hq * d))  # the scaled affine copies
     assert ola.orthros_prefill_workspace_size(B, T, Hq, Hkv, d, n_out, 4096) == want
