@@ -23,7 +23,7 @@
 //                 shared memory before one atomic add per channel
 // Lane l holds channels [l*E, l*E+E), E = d/32, of every row it touches.
 //
-// Tensor-core path (bf16, d = 128): the delta kernel also writes qa in bf16,
+// Tensor-core path (bf16, d = 64 or 128): the delta kernel also writes qa in bf16,
 // backward_tc.cu computes dk, dv and accumulates dqa in fp32, and the dq
 // kernel (FromAcc) applies the affine and reduces the affine gradients.
 #include "internal.cuh"
@@ -432,7 +432,7 @@ cudaError_t launch_t(const BwdArgs &a, cudaStream_t stream) {
         tp.scale_log2 = a.scale * 1.4426950408889634f;
         tp.status = a.status;
         ProfScope ps("bwd_tc", stream);
-        e = launch_backward_tc(tp, a.k, a.v, a.qa_base, a.do_base, a.qa_out, a.do_out, stream);
+        e = launch_backward_tc(tp, D, a.k, a.v, a.qa_base, a.do_base, a.qa_out, a.do_out, stream);
     } else {
         ProfScope ps("bwd_dkdv_simt", stream);
         const long long n = (long long)a.B * a.T * a.Hkv;
@@ -462,7 +462,7 @@ cudaError_t launch_t(const BwdArgs &a, cudaStream_t stream) {
 cudaError_t launch_backward(const BwdArgs &a, int d, orthros_dtype dtype, bool use_tc, cudaStream_t stream) {
     if (dtype == ORTHROS_F32)
         return d == 64 ? launch_t<float, 64, false>(a, stream) : launch_t<float, 128, false>(a, stream);
-    if (use_tc && d == 128) return launch_t<__nv_bfloat16, 128, true>(a, stream);
+    if (use_tc) return d == 64 ? launch_t<__nv_bfloat16, 64, true>(a, stream) : launch_t<__nv_bfloat16, 128, true>(a, stream);
     return d == 64 ? launch_t<__nv_bfloat16, 64, false>(a, stream) : launch_t<__nv_bfloat16, 128, false>(a, stream);
 }
 

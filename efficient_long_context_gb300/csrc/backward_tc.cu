@@ -1,5 +1,5 @@
 // backward_tc.cu -- gradients of the banded and cross rows on the 5th-generation
-// tensor cores (tcgen05, TMEM, TMA); bf16, head size 128.
+// tensor cores (tcgen05, TMEM, TMA); bf16, head size d = 128 or 64.
 //
 // What it computes: the chain rule through Sec. 3.1 Eq. 4 (base rows, keys
 // max(0, t-w+1) .. t) and Eq. 5 (output rows, keys 0 .. t_r). With the
@@ -22,6 +22,8 @@
 //     dK  += dS^T qa  (dS^T from shared memory)              TMEM [256, 384)
 //     dQ^T = K^T dS^T (M = d channels, N = 64 rows, both operands MN-major)
 //                                                            TMEM [384, 448)
+//     (d = 64: dV, dK take 64 columns each; dQ^T is an M = 64 accumulator,
+//     channel 16 q + i in TMEM lane 32 q + i, i < 16)
 //     P^T as packed bf16, two buffers                        TMEM [448, 512)
 //   warp 8: TMA producer (K, V once; qa and dO tiles, 3 stages) and the
 //           per-tile row metadata (positions, L, D), loaded while the tiles fly.
@@ -46,7 +48,6 @@ using namespace ptx;
 
 namespace {
 
-constexpr int kD = 128;
 constexpr int kKeys = 128;
 constexpr int kRows = 64;
 constexpr int kStages = 3;
@@ -57,14 +58,7 @@ constexpr int kSoftThreads = 256;
 
 constexpr int kBoxK = kKeys * 128;     // one 64-channel box of 128 keys: 16 KB
 constexpr int kBoxQ = kRows * 128;     // one 64-channel box of 64 rows: 8 KB
-constexpr int kKBytes = 2 * kBoxK;     // 32 KB
-constexpr int kQBytes = 2 * kBoxQ;     // 16 KB
 constexpr int kDSBytes = kKeys * kRows * 2;  // 16 KB
-constexpr int kOffK = 0;
-constexpr int kOffV = kOffK + kKBytes;
-constexpr int kOffQ = kOffV + kKBytes;            // stage s: qa at +s*2*kQBytes, dO after it
-constexpr int kOffDS = kOffQ + kStages * 2 * kQBytes;
-constexpr int kOffMeta = kOffDS + 2 * kDSBytes;
 // TMEM columns
 constexpr uint32_t kTS = 0, kTdP = 64, kTdV = 128, kTdK = 256, kTdQ = 384, kTP = 448;
 
@@ -126,7 +120,18 @@ struct Meta {
     StageMeta st[kStages];
 };
 
-constexpr int kSmem = kOffMeta + (int)sizeof(Meta) + 1024;
+// Shared-memory layout for head size D (D / 64 boxes of 64 channels per tile).
+template <int D> struct BCfg {
+    static constexpr int kAtoms = D / 64;
+    static constexpr int kKBytes = kAtoms * kBoxK;  // 32 KB (16 KB at d = 64)
+    static constexpr int kQBytes = kAtoms * kBoxQ;  // 16 KB (8 KB)
+    static constexpr int kOffK = 0;
+    static constexpr int kOffV = kOffK + kKBytes;
+    static constexpr int kOffQ = kOffV + kKBytes;  // stage s: qa at +s*2*kQBytes, dO after it
+    static constexpr int kOffDS = kOffQ + kStages * 2 * kQBytes;
+    static constexpr int kOffMeta = kOffDS + 2 * kDSBytes;
+    static constexpr int kSmem = kOffMeta + (int)sizeof(Meta) + 1024;
+};
 
 __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
     asm volatile(""
@@ -137,11 +142,15 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
                    "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
 }
 
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     backward_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_qb, const __grid_constant__ CUtensorMap tm_db,
                        const __grid_constant__ CUtensorMap tm_qo, const __grid_constant__ CUtensorMap tm_do,
                        const BwdTcParams p) {
+    using C = BCfg<D>;
+    constexpr int kOffK = C::kOffK, kOffV = C::kOffV, kOffQ = C::kOffQ, kOffDS = C::kOffDS, kOffMeta = C::kOffMeta;
+    constexpr int kKBytes = C::kKBytes, kQBytes = C::kQBytes;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Meta &mt = *reinterpret_cast<Meta *>(smem + kOffMeta);
@@ -213,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int issued = 0;
         if (lane == 0 && n_tiles > 0) {
             mbar_arrive_expect_tx(&mt.kv_full, 2 * kKBytes);
-            for (int j = 0; j < 2; ++j) {
+            for (int j = 0; j < C::kAtoms; ++j) {
                 tma_load_3d(smem + kOffK + j * kBoxK, &tm_k, &mt.kv_full, 64 * j, kv, (int)(seq_tok + j0));
                 tma_load_3d(smem + kOffV + j * kBoxK, &tm_v, &mt.kv_full, 64 * j, kv, (int)(seq_tok + j0));
             }
@@ -270,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int row_tok = kind == 0 ? (int)(seq_tok + row0) : row0;
                 const CUtensorMap *mq = kind == 0 ? &tm_qb : &tm_qo;
                 const CUtensorMap *md = kind == 0 ? &tm_db : &tm_do;
-                for (int j = 0; j < 2; ++j) {
+                for (int j = 0; j < C::kAtoms; ++j) {
                     tma_load_3d(qa + j * kBoxQ, mq, &mt.q_full[s], 64 * j, h, row_tok);
                     tma_load_3d(dO + j * kBoxQ, md, &mt.q_full[s], 64 * j, h, row_tok);
                 }
@@ -304,8 +313,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- tcgen05.mma issuer ----------------
         if (lane == 0 && n_tiles > 0) {
             constexpr uint32_t kIdS = idesc_f16(1, 1, 0, 0, kKeys, kRows);   // S^T, dP^T
-            constexpr uint32_t kIdKV = idesc_f16(1, 1, 0, 1, kKeys, kD);     // dV, dK: B MN-major
-            constexpr uint32_t kIdQ = idesc_f16(1, 1, 1, 1, kD, kRows);      // dQ^T: A and B MN-major
+            constexpr uint32_t kIdKV = idesc_f16(1, 1, 0, 1, kKeys, D);      // dV, dK: B MN-major
+            constexpr uint32_t kIdQ = idesc_f16(1, 1, 1, 1, D, kRows);       // dQ^T: A and B MN-major
             // start-address field is (byte address >> 4); all operands lie below
             // 256 KB, so adding (offset >> 4) never carries out of the field
             const uint64_t d_k = desc_sw128(smem_u32(smem + kOffK), 16, 1024);          // K-major
@@ -325,13 +334,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     const uint64_t dq = d_q0 + s * kStageU, ddo = dq + kQU;
 #pragma unroll
-                    for (int ks = 0; ks < kD / 16; ++ks) {
+                    for (int ks = 0; ks < D / 16; ++ks) {
                         const uint32_t ok_ = ((ks >> 2) * kBoxK + (ks & 3) * 32) >> 4;
                         const uint32_t oq = ((ks >> 2) * kBoxQ + (ks & 3) * 32) >> 4;
                         mma_ss(tmem + kTS, d_k + ok_, dq + oq, kIdS, ks > 0);
                     }
 #pragma unroll
-                    for (int ks = 0; ks < kD / 16; ++ks) {
+                    for (int ks = 0; ks < D / 16; ++ks) {
                         const uint32_t ok_ = ((ks >> 2) * kBoxK + (ks & 3) * 32) >> 4;
                         const uint32_t oq = ((ks >> 2) * kBoxQ + (ks & 3) * 32) >> 4;
                         mma_ss(tmem + kTdP, d_v + ok_, ddo + oq, kIdS, ks > 0);
@@ -386,18 +395,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&mt.dq_free);
             const int2 tl = prev_tile;
             const int h = tl.x >> 1, kind = tl.x & 1, row0 = tl.y;
-            const int ch = key;  // dQ^T lanes are channels
+            // dQ^T lanes are channels (d = 64: lanes 32 q .. 32 q + 15 hold channels 16 q ..)
+            const int ch = D == 128 ? key : qd * 16 + lane;
+            const bool own = D == 128 || lane < 16;
             if (kind == 0) {
-                float *dst = p.dq_acc + ((seq_tok + row0 + 32 * hh) * p.Hq + h) * kD + ch;
-                const long long stride = (long long)p.Hq * kD;
-                const int n = min(32, p.T - (row0 + 32 * hh));
+                float *dst = p.dq_acc + ((seq_tok + row0 + 32 * hh) * p.Hq + h) * D + ch;
+                const long long stride = (long long)p.Hq * D;
+                const int n = own ? min(32, p.T - (row0 + 32 * hh)) : 0;
 #pragma unroll
                 for (int e = 0; e < 32; ++e)
                     if (e < n) red_add_f32(dst + e * stride, __uint_as_float(v[e]));
             } else {
-                float *dst = p.dq_out_acc + ((long long)(row0 + 32 * hh) * p.Hq + h) * kD + ch;
-                const long long stride = (long long)p.Hq * kD;
-                const int n = min(32, r1b - (row0 + 32 * hh));
+                float *dst = p.dq_out_acc + ((long long)(row0 + 32 * hh) * p.Hq + h) * D + ch;
+                const long long stride = (long long)p.Hq * D;
+                const int n = own ? min(32, r1b - (row0 + 32 * hh)) : 0;
 #pragma unroll
                 for (int e = 0; e < 32; ++e)
                     if (e < n) red_add_f32(dst + e * stride, __uint_as_float(v[e]));
@@ -464,17 +475,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             prev_tile = cur_tile;
         }
         if (ok && n_tiles > 0) ok = drain(n_tiles - 1);
-        // dK, dV of this thread's key: columns [64 hh, 64 hh + 64) of each
+        // dK, dV of this thread's key: columns [D/2 hh, D/2 hh + D/2) of each
         const bool done = n_tiles > 0 && ok && mbar_wait_warp(&mt.mma_done, 0, abort, p.status);
         if (done) {
             tc_fence_after();
 #pragma unroll
             for (int which = 0; which < 2; ++which) {
-                __nv_bfloat16 *dst = (which ? p.dk : p.dv) + ((seq_tok + j) * p.Hkv + kv) * kD + 64 * hh;
+                __nv_bfloat16 *dst = (which ? p.dk : p.dv) + ((seq_tok + j) * p.Hkv + kv) * D + (D / 2) * hh;
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
+                for (int half = 0; half < D / 64; ++half) {
                     uint32_t v[32];
-                    tmem_ld32(tmem + lane_off + kTdV + 128 * which + 64 * hh + 32 * half, v);
+                    tmem_ld32(tmem + lane_off + kTdV + 128 * which + (D / 2) * hh + 32 * half, v);
                     tmem_ld_wait();
                     reg_fence(v);
                     if (j < p.T) {
@@ -501,23 +512,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_backward_tc(const BwdTcParams &p, const void *k, const void *v, const void *qa_base,
-                               const void *do_base, const void *qa_out, const void *do_out, cudaStream_t stream) {
+namespace {
+
+template <int D>
+cudaError_t launch_d(const BwdTcParams &p, const void *k, const void *v, const void *qa_base, const void *do_base,
+                     const void *qa_out, const void *do_out, cudaStream_t stream) {
     const long long tokens = (long long)p.B * p.T;
     CUtensorMap tk, tv, tqb, tdb, tqo, tdo;
     const long long n_out_rows = p.n_out > 0 ? p.n_out : 1;
-    if (!encode_kv_map_3d(&tk, k, tokens, p.Hkv, kD, kKeys) || !encode_kv_map_3d(&tv, v, tokens, p.Hkv, kD, kKeys) ||
-        !encode_kv_map_3d(&tqb, qa_base, tokens, p.Hq, kD, kRows) ||
-        !encode_kv_map_3d(&tdb, do_base, tokens, p.Hq, kD, kRows) ||
-        !encode_kv_map_3d(&tqo, p.n_out > 0 ? qa_out : qa_base, n_out_rows, p.Hq, kD, kRows) ||
-        !encode_kv_map_3d(&tdo, p.n_out > 0 ? do_out : do_base, n_out_rows, p.Hq, kD, kRows))
+    if (!encode_kv_map_3d(&tk, k, tokens, p.Hkv, D, kKeys) || !encode_kv_map_3d(&tv, v, tokens, p.Hkv, D, kKeys) ||
+        !encode_kv_map_3d(&tqb, qa_base, tokens, p.Hq, D, kRows) ||
+        !encode_kv_map_3d(&tdb, do_base, tokens, p.Hq, D, kRows) ||
+        !encode_kv_map_3d(&tqo, p.n_out > 0 ? qa_out : qa_base, n_out_rows, p.Hq, D, kRows) ||
+        !encode_kv_map_3d(&tdo, p.n_out > 0 ? do_out : do_base, n_out_rows, p.Hq, D, kRows))
         return cudaErrorInvalidValue;
     static SmemLimit limit;
-    if (cudaError_t e = limit.ensure((const void *)backward_tc_kernel, kSmem); e != cudaSuccess) return e;
+    if (cudaError_t e = limit.ensure((const void *)backward_tc_kernel<D>, BCfg<D>::kSmem); e != cudaSuccess) return e;
     const long long units = (long long)p.nkb * p.B * p.Hkv;
     if (units == 0) return cudaSuccess;
-    backward_tc_kernel<<<(unsigned)units, kThreads, kSmem, stream>>>(tk, tv, tqb, tdb, tqo, tdo, p);
+    backward_tc_kernel<D><<<(unsigned)units, kThreads, BCfg<D>::kSmem, stream>>>(tk, tv, tqb, tdb, tqo, tdo, p);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_backward_tc(const BwdTcParams &p, int d, const void *k, const void *v, const void *qa_base,
+                               const void *do_base, const void *qa_out, const void *do_out, cudaStream_t stream) {
+    return d == 128 ? launch_d<128>(p, k, v, qa_base, do_base, qa_out, do_out, stream)
+                    : launch_d<64>(p, k, v, qa_base, do_base, qa_out, do_out, stream);
 }
 
 }  // namespace orthros

@@ -236,13 +236,13 @@ struct BwdArgs {
     void *dq, *dk, *dv, *dq_out;
     float *d_alpha_base, *d_beta_base, *d_alpha_out, *d_beta_out;  // zeroed by the caller
     uint32_t *status;
-    // tensor-core path only (bf16, d = 128); nullptr otherwise
+    // tensor-core path only (bf16); nullptr otherwise
     __nv_bfloat16 *qa_base;  // [B,T,Hq,d] affined base queries
     __nv_bfloat16 *qa_out;   // [n_out,Hq,d] affined output-row queries
     float *dq_acc;           // [B,T,Hq,d] fp32 dqa of base rows
     int32_t *omax;           // [n_out]: largest position among rows r .. r+63 of r's sequence
 };
-// Runs the whole backward; use_tc selects the tensor-core kernel (bf16, d = 128,
+// Runs the whole backward; use_tc selects the tensor-core kernel (bf16, d = 64 or 128,
 // with the workspace regions above) for the dk/dv/dqa products.
 cudaError_t launch_backward(const BwdArgs &a, int d, orthros_dtype dtype, bool use_tc, cudaStream_t stream);
 
@@ -256,7 +256,7 @@ struct BwdTcParams {
     float scale, scale_log2;
     uint32_t *status;
 };
-cudaError_t launch_backward_tc(const BwdTcParams &p, const void *k, const void *v, const void *qa_base,
+cudaError_t launch_backward_tc(const BwdTcParams &p, int d, const void *k, const void *v, const void *qa_base,
                                const void *do_base, const void *qa_out, const void *do_out, cudaStream_t stream);
 
 // project_tc.cu: shared Q/K/V projection (bf16) with the query affines and

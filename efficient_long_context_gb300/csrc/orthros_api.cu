@@ -162,7 +162,7 @@ BackwardLayout backward_layout(int B, int T, int Hq, int d, int n_out, orthros_d
     at += align_up(sizeof(float) * (size_t)n_out * Hq, 256);
     L.dq_rows_off = at;
     at += align_up(sizeof(float) * (size_t)n_out * Hq * d, 256);
-    const bool tc = dtype == ORTHROS_BF16 && d == 128;
+    const bool tc = dtype == ORTHROS_BF16;
     L.qa_base_off = at;
     if (tc) at += align_up((size_t)2 * B * T * Hq * d, 256);
     L.qa_out_off = at;
@@ -704,7 +704,7 @@ orthros_status orthros_prefill_backward(const void *q, const void *k, const void
     a.d_alpha_out = d_alpha_out;
     a.d_beta_out = d_beta_out;
     a.status = status;
-    const bool use_tc = dtype == ORTHROS_BF16 && d == 128;
+    const bool use_tc = dtype == ORTHROS_BF16;
     if (use_tc) {
         a.qa_base = reinterpret_cast<__nv_bfloat16 *>(ws + lay.qa_base_off);
         a.qa_out = reinterpret_cast<__nv_bfloat16 *>(ws + lay.qa_out_off);

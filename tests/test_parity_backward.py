@@ -103,6 +103,8 @@ SMALL = [
     (1, 300, 4, 1, 128, 128, ("list", [[0, 5, 127, 128, 128, 129, 299, 5]]), torch.bfloat16),
     (2, 257, 4, 2, 64, 256, "all", torch.bfloat16),
     (1, 300, 2, 2, 64, 1, "last", torch.bfloat16),
+    (2, 333, 8, 2, 64, 65, ("span", 70), torch.bfloat16),
+    (1, 300, 4, 1, 64, 128, ("list", [[0, 5, 127, 128, 128, 129, 299, 5]]), torch.bfloat16),
     (1, 300, 4, 2, 128, 307, ("list", [[]]), torch.bfloat16),
     (3, 129, 32, 8, 128, 64, ("list", [[128], [], [0, 64, 128]]), torch.bfloat16),
     (1, 200, 4, 2, 64, 50, "all", torch.float32),
@@ -121,18 +123,20 @@ def test_backward_small(case, with_q_out):
     compare_backward(wl, gpu, ref, do_b, what=str(case))
 
 
-def test_backward_many_tiles_per_key_block():
+@pytest.mark.parametrize("d", [128, 64])
+def test_backward_many_tiles_per_key_block(d):
     """GQA 16/1 with every position an output row: the first key block visits
     16 x (3 band + 64 output-row) = 1072 query tiles on the tensor-core path
     (the tile list is generated while the tiles stream, with no cap)."""
-    wl = W.small_prefill(1, 4096, 16, 1, 128, 64, out_mode="all", seed=21)
+    wl = W.small_prefill(1, 4096, 16, 1, d, 64, out_mode="all", seed=21)
     do_b, do_o = W.make_grad_outputs(wl, seed=22)
     compare_backward(wl, run_gpu_backward(wl, do_b, do_o), run_oracle_backward(wl, do_b, do_o), do_b,
                      what="1072 tiles per key block")
 
 
-def test_backward_key_offsets():
-    wl = W.small_prefill(1, 400, 8, 2, 128, 100, out_mode=("span", 150), seed=9, k_offset_std=0.5)
+@pytest.mark.parametrize("d", [128, 64])
+def test_backward_key_offsets(d):
+    wl = W.small_prefill(1, 400, 8, 2, d, 100, out_mode=("span", 150), seed=9, k_offset_std=0.5)
     do_b, do_o = W.make_grad_outputs(wl, seed=4)
     compare_backward(wl, run_gpu_backward(wl, do_b, do_o), run_oracle_backward(wl, do_b, do_o), do_b,
                      what="offsets")
