@@ -24,8 +24,13 @@ def pytest_sessionfinish(session, exitstatus):
     if MARGINS:
         import json
 
+        merged = {}
+        if os.path.exists(path):  # entries of earlier sessions stay unless measured again
+            with open(path) as f:
+                merged = json.load(f)
+        merged.update(MARGINS)
         with open(path, "w") as f:
-            json.dump(MARGINS, f, indent=1, sort_keys=True)
+            json.dump(merged, f, indent=1, sort_keys=True)
             f.write("\n")
 
 

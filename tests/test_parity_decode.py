@@ -4,6 +4,8 @@ Each step appends one token per sequence and runs the base (windowed) and
 output (full-history) queries; the cache state carries over between steps,
 so later steps also check the earlier appends.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -107,6 +109,20 @@ def test_decode_workload_sampled():
     tol_o, tol_l = TOL[torch.bfloat16]
     record_margin(W.DECODE_32.name, worst, {"o_base": tol_o, "lse_base": tol_l, "o_out": tol_o, "lse_out": tol_l},
                   f"max abs error vs the oracle over {steps} steps of {len(seqs)} sampled sequences")
+
+
+@pytest.mark.skipif(os.environ.get("ORTHROS_FULL_PARITY") != "1",
+                    reason="about a minute of oracle time; set ORTHROS_FULL_PARITY=1")
+def test_decode_workload_every_sequence():
+    """The 32-sequence decoding workload over all 128 steps, every sequence
+    compared with the oracle (413 GB of cache reads in the oracle)."""
+    steps = W.DECODE_32.steps
+    st = W.make_decode(W.DECODE_32, steps=steps)
+    worst = run_and_compare(st, steps, what="decode workload, every sequence")
+    tol_o, tol_l = TOL[torch.bfloat16]
+    record_margin(W.DECODE_32.name + ", every sequence", worst,
+                  {"o_base": tol_o, "lse_base": tol_l, "o_out": tol_o, "lse_out": tol_l},
+                  f"max abs error vs the oracle over {steps} steps of all 32 sequences")
 
 
 def test_decode_steps_replayed_from_a_cuda_graph():

@@ -4,6 +4,8 @@ Small shapes are compared in full (several tiles and a ragged tail); the
 named workloads run at full size in the launch configuration the benchmark
 times and are compared on sampled rows that the oracle computes one by one.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -86,6 +88,29 @@ def test_tiny_fp32_full():
     wl = W.make_prefill(W.TINY_FP32)
     errs = compare_prefill(wl, run_gpu_prefill(wl), what=W.TINY_FP32.name)
     record_margin(W.TINY_FP32.name, errs, prefill_tolerances(torch.float32), "max abs error vs the oracle, every row")
+
+
+@pytest.mark.parametrize("work", [W.PT_2K, W.SFT_8K], ids=lambda x: x.name)
+def test_named_workload_every_row(work):
+    """The pre-training and fine-tuning workloads at full size, in the
+    benchmark's launch, compared with the oracle on every base position and
+    every output row (the oracle takes a few seconds for these)."""
+    wl = W.make_prefill(work)
+    errs = compare_prefill(wl, run_gpu_prefill(wl), what=work.name)
+    record_margin(work.name + ", every row", errs, prefill_tolerances(work.dtype),
+                  "max abs error vs the oracle over every base position and every output row")
+
+
+@pytest.mark.skipif(os.environ.get("ORTHROS_FULL_PARITY") != "1",
+                    reason="about three minutes of oracle time on 16 cores; set ORTHROS_FULL_PARITY=1")
+def test_128k_every_row():
+    """The 128K prefill compared with the oracle on all 131072 positions x 32
+    heads and the output row (8.66 TFLOP of oracle work)."""
+    work = W.PREFILL_128K
+    wl = W.make_prefill(work)
+    errs = compare_prefill(wl, run_gpu_prefill(wl), what=work.name)
+    record_margin(work.name + ", every row", errs, prefill_tolerances(work.dtype),
+                  "max abs error vs the oracle over every base position and the output row")
 
 
 @pytest.mark.parametrize("work", [W.PT_2K, W.SFT_8K, W.PREFILL_128K], ids=lambda x: x.name)
