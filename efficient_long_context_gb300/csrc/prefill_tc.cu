@@ -867,6 +867,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const float mb = m_ref == -INFINITY ? 0.f : m_ref * c2u;
                 float ls[4] = {0.f, 0.f, 0.f, 0.f};
+                // (c2, c2) and (-mb, -mb) as f32x2 operands: the scaled, shifted logits and
+                // the row sums take one packed instruction per pair of keys
+                const uint64_t cv = f32x2(c2u, c2u), mv = f32x2(-mb, -mb);
                 // P for keys 64 hh .. 64 hh + 63 -> packed columns 32 hh .. 32 hh + 31
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
@@ -874,9 +877,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
-                        const float p0 = ex2(fmaf(x[2 * e], c2u, -mb));
-                        const float p1 = ex2(fmaf(x[2 * e + 1], c2u, -mb));
-                        ls[e & 3] += p0 + p1;
+                        float a0, a1;
+                        fma_f32x2(x[2 * e], x[2 * e + 1], cv, mv, a0, a1);
+                        const float p0 = ex2(a0), p1 = ex2(a1);
+                        add_f32x2(ls[2 * (e & 1)], ls[2 * (e & 1) + 1], p0, p1);
                         pk[e] = pack_bf16(p0, p1);
                     }
                     tmem_st16(t_s + 32 * hh + 16 * j, pk);

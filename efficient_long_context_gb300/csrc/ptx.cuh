@@ -311,6 +311,27 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
     return d;
 }
 
+// Packed pairs of floats (sm_100 and later: one instruction for two fp32
+// fused multiply-adds or adds, each rounded as its scalar form).
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+// (d0, d1) = (x0, x1) * b + c, b and c given as packed pairs
+__device__ __forceinline__ void fma_f32x2(float x0, float x1, uint64_t b, uint64_t c, float &d0, float &d1) {
+    asm("{\n\t.reg .b64 xv, r;\n\tmov.b64 xv, {%2, %3};\n\tfma.rn.f32x2 r, xv, %4, %5;\n\tmov.b64 {%0, %1}, r;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(x0), "f"(x1), "l"(b), "l"(c));
+}
+// (a0, a1) += (p0, p1)
+__device__ __forceinline__ void add_f32x2(float &a0, float &a1, float p0, float p1) {
+    asm("{\n\t.reg .b64 av, pv;\n\tmov.b64 av, {%0, %1};\n\tmov.b64 pv, {%2, %3};\n\tadd.rn.f32x2 av, av, pv;\n\t"
+        "mov.b64 {%0, %1}, av;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(p0), "f"(p1));
+}
+
 // 2^x with the hardware approximation (ex2.approx, flush-to-zero).
 __device__ __forceinline__ float ex2(float x) {
     float y;
