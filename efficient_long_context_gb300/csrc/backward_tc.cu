@@ -445,13 +445,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float ll[4] = {l4.x, l4.y, l4.z, l4.w};
                 const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
                 float pv[4], dsv[4];
+                // pairs of rows: one packed instruction each for the exponent's argument,
+                // dP * scale + (-D * scale), and P times that
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
+                for (int u = 0; u < 4; u += 2) {
                     const int e = 4 * q4 + u;
-                    const float pr = ex2(fmaf(__uint_as_float(sv[e]), c2, -ll[u]));
-                    const float pp = (unsigned)(tt[u] - j) < wlim ? pr : 0.f;
-                    pv[u] = pp;
-                    dsv[u] = pp * fmaf(__uint_as_float(dv[e]), p.scale, dd[u]);
+                    float a0, a1, g0, g1;
+                    fma2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), c2, c2, -ll[u], -ll[u + 1], a0, a1);
+                    pv[u] = (unsigned)(tt[u] - j) < wlim ? ex2(a0) : 0.f;
+                    pv[u + 1] = (unsigned)(tt[u + 1] - j) < wlim ? ex2(a1) : 0.f;
+                    fma2(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1]), p.scale, p.scale, dd[u], dd[u + 1], g0, g1);
+                    mul2(pv[u], pv[u + 1], g0, g1, dsv[u], dsv[u + 1]);
                 }
                 pk[2 * q4] = pack_bf16(pv[0], pv[1]);
                 pk[2 * q4 + 1] = pack_bf16(pv[2], pv[3]);

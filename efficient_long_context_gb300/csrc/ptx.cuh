@@ -332,6 +332,22 @@ __device__ __forceinline__ void add_f32x2(float &a0, float &a1, float p0, float 
         : "f"(p0), "f"(p1));
 }
 
+// (d0, d1) = (a0, a1) * (b0, b1) + (c0, c1), one packed instruction
+__device__ __forceinline__ void fma2(float a0, float a1, float b0, float b1, float c0, float c1, float &d0,
+                                     float &d1) {
+    asm("{\n\t.reg .b64 av, bv, cv, r;\n\tmov.b64 av, {%2, %3};\n\tmov.b64 bv, {%4, %5};\n\t"
+        "mov.b64 cv, {%6, %7};\n\tfma.rn.f32x2 r, av, bv, cv;\n\tmov.b64 {%0, %1}, r;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+// (d0, d1) = (a0, a1) * (b0, b1), one packed instruction
+__device__ __forceinline__ void mul2(float a0, float a1, float b0, float b1, float &d0, float &d1) {
+    asm("{\n\t.reg .b64 av, bv, r;\n\tmov.b64 av, {%2, %3};\n\tmov.b64 bv, {%4, %5};\n\t"
+        "mul.rn.f32x2 r, av, bv;\n\tmov.b64 {%0, %1}, r;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // 2^x with the hardware approximation (ex2.approx, flush-to-zero).
 __device__ __forceinline__ float ex2(float x) {
     float y;
