@@ -206,7 +206,9 @@ cudaError_t launch_prefill_key_rescale(const void *k, void *k16, int B, int T, i
                                        const unsigned *kmax_bits, AffineSet src, float *aff, int n_aff,
                                        cudaStream_t stream) {
     const long long n = (long long)B * T * Hkv * d * 2 / 16;
-    prefill_key_rescale_kernel<<<grid_for(n > 4LL * n_aff ? n : 4LL * n_aff, 256, 8), 256, 0, stream>>>(
+    // one block per SM: the affine copies are small, and the key pass (only for
+    // keys past the fp16 range) strides over the keys
+    prefill_key_rescale_kernel<<<grid_for(n > 4LL * n_aff ? n : 4LL * n_aff, 256, 1), 256, 0, stream>>>(
         (const uint4 *)k, (uint4 *)k16, n, kmax_bits, src, aff, n_aff);
     return cudaGetLastError();
 }
