@@ -355,6 +355,60 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// 2^a for a pair of values on the FMA and integer pipes instead of the
+// special-function unit. Method (classical range reduction): j = a rounded to
+// the nearest integer (adding 1.5 * 2^23 leaves j in the low mantissa bits of
+// the sum), f = a - j in [-1/2, 1/2], 2^f from a cubic in Horner form, and j
+// added to the exponent field of the result. The cubic's coefficients are a
+// near-minimax fit of 2^f on [-1/2, 1/2] in relative error (Lawson's
+// iteratively reweighted least squares): 7.5e-5 at most, 26 times below the
+// bf16 rounding that P goes through. Inputs are first raised to -127 (NaN
+// kept): -inf and everything at or below -127 give exactly +0 (the integer sum
+// turns negative there and is clamped to zero), inputs between -127 and -126 a
+// subnormal, and a NaN input gives NaN.
+__device__ __forceinline__ void exp2_fma_x2(float a0, float a1, float &p0, float &p1) {
+    uint32_t r0, r1;
+    asm("{\n\t"
+        ".reg .b64 av, tv, rv, fv, pv, kv;\n\t"
+        ".reg .b32 k, t0, t1, q0, q1, x0, x1;\n\t"
+        ".reg .pred n0, n1;\n\t"
+        "max.NaN.f32 x0, %2, 0fC2FE0000;\n\t"  // -127
+        "max.NaN.f32 x1, %3, 0fC2FE0000;\n\t"
+        "mov.b64 av, {x0, x1};\n\t"
+        "mov.b32 k, 0f4B400000;\n\t"  // 1.5 * 2^23
+        "mov.b64 kv, {k, k};\n\t"
+        "add.rn.f32x2 tv, av, kv;\n\t"
+        "sub.rn.f32x2 rv, tv, kv;\n\t"  // j
+        "sub.rn.f32x2 fv, av, rv;\n\t"  // f, exact
+        "mov.b32 k, 0f3D61FBB0;\n\t"    // c3 = 0.05517167
+        "mov.b64 pv, {k, k};\n\t"
+        "mov.b32 k, 0f3E786F0E;\n\t"    // c2 = 0.24261114
+        "mov.b64 kv, {k, k};\n\t"
+        "fma.rn.f32x2 pv, pv, fv, kv;\n\t"
+        "mov.b32 k, 0f3F31798D;\n\t"    // c1 = 0.69326097
+        "mov.b64 kv, {k, k};\n\t"
+        "fma.rn.f32x2 pv, pv, fv, kv;\n\t"
+        "mov.b32 k, 0f3F7FFB49;\n\t"    // c0 = 0.99992806
+        "mov.b64 kv, {k, k};\n\t"
+        "fma.rn.f32x2 pv, pv, fv, kv;\n\t"
+        "mov.b64 {t0, t1}, tv;\n\t"
+        "mov.b64 {q0, q1}, pv;\n\t"
+        // bits(sum) << 23 is j << 23 modulo 2^32: the exponent field moves by j
+        "mad.lo.u32 x0, t0, 8388608, q0;\n\t"
+        "mad.lo.u32 x1, t1, 8388608, q1;\n\t"
+        "max.s32 x0, x0, 0;\n\t"
+        "max.s32 x1, x1, 0;\n\t"
+        "testp.notanumber.f32 n0, %2;\n\t"
+        "testp.notanumber.f32 n1, %3;\n\t"
+        "selp.b32 %0, 2147483647, x0, n0;\n\t"
+        "selp.b32 %1, 2147483647, x1, n1;\n\t"
+        "}"
+        : "=r"(r0), "=r"(r1)
+        : "f"(a0), "f"(a1));
+    p0 = __uint_as_float(r0);
+    p1 = __uint_as_float(r1);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));

@@ -289,3 +289,39 @@ def test_shard_partials_on_gpu_match_oracle_shard(oracle_mod):
     ro, rl = torch_merge(parts.double(), lses.double(), torch.float64)
     assert float((o.cpu().double() - ro).abs().max()) <= 1e-5
     assert float((lse.cpu().double() - rl).abs().max()) <= 1e-5
+
+
+@pytest.mark.gpu
+def test_shard_tile_path_rows_without_keys(oracle_mod):
+    """Enough output rows that the sequence takes the tensor-core tile kernel
+    (not the split-KV kernel), a third of them placed before the chunk's first
+    key: those rows share tiles with rows that have keys, see only masked
+    logits, and must come back exactly o = 0, lse = -inf."""
+    import efficient_long_context_gb300 as ola
+    from tests.parity_util import TOL
+
+    g = torch.Generator().manual_seed(22)
+    B, C, H, Hq, Hkv, d, w = 1, 256, 128, 8, 2, 128, 128
+    n = 1200  # more than 256 16-row groups of 4 query heads: the tile kernel
+    q = torch.randn((B, C, Hq, d), generator=g).to(torch.bfloat16)
+    k = torch.randn((B, H + C, Hkv, d), generator=g).to(torch.bfloat16)
+    v = torch.randn((B, H + C, Hkv, d), generator=g).to(torch.bfloat16)
+    aff = [1 + 0.1 * torch.randn((Hq, d), generator=g), 0.1 * torch.randn((Hq, d), generator=g),
+           1 + 0.1 * torch.randn((Hq, d), generator=g), 0.1 * torch.randn((Hq, d), generator=g)]
+    indptr = torch.tensor([0, n], dtype=torch.int32)
+    pos = torch.sort(torch.randint(0, H + C, (n,), generator=g, dtype=torch.int32)).values
+    assert int((pos < H).sum()) > n // 5
+    q_rows = torch.randn((n, Hq, d), generator=g).to(torch.bfloat16)
+    dev = "cuda"
+    got = ola.orthros_prefill_shard(q.to(dev), k.to(dev), v.to(dev), *(a.to(dev) for a in aff), indptr, pos.to(dev),
+                                    w, d ** -0.5, q_rows=q_rows.to(dev))
+    ref = oracle_shard(q.float(), k.float(), v.float(), *aff, indptr, pos, w, d ** -0.5, q_rows=q_rows.float())
+    tol_o, tol_l = TOL[torch.bfloat16]
+    for name, a, r, tol in zip(("o_base", "lse_base", "o_part", "lse_part"), got, ref, (tol_o, tol_l, tol_o, tol_l)):
+        a = a.float().cpu()
+        fin = torch.isfinite(r)
+        assert torch.equal(torch.isfinite(a), fin), name
+        assert float((a[fin] - r[fin]).abs().max()) <= tol, name
+    empty = pos < H
+    assert torch.equal(got[2].cpu()[empty], torch.zeros_like(got[2].cpu()[empty]))  # exactly zero
+    assert bool(torch.isneginf(got[3].cpu()[empty]).all())
