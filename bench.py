@@ -431,26 +431,37 @@ def bench_prefill(args, dist, dev, stream, peaks, ola, torch, W, wl, e2e=False):
                          "peak_source": f"{peaks['src']} bf16 dense (burst)", "avg_launch_ms": dom_ms / dom_n,
                          "useful_tflop_per_launch": dom_flops / 1e12})
     if e2e:
-        # end to end: pinned host buffers, host<->device copies inside the timed region
+        # end to end through orthros_prefill_from_host: pinned host buffers in
+        # and out, the copies inside the timed region (chunked, overlapping the
+        # compute on the library's copy streams), the same cache fill
         h_in = {n: inputs[n].pin_memory() for n in ("q", "k", "v")}
         h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+        h_pos = inputs["out_positions"].to(torch.int32).contiguous()
+        ws_fh = torch.empty(ola.orthros_prefill_from_host_workspace_size(wl.B, wl.T, wl.Hq, wl.Hkv, wl.d, n_out,
+                                                                         wl.window, wl.dtype),
+                            dtype=torch.uint8, device=dev)
 
         def e2e_step(_):
-            q.copy_(h_in["q"], non_blocking=True)
-            k.copy_(h_in["k"], non_blocking=True)
-            v.copy_(h_in["v"], non_blocking=True)
-            step()
-            for hbuf, dbuf in zip(h_out, outs):
-                hbuf.copy_(dbuf, non_blocking=True)
+            ola.orthros_prefill_from_host(h_in["q"], h_in["k"], h_in["v"], *aff, indptr, h_pos, wl.window, wl.scale,
+                                          out=h_out, k_cache=k_cache, v_cache=v_cache, block_table=block_table,
+                                          page_size=P, workspace=ws_fh, stream=stream)
 
         e2e_steps = max(1, min(args.steps, 3))
         e2e_step(0)
-        ms_e2e, _ = _timed(ola, torch, dist, stream, e2e_step, e2e_steps)
+        torch.cuda.synchronize()
+        rc, bits = ola.orthros_check(ws_fh)
+        if rc != 0:
+            raise RuntimeError(f"prefill from host flagged device status {rc} bits 0x{bits:x}")
+        ms_e2e, prof_e2e = _timed(ola, torch, dist, stream, e2e_step, e2e_steps)
         ms_e2e /= e2e_steps
+        # bytes copied per step: q, k, v, the output rows' queries and positions in; every output out
+        qrow = wl.Hq * wl.d * q.element_size()
+        h2d = sum(t.numel() * t.element_size() for t in h_in.values()) + n_out * (qrow + 4)
         res["e2e"] = {"value": flops["total"] * dist.world / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
-                      "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in h_in.values()),
+                      "h2d_bytes_per_step": h2d,
                       "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in h_out),
-                      "ms_per_step": ms_e2e, "steps": e2e_steps}
+                      "ms_per_step": ms_e2e, "steps": e2e_steps, "api": "orthros_prefill_from_host",
+                      "kernels": {n: {"launches": c, "total_ms": t} for n, (c, t) in prof_e2e.items()}}
     return res
 
 

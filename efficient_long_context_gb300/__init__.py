@@ -23,6 +23,8 @@ from ._binding import (  # noqa: F401
     orthros_prefill,
     orthros_prefill_backward,
     orthros_prefill_backward_workspace_size,
+    orthros_prefill_from_host,
+    orthros_prefill_from_host_workspace_size,
     orthros_prefill_shard,
     orthros_prefill_shard_workspace_size,
     orthros_prefill_workspace_size,

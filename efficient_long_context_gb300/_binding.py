@@ -21,7 +21,8 @@ STATUS_NAMES = {0: "ORTHROS_OK", 1: "ORTHROS_EINVAL", 2: "ORTHROS_EUNSUPPORTED",
                 4: "ORTHROS_EWORKSPACE", 5: "ORTHROS_EDEVICE", 6: "ORTHROS_ETIMEOUT"}
 
 # the public symbols of include/orthros_attn.h
-EXPORTS = ("orthros_prefill_workspace_size", "orthros_prefill", "orthros_prefill_shard_workspace_size",
+EXPORTS = ("orthros_prefill_workspace_size", "orthros_prefill", "orthros_prefill_from_host_workspace_size",
+           "orthros_prefill_from_host", "orthros_prefill_shard_workspace_size",
            "orthros_prefill_shard", "orthros_merge_partials", "orthros_prefill_backward_workspace_size",
            "orthros_prefill_backward", "orthros_extend_workspace_size", "orthros_extend", "orthros_qkv_project",
            "orthros_decode_workspace_size",
@@ -62,6 +63,12 @@ def load_library(path: str | None = None):
         lib.orthros_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32p, vp, i32, vp,
                                         i32, i32, i32, i32, i32, i32, ctypes.c_float, i32,
                                         vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp, sz, vp]
+        lib.orthros_prefill_from_host_workspace_size.restype = sz
+        lib.orthros_prefill_from_host_workspace_size.argtypes = [i32] * 8
+        lib.orthros_prefill_from_host.restype = i32
+        lib.orthros_prefill_from_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32p, i32p, i32, vp,
+                                                  i32, i32, i32, i32, i32, i32, ctypes.c_float, i32,
+                                                  vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp, sz, vp]
         lib.orthros_prefill_shard_workspace_size.restype = sz
         lib.orthros_prefill_shard_workspace_size.argtypes = [i32] * 9
         lib.orthros_prefill_shard.restype = i32
@@ -206,6 +213,69 @@ def orthros_prefill(q, k, v, alpha_base, beta_base, alpha_out, beta_out, out_ind
         indptr.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), _ptr(out_positions), n_out, _ptr(q_out),
         B, T, Hq, Hkv, d, int(window), float(scale), _dtype(q),
         _ptr(o_base), _ptr(lse_base), _ptr(o_out), _ptr(lse_out),
+        _ptr(k_cache), _ptr(v_cache), _ptr(block_table), max_pages, int(page_size), num_pages,
+        _ptr(workspace), workspace.numel(), _stream(stream))
+    _raise_if(rc, lib)
+    return o_base, lse_base, o_out, lse_out
+
+
+def _host_ptr(t):
+    """Host address of a CPU tensor argument of orthros_prefill_from_host."""
+    if t is None:
+        return None
+    if t.is_cuda:
+        raise OrthrosError(1, "orthros_prefill_from_host takes its inputs and outputs in host memory")
+    _contig("host tensor", t)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def orthros_prefill_from_host_workspace_size(B, T, Hq, Hkv, d, n_out, window, dtype=torch.bfloat16) -> int:
+    return int(load_library().orthros_prefill_from_host_workspace_size(B, T, Hq, Hkv, d, n_out, window,
+                                                                       _DTYPES[dtype]))
+
+
+def orthros_prefill_from_host(q, k, v, alpha_base, beta_base, alpha_out, beta_out, out_indptr, out_positions,
+                              window, scale=None, *, q_out=None, out=None, k_cache=None, v_cache=None,
+                              block_table=None, page_size=0, workspace=None, stream=None):
+    """orthros_prefill_from_host of include/orthros_attn.h.
+
+    q, k, v, out_positions, q_out and the outputs are CPU tensors (pinned, for
+    copies that overlap the compute); the affines, the optional cache and the
+    workspace are CUDA tensors. Returns (o_base, lse_base, o_out, lse_out) as
+    CPU tensors, allocated here (pinned) unless `out` gives all four. The
+    outputs are complete once `stream` has passed this call.
+    """
+    lib = load_library()
+    B, T, Hq, d = q.shape
+    Hkv = k.shape[2]
+    indptr = np.ascontiguousarray(np.asarray(out_indptr.cpu() if isinstance(out_indptr, torch.Tensor)
+                                             else out_indptr, dtype=np.int32))
+    n_out = int(indptr[-1]) if indptr.size else 0
+    pos = np.ascontiguousarray(np.asarray(out_positions.cpu() if isinstance(out_positions, torch.Tensor)
+                                          else out_positions, dtype=np.int32))
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        pin = torch.cuda.is_available()
+        o_base = torch.empty(q.shape, dtype=q.dtype, pin_memory=pin)
+        lse_base = torch.empty((B, Hq, T), dtype=torch.float32, pin_memory=pin)
+        o_out = torch.empty((n_out, Hq, d), dtype=q.dtype, pin_memory=pin)
+        lse_out = torch.empty((n_out, Hq), dtype=torch.float32, pin_memory=pin)
+    else:
+        o_base, lse_base, o_out, lse_out = out
+    dev = alpha_base.device
+    if workspace is None:
+        ws = orthros_prefill_from_host_workspace_size(B, T, Hq, Hkv, d, n_out, window, q.dtype)
+        workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev)
+    max_pages = block_table.shape[1] if block_table is not None else 0
+    num_pages = k_cache.shape[0] if k_cache is not None else 0
+    rc = lib.orthros_prefill_from_host(
+        _host_ptr(q), _host_ptr(k), _host_ptr(v), _ptr(alpha_base), _ptr(beta_base), _ptr(alpha_out),
+        _ptr(beta_out), indptr.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+        pos.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)) if n_out else None, n_out, _host_ptr(q_out),
+        B, T, Hq, Hkv, d, int(window), float(scale), _dtype(q),
+        _host_ptr(o_base), _host_ptr(lse_base), _host_ptr(o_out) if n_out else None,
+        _host_ptr(lse_out) if n_out else None,
         _ptr(k_cache), _ptr(v_cache), _ptr(block_table), max_pages, int(page_size), num_pages,
         _ptr(workspace), workspace.numel(), _stream(stream))
     _raise_if(rc, lib)

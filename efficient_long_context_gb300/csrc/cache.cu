@@ -263,4 +263,34 @@ cudaError_t launch_prefill_cache_fill(const void *k, const void *v, void *k_cach
     return cudaGetLastError();
 }
 
+// Output-row positions of one chunk of a chunked prefill, in that chunk's
+// key-buffer coordinates: global position - off, raised to 0 (a row before the
+// chunk's keys, whose buffer starts with at least one halo key, then reads
+// nothing).
+__global__ void shift_positions_kernel(const int32_t *__restrict__ src, int32_t *__restrict__ dst, int n, int off) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) dst[i] = max(src[i] - off, 0);
+}
+
+// dst[0] |= src[k * stride] for k < n: the status words of the calls a
+// chunked prefill made, folded into its own.
+__global__ void fold_status_kernel(uint32_t *dst, const uint32_t *__restrict__ src, int n, int stride) {
+    uint32_t bits = 0;
+    for (int k = threadIdx.x; k < n; k += blockDim.x) bits |= src[(long long)k * stride];
+    for (int o = 16; o > 0; o >>= 1) bits |= __shfl_xor_sync(0xffffffffu, bits, o);
+    if (threadIdx.x == 0 && bits) atomicOr(dst, bits);
+}
+
+cudaError_t launch_shift_positions(const int32_t *src, int32_t *dst, int n, int off, cudaStream_t stream) {
+    if (n <= 0) return cudaSuccess;
+    shift_positions_kernel<<<(n + 255) / 256, 256, 0, stream>>>(src, dst, n, off);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fold_status(uint32_t *dst, const uint32_t *src, int n, int stride_words, cudaStream_t stream) {
+    if (n <= 0) return cudaSuccess;
+    fold_status_kernel<<<1, 32, 0, stream>>>(dst, src, n, stride_words);
+    return cudaGetLastError();
+}
+
 }  // namespace orthros

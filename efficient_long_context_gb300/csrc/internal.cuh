@@ -312,5 +312,8 @@ cudaError_t launch_prefill_cache_fill(const void *k, const void *v, void *k_cach
                                       const int32_t *block_table, int B, int T, int Hkv, int d,
                                       int max_pages, int page_size, int num_pages, int elem_bytes,
                                       uint32_t *status, cudaStream_t stream);
+// cache.cu: chunked prefill helpers (output-row positions per chunk, status fold).
+cudaError_t launch_shift_positions(const int32_t *src, int32_t *dst, int n, int off, cudaStream_t stream);
+cudaError_t launch_fold_status(uint32_t *dst, const uint32_t *src, int n, int stride_words, cudaStream_t stream);
 
 }  // namespace orthros

@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -483,6 +484,341 @@ orthros_status prefill_core(const void *q, const void *k, const void *v, const f
     return ORTHROS_OK;
 }
 
+
+// ---------------------------------------------------------------------------
+// orthros_prefill_from_host: the prefill with its inputs and outputs in host
+// memory. Sequences longer than one chunk are cut into chunks of the token
+// axis that run as shards (base rows exact with a halo of keys; output rows as
+// partials merged at the end), so that the host-to-device copy of chunk c + 1,
+// the compute of chunk c and the device-to-host copy of chunk c - 1 overlap on
+// three streams.
+// ---------------------------------------------------------------------------
+constexpr int kHostChunkMin = 16384;
+constexpr size_t kSlotBytes = 256;  // one shard call's status words
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Rows per chunk: at least 16384 and at least four halos, so that the halo
+// keys each chunk converts again stay a small share of its work.
+int host_chunk_rows(int T, int window) {
+    const long long halo = std::max(window - 1, 1);
+    const long long c = std::max<long long>(kHostChunkMin, 4 * ((halo + 127) / 128) * 128);
+    return (int)std::min<long long>(c, std::max(T, 1));
+}
+
+// Chunk boundaries of a sequence of T tokens: a quarter chunk first (the
+// compute starts after a short copy in), full chunks, and the remainder ending
+// in a quarter chunk (a short copy out after the last compute).
+std::vector<int> chunk_starts(int T, int chunk) {
+    std::vector<int> st;
+    if (T <= chunk) {
+        st.push_back(0);
+    } else {
+        const int quarter = std::max(128, (chunk / 4) & ~127);
+        int t = 0;
+        st.push_back(t);
+        t += quarter;
+        while (T - t > chunk + quarter) {
+            st.push_back(t);
+            t += chunk;
+        }
+        if (T - t > quarter) {
+            st.push_back(t);
+            t = T - quarter;
+        }
+        st.push_back(t);
+    }
+    st.push_back(T);
+    return st;  // chunk c covers [st[c], st[c + 1])
+}
+
+struct FromHostLayout {
+    bool pipelined;
+    std::vector<int> starts;
+    int chunk, n_chunks, halo_max, max_rows;
+    size_t q_off, k_off, v_off, o_off, lse_off, qrows_off, pos_off, pos_chunk_off, parts_off, lparts_off, oout_off,
+        lout_off, core_off, core_bytes, total;
+};
+
+FromHostLayout from_host_layout(int B, int T, int Hq, int Hkv, int d, int n_out, int window, orthros_dtype dtype) {
+    FromHostLayout L{};
+    const size_t eb = elem_bytes(dtype);
+    L.chunk = host_chunk_rows(T, window);
+    L.starts = chunk_starts(T, L.chunk);
+    L.n_chunks = T > 0 ? (int)L.starts.size() - 1 : 0;
+    L.pipelined = dtype == ORTHROS_BF16 && L.n_chunks >= 2;
+    L.halo_max = std::min(std::max(window - 1, 1), std::max(T, 1));
+    L.max_rows = n_out;  // a sequence's output rows, at most
+    const size_t bt = (size_t)B * T;
+    size_t off;
+    if (L.pipelined) {
+        L.core_bytes = prefill_layout(1, L.chunk + L.halo_max, Hq, Hkv, d, L.max_rows, dtype).total;
+        off = kSlotBytes;  // this call's own status words
+        L.core_off = off;  // one status slot per shard call, then the shard workspace
+        off = align256(off + (size_t)B * L.n_chunks * kSlotBytes + L.core_bytes);
+        L.lse_off = off;  // two chunk-sized lse_base buffers (double-buffered against the copy out)
+        off = align256(off + 2 * (size_t)Hq * L.chunk * 4);
+        L.qrows_off = off;
+        off = align256(off + (size_t)n_out * Hq * d * eb);
+        L.pos_chunk_off = off;
+        off = align256(off + (size_t)n_out * 4);
+        L.parts_off = off;
+        off = align256(off + (size_t)L.n_chunks * n_out * Hq * d * 4);
+        L.lparts_off = off;
+        off = align256(off + (size_t)L.n_chunks * n_out * Hq * 4);
+    } else {
+        L.core_bytes = prefill_layout(B, T, Hq, Hkv, d, n_out, dtype).total;
+        L.core_off = 0;  // its status words are this call's
+        off = align256(L.core_bytes);
+        L.lse_off = off;
+        off = align256(off + (size_t)B * Hq * T * 4);
+        L.qrows_off = off;  // q_out, when given
+        off = align256(off + (size_t)n_out * Hq * d * eb);
+    }
+    L.pos_off = off;
+    off = align256(off + (size_t)n_out * 4);
+    L.oout_off = off;
+    off = align256(off + (size_t)n_out * Hq * d * eb);
+    L.lout_off = off;
+    off = align256(off + (size_t)n_out * Hq * 4);
+    L.q_off = off;
+    off = align256(off + bt * Hq * d * eb);
+    L.k_off = off;
+    off = align256(off + bt * Hkv * d * eb);
+    L.v_off = off;
+    off = align256(off + bt * Hkv * d * eb);
+    L.o_off = off;
+    off = align256(off + bt * Hq * d * eb);
+    L.total = off;
+    return L;
+}
+
+// Copy streams and events of the pipelined path, created once per device.
+struct HostPipe {
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t start = nullptr, in_done = nullptr, comp_done = nullptr, out_done[2] = {nullptr, nullptr},
+                end = nullptr;
+};
+constexpr int kPipeDevices = 64;
+std::mutex g_pipe_mu;  // held for a whole call's enqueueing: the events are shared
+HostPipe g_pipe[kPipeDevices];
+
+cudaError_t host_pipe(HostPipe **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kPipeDevices) return cudaErrorInvalidDevice;
+    HostPipe &hp = g_pipe[dev];
+    if (!hp.end) {
+        if ((e = cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking)) != cudaSuccess) return e;
+        if ((e = cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking)) != cudaSuccess) return e;
+        for (cudaEvent_t *ev : {&hp.start, &hp.in_done, &hp.comp_done, &hp.out_done[0], &hp.out_done[1], &hp.end})
+            if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess) return e;
+    }
+    *out = &hp;
+    return cudaSuccess;
+}
+
+// A host argument must not be device memory (page-locked host memory lets the
+// copies overlap; pageable memory works, with copies that do not).
+bool is_host_memory(const void *p) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return true;  // unknown to CUDA: plain pageable memory
+    }
+    return at.type == cudaMemoryTypeHost || at.type == cudaMemoryTypeUnregistered;
+}
+
+orthros_status from_host_core(const void *q, const void *k, const void *v, const float *alpha_base,
+                              const float *beta_base, const float *alpha_out, const float *beta_out,
+                              const int32_t *out_indptr, const int32_t *out_positions, int n_out, const void *q_out,
+                              int B, int T, int Hq, int Hkv, int d, int window, float scale, orthros_dtype dtype,
+                              void *o_base, float *lse_base, void *o_out, float *lse_out, void *k_cache,
+                              void *v_cache, const int32_t *block_table, int max_pages, int page_size, int num_pages,
+                              void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    orthros_status st = check_shapes(B, Hq, Hkv, d, window, scale, dtype);
+    if (st != ORTHROS_OK) return st;
+    if (T < 0 || n_out < 0) return fail(ORTHROS_EINVAL, "T = %d and n_out = %d must be >= 0", T, n_out);
+    if (B > 0 && !out_indptr) return fail(ORTHROS_EINVAL, "out_indptr (host) must not be NULL");
+    if (B > 0 && (out_indptr[0] != 0 || out_indptr[B] != n_out))
+        return fail(ORTHROS_EINVAL, "out_indptr must run from 0 to n_out = %d", n_out);
+    for (int b = 0; b < B; ++b)
+        if (out_indptr[b + 1] < out_indptr[b]) return fail(ORTHROS_EINVAL, "out_indptr decreases at %d", b);
+    if (n_out > 0) {
+        if (!out_positions || !o_out || !lse_out)
+            return fail(ORTHROS_EINVAL, "out_positions, o_out and lse_out must not be NULL when n_out > 0");
+        for (int r = 0; r < n_out; ++r)
+            if (out_positions[r] < 0 || out_positions[r] >= T)
+                return fail(ORTHROS_EINVAL, "out_positions[%d] = %d lies outside [0, T = %d)", r, out_positions[r], T);
+    }
+    const long long bt = (long long)B * T;
+    if (bt > 0 && (!q || !k || !v || !o_base || !lse_base))
+        return fail(ORTHROS_EINVAL, "q, k, v, o_base and lse_base must not be NULL");
+    for (const void *h : {q, k, v, (const void *)o_base, (const void *)lse_base, q_out, (const void *)o_out,
+                          (const void *)lse_out, (const void *)out_positions})
+        if (h && !is_host_memory(h)) return fail(ORTHROS_EINVAL, "inputs and outputs must be host memory");
+    const FromHostLayout L = from_host_layout(B, T, Hq, Hkv, d, n_out, window, dtype);
+    if (!workspace || workspace_bytes < L.total)
+        return fail(ORTHROS_EWORKSPACE, "workspace needs %zu bytes, got %zu", L.total, workspace ? workspace_bytes : (size_t)0);
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(ORTHROS_EINVAL, "workspace must be 256-byte aligned");
+    char *ws = static_cast<char *>(workspace);
+    const size_t eb = elem_bytes(dtype);
+    const size_t qrow = (size_t)Hq * d * eb, kvrow = (size_t)Hkv * d * eb;
+    char *qd = ws + L.q_off, *kd = ws + L.k_off, *vd = ws + L.v_off, *od = ws + L.o_off;
+    int32_t *pos_d = reinterpret_cast<int32_t *>(ws + L.pos_off);
+    char *oout_d = ws + L.oout_off;
+    float *lout_d = reinterpret_cast<float *>(ws + L.lout_off);
+    cudaError_t e;
+#define ORTHROS_CU(call, what)                          \
+    do {                                                \
+        if ((e = (call)) != cudaSuccess) return cuda_fail(e, what); \
+    } while (0)
+
+    if (!L.pipelined) {
+        // one chunk per sequence: copy in, compute, copy out, all on the caller's stream
+        ORTHROS_CU(cudaMemcpyAsync(qd, q, bt * qrow, cudaMemcpyHostToDevice, stream), "q copy in");
+        ORTHROS_CU(cudaMemcpyAsync(kd, k, bt * kvrow, cudaMemcpyHostToDevice, stream), "k copy in");
+        ORTHROS_CU(cudaMemcpyAsync(vd, v, bt * kvrow, cudaMemcpyHostToDevice, stream), "v copy in");
+        const void *qo_d = nullptr;
+        if (n_out > 0) {
+            ORTHROS_CU(cudaMemcpyAsync(pos_d, out_positions, (size_t)n_out * 4, cudaMemcpyHostToDevice, stream),
+                       "positions copy in");
+            if (q_out) {
+                ORTHROS_CU(cudaMemcpyAsync(ws + L.qrows_off, q_out, (size_t)n_out * qrow, cudaMemcpyHostToDevice, stream),
+                           "q_out copy in");
+                qo_d = ws + L.qrows_off;
+            }
+        }
+        float *lse_d = reinterpret_cast<float *>(ws + L.lse_off);
+        st = prefill_core(qd, kd, vd, alpha_base, beta_base, alpha_out, beta_out, out_indptr, pos_d, n_out, qo_d, B, T,
+                          T, false, Hq, Hkv, d, window, scale, dtype, od, lse_d, oout_d, nullptr, lout_d, k_cache,
+                          v_cache, block_table, max_pages, page_size, num_pages, ws + L.core_off, L.core_bytes, stream);
+        if (st != ORTHROS_OK) return st;
+        ORTHROS_CU(cudaMemcpyAsync(o_base, od, bt * qrow, cudaMemcpyDeviceToHost, stream), "o_base copy out");
+        ORTHROS_CU(cudaMemcpyAsync(lse_base, lse_d, bt * Hq * 4, cudaMemcpyDeviceToHost, stream), "lse_base copy out");
+        if (n_out > 0) {
+            ORTHROS_CU(cudaMemcpyAsync(o_out, oout_d, (size_t)n_out * qrow, cudaMemcpyDeviceToHost, stream),
+                       "o_out copy out");
+            ORTHROS_CU(cudaMemcpyAsync(lse_out, lout_d, (size_t)n_out * Hq * 4, cudaMemcpyDeviceToHost, stream),
+                       "lse_out copy out");
+        }
+        return ORTHROS_OK;
+    }
+
+    // ---- pipelined: chunks of the token axis as shards ----
+    if (n_out > 0 && (!alpha_out || !beta_out)) return fail(ORTHROS_EINVAL, "alpha_out and beta_out must not be NULL");
+    const bool fill = k_cache || v_cache || block_table;
+    if (fill) {
+        if (!k_cache || !v_cache || !block_table)
+            return fail(ORTHROS_EINVAL, "k_cache, v_cache and block_table must be all NULL or all set");
+        if (page_size < 1 || max_pages < 1 || num_pages < 1 || (long long)max_pages * page_size < T)
+            return fail(ORTHROS_EINVAL, "the cache fill needs page_size, max_pages, num_pages >= 1, max_pages * page_size >= T");
+    }
+    HostPipe *hp = nullptr;
+    std::lock_guard<std::mutex> lock(g_pipe_mu);
+    ORTHROS_CU(host_pipe(&hp), "copy streams");
+    uint32_t *status = reinterpret_cast<uint32_t *>(ws);
+    ORTHROS_CU(cudaMemsetAsync(status, 0, 4 * sizeof(uint32_t), stream), "status reset");
+    if (n_out > 0)
+        ORTHROS_CU(cudaMemcpyAsync(pos_d, out_positions, (size_t)n_out * 4, cudaMemcpyHostToDevice, stream),
+                   "positions copy in");
+    ORTHROS_CU(cudaEventRecord(hp->start, stream), "event");
+    ORTHROS_CU(cudaStreamWaitEvent(hp->in, hp->start, 0), "event wait");
+    ORTHROS_CU(cudaStreamWaitEvent(hp->out, hp->start, 0), "event wait");
+    // the output rows' raw queries, needed by every chunk: q_out, or runs of
+    // consecutive positions of q
+    char *qrows_d = ws + L.qrows_off;
+    if (n_out > 0) {
+        if (q_out) {
+            ORTHROS_CU(cudaMemcpyAsync(qrows_d, q_out, (size_t)n_out * qrow, cudaMemcpyHostToDevice, hp->in),
+                       "q_out copy in");
+        } else {
+            for (int b = 0; b < B; ++b)
+                for (int r = out_indptr[b]; r < out_indptr[b + 1];) {
+                    int n = 1;
+                    while (r + n < out_indptr[b + 1] && out_positions[r + n] == out_positions[r] + n) ++n;
+                    ORTHROS_CU(cudaMemcpyAsync(qrows_d + (size_t)r * qrow,
+                                               static_cast<const char *>(q) + ((size_t)b * T + out_positions[r]) * qrow,
+                                               (size_t)n * qrow, cudaMemcpyHostToDevice, hp->in),
+                               "output-row queries copy in");
+                    r += n;
+                }
+        }
+    }
+    int32_t *pos_chunk = reinterpret_cast<int32_t *>(ws + L.pos_chunk_off);
+    float *parts = reinterpret_cast<float *>(ws + L.parts_off);
+    float *lparts = reinterpret_cast<float *>(ws + L.lparts_off);
+    const size_t part_stride = (size_t)n_out * Hq * d, lpart_stride = (size_t)n_out * Hq;
+    int slot = 0;
+    for (int b = 0; b < B; ++b) {
+        const int r0 = out_indptr[b], nb = out_indptr[b + 1] - out_indptr[b];
+        for (int c = 0; c < L.n_chunks; ++c, ++slot) {
+            const int t0 = L.starts[c], tq = L.starts[c + 1] - t0;
+            const int halo = c == 0 ? 0 : std::min(L.halo_max, t0);
+            const size_t row0 = (size_t)b * T + t0;
+            // in: this chunk's rows (its halo came with the chunks before it)
+            ORTHROS_CU(cudaMemcpyAsync(qd + row0 * qrow, static_cast<const char *>(q) + row0 * qrow, (size_t)tq * qrow,
+                                       cudaMemcpyHostToDevice, hp->in), "q copy in");
+            ORTHROS_CU(cudaMemcpyAsync(kd + row0 * kvrow, static_cast<const char *>(k) + row0 * kvrow,
+                                       (size_t)tq * kvrow, cudaMemcpyHostToDevice, hp->in), "k copy in");
+            ORTHROS_CU(cudaMemcpyAsync(vd + row0 * kvrow, static_cast<const char *>(v) + row0 * kvrow,
+                                       (size_t)tq * kvrow, cudaMemcpyHostToDevice, hp->in), "v copy in");
+            ORTHROS_CU(cudaEventRecord(hp->in_done, hp->in), "event");
+            ORTHROS_CU(cudaStreamWaitEvent(stream, hp->in_done, 0), "event wait");
+            // compute: the chunk as a shard (its lse_base buffer waits for the copy
+            // out of the chunk that used it two chunks ago)
+            if (slot >= 2) ORTHROS_CU(cudaStreamWaitEvent(stream, hp->out_done[slot & 1], 0), "event wait");
+            float *lse_c = reinterpret_cast<float *>(ws + L.lse_off) + (size_t)(slot & 1) * Hq * L.chunk;
+            if (nb > 0) ORTHROS_CU(launch_shift_positions(pos_d + r0, pos_chunk + r0, nb, t0 - halo, stream), "positions");
+            const int32_t rows_indptr[2] = {0, nb};
+            st = prefill_core(qd + row0 * qrow, kd + (row0 - halo) * kvrow, vd + (row0 - halo) * kvrow, alpha_base,
+                              beta_base, alpha_out, beta_out, rows_indptr, pos_chunk + r0, nb,
+                              nb > 0 ? qrows_d + (size_t)r0 * qrow : nullptr, 1, halo + tq, tq, true, Hq, Hkv, d,
+                              window, scale, dtype, od + row0 * qrow, lse_c, nullptr,
+                              nb > 0 ? parts + c * part_stride + (size_t)r0 * Hq * d : nullptr,
+                              nb > 0 ? lparts + c * lpart_stride + (size_t)r0 * Hq : nullptr, nullptr, nullptr,
+                              nullptr, 0, 0, 0, ws + L.core_off + (size_t)slot * kSlotBytes, L.core_bytes, stream);
+            if (st != ORTHROS_OK) return st;
+            ORTHROS_CU(cudaEventRecord(hp->comp_done, stream), "event");
+            // out: the chunk's o_base rows and its lse_base columns
+            ORTHROS_CU(cudaStreamWaitEvent(hp->out, hp->comp_done, 0), "event wait");
+            ORTHROS_CU(cudaMemcpyAsync(static_cast<char *>(o_base) + row0 * qrow, od + row0 * qrow, (size_t)tq * qrow,
+                                       cudaMemcpyDeviceToHost, hp->out), "o_base copy out");
+            ORTHROS_CU(cudaMemcpy2DAsync(lse_base + (size_t)b * Hq * T + t0, (size_t)T * 4, lse_c, (size_t)tq * 4,
+                                         (size_t)tq * 4, Hq, cudaMemcpyDeviceToHost, hp->out), "lse_base copy out");
+            ORTHROS_CU(cudaEventRecord(hp->out_done[slot & 1], hp->out), "event");
+        }
+    }
+    // the output rows' partials merged; the cache filled from the keys and values
+    // now on the device; every shard's status folded into this call's
+    if (n_out > 0) {
+        ProfScope ps("merge_partials", stream);
+        ORTHROS_CU(launch_merge_partials(parts, lparts, L.n_chunks, n_out, Hq, d, false, oout_d, lout_d, stream),
+                   "merge launch");
+    }
+    if (fill) {
+        ProfScope ps("cache_fill", stream);
+        ORTHROS_CU(launch_prefill_cache_fill(kd, vd, k_cache, v_cache, block_table, B, T, Hkv, d, max_pages, page_size,
+                                             num_pages, (int)eb, status, stream), "cache fill launch");
+    }
+    ORTHROS_CU(launch_fold_status(status, reinterpret_cast<const uint32_t *>(ws + L.core_off), slot,
+                                  (int)(kSlotBytes / 4), stream), "status fold");
+    if (n_out > 0) {
+        ORTHROS_CU(cudaEventRecord(hp->comp_done, stream), "event");
+        ORTHROS_CU(cudaStreamWaitEvent(hp->out, hp->comp_done, 0), "event wait");
+        ORTHROS_CU(cudaMemcpyAsync(o_out, oout_d, (size_t)n_out * qrow, cudaMemcpyDeviceToHost, hp->out), "o_out copy out");
+        ORTHROS_CU(cudaMemcpyAsync(lse_out, lout_d, (size_t)n_out * Hq * 4, cudaMemcpyDeviceToHost, hp->out),
+                   "lse_out copy out");
+    }
+    // the caller's stream resumes once everything above, copies out included, is done
+    ORTHROS_CU(cudaEventRecord(hp->end, hp->out), "event");
+    ORTHROS_CU(cudaStreamWaitEvent(stream, hp->end, 0), "event wait");
+#undef ORTHROS_CU
+    return ORTHROS_OK;
+}
+
 }  // namespace
 
 orthros_status report_error(orthros_status s, const char *fmt, ...) {
@@ -558,6 +894,28 @@ orthros_status orthros_prefill_shard(const void *q, const void *k, const void *v
                         q_rows, B, Tkv, Tq, true, Hq, Hkv, d, window, scale, dtype, o_base, lse_base, nullptr,
                         o_part, lse_part, nullptr, nullptr, nullptr, 0, 0, 0, workspace, workspace_bytes,
                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t orthros_prefill_from_host_workspace_size(int B, int T, int Hq, int Hkv, int d, int n_out, int window,
+                                                orthros_dtype dtype) {
+    if (T < 0 || n_out < 0) return 0;
+    if (check_shapes(B, Hq, Hkv, d, window, 1.0f, dtype) != ORTHROS_OK) return 0;
+    return from_host_layout(B, T, Hq, Hkv, d, n_out, window, dtype).total;
+}
+
+orthros_status orthros_prefill_from_host(const void *q, const void *k, const void *v, const float *alpha_base,
+                                         const float *beta_base, const float *alpha_out, const float *beta_out,
+                                         const int32_t *out_indptr, const int32_t *out_positions, int n_out,
+                                         const void *q_out, int B, int T, int Hq, int Hkv, int d, int window,
+                                         float scale, orthros_dtype dtype, void *o_base, float *lse_base, void *o_out,
+                                         float *lse_out, void *k_cache, void *v_cache, const int32_t *block_table,
+                                         int max_pages, int page_size, int num_pages, void *workspace,
+                                         size_t workspace_bytes, orthros_stream_t stream) {
+    g_last_error.clear();
+    return from_host_core(q, k, v, alpha_base, beta_base, alpha_out, beta_out, out_indptr, out_positions, n_out, q_out,
+                          B, T, Hq, Hkv, d, window, scale, dtype, o_base, lse_base, o_out, lse_out, k_cache, v_cache,
+                          block_table, max_pages, page_size, num_pages, workspace, workspace_bytes,
+                          reinterpret_cast<cudaStream_t>(stream));
 }
 
 orthros_status orthros_merge_partials(const float *o_parts, const float *lse_parts, int n_parts, int n_rows, int Hq,

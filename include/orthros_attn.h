@@ -130,6 +130,55 @@ ORTHROS_API orthros_status orthros_prefill(
     int max_pages, int page_size, int num_pages,
     void *workspace, size_t workspace_bytes, orthros_stream_t stream);
 
+/* Workspace bytes orthros_prefill_from_host needs for these sizes (0 if rejected). */
+ORTHROS_API size_t orthros_prefill_from_host_workspace_size(int B, int T, int Hq, int Hkv, int d, int n_out,
+                                                            int window, orthros_dtype dtype);
+
+/*
+ * orthros_prefill with the step's inputs and outputs in HOST memory: the
+ * same computation (Eq. 4 for every position, Eq. 5 for the output rows, the
+ * optional cache fill), the host-to-device and device-to-host copies included.
+ *
+ * HOST:   q, k, v, o_base, lse_base, out_indptr, out_positions, q_out, o_out,
+ *         lse_out, with the shapes of orthros_prefill. Page-locked memory
+ *         (cudaHostAlloc / cudaHostRegister) lets the copies overlap the
+ *         compute; pageable memory gives the same results with copies that do
+ *         not overlap. Device memory passed here is rejected (ORTHROS_EINVAL).
+ * DEVICE: alpha_base, beta_base, alpha_out, beta_out (model parameters), the
+ *         optional k_cache, v_cache, block_table, and the workspace (at least
+ *         orthros_prefill_from_host_workspace_size() bytes, 256-byte aligned;
+ *         it holds device copies of q, k, v and o_base besides the scratch).
+ * out_positions are checked on the host: a position outside [0, T) returns
+ * ORTHROS_EINVAL before anything is enqueued.
+ *
+ * A sequence longer than one chunk (at least 16384 tokens and four halos of
+ * w - 1 keys; bf16 only) is computed chunk by chunk as orthros_prefill_shard
+ * calls (each chunk's keys with the halo before it, so its base rows are
+ * exact, and each output row's partial over the chunk's keys), and the
+ * partials are merged as orthros_merge_partials does, so the results equal
+ * orthros_prefill's up to the rounding of that merge. Chunk c + 1 is copied
+ * in while chunk c computes and chunk c - 1 is copied out, on two copy streams
+ * of the library's own (created once per device) ordered after the work
+ * already on `stream`; `stream` itself runs the compute and waits for the
+ * last copy out, so every output is in host memory once `stream` reaches the
+ * point after this call. Calls are enqueued one at a time (an internal lock).
+ * Shorter sequences, and f32, copy everything in, compute, and copy out on
+ * `stream`. Device-side status as for orthros_prefill (orthros_check on this
+ * call's workspace).
+ */
+ORTHROS_API orthros_status orthros_prefill_from_host(
+    const void *q, const void *k, const void *v,
+    const float *alpha_base, const float *beta_base,
+    const float *alpha_out, const float *beta_out,
+    const int32_t *out_indptr, const int32_t *out_positions, int n_out,
+    const void *q_out,
+    int B, int T, int Hq, int Hkv, int d, int window, float scale,
+    orthros_dtype dtype,
+    void *o_base, float *lse_base, void *o_out, float *lse_out,
+    void *k_cache, void *v_cache, const int32_t *block_table,
+    int max_pages, int page_size, int num_pages,
+    void *workspace, size_t workspace_bytes, orthros_stream_t stream);
+
 /* Workspace bytes orthros_prefill_shard needs for these sizes (0 if rejected). */
 ORTHROS_API size_t orthros_prefill_shard_workspace_size(int B, int Tq, int Tkv, int Hq, int Hkv, int d,
                                                        int n_rows, int window, orthros_dtype dtype);
