@@ -9,25 +9,32 @@
 // kernel (those of sequences with many output rows; sequences with few output
 // rows take the split-KV kernel instead).
 //
-// Design (one CTA per SM, 576 threads):
+// Design (one CTA per SM; 576 threads, or 320 for windows of 4096 keys and more):
 //   * A work unit is two 128-row query tiles that read the SAME key/value
 //     tiles: two query heads of one GQA group at the same positions, or (when
 //     the group size is odd, e.g. plain multi-head) two consecutive row blocks
 //     of one head. Key/value tiles of 128 tokens are visited only inside the
 //     union of the tiles' bands; tiles outside the band are never loaded.
-//   * warp 16 (one thread): TMA producer. Keys come from an fp16 copy made by
-//     the pre-pass kernel (3 stages), values in bf16 (2 stages), 128B swizzle.
-//   * warp 17 (one thread): tcgen05.mma issuer. S_s = Q_s K^T (M=128, N=128,
-//     fp16 operands from shared memory) into TMEM; O_s += P_s V (M=128, N=d,
-//     P read from TMEM as bf16, V from shared memory, MN-major).
-//   * warps 0-15: softmax, two threads per row. Warp w serves slot
-//     (w >> 2) & 1, key half w >> 3 of each 128-key tile, rows 32 (w & 3) ..
-//     +31 (TMEM lane quarter w & 3). A thread reads its 64 logits with
-//     tcgen05.ld, masks the two band edge tiles, agrees with its partner on
-//     the row's shift, keeps a running max with lazy rescaling (O in TMEM is
-//     only rescaled when the max grows by more than 2^8), writes P as packed
-//     bf16 back over its logits, and finally normalises its half of O and
-//     stores o and lse.
+//   * the warp after the softmax warps (one thread): TMA producer. Keys come
+//     from an fp16 copy made by the pre-pass kernel (3 stages), values in bf16
+//     (2 stages), 128B swizzle.
+//   * the last warp (one thread): tcgen05.mma issuer. S_s = Q_s K^T (M=128,
+//     N=128, fp16 operands from shared memory) into TMEM; O_s += P_s V (M=128,
+//     N=d, P read from TMEM as bf16, V from shared memory, MN-major).
+//   * softmax warps, two layouts (template kRow):
+//     - two threads per row (warps 0-15): warp w serves slot (w >> 2) & 1, key
+//       half w >> 3 of each 128-key tile, rows 32 (w & 3) .. +31 (TMEM lane
+//       quarter w & 3). A thread reads its 64 logits with tcgen05.ld, masks
+//       the two band edge tiles, agrees with its partner on the row's shift,
+//       keeps a running max with lazy rescaling (O in TMEM is only rescaled
+//       when the max grows by more than 2^8), writes P as packed bf16 back
+//       over its logits, and finally normalises its half of O and stores o
+//       and lse. 96 registers a thread.
+//     - one thread per row (warps 0-7, windows of 4096 keys and more): warp w
+//       serves slot w >> 2, rows 32 (w & 3) .. +31, all 128 logits of a tile
+//       at once, with no exchange between threads; it stages and stores the
+//       whole row. 168 registers a thread: its tiles are faster, its unit
+//       boundaries slower, so it is taken where units are long.
 //   TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [384,384+d).
 //
 // Precision: the query affine runs in fp32 and is rounded to fp16 (11-bit
@@ -49,10 +56,20 @@ namespace {
 
 constexpr int kRowsPerTile = 128;  // M of every MMA, rows of a query tile
 constexpr int kKeysPerTile = 128;  // N of QK^T, K of PV
-constexpr int kSoftmaxWarps = 16;  // 2 slots x 2 column halves x 4 lane quarters
-constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
-constexpr int kProducerWarp = 16;
-constexpr int kMmaWarp = 17;
+// Two layouts of the softmax warps. kRow = false: two threads per row (one per
+// 64-key half), 16 softmax warps, 18 in all: five warps on two of the four
+// schedulers leave 96 registers a thread. kRow = true: one thread per row, 8
+// softmax warps, 10 in all: three warps on two schedulers leave 168 registers
+// a thread (3 x 32 x 168 fits a scheduler's 16K), so the register bound is
+// taken for 384 threads while the launch has 320.
+template <bool kRow> struct Warps {
+    static constexpr int kSoftmax = kRow ? 8 : 16;   // 2 slots x (2 halves x) 4 lane quarters
+    static constexpr int kThreads = (kSoftmax + 2) * 32;
+    static constexpr int kProducer = kSoftmax;
+    static constexpr int kMma = kSoftmax + 1;
+    static constexpr int kBound = kRow ? 384 : kThreads;
+    static constexpr int kPerRow = kRow ? 1 : 2;      // softmax threads per row
+};
 constexpr int kNumK = 3;  // key stages
 constexpr int kNumV = 2;  // value stages
 
@@ -315,12 +332,13 @@ __device__ void make_desc(const TcParams &p, int u, int lane, UnitDesc &D, bool 
 // past the fp16 range gives such rows) and computes their row blocks again,
 // every row staged with its own power-of-two shift and the inverse shift on
 // its logit scale. Without such rows every CTA leaves after the scan.
-template <int D, bool kRedo>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, bool kRedo, bool kRow>
+__global__ void __launch_bounds__(Warps<kRow>::kBound, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qo,
                       const __grid_constant__ CUtensorMap tm_ob, const TcParams p) {
     using C = Cfg<D>;
+    using Wp = Warps<kRow>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Meta &mt = *reinterpret_cast<Meta *>(smem + C::kBar);
@@ -345,25 +363,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&mt.s_full[s], 1);
-            mbar_init(&mt.p_full[s], 2 * kRowsPerTile);
+            mbar_init(&mt.p_full[s], Wp::kPerRow * kRowsPerTile);
             mbar_init(&mt.o_full[s], 1);
             mbar_init(&mt.xm_bar[s], 2 * kRowsPerTile);
             mbar_init(&mt.lx_bar[s], 2 * kRowsPerTile);
             mbar_init(&mt.q_full[s], 1);
-            mbar_init(&mt.q_ready[s], 2 * kRowsPerTile);
-            mbar_init(&mt.q_free[s], 2 * kRowsPerTile);
-            mbar_init(&mt.os_bar[s], 2 * kRowsPerTile);
+            mbar_init(&mt.q_ready[s], Wp::kPerRow * kRowsPerTile);
+            mbar_init(&mt.q_free[s], Wp::kPerRow * kRowsPerTile);
+            mbar_init(&mt.os_bar[s], Wp::kPerRow * kRowsPerTile);
         }
         for (int r = 0; r < kDescRing; ++r) {
             mbar_init(&mt.u_full[r], 1);
-            mbar_init(&mt.u_empty[r], kSoftmaxWarps + 1);
+            mbar_init(&mt.u_empty[r], Wp::kSoftmax + 1);
         }
         mbar_init(&mt.mma_done, 1);
         mt.abort = 0;
         mt.n_redo = 0;
         fence_mbar_init();
     }
-    if (warp == kProducerWarp && lane == 0) {
+    if (warp == Wp::kProducer && lane == 0) {
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_q);
@@ -406,21 +424,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(atomicOr(&p.redo_bits[idx >> 5], m) & m)) p.redo_list[redo_lo + atomicAdd(&mt.n_redo, 1)] = idx;
         };
         constexpr int kBatch = 8;  // loads in flight per thread
-        for (long long f0 = redo_lo + tid; f0 < redo_hi; f0 += (long long)kBatch * kThreads) {
+        for (long long f0 = redo_lo + tid; f0 < redo_hi; f0 += (long long)kBatch * Wp::kThreads) {
             float x[kBatch];
 #pragma unroll
             for (int j = 0; j < kBatch; ++j) {
-                const long long f = f0 + (long long)j * kThreads;
+                const long long f = f0 + (long long)j * Wp::kThreads;
                 x[j] = f >= redo_hi ? 0.f : __ldcg(f < fb ? p.lse_base + f : p.lse_out + (f - fb));
             }
 #pragma unroll
             for (int j = 0; j < kBatch; ++j)
-                if (!(fabsf(x[j]) <= 3.4e38f)) claim(f0 + (long long)j * kThreads);
+                if (!(fabsf(x[j]) <= 3.4e38f)) claim(f0 + (long long)j * Wp::kThreads);
         }
         __syncthreads();
         if (mt.n_redo == 0) return;  // the common case: nothing to compute again
     }
-    if (warp == kMmaWarp) {
+    if (warp == Wp::kMma) {
         tmem_alloc(&mt.tmem_base, 512);
         tmem_relinquish();
     }
@@ -434,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // TMA as raw bf16 and are turned into affined fp16 in place; other output
     // rows are gathered by the softmax threads.
 
-    if (warp == kProducerWarp) {
+    if (warp == Wp::kProducer) {
         // ---------------- producer: unit descriptors, then TMA loads ----------------
         // Takes units from a device-wide counter (heaviest first: the numbering
         // puts output-row units and late row blocks first), publishes each
@@ -534,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < 2; ++s)
                 if (nq[s] > 0) mbar_wait_drain(&mt.q_full[s], (nq[s] - 1) & 1, p.status);
         }
-    } else if (warp == kMmaWarp) {
+    } else if (warp == Wp::kMma) {
         // ---------------- tcgen05.mma issuer ----------------
         if (lane == 0) {
             constexpr uint32_t kIdescS = idesc_f16(0, 0, 0, 0, kRowsPerTile, kKeysPerTile);  // fp16, K-major
@@ -667,6 +685,310 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_commit(&mt.mma_done);
             mbar_wait_drain(&mt.mma_done, 0, p.status);
         }
+    } else if constexpr (kRow) {
+        // ---------------- softmax: one thread per row ----------------
+        // Softmax warp w: slot w >> 2, rows 32 (w & 3) .. +31 (TMEM lane quarter
+        // w & 3); each thread holds its row's 128 logits of a tile at once.
+        const int s = warp >> 2;
+        const int row = ((warp & 3) << 5) | lane;
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t t_s = tmem + lane_off + s * 128;               // S_s columns of this lane quarter
+        const uint32_t t_o = tmem + lane_off + C::kTmemO + s * 128;  // O_s
+        const float c2 = p.scale_log2;
+        uint8_t *qs = smem + C::kQ0 + s * C::kTileBytes;
+        constexpr int kChunks = D / 8;  // 16-byte chunks of a row
+        uint32_t cnt = 0;    // S tiles of this slot handled (all units so far)
+        uint32_t ucnt = 0;   // units in which this slot had tiles
+        uint32_t bcnt = 0;   // base-position tiles stored
+        bool stored = false; // this thread issued TMA stores
+        for (int i = 0;; ++i) {
+            const int r = i % kDescRing;
+            if (!mbar_wait_warp(&mt.u_full[r], (i / kDescRing) & 1, abort, p.status)) break;
+            const UnitDesc &dr = mt.desc[r];
+            const int end = dr.end;
+            const Slot S = dr.sl[s];
+            const Band bd = dr.bd[s];
+            const int kt_min = dr.kt_min, n_it = dr.n_it;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&mt.u_empty[r]);
+            if (end) break;
+
+            // ---- the row's position and its query, affine fused ----
+            int my_t = 0;  // the row's position in key coordinates
+            bool my_valid = false, my_bad = false;
+            if (S.kind >= 0 && row < S.n) {
+                if (S.kind == 0) {
+                    my_t = S.row0 + row + p.q_off;
+                    my_valid = true;
+                } else {
+                    my_valid = out_row_position(p, S.row0 + row, my_t);
+                }
+                my_bad = !my_valid;
+                if (my_bad) set_status(p.status, ORTHROS_DEV_BAD_POSITION);
+            }
+            const bool tma = S.qrow >= 0;
+            if (!mbar_wait_warp(&mt.q_full[s], i & 1, abort, p.status)) break;
+            if (S.kind >= 0) {
+                if (my_valid) {
+                    const float *al = (S.kind == 0 ? p.alpha_base : p.alpha_out) + S.h * D;
+                    const float *be = (S.kind == 0 ? p.beta_base : p.beta_out) + S.h * D;
+                    const __nv_bfloat16 *src =
+                        tma ? nullptr : p.q + (((long long)S.b * p.Tq + (my_t - p.q_off)) * p.Hq + S.h) * D;
+                    // two passes of half a row each: every load of a pass in flight at once
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint4 raws[kChunks / 2];
+#pragma unroll
+                        for (int cc = 0; cc < kChunks / 2; ++cc) {
+                            const int c = hh * (kChunks / 2) + cc;
+                            raws[cc] = tma ? *reinterpret_cast<const uint4 *>(qs + sw128_offset<D>(row, c))
+                                           : reinterpret_cast<const uint4 *>(src)[c];
+                        }
+#pragma unroll
+                        for (int cc = 0; cc < kChunks / 2; ++cc) {
+                            const int c = hh * (kChunks / 2) + cc;
+                            const uint4 raw = raws[cc];
+                            const float4 a0 = reinterpret_cast<const float4 *>(al)[2 * c];
+                            const float4 a1 = reinterpret_cast<const float4 *>(al)[2 * c + 1];
+                            const float4 b0 = reinterpret_cast<const float4 *>(be)[2 * c];
+                            const float4 b1 = reinterpret_cast<const float4 *>(be)[2 * c + 1];
+                            const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+                            float2 x0 = __bfloat1622float2(h2[0]), x1 = __bfloat1622float2(h2[1]);
+                            float2 x2 = __bfloat1622float2(h2[2]), x3 = __bfloat1622float2(h2[3]);
+                            uint4 o;
+                            o.x = pack_f16(fmaf(a0.x, x0.x, b0.x), fmaf(a0.y, x0.y, b0.y));
+                            o.y = pack_f16(fmaf(a0.z, x1.x, b0.z), fmaf(a0.w, x1.y, b0.w));
+                            o.z = pack_f16(fmaf(a1.x, x2.x, b1.x), fmaf(a1.y, x2.y, b1.y));
+                            o.w = pack_f16(fmaf(a1.z, x3.x, b1.z), fmaf(a1.w, x3.y, b1.w));
+                            *reinterpret_cast<uint4 *>(qs + sw128_offset<D>(row, c)) = o;
+                        }
+                    }
+                } else {
+#pragma unroll 4
+                    for (int c = 0; c < kChunks; ++c)
+                        *reinterpret_cast<uint4 *>(qs + sw128_offset<D>(row, c)) = make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+            }
+            mbar_arrive(&mt.q_ready[s]);
+
+            // ---- tiles: S -> P (online softmax), band mask on edge tiles only ----
+            const int t_row = my_valid ? my_t : bd.t_max;
+            const int lo_row = S.kind == 0 ? max(0, t_row - p.window + 1) : p.key_lo;
+            const int t_min_s = bd.t_min;
+            float m_ref = -INFINITY, l = 0.f;
+            bool ok = true;
+            uint32_t tiles = 0;
+            int row_shift = 0;  // second launch: the products give this row's logits times 2^-row_shift
+            if (kRedo && max(bd.kt_lo, kt_min) <= min(bd.kt_hi, kt_min + n_it - 1)) {
+                // The issuer's go-ahead comes in place of the first product: each row is
+                // staged again as qa * 2^-r, r the smallest shift that brings its largest
+                // value below 2^15.
+                ok = __all_sync(0xffffffffu, mbar_wait(&mt.s_full[s], cnt & 1, abort, p.status));
+                ++cnt;
+                if (ok) {
+                    const float *al = (S.kind == 0 ? p.alpha_base : p.alpha_out) + S.h * D;
+                    const float *be = (S.kind == 0 ? p.beta_base : p.beta_out) + S.h * D;
+                    float amax = 0.f;
+                    const __nv_bfloat16 *src = nullptr;
+                    if (my_valid) {
+                        src = S.qrow >= 0
+                                  ? (S.kind == 1 && p.q_out ? p.q_out : p.q) + ((long long)(S.qrow + row) * p.Hq + S.h) * D
+                                  : p.q + (((long long)S.b * p.Tq + (my_t - p.q_off)) * p.Hq + S.h) * D;
+                        for (int ch = 0; ch < D; ++ch)
+                            amax = fmaxf(amax, fabsf(fmaf(al[ch], __bfloat162float(src[ch]), be[ch])));
+                    }
+                    if (amax > 65504.f && __float_as_uint(amax) < 0x7f800000u)
+                        row_shift = min((int)((__float_as_uint(amax) >> 23) & 0xff) - 127 - 14, 126);
+                    if (my_valid && row_shift > 0) {
+                        const float f = exp2_int(-row_shift);
+                        for (int c = 0; c < kChunks; ++c) {
+                            float qa[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                qa[e] = fmaf(al[8 * c + e], __bfloat162float(src[8 * c + e]), be[8 * c + e]) * f;
+                            uint4 o;
+                            o.x = pack_f16(qa[0], qa[1]);
+                            o.y = pack_f16(qa[2], qa[3]);
+                            o.z = pack_f16(qa[4], qa[5]);
+                            o.w = pack_f16(qa[6], qa[7]);
+                            *reinterpret_cast<uint4 *>(qs + sw128_offset<D>(row, c)) = o;
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    mbar_arrive(&mt.q_ready[s]);
+                    ok = __all_sync(0xffffffffu, mbar_wait(&mt.s_full[s], cnt & 1, abort, p.status));
+                }
+                if (!ok) break;
+            }
+            const float c2u = kRedo ? c2 * exp2_int(row_shift) : c2;  // the row's logit scale
+            for (int it = 0; it < n_it; ++it) {
+                const int kt = kt_min + it;
+                if (kt < bd.kt_lo || kt > bd.kt_hi) continue;
+                if (!kRedo || tiles > 0) {  // (second launch: the first tile's wait came above)
+                    const bool got = mbar_wait(&mt.s_full[s], cnt & 1, abort, p.status);
+                    if (!(ok = __all_sync(0xffffffffu, got))) break;
+                }
+                tc_fence_after();
+                // the row's 128 logits, in four 32-column loads, one wait
+                uint32_t xr[kKeysPerTile];
+                using Cols = uint32_t[32];
+#pragma unroll
+                for (int q = 0; q < kKeysPerTile / 32; ++q)
+                    tmem_ld32(t_s + 32 * q, *reinterpret_cast<Cols *>(xr + 32 * q));
+                tmem_ld_wait();
+#pragma unroll
+                for (int q = 0; q < kKeysPerTile / 32; ++q) reg_fence(*reinterpret_cast<Cols *>(xr + 32 * q));
+                const int key0 = kt * kKeysPerTile;
+                if (key0 + kKeysPerTile - 1 > t_min_s || key0 < bd.lo_max) {
+#pragma unroll
+                    for (int c = 0; c < kKeysPerTile; ++c)
+                        if (key0 + c > t_row || key0 + c < lo_row) xr[c] = __float_as_uint(-INFINITY);
+                }
+                const float *x = reinterpret_cast<const float *>(xr);
+                float mq[16];
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+                    mq[q] = max3(max3(x[8 * q], x[8 * q + 1], x[8 * q + 2]), max3(x[8 * q + 3], x[8 * q + 4], x[8 * q + 5]),
+                                 fmaxf(x[8 * q + 6], x[8 * q + 7]));
+                const float m_tile = max3(max3(max3(mq[0], mq[1], mq[2]), max3(mq[3], mq[4], mq[5]), max3(mq[6], mq[7], mq[8])),
+                                          max3(mq[9], mq[10], mq[11]), max3(mq[12], mq[13], fmaxf(mq[14], mq[15])));
+                const float m_new = fmaxf(m_ref, m_tile);
+                const bool resc = (m_new - m_ref) * c2u > 8.f;  // true on the first finite max
+                const bool any_resc = __any_sync(0xffffffffu, resc);
+                const float alpha = resc ? ex2((m_ref - m_new) * c2u) : 1.f;
+                if (resc) {
+                    l *= alpha;
+                    m_ref = m_new;
+                }
+                const float mb = m_ref == -INFINITY ? 0.f : m_ref * c2u;
+                float ls[4] = {0.f, 0.f, 0.f, 0.f};
+                // (c2, c2) and (-mb, -mb) as f32x2 operands: the scaled, shifted logits and
+                // the row sums take one packed instruction per pair of keys
+                const uint64_t cv = f32x2(c2u, c2u), mv = f32x2(-mb, -mb);
+                // P for keys 32 j .. 32 j + 31 -> packed columns 16 j .. 16 j + 15 (over
+                // logits this thread has already read)
+#pragma unroll
+                for (int j = 0; j < kKeysPerTile / 32; ++j) {
+                    const float *xj = x + 32 * j;
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        float a0, a1;
+                        fma_f32x2(xj[2 * e], xj[2 * e + 1], cv, mv, a0, a1);
+                        // the row's last pair on the FMA pipe, the other 126
+                        // exponentials on the special-function unit
+                        float p0, p1;
+                        if (j == kKeysPerTile / 32 - 1 && e == 15) exp2_fma_x2(a0, a1, p0, p1);
+                        else p0 = ex2(a0), p1 = ex2(a1);
+                        add_f32x2(ls[2 * (e & 1)], ls[2 * (e & 1) + 1], p0, p1);
+                        pk[e] = pack_bf16(p0, p1);
+                    }
+                    tmem_st16(t_s + 16 * j, pk);
+                }
+                l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                // O_s is idle here (PV_s of the previous tile completed before S_s of
+                // this tile was signalled; the next PV_s waits for p_full)
+                if (any_resc && tiles > 0) {
+#pragma unroll
+                    for (int j = 0; j < D / 32; ++j) {
+                        uint32_t o[32];
+                        tmem_ld32(t_o + 32 * j, o);
+                        tmem_ld_wait();
+                        reg_fence(o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st32(t_o + 32 * j, o);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&mt.p_full[s]);
+                ++cnt;
+                ++tiles;
+            }
+            if (!ok) break;
+            if (kRedo) m_ref *= exp2_int(row_shift);  // back to logit units for the epilogue
+
+            // ---- epilogue: o = O / l, lse = scale*m + ln l ----
+            // o_full fires once every product of the slot's unit has completed, so
+            // the slot's query tile is idle: a base-position tile's normalised output
+            // is staged in it (128-byte swizzle) and leaves by one TMA store (rows
+            // past the query rows fall outside the map); output-row tiles store row
+            // by row.
+            if (tiles > 0) {
+                if (!mbar_wait_warp(&mt.o_full[s], ucnt & 1, abort, p.status)) break;
+                tc_fence_after();
+                ++ucnt;
+                const bool tile_store = S.kind == 0;  // warp-uniform
+                const bool store = S.kind >= 0 && row < S.n;
+                __nv_bfloat16 *dst = nullptr;
+                float *dst32 = nullptr;  // output rows written as float (shard partials)
+                float *lse_dst = nullptr;
+                if (store && S.kind == 0) {
+                    lse_dst = p.lse_base + ((long long)S.b * p.Hq + S.h) * p.Tq + (my_t - p.q_off);
+                } else if (store) {
+                    const long long o_off = ((long long)(S.row0 + row) * p.Hq + S.h) * D;
+                    if (p.o_out_f32) dst32 = p.o_out_f32 + o_off;
+                    else dst = p.o_out + o_off;
+                    lse_dst = p.lse_out + (long long)(S.row0 + row) * p.Hq + S.h;
+                }
+                // a shard's output row before the shard's first key has no keys: o = 0, lse = -inf
+                const float inv = my_bad ? __int_as_float(0x7fc00000) : (l > 0.f ? 1.f / l : 0.f);
+#pragma unroll
+                for (int j = 0; j < D / 32; ++j) {
+                    uint32_t o[32];
+                    tmem_ld32(t_o + 32 * j, o);
+                    tmem_ld_wait();
+                    reg_fence(o);
+                    uint4 w[4];
+                    uint32_t *wp = reinterpret_cast<uint32_t *>(w);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        wp[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+                    if (tile_store) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            *reinterpret_cast<uint4 *>(qs + sw128_offset<D>(row, 4 * j + e)) = w[e];
+                    } else if (dst32) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            reinterpret_cast<float4 *>(dst32 + 32 * j)[e] =
+                                make_float4(__uint_as_float(o[4 * e]) * inv, __uint_as_float(o[4 * e + 1]) * inv,
+                                            __uint_as_float(o[4 * e + 2]) * inv, __uint_as_float(o[4 * e + 3]) * inv);
+                    } else if (store) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) reinterpret_cast<uint4 *>(dst + 32 * j)[e] = w[e];
+                    }
+                }
+                if (store)
+                    *lse_dst = my_bad ? __int_as_float(0x7fc00000) : (l > 0.f ? m_ref * p.scale + logf(l) : -INFINITY);
+                if (tile_store) {
+                    fence_proxy_async_smem();
+                    mbar_arrive(&mt.os_bar[s]);
+                    if (!mbar_wait_warp(&mt.os_bar[s], bcnt & 1, abort, p.status)) break;
+                    ++bcnt;
+                    if (row == 0) {
+                        for (int j = 0; j < C::kSub; ++j)
+                            tma_store_4d(&tm_ob, qs + j * (kRowsPerTile * 128), 64 * j, S.h, S.row0, S.b);
+                        bulk_commit();
+                        bulk_wait_read();  // the query tile is free again once the store has read it
+                        stored = true;
+                    }
+                }
+            } else if (S.kind == 1 && row < S.n && my_valid) {
+                // no key tile in the slot's band (a shard's rows that all precede its keys)
+                const long long o_off = ((long long)(S.row0 + row) * p.Hq + S.h) * D;
+                for (int c = 0; c < D; ++c) {
+                    if (p.o_out_f32) p.o_out_f32[o_off + c] = 0.f;
+                    else p.o_out[o_off + c] = __float2bfloat16_rn(0.f);
+                }
+                p.lse_out[(long long)(S.row0 + row) * p.Hq + S.h] = -INFINITY;
+            }
+            tc_fence_before();
+            mbar_arrive(&mt.q_free[s]);
+        }
+        if (stored) bulk_wait_all();
     } else {
         // ---------------- softmax: two threads per row (one per 64-key half) ----------------
         // Softmax warp w: slot (w >> 2) & 1, column half w >> 3, rows 32 (w & 3) .. +31;
@@ -1012,7 +1334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == kMmaWarp) {
+    if (warp == Wp::kMma) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -1046,6 +1368,47 @@ bool make_kv_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int B
     return r == CUDA_SUCCESS;
 }
 
+template <int D, bool kRow>
+cudaError_t launch_dr(const TcParams &p, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tq,
+                      const CUtensorMap &tqo, const CUtensorMap &tob, int units, cudaStream_t stream) {
+    using Wp = Warps<kRow>;
+    static SmemLimit limit, limit_redo;
+    if (cudaError_t e = limit.ensure((const void *)prefill_tc_kernel<D, false, kRow>, Cfg<D>::kSmem); e != cudaSuccess)
+        return e;
+    if (cudaError_t e = limit_redo.ensure((const void *)prefill_tc_kernel<D, true, kRow>, Cfg<D>::kSmem); e != cudaSuccess)
+        return e;
+    // persistent: one CTA per SM takes units from the counter until none is left
+    int dev = 0, sms = 152;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int grid = units < sms ? units : sms;
+    prefill_tc_kernel<D, false, kRow><<<grid, Wp::kThreads, Cfg<D>::kSmem, stream>>>(tk, tv, tq, tqo, tob, p);
+    if (cudaError_t e = cudaGetLastError(); e != cudaSuccess) return e;
+    // second launch: scans the log-sum-exps for rows with a query past the fp16
+    // range and computes their blocks again (none: every CTA leaves after the scan)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(sms);
+    cfg.blockDim = dim3(Wp::kThreads);
+    cfg.dynamicSmemBytes = Cfg<D>::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D, true, kRow>, tk, tv, tq, tqo, tob, p);
+        e != cudaSuccess)
+        return e;
+    return cudaGetLastError();
+}
+
+// Windows of at least this many keys take the one-thread-per-row softmax:
+// their base units run 33 key tiles or more, where its shorter per-tile
+// softmax wins (128K shape: 7.18 vs 7.35 ms), while the per-unit query
+// staging and epilogue, twice as long per thread, cost more than that on
+// short units (fine-tuning shape, w = 1024: 1.14 vs 1.08 ms; pre-training
+// shape, w = 512: 0.41 vs 0.33 ms).
+constexpr int kRowWindowMin = 4096;
+
 template <int D>
 cudaError_t launch_d(const TcParams &p, const void *k16, const void *v, int units, cudaStream_t stream) {
     CUtensorMap tk, tv, tq, tqo, tob;
@@ -1056,32 +1419,8 @@ cudaError_t launch_d(const TcParams &p, const void *k16, const void *v, int unit
         !encode_kv_map_3d(&tqo, p.q_out ? (const void *)p.q_out : (const void *)p.q,
                           p.q_out ? (long long)p.n_out : (long long)p.B * p.Tq, p.Hq, D, kRowsPerTile))
         return cudaErrorInvalidValue;
-    static SmemLimit limit, limit_redo;
-    if (cudaError_t e = limit.ensure((const void *)prefill_tc_kernel<D, false>, Cfg<D>::kSmem); e != cudaSuccess)
-        return e;
-    if (cudaError_t e = limit_redo.ensure((const void *)prefill_tc_kernel<D, true>, Cfg<D>::kSmem); e != cudaSuccess)
-        return e;
-    // persistent: one CTA per SM takes units from the counter until none is left
-    int dev = 0, sms = 152;
-    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int grid = units < sms ? units : sms;
-    prefill_tc_kernel<D, false><<<grid, kThreads, Cfg<D>::kSmem, stream>>>(tk, tv, tq, tqo, tob, p);
-    if (cudaError_t e = cudaGetLastError(); e != cudaSuccess) return e;
-    // second launch: scans the log-sum-exps for rows with a query past the fp16
-    // range and computes their blocks again (none: every CTA leaves after the scan)
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(sms);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = Cfg<D>::kSmem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D, true>, tk, tv, tq, tqo, tob, p); e != cudaSuccess)
-        return e;
-    return cudaGetLastError();
+    return p.window >= kRowWindowMin ? launch_dr<D, true>(p, tk, tv, tq, tqo, tob, units, stream)
+                                     : launch_dr<D, false>(p, tk, tv, tq, tqo, tob, units, stream);
 }
 
 }  // namespace

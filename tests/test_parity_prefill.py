@@ -28,6 +28,10 @@ SMALL = [
     (1, 300, 4, 2, 128, 300, "all", torch.bfloat16),
     (1, 300, 4, 2, 128, 307, ("list", [[]]), torch.bfloat16),
     (3, 129, 32, 8, 128, 64, ("list", [[128], [], [0, 64, 128]]), torch.bfloat16),
+    # windows of 4096 keys and more take the one-thread-per-row softmax
+    (1, 300, 4, 2, 128, 4096, "all", torch.bfloat16),
+    (2, 257, 4, 2, 64, 5000, ("span", 40), torch.bfloat16),
+    (1, 700, 8, 2, 128, 4096, ("list", [[0, 5, 127, 128, 129, 400, 699]]), torch.bfloat16),
     (1, 200, 4, 2, 64, 50, "all", torch.float32),
     (2, 150, 2, 1, 128, 17, ("span", 40), torch.float32),
 ]
@@ -46,13 +50,14 @@ def test_key_offsets_small():
     compare_prefill(wl, run_gpu_prefill(wl), what="offsets")
 
 
+@pytest.mark.parametrize("window", [200, 4096], ids=["w200", "w4096_row_softmax"])
 @pytest.mark.parametrize("mode", ["all", ("span", 70)], ids=["all", "span"])
-def test_key_beyond_fp16_range(mode):
+def test_key_beyond_fp16_range(mode, window):
     """Single keys of 7e4 and -9e4 (fp16 stops at 65504): the fp16 key copy is
     scaled by 2^-2 and the logit scale by 2^2. The query channel that meets
     them is small (subnormal in fp16), so every logit stays moderate and the
     usual tolerances hold."""
-    wl = W.small_prefill(2, 300, 4, 2, 128, 200, out_mode=mode, seed=11)
+    wl = W.small_prefill(2, 300, 4, 2, 128, window, out_mode=mode, seed=11)
     c = 5
     wl["k"][0, 100, 1, c] = 70000.0
     wl["k"][1, 7, 0, c] = -90000.0
@@ -62,16 +67,18 @@ def test_key_beyond_fp16_range(mode):
     compare_prefill(wl, run_gpu_prefill(wl), what="keys beyond fp16")
 
 
+@pytest.mark.parametrize("window", [200, 4096], ids=["w200", "w4096_row_softmax"])
 @pytest.mark.parametrize("mode", ["all", ("span", 70)], ids=["all", "span"])
-def test_query_beyond_fp16_range(mode):
+def test_query_beyond_fp16_range(mode, window):
     """Affine weights of +-1e5 on one channel lift about half of the rows of a
     base head and of an output head past 65504; those rows are staged as
     q * 2^-r and their logit scale takes 2^r, the other rows of the same tiles
     keep r = 0. The keys' values in that channel are small multiples of 2^-16
     (exact in bf16 and fp16), so the logits stay moderate. One query sits just
     below 2^17 (130781.25), where rounding the row maximum up crosses the
-    power of two: both column halves must still pick the same shift."""
-    wl = W.small_prefill(2, 300, 4, 2, 128, 200, out_mode=mode, seed=12)
+    power of two: both column halves must still pick the same shift (window
+    200; with the 4096-key window one thread holds the whole row)."""
+    wl = W.small_prefill(2, 300, 4, 2, 128, window, out_mode=mode, seed=12)
     c = 9
     wl["alpha_base"][0, c] = 1e5
     wl["beta_base"][0, c] = 0.0

@@ -292,7 +292,8 @@ def test_shard_partials_on_gpu_match_oracle_shard(oracle_mod):
 
 
 @pytest.mark.gpu
-def test_shard_tile_path_rows_without_keys(oracle_mod):
+@pytest.mark.parametrize("w", [128, 4096], ids=["w128", "w4096_row_softmax"])
+def test_shard_tile_path_rows_without_keys(oracle_mod, w):
     """Enough output rows that the sequence takes the tensor-core tile kernel
     (not the split-KV kernel), a third of them placed before the chunk's first
     key: those rows share tiles with rows that have keys, see only masked
@@ -301,7 +302,7 @@ def test_shard_tile_path_rows_without_keys(oracle_mod):
     from tests.parity_util import TOL
 
     g = torch.Generator().manual_seed(22)
-    B, C, H, Hq, Hkv, d, w = 1, 256, 128, 8, 2, 128, 128
+    B, C, H, Hq, Hkv, d = 1, 256, 128, 8, 2, 128
     n = 1200  # more than 256 16-row groups of 4 query heads: the tile kernel
     q = torch.randn((B, C, Hq, d), generator=g).to(torch.bfloat16)
     k = torch.randn((B, H + C, Hkv, d), generator=g).to(torch.bfloat16)
