@@ -727,6 +727,21 @@ orthros_status from_host_core(const void *q, const void *k, const void *v, const
     ORTHROS_CU(cudaEventRecord(hp->start, stream), "event");
     ORTHROS_CU(cudaStreamWaitEvent(hp->in, hp->start, 0), "event wait");
     ORTHROS_CU(cudaStreamWaitEvent(hp->out, hp->start, 0), "event wait");
+    // On an error return, the caller's stream still waits for whatever this
+    // call has put on the copy streams, so that its buffers may be freed once
+    // `stream` has passed this call.
+    struct JoinOnError {
+        HostPipe *hp;
+        cudaStream_t s;
+        bool armed = true;
+        ~JoinOnError() {
+            if (!armed) return;
+            cudaEventRecord(hp->in_done, hp->in);
+            cudaStreamWaitEvent(s, hp->in_done, 0);
+            cudaEventRecord(hp->end, hp->out);
+            cudaStreamWaitEvent(s, hp->end, 0);
+        }
+    } join{hp, stream};
     // the output rows' raw queries, needed by every chunk: q_out, or runs of
     // consecutive positions of q
     char *qrows_d = ws + L.qrows_off;
@@ -815,6 +830,7 @@ orthros_status from_host_core(const void *q, const void *k, const void *v, const
     // the caller's stream resumes once everything above, copies out included, is done
     ORTHROS_CU(cudaEventRecord(hp->end, hp->out), "event");
     ORTHROS_CU(cudaStreamWaitEvent(stream, hp->end, 0), "event wait");
+    join.armed = false;
 #undef ORTHROS_CU
     return ORTHROS_OK;
 }

@@ -161,7 +161,9 @@ ORTHROS_API size_t orthros_prefill_from_host_workspace_size(int B, int T, int Hq
  * of the library's own (created once per device) ordered after the work
  * already on `stream`; `stream` itself runs the compute and waits for the
  * last copy out, so every output is in host memory once `stream` reaches the
- * point after this call. Calls are enqueued one at a time (an internal lock).
+ * point after this call (also after an error return: what the call had
+ * already enqueued on its copy streams is joined to `stream`). Calls are
+ * enqueued one at a time (an internal lock).
  * Shorter sequences, and f32, copy everything in, compute, and copy out on
  * `stream`. Device-side status as for orthros_prefill (orthros_check on this
  * call's workspace).
