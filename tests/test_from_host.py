@@ -34,6 +34,8 @@ def _from_host(w, cache=None, workspace=None):
     kw = {}
     if cache is not None:
         kw = dict(k_cache=cache[0], v_cache=cache[1], block_table=cache[2], page_size=cache[0].shape[1])
+    if w.get("q_out") is not None:
+        kw["q_out"] = w["q_out"].pin_memory()
     out = ola.orthros_prefill_from_host(w["q"].pin_memory(), w["k"].pin_memory(), w["v"].pin_memory(), *aff,
                                         w["out_indptr"], w["out_positions"], w["window"], w["scale"],
                                         workspace=workspace, **kw)
@@ -49,6 +51,8 @@ def _device(w, cache=None):
     kw = {}
     if cache is not None:
         kw = dict(k_cache=cache[0], v_cache=cache[1], block_table=cache[2], page_size=cache[0].shape[1])
+    if w.get("q_out") is not None:
+        kw["q_out"] = w["q_out"].cuda()
     out = ola.orthros_prefill(q, k, v, *aff, w["out_indptr"], w["out_positions"].cuda(), w["window"], w["scale"],
                               **kw)
     torch.cuda.synchronize()
@@ -114,6 +118,44 @@ def test_chunked_from_host_matches_oracle_and_device_call(B, T, window):
         assert err <= 2 * tol, (name, err)
     # the cache fill, byte for byte
     assert torch.equal(cache_h[0], cache_d[0]) and torch.equal(cache_h[1], cache_d[1])
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("variant", ["q_out", "no_output_rows"])
+def test_chunked_from_host_variants(variant):
+    """Chunked path with the output rows' own raw queries (q_out, copied in
+    once) and with no output rows at all, against orthros_prefill."""
+    T = 36000
+    if variant == "q_out":
+        pos = [np.array([3, 4100, 4101, 20000, 35999], np.int32)]
+    else:
+        pos = [np.zeros(0, np.int32)]
+    w = _workload(1, T, 2048, pos, seed=21)
+    if variant == "q_out":
+        w["q_out"] = torch.randn((len(pos[0]), 8, 128), generator=torch.Generator().manual_seed(5)).to(torch.bfloat16)
+    got = _from_host(w)
+    ref = _device(w)
+    tol_o, tol_l = TOL[torch.bfloat16]
+    for name, a, r, tol in zip(("o_base", "lse_base", "o_out", "lse_out"), got, ref, (tol_o, tol_l, tol_o, tol_l)):
+        assert a.shape == r.shape, name
+        err = max_err(a, r.float())
+        assert err <= 2 * tol, (name, err)
+    if variant == "q_out":
+        compare_prefill(w, got, base_rows=np.array([0, 4095, 4096, 20479, 20480, T - 1], np.int32), what="q_out")
+
+
+@pytest.mark.gpu
+def test_single_chunk_from_host_f32_equals_device_call():
+    """f32 takes the copy / compute / copy path (no chunks)."""
+    T = 300
+    wdef = W.PrefillWorkload("from_host_f32", 1, T, 4, 2, 64, 50, torch.float32, "last", seed=4)
+    w = W.make_prefill(wdef)
+    w["out_indptr"] = torch.tensor([0, 3], dtype=torch.int32)
+    w["out_positions"] = torch.tensor([0, 150, 299], dtype=torch.int32)
+    got = _from_host(w)
+    ref = _device(w)
+    for name, a, r in zip(("o_base", "lse_base", "o_out", "lse_out"), got, ref):
+        assert torch.equal(a, r), name
 
 
 @pytest.mark.gpu
