@@ -33,8 +33,10 @@
 //     - one thread per row (warps 0-7, windows of 4096 keys and more): warp w
 //       serves slot w >> 2, rows 32 (w & 3) .. +31, all 128 logits of a tile
 //       at once, with no exchange between threads; it stages and stores the
-//       whole row. 168 registers a thread: its tiles are faster, its unit
-//       boundaries slower, so it is taken where units are long.
+//       whole row, gathering its query from global memory (prefetched into L2
+//       one unit ahead) instead of a TMA tile. 168 registers a thread: its
+//       tiles are faster, its unit boundaries slower, so it is taken where
+//       units are long.
 //   TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [384,384+d).
 //
 // Precision: the query affine runs in fp32 and is rounded to fp16 (11-bit
@@ -520,7 +522,7 @@ __global__ void __launch_bounds__(Warps<kRow>::kBound, 1)
                     if (i >= 1 && !mbar_wait(&mt.q_free[s], (i - 1) & 1, abort, p.status)) return false;
                     const Slot &S = dsc.sl[s];
                     nq[s] = i + 1;
-                    if (S.qrow >= 0) {
+                    if (!kRow && S.qrow >= 0) {  // (the one-thread-per-row layout gathers its rows)
                         mbar_arrive_expect_tx(&mt.q_full[s], C::kTileBytes);
                         for (int j = 0; j < C::kSub; ++j)
                             tma_load_3d(smem + C::kQ0 + s * C::kTileBytes + j * (kRowsPerTile * 128),
@@ -726,14 +728,15 @@ __global__ void __launch_bounds__(Warps<kRow>::kBound, 1)
                 my_bad = !my_valid;
                 if (my_bad) set_status(p.status, ORTHROS_DEV_BAD_POSITION);
             }
-            const bool tma = S.qrow >= 0;
+            const bool tma = false;  // gathered in this layout
             if (!mbar_wait_warp(&mt.q_full[s], i & 1, abort, p.status)) break;
             if (S.kind >= 0) {
                 if (my_valid) {
                     const float *al = (S.kind == 0 ? p.alpha_base : p.alpha_out) + S.h * D;
                     const float *be = (S.kind == 0 ? p.beta_base : p.beta_out) + S.h * D;
                     const __nv_bfloat16 *src =
-                        tma ? nullptr : p.q + (((long long)S.b * p.Tq + (my_t - p.q_off)) * p.Hq + S.h) * D;
+                        (S.kind == 1 && p.q_out) ? p.q_out + ((long long)(S.row0 + row) * p.Hq + S.h) * D
+                                                 : p.q + (((long long)S.b * p.Tq + (my_t - p.q_off)) * p.Hq + S.h) * D;
                     // two passes of half a row each: every load of a pass in flight at once
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
@@ -909,6 +912,29 @@ __global__ void __launch_bounds__(Warps<kRow>::kBound, 1)
             }
             if (!ok) break;
             if (kRedo) m_ref *= exp2_int(row_shift);  // back to logit units for the epilogue
+            // The next unit's query rows into L2 now (this layout gathers its rows
+            // from global memory at the staging), so that their loads there hit
+            // L2: the descriptor ring runs a unit ahead of the softmax.
+            {
+                const int r2 = (i + 1) % kDescRing;
+                if (mbar_wait_warp(&mt.u_full[r2], ((i + 1) / kDescRing) & 1, abort, p.status)) {
+                    const UnitDesc &d2 = mt.desc[r2];
+                    const Slot S2 = d2.sl[s];
+                    if (!d2.end && S2.kind >= 0 && row < S2.n) {
+                        int t2 = 0;
+                        bool v2 = true;
+                        if (S2.kind == 0) t2 = S2.row0 + row + p.q_off;
+                        else if (!p.q_out) v2 = out_row_position(p, S2.row0 + row, t2);
+                        if (v2) {
+                            const char *a2 = reinterpret_cast<const char *>(
+                                (S2.kind == 1 && p.q_out) ? p.q_out + ((long long)(S2.row0 + row) * p.Hq + S2.h) * D
+                                                          : p.q + (((long long)S2.b * p.Tq + (t2 - p.q_off)) * p.Hq + S2.h) * D);
+#pragma unroll
+                            for (int cb = 0; cb < D * 2; cb += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(a2 + cb));
+                        }
+                    }
+                }
+            }
 
             // ---- epilogue: o = O / l, lse = scale*m + ln l ----
             // o_full fires once every product of the slot's unit has completed, so
