@@ -100,6 +100,24 @@ def test_projection_decode_shape_full():
     run(W.PROJ_DECODE_32)
 
 
+def test_projection_decoding_pair_is_deterministic():
+    """Calls of at most 64 rows may split the d_model walk over a cluster of
+    CTAs, which add their partials in a fixed order: two calls agree bit for
+    bit."""
+    import efficient_long_context_gb300 as ola
+
+    wl = W.make_projection(W.PROJ_DECODE_32)
+    dev = "cuda"
+    nb = wl["n_base"]
+    aff = [wl[n].to(dev) for n in ("alpha_base", "beta_base", "alpha_out", "beta_out")]
+    x, w = wl["x"].to(dev), wl["w_t"].to(dev)
+    a = ola.orthros_qkv_project(x, nb, w, wl["Hq"], wl["Hkv"], wl["d"], *aff, kv_out=True)
+    b = ola.orthros_qkv_project(x, nb, w, wl["Hq"], wl["Hkv"], wl["d"], *aff, kv_out=True)
+    torch.cuda.synchronize()
+    for ta, tb in zip(a, b):
+        assert torch.equal(ta, tb)
+
+
 def test_projection_prefill_shape_sampled():
     """8192 base rows at the Llama-8B shape (256-wide tiles), checked on sampled rows."""
     rng = np.random.default_rng(0)
