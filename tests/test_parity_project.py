@@ -101,9 +101,8 @@ def test_projection_decode_shape_full():
 
 
 def test_projection_decoding_pair_is_deterministic():
-    """Calls of at most 64 rows may split the d_model walk over a cluster of
-    CTAs, which add their partials in a fixed order: two calls agree bit for
-    bit."""
+    """Two calls on the decoding pair agree bit for bit (each output column is
+    one CTA's accumulation in a fixed order)."""
     import efficient_long_context_gb300 as ola
 
     wl = W.make_projection(W.PROJ_DECODE_32)
